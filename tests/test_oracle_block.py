@@ -1,0 +1,258 @@
+"""Pins for the oracle's MTP draft block.
+
+The pages print no worked example for the block's numbers, so these checks pin
+its structure instead: closed forms and special cases of each step, invariants
+(causality, order-free attention, the GQA head map, the concatenation order, the
+residual paths), an independent element-by-element evaluation on the tiny
+workload, and the module's size against the figure the pages give.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import scipy.special
+
+from oracle.block import (GREEDY, STOCHASTIC, Dims, draft_depth, gqa_attention,
+                          mtp_draft, rmsnorm, silu)
+from oracle.numerics import as_f64, bf16_bits_to_f64, round_bf16, round_f32
+from mtp_speculative_decoding_draft_gb300 import workloads as W
+
+
+def _tiny(seed_shift=0):
+    w = W.TINY
+    wts, master = W.make_weights(w, master=True)
+    ctx = W.make_context(w)
+    dims = Dims(w.B, w.d, w.Hq, w.Hkv, w.Dh, w.F, w.V, w.Lmax, w.eps)
+    return w, wts, master, ctx, dims
+
+
+# ---------------------------------------------------------------- element ops
+
+def test_rmsnorm_closed_forms():
+    rng = np.random.default_rng(0)
+    v = rng.standard_normal((5, 77)) * 3
+    y = rmsnorm(v, np.ones(77), 0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=-1)), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(rmsnorm(7.5 * v, np.ones(77), 0.0), y, rtol=1e-13)   # scale invariant
+    g = rng.standard_normal(77)
+    np.testing.assert_allclose(rmsnorm(v, g, 0.0), y * g, rtol=1e-14)                # gain multiplies
+    assert np.all(rmsnorm(np.zeros(8), np.ones(8), 1e-6) == 0.0)                     # eps guards 0/0
+    c = np.full(16, 2.0)                                                             # constant vector
+    np.testing.assert_allclose(rmsnorm(c, np.ones(16), 1e-6), 2.0 / math.sqrt(4.0 + 1e-6), rtol=1e-15)
+
+
+def test_silu_matches_library():
+    z = np.linspace(-30, 30, 20001)
+    np.testing.assert_allclose(silu(z), z * scipy.special.expit(z), rtol=1e-13, atol=1e-300)
+    assert silu(np.array([0.0]))[0] == 0.0
+
+
+# ---------------------------------------------------------------- attention
+
+def test_attention_single_key_returns_its_value():
+    rng = np.random.default_rng(1)
+    q = rng.standard_normal((4, 16))
+    K = rng.standard_normal((2, 1, 16))
+    V = rng.standard_normal((2, 1, 16))
+    o = gqa_attention(q, K, V)
+    np.testing.assert_allclose(o, V[[0, 0, 1, 1], 0], rtol=0, atol=0)
+
+
+def test_attention_equal_scores_average_values():
+    rng = np.random.default_rng(2)
+    q = np.zeros((3, 8))
+    K = rng.standard_normal((3, 10, 8))
+    V = rng.standard_normal((3, 10, 8))
+    np.testing.assert_allclose(gqa_attention(q, K, V), V.mean(axis=1), rtol=1e-14)
+
+
+def test_attention_dominant_key():
+    rng = np.random.default_rng(3)
+    K = rng.standard_normal((1, 20, 8)) * 0.01
+    K[0, 13] = 100.0
+    q = np.ones((1, 8))
+    V = rng.standard_normal((1, 20, 8))
+    np.testing.assert_allclose(gqa_attention(q, K, V)[0], V[0, 13], rtol=1e-12)
+
+
+def test_attention_order_free_and_head_map():
+    rng = np.random.default_rng(4)
+    Hq, Hkv, T, Dh = 8, 2, 30, 16
+    q = rng.standard_normal((Hq, Dh))
+    K = rng.standard_normal((Hkv, T, Dh))
+    V = rng.standard_normal((Hkv, T, Dh))
+    perm = rng.permutation(T)
+    np.testing.assert_allclose(gqa_attention(q, K[:, perm], V[:, perm]), gqa_attention(q, K, V), rtol=1e-13)
+    # kv head g holds constant values c_g: query head h must return c_{h // 4}
+    Vc = np.zeros_like(V)
+    Vc[0] += 1.0
+    Vc[1] += 2.0
+    o = gqa_attention(q, K, Vc)
+    np.testing.assert_allclose(o[:4], 1.0, rtol=1e-14)
+    np.testing.assert_allclose(o[4:], 2.0, rtol=1e-14)
+
+
+# ---------------------------------------------------------------- block structure
+
+def _one_depth(wts, dims, ctx, k_cache=None, h=None, tok=None, W_over=None):
+    Wd = dict(wts)
+    if W_over:
+        Wd.update(W_over)
+    kc = ctx["k_cache"] if k_cache is None else k_cache
+    L = int(ctx["ctx_len"][0])
+    keys = [as_f64(kc[0, :, :L, :])]
+    values = [as_f64(ctx["v_cache"][0, :, :L, :])]
+    hh = as_f64(ctx["h"]) if h is None else h
+    tt = ctx["last_tok"] if tok is None else tok
+    return draft_depth(Wd, dims, hh, tt, keys, values)
+
+
+def test_rows_past_the_context_are_never_read():
+    w, wts, _, ctx, dims = _tiny()
+    ref = mtp_draft(wts, dims, ctx["h"], ctx["last_tok"], ctx["k_cache"], ctx["v_cache"],
+                    ctx["ctx_len"], w.k, 1.0, GREEDY)
+    L = int(ctx["ctx_len"][0])
+    kc = ctx["k_cache"].copy()
+    vc = ctx["v_cache"].copy()
+    kc[:, :, L:, :] = 0x7FC0      # bf16 NaN
+    vc[:, :, L:, :] = 0x7FC0
+    got = mtp_draft(wts, dims, ctx["h"], ctx["last_tok"], kc, vc, ctx["ctx_len"], w.k, 1.0, GREEDY)
+    for key in ("draft_tok", "draft_logits", "hidden", "k_new", "v_new"):
+        np.testing.assert_array_equal(got[key], ref[key])
+
+
+def test_concat_order_embedding_first():
+    w, wts, _, ctx, dims = _tiny()
+    d = w.d
+    fc = bf16_bits_to_f64(wts["fc"])
+    fc_emb_only = fc.copy()
+    fc_emb_only[:, d:] = 0.0               # columns that multiply the normalised hidden state
+    rng = np.random.default_rng(5)
+    h2 = rng.standard_normal((1, d))
+    x_a = _one_depth(wts, dims, ctx, W_over={"fc": fc_emb_only})[0]
+    x_b = _one_depth(wts, dims, ctx, h=h2, W_over={"fc": fc_emb_only})[0]
+    np.testing.assert_array_equal(x_a, x_b)        # hidden state has no path into x0
+    fc_hid_only = fc.copy()
+    fc_hid_only[:, :d] = 0.0
+    x_c = _one_depth(wts, dims, ctx, W_over={"fc": fc_hid_only})[0]
+    x_d = _one_depth(wts, dims, ctx, tok=np.array([7]), W_over={"fc": fc_hid_only})[0]
+    np.testing.assert_array_equal(x_c, x_d)        # token has no path into x0
+
+
+def test_residual_paths():
+    """With Wo = 0 and Wdown = 0 the block output is x0 = W_fc u."""
+    w, wts, _, ctx, dims = _tiny()
+    x2, logits, _, _ = _one_depth(wts, dims, ctx, W_over={
+        "wo": np.zeros((w.d, w.Hq * w.Dh)), "wdown": np.zeros((w.d, w.F))})
+    e = as_f64(wts["E"][ctx["last_tok"]])
+    u = np.concatenate([rmsnorm(e, wts["g_emb"], w.eps), rmsnorm(as_f64(ctx["h"]), wts["g_hid"], w.eps)], -1)
+    np.testing.assert_allclose(x2, u @ bf16_bits_to_f64(wts["fc"]).T, rtol=1e-13)
+    # tied head: logits are the embedding matrix times the normalised output
+    np.testing.assert_allclose(logits, rmsnorm(x2, wts["g_final"], w.eps) @ bf16_bits_to_f64(wts["E"]).T,
+                               rtol=1e-12)
+
+
+def _naive_block(Wf, w, x, tok, keys, values):
+    """Independent element-by-element evaluation of one depth (explicit loops)."""
+    d, Hq, Hkv, Dh, F, V, eps = w.d, w.Hq, w.Hkv, w.Dh, w.F, w.V, w.eps
+
+    def norm(v, g):
+        ms = sum(t * t for t in v) / len(v)
+        r = 1.0 / math.sqrt(ms + eps)
+        return [v[i] * r * g[i] for i in range(len(v))]
+
+    def matvec(M, v):
+        return [sum(M[i][c] * v[c] for c in range(len(v))) for i in range(len(M))]
+
+    e = list(Wf["E"][tok])
+    u = norm(e, Wf["g_emb"]) + norm(list(x), Wf["g_hid"])
+    x0 = matvec(Wf["fc"], u)
+    n = norm(x0, Wf["g_attn"])
+    q = matvec(Wf["wq"], n)
+    kk = [float(round_bf16(t)) for t in matvec(Wf["wk"], n)]
+    vv = [float(round_bf16(t)) for t in matvec(Wf["wv"], n)]
+    o = []
+    for h in range(Hq):
+        g = h // (Hq // Hkv)
+        Ks = [list(keys[g][t]) for t in range(keys.shape[1])] + [kk[g * Dh:(g + 1) * Dh]]
+        Vs = [list(values[g][t]) for t in range(values.shape[1])] + [vv[g * Dh:(g + 1) * Dh]]
+        s = [sum(q[h * Dh + c] * Kt[c] for c in range(Dh)) / math.sqrt(Dh) for Kt in Ks]
+        m = max(s)
+        p = [math.exp(t - m) for t in s]
+        Z = sum(p)
+        o += [sum(p[t] * Vs[t][c] for t in range(len(Vs))) / Z for c in range(Dh)]
+    x1 = [a + b for a, b in zip(x0, matvec(Wf["wo"], o))]
+    n2 = norm(x1, Wf["g_mlp"])
+    gt = matvec(Wf["wgate"], n2)
+    up = matvec(Wf["wup"], n2)
+    act = [gt[i] / (1.0 + math.exp(-gt[i])) * up[i] for i in range(F)]
+    x2 = [a + b for a, b in zip(x1, matvec(Wf["wdown"], act))]
+    logits = matvec(Wf["E"], norm(x2, Wf["g_final"]))
+    return x2, logits, kk, vv
+
+
+def test_tiny_block_against_independent_loops():
+    w, wts, _, ctx, dims = _tiny()
+    Wf = {k: bf16_bits_to_f64(v).tolist() for k, v in wts.items()}
+    L = int(ctx["ctx_len"][0])
+    keys = as_f64(ctx["k_cache"][0, :, :L, :])
+    values = as_f64(ctx["v_cache"][0, :, :L, :])
+    res = mtp_draft(wts, dims, ctx["h"], ctx["last_tok"], ctx["k_cache"], ctx["v_cache"],
+                    ctx["ctx_len"], w.k, 1.0, GREEDY)
+    x = as_f64(ctx["h"][0])
+    tok = int(ctx["last_tok"][0])
+    for j in range(w.k):
+        x2, logits, kk, vv = _naive_block(Wf, w, x, tok, keys, values)
+        np.testing.assert_allclose(res["hidden"][0, j], x2, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(res["draft_logits"][0, j], round_f32(np.array(logits)), rtol=1e-6)
+        np.testing.assert_array_equal(res["k_new"][0, j].reshape(-1), kk)
+        np.testing.assert_array_equal(res["v_new"][0, j].reshape(-1), vv)
+        nxt = int(np.argmax(round_f32(np.array(logits))))
+        assert res["draft_tok"][0, j] == nxt
+        keys = np.concatenate([keys, np.array(kk).reshape(w.Hkv, 1, w.Dh)], axis=1)
+        values = np.concatenate([values, np.array(vv).reshape(w.Hkv, 1, w.Dh)], axis=1)
+        x, tok = np.array(x2), nxt
+
+
+def test_chain_feeds_back_hidden_and_token():
+    """Depth j+1 equals one module application on (x2 of depth j, draft j) with
+    the cache extended by every row appended so far."""
+    w, wts, _, ctx, dims = _tiny()
+    for mode in (GREEDY, STOCHASTIC):
+        u = W.make_uniforms(w)["u_draft"]
+        res = mtp_draft(wts, dims, ctx["h"], ctx["last_tok"], ctx["k_cache"], ctx["v_cache"],
+                        ctx["ctx_len"], w.k, 0.8, mode, u)
+        L = int(ctx["ctx_len"][0])
+        keys = as_f64(ctx["k_cache"][0, :, :L, :])
+        values = as_f64(ctx["v_cache"][0, :, :L, :])
+        x = as_f64(ctx["h"])
+        tok = ctx["last_tok"]
+        for j in range(w.k):
+            x, logits, kn, vn = draft_depth(wts, dims, x, tok, [keys], [values])
+            np.testing.assert_array_equal(round_f32(logits), res["draft_logits"][:, j])
+            keys = np.concatenate([keys, kn[0][:, None]], axis=1)
+            values = np.concatenate([values, vn[0][:, None]], axis=1)
+            tok = res["draft_tok"][:, j]
+
+
+def test_master_and_bf16_weights_agree_within_tolerance():
+    """The bf16-rounded weights the GPU uses stay within the stated 1e-2 relative
+    L2 of the fp32-master evaluation on the tiny workload."""
+    w, wts, master, ctx, dims = _tiny()
+    a = mtp_draft(wts, dims, ctx["h"], ctx["last_tok"], ctx["k_cache"], ctx["v_cache"],
+                  ctx["ctx_len"], 1, 1.0, GREEDY)
+    b = mtp_draft(master, dims, ctx["h"], ctx["last_tok"], ctx["k_cache"], ctx["v_cache"],
+                  ctx["ctx_len"], 1, 1.0, GREEDY)
+    la, lb = a["draft_logits"][0, 0], b["draft_logits"][0, 0]
+    assert np.linalg.norm(la - lb) / np.linalg.norm(lb) < 1e-2
+
+
+def test_module_size_matches_the_pages():
+    """The larger dense workload's block matrices come to ~0.383B parameters, in
+    line with the roughly 0.39 billion the pages give for the dense 27B model's
+    MTP module ("The Tiny Draft Model Hidden Inside Qwen", opening section)."""
+    w = W.DEEP_CHAIN
+    shapes = W.weight_shapes(w)
+    n = sum(int(np.prod(s)) for k, s in shapes.items() if k != "E") + 5 * w.d
+    assert abs(n / 0.39e9 - 1.0) < 0.02
