@@ -1,0 +1,380 @@
+#!/usr/bin/env python3
+"""Benchmark of the MTP draft + verify step (spec_step) on GB300.
+
+Default workload: one sequence, greedy, k = 3 drafts, hidden 4096, 32/8 heads of
+128, SwiGLU 12288, vocabulary 151936, 4096 context tokens (all synthetic and
+seeded; random bf16 weights of that shape).  One "step" is one spec_step call:
+k chained draft-module applications followed by verification.
+
+Prints one JSON line (rank 0).  With --impl reference it times the CPU oracle on
+the host cores instead.  Under torchrun every rank runs an independent replica
+of the workload (the path has no cross-sequence exchange); the reported time is
+the maximum over ranks.
+"""
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mtp_speculative_decoding_draft_gb300 import workloads as W  # noqa: E402
+
+METRIC = "spec-decode steps/s & accepted tok/s (MTP draft+verify); % of HBM roofline"
+
+
+def block_elements(w):
+    return (w.d * 2 * w.d + (w.Hq + 2 * w.Hkv) * w.Dh * w.d + w.d * w.Hq * w.Dh + 3 * w.d * w.F + 5 * w.d)
+
+
+def step_bytes(w, ctx_len, logits_out):
+    """Algorithmic HBM bytes of one spec_step: weights re-streamed at every
+    depth, the visible KV rows read once per depth, target logits read once,
+    draft logits written and read once when they are materialised."""
+    k = w.k
+    weights = k * (block_elements(w) + w.V * w.d) * 2
+    kv = sum(int(L) + j + 1 for L in ctx_len for j in range(k)) * w.Hkv * w.Dh * 2 * 2
+    target = w.B * (k + 1) * w.V * 4
+    draft = 2 * w.B * k * w.V * 4 if logits_out else 0
+    return weights + kv + target + draft
+
+
+def lmhead_bytes(w, logits_out):
+    return w.V * w.d * 2 + (w.B * w.V * 4 if logits_out else 0)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_rank%d.csv" % index)
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+
+def _oracle_sample(workload_name, depths):
+    """Run the oracle on `depths` draft depths plus the verification of one
+    step of the workload; return (seconds for the depths, seconds for verify)."""
+    from oracle.block import Dims, mtp_draft
+    from oracle.verify import spec_verify
+    w = W.WORKLOADS[workload_name]
+    wts = W.make_weights(w)
+    ctx = W.make_context(w)
+    u = W.make_uniforms(w)
+    tl = W.target_logits(w)
+    dims = Dims(w.B, w.d, w.Hq, w.Hkv, w.Dh, w.F, w.V, w.Lmax, w.eps)
+    t0 = time.perf_counter()
+    dr = mtp_draft(wts, dims, ctx["h"], ctx["last_tok"], ctx["k_cache"], ctx["v_cache"], ctx["ctx_len"],
+                   depths, w.T, w.mode, u["u_draft"])
+    t1 = time.perf_counter()
+    dt = np.zeros((w.B, w.k), np.int64)
+    dt[:, :depths] = dr["draft_tok"]
+    dl = np.zeros((w.B, w.k, w.V))
+    dl[:, :depths] = dr["draft_logits"]
+    spec_verify(tl, dl, dt, w.mode, w.T, u["u_accept"], u["u_final"])
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1
+
+
+def cpu_oracle_steps_per_s(workload_name, depths):
+    """Time the oracle in a fresh single-threaded process (BLAS pinned to 1 thread)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench._oracle_sample(%r, %d)))" % (ROOT, workload_name, depths))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError("oracle timing failed: " + r.stderr[-2000:])
+    t_depths, t_verify = json.loads(r.stdout.strip().splitlines()[-1])
+    w = W.WORKLOADS[workload_name]
+    t_step = t_depths / depths * w.k + t_verify
+    return 1.0 / t_step, t_step
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = W.WORKLOADS[args.workload]
+    times = []
+    for i in range(args.warmup + args.steps):
+        sps, t_step = cpu_oracle_steps_per_s(args.workload, 1)
+        if i >= args.warmup:
+            times.append(t_step)
+    t = float(np.mean(times))
+    value = 1.0 / t
+    sample = ("per step: the oracle runs one draft depth of this workload plus its verification in a "
+              "single-threaded process; step time = %d x depth time + verify time" % w.k)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, args),
+            "cpu_baseline": {"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, args):
+    return {"workload": w.name, "B": w.B, "k": w.k, "d": w.d, "Hq": w.Hq, "Hkv": w.Hkv, "Dh": w.Dh, "F": w.F,
+            "V": w.V, "ctx": w.ctx if not isinstance(w.ctx, tuple) else list(w.ctx),
+            "mode": "greedy" if w.mode == 0 else "stochastic", "T": w.T,
+            "parallelism": "replicas%d" % args.gpus, "l2": "inputs larger than L2 (weights %.2f GB re-streamed per depth)"
+            % ((block_elements(w) + w.V * w.d) * 2 / 1e9)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from mtp_speculative_decoding_draft_gb300 import binding as bd
+    from mtp_speculative_decoding_draft_gb300.build import build
+    from mtp_speculative_decoding_draft_gb300.model import DraftModule, to_device
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    if rank == 0 or world == 1:
+        build()
+    if world > 1:
+        dist.barrier()
+        build()
+
+    w = W.WORKLOADS[args.workload]
+    stoch = w.mode == 1
+    wts = W.make_weights(w)
+    ctx = W.make_context(w)
+    u = W.make_uniforms(w)
+    m = DraftModule(w, wts)
+    m.set_context(ctx)
+    if w.mode == 1:
+        # target = the module's own draft logits + noise growing with position
+        m.draft(w.T, w.mode, to_device(u["u_draft"]), logits=True)
+        torch.cuda.synchronize()
+        dl = m.draft_logits.view(w.B, w.k, w.V).cpu().numpy()
+        target = W.draft_noise(W.Workload(w.name, B=w.B, k=w.k + 1, V=w.V, seed=w.seed,
+                                          draft_noise_std0=w.draft_noise_std0, noise_growth=w.noise_growth),
+                               w.k + 1)
+        for j in range(w.k + 1):
+            target[:, j] += dl[:, min(j, w.k - 1)]
+        m.set_context(ctx)
+    else:
+        target = W.target_logits(w)
+    target_d = to_device(target)
+    ud = to_device(u["u_draft"]) if stoch else None
+    ua = to_device(u["u_accept"]) if stoch else None
+    uf = to_device(u["u_final"]) if stoch else None
+    logits_out = stoch
+
+    def step(stream=None):
+        m.step(w.T, w.mode, target_d, ud, ua, uf, logits=logits_out, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    n0 = bd.launch_count()
+    stream = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    launches = bd.launch_count() - n0
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    assert m.status() == 0, "device status word %d" % m.status()
+    L = m.accept_len.cpu().numpy()
+
+    # per-kernel durations: the same steps with an event pair around each launch
+    bd.profiler_enable(True)
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize()
+    lm_ms, lm_n = bd.profiler_read(bd.KC_LMHEAD)
+    ver_ms, ver_n = bd.profiler_read(bd.KC_VERIFY)
+    att_ms, att_n = bd.profiler_read(bd.KC_ATTN)
+    gem_ms, gem_n = bd.profiler_read(bd.KC_GEMV)
+    bd.profiler_enable(False)
+
+    # end to end: per-step inputs from pinned host memory, results read back
+    h_h = torch.from_numpy(ctx["h"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_tok = torch.from_numpy(ctx["last_tok"].astype(np.int32)).pin_memory()
+    h_ctx = torch.from_numpy(ctx["ctx_len"].astype(np.int32)).pin_memory()
+    h_tgt = torch.from_numpy(target).pin_memory()
+    h_u = [torch.from_numpy(u[n]).pin_memory() for n in ("u_draft", "u_accept", "u_final")] if stoch else []
+    d_u = [ud, ua, uf] if stoch else []
+    o_out = torch.empty(m.out_tok.numel(), dtype=torch.int32).pin_memory()
+    o_len = torch.empty(w.B, dtype=torch.int32).pin_memory()
+    o_acc = torch.empty(w.B, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in [h_h, h_tok, h_ctx, h_tgt] + h_u)
+    d2h = sum(t.numel() * t.element_size() for t in [o_out, o_len, o_acc])
+
+    def e2e_step():
+        m.h.copy_(h_h, non_blocking=True)
+        m.last_tok.copy_(h_tok, non_blocking=True)
+        m.ctx_len.copy_(h_ctx, non_blocking=True)
+        target_d.copy_(h_tgt.view(-1) if target_d.dim() == 1 else h_tgt, non_blocking=True)
+        for hd, dd in zip(h_u, d_u):
+            dd.copy_(hd, non_blocking=True)
+        step()
+        o_out.copy_(m.out_tok, non_blocking=True)
+        o_len.copy_(m.accept_len, non_blocking=True)
+        o_acc.copy_(m.num_accepted, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = measured_peaks()
+    sb = step_bytes(w, ctx["ctx_len"], logits_out)
+    steps_s = 1e3 / ms * world
+    tokens_per_step = float(L.sum())
+    lm_avg = lm_ms / max(lm_n, 1)
+    lm_b = lmhead_bytes(w, logits_out)
+    ach = lm_b / (lm_avg * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": steps_s, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 weights / fp32 accumulate", "data": "synthetic (seeded, random weights)",
+        "config": config_of(w, args),
+        "accepted_tok_s": steps_s * tokens_per_step,
+        "accept_len_mean": float(L.mean()),
+        "hbm_bytes_per_step": sb,
+        "hbm_roofline_frac": sb / (ms * 1e-3) / 1e9 / peak,
+        "roofline": {"bound": "hbm", "kernel": "lm_head_gemv", "achieved": ach, "peak": peak, "unit": "GB/s",
+                     "frac": ach / peak, "peak_kind": peak_kind, "traffic": None,
+                     "bytes_per_launch": lm_b, "avg_launch_ms": lm_avg, "launches": lm_n},
+        "kernel_ms_per_step": {"lm_head": lm_ms / args.steps, "verify": ver_ms / args.steps,
+                               "attention": att_ms / args.steps, "gemv_other": gem_ms / args.steps},
+        "e2e": {"value": 1e3 / e2e_ms * world, "unit": "steps/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline and world >= 1:
+        try:
+            sps, t_step = cpu_oracle_steps_per_s(args.workload, w.k)
+            line["cpu_baseline"] = {"value": sps, "unit": "steps/s", "cores": 1, "kind": "oracle",
+                                    "sample": "one full step (all %d depths + verification) of this workload, "
+                                              "single-threaded float64 numpy" % w.k}
+        except Exception as e:  # report, do not hide
+            line["cpu_baseline"] = {"value": None, "error": str(e)[:300]}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=W.SINGLE_GREEDY.name, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

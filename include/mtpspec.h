@@ -1,0 +1,207 @@
+/*
+ * mtpspec -- the hot path of MTP speculative decoding on one GB300 (sm_103a):
+ * a single Multi-Token-Prediction draft block chained k times, then
+ * verification of the k drafted tokens against the target's distributions.
+ *
+ * Sources (web pages; section names as printed on them):
+ *  [P1] "Optimize vLLM speculative decoding with FastMTP heads"
+ *  [P2] "Faster Rollouts with MTP Speculative Decoding"
+ *  [P3] "Speculative Decoding and MTP: Why Guessing Is Free"
+ *  [P4] "The Tiny Draft Model Hidden Inside Qwen"
+ *
+ * Conventions shared by every entry point
+ *  - Every array argument is a DEVICE pointer owned by the caller, aligned to
+ *    16 bytes; the workspace is aligned to 256 bytes.  Nothing here allocates
+ *    or frees device memory.
+ *  - Calls are asynchronous on the given stream (a cudaStream_t; NULL is the
+ *    legacy default stream).  They return MTP_OK or a negative MTP_ERR_* code
+ *    for errors the host can see (bad argument, unsupported shape, workspace too
+ *    small, failed launch).  Conditions only the device can see (a token id out
+ *    of range, a context length past the cache, a non-finite logit row, a
+ *    bounded wait that ran out) set bits of a status word inside the workspace;
+ *    mtp_get_status() reads it.
+ *  - Random draws use caller-supplied uniforms in [0, 1), so every result is a
+ *    deterministic function of the inputs, bit for bit from run to run.
+ *  - bf16 means IEEE binary32's upper 16 bits (the storage type of the weights,
+ *    the trunk hidden state and the KV cache).  Logits are float32.
+ */
+#ifndef MTPSPEC_H
+#define MTPSPEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *mtp_stream_t; /* identical to cudaStream_t */
+
+/* Host-visible return codes. */
+enum {
+    MTP_OK = 0,
+    MTP_ERR_INVALID_ARG = -1,       /* null / misaligned pointer, k outside 1..8, T <= 0, ... */
+    MTP_ERR_UNSUPPORTED_SHAPE = -2, /* dims the kernels do not implement (see MtpDims) */
+    MTP_ERR_WORKSPACE = -3,         /* workspace smaller than the *_workspace_size() answer */
+    MTP_ERR_CUDA = -4               /* a CUDA runtime call or launch failed */
+};
+
+/* Bits of the device status word (sticky until mtp_clear_status()). */
+enum {
+    MTP_STATUS_TIMEOUT = 1,    /* a bounded wait gave up; results of that call are invalid */
+    MTP_STATUS_BAD_TOKEN = 2,  /* a token id outside [0, V); token 0 was used instead */
+    MTP_STATUS_BAD_CTX = 4,    /* ctx_len[b] < 0 or ctx_len[b] + k > Lmax; clamped */
+    MTP_STATUS_NONFINITE = 8   /* a logit row without a finite maximum */
+};
+
+typedef enum { MTP_GREEDY = 0, MTP_STOCHASTIC = 1 } MtpMode;
+
+/*
+ * Shape of the draft module and of the batch.  [P4] "The Tiny Draft Model
+ * Hidden Inside Qwen", opening section: the module is one input projection
+ * mtp.fc, one full-attention transformer block and three normalisation weights,
+ * and it reuses the trunk's token embedding.
+ *   B     sequences in the batch (>= 1)
+ *   d     hidden width (multiple of 8)
+ *   Hq    query heads; Hkv key/value heads (Hq % Hkv == 0, Hq / Hkv <= 8)
+ *   Dh    head size: 32, 64 or 128
+ *   F     SwiGLU inner width (multiple of 8)
+ *   V     vocabulary size (>= 1; any value)
+ *   Lmax  KV-cache capacity per sequence (positions)
+ *   rms_eps  RMSNorm epsilon: rms(v) = v / sqrt(mean(v^2) + eps)
+ */
+typedef struct {
+    int32_t B, d, Hq, Hkv, Dh, F, V, Lmax;
+    float rms_eps;
+} MtpDims;
+
+/*
+ * Weights, all bf16 row-major [out, in], no biases.  E [V, d] is the shared
+ * embedding AND the vocabulary head ([P1] "Key features": full-vocabulary head
+ * shared with the verifier; [P4] opening section: no second embedding table).
+ *   fc [d, 2d] applied to [rms(E[tok]) * g_emb ; rms(x) * g_hid]
+ *   wq [Hq*Dh, d], wk [Hkv*Dh, d], wv [Hkv*Dh, d], wo [d, Hq*Dh]
+ *   wgate [F, d], wup [F, d], wdown [d, F]                     (SwiGLU)
+ *   g_emb, g_hid, g_attn, g_mlp, g_final [d]                   (norm gains)
+ */
+typedef struct {
+    const void *E, *fc, *wq, *wk, *wv, *wo, *wgate, *wup, *wdown;
+    const void *g_emb, *g_hid, *g_attn, *g_mlp, *g_final;
+} MtpWeights;
+
+/* Bytes of workspace mtp_draft / spec_step need for these dims and depth k
+ * (0 if the arguments are invalid). */
+size_t mtp_workspace_size(const MtpDims *dims, int k);
+
+/*
+ * mtp_draft -- run the MTP module k times in a chain ([P4] "One step deeper
+ * than the main model" and "What vLLM and SGLang do with the weights"; [P1]
+ * "Why fine-tune a single MTP head": the same module is applied autoregressively,
+ * fed its own output hidden state and the token it just drafted).
+ *
+ * Depth j = 0..k-1 computes, per sequence b:
+ *   u  = [rms(E[tok]) * g_emb ; rms(x) * g_hid];  x0 = fc u
+ *   n  = rms(x0) * g_attn;  q = wq n;  K/V rows wk n, wv n stored (bf16) at
+ *        position ctx_len[b] + j of the cache
+ *   o  = softmax attention of q over cache positions 0 .. ctx_len[b] + j
+ *        (query head h uses kv head h / (Hq/Hkv); scale 1/sqrt(Dh))
+ *   x1 = x0 + wo o;  x2 = x1 + wdown(silu(wgate rms(x1)*g_mlp) * wup rms(x1)*g_mlp)
+ *   logits = E (rms(x2) * g_final)
+ *   draft token: argmax (lowest index on ties) if greedy; else the inverse-CDF
+ *   draw of softmax(logits / T) at u_draft[b, j]
+ * with x = h, tok = last_tok at depth 0 and x = x2, tok = the new draft after.
+ *
+ *   h         [B, d] bf16 trunk hidden state h_t
+ *   last_tok  [B] int32, the token the trunk just produced
+ *   k_cache, v_cache  [B, Hkv, Lmax, Dh] bf16; rows [0, ctx_len[b]) hold the
+ *             context.  Rows ctx_len[b] .. ctx_len[b]+k-1 are overwritten with
+ *             the drafts' keys/values; ctx_len is not changed (after verifying,
+ *             the caller advances it by num_accepted + 1: rejected rows are
+ *             simply overwritten next step).  Requires ctx_len[b] + k <= Lmax.
+ *   ctx_len   [B] int32
+ *   k         draft depth, 1..8;  T  temperature (> 0; ignored when greedy)
+ *   u_draft   [B, k] float32 uniforms (may be NULL when greedy)
+ *   draft_tok [B, k] int32 output
+ *   draft_logits [B, k, V] float32 output, or NULL when greedy
+ *   ws, ws_bytes  workspace of at least mtp_workspace_size(dims, k) bytes
+ * Returns MTP_OK or MTP_ERR_*.
+ */
+int mtp_draft(const MtpDims *dims, const MtpWeights *w, const void *h,
+              const int32_t *last_tok, void *k_cache, void *v_cache,
+              const int32_t *ctx_len, int k, float T, int mode,
+              const float *u_draft, int32_t *draft_tok, float *draft_logits,
+              void *ws, size_t ws_bytes, mtp_stream_t stream);
+
+/* Bytes of workspace spec_verify needs (0 if the arguments are invalid). */
+size_t spec_verify_workspace_size(int B, int k, int V);
+
+/*
+ * spec_verify -- accept or reject k drafts per sequence against the target
+ * ([P4] "How the draft becomes real output": longest agreeing prefix, then the
+ * corrected replacement at the first rejection; [P3] "Speculative decoding:
+ * draft, then verify" and "It's exact, not approximate").
+ *
+ * Greedy: draft j+1 is accepted while it equals argmax(target row j) (lowest
+ * index on ties); the emitted token after the accepted prefix is argmax of the
+ * first disagreeing row (or of row k when all k agree).  Equals plain greedy.
+ *
+ * Stochastic, with p_j = softmax(target_j / T), q_j = softmax(draft_j / T) and
+ * d = draft_tok[b, j]: accept iff u_accept[b, j] * q_j(d) < p_j(d), i.e. with
+ * probability min(1, p/q); at the first rejection r emit the inverse-CDF draw at
+ * u_final[b] of max(0, p_r - q_r) (of p_r if that is identically zero); if all
+ * k are accepted emit the draw at u_final[b] of p_k (the bonus token).
+ *
+ *   target_logits [B, k+1, V] float32;  draft_logits [B, k, V] float32 (NULL ok
+ *   when greedy);  draft_tok [B, k] int32;  u_accept [B, k], u_final [B] float32
+ *   (NULL ok when greedy)
+ *   out_tok [B, k+1] int32: accepted drafts then the emitted token, -1 padded
+ *   accept_len [B] int32 = tokens emitted (1 .. k+1); num_accepted [B] = accept_len - 1
+ */
+int spec_verify(int B, int k, int V, float T, int mode,
+                const float *target_logits, const float *draft_logits,
+                const int32_t *draft_tok, const float *u_accept, const float *u_final,
+                int32_t *out_tok, int32_t *accept_len, int32_t *num_accepted,
+                void *ws, size_t ws_bytes, mtp_stream_t stream);
+
+/*
+ * spec_step -- mtp_draft followed by spec_verify on the same stream, with the
+ * kernels of the two chained back to back.  Arguments as above; draft_logits
+ * may be NULL in either mode (stochastic mode then keeps them in the
+ * workspace, which mtp_workspace_size() already counts).
+ */
+int spec_step(const MtpDims *dims, const MtpWeights *w, const void *h,
+              const int32_t *last_tok, void *k_cache, void *v_cache,
+              const int32_t *ctx_len, int k, float T, int mode,
+              const float *u_draft, const float *target_logits,
+              const float *u_accept, const float *u_final,
+              int32_t *draft_tok, float *draft_logits,
+              int32_t *out_tok, int32_t *accept_len, int32_t *num_accepted,
+              void *ws, size_t ws_bytes, mtp_stream_t stream);
+
+/* Wait for the stream, then copy the workspace's status word (MTP_STATUS_* bits)
+ * to *status.  Returns MTP_OK or MTP_ERR_*. */
+int mtp_get_status(const void *ws, mtp_stream_t stream, int32_t *status);
+
+/* Zero the status word (asynchronously, on the stream). */
+int mtp_clear_status(void *ws, mtp_stream_t stream);
+
+/* Human-readable text for an MTP_ERR_* code. */
+const char *mtp_error_string(int code);
+
+/*
+ * Instrumentation.  mtp_profiler_enable(1) makes later calls record a CUDA
+ * event pair around every launch of the kernel classes below (this splits the
+ * programmatic launch chain at those points, so time steps with it off);
+ * mtp_profiler_read() waits for the events and returns the summed time and the
+ * launch count since the last enable.  mtp_launch_count() counts every kernel
+ * this library has launched in the process.
+ */
+enum { MTP_KC_LMHEAD = 0, MTP_KC_VERIFY = 1, MTP_KC_ATTN = 2, MTP_KC_GEMV = 3, MTP_KC_COUNT = 4 };
+int mtp_profiler_enable(int on);
+int mtp_profiler_read(int kernel_class, double *total_ms, int64_t *launches);
+int64_t mtp_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MTPSPEC_H */

@@ -1,0 +1,212 @@
+"""ctypes binding of libmtpspec (include/mtpspec.h).
+
+Argument marshalling only: every step of the path runs in the CUDA library.
+Tensors are torch CUDA tensors; their device pointers are passed through the
+C ABI unchanged.  If the library is missing or cannot be loaded this module
+raises: there is no fallback implementation.
+"""
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB
+
+GREEDY = 0
+STOCHASTIC = 1
+
+KC_LMHEAD, KC_VERIFY, KC_ATTN, KC_GEMV = 0, 1, 2, 3
+
+STATUS_TIMEOUT = 1
+STATUS_BAD_TOKEN = 2
+STATUS_BAD_CTX = 4
+STATUS_NONFINITE = 8
+
+
+class MtpError(RuntimeError):
+    def __init__(self, code, what):
+        self.code = code
+        super().__init__("%s failed: %s (%d)" % (what, _lib().mtp_error_string(code).decode(), code))
+
+
+class MtpDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("d", ctypes.c_int32), ("Hq", ctypes.c_int32),
+                ("Hkv", ctypes.c_int32), ("Dh", ctypes.c_int32), ("F", ctypes.c_int32),
+                ("V", ctypes.c_int32), ("Lmax", ctypes.c_int32), ("rms_eps", ctypes.c_float)]
+
+
+WEIGHT_FIELDS = ("E", "fc", "wq", "wk", "wv", "wo", "wgate", "wup", "wdown",
+                 "g_emb", "g_hid", "g_attn", "g_mlp", "g_final")
+
+
+class MtpWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_FIELDS]
+
+
+_LIB = None
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB):
+            raise RuntimeError("libmtpspec.so is not built (%s); run __graft_entry__.build()" % LIB)
+        L = ctypes.CDLL(LIB)
+        P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        L.mtp_workspace_size.argtypes = [ctypes.POINTER(MtpDims), I]
+        L.mtp_workspace_size.restype = Z
+        L.mtp_draft.argtypes = [ctypes.POINTER(MtpDims), ctypes.POINTER(MtpWeights), P, P, P, P, P, I, F, I,
+                                P, P, P, P, Z, P]
+        L.mtp_draft.restype = I
+        L.spec_verify_workspace_size.argtypes = [I, I, I]
+        L.spec_verify_workspace_size.restype = Z
+        L.spec_verify.argtypes = [I, I, I, F, I, P, P, P, P, P, P, P, P, P, Z, P]
+        L.spec_verify.restype = I
+        L.spec_step.argtypes = [ctypes.POINTER(MtpDims), ctypes.POINTER(MtpWeights), P, P, P, P, P, I, F, I,
+                                P, P, P, P, P, P, P, P, P, P, Z, P]
+        L.spec_step.restype = I
+        L.mtp_get_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
+        L.mtp_get_status.restype = I
+        L.mtp_clear_status.argtypes = [P, P]
+        L.mtp_clear_status.restype = I
+        L.mtp_error_string.argtypes = [I]
+        L.mtp_error_string.restype = ctypes.c_char_p
+        L.mtp_profiler_enable.argtypes = [I]
+        L.mtp_profiler_enable.restype = I
+        L.mtp_profiler_read.argtypes = [I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)]
+        L.mtp_profiler_read.restype = I
+        L.mtp_launch_count.argtypes = []
+        L.mtp_launch_count.restype = ctypes.c_int64
+        _LIB = L
+    return _LIB
+
+
+def library():
+    """The loaded ctypes library (loads it on first use)."""
+    return _lib()
+
+
+def _ptr(t, name, dtype=None, numel=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if numel is not None and t.numel() < numel:
+        raise ValueError("%s has %d elements, needs %d" % (name, t.numel(), numel))
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def make_dims(B, d, Hq, Hkv, Dh, F, V, Lmax, eps=1e-6):
+    return MtpDims(B, d, Hq, Hkv, Dh, F, V, Lmax, eps)
+
+
+def make_weights(w):
+    """MtpWeights from a dict of bf16 CUDA tensors keyed by WEIGHT_FIELDS."""
+    return MtpWeights(*[_ptr(w[n], n, torch.bfloat16) for n in WEIGHT_FIELDS])
+
+
+def workspace_size(dims, k):
+    return int(_lib().mtp_workspace_size(ctypes.byref(dims), int(k)))
+
+
+def verify_workspace_size(B, k, V):
+    return int(_lib().spec_verify_workspace_size(int(B), int(k), int(V)))
+
+
+def alloc_workspace(nbytes, device=None):
+    """A 256-byte aligned uint8 CUDA buffer of at least nbytes."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def mtp_draft(dims, weights, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode, u_draft,
+              draft_tok, draft_logits, ws, stream=None):
+    B, V = dims.B, dims.V
+    rc = _lib().mtp_draft(
+        ctypes.byref(dims), ctypes.byref(weights), _ptr(h, "h", torch.bfloat16, B * dims.d),
+        _ptr(last_tok, "last_tok", torch.int32, B), _ptr(k_cache, "k_cache", torch.bfloat16),
+        _ptr(v_cache, "v_cache", torch.bfloat16), _ptr(ctx_len, "ctx_len", torch.int32, B), int(k),
+        float(T), int(mode), _ptr(u_draft, "u_draft", torch.float32, B * k),
+        _ptr(draft_tok, "draft_tok", torch.int32, B * k),
+        _ptr(draft_logits, "draft_logits", torch.float32, B * k * V),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
+    if rc != 0:
+        raise MtpError(rc, "mtp_draft")
+
+
+def spec_verify(B, k, V, T, mode, target_logits, draft_logits, draft_tok, u_accept, u_final,
+                out_tok, accept_len, num_accepted, ws, stream=None):
+    rc = _lib().spec_verify(
+        int(B), int(k), int(V), float(T), int(mode),
+        _ptr(target_logits, "target_logits", torch.float32, B * (k + 1) * V),
+        _ptr(draft_logits, "draft_logits", torch.float32, B * k * V),
+        _ptr(draft_tok, "draft_tok", torch.int32, B * k),
+        _ptr(u_accept, "u_accept", torch.float32, B * k), _ptr(u_final, "u_final", torch.float32, B),
+        _ptr(out_tok, "out_tok", torch.int32, B * (k + 1)), _ptr(accept_len, "accept_len", torch.int32, B),
+        _ptr(num_accepted, "num_accepted", torch.int32, B),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
+    if rc != 0:
+        raise MtpError(rc, "spec_verify")
+
+
+def spec_step(dims, weights, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode, u_draft,
+              target_logits, u_accept, u_final, draft_tok, draft_logits, out_tok, accept_len,
+              num_accepted, ws, stream=None):
+    B, V = dims.B, dims.V
+    rc = _lib().spec_step(
+        ctypes.byref(dims), ctypes.byref(weights), _ptr(h, "h", torch.bfloat16, B * dims.d),
+        _ptr(last_tok, "last_tok", torch.int32, B), _ptr(k_cache, "k_cache", torch.bfloat16),
+        _ptr(v_cache, "v_cache", torch.bfloat16), _ptr(ctx_len, "ctx_len", torch.int32, B), int(k),
+        float(T), int(mode), _ptr(u_draft, "u_draft", torch.float32, B * k),
+        _ptr(target_logits, "target_logits", torch.float32, B * (k + 1) * V),
+        _ptr(u_accept, "u_accept", torch.float32, B * k), _ptr(u_final, "u_final", torch.float32, B),
+        _ptr(draft_tok, "draft_tok", torch.int32, B * k),
+        _ptr(draft_logits, "draft_logits", torch.float32, B * k * V),
+        _ptr(out_tok, "out_tok", torch.int32, B * (k + 1)), _ptr(accept_len, "accept_len", torch.int32, B),
+        _ptr(num_accepted, "num_accepted", torch.int32, B),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
+    if rc != 0:
+        raise MtpError(rc, "spec_step")
+
+
+def get_status(ws, stream=None):
+    v = ctypes.c_int32(0)
+    rc = _lib().mtp_get_status(_ptr(ws, "ws"), _stream(stream), ctypes.byref(v))
+    if rc != 0:
+        raise MtpError(rc, "mtp_get_status")
+    return int(v.value)
+
+
+def clear_status(ws, stream=None):
+    rc = _lib().mtp_clear_status(_ptr(ws, "ws"), _stream(stream))
+    if rc != 0:
+        raise MtpError(rc, "mtp_clear_status")
+
+
+def profiler_enable(on=True):
+    _lib().mtp_profiler_enable(1 if on else 0)
+
+
+def profiler_read(kernel_class):
+    ms = ctypes.c_double(0.0)
+    n = ctypes.c_int64(0)
+    rc = _lib().mtp_profiler_read(int(kernel_class), ctypes.byref(ms), ctypes.byref(n))
+    if rc != 0:
+        raise MtpError(rc, "mtp_profiler_read")
+    return float(ms.value), int(n.value)
+
+
+def launch_count():
+    return int(_lib().mtp_launch_count())

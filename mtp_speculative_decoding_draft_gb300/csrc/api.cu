@@ -1,0 +1,366 @@
+// C-ABI entry points of libmtpspec: argument validation, workspace layout and
+// the launch sequence of the draft chain and the verifier on one stream.
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+#include "mtpspec.h"
+
+namespace mtp {
+
+static std::atomic<long long> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+namespace {
+
+constexpr int kMaxLmGrid = 2048;   // upper bound on LM-head CTAs (workspace sizing)
+constexpr size_t kAlign = 256;
+
+size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct DevInfo {
+  bool init = false;
+  int sms = 0;
+  int max_cluster = 8;
+};
+std::mutex g_mu;
+DevInfo g_dev[64];
+
+int device_info(DevInfo *out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MTP_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo &di = g_dev[dev];
+  if (!di.init) {
+    if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MTP_ERR_CUDA;
+    // clusters of 16 CTAs are a non-portable size: use them only if the device
+    // can keep one resident with the verifier's shared-memory footprint
+    di.max_cluster = 8;
+    if (verify_set_attributes(16) == cudaSuccess && verify_max_active_clusters(16) > 0) {
+      di.max_cluster = 16;
+    } else {
+      cudaGetLastError();
+      if (verify_set_attributes(8) != cudaSuccess) return MTP_ERR_CUDA;
+    }
+    di.init = true;
+  }
+  *out = di;
+  return MTP_OK;
+}
+
+bool aligned16(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_dims(const MtpDims *d, int k) {
+  if (!d) return MTP_ERR_INVALID_ARG;
+  if (k < 1 || k > 8) return MTP_ERR_INVALID_ARG;
+  if (d->B < 1 || d->d < 8 || d->Hq < 1 || d->Hkv < 1 || d->F < 8 || d->V < 1) return MTP_ERR_INVALID_ARG;
+  if (!(d->rms_eps >= 0.f)) return MTP_ERR_INVALID_ARG;
+  if (d->Lmax < k + 1) return MTP_ERR_INVALID_ARG;
+  if (d->d % 8 || d->F % 8) return MTP_ERR_UNSUPPORTED_SHAPE;
+  if (d->Hq % d->Hkv || d->Hq / d->Hkv > kMaxGroup) return MTP_ERR_UNSUPPORTED_SHAPE;
+  if (d->Dh != 32 && d->Dh != 64 && d->Dh != 128) return MTP_ERR_UNSUPPORTED_SHAPE;
+  if ((long long)d->B * d->V * 8 >= (1ll << 62)) return MTP_ERR_UNSUPPORTED_SHAPE;
+  if (d->V > (1 << 30) || d->B > (1 << 20)) return MTP_ERR_UNSUPPORTED_SHAPE;
+  return MTP_OK;
+}
+
+struct WsLayout {
+  size_t status, lm_cnt, attn_cnt, x0, x1, x2, q, o, act, lm_part, attn_part, logits, total;
+};
+
+WsLayout draft_layout(const MtpDims &d, int k) {
+  WsLayout L{};
+  size_t off = 0;
+  L.status = off;
+  off += kAlign;
+  L.lm_cnt = off;
+  off += kAlign;
+  L.attn_cnt = off;
+  off += up((size_t)d.B * d.Hkv * 4);
+  L.x0 = off;
+  off += up((size_t)d.B * d.d * 4);
+  L.x1 = off;
+  off += up((size_t)d.B * d.d * 4);
+  L.x2 = off;
+  off += up((size_t)d.B * d.d * 4);
+  L.q = off;
+  off += up((size_t)d.B * d.Hq * d.Dh * 4);
+  L.o = off;
+  off += up((size_t)d.B * d.Hq * d.Dh * 4);
+  L.act = off;
+  off += up((size_t)d.B * d.F * 4);
+  L.lm_part = off;
+  off += up((size_t)d.B * kMaxLmGrid * 4 * 4);
+  const int chunks = (d.Lmax + kAttnChunk - 1) / kAttnChunk;
+  const int group = d.Hq / d.Hkv;
+  L.attn_part = off;
+  off += up((size_t)d.B * d.Hkv * chunks * group * (d.Dh + 2) * 4);
+  L.logits = off;
+  off += up((size_t)d.B * k * d.V * 4);
+  L.total = off;
+  return L;
+}
+
+// profiler state
+struct Prof {
+  bool on = false;
+  std::vector<cudaEvent_t> ev[MTP_KC_COUNT];  // start/stop pairs
+  size_t used[MTP_KC_COUNT] = {0, 0, 0, 0};
+};
+Prof g_prof;
+std::mutex g_prof_mu;
+
+template <class F>
+cudaError_t timed(int kc, cudaStream_t s, F &&launch) {
+  if (!g_prof.on) return launch();
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  auto &v = g_prof.ev[kc];
+  size_t i = g_prof.used[kc];
+  if (2 * i + 2 > v.size()) {
+    for (int t = 0; t < 256; ++t) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return cudaErrorMemoryAllocation;
+      v.push_back(e);
+    }
+  }
+  cudaEventRecord(v[2 * i], s);
+  cudaError_t e = launch();
+  cudaEventRecord(v[2 * i + 1], s);
+  g_prof.used[kc] = i + 1;
+  return e;
+}
+
+struct Draft {
+  DraftCtx c;
+  GemvPlan fc, qkv, wo, gateup, down, lm;
+};
+
+int prepare_draft(const MtpDims *dims, const MtpWeights *w, const void *h, const int32_t *last_tok, void *k_cache,
+                  void *v_cache, const int32_t *ctx_len, int k, float T, int mode, const float *u_draft,
+                  int32_t *draft_tok, float *draft_logits, void *ws, size_t ws_bytes, bool logits_in_ws,
+                  Draft *out) {
+  int rc = check_dims(dims, k);
+  if (rc) return rc;
+  if (!w) return MTP_ERR_INVALID_ARG;
+  if (mode != MTP_GREEDY && mode != MTP_STOCHASTIC) return MTP_ERR_INVALID_ARG;
+  if (mode == MTP_STOCHASTIC && !(T > 0.f && T < 1e30f)) return MTP_ERR_INVALID_ARG;
+  const void *ptrs[] = {w->E, w->fc, w->wq, w->wk, w->wv, w->wo, w->wgate, w->wup, w->wdown, w->g_emb,
+                        w->g_hid, w->g_attn, w->g_mlp, w->g_final, h, last_tok, k_cache, v_cache, ctx_len,
+                        draft_tok, ws};
+  for (const void *p : ptrs)
+    if (!aligned16(p)) return MTP_ERR_INVALID_ARG;
+  if (mode == MTP_STOCHASTIC && !aligned16(u_draft)) return MTP_ERR_INVALID_ARG;
+  if (mode == MTP_STOCHASTIC && !logits_in_ws && !aligned16(draft_logits)) return MTP_ERR_INVALID_ARG;
+  if (draft_logits && !aligned16(draft_logits)) return MTP_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MTP_ERR_INVALID_ARG;
+  const WsLayout L = draft_layout(*dims, k);
+  if (ws_bytes < L.total) return MTP_ERR_WORKSPACE;
+  DevInfo di;
+  if ((rc = device_info(&di))) return rc;
+
+  const MtpDims &d = *dims;
+  DraftCtx &c = out->c;
+  c = DraftCtx{};
+  c.B = d.B; c.d = d.d; c.Hq = d.Hq; c.Hkv = d.Hkv; c.Dh = d.Dh; c.F = d.F; c.V = d.V; c.Lmax = d.Lmax;
+  c.k = k; c.j = 0; c.mode = mode; c.eps = d.rms_eps; c.T = mode == MTP_STOCHASTIC ? T : 1.f;
+  auto bf = [](const void *p) { return static_cast<const uint16_t *>(p); };
+  c.E = bf(w->E); c.fc = bf(w->fc); c.wq = bf(w->wq); c.wk = bf(w->wk); c.wv = bf(w->wv); c.wo = bf(w->wo);
+  c.wgate = bf(w->wgate); c.wup = bf(w->wup); c.wdown = bf(w->wdown);
+  c.g_emb = bf(w->g_emb); c.g_hid = bf(w->g_hid); c.g_attn = bf(w->g_attn); c.g_mlp = bf(w->g_mlp);
+  c.g_final = bf(w->g_final);
+  c.h = bf(h); c.last_tok = last_tok; c.ctx_len = ctx_len; c.u_draft = u_draft;
+  c.kc = static_cast<uint16_t *>(k_cache); c.vc = static_cast<uint16_t *>(v_cache);
+  c.draft_tok = draft_tok;
+  char *base = static_cast<char *>(ws);
+  c.logits = draft_logits ? draft_logits : (logits_in_ws ? reinterpret_cast<float *>(base + L.logits) : nullptr);
+  c.status = reinterpret_cast<int *>(base + L.status);
+  c.lm_cnt = reinterpret_cast<unsigned *>(base + L.lm_cnt);
+  c.attn_cnt = reinterpret_cast<unsigned *>(base + L.attn_cnt);
+  c.x0 = reinterpret_cast<float *>(base + L.x0);
+  c.x1 = reinterpret_cast<float *>(base + L.x1);
+  c.x2 = reinterpret_cast<float *>(base + L.x2);
+  c.q = reinterpret_cast<float *>(base + L.q);
+  c.o = reinterpret_cast<float *>(base + L.o);
+  c.act = reinterpret_cast<float *>(base + L.act);
+  c.lm_part = reinterpret_cast<float *>(base + L.lm_part);
+  c.attn_part = reinterpret_cast<float *>(base + L.attn_part);
+  c.attn_chunks = (d.Lmax + kAttnChunk - 1) / kAttnChunk;
+
+  out->fc = plan_gemv(OP_FC, d.d, 2 * d.d, d.B, di.sms);
+  out->qkv = plan_gemv(OP_QKV, (d.Hq + 2 * d.Hkv) * d.Dh, d.d, d.B, di.sms);
+  out->wo = plan_gemv(OP_WO, d.d, d.Hq * d.Dh, d.B, di.sms);
+  out->gateup = plan_gemv(OP_GATEUP, 2 * d.F, d.d, d.B, di.sms);
+  out->down = plan_gemv(OP_DOWN, d.d, d.F, d.B, di.sms);
+  out->lm = plan_gemv(OP_LMHEAD, d.V, d.d, d.B, di.sms);
+  if (out->lm.grid > kMaxLmGrid) return MTP_ERR_UNSUPPORTED_SHAPE;
+  c.lm_grid = out->lm.grid;
+  c.lm_rpc = out->lm.rows_per_cta;
+  return MTP_OK;
+}
+
+cudaError_t run_draft(Draft &D, cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
+  for (int j = 0; j < D.c.k && e == cudaSuccess; ++j) {
+    DraftCtx c = D.c;
+    c.j = j;
+    c.zero_counters = j == 0;
+    if ((e = timed(MTP_KC_GEMV, s, [&] { return launch_gemv(c, D.fc, s, true); }))) break;
+    if ((e = timed(MTP_KC_GEMV, s, [&] { return launch_gemv(c, D.qkv, s, true); }))) break;
+    if ((e = timed(MTP_KC_ATTN, s, [&] { return launch_attention(c, s, true); }))) break;
+    if ((e = timed(MTP_KC_GEMV, s, [&] { return launch_gemv(c, D.wo, s, true); }))) break;
+    if ((e = timed(MTP_KC_GEMV, s, [&] { return launch_gemv(c, D.gateup, s, true); }))) break;
+    if ((e = timed(MTP_KC_GEMV, s, [&] { return launch_gemv(c, D.down, s, true); }))) break;
+    if ((e = timed(MTP_KC_LMHEAD, s, [&] { return launch_gemv(c, D.lm, s, true); }))) break;
+  }
+  return e;
+}
+
+int prepare_verify(int B, int k, int V, float T, int mode, const float *target, const float *draft,
+                   const int32_t *draft_tok, const float *u_accept, const float *u_final, int32_t *out_tok,
+                   int32_t *accept_len, int32_t *num_accepted, void *ws, size_t ws_bytes, bool draft_check,
+                   VerifyArgs *a, int *cluster) {
+  if (B < 1 || k < 1 || k > 8 || V < 1 || V > (1 << 30) || B > (1 << 20)) return MTP_ERR_INVALID_ARG;
+  if (mode != MTP_GREEDY && mode != MTP_STOCHASTIC) return MTP_ERR_INVALID_ARG;
+  if (mode == MTP_STOCHASTIC && !(T > 0.f && T < 1e30f)) return MTP_ERR_INVALID_ARG;
+  const void *ptrs[] = {target, draft_tok, out_tok, accept_len, num_accepted, ws};
+  for (const void *p : ptrs)
+    if (!aligned16(p)) return MTP_ERR_INVALID_ARG;
+  if (mode == MTP_STOCHASTIC) {
+    if (draft_check && !aligned16(draft)) return MTP_ERR_INVALID_ARG;
+    if (!aligned16(u_accept) || !aligned16(u_final)) return MTP_ERR_INVALID_ARG;
+  }
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MTP_ERR_INVALID_ARG;
+  if (ws_bytes < kAlign) return MTP_ERR_WORKSPACE;
+  DevInfo di;
+  int rc = device_info(&di);
+  if (rc) return rc;
+  a->B = B; a->k = k; a->V = V; a->mode = mode; a->T = mode == MTP_STOCHASTIC ? T : 1.f;
+  a->target = target; a->draft = draft; a->draft_tok = draft_tok; a->u_accept = u_accept; a->u_final = u_final;
+  a->out_tok = out_tok; a->accept_len = accept_len; a->num_accepted = num_accepted;
+  a->status = static_cast<int *>(ws);
+  *cluster = verify_cluster_size(B, di.sms, di.max_cluster);
+  return MTP_OK;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MTP_OK : MTP_ERR_CUDA; }
+
+}  // namespace
+}  // namespace mtp
+
+using namespace mtp;
+
+extern "C" {
+
+size_t mtp_workspace_size(const MtpDims *dims, int k) {
+  if (check_dims(dims, k) != MTP_OK) return 0;
+  return draft_layout(*dims, k).total;
+}
+
+int mtp_draft(const MtpDims *dims, const MtpWeights *w, const void *h, const int32_t *last_tok, void *k_cache,
+              void *v_cache, const int32_t *ctx_len, int k, float T, int mode, const float *u_draft,
+              int32_t *draft_tok, float *draft_logits, void *ws, size_t ws_bytes, mtp_stream_t stream) {
+  Draft D;
+  int rc = prepare_draft(dims, w, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode, u_draft, draft_tok,
+                         draft_logits, ws, ws_bytes, false, &D);
+  if (rc) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = run_draft(D, s);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return cuda_rc(e);
+}
+
+size_t spec_verify_workspace_size(int B, int k, int V) {
+  if (B < 1 || k < 1 || k > 8 || V < 1) return 0;
+  return kAlign;
+}
+
+int spec_verify(int B, int k, int V, float T, int mode, const float *target_logits, const float *draft_logits,
+                const int32_t *draft_tok, const float *u_accept, const float *u_final, int32_t *out_tok,
+                int32_t *accept_len, int32_t *num_accepted, void *ws, size_t ws_bytes, mtp_stream_t stream) {
+  VerifyArgs a{};
+  int cluster = 1;
+  int rc = prepare_verify(B, k, V, T, mode, target_logits, draft_logits, draft_tok, u_accept, u_final, out_tok,
+                          accept_len, num_accepted, ws, ws_bytes, true, &a, &cluster);
+  if (rc) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = timed(MTP_KC_VERIFY, s, [&] { return launch_verify(a, cluster, s, false); });
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return cuda_rc(e);
+}
+
+int spec_step(const MtpDims *dims, const MtpWeights *w, const void *h, const int32_t *last_tok, void *k_cache,
+              void *v_cache, const int32_t *ctx_len, int k, float T, int mode, const float *u_draft,
+              const float *target_logits, const float *u_accept, const float *u_final, int32_t *draft_tok,
+              float *draft_logits, int32_t *out_tok, int32_t *accept_len, int32_t *num_accepted, void *ws,
+              size_t ws_bytes, mtp_stream_t stream) {
+  Draft D;
+  int rc = prepare_draft(dims, w, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode, u_draft, draft_tok,
+                         draft_logits, ws, ws_bytes, mode == MTP_STOCHASTIC, &D);
+  if (rc) return rc;
+  VerifyArgs a{};
+  int cluster = 1;
+  rc = prepare_verify(dims->B, k, dims->V, T, mode, target_logits, D.c.logits, draft_tok, u_accept, u_final, out_tok,
+                      accept_len, num_accepted, ws, ws_bytes, false, &a, &cluster);
+  if (rc) return rc;
+  a.status = D.c.status;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = run_draft(D, s);
+  if (e == cudaSuccess) e = timed(MTP_KC_VERIFY, s, [&] { return launch_verify(a, cluster, s, true); });
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return cuda_rc(e);
+}
+
+int mtp_get_status(const void *ws, mtp_stream_t stream, int32_t *status) {
+  if (!ws || !status) return MTP_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return MTP_ERR_CUDA;
+  *status = v;
+  return MTP_OK;
+}
+
+int mtp_clear_status(void *ws, mtp_stream_t stream) {
+  if (!ws) return MTP_ERR_INVALID_ARG;
+  return cuda_rc(cudaMemsetAsync(ws, 0, sizeof(int32_t), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char *mtp_error_string(int code) {
+  switch (code) {
+    case MTP_OK: return "ok";
+    case MTP_ERR_INVALID_ARG: return "invalid argument";
+    case MTP_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MTP_ERR_WORKSPACE: return "workspace too small";
+    case MTP_ERR_CUDA: return "CUDA error";
+    default: return "unknown error";
+  }
+}
+
+int mtp_profiler_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof.on = on != 0;
+  for (int i = 0; i < MTP_KC_COUNT; ++i) g_prof.used[i] = 0;
+  return MTP_OK;
+}
+
+int mtp_profiler_read(int kernel_class, double *total_ms, int64_t *launches) {
+  if (kernel_class < 0 || kernel_class >= MTP_KC_COUNT || !total_ms || !launches) return MTP_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  double t = 0.0;
+  auto &v = g_prof.ev[kernel_class];
+  for (size_t i = 0; i < g_prof.used[kernel_class]; ++i) {
+    if (cudaEventSynchronize(v[2 * i + 1]) != cudaSuccess) return MTP_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, v[2 * i], v[2 * i + 1]) != cudaSuccess) return MTP_ERR_CUDA;
+    t += ms;
+  }
+  *total_ms = t;
+  *launches = (int64_t)g_prof.used[kernel_class];
+  return MTP_OK;
+}
+
+int64_t mtp_launch_count(void) { return (int64_t)g_launches.load(); }
+
+}  // extern "C"

@@ -1,0 +1,101 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Plain structs of pointers and sizes, passed by value to
+// the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mtp {
+
+// Everything one depth of the draft chain reads or writes.
+struct DraftCtx {
+  // shape
+  int B, d, Hq, Hkv, Dh, F, V, Lmax, k, j, mode;
+  float eps, T;
+  // weights (bf16)
+  const uint16_t *E, *fc, *wq, *wk, *wv, *wo, *wgate, *wup, *wdown;
+  const uint16_t *g_emb, *g_hid, *g_attn, *g_mlp, *g_final;
+  // caller inputs
+  const uint16_t *h;      // [B, d] trunk hidden state
+  const int *last_tok;    // [B]
+  const int *ctx_len;     // [B]
+  const float *u_draft;   // [B, k]
+  uint16_t *kc, *vc;      // [B, Hkv, Lmax, Dh]
+  // outputs
+  int *draft_tok;         // [B, k]
+  float *logits;          // [B, k, V] or null (greedy without logits)
+  // workspace
+  int *status;
+  unsigned *lm_cnt;       // 1 ticket counter
+  unsigned *attn_cnt;     // [B * Hkv] ticket counters
+  float *x0, *x1, *x2;    // [B, d]
+  float *q, *o;           // [B, Hq*Dh]
+  float *act;             // [B, F]
+  float *lm_part;         // [B, lm_grid, 4]
+  float *attn_part;       // [B, Hkv, attn_chunks, group*(Dh+2)]
+  int lm_grid;            // CTAs of the LM-head launch
+  int lm_rpc;             // vocabulary rows per LM-head CTA
+  int attn_chunks;        // chunk slots per (b, kv head)
+  int zero_counters;      // this launch clears the ticket counters first
+};
+
+enum GemvOp { OP_FC = 0, OP_QKV = 1, OP_WO = 2, OP_GATEUP = 3, OP_DOWN = 4, OP_LMHEAD = 5 };
+
+// How one weight-streaming GEMV launch is cut up.
+struct GemvPlan {
+  int op;
+  int N;             // virtual rows
+  int K;             // columns
+  int P;             // column pieces per row (divides the warps per CTA)
+  int PC;            // columns per piece (multiple of 8)
+  int nv;            // 16-byte vectors per lane per piece = ceil(PC / 256)
+  int rows_per_cta;  // contiguous rows per CTA (even for the gate/up pair layout)
+  int grid;          // CTAs
+  int bg;            // batch rows per group (activation registers per lane)
+  int ngroups;       // batch groups = ceil(B / bg)
+  int stages;        // TMA ring depth per warp
+  size_t smem;       // dynamic shared memory bytes
+};
+
+constexpr int kGemvWarps = 8;
+constexpr int kGemvThreads = kGemvWarps * 32;
+constexpr int kAttnChunk = 64;      // tokens per attention CTA
+constexpr int kAttnThreads = 128;
+constexpr int kMaxGroup = 8;        // Hq / Hkv
+
+GemvPlan plan_gemv(int op, int N, int K, int B, int num_sms);
+cudaError_t launch_gemv(const DraftCtx &c, const GemvPlan &g, cudaStream_t s, bool pdl);
+cudaError_t launch_attention(const DraftCtx &c, cudaStream_t s, bool pdl);
+size_t attention_smem_bytes(int Dh);
+
+// Verification launch.
+struct VerifyArgs {
+  int B, k, V, mode;
+  float T;
+  const float *target;   // [B, k+1, V]
+  const float *draft;    // [B, k, V]
+  const int *draft_tok;  // [B, k]
+  const float *u_accept; // [B, k]
+  const float *u_final;  // [B]
+  int *out_tok;          // [B, k+1]
+  int *accept_len;       // [B]
+  int *num_accepted;     // [B]
+  int *status;
+};
+
+constexpr int kVerifyThreads = 256;
+constexpr int kVerifyPiece = 4096;  // floats per TMA piece (16 KB)
+constexpr int kVerifyStages = 4;
+
+int verify_cluster_size(int B, int num_sms, int max_cluster);
+size_t verify_smem_bytes(int B, int k, int V, int cluster);
+cudaError_t launch_verify(const VerifyArgs &a, int cluster, cudaStream_t s, bool pdl);
+cudaError_t verify_set_attributes(int max_cluster);
+int verify_max_active_clusters(int cluster);
+
+// bookkeeping shared with api.cu
+void note_launch();
+
+}  // namespace mtp

@@ -1,0 +1,58 @@
+"""The C-ABI library builds, loads and exports every declared entry point.
+
+No compute call is made here (no GPU needed); only host-side validation paths.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "mtpspec.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?(?:int|size_t|int64_t|char)\s*\*?\s*(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mtp_speculative_decoding_draft_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("mtp_draft", "spec_verify", "spec_step", "mtp_workspace_size", "spec_verify_workspace_size",
+              "mtp_get_status", "mtp_clear_status", "mtp_error_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in _declared_functions():
+        assert hasattr(lib, n), "missing export %s" % n
+
+
+def test_host_side_validation_without_gpu(lib):
+    from mtp_speculative_decoding_draft_gb300 import binding as bd
+    L = bd.library()
+    dims = bd.make_dims(1, 4096, 32, 8, 128, 12288, 151936, 4099)
+    n = L.mtp_workspace_size(ctypes.byref(dims), 3)
+    assert n > 3 * 4096 * 4
+    assert L.mtp_workspace_size(ctypes.byref(dims), 0) == 0           # k outside 1..8
+    assert L.mtp_workspace_size(ctypes.byref(dims), 9) == 0
+    bad = bd.make_dims(1, 4096, 32, 6, 128, 12288, 151936, 4099)      # Hq % Hkv != 0
+    assert L.mtp_workspace_size(ctypes.byref(bad), 3) == 0
+    bad = bd.make_dims(1, 4096, 32, 8, 96, 12288, 151936, 4099)       # unsupported head size
+    assert L.mtp_workspace_size(ctypes.byref(bad), 3) == 0
+    # argument errors are reported before any device work
+    assert L.spec_verify(4, 0, 100, 1.0, 0, None, None, None, None, None, None, None, None, None, 0, None) == -1
+    assert L.spec_verify(4, 3, 100, 1.0, 0, None, None, None, None, None, None, None, None, None, 0, None) == -1
+    assert L.mtp_draft(None, None, None, None, None, None, None, 3, 1.0, 0, None, None, None, None, 0, None) == -1
+    assert L.mtp_error_string(-3) == b"workspace too small"
+    assert L.spec_verify_workspace_size(4, 3, 100) >= 4
