@@ -110,9 +110,10 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- CPU oracle timing
 
-def _oracle_sample(workload_name, depths):
-    """Run the oracle on `depths` draft depths plus the verification of one
-    step of the workload; return (seconds for the depths, seconds for verify)."""
+def _oracle_samples(workload_name, depths, n):
+    """Generate the workload once, then time the oracle n times on `depths`
+    draft depths plus the verification of one step; returns a list of
+    (seconds for the depths, seconds for the verification)."""
     from oracle.block import Dims, mtp_draft
     from oracle.verify import spec_verify
     w = W.WORKLOADS[workload_name]
@@ -121,32 +122,34 @@ def _oracle_sample(workload_name, depths):
     u = W.make_uniforms(w)
     tl = W.target_logits(w)
     dims = Dims(w.B, w.d, w.Hq, w.Hkv, w.Dh, w.F, w.V, w.Lmax, w.eps)
-    t0 = time.perf_counter()
-    dr = mtp_draft(wts, dims, ctx["h"], ctx["last_tok"], ctx["k_cache"], ctx["v_cache"], ctx["ctx_len"],
-                   depths, w.T, w.mode, u["u_draft"])
-    t1 = time.perf_counter()
-    dt = np.zeros((w.B, w.k), np.int64)
-    dt[:, :depths] = dr["draft_tok"]
-    dl = np.zeros((w.B, w.k, w.V))
-    dl[:, :depths] = dr["draft_logits"]
-    spec_verify(tl, dl, dt, w.mode, w.T, u["u_accept"], u["u_final"])
-    t2 = time.perf_counter()
-    return t1 - t0, t2 - t1
+    out = []
+    for _ in range(n):
+        t0 = time.perf_counter()
+        dr = mtp_draft(wts, dims, ctx["h"], ctx["last_tok"], ctx["k_cache"], ctx["v_cache"], ctx["ctx_len"],
+                       depths, w.T, w.mode, u["u_draft"])
+        t1 = time.perf_counter()
+        dt = np.zeros((w.B, w.k), np.int64)
+        dt[:, :depths] = dr["draft_tok"]
+        dl = np.zeros((w.B, w.k, w.V))
+        dl[:, :depths] = dr["draft_logits"]
+        spec_verify(tl, dl, dt, w.mode, w.T, u["u_accept"], u["u_final"])
+        out.append((t1 - t0, time.perf_counter() - t1))
+    return out
 
 
-def cpu_oracle_steps_per_s(workload_name, depths):
-    """Time the oracle in a fresh single-threaded process (BLAS pinned to 1 thread)."""
+def cpu_oracle_step_times(workload_name, depths, n):
+    """Step times of the oracle, measured in a fresh single-threaded process
+    (BLAS pinned to one thread); each sample runs `depths` draft depths and
+    the verification, and is scaled to the workload's k depths."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     code = ("import json,sys; sys.path.insert(0, %r); import bench; "
-            "print(json.dumps(bench._oracle_sample(%r, %d)))" % (ROOT, workload_name, depths))
-    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=1800)
+            "print(json.dumps(bench._oracle_samples(%r, %d, %d)))" % (ROOT, workload_name, depths, n))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=3600)
     if r.returncode != 0:
         raise RuntimeError("oracle timing failed: " + r.stderr[-2000:])
-    t_depths, t_verify = json.loads(r.stdout.strip().splitlines()[-1])
     w = W.WORKLOADS[workload_name]
-    t_step = t_depths / depths * w.k + t_verify
-    return 1.0 / t_step, t_step
+    return [td / depths * w.k + tv for td, tv in json.loads(r.stdout.strip().splitlines()[-1])]
 
 
 def run_reference(args):
@@ -154,11 +157,7 @@ def run_reference(args):
     if rank != 0:
         return
     w = W.WORKLOADS[args.workload]
-    times = []
-    for i in range(args.warmup + args.steps):
-        sps, t_step = cpu_oracle_steps_per_s(args.workload, 1)
-        if i >= args.warmup:
-            times.append(t_step)
+    times = cpu_oracle_step_times(args.workload, 1, args.warmup + args.steps)[args.warmup:]
     t = float(np.mean(times))
     value = 1.0 / t
     sample = ("per step: the oracle runs one draft depth of this workload plus its verification in a "
@@ -182,6 +181,65 @@ def config_of(w, args):
 
 # ----------------------------------------------------------------------------- GPU arm
 
+def verify_bytes(w):
+    """Algorithmic bytes of one spec_verify: every logit row read once."""
+    rows = w.B * (w.k + 1) + (w.B * w.k if w.mode == 1 else 0)
+    return rows * w.V * 4
+
+
+def run_verify_only(args, w):
+    """spec_verify on the verify sweep: B sequences, k drafts, V-wide rows."""
+    import torch
+    from mtp_speculative_decoding_draft_gb300 import binding as bd
+    from mtp_speculative_decoding_draft_gb300.build import build
+    from mtp_speculative_decoding_draft_gb300.model import Verifier, to_device
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    build()
+    inp = W.verify_inputs(w)
+    # drafts: the argmax of each draft row (a deterministic stand-in for a draw
+    # from q; the verifier reads every row whatever the drafts are)
+    d = inp["draft_logits"].argmax(axis=2).astype(np.int32)
+    t_d, l_d, d_d = to_device(inp["target_logits"]), to_device(inp["draft_logits"]), to_device(d)
+    ua, uf = to_device(inp["u_accept"]), to_device(inp["u_final"])
+    ver = Verifier(w.B, w.k, w.V)
+    stoch = w.mode == 1
+
+    def step():
+        ver(w.T, w.mode, t_d, l_d if stoch else None, d_d, ua if stoch else None, uf if stoch else None)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    n0 = bd.launch_count()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    launches = bd.launch_count() - n0
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    assert bd.get_status(ver.ws) == 0
+    out, L, acc = ver.results()
+    peak, peak_kind = measured_peaks()
+    vb = verify_bytes(w)
+    ach = vb / (ms * 1e-3) / 1e9
+    line = {"metric": METRIC, "value": 1e3 / ms, "unit": "verify calls/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32 logits", "data": "synthetic (seeded)", "config": config_of(w, args),
+            "accept_len_mean": float(L.mean()),
+            "roofline": {"bound": "hbm", "kernel": "verify_kernel", "achieved": ach, "peak": peak, "unit": "GB/s",
+                         "frac": ach / peak, "peak_kind": peak_kind, "traffic": None, "bytes_per_launch": vb,
+                         "avg_launch_ms": ms, "launches": args.steps},
+            "gpu_launches": int(launches), "clocks": clk}
+    print(json.dumps(line), flush=True)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -195,13 +253,18 @@ def run_ours(args):
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl")
+    w = W.WORKLOADS[args.workload]
+    if w.verify_only:
+        if args.k:
+            w = W.with_k(w, args.k)
+        if args.greedy:
+            w = W.replace(w, mode=W.GREEDY)
+        return run_verify_only(args, w)
     if rank == 0 or world == 1:
         build()
     if world > 1:
         dist.barrier()
         build()
-
-    w = W.WORKLOADS[args.workload]
     stoch = w.mode == 1
     wts = W.make_weights(w)
     ctx = W.make_context(w)
@@ -347,8 +410,8 @@ def run_ours(args):
     }
     if not args.no_cpu_baseline and world >= 1:
         try:
-            sps, t_step = cpu_oracle_steps_per_s(args.workload, w.k)
-            line["cpu_baseline"] = {"value": sps, "unit": "steps/s", "cores": 1, "kind": "oracle",
+            t_step = cpu_oracle_step_times(args.workload, w.k, 1)[0]
+            line["cpu_baseline"] = {"value": 1.0 / t_step, "unit": "steps/s", "cores": 1, "kind": "oracle",
                                     "sample": "one full step (all %d depths + verification) of this workload, "
                                               "single-threaded float64 numpy" % w.k}
         except Exception as e:  # report, do not hide
@@ -367,6 +430,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=W.SINGLE_GREEDY.name, choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--k", type=int, default=0, help="draft depth for the verify sweep (1..5)")
+    ap.add_argument("--greedy", action="store_true", help="greedy verification for the verify sweep")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

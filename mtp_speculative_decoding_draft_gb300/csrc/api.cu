@@ -1,5 +1,7 @@
 // C-ABI entry points of libmtpspec: argument validation, workspace layout and
 // the launch sequence of the draft chain and the verifier on one stream.
+#include <stdlib.h>
+
 #include <atomic>
 #include <mutex>
 #include <vector>
@@ -66,7 +68,7 @@ int check_dims(const MtpDims *d, int k) {
 }
 
 struct WsLayout {
-  size_t status, lm_cnt, attn_cnt, x0, x1, x2, q, o, act, lm_part, attn_part, logits, total;
+  size_t status, lm_cnt, x0, x1, x2, q, o, act, lm_part, logits, total;
 };
 
 WsLayout draft_layout(const MtpDims &d, int k) {
@@ -76,8 +78,6 @@ WsLayout draft_layout(const MtpDims &d, int k) {
   off += kAlign;
   L.lm_cnt = off;
   off += kAlign;
-  L.attn_cnt = off;
-  off += up((size_t)d.B * d.Hkv * 4);
   L.x0 = off;
   off += up((size_t)d.B * d.d * 4);
   L.x1 = off;
@@ -92,10 +92,6 @@ WsLayout draft_layout(const MtpDims &d, int k) {
   off += up((size_t)d.B * d.F * 4);
   L.lm_part = off;
   off += up((size_t)d.B * kMaxLmGrid * 4 * 4);
-  const int chunks = (d.Lmax + kAttnChunk - 1) / kAttnChunk;
-  const int group = d.Hq / d.Hkv;
-  L.attn_part = off;
-  off += up((size_t)d.B * d.Hkv * chunks * group * (d.Dh + 2) * 4);
   L.logits = off;
   off += up((size_t)d.B * k * d.V * 4);
   L.total = off;
@@ -134,6 +130,7 @@ cudaError_t timed(int kc, cudaStream_t s, F &&launch) {
 struct Draft {
   DraftCtx c;
   GemvPlan fc, qkv, wo, gateup, down, lm;
+  int attn_cluster;
 };
 
 int prepare_draft(const MtpDims *dims, const MtpWeights *w, const void *h, const int32_t *last_tok, void *k_cache,
@@ -176,7 +173,6 @@ int prepare_draft(const MtpDims *dims, const MtpWeights *w, const void *h, const
   c.logits = draft_logits ? draft_logits : (logits_in_ws ? reinterpret_cast<float *>(base + L.logits) : nullptr);
   c.status = reinterpret_cast<int *>(base + L.status);
   c.lm_cnt = reinterpret_cast<unsigned *>(base + L.lm_cnt);
-  c.attn_cnt = reinterpret_cast<unsigned *>(base + L.attn_cnt);
   c.x0 = reinterpret_cast<float *>(base + L.x0);
   c.x1 = reinterpret_cast<float *>(base + L.x1);
   c.x2 = reinterpret_cast<float *>(base + L.x2);
@@ -184,8 +180,7 @@ int prepare_draft(const MtpDims *dims, const MtpWeights *w, const void *h, const
   c.o = reinterpret_cast<float *>(base + L.o);
   c.act = reinterpret_cast<float *>(base + L.act);
   c.lm_part = reinterpret_cast<float *>(base + L.lm_part);
-  c.attn_part = reinterpret_cast<float *>(base + L.attn_part);
-  c.attn_chunks = (d.Lmax + kAttnChunk - 1) / kAttnChunk;
+  out->attn_cluster = attention_cluster_size(d.Lmax, di.max_cluster);
 
   out->fc = plan_gemv(OP_FC, d.d, 2 * d.d, d.B, di.sms);
   out->qkv = plan_gemv(OP_QKV, (d.Hq + 2 * d.Hkv) * d.Dh, d.d, d.B, di.sms);
@@ -199,19 +194,27 @@ int prepare_draft(const MtpDims *dims, const MtpWeights *w, const void *h, const
   return MTP_OK;
 }
 
+// Programmatic dependent launch between the chained kernels (MTP_PDL=0 turns it
+// off, for measurement).
+bool use_pdl() {
+  const char *v = getenv("MTP_PDL");
+  return !(v && v[0] == '0');
+}
+
 cudaError_t run_draft(Draft &D, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
+  const bool pdl = use_pdl();
   for (int j = 0; j < D.c.k && e == cudaSuccess; ++j) {
     DraftCtx c = D.c;
     c.j = j;
     c.zero_counters = j == 0;
-    if ((e = timed(MTP_KC_GEMV, s, [&] { return launch_gemv(c, D.fc, s, true); }))) break;
-    if ((e = timed(MTP_KC_GEMV, s, [&] { return launch_gemv(c, D.qkv, s, true); }))) break;
-    if ((e = timed(MTP_KC_ATTN, s, [&] { return launch_attention(c, s, true); }))) break;
-    if ((e = timed(MTP_KC_GEMV, s, [&] { return launch_gemv(c, D.wo, s, true); }))) break;
-    if ((e = timed(MTP_KC_GEMV, s, [&] { return launch_gemv(c, D.gateup, s, true); }))) break;
-    if ((e = timed(MTP_KC_GEMV, s, [&] { return launch_gemv(c, D.down, s, true); }))) break;
-    if ((e = timed(MTP_KC_LMHEAD, s, [&] { return launch_gemv(c, D.lm, s, true); }))) break;
+    if ((e = timed(MTP_KC_GEMV, s, [&] { return launch_gemv(c, D.fc, s, pdl); }))) break;
+    if ((e = timed(MTP_KC_GEMV, s, [&] { return launch_gemv(c, D.qkv, s, pdl); }))) break;
+    if ((e = timed(MTP_KC_ATTN, s, [&] { return launch_attention(c, D.attn_cluster, s, pdl); }))) break;
+    if ((e = timed(MTP_KC_GEMV, s, [&] { return launch_gemv(c, D.wo, s, pdl); }))) break;
+    if ((e = timed(MTP_KC_GEMV, s, [&] { return launch_gemv(c, D.gateup, s, pdl); }))) break;
+    if ((e = timed(MTP_KC_GEMV, s, [&] { return launch_gemv(c, D.down, s, pdl); }))) break;
+    if ((e = timed(MTP_KC_LMHEAD, s, [&] { return launch_gemv(c, D.lm, s, pdl); }))) break;
   }
   return e;
 }
@@ -306,7 +309,7 @@ int spec_step(const MtpDims *dims, const MtpWeights *w, const void *h, const int
   a.status = D.c.status;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = run_draft(D, s);
-  if (e == cudaSuccess) e = timed(MTP_KC_VERIFY, s, [&] { return launch_verify(a, cluster, s, true); });
+  if (e == cudaSuccess) e = timed(MTP_KC_VERIFY, s, [&] { return launch_verify(a, cluster, s, use_pdl()); });
   if (e == cudaSuccess) e = cudaGetLastError();
   return cuda_rc(e);
 }

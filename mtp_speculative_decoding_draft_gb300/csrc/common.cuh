@@ -158,6 +158,16 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void *local, uint32_t rank)
   return out;
 }
 
+// Generic pointer to the same shared variable in CTA `rank` of this cluster.
+// Loads through it are ordinary memory operations: the compiler may batch
+// independent ones, and the cluster barrier's memory clobber orders them.
+template <class T>
+__device__ __forceinline__ const T *dsmem_ptr(const T *local, uint32_t rank) {
+  uint64_t out;
+  asm("mapa.u64 %0, %1, %2;" : "=l"(out) : "l"(reinterpret_cast<uint64_t>(local)), "r"(rank));
+  return reinterpret_cast<const T *>(out);
+}
+
 __device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");

@@ -25,154 +25,13 @@
 // kv head); the GQA group's query heads share each K/V chunk, which is staged by
 // TMA.  The last chunk CTA of a (sequence, kv head) combines the partial
 // (max, sum, output) triples.
+#include <stdlib.h>
+
 #include "common.cuh"
+#include "draft_ops.cuh"
 #include "internal.h"
 
 namespace mtp {
-
-// ---------------------------------------------------------------- helpers
-
-__device__ __forceinline__ void load8_bf16(const uint16_t *p, float *out) {
-  uint4 w = __ldg(reinterpret_cast<const uint4 *>(p));
-  out[0] = bf16_lo(w.x); out[1] = bf16_hi(w.x);
-  out[2] = bf16_lo(w.y); out[3] = bf16_hi(w.y);
-  out[4] = bf16_lo(w.z); out[5] = bf16_hi(w.z);
-  out[6] = bf16_lo(w.w); out[7] = bf16_hi(w.w);
-}
-
-// fp32 data produced by an earlier kernel of the chain: read through L2.
-__device__ __forceinline__ void load8_f32(const float *p, float *out) {
-  float4 a = __ldcg(reinterpret_cast<const float4 *>(p));
-  float4 b = __ldcg(reinterpret_cast<const float4 *>(p) + 1);
-  out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
-  out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
-}
-
-__device__ __forceinline__ float block_sum_256(float v, float *red) {
-  v = warp_sum(v);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float t = 0.f;
-#pragma unroll
-  for (int i = 0; i < kGemvWarps; ++i) t += red[i];
-  return t;
-}
-
-// Token feeding depth j of sequence b (validated).
-__device__ __forceinline__ int depth_token(const DraftCtx &c, int b) {
-  int t = c.j == 0 ? __ldg(&c.last_tok[b]) : __ldcg(&c.draft_tok[b * c.k + c.j - 1]);
-  if (t < 0 || t >= c.V) {
-    set_status(c.status, kStatusBadToken);
-    t = 0;
-  }
-  return t;
-}
-
-__device__ __forceinline__ int clamped_ctx(const DraftCtx &c, int b) {
-  int L = __ldg(&c.ctx_len[b]);
-  return min(max(L, 0), c.Lmax - c.k);
-}
-
-// RMSNorm scale factors 1/sqrt(mean(v^2)+eps) of the vectors this op
-// normalises, for every batch row.  scales[2*b] is the first vector's (for the
-// input projection: the token embedding), scales[2*b+1] the second's (the
-// hidden state).
-template <int OP>
-__device__ void compute_scales(const DraftCtx &c, float *scales, float *red) {
-  if (OP == OP_WO || OP == OP_DOWN) return;
-  const int d = c.d;
-  for (int b = 0; b < c.B; ++b) {
-    float s0 = 0.f, s1 = 0.f;
-    if (OP == OP_FC) {
-      const uint16_t *e = c.E + (size_t)depth_token(c, b) * d;
-      for (int i = threadIdx.x * 8; i < d; i += kGemvThreads * 8) {
-        float v[8];
-        load8_bf16(e + i, v);
-#pragma unroll
-        for (int t = 0; t < 8; ++t) s0 = fmaf(v[t], v[t], s0);
-      }
-      for (int i = threadIdx.x * 8; i < d; i += kGemvThreads * 8) {
-        float v[8];
-        if (c.j == 0) load8_bf16(c.h + (size_t)b * d + i, v);
-        else load8_f32(c.x2 + (size_t)b * d + i, v);
-#pragma unroll
-        for (int t = 0; t < 8; ++t) s1 = fmaf(v[t], v[t], s1);
-      }
-    } else {
-      const float *x = OP == OP_QKV ? c.x0 : (OP == OP_GATEUP ? c.x1 : c.x2);
-      for (int i = threadIdx.x * 8; i < d; i += kGemvThreads * 8) {
-        float v[8];
-        load8_f32(x + (size_t)b * d + i, v);
-#pragma unroll
-        for (int t = 0; t < 8; ++t) s0 = fmaf(v[t], v[t], s0);
-      }
-    }
-    s0 = block_sum_256(s0, red);
-    if (OP == OP_FC) s1 = block_sum_256(s1, red);
-    if (threadIdx.x == 0) {
-      scales[2 * b] = rsqrtf(s0 / (float)d + c.eps);
-      scales[2 * b + 1] = rsqrtf(s1 / (float)d + c.eps);
-    }
-  }
-  __syncthreads();
-}
-
-// Eight consecutive activation values (columns col .. col+7) of batch row b.
-template <int OP>
-__device__ __forceinline__ void act8(const DraftCtx &c, int b, int col, const float *scales, float *out) {
-  const int d = c.d;
-  if (OP == OP_FC) {
-    float g[8];
-    if (col < d) {
-      load8_bf16(c.E + (size_t)depth_token(c, b) * d + col, out);
-      load8_bf16(c.g_emb + col, g);
-      const float s = scales[2 * b];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) out[t] = out[t] * s * g[t];
-    } else {
-      const int cc = col - d;
-      if (c.j == 0) load8_bf16(c.h + (size_t)b * d + cc, out);
-      else load8_f32(c.x2 + (size_t)b * d + cc, out);
-      load8_bf16(c.g_hid + cc, g);
-      const float s = scales[2 * b + 1];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) out[t] = out[t] * s * g[t];
-    }
-  } else if (OP == OP_WO) {
-    load8_f32(c.o + (size_t)b * c.Hq * c.Dh + col, out);
-  } else if (OP == OP_DOWN) {
-    load8_f32(c.act + (size_t)b * c.F + col, out);
-  } else {
-    const float *x = OP == OP_QKV ? c.x0 : (OP == OP_GATEUP ? c.x1 : c.x2);
-    const uint16_t *gp = OP == OP_QKV ? c.g_attn : (OP == OP_GATEUP ? c.g_mlp : c.g_final);
-    float g[8];
-    load8_f32(x + (size_t)b * d + col, out);
-    load8_bf16(gp + col, g);
-    const float s = scales[2 * b];
-#pragma unroll
-    for (int t = 0; t < 8; ++t) out[t] = out[t] * s * g[t];
-  }
-}
-
-template <int OP>
-__device__ __forceinline__ const uint16_t *weight_row(const DraftCtx &c, int row, int K) {
-  if (OP == OP_FC) return c.fc + (size_t)row * K;
-  if (OP == OP_QKV) {
-    const int nq = c.Hq * c.Dh, nkv = c.Hkv * c.Dh;
-    if (row < nq) return c.wq + (size_t)row * K;
-    row -= nq;
-    if (row < nkv) return c.wk + (size_t)row * K;
-    return c.wv + (size_t)(row - nkv) * K;
-  }
-  if (OP == OP_WO) return c.wo + (size_t)row * K;
-  if (OP == OP_GATEUP) return ((row & 1) ? c.wup : c.wgate) + (size_t)(row >> 1) * K;
-  if (OP == OP_DOWN) return c.wdown + (size_t)row * K;
-  return c.E + (size_t)row * K;
-}
-
-__device__ __forceinline__ float silu_f(float z) { return z / (1.f + __expf(-z)); }
 
 // ---------------------------------------------------------------- GEMV kernel
 
@@ -221,10 +80,7 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(DraftCtx c, GemvPlan
   grid_dep_wait();
   grid_dep_launch();
 
-  if (OP == OP_FC && c.zero_counters && blockIdx.x == 0) {
-    for (int i = threadIdx.x; i < c.B * c.Hkv; i += kGemvThreads) c.attn_cnt[i] = 0u;
-    if (threadIdx.x == 0) *c.lm_cnt = 0u;
-  }
+  if (OP == OP_FC && c.zero_counters && blockIdx.x == 0 && threadIdx.x == 0) *c.lm_cnt = 0u;
   compute_scales<OP>(c, scales, red);
 
   int n = 0;
@@ -364,105 +220,32 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(DraftCtx c, GemvPlan
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  const float cT = kLog2e / c.T;
-  const int G = c.lm_grid;
-  if (warp != 0) return;
-  for (int b = 0; b < c.B; ++b) {
-    const float *pb = c.lm_part + (size_t)b * G * 4;
-    float M = -INFINITY;
-    int Mi = 0x7fffffff;
-    for (int cta = lane; cta < G; cta += 32) argmax_merge(M, Mi, __ldcg(&pb[cta * 4]), __float_as_int(__ldcg(&pb[cta * 4 + 2])));
-    warp_argmax(M, Mi);
-    int tok = Mi;
-    if (M == -INFINITY || !(M == M)) {
-      if (lane == 0) set_status(c.status, kStatusNonFinite);
-      tok = 0;
-    } else if (c.mode == 1) {
-      // Inverse CDF of softmax(logits / T) at u: walk the per-CTA masses in
-      // vocabulary order, then rescan the CTA that holds the crossing.
-      const double u = (double)__ldg(&c.u_draft[b * c.k + c.j]);
-      double Z = 0.0;
-      if (lane == 0)
-        for (int cta = 0; cta < G; ++cta) {
-          const float mc = __ldcg(&pb[cta * 4]);
-          if (mc != -INFINITY) Z += (double)__ldcg(&pb[cta * 4 + 1]) * (double)exp2f((mc - M) * cT);
-        }
-      Z = __shfl_sync(0xffffffffu, Z, 0);
-      const double target = u * Z;
-      int cstar = -1, clast = -1;
-      double before = 0.0;
-      if (lane == 0) {
-        double cum = 0.0;
-        for (int cta = 0; cta < G; ++cta) {
-          const float mc = __ldcg(&pb[cta * 4]);
-          if (mc == -INFINITY) continue;
-          const double mass = (double)__ldcg(&pb[cta * 4 + 1]) * (double)exp2f((mc - M) * cT);
-          if (mass > 0.0) clast = cta;
-          if (cstar < 0 && cum + mass > target) {
-            cstar = cta;
-            before = cum;
-          }
-          cum += mass;
-        }
-        if (cstar < 0) {
-          cstar = clast;
-          before = -1.0;  // no crossing: take the last positive index
-        }
-      }
-      cstar = __shfl_sync(0xffffffffu, cstar, 0);
-      before = __shfl_sync(0xffffffffu, before, 0);
-      // rows of CTA cstar (same split as the launch)
-      const int lo = cstar * c.lm_rpc, hi = min(c.V, lo + c.lm_rpc);
-      const float *lg = c.logits + ((size_t)b * c.k + c.j) * c.V;
-      const int per = (hi - lo + 31) / 32;
-      const int a0 = lo + lane * per, a1 = min(hi, a0 + per);
-      double ls = 0.0;
-      int lastpos = -1;
-      for (int i = a0; i < a1; ++i) {
-        const float w = exp2f((__ldcg(&lg[i]) - M) * cT);
-        ls += (double)w;
-        if (w > 0.f) lastpos = i;
-      }
-      // exclusive prefix of lane sums
-      double incl = ls;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const double t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      const double excl = incl - ls;
-      int found = 0x7fffffff;
-      if (before >= 0.0 && before + incl > target) {
-        double cum = before + excl;
-        for (int i = a0; i < a1; ++i) {
-          cum += (double)exp2f((__ldcg(&lg[i]) - M) * cT);
-          if (cum > target) {
-            found = i;
-            break;
-          }
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) found = min(found, __shfl_xor_sync(0xffffffffu, found, o));
-      int lp = lastpos;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
-      tok = found != 0x7fffffff ? found : (lp >= 0 ? lp : Mi);
-    }
-    if (lane == 0) c.draft_tok[b * c.k + c.j] = tok;
+  if (warp == 0) {
+    lm_select_warp(c, c.lm_grid, c.lm_rpc);
+    if (lane == 0) *c.lm_cnt = 0u;
   }
-  if (lane == 0) *c.lm_cnt = 0u;
 }
 
 // ---------------------------------------------------------------- planning / launch
+
+// Tuning knobs (environment, read per call): MTP_GEMV_CTAS_PER_SM (default 2),
+// MTP_GEMV_STAGES (ring depth per warp, default 6), MTP_GEMV_PIECE (maximum
+// columns per TMA piece, default 1024), MTP_GEMV_SMEM_KB (shared-memory cap per
+// CTA, default 110).  Two CTAs of 8 warps per SM with 6 stages of 2 KB each keep
+// about 190 KB of weight copies in flight per SM.
+static int env_int(const char *name, int dflt) {
+  const char *v = getenv(name);
+  return v && *v ? atoi(v) : dflt;
+}
 
 GemvPlan plan_gemv(int op, int N, int K, int B, int num_sms) {
   GemvPlan g{};
   g.op = op;
   g.N = N;
   g.K = K;
+  const int piece_max = env_int("MTP_GEMV_PIECE", 1024);
   int P = 1;
-  while (P < kGemvWarps && (K + P - 1) / P > 1024) P *= 2;
+  while (P < kGemvWarps && (K + P - 1) / P > piece_max) P *= 2;
   g.P = P;
   g.PC = (((K + P - 1) / P) + 7) / 8 * 8;
   int nv = (g.PC + 255) / 256;
@@ -470,12 +253,12 @@ GemvPlan plan_gemv(int op, int N, int K, int B, int num_sms) {
   g.nv = nv;
   g.bg = (B > 1 && nv <= 4) ? 2 : 1;
   g.ngroups = (B + g.bg - 1) / g.bg;
-  int grid = num_sms;
+  int grid = num_sms * env_int("MTP_GEMV_CTAS_PER_SM", 2);
   int rpc = (N + grid - 1) / grid;
   if (op == OP_GATEUP && (rpc & 1)) ++rpc;
   g.rows_per_cta = rpc;
   g.grid = (N + rpc - 1) / rpc;
-  g.stages = 4;
+  g.stages = env_int("MTP_GEMV_STAGES", 6);
   auto smem_for = [&](int stages) {
     size_t s = (size_t)kGemvWarps * stages * (g.PC * 2 + 8);
     s += (size_t)g.rows_per_cta * g.P * g.bg * 4;
@@ -483,7 +266,8 @@ GemvPlan plan_gemv(int op, int N, int K, int B, int num_sms) {
     s += (size_t)2 * B * 4 + 64 * 4;
     return s;
   };
-  while (g.stages > 2 && smem_for(g.stages) > 110 * 1024) --g.stages;
+  const int smem_cap = env_int("MTP_GEMV_SMEM_KB", 110) * 1024;
+  while (g.stages > 2 && smem_for(g.stages) > (size_t)smem_cap) --g.stages;
   g.smem = smem_for(g.stages);
   return g;
 }
@@ -541,202 +325,305 @@ cudaError_t launch_gemv(const DraftCtx &c, const GemvPlan &g, cudaStream_t s, bo
 }
 
 // ---------------------------------------------------------------- decode attention
+//
+// One thread-block cluster per (sequence b, kv head g); CTA r of the cluster
+// owns the contiguous cache positions [r*T, (r+1)*T) of the ntok = L_b + j + 1
+// visible ones, and each of its 8 warps a contiguous eighth of those.  A warp
+// works on two cache rows at a time, one per half-warp (DH/16 dims per lane),
+// and keeps a private online softmax (running max, sum, rescaled output) for
+// every query head of the GQA group, with the K/V rows of the next batch loaded
+// into registers while the current batch is computed -- no barriers inside the
+// loop.  Warps are merged through shared memory, CTAs through distributed
+// shared memory (each CTA finalises a slice of the output).
+
+constexpr int kAttnUnroll = 4;   // row pairs per batch and warp
 
 size_t attention_smem_bytes(int Dh) {
-  return (size_t)2 * kAttnChunk * Dh * 2        // K, V chunk (bf16)
-         + (size_t)kMaxGroup * Dh * 4           // q
-         + (size_t)kMaxGroup * kAttnChunk * 4   // scores / probabilities
-         + (size_t)4 * kMaxGroup * Dh * 4       // per-warp partial outputs
-         + (size_t)kMaxGroup * 2 * 4 + 16;      // (max, sum) per head + mbarrier
+  return (size_t)kAttnThreads / 32 * kMaxGroup * (Dh + 2) * 4   // per-warp (max, sum, output)
+         + (size_t)kMaxGroup * Dh * 4                           // q, then the CTA's output
+         + (size_t)kMaxGroup * 2 * 4 + 16;                      // CTA (max, sum)
 }
 
-template <int DH>
-__global__ void __launch_bounds__(kAttnThreads) attn_kernel(DraftCtx c) {
-  constexpr int CH = kAttnChunk, G8 = kMaxGroup, VPL = DH / 32, NW = kAttnThreads / 32;
-  extern __shared__ __align__(128) unsigned char smem[];
-  uint16_t *Ks = reinterpret_cast<uint16_t *>(smem);
-  uint16_t *Vs = Ks + CH * DH;
-  float *qs = reinterpret_cast<float *>(Vs + CH * DH);
-  float *sc = qs + G8 * DH;
-  float *red = sc + G8 * CH;
-  float *ml = red + NW * G8 * DH;
-  uint64_t *bar = reinterpret_cast<uint64_t *>(ml + G8 * 2);
+template <int DPL>
+struct RowVec;
+template <>
+struct RowVec<2> { uint32_t x; };
+template <>
+struct RowVec<4> { uint2 x; };
+template <>
+struct RowVec<8> { uint4 x; };
 
-  const int ch = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+template <int DPL>
+__device__ __forceinline__ RowVec<DPL> load_row(const uint16_t *p) {
+  RowVec<DPL> r;
+  if constexpr (DPL == 2) r.x = __ldcg(reinterpret_cast<const unsigned int *>(p));
+  else if constexpr (DPL == 4) r.x = __ldcg(reinterpret_cast<const uint2 *>(p));
+  else r.x = __ldcg(reinterpret_cast<const uint4 *>(p));
+  return r;
+}
+
+template <int DPL>
+__device__ __forceinline__ void unpack_row(const RowVec<DPL> &r, float *out) {
+  const uint32_t *w = reinterpret_cast<const uint32_t *>(&r.x);
+#pragma unroll
+  for (int i = 0; i < DPL / 2; ++i) {
+    out[2 * i] = bf16_lo(w[i]);
+    out[2 * i + 1] = bf16_hi(w[i]);
+  }
+}
+
+template <int DH, int GM>
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(DraftCtx c) {
+  constexpr int DPL = DH / 16, NW = kAttnThreads / 32, U = kAttnUnroll;
+  extern __shared__ __align__(128) unsigned char smem[];
+  float *wst = reinterpret_cast<float *>(smem);           // [NW][GM][DH+2]: max, sum, output
+  float *qo = wst + NW * kMaxGroup * (DH + 2);            // [GM][DH]
+  float *mrun = qo + kMaxGroup * DH;                      // [GM]
+  float *lrun = mrun + kMaxGroup;                         // [GM]
+
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int C = (int)cluster_size(), rank = (int)cluster_rank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const int half = lane >> 4, hl = lane & 15;
   const int group = c.Hq / c.Hkv;
   int L = __ldg(&c.ctx_len[b]);
   L = min(max(L, 0), c.Lmax - c.k);
   const int ntok = L + c.j + 1;
-  const int t0 = ch * CH;
-  if (t0 >= ntok) return;
-  const int t1 = min(t0 + CH, ntok);
-  const int n = t1 - t0;
-  const int nctx = max(0, min(t1, L) - t0);
-  const size_t base = (((size_t)b * c.Hkv + g) * c.Lmax + t0) * DH;
+  const int T = (ntok + C - 1) / C;
+  const int r0 = min(ntok, rank * T), r1 = min(ntok, r0 + T);
+  const int Tw = (r1 - r0 + NW - 1) / NW;
+  const int w0 = min(r1, r0 + warp * Tw), w1 = min(r1, w0 + Tw);
+  const int npairs = (w1 - w0 + 1) / 2;
+  const int nbatch = (npairs + U - 1) / U;
+  const size_t base = ((size_t)b * c.Hkv + g) * c.Lmax * DH + hl * DPL;
+  const uint16_t *kb = c.kc + base;
+  const uint16_t *vb = c.vc + base;
 
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    fence_barrier_init();
-  }
-  __syncthreads();
-  // context rows were written by the caller: stage them before waiting
-  if (tid == 0 && nctx > 0) {
-    const uint32_t bytes = (uint32_t)nctx * DH * 2;
-    mbar_arrive_expect_tx(bar, 2 * bytes);
-    bulk_g2s(Ks, c.kc + base, bytes, bar);
-    bulk_g2s(Vs, c.vc + base, bytes, bar);
-  }
+  RowVec<DPL> kbuf[U], vbuf[U];
+  auto load_batch = [&](int bi) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int t = min(w0 + 2 * (bi * U + u) + half, max(w1 - 1, 0));
+      kbuf[u] = load_row<DPL>(kb + (size_t)t * DH);
+      vbuf[u] = load_row<DPL>(vb + (size_t)t * DH);
+    }
+  };
+  // the first batch can be fetched before the previous kernel finishes when it
+  // holds only context rows, which the caller wrote
+  const bool early = nbatch > 0 && w0 + 2 * U <= L;
+  if (early) load_batch(0);
   grid_dep_wait();
   grid_dep_launch();
+  if (nbatch > 0 && !early) load_batch(0);
 
-  // rows appended by this call's draft depths, and the queries
-  const int napp = n - nctx;
-  for (int idx = tid; idx < napp * (DH / 8); idx += kAttnThreads) {
-    const int r = nctx + idx / (DH / 8), e = (idx % (DH / 8)) * 8;
-    *reinterpret_cast<uint4 *>(Ks + r * DH + e) = __ldcg(reinterpret_cast<const uint4 *>(c.kc + base + (size_t)r * DH + e));
-    *reinterpret_cast<uint4 *>(Vs + r * DH + e) = __ldcg(reinterpret_cast<const uint4 *>(c.vc + base + (size_t)r * DH + e));
-  }
   const int nq = c.Hq * DH;
-  for (int idx = tid; idx < group * DH; idx += kAttnThreads) qs[idx] = __ldcg(&c.q[(size_t)b * nq + (size_t)g * group * DH + idx]);
-  bool ok = true;
-  if (nctx > 0) ok = mbar_wait(bar, 0, c.status);
-  __syncthreads();
-
-  float qr[G8][VPL];
+  float q[GM][DPL];
 #pragma unroll
-  for (int h = 0; h < G8; ++h)
+  for (int h = 0; h < GM; ++h)
 #pragma unroll
-    for (int e = 0; e < VPL; ++e) qr[h][e] = h < group ? qs[h * DH + lane * VPL + e] : 0.f;
-
+    for (int e = 0; e < DPL; ++e)
+      q[h][e] = h < group ? __ldcg(&c.q[(size_t)b * nq + ((size_t)g * group + h) * DH + hl * DPL + e]) : 0.f;
+  float m[GM], l[GM], acc[GM][DPL];
+#pragma unroll
+  for (int h = 0; h < GM; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) acc[h][e] = 0.f;
+  }
   const float scale = rsqrtf((float)DH) * kLog2e;
-  for (int t = warp; t < n; t += NW) {
-    float kv[VPL];
+
+  for (int bi = 0; bi < nbatch; ++bi) {
+    RowVec<DPL> kc_[U], vc_[U];
 #pragma unroll
-    for (int e = 0; e < VPL; ++e) kv[e] = __uint_as_float((uint32_t)Ks[t * DH + lane * VPL + e] << 16);
+    for (int u = 0; u < U; ++u) {
+      kc_[u] = kbuf[u];
+      vc_[u] = vbuf[u];
+    }
+    if (bi + 1 < nbatch) load_batch(bi + 1);
+    // scores of the batch's U rows (one per pair and half-warp), all heads
+    float sc[U][GM];
 #pragma unroll
-    for (int h = 0; h < G8; ++h) {
+    for (int u = 0; u < U; ++u) {
+      const bool live = w0 + 2 * (bi * U + u) + half < w1;
+      float kv[DPL];
+      unpack_row<DPL>(kc_[u], kv);
+#pragma unroll
+      for (int h = 0; h < GM; ++h) {
+        float sdot = 0.f;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) sdot = fmaf(q[h][e], kv[e], sdot);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) sdot += __shfl_xor_sync(0xffffffffu, sdot, o);
+        sc[u][h] = live ? sdot * scale : -INFINITY;
+      }
+    }
+    // one online-softmax update per head for the whole batch
+    float vv[U][DPL];
+#pragma unroll
+    for (int u = 0; u < U; ++u) unpack_row<DPL>(vc_[u], vv[u]);
+#pragma unroll
+    for (int h = 0; h < GM; ++h) {
       if (h < group) {
-        float s = 0.f;
+        float bm = sc[0][h];
 #pragma unroll
-        for (int e = 0; e < VPL; ++e) s = fmaf(qr[h][e], kv[e], s);
-        s = warp_sum(s);
-        if (lane == 0) sc[h * CH + t] = s * scale;
+        for (int u = 1; u < U; ++u) bm = fmaxf(bm, sc[u][h]);
+        const float mn = fmaxf(m[h], bm);
+        if (mn != -INFINITY) {
+          const float f = exp2f(m[h] - mn);   // 0 while m is -inf
+          float pw[U], ps = 0.f;
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            pw[u] = exp2f(sc[u][h] - mn);
+            ps += pw[u];
+          }
+          l[h] = l[h] * f + ps;
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) {
+            float a = acc[h][e] * f;
+#pragma unroll
+            for (int u = 0; u < U; ++u) a = fmaf(pw[u], vv[u][e], a);
+            acc[h][e] = a;
+          }
+          m[h] = mn;
+        }
+      }
+    }
+  }
+
+  // merge the two half-warps, then the warps of the CTA
+#pragma unroll
+  for (int h = 0; h < GM; ++h) {
+    if (h < group) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m[h], 16);
+      const float l2 = __shfl_xor_sync(0xffffffffu, l[h], 16);
+      const float M = fmaxf(m[h], m2);
+      const float f1 = m[h] == -INFINITY ? 0.f : exp2f(m[h] - M);
+      const float f2 = m2 == -INFINITY ? 0.f : exp2f(m2 - M);
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) {
+        const float a2 = __shfl_xor_sync(0xffffffffu, acc[h][e], 16);
+        acc[h][e] = acc[h][e] * f1 + a2 * f2;
+      }
+      l[h] = l[h] * f1 + l2 * f2;
+      m[h] = M;
+      if (half == 0) {
+        float *ws = wst + ((size_t)warp * kMaxGroup + h) * (DH + 2);
+        if (hl == 0) {
+          ws[0] = m[h];
+          ws[1] = l[h];
+        }
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) ws[2 + hl * DPL + e] = acc[h][e];
       }
     }
   }
   __syncthreads();
-  for (int h = warp; h < group; h += NW) {
-    float m = -INFINITY;
-    for (int t = lane; t < n; t += 32) m = fmaxf(m, sc[h * CH + t]);
-    m = warp_max(m);
-    float s = 0.f;
-    for (int t = lane; t < n; t += 32) {
-      const float pexp = exp2f(sc[h * CH + t] - m);
-      sc[h * CH + t] = pexp;
-      s += pexp;
-    }
-    s = warp_sum(s);
-    if (lane == 0) {
-      ml[2 * h] = m;
-      ml[2 * h + 1] = s;
-    }
-  }
-  __syncthreads();
-  float acc[G8][VPL];
-#pragma unroll
-  for (int h = 0; h < G8; ++h)
-#pragma unroll
-    for (int e = 0; e < VPL; ++e) acc[h][e] = 0.f;
-  for (int t = warp; t < n; t += NW) {
-    float vv[VPL];
-#pragma unroll
-    for (int e = 0; e < VPL; ++e) vv[e] = __uint_as_float((uint32_t)Vs[t * DH + lane * VPL + e] << 16);
-#pragma unroll
-    for (int h = 0; h < G8; ++h) {
-      if (h < group) {
-        const float pw = sc[h * CH + t];
-#pragma unroll
-        for (int e = 0; e < VPL; ++e) acc[h][e] = fmaf(pw, vv[e], acc[h][e]);
-      }
-    }
-  }
-#pragma unroll
-  for (int h = 0; h < G8; ++h)
-    if (h < group)
-#pragma unroll
-      for (int e = 0; e < VPL; ++e) red[(warp * G8 + h) * DH + lane * VPL + e] = acc[h][e];
-  __syncthreads();
-
-  float *part = c.attn_part + (((size_t)b * c.Hkv + g) * c.attn_chunks + ch) * group * (DH + 2);
-  for (int idx = tid; idx < group * DH; idx += kAttnThreads) {
-    const int h = idx / DH, e = idx % DH;
-    float o = 0.f;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) o += red[(w * G8 + h) * DH + e];
-    part[h * (DH + 2) + 2 + e] = o;
-  }
-  if (tid < group) {
-    part[tid * (DH + 2)] = ml[2 * tid];
-    part[tid * (DH + 2) + 1] = ml[2 * tid + 1];
-  }
-  (void)ok;
-
-  // the last chunk of this (sequence, kv head) to finish combines the partials
-  __shared__ int s_last;
-  __threadfence();
-  __syncthreads();
-  const int nchunks = (ntok + CH - 1) / CH;
-  if (tid == 0) s_last = atomicAdd(&c.attn_cnt[b * c.Hkv + g], 1u) == (unsigned)(nchunks - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  const float *p0 = c.attn_part + ((size_t)b * c.Hkv + g) * c.attn_chunks * group * (DH + 2);
   for (int idx = tid; idx < group * DH; idx += kAttnThreads) {
     const int h = idx / DH, e = idx % DH;
     float M = -INFINITY;
-    for (int cc = 0; cc < nchunks; ++cc) M = fmaxf(M, __ldcg(&p0[((size_t)cc * group + h) * (DH + 2)]));
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, wst[((size_t)w * kMaxGroup + h) * (DH + 2)]);
     float Ls = 0.f, O = 0.f;
-    for (int cc = 0; cc < nchunks; ++cc) {
-      const float *pc = p0 + ((size_t)cc * group + h) * (DH + 2);
-      const float wgt = exp2f(__ldcg(&pc[0]) - M);
-      Ls = fmaf(__ldcg(&pc[1]), wgt, Ls);
-      O = fmaf(__ldcg(&pc[2 + e]), wgt, O);
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float *ws = wst + ((size_t)w * kMaxGroup + h) * (DH + 2);
+      if (ws[0] == -INFINITY) continue;
+      const float f = exp2f(ws[0] - M);
+      Ls = fmaf(ws[1], f, Ls);
+      O = fmaf(ws[2 + e], f, O);
+    }
+    qo[h * DH + e] = O;
+    if (e == 0) {
+      mrun[h] = M;
+      lrun[h] = Ls;
+    }
+  }
+
+  // combine across the cluster: CTA r finalises pairs (h, e) r, r + C, ...
+  cluster_sync();
+  for (int idx = rank + C * tid; idx < group * DH; idx += C * kAttnThreads) {
+    const int h = idx / DH, e = idx % DH;
+    float mr[16], lr[16], orr[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      if (r < C) {
+        mr[r] = *dsmem_ptr(&mrun[h], r);
+        lr[r] = *dsmem_ptr(&lrun[h], r);
+        orr[r] = *dsmem_ptr(&qo[h * DH + e], r);
+      }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < 16; ++r)
+      if (r < C) M = fmaxf(M, mr[r]);
+    float Ls = 0.f, O = 0.f;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      if (r < C && mr[r] != -INFINITY) {
+        const float wgt = exp2f(mr[r] - M);
+        Ls = fmaf(lr[r], wgt, Ls);
+        O = fmaf(orr[r], wgt, O);
+      }
     }
     c.o[(size_t)b * nq + ((size_t)g * group + h) * DH + e] = O / Ls;
   }
-  if (tid == 0) c.attn_cnt[b * c.Hkv + g] = 0u;
+  cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
 }
 
-template <int DH>
-static cudaError_t launch_attn_dh(const DraftCtx &c, cudaStream_t s, bool pdl) {
-  auto kern = attn_kernel<DH>;
+int attention_cluster_size(int ctx_max, int max_cluster) {
+  const int forced = env_int("MTP_ATTN_CLUSTER", 0);
+  if (forced > 0) return forced < max_cluster ? forced : max_cluster;
+  // up to 8 CTAs per (sequence, kv head): a 16-CTA cluster of one-CTA-per-SM
+  // kernels does not fit every GPC at once
+  int C = (ctx_max + 255) / 256;
+  const int cap = max_cluster < 8 ? max_cluster : 8;
+  return C < 1 ? 1 : (C > cap ? cap : C);
+}
+
+template <int DH, int GM>
+static cudaError_t launch_attn(const DraftCtx &c, int cluster, cudaStream_t s, bool pdl) {
+  auto kern = attn_kernel<DH, GM>;
   static bool attr_done = false;
   const size_t smem = attention_smem_bytes(DH);
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(c.attn_chunks, c.Hkv, c.B);
+  cfg.gridDim = dim3(cluster, c.Hkv, c.B);
   cfg.blockDim = dim3(kAttnThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = pdl ? 2 : 1;
   note_launch();
   return cudaLaunchKernelEx(&cfg, kern, c);
 }
 
-cudaError_t launch_attention(const DraftCtx &c, cudaStream_t s, bool pdl) {
+template <int DH>
+static cudaError_t launch_attn_g(const DraftCtx &c, int cluster, cudaStream_t s, bool pdl) {
+  const int group = c.Hq / c.Hkv;
+  if (group <= 1) return launch_attn<DH, 1>(c, cluster, s, pdl);
+  if (group <= 2) return launch_attn<DH, 2>(c, cluster, s, pdl);
+  if (group <= 4) return launch_attn<DH, 4>(c, cluster, s, pdl);
+  return launch_attn<DH, 8>(c, cluster, s, pdl);
+}
+
+cudaError_t launch_attention(const DraftCtx &c, int cluster, cudaStream_t s, bool pdl) {
   switch (c.Dh) {
-    case 32: return launch_attn_dh<32>(c, s, pdl);
-    case 64: return launch_attn_dh<64>(c, s, pdl);
-    default: return launch_attn_dh<128>(c, s, pdl);
+    case 32: return launch_attn_g<32>(c, cluster, s, pdl);
+    case 64: return launch_attn_g<64>(c, cluster, s, pdl);
+    default: return launch_attn_g<128>(c, cluster, s, pdl);
   }
 }
 

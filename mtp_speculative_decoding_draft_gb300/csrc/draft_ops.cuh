@@ -1,0 +1,253 @@
+// Device helpers shared by the draft-chain kernels (the weight-streaming GEMV
+// path and the tensor-core path): RMSNorm scale factors, activation loads, the
+// weight-row map of each operation and the draft-token selection over the
+// vocabulary.
+#pragma once
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mtp {
+
+
+__device__ __forceinline__ void load8_bf16(const uint16_t *p, float *out) {
+  uint4 w = __ldg(reinterpret_cast<const uint4 *>(p));
+  out[0] = bf16_lo(w.x); out[1] = bf16_hi(w.x);
+  out[2] = bf16_lo(w.y); out[3] = bf16_hi(w.y);
+  out[4] = bf16_lo(w.z); out[5] = bf16_hi(w.z);
+  out[6] = bf16_lo(w.w); out[7] = bf16_hi(w.w);
+}
+
+// fp32 data produced by an earlier kernel of the chain: read through L2.
+__device__ __forceinline__ void load8_f32(const float *p, float *out) {
+  float4 a = __ldcg(reinterpret_cast<const float4 *>(p));
+  float4 b = __ldcg(reinterpret_cast<const float4 *>(p) + 1);
+  out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+  out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+}
+
+__device__ __forceinline__ float block_sum_256(float v, float *red) {
+  v = warp_sum(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int i = 0; i < kGemvWarps; ++i) t += red[i];
+  return t;
+}
+
+// Token feeding depth j of sequence b (validated).
+__device__ __forceinline__ int depth_token(const DraftCtx &c, int b) {
+  int t = c.j == 0 ? __ldg(&c.last_tok[b]) : __ldcg(&c.draft_tok[b * c.k + c.j - 1]);
+  if (t < 0 || t >= c.V) {
+    set_status(c.status, kStatusBadToken);
+    t = 0;
+  }
+  return t;
+}
+
+__device__ __forceinline__ int clamped_ctx(const DraftCtx &c, int b) {
+  int L = __ldg(&c.ctx_len[b]);
+  return min(max(L, 0), c.Lmax - c.k);
+}
+
+// RMSNorm scale factors 1/sqrt(mean(v^2)+eps) of the vectors this op
+// normalises, for every batch row.  scales[2*b] is the first vector's (for the
+// input projection: the token embedding), scales[2*b+1] the second's (the
+// hidden state).
+template <int OP>
+__device__ void compute_scales(const DraftCtx &c, float *scales, float *red) {
+  if (OP == OP_WO || OP == OP_DOWN) return;
+  const int d = c.d;
+  for (int b = 0; b < c.B; ++b) {
+    float s0 = 0.f, s1 = 0.f;
+    if (OP == OP_FC) {
+      const uint16_t *e = c.E + (size_t)depth_token(c, b) * d;
+      for (int i = threadIdx.x * 8; i < d; i += kGemvThreads * 8) {
+        float v[8];
+        load8_bf16(e + i, v);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) s0 = fmaf(v[t], v[t], s0);
+      }
+      for (int i = threadIdx.x * 8; i < d; i += kGemvThreads * 8) {
+        float v[8];
+        if (c.j == 0) load8_bf16(c.h + (size_t)b * d + i, v);
+        else load8_f32(c.x2 + (size_t)b * d + i, v);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) s1 = fmaf(v[t], v[t], s1);
+      }
+    } else {
+      const float *x = OP == OP_QKV ? c.x0 : (OP == OP_GATEUP ? c.x1 : c.x2);
+      for (int i = threadIdx.x * 8; i < d; i += kGemvThreads * 8) {
+        float v[8];
+        load8_f32(x + (size_t)b * d + i, v);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) s0 = fmaf(v[t], v[t], s0);
+      }
+    }
+    s0 = block_sum_256(s0, red);
+    if (OP == OP_FC) s1 = block_sum_256(s1, red);
+    if (threadIdx.x == 0) {
+      scales[2 * b] = rsqrtf(s0 / (float)d + c.eps);
+      scales[2 * b + 1] = rsqrtf(s1 / (float)d + c.eps);
+    }
+  }
+  __syncthreads();
+}
+
+// Eight consecutive activation values (columns col .. col+7) of batch row b.
+template <int OP>
+__device__ __forceinline__ void act8(const DraftCtx &c, int b, int col, const float *scales, float *out) {
+  const int d = c.d;
+  if (OP == OP_FC) {
+    float g[8];
+    if (col < d) {
+      load8_bf16(c.E + (size_t)depth_token(c, b) * d + col, out);
+      load8_bf16(c.g_emb + col, g);
+      const float s = scales[2 * b];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) out[t] = out[t] * s * g[t];
+    } else {
+      const int cc = col - d;
+      if (c.j == 0) load8_bf16(c.h + (size_t)b * d + cc, out);
+      else load8_f32(c.x2 + (size_t)b * d + cc, out);
+      load8_bf16(c.g_hid + cc, g);
+      const float s = scales[2 * b + 1];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) out[t] = out[t] * s * g[t];
+    }
+  } else if (OP == OP_WO) {
+    load8_f32(c.o + (size_t)b * c.Hq * c.Dh + col, out);
+  } else if (OP == OP_DOWN) {
+    load8_f32(c.act + (size_t)b * c.F + col, out);
+  } else {
+    const float *x = OP == OP_QKV ? c.x0 : (OP == OP_GATEUP ? c.x1 : c.x2);
+    const uint16_t *gp = OP == OP_QKV ? c.g_attn : (OP == OP_GATEUP ? c.g_mlp : c.g_final);
+    float g[8];
+    load8_f32(x + (size_t)b * d + col, out);
+    load8_bf16(gp + col, g);
+    const float s = scales[2 * b];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) out[t] = out[t] * s * g[t];
+  }
+}
+
+template <int OP>
+__device__ __forceinline__ const uint16_t *weight_row(const DraftCtx &c, int row, int K) {
+  if (OP == OP_FC) return c.fc + (size_t)row * K;
+  if (OP == OP_QKV) {
+    const int nq = c.Hq * c.Dh, nkv = c.Hkv * c.Dh;
+    if (row < nq) return c.wq + (size_t)row * K;
+    row -= nq;
+    if (row < nkv) return c.wk + (size_t)row * K;
+    return c.wv + (size_t)(row - nkv) * K;
+  }
+  if (OP == OP_WO) return c.wo + (size_t)row * K;
+  if (OP == OP_GATEUP) return ((row & 1) ? c.wup : c.wgate) + (size_t)(row >> 1) * K;
+  if (OP == OP_DOWN) return c.wdown + (size_t)row * K;
+  return c.E + (size_t)row * K;
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.f + __expf(-z)); }
+
+
+// Draft-token selection over the vocabulary, run by one warp after every
+// LM-head CTA has written its per-sequence partials lm_part[b][cta] =
+// (max, sum of exp2((logit - max) * log2e / T), argmax).  CTA cta owns the
+// vocabulary rows [cta * rpc, (cta + 1) * rpc).
+// Greedy: the argmax, lowest index on ties.  Stochastic: the inverse CDF of
+// softmax(logits / T) at u_draft[b, j] -- walk the per-CTA masses in vocabulary
+// order, then rescan the CTA that holds the crossing in float64.
+__device__ void lm_select_warp(const DraftCtx &c, int G, int rpc) {
+  const int lane = threadIdx.x & 31;
+  const float cT = kLog2e / c.T;
+  for (int b = 0; b < c.B; ++b) {
+    const float *pb = c.lm_part + (size_t)b * G * 4;
+    float M = -INFINITY;
+    int Mi = 0x7fffffff;
+    for (int cta = lane; cta < G; cta += 32) argmax_merge(M, Mi, __ldcg(&pb[cta * 4]), __float_as_int(__ldcg(&pb[cta * 4 + 2])));
+    warp_argmax(M, Mi);
+    int tok = Mi;
+    if (M == -INFINITY || !(M == M)) {
+      if (lane == 0) set_status(c.status, kStatusNonFinite);
+      tok = 0;
+    } else if (c.mode == 1) {
+      // Inverse CDF of softmax(logits / T) at u: walk the per-CTA masses in
+      // vocabulary order, then rescan the CTA that holds the crossing.
+      const double u = (double)__ldg(&c.u_draft[b * c.k + c.j]);
+      double Z = 0.0;
+      if (lane == 0)
+        for (int cta = 0; cta < G; ++cta) {
+          const float mc = __ldcg(&pb[cta * 4]);
+          if (mc != -INFINITY) Z += (double)__ldcg(&pb[cta * 4 + 1]) * (double)exp2f((mc - M) * cT);
+        }
+      Z = __shfl_sync(0xffffffffu, Z, 0);
+      const double target = u * Z;
+      int cstar = -1, clast = -1;
+      double before = 0.0;
+      if (lane == 0) {
+        double cum = 0.0;
+        for (int cta = 0; cta < G; ++cta) {
+          const float mc = __ldcg(&pb[cta * 4]);
+          if (mc == -INFINITY) continue;
+          const double mass = (double)__ldcg(&pb[cta * 4 + 1]) * (double)exp2f((mc - M) * cT);
+          if (mass > 0.0) clast = cta;
+          if (cstar < 0 && cum + mass > target) {
+            cstar = cta;
+            before = cum;
+          }
+          cum += mass;
+        }
+        if (cstar < 0) {
+          cstar = clast;
+          before = -1.0;  // no crossing: take the last positive index
+        }
+      }
+      cstar = __shfl_sync(0xffffffffu, cstar, 0);
+      before = __shfl_sync(0xffffffffu, before, 0);
+      // rows of CTA cstar (same split as the launch)
+      const int lo = cstar * rpc, hi = min(c.V, lo + rpc);
+      const float *lg = c.logits + ((size_t)b * c.k + c.j) * c.V;
+      const int per = (hi - lo + 31) / 32;
+      const int a0 = lo + lane * per, a1 = min(hi, a0 + per);
+      double ls = 0.0;
+      int lastpos = -1;
+      for (int i = a0; i < a1; ++i) {
+        const float w = exp2f((__ldcg(&lg[i]) - M) * cT);
+        ls += (double)w;
+        if (w > 0.f) lastpos = i;
+      }
+      // exclusive prefix of lane sums
+      double incl = ls;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const double excl = incl - ls;
+      int found = 0x7fffffff;
+      if (before >= 0.0 && before + incl > target) {
+        double cum = before + excl;
+        for (int i = a0; i < a1; ++i) {
+          cum += (double)exp2f((__ldcg(&lg[i]) - M) * cT);
+          if (cum > target) {
+            found = i;
+            break;
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) found = min(found, __shfl_xor_sync(0xffffffffu, found, o));
+      int lp = lastpos;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
+      tok = found != 0x7fffffff ? found : (lp >= 0 ? lp : Mi);
+    }
+    if (lane == 0) c.draft_tok[b * c.k + c.j] = tok;
+  }
+  if (lane == 0) *c.lm_cnt = 0u;
+}
+
+}  // namespace mtp

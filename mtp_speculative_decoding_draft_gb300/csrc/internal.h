@@ -29,15 +29,12 @@ struct DraftCtx {
   // workspace
   int *status;
   unsigned *lm_cnt;       // 1 ticket counter
-  unsigned *attn_cnt;     // [B * Hkv] ticket counters
   float *x0, *x1, *x2;    // [B, d]
   float *q, *o;           // [B, Hq*Dh]
   float *act;             // [B, F]
   float *lm_part;         // [B, lm_grid, 4]
-  float *attn_part;       // [B, Hkv, attn_chunks, group*(Dh+2)]
   int lm_grid;            // CTAs of the LM-head launch
   int lm_rpc;             // vocabulary rows per LM-head CTA
-  int attn_chunks;        // chunk slots per (b, kv head)
   int zero_counters;      // this launch clears the ticket counters first
 };
 
@@ -61,14 +58,14 @@ struct GemvPlan {
 
 constexpr int kGemvWarps = 8;
 constexpr int kGemvThreads = kGemvWarps * 32;
-constexpr int kAttnChunk = 64;      // tokens per attention CTA
-constexpr int kAttnThreads = 128;
+constexpr int kAttnThreads = 256;
 constexpr int kMaxGroup = 8;        // Hq / Hkv
 
 GemvPlan plan_gemv(int op, int N, int K, int B, int num_sms);
 cudaError_t launch_gemv(const DraftCtx &c, const GemvPlan &g, cudaStream_t s, bool pdl);
-cudaError_t launch_attention(const DraftCtx &c, cudaStream_t s, bool pdl);
+cudaError_t launch_attention(const DraftCtx &c, int cluster, cudaStream_t s, bool pdl);
 size_t attention_smem_bytes(int Dh);
+int attention_cluster_size(int ctx_max, int max_cluster);
 
 // Verification launch.
 struct VerifyArgs {
@@ -87,7 +84,7 @@ struct VerifyArgs {
 
 constexpr int kVerifyThreads = 256;
 constexpr int kVerifyPiece = 4096;  // floats per TMA piece (16 KB)
-constexpr int kVerifyStages = 4;
+constexpr int kVerifyStages = 6;
 
 int verify_cluster_size(int B, int num_sms, int max_cluster);
 size_t verify_smem_bytes(int B, int k, int V, int cluster);

@@ -269,26 +269,32 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_kernel(VerifyArgs a) {
     // ---------------- combine across the cluster (rank order)
     cluster_sync();
     if (tid < nrows) {
-      float M = -INFINITY, Sx = 0.f;
+      float pm[16], ps[16];
+      int pi[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        if (r < C) {
+          const float *src = dsmem_ptr(&sm.rowpart[buf][tid][0], r);
+          pm[r] = src[0];
+          ps[r] = src[1];
+          pi[r] = __float_as_int(src[2]);
+        }
+      }
+      float M = -INFINITY;
       int I = 0x7fffffff;
       double Z = 0.0;
-      for (int r = 0; r < C; ++r) {
-        const float pm = dsmem_ld_f32(dsmem_addr(&sm.rowpart[buf][tid][0], r));
-        const float ps = dsmem_ld_f32(dsmem_addr(&sm.rowpart[buf][tid][1], r));
-        const int pi = __float_as_int(dsmem_ld_f32(dsmem_addr(&sm.rowpart[buf][tid][2], r)));
-        if (stoch) {
-          if (pm > M) M = pm;
-        } else {
-          argmax_merge(M, I, pm, pi);
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        if (r < C) {
+          if (stoch) M = fmaxf(M, pm[r]);
+          else argmax_merge(M, I, pm[r], pi[r]);
         }
-        (void)ps;
       }
-      if (stoch && M != -INFINITY)
-        for (int r = 0; r < C; ++r) {
-          const float pm = dsmem_ld_f32(dsmem_addr(&sm.rowpart[buf][tid][0], r));
-          const float ps = dsmem_ld_f32(dsmem_addr(&sm.rowpart[buf][tid][1], r));
-          if (pm != -INFINITY) Z += (double)ps * (double)exp2f((pm - M) * c);
-        }
+      if (stoch && M != -INFINITY) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+          if (r < C && pm[r] != -INFINITY) Z += (double)ps[r] * (double)exp2f((pm[r] - M) * c);
+      }
       sm.rowM[tid] = M;
       sm.rowZ[tid] = Z;
       sm.rowI[tid] = I;
@@ -357,17 +363,45 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_kernel(VerifyArgs a) {
     const float *dr_ptr = bonus ? nullptr : a.draft + ((size_t)b * k + pos) * V;
     float *subR = subs + (size_t)buf * 2 * nsub;
     float *subP = subR + nsub;
+    // rows whose every element is 16-byte aligned in this slice take float4
+    // loads, 4 per lane and row in flight; others take scalar loads
+    const bool vec = ((((size_t)b * (k + 1) + pos) * (size_t)V) & 3) == 0 &&
+                     (bonus || ((((size_t)b * k + pos) * (size_t)V) & 3) == 0);
     for (int sb = warp; sb < nsub; sb += kWarps) {
       const int e0 = v0 + sb * kSub, e1 = min(v1, e0 + kSub);
       float sr = 0.f, sp = 0.f;
-      for (int v = e0 + lane; v < e1; v += 32) {
-        const float t = __ldg(tr_ptr + v);
-        if (bonus) {
-          sp += exp2f((t - Mt) * c);
-        } else {
-          const float l = __ldcg(dr_ptr + v);
-          sr += p2_weight(0, t, l, Mt, Ml, iZt, iZl, c);
-          sp += p2_weight(1, t, l, Mt, Ml, iZt, iZl, c);
+      if (vec && e1 - e0 == kSub) {
+        float4 tv[kSub / 128], lv[kSub / 128];
+#pragma unroll
+        for (int i = 0; i < kSub / 128; ++i) {
+          tv[i] = __ldg(reinterpret_cast<const float4 *>(tr_ptr + e0) + lane + 32 * i);
+          if (!bonus) lv[i] = __ldcg(reinterpret_cast<const float4 *>(dr_ptr + e0) + lane + 32 * i);
+        }
+#pragma unroll
+        for (int i = 0; i < kSub / 128; ++i) {
+          const float t4[4] = {tv[i].x, tv[i].y, tv[i].z, tv[i].w};
+          if (bonus) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) sp += exp2f((t4[q] - Mt) * c);
+          } else {
+            const float l4[4] = {lv[i].x, lv[i].y, lv[i].z, lv[i].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              sr += p2_weight(0, t4[q], l4[q], Mt, Ml, iZt, iZl, c);
+              sp += p2_weight(1, t4[q], l4[q], Mt, Ml, iZt, iZl, c);
+            }
+          }
+        }
+      } else {
+        for (int v = e0 + lane; v < e1; v += 32) {
+          const float t = __ldg(tr_ptr + v);
+          if (bonus) {
+            sp += exp2f((t - Mt) * c);
+          } else {
+            const float l = __ldcg(dr_ptr + v);
+            sr += p2_weight(0, t, l, Mt, Ml, iZt, iZl, c);
+            sp += p2_weight(1, t, l, Mt, Ml, iZt, iZl, c);
+          }
         }
       }
       sr = warp_sum(sr);
@@ -391,9 +425,15 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_kernel(VerifyArgs a) {
     if (tid == 0) {
       double tr[16], tp[16];
       double SR = 0.0, SP = 0.0;
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        if (r < C) {
+          const double *src = dsmem_ptr(&sm.tot[buf][0], r);
+          tr[r] = src[0];
+          tp[r] = src[1];
+        }
+      }
       for (int r = 0; r < C; ++r) {
-        tr[r] = dsmem_ld_f64(dsmem_addr(&sm.tot[buf][0], r));
-        tp[r] = dsmem_ld_f64(dsmem_addr(&sm.tot[buf][1], r));
         SR += tr[r];
         SP += tp[r];
       }

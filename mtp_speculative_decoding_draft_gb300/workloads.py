@@ -19,7 +19,7 @@ bf16 tensors are returned as their raw bit patterns in ``numpy.uint16`` arrays.
 
 import zlib
 from concurrent.futures import ThreadPoolExecutor
-from dataclasses import dataclass, field, replace
+from dataclasses import dataclass, field, replace  # noqa: F401 (replace is re-exported)
 
 import numpy as np
 import torch
