@@ -83,6 +83,40 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *s
   }
 }
 
+// Cross-CTA flavour: acquire at cluster scope, so stores other CTAs of the
+// cluster made before their (release) arrivals are visible afterwards.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, int *status) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 255u) == 255u && global_timer_ns() - t0 > kWaitLimitNs) {
+      set_status(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+// Arrive (release, cluster scope) on the mbarrier at the same shared-memory
+// location in CTA `rank` of this cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint64_t *local_bar, uint32_t rank) {
+  uint32_t raddr;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_u32(local_bar)), "r"(rank));
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(raddr) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA bulk copy
 
 // 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
@@ -99,6 +133,12 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
 
@@ -166,6 +206,18 @@ __device__ __forceinline__ const T *dsmem_ptr(const T *local, uint32_t rank) {
   uint64_t out;
   asm("mapa.u64 %0, %1, %2;" : "=l"(out) : "l"(reinterpret_cast<uint64_t>(local)), "r"(rank));
   return reinterpret_cast<const T *>(out);
+}
+
+template <class T>
+__device__ __forceinline__ T *dsmem_ptr_mut(T *local, uint32_t rank) {
+  uint64_t out;
+  asm("mapa.u64 %0, %1, %2;" : "=l"(out) : "l"(reinterpret_cast<uint64_t>(local)), "r"(rank));
+  return reinterpret_cast<T *>(out);
+}
+
+// Named barrier over the first `nthreads` threads of the CTA (warp-aligned).
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 __device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {

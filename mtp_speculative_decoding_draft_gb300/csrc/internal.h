@@ -82,9 +82,7 @@ struct VerifyArgs {
   int *status;
 };
 
-constexpr int kVerifyThreads = 256;
-constexpr int kVerifyPiece = 4096;  // floats per TMA piece (16 KB)
-constexpr int kVerifyStages = 6;
+constexpr int kVerifyThreads = 320;  // 8 consumer warps, a producer warp, an agent warp
 
 int verify_cluster_size(int B, int num_sms, int max_cluster);
 size_t verify_smem_bytes(int B, int k, int V, int cluster);

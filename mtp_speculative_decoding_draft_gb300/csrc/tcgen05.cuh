@@ -20,12 +20,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
       : "memory");
 }
 
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-
 // Shared-memory descriptor of a K-major operand tile written by TMA with the
 // 128-byte swizzle: rows of 128 bytes (64 bf16 of K), 8-row groups 1024 bytes
 // apart (stride byte offset), leading byte offset unused for this layout,
