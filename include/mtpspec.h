@@ -43,7 +43,9 @@ enum {
     MTP_ERR_INVALID_ARG = -1,       /* null / misaligned pointer, k outside 1..8, T <= 0, ... */
     MTP_ERR_UNSUPPORTED_SHAPE = -2, /* dims the kernels do not implement (see MtpDims) */
     MTP_ERR_WORKSPACE = -3,         /* workspace smaller than the *_workspace_size() answer */
-    MTP_ERR_CUDA = -4               /* a CUDA runtime call or launch failed */
+    MTP_ERR_CUDA = -4,              /* a CUDA runtime call or launch failed */
+    MTP_ERR_SCRATCH_LIMIT = -5      /* mtp_draft_noalloc: the problem needs more
+                                       than MTP_STATIC_SCRATCH_BYTES of scratch */
 };
 
 /* Bits of the device status word (sticky until mtp_clear_status()). */
@@ -131,6 +133,35 @@ int mtp_draft(const MtpDims *dims, const MtpWeights *w, const void *h,
               const int32_t *ctx_len, int k, float T, int mode,
               const float *u_draft, int32_t *draft_tok, float *draft_logits,
               void *ws, size_t ws_bytes, mtp_stream_t stream);
+
+/*
+ * mtp_draft_noalloc -- mtp_draft without a caller-supplied workspace and
+ * without allocating: its scratch is a fixed device array of
+ * MTP_STATIC_SCRATCH_BYTES that is part of the library's image.  The pages
+ * describe no such call; it exists for callers that cannot hand over device
+ * memory: a host engine that has already given all free HBM to its KV-cache
+ * pool (a cudaMalloc would then fail, and it synchronises the device in any
+ * case), or code embedded in another runtime that passes in a stream but no
+ * allocator.
+ *
+ * Arguments and results as mtp_draft, except:
+ *   status  optional device int32: if not NULL, the status word (MTP_STATUS_*
+ *           bits) of this call is copied there, on the stream, after the chain.
+ * Limits: mtp_workspace_size(dims, k) must not exceed MTP_STATIC_SCRATCH_BYTES
+ * (else MTP_ERR_SCRATCH_LIMIT, nothing launched).  The first call on a device
+ * does that device's set-up (it loads the library's device image and looks up
+ * the scratch array's address), so make it before any stream capture.  Each
+ * call zeroes the scratch's status word and counters on the stream before the
+ * chain.  There is one scratch array per device: calls that overlap in time on
+ * the same device (two streams, or two host threads) race on it and must be
+ * serialised by the caller.
+ */
+#define MTP_STATIC_SCRATCH_BYTES ((size_t)4 << 20)
+int mtp_draft_noalloc(const MtpDims *dims, const MtpWeights *w, const void *h,
+                      const int32_t *last_tok, void *k_cache, void *v_cache,
+                      const int32_t *ctx_len, int k, float T, int mode,
+                      const float *u_draft, int32_t *draft_tok, float *draft_logits,
+                      int32_t *status, mtp_stream_t stream);
 
 /* Bytes of workspace spec_verify needs (0 if the arguments are invalid). */
 size_t spec_verify_workspace_size(int B, int k, int V);

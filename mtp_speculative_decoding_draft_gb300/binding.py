@@ -59,6 +59,9 @@ def _lib():
         L.mtp_draft.argtypes = [ctypes.POINTER(MtpDims), ctypes.POINTER(MtpWeights), P, P, P, P, P, I, F, I,
                                 P, P, P, P, Z, P]
         L.mtp_draft.restype = I
+        L.mtp_draft_noalloc.argtypes = [ctypes.POINTER(MtpDims), ctypes.POINTER(MtpWeights), P, P, P, P, P, I,
+                                        F, I, P, P, P, P, P]
+        L.mtp_draft_noalloc.restype = I
         L.spec_verify_workspace_size.argtypes = [I, I, I]
         L.spec_verify_workspace_size.restype = Z
         L.spec_verify.argtypes = [I, I, I, F, I, P, P, P, P, P, P, P, P, P, Z, P]
@@ -144,6 +147,22 @@ def mtp_draft(dims, weights, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode,
         _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
     if rc != 0:
         raise MtpError(rc, "mtp_draft")
+
+
+def mtp_draft_noalloc(dims, weights, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode, u_draft,
+                      draft_tok, draft_logits, status=None, stream=None):
+    """mtp_draft on the library's static scratch (no workspace argument)."""
+    B, V = dims.B, dims.V
+    rc = _lib().mtp_draft_noalloc(
+        ctypes.byref(dims), ctypes.byref(weights), _ptr(h, "h", torch.bfloat16, B * dims.d),
+        _ptr(last_tok, "last_tok", torch.int32, B), _ptr(k_cache, "k_cache", torch.bfloat16),
+        _ptr(v_cache, "v_cache", torch.bfloat16), _ptr(ctx_len, "ctx_len", torch.int32, B), int(k),
+        float(T), int(mode), _ptr(u_draft, "u_draft", torch.float32, B * k),
+        _ptr(draft_tok, "draft_tok", torch.int32, B * k),
+        _ptr(draft_logits, "draft_logits", torch.float32, B * k * V),
+        _ptr(status, "status", torch.int32, 1), _stream(stream))
+    if rc != 0:
+        raise MtpError(rc, "mtp_draft_noalloc")
 
 
 def spec_verify(B, k, V, T, mode, target_logits, draft_logits, draft_tok, u_accept, u_final,

@@ -248,6 +248,36 @@ int prepare_verify(int B, int k, int V, float T, int mode, const float *target, 
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MTP_OK : MTP_ERR_CUDA; }
 
+// Scratch of mtp_draft_noalloc: one array per device, part of this module's
+// device image, so no call allocates.  Static device memory starts zeroed.
+__device__ __align__(256) unsigned char g_static_scratch[MTP_STATIC_SCRATCH_BYTES];
+
+struct ScratchSlot {
+  bool init = false;
+  void *ptr = nullptr;
+};
+ScratchSlot g_scratch_slot[64];
+
+// The device address of g_static_scratch on the current device, looked up once
+// per device (with that device current).
+int static_scratch(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MTP_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  ScratchSlot &sl = g_scratch_slot[dev];
+  if (!sl.init) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return MTP_ERR_CUDA;
+    }
+    sl.ptr = p;
+    sl.init = true;
+  }
+  *out = sl.ptr;
+  return MTP_OK;
+}
+
 }  // namespace
 }  // namespace mtp
 
@@ -269,6 +299,31 @@ int mtp_draft(const MtpDims *dims, const MtpWeights *w, const void *h, const int
   if (rc) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = run_draft(D, s);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return cuda_rc(e);
+}
+
+int mtp_draft_noalloc(const MtpDims *dims, const MtpWeights *w, const void *h, const int32_t *last_tok,
+                      void *k_cache, void *v_cache, const int32_t *ctx_len, int k, float T, int mode,
+                      const float *u_draft, int32_t *draft_tok, float *draft_logits, int32_t *status,
+                      mtp_stream_t stream) {
+  int rc = check_dims(dims, k);
+  if (rc) return rc;
+  if (draft_layout(*dims, k).total > MTP_STATIC_SCRATCH_BYTES) return MTP_ERR_SCRATCH_LIMIT;
+  if (status && (reinterpret_cast<uintptr_t>(status) & 3u) != 0) return MTP_ERR_INVALID_ARG;
+  void *scratch = nullptr;
+  if ((rc = static_scratch(&scratch))) return rc;
+  Draft D;
+  rc = prepare_draft(dims, w, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode, u_draft, draft_tok, draft_logits,
+                     scratch, MTP_STATIC_SCRATCH_BYTES, false, &D);
+  if (rc) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the status word and the LM-head ticket counter (the first two aligned
+  // slots) must start at zero
+  cudaError_t e = cudaMemsetAsync(scratch, 0, 2 * kAlign, s);
+  if (e == cudaSuccess) e = run_draft(D, s);
+  if (e == cudaSuccess && status)
+    e = cudaMemcpyAsync(status, D.c.status, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess) e = cudaGetLastError();
   return cuda_rc(e);
 }
@@ -337,6 +392,7 @@ const char *mtp_error_string(int code) {
     case MTP_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
     case MTP_ERR_WORKSPACE: return "workspace too small";
     case MTP_ERR_CUDA: return "CUDA error";
+    case MTP_ERR_SCRATCH_LIMIT: return "problem needs more scratch than MTP_STATIC_SCRATCH_BYTES";
     default: return "unknown error";
   }
 }
