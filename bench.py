@@ -49,6 +49,35 @@ def lmhead_bytes(w, logits_out):
     return w.V * w.d * 2 + (w.B * w.V * 4 if logits_out else 0)
 
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a
+# kernel from one ncu capture, with the SHA-256 of the sources the kernel is
+# built from at capture time.  A figure is reported only while those sources
+# are unchanged; the summaries of the captures are kept under profiles/.
+NCU_TRAFFIC = {
+    ("lm_head_gemv", "single_greedy_b1_d4096_v151936_ctx4096"): {
+        "bytes": 1244746240 + 2924800,
+        "sources": {
+            "csrc/draft.cu": "79780104dbc932848f791ad1fc2472422a3f9590b82cf6fa3caf919609e8e453",
+            "csrc/draft_ops.cuh": "ee49d719a429f452c36d9668dfe63f0e031b4af814a8cad66a458d8eba41d1c3",
+            "csrc/common.cuh": "b0c0558dd02abe592f024b86032afd9c52bdeb68988177d7046fef9e10f74863",
+        },
+    },
+}
+
+
+def ncu_traffic(kernel, workload):
+    import hashlib
+    rec = NCU_TRAFFIC.get((kernel, workload))
+    if rec is None:
+        return None
+    pkg = os.path.join(ROOT, "mtp_speculative_decoding_draft_gb300")
+    for rel, digest in rec["sources"].items():
+        with open(os.path.join(pkg, rel), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != digest:
+                return None
+    return rec["bytes"]
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -74,7 +103,7 @@ class ClockSampler:
                  "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
@@ -399,7 +428,8 @@ def run_ours(args):
         "hbm_bytes_per_step": sb,
         "hbm_roofline_frac": sb / (ms * 1e-3) / 1e9 / peak,
         "roofline": {"bound": "hbm", "kernel": "lm_head_gemv", "achieved": ach, "peak": peak, "unit": "GB/s",
-                     "frac": ach / peak, "peak_kind": peak_kind, "traffic": None,
+                     "frac": ach / peak, "peak_kind": peak_kind,
+                     "traffic": ncu_traffic("lm_head_gemv", w.name) if not logits_out else None,
                      "bytes_per_launch": lm_b, "avg_launch_ms": lm_avg, "launches": lm_n},
         "kernel_ms_per_step": {"lm_head": lm_ms / args.steps, "verify": ver_ms / args.steps,
                                "attention": att_ms / args.steps, "gemv_other": gem_ms / args.steps},
@@ -425,7 +455,7 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=W.SINGLE_GREEDY.name, choices=sorted(W.WORKLOADS))
