@@ -20,6 +20,11 @@
  *    of range, a context length past the cache, a non-finite logit row, a
  *    bounded wait that ran out) set bits of a status word inside the workspace;
  *    mtp_get_status() reads it.
+ *  - A workspace must be zero-filled (cudaMemset) before its first use.  It
+ *    holds the status word and the verifier's work counters and tickets, which
+ *    every call leaves at zero for the next one; zero it again after a call
+ *    that set MTP_STATUS_TIMEOUT.  Calls that share a workspace must not
+ *    overlap in time.
  *  - Random draws use caller-supplied uniforms in [0, 1), so every result is a
  *    deterministic function of the inputs, bit for bit from run to run.
  *  - bf16 means IEEE binary32's upper 16 bits (the storage type of the weights,

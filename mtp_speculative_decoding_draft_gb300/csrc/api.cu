@@ -25,6 +25,7 @@ struct DevInfo {
   bool init = false;
   int sms = 0;
   int max_cluster = 8;
+  int verify_bps = 1;  // verifier CTAs resident per SM
 };
 std::mutex g_mu;
 DevInfo g_dev[64];
@@ -36,15 +37,9 @@ int device_info(DevInfo *out) {
   DevInfo &di = g_dev[dev];
   if (!di.init) {
     if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MTP_ERR_CUDA;
-    // clusters of 16 CTAs are a non-portable size: use them only if the device
-    // can keep one resident with the verifier's shared-memory footprint
     di.max_cluster = 8;
-    if (verify_set_attributes(16) == cudaSuccess && verify_max_active_clusters(16) > 0) {
-      di.max_cluster = 16;
-    } else {
-      cudaGetLastError();
-      if (verify_set_attributes(8) != cudaSuccess) return MTP_ERR_CUDA;
-    }
+    if (verify_set_attributes() != cudaSuccess) return MTP_ERR_CUDA;
+    di.verify_bps = verify_blocks_per_sm();
     di.init = true;
   }
   *out = di;
@@ -68,7 +63,7 @@ int check_dims(const MtpDims *d, int k) {
 }
 
 struct WsLayout {
-  size_t status, lm_cnt, x0, x1, x2, q, o, act, lm_part, logits, total;
+  size_t status, lm_cnt, x0, x1, x2, q, o, act, lm_part, logits, vstate, total;
 };
 
 WsLayout draft_layout(const MtpDims &d, int k) {
@@ -94,6 +89,8 @@ WsLayout draft_layout(const MtpDims &d, int k) {
   off += up((size_t)d.B * kMaxLmGrid * 4 * 4);
   L.logits = off;
   off += up((size_t)d.B * k * d.V * 4);
+  L.vstate = off;
+  off += up(verify_state_bytes(d.B, k, d.V));
   L.total = off;
   return L;
 }
@@ -221,28 +218,28 @@ cudaError_t run_draft(Draft &D, cudaStream_t s) {
 
 int prepare_verify(int B, int k, int V, float T, int mode, const float *target, const float *draft,
                    const int32_t *draft_tok, const float *u_accept, const float *u_final, int32_t *out_tok,
-                   int32_t *accept_len, int32_t *num_accepted, void *ws, size_t ws_bytes, bool draft_check,
-                   VerifyArgs *a, int *cluster) {
+                   int32_t *accept_len, int32_t *num_accepted, void *state, size_t state_bytes, bool draft_check,
+                   VerifyArgs *a) {
   if (B < 1 || k < 1 || k > 8 || V < 1 || V > (1 << 30) || B > (1 << 20)) return MTP_ERR_INVALID_ARG;
   if (mode != MTP_GREEDY && mode != MTP_STOCHASTIC) return MTP_ERR_INVALID_ARG;
   if (mode == MTP_STOCHASTIC && !(T > 0.f && T < 1e30f)) return MTP_ERR_INVALID_ARG;
-  const void *ptrs[] = {target, draft_tok, out_tok, accept_len, num_accepted, ws};
+  const void *ptrs[] = {target, draft_tok, out_tok, accept_len, num_accepted, state};
   for (const void *p : ptrs)
     if (!aligned16(p)) return MTP_ERR_INVALID_ARG;
   if (mode == MTP_STOCHASTIC) {
     if (draft_check && !aligned16(draft)) return MTP_ERR_INVALID_ARG;
     if (!aligned16(u_accept) || !aligned16(u_final)) return MTP_ERR_INVALID_ARG;
   }
-  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MTP_ERR_INVALID_ARG;
-  if (ws_bytes < kAlign) return MTP_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(state) & (kAlign - 1)) != 0) return MTP_ERR_INVALID_ARG;
+  if (state_bytes < verify_state_bytes(B, k, V)) return MTP_ERR_WORKSPACE;
   DevInfo di;
   int rc = device_info(&di);
   if (rc) return rc;
   a->B = B; a->k = k; a->V = V; a->mode = mode; a->T = mode == MTP_STOCHASTIC ? T : 1.f;
   a->target = target; a->draft = draft; a->draft_tok = draft_tok; a->u_accept = u_accept; a->u_final = u_final;
   a->out_tok = out_tok; a->accept_len = accept_len; a->num_accepted = num_accepted;
-  a->status = static_cast<int *>(ws);
-  *cluster = verify_cluster_size(B, di.sms, di.max_cluster);
+  if (!plan_verify(B, k, V, mode, di.sms, di.verify_bps, &a->p)) return MTP_ERR_UNSUPPORTED_SHAPE;
+  verify_bind_state(*a, state);
   return MTP_OK;
 }
 
@@ -330,19 +327,21 @@ int mtp_draft_noalloc(const MtpDims *dims, const MtpWeights *w, const void *h, c
 
 size_t spec_verify_workspace_size(int B, int k, int V) {
   if (B < 1 || k < 1 || k > 8 || V < 1) return 0;
-  return kAlign;
+  return kAlign + up(verify_state_bytes(B, k, V));
 }
 
 int spec_verify(int B, int k, int V, float T, int mode, const float *target_logits, const float *draft_logits,
                 const int32_t *draft_tok, const float *u_accept, const float *u_final, int32_t *out_tok,
                 int32_t *accept_len, int32_t *num_accepted, void *ws, size_t ws_bytes, mtp_stream_t stream) {
   VerifyArgs a{};
-  int cluster = 1;
+  if (!aligned16(ws) || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MTP_ERR_INVALID_ARG;
+  if (ws_bytes < kAlign) return MTP_ERR_WORKSPACE;
   int rc = prepare_verify(B, k, V, T, mode, target_logits, draft_logits, draft_tok, u_accept, u_final, out_tok,
-                          accept_len, num_accepted, ws, ws_bytes, true, &a, &cluster);
+                          accept_len, num_accepted, static_cast<char *>(ws) + kAlign, ws_bytes - kAlign, true, &a);
   if (rc) return rc;
+  a.status = static_cast<int *>(ws);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = timed(MTP_KC_VERIFY, s, [&] { return launch_verify(a, cluster, s, false); });
+  cudaError_t e = timed(MTP_KC_VERIFY, s, [&] { return launch_verify(a, s, false); });
   if (e == cudaSuccess) e = cudaGetLastError();
   return cuda_rc(e);
 }
@@ -357,14 +356,14 @@ int spec_step(const MtpDims *dims, const MtpWeights *w, const void *h, const int
                          draft_logits, ws, ws_bytes, mode == MTP_STOCHASTIC, &D);
   if (rc) return rc;
   VerifyArgs a{};
-  int cluster = 1;
+  const WsLayout L = draft_layout(*dims, k);
   rc = prepare_verify(dims->B, k, dims->V, T, mode, target_logits, D.c.logits, draft_tok, u_accept, u_final, out_tok,
-                      accept_len, num_accepted, ws, ws_bytes, false, &a, &cluster);
+                      accept_len, num_accepted, static_cast<char *>(ws) + L.vstate, L.total - L.vstate, false, &a);
   if (rc) return rc;
   a.status = D.c.status;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = run_draft(D, s);
-  if (e == cudaSuccess) e = timed(MTP_KC_VERIFY, s, [&] { return launch_verify(a, cluster, s, use_pdl()); });
+  if (e == cudaSuccess) e = timed(MTP_KC_VERIFY, s, [&] { return launch_verify(a, s, use_pdl()); });
   if (e == cudaSuccess) e = cudaGetLastError();
   return cuda_rc(e);
 }

@@ -68,6 +68,25 @@ size_t attention_smem_bytes(int Dh);
 int attention_cluster_size(int ctx_max, int max_cluster);
 
 // Verification launch.
+struct VerifyPlan {
+  int NS;          // 512-element sub-chunks per logit row
+  int m;           // sub-chunks per worker-warp slice of a chunk
+  int U;           // chunks (8 slices) per logit row
+  int nrows;       // logit rows per sequence: k+1 (greedy) or 2k+1 (stochastic)
+  int n1;          // work items per sequence (one per row and chunk)
+  unsigned total;  // work items
+  int grid;        // CTAs
+  int pol;         // L2 policy of rows a rejection may re-read: 0 evict-last on
+                   // position 0, 1 evict-normal on all, 2 evict-last on all
+};
+
+// A stochastic sequence's decision, published for its pass-2 items.
+struct VerifyDecision {
+  int acc_n, rej, kind;  // kind 0: residual at rej; 2: bonus draw from row k
+  float uf;
+  float Mt, Ml, iZt, iZl;  // row maxima and reciprocal partition sums
+};
+
 struct VerifyArgs {
   int B, k, V, mode;
   float T;
@@ -80,15 +99,24 @@ struct VerifyArgs {
   int *accept_len;       // [B]
   int *num_accepted;     // [B]
   int *status;
+  // state in the workspace: zero before the first call, left zero by each call
+  unsigned *ctl;          // [0] claim counter, [1] CTAs finished
+  unsigned *cnt1, *cnt2;  // [B] pass-1 / pass-2 tickets
+  unsigned *flag;         // [B] decision published
+  VerifyDecision *dec;    // [B]
+  float2 *part1;          // [B][nrows][U] published per-chunk partials
+  float2 *mass2;          // [B][NS] published sub-chunk sampling masses
+  VerifyPlan p;
 };
 
-constexpr int kVerifyThreads = 320;  // 8 consumer warps, a producer warp, an agent warp
+constexpr int kVerifyThreads = 320;  // 8 streaming worker warps, a coordinator and a decider warp
 
-int verify_cluster_size(int B, int num_sms, int max_cluster);
-size_t verify_smem_bytes(int B, int k, int V, int cluster);
-cudaError_t launch_verify(const VerifyArgs &a, int cluster, cudaStream_t s, bool pdl);
-cudaError_t verify_set_attributes(int max_cluster);
-int verify_max_active_clusters(int cluster);
+size_t verify_state_bytes(int B, int k, int V);
+void verify_bind_state(VerifyArgs &a, void *state);
+bool plan_verify(int B, int k, int V, int mode, int num_sms, int blocks_per_sm, VerifyPlan *p);
+cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s, bool pdl);
+cudaError_t verify_set_attributes();
+int verify_blocks_per_sm();
 
 // bookkeeping shared with api.cu
 void note_launch();

@@ -3,34 +3,41 @@
 // Decoding and MTP: Why Guessing Is Free", sections "Speculative decoding:
 // draft, then verify" and "It's exact, not approximate").
 //
-// One thread-block cluster of C CTAs handles one sequence at a time; CTA r owns
-// the vocabulary slice [r*S, (r+1)*S) of every logit row of the sequence.  At
-// most 64 sequences are in flight (persistent clusters loop over the rest).
+// Every logit row is cut into chunks of 8 slices, a slice being m sub-chunks
+// of 512 elements.  Each CTA has 8 worker warps and a coordinator warp; work
+// items are chunks:
+//  pass-1 item (b, row, chunk)  reduced to (max, lowest argmax) -- greedy -- or
+//                               to the max and sum exp2((x - max) * log2e / T);
+//  pass-2 item (b, chunk)       stochastic only: the sampling weights -- max(0,
+//                               p - q) and p at the first rejection, or p at the
+//                               bonus position -- summed per sub-chunk.
+// Coordinators claim the pass-1 items in index order (sequence by sequence)
+// from one atomic counter and queue them in shared memory; worker w streams
+// slice w of every queued chunk through its own ring of 4 KB shared-memory
+// stages (1-D TMA bulk copies issued up to three stages ahead, across items)
+// and hands its partial back through shared memory.  The coordinator merges
+// the slices and publishes the chunk's partial; a third role, the decider
+// warp, takes the tickets (up to 32 per round trip) so that the coordinator
+// never waits on one.  The decider that takes a sequence's last ticket
+// combines the partials in chunk order, takes the accept / reject decisions
+// and publishes them.  Pass-2 item (b, u) is
+// owned by CTA (b U + u) mod G, which queues it ahead of new claims as soon as
+// b is decided -- so the re-read rows are still in L2 and the work is spread
+// evenly -- and the decider that takes its last pass-2 ticket locates the
+// sub-chunk holding the inverse-CDF crossing and rescans it in float64.  No
+// result depends on which CTA ran which pass-1 item.
 //
-// Warp roles in every CTA:
-//  producer (1 warp)   streams the rows of its slices -- target k, then target /
-//                      draft k-1 .. 1, then target / draft 0 -- through a ring
-//                      of 16 KB shared-memory pieces with 1-D TMA bulk copies,
-//                      paced by per-piece full / empty mbarriers;
-//  consumers (8 warps) reduce every slice to (max, lowest argmax) -- greedy --
-//                      or to the max and sum exp2((x - max) * log2e / T)
-//                      (per piece: its max, then one exp pass), send the
-//                      per-row partials to CTA 0 of the cluster (remote stores
-//                      and a remote mbarrier arrive), and, at the first
-//                      rejection r or for the bonus token, sum the sampling
-//                      weights max(0, p - q) (or p) of their slices of the rows
-//                      at r per 512-element sub-chunk;
-//  agent (1 warp, CTA 0 only) combines the partials in rank order, takes the
-//                      accept / reject decisions, picks the CTA that holds the
-//                      inverse-CDF crossing and broadcasts both through remote
-//                      stores and arrives.  That CTA rescans one sub-chunk in
-//                      float64 and writes the outputs.
-//
-// No cluster barrier runs inside the loop, so the producer keeps streaming
-// while a sequence is decided.  The rows of position 0 are read last with an
-// L2 evict-last hint: with at most 64 sequences in flight they are still in L2
-// when a rejection at position 0 re-reads them.  Every wait is a bounded
-// mbarrier wait that gives up after a time limit and flags the status word.
+// Partials and masses are published with relaxed stores of words that are
+// never zero and read by polling until non-zero; decisions with a release /
+// acquire flag.  Readers zero what they consumed, as they do the tickets and
+// flags, so each call leaves the state in the workspace zero for the next
+// one.  A coordinator never blocks: it waits for nothing but published data
+// whose producers were all claimed by running CTAs.  Every wait is bounded and
+// flags the status word when it gives up.
+#include <stdlib.h>
+
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -38,637 +45,1183 @@ namespace mtp {
 
 namespace {
 
-constexpr int kSub = 512;      // sampling sub-chunk (elements)
-constexpr int kPiece = 4096;   // floats per ring piece (16 KB)
-constexpr int kCons = 256;     // consumer threads (warps 0..7)
-constexpr int kConsWarps = kCons / 32;
-constexpr int kProducerWarp = 8, kAgentWarp = 9;
-constexpr int kMaxRows = 17;   // 2k+1 rows for k <= 8
-constexpr int kMaxRing = 8;
-constexpr int kMaxC = 16;
+constexpr int kWorkers = 8;      // worker warps; then the coordinator and the decider warp
+constexpr int kDQ = 64;          // published items waiting for their tickets
+constexpr int kStages = 3;       // ring stages per worker
+#ifndef MTP_VERIFY_STAGE
+#define MTP_VERIFY_STAGE 1024
+#endif
+constexpr int kStage = MTP_VERIFY_STAGE;  // floats per stage
+constexpr int kSub = 512;        // sampling sub-chunk (elements)
+#ifndef MTP_VERIFY_Q
+#define MTP_VERIFY_Q 3
+#endif
+constexpr int kQ = MTP_VERIFY_Q;  // queued items per CTA
+constexpr int kMaxM = 16;        // sub-chunks per slice, at most
+constexpr unsigned kFull = 0xffffffffu;
 
-struct RowSlice {  // one row's slice: the 16-byte aligned body [h1, b1) of [v0, v1)
-  const float *row;
-  int h1, b1;
+// One queued item.
+struct Slot {
+  int pass, b, r, u;        // pass 0: stop
+  const float *p0, *p1;     // row bases: the row (pass 1); target, draft (pass 2)
+  int draft, keep, kind, pad;
+  float Mt, Ml, iZt, iZl;   // pass 2: the sequence's decision
+  float2 part[kWorkers];    // pass 1: per-slice partials
+  float2 mass[kWorkers][kMaxM];  // pass 2: per-sub-chunk (residual, target) masses
 };
 
-struct Smem {
-  // CTA 0 (leader) side: the cluster's partials, per sequence parity
-  float part[2][kMaxC][kMaxRows][2];  // max, sum | argmax bits
-  double tot[2][kMaxC][2];            // residual mass, target mass
-  uint64_t stats_bar, samp_bar;       // C arrivals per sequence
-  // every CTA: the leader's broadcasts
-  uint64_t dec_bar, sdec_bar;         // 1 arrival per sequence
-  uint64_t full[kMaxRing], empty[kMaxRing];
-  int acc_n, rej, kind;
-  float Mt, Ml, iZt, iZl;
-  int owner, use_p;
-  double target;
-  float red[2 * kConsWarps];
-  float subR[2], subP[2];  // placeholders; the sub-chunk arrays follow the ring
+struct Shared {
+  Slot slot[kQ];
+  uint64_t ready[kQ];  // coordinator -> workers
+  uint64_t done[kQ];   // workers -> coordinator
+  uint64_t ring_bar[kWorkers][kStages];
+  // coordinator -> decider: published items (b, pass) awaiting their tickets
+  int dq_b[kDQ], dq_pass[kDQ];
+  unsigned dq_tail, dq_head;
+  int coord_done;
 };
 
-__host__ __device__ constexpr size_t smem_hdr() { return (sizeof(Smem) + 127) / 128 * 128; }
+constexpr size_t kHdr = (sizeof(Shared) + 127) / 128 * 128;
+constexpr size_t kSmemBytes = kHdr + (size_t)kWorkers * kStages * kStage * 4;
 
-__host__ __device__ inline int slice_len(int V, int C) { return ((V + C - 1) / C + 3) / 4 * 4; }
+// ---------------------------------------------------------------- gpu-scope memory
 
-__device__ __forceinline__ void slice_bounds(size_t row_index, int V, int v0, int v1, int &h1, int &b1) {
-  const size_t e0 = row_index * (size_t)V + v0;
-  h1 = min(v1, v0 + (int)((4 - (e0 & 3)) & 3));
-  b1 = h1 + (v1 - h1) / 4 * 4;
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed64(const void *p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed64(void *p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// A published word: poll until it is non-zero (bounded).
+__device__ unsigned long long poll64(const void *p, int *status) {
+  unsigned long long v = ld_relaxed64(p);
+  if (v) return v;
+  const uint64_t t0 = global_timer_ns();
+  while ((v = ld_relaxed64(p)) == 0ull) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      set_status(status, kStatusTimeout);
+      return 0ull;
+    }
+    __nanosleep(32);
+  }
+  return v;
+}
+
+// Up to kBatch published words per lane (lane + 32 i < n): all loads issued
+// first, then the few that had not landed are polled.
+constexpr int kBatch = 4;
+__device__ __forceinline__ void load_batch(const unsigned long long *base, int n, int lane, unsigned long long *w,
+                                           int *status) {
+#pragma unroll
+  for (int i = 0; i < kBatch; ++i) w[i] = lane + 32 * i < n ? ld_relaxed64(base + lane + 32 * i) : 1ull;
+#pragma unroll
+  for (int i = 0; i < kBatch; ++i)
+    if (w[i] == 0ull) w[i] = poll64(base + lane + 32 * i, status);
+}
+
+__device__ __forceinline__ unsigned long long pack(float lo, float hi) {
+  return (unsigned long long)__float_as_uint(lo) | ((unsigned long long)__float_as_uint(hi) << 32);
+}
+__device__ __forceinline__ float lo_f(unsigned long long w) { return __uint_as_float((unsigned)w); }
+__device__ __forceinline__ float hi_f(unsigned long long w) { return __uint_as_float((unsigned)(w >> 32)); }
+
+// Non-zero encodings of a published partial.  Stochastic (max, sum): a finite
+// max has sum >= 1 and -inf is not zero.  Greedy (max, argmax + 1).
+__device__ __forceinline__ unsigned long long enc_greedy(float v, int i) {
+  return (unsigned long long)__float_as_uint(v) | ((unsigned long long)((unsigned)i + 1u) << 32);
+}
+__device__ __forceinline__ int dec_greedy_idx(unsigned long long w) { return (int)((unsigned)(w >> 32) - 1u); }
+// Masses (>= 0) carry the sign bit.
+__device__ __forceinline__ unsigned long long enc_mass(float r, float p) {
+  return pack(__uint_as_float(__float_as_uint(r) | 0x80000000u), __uint_as_float(__float_as_uint(p) | 0x80000000u));
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase that parks the warp (suspend-time hint)
+// instead of spinning; the hardware wakes it when the phase completes.
+__device__ __forceinline__ bool mbar_sleep_wait(uint64_t *bar, uint32_t parity, int *status) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
+        : "memory");
+    if (ok) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      set_status(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+// 2^x, hardware approximation (relative error about 2^-22; -inf gives +0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Sampling weight of one element: residual max(0, p - q) (kind 0), target p
 // (kind 1), unnormalised target weight exp2((t - Mt) c) (kind 2).
 __device__ __forceinline__ float weight(int kind, float t, float l, float Mt, float Ml, float iZt, float iZl,
                                         float c) {
-  const float e = exp2f((t - Mt) * c);
+  const float e = ex2((t - Mt) * c);
   if (kind == 2) return e;
   const float p = e * iZt;
   if (kind == 1) return p;
-  return fmaxf(0.f, p - exp2f((l - Ml) * c) * iZl);
+  return fmaxf(0.f, p - ex2((l - Ml) * c) * iZl);
 }
 
-struct Layout {
-  int ring;  // ring pieces
-  size_t bytes;
+// ---------------------------------------------------------------- items
+
+struct Item {
+  int pass;  // 1, 2; 0: none
+  int b, r, u;
 };
 
-__host__ __device__ inline Layout layout(int V, int C) {
-  Layout L{};
-  const int chunk = slice_len(V, C);
-  const int nsub = (chunk + kSub - 1) / kSub + 2;
-  const size_t fixed = smem_hdr() + (size_t)2 * nsub * 4 + 64;
-  const size_t budget = 108 * 1024;  // two CTAs per SM
-  L.ring = (int)((budget - fixed) / ((size_t)kPiece * 4));
-  if (L.ring > kMaxRing) L.ring = kMaxRing;
-  if (L.ring < 2) L.ring = 2;
-  L.bytes = fixed + (size_t)L.ring * kPiece * 4;
-  return L;
+__device__ __forceinline__ Item decode(const VerifyArgs &a, unsigned idx) {
+  const VerifyPlan &p = a.p;
+  Item it{0, 0, 0, 0};
+  if (idx >= p.total) return it;
+  const unsigned n1 = (unsigned)p.n1, U = (unsigned)p.U;
+  const unsigned rem = idx % n1;
+  it.pass = 1;
+  it.b = (int)(idx / n1);
+  it.r = (int)(rem / U);
+  it.u = (int)(rem % U);
+  return it;
 }
 
-}  // namespace
-
-size_t verify_smem_bytes(int B, int k, int V, int cluster) {
-  (void)B;
-  (void)k;
-  return layout(V, cluster).bytes;
+// Stream row r of a sequence -- greedy: target k .. 0; stochastic: target
+// k .. 1, draft k-1 .. 1, target 0, draft 0 -- as an index into the target
+// [B, k+1] or draft [B, k] row arrays.
+__device__ __forceinline__ size_t stream_row(const VerifyArgs &a, int b, int r, bool &draft) {
+  const int k = a.k;
+  int pos;
+  draft = false;
+  if (a.mode == 0 || r < k) {
+    pos = k - r;
+  } else if (r < 2 * k - 1) {
+    pos = 2 * k - 1 - r;
+    draft = true;
+  } else {
+    pos = 0;
+    draft = r == 2 * k;
+  }
+  return draft ? (size_t)b * k + pos : (size_t)b * (k + 1) + pos;
 }
 
-__global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(VerifyArgs a) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int C = (int)cluster_size();
-  const int rank = (int)cluster_rank();
-  const int V = a.V, k = a.k;
+// Stream rows of target position j and of draft position j.
+__device__ __forceinline__ int trow(int mode, int k, int j) { return mode == 0 ? k - j : (j == 0 ? 2 * k - 1 : k - j); }
+__device__ __forceinline__ int drow(int k, int j) { return j == 0 ? 2 * k : 2 * k - 1 - j; }
+
+// Sub-chunks [s0, s1) of slice w of chunk u.
+__device__ __forceinline__ void slice_subs(const VerifyPlan &p, int u, int w, int &s0, int &s1) {
+  s0 = min(p.NS, (u * kWorkers + w) * p.m);
+  s1 = min(p.NS, s0 + p.m);
+}
+
+// What a worker's ring streams for one item: nq pieces of `per` elements from
+// p0 (and, for the residual, the same from p1 into the second half of the stage).
+struct Src {
+  const float *p0, *p1;
+  int len, per, nq;
+  uint64_t pol;
+  bool draft;  // reads draft logits: the drafter must have finished
+  bool valid;
+};
+
+// ---------------------------------------------------------------- decisions
+
+__device__ __forceinline__ const unsigned long long *part1_row(const VerifyArgs &a, int b, int r) {
+  return reinterpret_cast<const unsigned long long *>(a.part1) + ((size_t)b * a.p.nrows + r) * a.p.U;
+}
+
+// Combined (max, sum) of stream row r of sequence b over its U chunks, in
+// chunk order; every lane gets the result.
+__device__ void row_lse(const VerifyArgs &a, int b, int r, float c, float &M, double &Z) {
+  const int U = a.p.U, lane = threadIdx.x & 31;
+  const unsigned long long *row = part1_row(a, b, r);
+  float m = -INFINITY;
+  double z = 0.0;
+  for (int u0 = 0; u0 < U; u0 += 32 * kBatch) {  // one round of loads per 128 chunks
+    unsigned long long w[kBatch];
+    load_batch(row + u0, U - u0, lane, w, a.status);
+    float mm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i)
+      if (lane + 32 * i < U - u0) mm = fmaxf(mm, lo_f(w[i]));
+    mm = warp_max(mm);
+    const float mn = fmaxf(m, mm);
+    if (mn != -INFINITY) {
+      double zz = 0.0;
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const float pm = lo_f(w[i]);
+        if (lane + 32 * i < U - u0 && pm != -INFINITY) zz += (double)hi_f(w[i]) * (double)ex2((pm - mn) * c);
+      }
+      z = (m == -INFINITY ? 0.0 : z * (double)ex2((m - mn) * c)) + zz;
+      m = mn;
+    }
+  }
+  M = m;
+  Z = warp_sum_d(z);
+}
+
+// (max, lowest argmax) of stream row r of sequence b; every lane gets it.
+__device__ void row_argmax(const VerifyArgs &a, int b, int r, float &M, int &I) {
+  const int U = a.p.U, lane = threadIdx.x & 31;
+  const unsigned long long *row = part1_row(a, b, r);
+  M = -INFINITY;
+  I = 0x7fffffff;
+  for (int u0 = 0; u0 < U; u0 += 32 * kBatch) {
+    unsigned long long w[kBatch];
+    load_batch(row + u0, U - u0, lane, w, a.status);
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i)
+      if (lane + 32 * i < U - u0) argmax_merge(M, I, lo_f(w[i]), dec_greedy_idx(w[i]));
+  }
+  warp_argmax(M, I);
+}
+
+// Zero the sequence's published partials for the next call (each is read,
+// i.e. has landed, before it is overwritten).
+__device__ void clear_part1(const VerifyArgs &a, int b) {
+  const int lane = threadIdx.x & 31, n = a.p.nrows * a.p.U;
+  unsigned long long *base = reinterpret_cast<unsigned long long *>(a.part1) + (size_t)b * n;
+  for (int i0 = 0; i0 < n; i0 += 32 * kBatch) {
+    unsigned long long w[kBatch];
+    load_batch(base + i0, n - i0, lane, w, a.status);
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i)
+      if (lane + 32 * i < n - i0) st_relaxed64(base + i0 + lane + 32 * i, 0ull);
+  }
+}
+
+// Greedy decision of sequence b (warp-collective): accept drafts while they
+// equal the target argmax, then emit the argmax of the first disagreeing row.
+__device__ void decide_greedy(const VerifyArgs &a, int b) {
+  const int k = a.k, V = a.V, lane = threadIdx.x & 31;
+  grid_dep_wait();  // the drafts come from the drafter
+  const int my = lane < k ? __ldcg(&a.draft_tok[(size_t)b * k + lane]) : 0;
+  int acc_n = 0;
+  float M;
+  int I;
+  for (;;) {
+    row_argmax(a, b, trow(0, k, acc_n), M, I);
+    if (acc_n == k) break;
+    const int d = __shfl_sync(kFull, my, acc_n);
+    if (d < 0 || d >= V) {
+      if (lane == 0) set_status(a.status, kStatusBadToken);
+      break;
+    }
+    if (!(M > -INFINITY) && lane == 0) set_status(a.status, kStatusNonFinite);
+    if (I != d) break;
+    ++acc_n;
+  }
+  int *o = a.out_tok + (size_t)b * (k + 1);
+  if (lane <= k) o[lane] = lane < acc_n ? my : (lane == acc_n ? (I == 0x7fffffff ? 0 : I) : -1);
+  if (lane == 0) {
+    a.accept_len[b] = acc_n + 1;
+    a.num_accepted[b] = acc_n;
+    a.cnt1[b] = 0u;
+  }
+  clear_part1(a, b);
+}
+
+// Stochastic decision of sequence b (warp-collective): the ratio tests in
+// position order; publishes the sampling task for the pass-2 items.
+__device__ void decide_stochastic(const VerifyArgs &a, int b, float c) {
+  const int k = a.k, V = a.V, lane = threadIdx.x & 31;
+  grid_dep_wait();
+  // lanes 0-7: target logit at drafted token j; 8-15: draft logit at it;
+  // 16-23: u_accept; lane 24: u_final
+  const int j = lane & 7, g = lane >> 3;
+  const int dj = j < k ? __ldcg(&a.draft_tok[(size_t)b * k + j]) : -1;
+  const bool valid = dj >= 0 && dj < V;
+  float val = 0.f;
+  if (g == 0 && j < k && valid) val = __ldg(&a.target[((size_t)b * (k + 1) + j) * V + dj]);
+  if (g == 1 && j < k && valid) val = __ldcg(&a.draft[((size_t)b * k + j) * V + dj]);
+  if (g == 2 && j < k) val = __ldg(&a.u_accept[(size_t)b * k + j]);
+  if (lane == 24) val = __ldg(&a.u_final[b]);
+  int acc_n = 0, rej = k;
+  float Mt = 0.f, Ml = 0.f;
+  double Zt = 1.0, Zl = 1.0;
+  for (int q = 0; q < k; ++q) {
+    const int d = __shfl_sync(kFull, dj, q);
+    const float td = __shfl_sync(kFull, val, q), ld = __shfl_sync(kFull, val, 8 + q);
+    const float ua = __shfl_sync(kFull, val, 16 + q);
+    bool accept = false;
+    row_lse(a, b, trow(1, k, q), c, Mt, Zt);
+    row_lse(a, b, drow(k, q), c, Ml, Zl);
+    if (d < 0 || d >= V) {
+      if (lane == 0) set_status(a.status, kStatusBadToken);
+    } else {
+      if ((Mt == -INFINITY || Ml == -INFINITY) && lane == 0) set_status(a.status, kStatusNonFinite);
+      const double p = exp2(((double)td - (double)Mt) * (double)c) / Zt;
+      const double qq = exp2(((double)ld - (double)Ml) * (double)c) / Zl;
+      accept = (double)ua * qq < p;
+    }
+    if (!accept) {
+      rej = q;
+      break;
+    }
+    ++acc_n;
+  }
+  if (rej == k) row_lse(a, b, trow(1, k, k), c, Mt, Zt);  // bonus token from target row k
+  const float uf = __shfl_sync(kFull, val, 24);
+  clear_part1(a, b);
+  if (lane == 0) {
+    VerifyDecision &dd = a.dec[b];
+    dd.acc_n = acc_n;
+    dd.rej = rej;
+    dd.kind = rej == k ? 2 : 0;
+    dd.uf = uf;
+    dd.Mt = Mt;
+    dd.iZt = (float)(1.0 / Zt);
+    dd.Ml = rej < k ? Ml : 0.f;
+    dd.iZl = rej < k ? (float)(1.0 / Zl) : 0.f;
+    a.cnt1[b] = 0u;
+    st_release(&a.flag[b], 1u);
+  }
+}
+
+// Final sampling of sequence b (warp-collective): locate the sub-chunk holding
+// the inverse-CDF crossing from the per-sub-chunk masses, rescan it in
+// float64, write the outputs.
+__device__ void sample_final(const VerifyArgs &a, int b, const VerifyDecision &dd, float c) {
+  const int k = a.k, V = a.V, lane = threadIdx.x & 31;
+  grid_dep_wait();
+  const int NS = a.p.NS;
+  unsigned long long *ms = reinterpret_cast<unsigned long long *>(a.mass2) + (size_t)b * NS;
+  const int per = (NS + 31) / 32;
+  const int s0 = min(NS, lane * per), s1 = min(NS, s0 + per);
+  double lr = 0.0, lp = 0.0;
+  int lastR = -1, lastP = -1;
+  for (int q0 = s0; q0 < s1; q0 += kBatch) {  // this lane's run, kBatch loads at a time
+    unsigned long long w[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) w[i] = q0 + i < s1 ? ld_relaxed64(ms + q0 + i) : 1ull;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      if (q0 + i >= s1) continue;
+      if (w[i] == 0ull) w[i] = poll64(ms + q0 + i, a.status);
+      const float mr = fabsf(lo_f(w[i])), mp = fabsf(hi_f(w[i]));
+      lr += (double)mr;
+      lp += (double)mp;
+      if (mr > 0.f) lastR = q0 + i;
+      if (mp > 0.f) lastP = q0 + i;
+    }
+  }
+  const double SR = warp_sum_d(lr);
+  const double SP = warp_sum_d(lp);
+  // weights: the residual; the target itself if the residual is identically
+  // zero; the unnormalised target row k for the bonus token
+  const bool use_p = dd.kind == 2 || !(SR > 0.0);
+  const double own = use_p ? lp : lr;
+  const double tgt = (double)dd.uf * (use_p ? SP : SR);
+  double incl = own;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double t = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const unsigned cross = __ballot_sync(kFull, s1 > s0 && incl > tgt);
+  int sstar = -1;
+  double before = 0.0;
+  if (cross) {
+    const int cl = __ffs(cross) - 1;
+    if (lane == cl) {
+      double cum = incl - own;
+      for (int s = s0; s < s1; ++s) {
+        const unsigned long long w = ld_relaxed64(ms + s);
+        const double m = use_p ? (double)fabsf(hi_f(w)) : (double)fabsf(lo_f(w));
+        if (cum + m > tgt) {
+          sstar = s;
+          before = cum;
+          break;
+        }
+        cum += m;
+      }
+    }
+    sstar = __shfl_sync(kFull, sstar, cl);
+    before = __shfl_sync(kFull, before, cl);
+  }
+  int slast = use_p ? lastP : lastR;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) slast = max(slast, __shfl_xor_sync(kFull, slast, o));
+  const int sb = sstar >= 0 ? sstar : slast;
+
+  const int pos = dd.kind == 2 ? k : dd.rej;
+  const float *rt = a.target + ((size_t)b * (k + 1) + pos) * V;
+  const float *rl = dd.kind == 2 ? rt : a.draft + ((size_t)b * k + pos) * V;
+  const int wk = dd.kind == 2 ? 2 : (use_p ? 1 : 0);
+  int chosen = -1;
+  if (sb >= 0) {
+    // each lane a contiguous run of 16 elements, float64 prefix sums
+    constexpr int RUN = kSub / 32;
+    const int e0 = sb * kSub, e1 = min(V, e0 + kSub);
+    const int a0 = min(e1, e0 + lane * RUN), a1 = min(e1, a0 + RUN);
+    float wv[RUN];
+#pragma unroll
+    for (int i = 0; i < RUN; ++i)
+      wv[i] = a0 + i < a1 ? weight(wk, __ldcg(rt + a0 + i), wk == 2 ? 0.f : __ldcg(rl + a0 + i), dd.Mt, dd.Ml,
+                                   dd.iZt, dd.iZl, c)
+                          : 0.f;
+    double ls = 0.0;
+    int lastpos = -1;
+#pragma unroll
+    for (int i = 0; i < RUN; ++i) {
+      ls += (double)wv[i];
+      if (wv[i] > 0.f) lastpos = a0 + i;
+    }
+    double inc = ls;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double t = __shfl_up_sync(kFull, inc, o);
+      if (lane >= o) inc += t;
+    }
+    int found = 0x7fffffff;
+    if (sstar >= 0 && before + inc > tgt) {
+      double run = before + (inc - ls);
+#pragma unroll
+      for (int i = 0; i < RUN; ++i) {
+        run += (double)wv[i];
+        if (found == 0x7fffffff && run > tgt && a0 + i < a1) found = a0 + i;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      found = min(found, __shfl_xor_sync(kFull, found, o));
+      lastpos = max(lastpos, __shfl_xor_sync(kFull, lastpos, o));
+    }
+    chosen = found != 0x7fffffff ? found : lastpos;
+  }
+  if (chosen < 0) {
+    if (lane == 0) set_status(a.status, kStatusNonFinite);
+    chosen = 0;
+  }
+  int *o = a.out_tok + (size_t)b * (k + 1);
+  if (lane <= k)
+    o[lane] = lane < dd.acc_n ? __ldcg(&a.draft_tok[(size_t)b * k + lane]) : (lane == dd.acc_n ? chosen : -1);
+  // every mass was read above, so it has landed: zero them for the next call
+  for (int s = s0; s < s1; ++s) st_relaxed64(ms + s, 0ull);
+  if (lane == 0) {
+    a.accept_len[b] = dd.acc_n + 1;
+    a.num_accepted[b] = dd.acc_n;
+    a.cnt2[b] = 0u;
+    a.flag[b] = 0u;
+  }
+}
+
+// ---------------------------------------------------------------- worker warp
+
+__device__ void worker(const VerifyArgs &a, Shared &sh, float *ring, uint64_t *bar, int w) {
+  const int lane = threadIdx.x & 31;
+  const int V = a.V;
   const bool stoch = a.mode == 1;
   const float c = kLog2e / a.T;
-  const int chunk = slice_len(V, C);
-  const int v0 = min(V, rank * chunk), v1 = min(V, v0 + chunk);
-  const Layout L = layout(V, C);
-  const int R = L.ring;
-  float *ring = reinterpret_cast<float *>(smem_raw + smem_hdr());
-  const int nsub = (chunk + kSub - 1) / kSub + 2;  // head, body sub-chunks, tail
-  float *subR = ring + (size_t)R * kPiece;
-  float *subP = subR + nsub;
+  const uint64_t pol_first = l2_policy_evict_first();
+  const uint64_t pol_keep = a.p.pol == 1 ? l2_policy_evict_normal() : l2_policy_evict_last();
 
-  const int b_first = (int)cluster_id_x(), b_step = (int)cluster_count_x();
-  const int nseq = b_first < a.B ? (a.B - 1 - b_first) / b_step + 1 : 0;
-  const int nrows = stoch ? 2 * k + 1 : k + 1;
+  uint32_t n_iss = 0, n_cons = 0, n_done = 0;  // ring pieces: issued (lane 0), consumed, confirmed
+  bool ok = true, dep_waited = false;
+  // issue cursor (lane 0): source `is` of queue position n_is, piece qi
+  Src is{};
+  uint32_t n_is = 0xffffffffu;
+  int qi = 0;
 
-  if (tid == 0) {
-    for (int s = 0; s < R; ++s) {
-      mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], kConsWarps);
-    }
-    mbar_init(&sm.stats_bar, C);
-    mbar_init(&sm.samp_bar, C);
-    mbar_init(&sm.dec_bar, 1);
-    mbar_init(&sm.sdec_bar, 1);
-    fence_barrier_init();
-  }
-  // every CTA's barriers are initialised before any remote arrival
-  cluster_sync();
-
-  // Row r of the stream order: target k, (target j, draft j) for j = k-1..1,
-  // then target 0 and draft 0 (greedy: target k .. target 0).
-  auto row_desc = [&](int b, int r, RowSlice &rs, int &isd) {
-    int pos;
-    if (!stoch) {
-      pos = k - r;
-      isd = 0;
-    } else if (r == 0) {
-      pos = k;
-      isd = 0;
-    } else if (r < 2 * k - 1) {
-      pos = k - (r + 1) / 2;
-      isd = (r & 1) == 0;
+  auto src_for = [&](const Slot &sl) {
+    Src s{};
+    int s0, s1;
+    slice_subs(a.p, sl.u, w, s0, s1);
+    const int e0 = s0 * kSub, e1 = min(V, s1 * kSub);
+    s.valid = true;
+    s.draft = sl.draft != 0;
+    if (sl.pass == 1) {
+      const int mis = (int)((reinterpret_cast<uintptr_t>(sl.p0 + e0) >> 2) & 3u);
+      const int h1 = min(e1, e0 + ((4 - mis) & 3));
+      const int b1 = h1 + max(0, e1 - h1) / 4 * 4;
+      s.p0 = sl.p0 + h1;
+      s.p1 = nullptr;
+      s.len = b1 - h1;
+      s.per = kStage;
+      s.nq = s.len > 0 ? (s.len + kStage - 1) / kStage : 0;
+      s.pol = sl.keep ? pol_keep : pol_first;
+    } else if ((V & 3) == 0) {
+      s.p0 = sl.p0 + e0;
+      s.p1 = sl.p1 ? sl.p1 + e0 : nullptr;
+      s.len = e1 - e0;
+      s.per = kSub;
+      s.nq = max(0, s1 - s0);
+      s.pol = pol_first;
     } else {
-      pos = 0;
-      isd = r == 2 * k;
+      s.nq = 0;  // unaligned rows: plain loads
     }
-    const size_t idx = isd ? (size_t)b * k + pos : (size_t)b * (k + 1) + pos;
-    rs.row = (isd ? a.draft : a.target) + idx * (size_t)V;
-    slice_bounds(idx, V, v0, v1, rs.h1, rs.b1);
+    return s;
+  };
+  // lane 0: keep up to kStages pieces in flight, moving on to the next queued
+  // item once it is ready
+  auto top_up = [&](uint32_t n) {
+    while (ok && n_iss - n_cons < (uint32_t)kStages) {
+      if (qi >= is.nq) {
+        if (n_is != n) break;  // already one item ahead
+        const uint32_t nn = n + 1;
+        if (!mbar_test(&sh.ready[nn % kQ], (nn / kQ) & 1u)) break;
+        const Slot &sl = sh.slot[nn % kQ];
+        if (sl.pass == 0) break;
+        is = src_for(sl);
+        n_is = nn;
+        qi = 0;
+        continue;
+      }
+      if (is.draft && !dep_waited) {
+        grid_dep_wait();
+        dep_waited = true;
+      }
+      const int st = (int)(n_iss % kStages);
+      const int cnt = min(is.per, is.len - qi * is.per);
+      const uint32_t bytes = (uint32_t)cnt * 4u;
+      float *dst = ring + (size_t)st * kStage;
+      mbar_arrive_expect_tx(&bar[st], is.p1 ? 2u * bytes : bytes);
+      bulk_g2s_hint(dst, is.p0 + (size_t)qi * is.per, bytes, &bar[st], is.pol);
+      if (is.p1) bulk_g2s_hint(dst + kStage / 2, is.p1 + (size_t)qi * is.per, bytes, &bar[st], is.pol);
+      ++qi;
+      ++n_iss;
+    }
+  };
+  auto wait_piece = [&]() -> const float * {
+    const int st = (int)(n_cons % kStages);
+    if (ok) ok = mbar_sleep_wait(&bar[st], (n_cons / kStages) & 1u, a.status);
+    ok = __all_sync(kFull, ok);
+    if (ok) n_done = n_cons + 1;
+    return ring + (size_t)st * kStage;
   };
 
-  bool ok = true;
-  if (warp == kProducerWarp) {
-    // ================================================================ producer
+  for (uint32_t n = 0;; ++n) {
+    const int q = (int)(n % kQ);
+    if (ok) ok = mbar_sleep_wait(&sh.ready[q], (n / kQ) & 1u, a.status);
+    ok = __all_sync(kFull, ok);
+    if (!ok) break;
+    const Slot &sl = sh.slot[q];
+    if (sl.pass == 0) break;
     if (lane == 0) {
-      const uint64_t pol_stream = l2_policy_evict_first();  // rows read once
-      const uint64_t pol_keep = l2_policy_evict_last();     // position 0: likely re-read
-      bool waited = false;
-      uint32_t n = 0;
-      for (int it = 0; it < nseq && ok; ++it) {
-        const int b = b_first + it * b_step;
-        for (int r = 0; r < nrows && ok; ++r) {
-          RowSlice rs;
-          int isd;
-          row_desc(b, r, rs, isd);
-          if (isd && !waited) {  // draft rows come from the drafter launched just before
-            grid_dep_wait();
-            waited = true;
-          }
-          const uint64_t pol = (stoch && r >= nrows - 2) ? pol_keep : pol_stream;
-          for (int off = 0; off < rs.b1 - rs.h1 && ok; off += kPiece, ++n) {
-            const int slot = (int)(n % R);
-            ok = mbar_wait(&sm.empty[slot], ((n / R) & 1u) ^ 1u, a.status);
-            if (!ok) break;
-            const int cnt = min(kPiece, rs.b1 - rs.h1 - off);
-            mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)cnt * 4u);
-            bulk_g2s_hint(ring + (size_t)slot * kPiece, rs.row + rs.h1 + off, (uint32_t)cnt * 4u, &sm.full[slot],
-                          pol);
-          }
-        }
+      if (n_is != n) {  // the cursor had not reached this item yet
+        is = src_for(sl);
+        n_is = n;
+        qi = 0;
       }
-      if (!waited) grid_dep_wait();
+      top_up(n);
     }
-    grid_dep_launch();
-  } else if (warp == kAgentWarp) {
-    // ================================================================ agent (CTA 0)
-    if (rank == 0 && lane == 0) {
-      grid_dep_wait();  // the decisions read the drafts
-      auto trow = [&](int j) { return !stoch ? k - j : (j == k ? 0 : (j == 0 ? 2 * k - 1 : 2 * (k - j) - 1)); };
-      auto drow = [&](int j) { return j == 0 ? 2 * k : 2 * (k - j); };
-      for (int it = 0; it < nseq; ++it) {
-        const int b = b_first + it * b_step;
-        const int par = it & 1;
-        // the sequence's drafts, uniforms and logits at the drafts, fetched
-        // while its rows stream in
-        int dtok[8];
-        float td[8], ld[8], ua[8], uf = 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (j < k) dtok[j] = __ldcg(&a.draft_tok[(size_t)b * k + j]);
-        if (stoch) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (j < k) {
-              const int d = dtok[j];
-              const bool valid = d >= 0 && d < V;
-              td[j] = valid ? __ldg(&a.target[((size_t)b * (k + 1) + j) * V + d]) : 0.f;
-              ld[j] = valid ? __ldcg(&a.draft[((size_t)b * k + j) * V + d]) : 0.f;
-              ua[j] = __ldg(&a.u_accept[(size_t)b * k + j]);
-            }
-          uf = __ldg(&a.u_final[b]);
-        }
-        if (ok) ok = mbar_wait_cluster(&sm.stats_bar, (uint32_t)par, a.status);
-        // combine every row's partials in rank order
-        float M[kMaxRows];
-        double Z[kMaxRows];
-        int I[kMaxRows];
-        for (int r = 0; r < nrows; ++r) {
-          M[r] = -INFINITY;
-          Z[r] = 0.0;
-          I[r] = 0x7fffffff;
-          for (int q = 0; q < C; ++q) {
-            if (stoch) M[r] = fmaxf(M[r], sm.part[par][q][r][0]);
-            else argmax_merge(M[r], I[r], sm.part[par][q][r][0], __float_as_int(sm.part[par][q][r][1]));
-          }
-          if (stoch && M[r] != -INFINITY)
-            for (int q = 0; q < C; ++q) {
-              const float pm = sm.part[par][q][r][0];
-              if (pm != -INFINITY) Z[r] += (double)sm.part[par][q][r][1] * (double)exp2f((pm - M[r]) * c);
-            }
-        }
-        int acc_n = 0, rej = k;
-        for (int j = 0; j < k; ++j) {
-          const int d = dtok[j];
-          bool accept = false;
-          if (d < 0 || d >= V) {
-            set_status(a.status, kStatusBadToken);
-          } else if (!stoch) {
-            if (!(M[trow(j)] > -INFINITY)) set_status(a.status, kStatusNonFinite);
-            accept = I[trow(j)] == d;
-          } else {
-            const int tr = trow(j), dr = drow(j);
-            if (M[tr] == -INFINITY || M[dr] == -INFINITY) set_status(a.status, kStatusNonFinite);
-            const double p = exp2(((double)td[j] - (double)M[tr]) * (double)c) / Z[tr];
-            const double q = exp2(((double)ld[j] - (double)M[dr]) * (double)c) / Z[dr];
-            accept = (double)ua[j] * q < p;
-          }
-          if (!accept) {
-            rej = j;
-            break;
-          }
-          ++acc_n;
-        }
+    int s0, s1;
+    slice_subs(a.p, sl.u, w, s0, s1);
+    const int e0 = s0 * kSub, e1 = min(V, s1 * kSub);
+
+    if (sl.pass == 1) {
+      // ------------------------------------------------------------ pass 1
+      const float *rowp = sl.p0;
+      const bool draft = sl.draft != 0;
+      const int mis = (int)((reinterpret_cast<uintptr_t>(rowp + e0) >> 2) & 3u);
+      const int h1 = min(e1, e0 + ((4 - mis) & 3));
+      const int b1 = h1 + max(0, e1 - h1) / 4 * 4;
+      const int len = b1 - h1, nq = len > 0 ? (len + kStage - 1) / kStage : 0;
+      float bv = -INFINITY, m = -INFINITY, s = 0.f;
+      int bi = 0x7fffffff;
+      for (int p = 0; p < nq; ++p) {
+        const float4 *b4 = reinterpret_cast<const float4 *>(wait_piece());
+        const int nf4 = min(kStage, len - p * kStage) / 4;
+        const int vbase = h1 + p * kStage;
         if (!stoch) {
-          // greedy: the emitted token is the argmax of the first disagreeing row
-          int *o = a.out_tok + (size_t)b * (k + 1);
-          for (int q = 0; q < acc_n; ++q) o[q] = dtok[q];
-          const int e = I[trow(acc_n)];
-          o[acc_n] = e == 0x7fffffff ? 0 : e;
-          for (int q = acc_n + 1; q <= k; ++q) o[q] = -1;
-          a.accept_len[b] = acc_n + 1;
-          a.num_accepted[b] = acc_n;
-          for (int q = 0; q < C; ++q) mbar_arrive_remote(&sm.dec_bar, q);
-          continue;
-        }
-        // stochastic: broadcast the sampling task
-        const int tr = trow(rej);
-        const int kind = rej == k ? 2 : 0;
-        const float Mt = M[tr], iZt = (float)(1.0 / Z[tr]);
-        const float Ml = rej < k ? M[drow(rej)] : 0.f;
-        const float iZl = rej < k ? (float)(1.0 / Z[drow(rej)]) : 0.f;
-        for (int q = 0; q < C; ++q) {
-          Smem *rm = dsmem_ptr_mut(&sm, q);
-          rm->acc_n = acc_n;
-          rm->rej = rej;
-          rm->kind = kind;
-          rm->Mt = Mt;
-          rm->Ml = Ml;
-          rm->iZt = iZt;
-          rm->iZl = iZl;
-        }
-        for (int q = 0; q < C; ++q) mbar_arrive_remote(&sm.dec_bar, q);
-        // gather the per-CTA sampling masses, find the CTA holding the crossing
-        if (ok) ok = mbar_wait_cluster(&sm.samp_bar, (uint32_t)par, a.status);
-        double SR = 0.0, SP = 0.0;
-        for (int q = 0; q < C; ++q) {
-          SR += sm.tot[par][q][0];
-          SP += sm.tot[par][q][1];
-        }
-        // weights: the residual; the target itself if the residual is
-        // identically zero; the unnormalised target row k for the bonus token
-        const bool use_p = kind == 2 || !(SR > 0.0);
-        const double target = (double)uf * (use_p ? SP : SR);
-        int owner = -1, last = -1;
-        double before = 0.0, cum = 0.0;
-        for (int q = 0; q < C; ++q) {
-          const double m = use_p ? sm.tot[par][q][1] : sm.tot[par][q][0];
-          if (m > 0.0) last = q;
-          if (owner < 0 && cum + m > target) {
-            owner = q;
-            before = cum;
+          // this lane's maximum over the piece (a balanced tree), then -- only
+          // when it beats the running maximum -- its lowest index
+          float4 x[kStage / 128];
+          float mi[kStage / 128];
+#pragma unroll
+          for (int i = 0; i < kStage / 128; ++i) {
+            const int f = lane + 32 * i;
+            x[i] = f < nf4 ? b4[f] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            mi[i] = fmaxf(fmaxf(x[i].x, x[i].y), fmaxf(x[i].z, x[i].w));
           }
-          cum += m;
-        }
-        const int own = owner >= 0 ? owner : (last >= 0 ? last : 0);
-        const double tg = owner >= 0 ? target - before : -1.0;  // -1: no crossing, the last positive
-        for (int q = 0; q < C; ++q) {
-          Smem *rm = dsmem_ptr_mut(&sm, q);
-          rm->owner = own;
-          rm->use_p = use_p;
-          rm->target = tg;
-        }
-        for (int q = 0; q < C; ++q) mbar_arrive_remote(&sm.sdec_bar, q);
-      }
-    }
-    grid_dep_launch();
-  } else {
-    // ================================================================ consumers
-    uint32_t n = 0;
-    const int ctid = tid;  // 0..255
-    if (stoch) grid_dep_wait();  // the sampling pass reads draft rows directly
-    for (int it = 0; it < nseq; ++it) {
-      const int b = b_first + it * b_step;
-      const int par = it & 1;
-      Smem *leader = dsmem_ptr_mut(&sm, 0);
-      for (int r = 0; r < nrows; ++r) {
-        RowSlice rs;
-        int isd;
-        row_desc(b, r, rs, isd);
-        float m = -INFINITY, s = 0.f;  // stochastic: running (max, sum)
-        float bv = -INFINITY;          // greedy: (max, lowest argmax)
-        int bi = 0x7fffffff;
-        for (int off = 0; off < rs.b1 - rs.h1; off += kPiece, ++n) {
-          const int slot = (int)(n % R);
-          if (ok) ok = mbar_wait(&sm.full[slot], (n / R) & 1u, a.status);
-          const float4 *b4 = reinterpret_cast<const float4 *>(ring + (size_t)slot * kPiece);
-          const int nf = min(kPiece, rs.b1 - rs.h1 - off) / 4;
-          const int vbase = rs.h1 + off;
+#pragma unroll
+          for (int h = kStage / 256; h > 0; h >>= 1)
+#pragma unroll
+            for (int i = 0; i < h; ++i) mi[i] = fmaxf(mi[i], mi[i + h]);
+          const float pm = mi[0];
+          if (pm > bv) {
+            int idx = 0x7fffffff;
+#pragma unroll
+            for (int i = kStage / 128 - 1; i >= 0; --i) {  // the last assignment is the lowest index
+              const int v = vbase + 4 * (lane + 32 * i);
+              if (x[i].w == pm) idx = v + 3;
+              if (x[i].z == pm) idx = v + 2;
+              if (x[i].y == pm) idx = v + 1;
+              if (x[i].x == pm) idx = v;
+            }
+            bv = pm;
+            bi = idx;
+          }
+        } else {
+          float4 x[kStage / 128];
           float pm = -INFINITY;
-          for (int f = ctid; f < nf; f += kCons) {
-            const float4 x = b4[f];
-            const float m4 = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
-            if (!stoch && m4 > bv) {
-              const int v = vbase + 4 * f;
-              bi = x.x == m4 ? v : (x.y == m4 ? v + 1 : (x.z == m4 ? v + 2 : v + 3));
-              bv = m4;
-            }
-            pm = fmaxf(pm, m4);
+#pragma unroll
+          for (int i = 0; i < kStage / 128; ++i) {
+            const int f = lane + 32 * i;
+            x[i] = f < nf4 ? b4[f] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            pm = fmaxf(pm, fmaxf(fmaxf(x[i].x, x[i].y), fmaxf(x[i].z, x[i].w)));
           }
-          if (stoch && pm != -INFINITY) {
-            const float mn = fmaxf(m, pm);
-            float acc = m == -INFINITY ? 0.f : s * exp2f((m - mn) * c);
-            for (int f = ctid; f < nf; f += kCons) {
-              const float4 x = b4[f];
-              acc += exp2f((x.x - mn) * c) + exp2f((x.y - mn) * c);
-              acc += exp2f((x.z - mn) * c) + exp2f((x.w - mn) * c);
+          if (pm > m) {
+            s = m == -INFINITY ? 0.f : s * ex2((m - pm) * c);
+            m = pm;
+          }
+          if (m != -INFINITY) {
+            const float mc = m * c;
+#pragma unroll
+            for (int i = 0; i < kStage / 128; ++i) {
+              s += ex2(fmaf(x[i].x, c, -mc)) + ex2(fmaf(x[i].y, c, -mc));
+              s += ex2(fmaf(x[i].z, c, -mc)) + ex2(fmaf(x[i].w, c, -mc));
             }
-            m = mn;
-            s = acc;
+          }
+        }
+        __syncwarp();
+        ++n_cons;
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          top_up(n);
+        }
+      }
+      if (lane < 4) {  // unaligned head / tail elements of the slice
+        for (int h = 0; h < 2; ++h) {
+          const int v = h == 0 ? e0 + lane : b1 + lane;
+          if (h == 0 ? v < h1 : v < e1) {
+            if (draft) grid_dep_wait();
+            const float x = __ldcg(rowp + v);
+            if (!stoch) {
+              argmax_merge(bv, bi, x, v);
+            } else if (x != -INFINITY) {
+              if (x > m) {
+                s = (m == -INFINITY ? 0.f : s * ex2((m - x) * c)) + 1.f;
+                m = x;
+              } else {
+                s += ex2((x - m) * c);
+              }
+            }
+          }
+        }
+      }
+      if (!stoch) warp_argmax(bv, bi);
+      else warp_lse(m, s, c);
+      if (lane == 0) sh.slot[q].part[w] = stoch ? make_float2(m, s) : make_float2(bv, __int_as_float(bi));
+    } else {
+      // ------------------------------------------------------------ pass 2
+      const int kind = sl.kind;
+      const float Mt = sl.Mt, Ml = sl.Ml, iZt = sl.iZt, iZl = sl.iZl;
+      if (sl.draft) grid_dep_wait();
+      if ((V & 3) == 0) {
+        // ring pieces of 512 target (and draft) elements, one sub-chunk each
+        for (int p = 0; p < s1 - s0; ++p) {
+          const float *buf = wait_piece();
+          const int nf4 = min(kSub, e1 - e0 - p * kSub) / 4;
+          float sr = 0.f, sp = 0.f;
+#pragma unroll
+          for (int i = 0; i < kSub / 128; ++i) {
+            const int f = lane + 32 * i;
+            if (f < nf4) {
+              const float4 t = reinterpret_cast<const float4 *>(buf)[f];
+              if (kind == 2) {
+                sp += weight(2, t.x, 0.f, Mt, Ml, iZt, iZl, c) + weight(2, t.y, 0.f, Mt, Ml, iZt, iZl, c);
+                sp += weight(2, t.z, 0.f, Mt, Ml, iZt, iZl, c) + weight(2, t.w, 0.f, Mt, Ml, iZt, iZl, c);
+              } else {
+                const float4 l = reinterpret_cast<const float4 *>(buf + kStage / 2)[f];
+                sr += weight(0, t.x, l.x, Mt, Ml, iZt, iZl, c) + weight(0, t.y, l.y, Mt, Ml, iZt, iZl, c);
+                sr += weight(0, t.z, l.z, Mt, Ml, iZt, iZl, c) + weight(0, t.w, l.w, Mt, Ml, iZt, iZl, c);
+                sp += weight(1, t.x, l.x, Mt, Ml, iZt, iZl, c) + weight(1, t.y, l.y, Mt, Ml, iZt, iZl, c);
+                sp += weight(1, t.z, l.z, Mt, Ml, iZt, iZl, c) + weight(1, t.w, l.w, Mt, Ml, iZt, iZl, c);
+              }
+            }
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.empty[slot]);  // this warp is done with the piece
-        }
-        if (ctid < 4) {  // unaligned head / tail elements of the slice
-          for (int q = 0; q < 2; ++q) {
-            const int v = q == 0 ? v0 + ctid : rs.b1 + ctid;
-            if (q == 0 ? v < rs.h1 : v < v1) {
-              if (isd) grid_dep_wait();
-              const float x = __ldcg(rs.row + v);
-              if (!stoch) {
-                argmax_merge(bv, bi, x, v);
-              } else if (x != -INFINITY) {
-                if (x > m) {
-                  s = (m == -INFINITY ? 0.f : s * exp2f((m - x) * c)) + 1.f;
-                  m = x;
-                } else {
-                  s += exp2f((x - m) * c);
-                }
-              }
-            }
-          }
-        }
-        // reduction of this row's slice over the consumer warps
-        if (!stoch) {
-          warp_argmax(bv, bi);
+          ++n_cons;
           if (lane == 0) {
-            sm.red[warp] = bv;
-            sm.red[kConsWarps + warp] = __int_as_float(bi);
+            fence_proxy_async_smem();
+            top_up(n);
           }
-        } else {
-          warp_lse(m, s, c);
-          if (lane == 0) {
-            sm.red[warp] = m;
-            sm.red[kConsWarps + warp] = s;
-          }
+          sr = warp_sum(sr);
+          sp = warp_sum(sp);
+          if (lane == 0) sh.slot[q].mass[w][p] = make_float2(sr, sp);
         }
-        named_sync(1, kCons);
-        if (ctid == 0) {
-          float M = -INFINITY, Sx = 0.f;
-          int I = 0x7fffffff;
-          for (int w = 0; w < kConsWarps; ++w) {
-            if (stoch) lse_merge(M, Sx, sm.red[w], sm.red[kConsWarps + w], c);
-            else argmax_merge(M, I, sm.red[w], __float_as_int(sm.red[kConsWarps + w]));
-          }
-          leader->part[par][rank][r][0] = M;
-          leader->part[par][rank][r][1] = stoch ? Sx : __int_as_float(I);
-        }
-        named_sync(1, kCons);
-      }
-      if (ctid == 0) mbar_arrive_remote(&sm.stats_bar, 0);
-      // the leader's decision (greedy: it only paces the partial buffers); the
-      // bounded wait starts once the drafter has finished
-      if (it == 0 && !stoch) grid_dep_wait();
-      if (ok) ok = mbar_wait_cluster(&sm.dec_bar, (uint32_t)par, a.status);
-      if (!stoch) continue;
-
-      // ---------------- sampling at the rejected position / the bonus row
-      const int kind = sm.kind, pos = sm.rej, acc_n = sm.acc_n;
-      const float Mt = sm.Mt, Ml = sm.Ml, iZt = sm.iZt, iZl = sm.iZl;
-      RowSlice rt, rl;
-      {
-        const size_t ti = (size_t)b * (k + 1) + pos;
-        rt.row = a.target + ti * (size_t)V;
-        slice_bounds(ti, V, v0, v1, rt.h1, rt.b1);
-        if (kind == 0) {
-          const size_t li = (size_t)b * k + pos;
-          rl.row = a.draft + li * (size_t)V;
-          slice_bounds(li, V, v0, v1, rl.h1, rl.b1);
-        } else {
-          rl = rt;
-        }
-      }
-      auto sub_range = [&](int sb, int &e0, int &e1) {  // 0: head, nsub-1: tail, else body
-        if (sb == 0) {
-          e0 = v0;
-          e1 = rt.h1;
-        } else if (sb == nsub - 1) {
-          e0 = rt.b1;
-          e1 = v1;
-        } else {
-          e0 = min(rt.b1, rt.h1 + (sb - 1) * kSub);
-          e1 = min(rt.b1, e0 + kSub);
-        }
-      };
-      const bool vec = kind == 2 || rt.h1 == rl.h1;
-      for (int sb = warp; sb < nsub; sb += kConsWarps) {
-        int e0, e1;
-        sub_range(sb, e0, e1);
-        float sr = 0.f, sp = 0.f;
-        if (sb > 0 && sb < nsub - 1 && vec && e1 - e0 == kSub) {
-          float4 tv[kSub / 128], lv[kSub / 128];
-#pragma unroll
-          for (int i = 0; i < kSub / 128; ++i) {
-            tv[i] = __ldcg(reinterpret_cast<const float4 *>(rt.row + e0) + lane + 32 * i);
-            if (kind == 0) lv[i] = __ldcg(reinterpret_cast<const float4 *>(rl.row + e0) + lane + 32 * i);
-          }
-#pragma unroll
-          for (int i = 0; i < kSub / 128; ++i) {
-            const float t4[4] = {tv[i].x, tv[i].y, tv[i].z, tv[i].w};
-            if (kind == 2) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) sp += weight(2, t4[q], 0.f, Mt, Ml, iZt, iZl, c);
-            } else {
-              const float l4[4] = {lv[i].x, lv[i].y, lv[i].z, lv[i].w};
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                sr += weight(0, t4[q], l4[q], Mt, Ml, iZt, iZl, c);
-                sp += weight(1, t4[q], l4[q], Mt, Ml, iZt, iZl, c);
-              }
-            }
-          }
-        } else {
-          for (int v = e0 + lane; v < e1; v += 32) {
-            const float t = __ldcg(rt.row + v);
+      } else {
+        // unaligned rows: plain loads, one sub-chunk at a time
+        for (int p = 0; p < s1 - s0; ++p) {
+          const int v0 = e0 + p * kSub, v1 = min(e1, v0 + kSub);
+          float sr = 0.f, sp = 0.f;
+          for (int v = v0 + lane; v < v1; v += 32) {
+            const float t = __ldcg(sl.p0 + v);
             if (kind == 2) {
               sp += weight(2, t, 0.f, Mt, Ml, iZt, iZl, c);
             } else {
-              const float l = __ldcg(rl.row + v);
+              const float l = __ldcg(sl.p1 + v);
               sr += weight(0, t, l, Mt, Ml, iZt, iZl, c);
               sp += weight(1, t, l, Mt, Ml, iZt, iZl, c);
             }
           }
-        }
-        sr = warp_sum(sr);
-        sp = warp_sum(sp);
-        if (lane == 0) {
-          subR[sb] = sr;
-          subP[sb] = sp;
+          sr = warp_sum(sr);
+          sp = warp_sum(sp);
+          if (lane == 0) sh.slot[q].mass[w][p] = make_float2(sr, sp);
         }
       }
-      named_sync(1, kCons);
-      if (ctid == 0) {
-        double tR = 0.0, tP = 0.0;
-        for (int sb = 0; sb < nsub; ++sb) {
-          tR += (double)subR[sb];
-          tP += (double)subP[sb];
-        }
-        leader->tot[par][rank][0] = tR;
-        leader->tot[par][rank][1] = tP;
-        mbar_arrive_remote(&sm.samp_bar, 0);
-      }
-      if (ok) ok = mbar_wait_cluster(&sm.sdec_bar, (uint32_t)par, a.status);
-      if (rank == sm.owner && warp == 0) {
-        const bool use_p = sm.use_p;
-        const double tgt = sm.target;
-        const float *wsub = use_p ? subP : subR;
-        const int wk = kind == 2 ? 2 : (use_p ? 1 : 0);
-        auto elem = [&](int v) -> float {
-          return weight(wk, __ldcg(rt.row + v), wk == 2 ? 0.f : __ldcg(rl.row + v), Mt, Ml, iZt, iZl, c);
-        };
-        int sstar = -1, slast = -1;
-        double before = 0.0;
-        if (lane == 0) {
-          double cum = 0.0;
-          for (int sb = 0; sb < nsub; ++sb) {
-            const double m = (double)wsub[sb];
-            if (m > 0.0) slast = sb;
-            if (tgt >= 0.0 && sstar < 0 && cum + m > tgt) {
-              sstar = sb;
-              before = cum;
-            }
-            cum += m;
-          }
-        }
-        sstar = __shfl_sync(0xffffffffu, sstar, 0);
-        slast = __shfl_sync(0xffffffffu, slast, 0);
-        before = __shfl_sync(0xffffffffu, before, 0);
-        const int sb = sstar >= 0 ? sstar : slast;
-        int chosen = -1;
-        if (sb >= 0) {
-          int e0, e1;
-          sub_range(sb, e0, e1);
-          // each lane a contiguous run of 16 elements (loaded first), float64 prefix sums
-          constexpr int RUN = kSub / 32;
-          const int a0 = min(e1, e0 + lane * RUN), a1 = min(e1, a0 + RUN);
-          float wv[RUN];
-#pragma unroll
-          for (int i = 0; i < RUN; ++i) wv[i] = a0 + i < a1 ? elem(a0 + i) : 0.f;
-          double ls = 0.0;
-          int lastpos = -1;
-#pragma unroll
-          for (int i = 0; i < RUN; ++i) {
-            ls += (double)wv[i];
-            if (wv[i] > 0.f) lastpos = a0 + i;
-          }
-          double incl = ls;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const double t = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += t;
-          }
-          int found = 0x7fffffff;
-          if (sstar >= 0 && before + incl > tgt) {
-            double run = before + (incl - ls);
-#pragma unroll
-            for (int i = 0; i < RUN; ++i) {
-              run += (double)wv[i];
-              if (found == 0x7fffffff && run > tgt && a0 + i < a1) found = a0 + i;
-            }
-          }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            found = min(found, __shfl_xor_sync(0xffffffffu, found, o));
-            lastpos = max(lastpos, __shfl_xor_sync(0xffffffffu, lastpos, o));
-          }
-          chosen = found != 0x7fffffff ? found : lastpos;
-        }
-        if (lane == 0) {
-          if (chosen < 0) {
-            set_status(a.status, kStatusNonFinite);
-            chosen = 0;
-          }
-          int *o = a.out_tok + (size_t)b * (k + 1);
-          for (int q = 0; q < acc_n; ++q) o[q] = __ldcg(&a.draft_tok[(size_t)b * k + q]);
-          o[acc_n] = chosen;
-          for (int q = acc_n + 1; q <= k; ++q) o[q] = -1;
-          a.accept_len[b] = acc_n + 1;
-          a.num_accepted[b] = acc_n;
-        }
-      }
-      named_sync(1, kCons);  // the sub-chunk masses may be overwritten by the next sequence
     }
-    grid_dep_wait();
-    grid_dep_launch();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.done[q]);
   }
-  // no CTA may leave while another can still read or arrive on its shared memory
-  cluster_sync();
+
+  if (lane == 0) {
+    // after a timeout, let copies still in flight land before the CTA exits
+    for (uint32_t n = n_done; n < n_iss; ++n)
+      if (!mbar_wait(&bar[n % kStages], (n / kStages) & 1u, a.status)) break;
+  }
 }
 
-// Clusters: at most 64 sequences in flight (their position-0 rows then fit in
-// L2), about 256 CTAs in all, at least 4 CTAs per sequence.
-static int verify_clusters(int B) { return B < 64 ? B : 64; }
+// ---------------------------------------------------------------- coordinator warp
 
-int verify_cluster_size(int B, int num_sms, int max_cluster) {
-  (void)num_sms;
-  const int n = verify_clusters(B);
-  int C = 4;
-  while (C < max_cluster && C * 2 * n <= 256) C *= 2;
-  return C;
+__device__ void coordinator(const VerifyArgs &a, Shared &sh) {
+  const int lane = threadIdx.x & 31;
+  const int k = a.k, V = a.V, U = a.p.U;
+  const bool stoch = a.mode == 1;
+  const float c = kLog2e / a.T;
+
+  // pass-1 claims run one ahead: the next index is requested when one is consumed
+  unsigned pre = 0;
+  bool have_pre = false, claims_done = false;
+  auto claim = [&]() -> unsigned {
+    unsigned i = 0;
+    if (lane == 0) i = have_pre ? pre : atomicAdd(&a.ctl[0], 1u);
+    i = __shfl_sync(kFull, i, 0);
+    have_pre = i < a.p.total;
+    if (lane == 0 && have_pre) pre = atomicAdd(&a.ctl[0], 1u);
+    return i;
+  };
+
+  // pass-2 items owned by this CTA: g = blockIdx.x + t * gridDim.x < B * U.
+  // Their readiness is probed without waiting: the flag is loaded, looked at
+  // on a later iteration, then the decision is loaded and looked at later still.
+  const unsigned n2 = stoch ? (unsigned)a.B * (unsigned)U : 0u;
+  const unsigned own = blockIdx.x < n2 ? (n2 - blockIdx.x + gridDim.x - 1) / gridDim.x : 0u;
+  unsigned t2 = 0;
+  int p2 = 0;  // 0: to probe, 1: flag load in flight, 2: decision load in flight
+  unsigned fl = 0;
+  long long p2_at = 0;  // when the in-flight load may be looked at / the next probe may go
+  int d_kind = 0, d_rej = 0;
+  float d_Mt = 0.f, d_Ml = 0.f, d_iZt = 0.f, d_iZl = 0.f;
+  auto owned_b = [&]() { return (int)((blockIdx.x + t2 * gridDim.x) / (unsigned)U); };
+  auto owned_u = [&]() { return (int)((blockIdx.x + t2 * gridDim.x) % (unsigned)U); };
+  // Loads are only looked at a round trip after they were issued, so a probe
+  // never stalls the coordinator.
+  constexpr long long kRoundTrip = 3000, kReprobe = 6000;  // SM clocks
+  auto probe = [&]() {  // advance the readiness pipeline of the next owned item
+    if (t2 >= own) return;
+    const long long now = clock64();
+    if (now < p2_at || p2 == 2) return;
+    if (p2 == 0) {
+      if (lane == 0) fl = ld_acquire(&a.flag[owned_b()]);
+      p2 = 1;
+      p2_at = now + kRoundTrip;
+    } else if (__shfl_sync(kFull, fl, 0) != 0u) {
+      if (lane == 0) {
+        const VerifyDecision *g = &a.dec[owned_b()];
+        d_kind = __ldcg(&g->kind);
+        d_rej = __ldcg(&g->rej);
+        d_Mt = __ldcg(&g->Mt);
+        d_Ml = __ldcg(&g->Ml);
+        d_iZt = __ldcg(&g->iZt);
+        d_iZl = __ldcg(&g->iZl);
+      }
+      p2 = 2;
+      p2_at = now + kRoundTrip;
+    } else {
+      p2 = 0;
+      p2_at = now + kReprobe;
+    }
+  };
+
+  // hand a published item to the decider warp (lane 0; waits for ring space)
+  auto push = [&](int b, int pass) {
+    if (lane == 0) {
+      volatile unsigned *vh = &sh.dq_head;
+      if (sh.dq_tail - *vh >= (unsigned)kDQ) {
+        const uint64_t t0 = global_timer_ns();
+        while (sh.dq_tail - *vh >= (unsigned)kDQ) {
+          if (global_timer_ns() - t0 > kWaitLimitNs) {
+            set_status(a.status, kStatusTimeout);
+            break;
+          }
+          __nanosleep(64);
+        }
+      }
+      const unsigned t = sh.dq_tail;
+      sh.dq_b[t % kDQ] = b;
+      sh.dq_pass[t % kDQ] = pass;
+      __threadfence_block();
+      *(volatile unsigned *)&sh.dq_tail = t + 1;
+    }
+  };
+
+  auto enqueue = [&](uint32_t n, const Item &it) {
+    if (lane == 0) {
+      Slot &sl = sh.slot[n % kQ];
+      sl.pass = it.pass;
+      sl.b = it.b;
+      sl.r = it.r;
+      sl.u = it.u;
+      if (it.pass == 1) {
+        bool draft;
+        const size_t row = stream_row(a, it.b, it.r, draft);
+        sl.p0 = (draft ? a.draft : a.target) + row * (size_t)V;
+        sl.p1 = nullptr;
+        sl.draft = draft;
+        sl.keep = stoch && (a.p.pol != 0 || it.r >= 2 * k - 1);  // rows a rejection may read again
+      } else if (it.pass == 2) {
+        const int pos = d_kind == 2 ? k : d_rej;
+        sl.p0 = a.target + ((size_t)it.b * (k + 1) + pos) * V;
+        sl.p1 = d_kind == 2 ? nullptr : a.draft + ((size_t)it.b * k + pos) * V;
+        sl.draft = d_kind != 2;
+        sl.keep = 0;
+        sl.kind = d_kind;
+        sl.Mt = d_Mt;
+        sl.Ml = d_Ml;
+        sl.iZt = d_iZt;
+        sl.iZl = d_iZl;
+      }
+      mbar_arrive(&sh.ready[n % kQ]);
+    }
+    __syncwarp();
+  };
+
+  // a finished item: publish its partial or masses, pass it to the decider
+  auto complete = [&](uint32_t n) {
+    const Slot &sl = sh.slot[n % kQ];
+    const int b = sl.b;
+    if (sl.pass == 1) {
+      float m = -INFINITY, s = 0.f;
+      int i = 0x7fffffff;
+      if (lane < kWorkers) {
+        const float2 p = sl.part[lane];
+        m = p.x;
+        if (stoch) s = p.y;
+        else i = __float_as_int(p.y);
+      }
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) {  // the 8 slices, a fixed merge tree
+        const float m2 = __shfl_xor_sync(kFull, m, o), s2 = __shfl_xor_sync(kFull, s, o);
+        const int i2 = __shfl_xor_sync(kFull, i, o);
+        if (stoch) lse_merge(m, s, m2, s2, c);
+        else argmax_merge(m, i, m2, i2);
+      }
+      if (lane == 0) {
+        void *dst = a.part1 + ((size_t)b * a.p.nrows + sl.r) * U + sl.u;
+        st_relaxed64(dst, stoch ? pack(m, s) : enc_greedy(m, i));
+      }
+      push(b, 1);
+    } else {
+      unsigned long long *ms = reinterpret_cast<unsigned long long *>(a.mass2) + (size_t)b * a.p.NS;
+      const int base = sl.u * kWorkers * a.p.m;
+      for (int e = lane; e < kWorkers * a.p.m; e += 32) {
+        const int s = base + e;
+        if (s < a.p.NS) {
+          const float2 v = sl.mass[e / a.p.m][e % a.p.m];
+          st_relaxed64(ms + s, enc_mass(v.x, v.y));
+        }
+      }
+      __syncwarp();
+      push(b, 2);
+    }
+    __syncwarp();
+  };
+
+  uint32_t fill = 0, drain = 0;
+  uint64_t idle_since = 0;
+  for (;;) {
+    bool did = false;
+    if (drain < fill) {
+      bool fin = false;
+      if (lane == 0) {
+        if (fill - drain == (uint32_t)kQ)  // nothing else to do: park until it is done
+          fin = mbar_sleep_wait(&sh.done[drain % kQ], (drain / kQ) & 1u, a.status);
+        else
+          fin = mbar_test(&sh.done[drain % kQ], (drain / kQ) & 1u);
+      }
+      if (__shfl_sync(kFull, fin, 0)) {
+        complete(drain);
+        ++drain;
+        did = true;
+      }
+    }
+    probe();
+    if (fill - drain < (uint32_t)kQ) {
+      if (p2 == 2 && clock64() >= p2_at) {  // an owned pass-2 item whose sequence is decided goes first
+        enqueue(fill, Item{2, owned_b(), 0, owned_u()});
+        ++fill;
+        ++t2;
+        p2 = 0;
+        p2_at = 0;
+        did = true;
+      } else if (!claims_done) {
+        const Item it = decode(a, claim());
+        if (it.pass) {
+          enqueue(fill, it);
+          ++fill;
+        } else {
+          claims_done = true;
+        }
+        did = true;
+      }
+    }
+    if (claims_done && t2 >= own && drain == fill) {
+      enqueue(fill, Item{0, 0, 0, 0});  // stop: the workers leave
+      break;
+    }
+    if (did) {
+      idle_since = 0;
+    } else {
+      const uint64_t now = global_timer_ns();
+      if (idle_since == 0) idle_since = now;
+      if (now - idle_since > kWaitLimitNs) {  // nothing moved for too long
+        if (lane == 0) set_status(a.status, kStatusTimeout);
+        if (drain == fill) enqueue(fill, Item{0, 0, 0, 0});
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  if (lane == 0) *(volatile int *)&sh.coord_done = 1;
 }
 
-cudaError_t verify_set_attributes(int max_cluster) {
-  cudaError_t e = cudaFuncSetAttribute(verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 112 * 1024);
-  if (e != cudaSuccess) return e;
-  if (max_cluster > 8) {
-    e = cudaFuncSetAttribute(verify_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
+// ---------------------------------------------------------------- decider warp
+
+// Takes the tickets of the items the coordinator published -- one atomic per
+// lane, up to 32 in flight together -- and, for a sequence's last pass-1
+// ticket, decides it; for its last pass-2 ticket, samples it.
+__device__ void decider(const VerifyArgs &a, Shared &sh) {
+  const int lane = threadIdx.x & 31;
+  const bool stoch = a.mode == 1;
+  const float c = kLog2e / a.T;
+  unsigned head = 0;
+  for (;;) {
+    unsigned tail = 0;
+    int cdone = 0;
+    if (lane == 0) {
+      cdone = *(volatile int *)&sh.coord_done;
+      __threadfence_block();
+      tail = *(volatile unsigned *)&sh.dq_tail;
+    }
+    tail = __shfl_sync(kFull, tail, 0);
+    cdone = __shfl_sync(kFull, cdone, 0);
+    if (tail == head) {
+      if (cdone) break;
+      __nanosleep(128);
+      continue;
+    }
+    const unsigned n = min(tail - head, 32u);
+    int b = 0, pass = 0;
+    unsigned old = 0;
+    if ((unsigned)lane < n) {
+      b = *(volatile int *)&sh.dq_b[(head + lane) % kDQ];
+      pass = *(volatile int *)&sh.dq_pass[(head + lane) % kDQ];
+      old = atomicAdd(pass == 1 ? &a.cnt1[b] : &a.cnt2[b], 1u);
+    }
+    head += n;
+    __syncwarp();
+    if (lane == 0) *(volatile unsigned *)&sh.dq_head = head;
+    const bool last = (unsigned)lane < n && old == (pass == 1 ? (unsigned)a.p.n1 - 1u : (unsigned)a.p.U - 1u);
+    unsigned mask = __ballot_sync(kFull, last);
+    while (mask) {
+      const int j = __ffs(mask) - 1;
+      mask &= mask - 1;
+      const int bj = __shfl_sync(kFull, b, j), pj = __shfl_sync(kFull, pass, j);
+      if (pj == 1) {
+        if (stoch) decide_stochastic(a, bj, c);
+        else decide_greedy(a, bj);
+      } else {
+        VerifyDecision dd;
+        const VerifyDecision *g = &a.dec[bj];
+        dd.acc_n = __ldcg(&g->acc_n);
+        dd.rej = __ldcg(&g->rej);
+        dd.kind = __ldcg(&g->kind);
+        dd.uf = __ldcg(&g->uf);
+        dd.Mt = __ldcg(&g->Mt);
+        dd.Ml = __ldcg(&g->Ml);
+        dd.iZt = __ldcg(&g->iZt);
+        dd.iZl = __ldcg(&g->iZl);
+        sample_final(a, bj, dd, c);
+      }
+    }
   }
-  return cudaSuccess;
+  // the last CTA out resets the claim counter for the next call
+  if (lane == 0 && atomicAdd(&a.ctl[1], 1u) == gridDim.x - 1u) {
+    a.ctl[0] = 0u;
+    a.ctl[1] = 0u;
+  }
 }
 
-int verify_max_active_clusters(int cluster) {
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(cluster);
-  cfg.blockDim = dim3(kVerifyThreads);
-  cfg.dynamicSmemBytes = verify_smem_bytes(1, 8, 151936, cluster);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, verify_kernel, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
+}  // namespace
+
+constexpr int kMinBlocks = kStage > 1024 ? 1 : 2;  // CTAs per SM the rings allow
+
+__global__ void __launch_bounds__(kVerifyThreads, kMinBlocks) verify_kernel(VerifyArgs a) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  Shared &sh = *reinterpret_cast<Shared *>(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    sh.dq_tail = 0u;
+    sh.dq_head = 0u;
+    sh.coord_done = 0;
+    for (int q = 0; q < kQ; ++q) {
+      mbar_init(&sh.ready[q], 1);
+      mbar_init(&sh.done[q], kWorkers);
+    }
+    for (int w = 0; w < kWorkers; ++w)
+      for (int s = 0; s < kStages; ++s) mbar_init(&sh.ring_bar[w][s], 1);
+    fence_barrier_init();
   }
+  __syncthreads();
+  grid_dep_launch();
+  (void)lane;
+  if (warp < kWorkers) {
+    float *ring = reinterpret_cast<float *>(smem_raw + kHdr) + (size_t)warp * kStages * kStage;
+    worker(a, sh, ring, sh.ring_bar[warp], warp);
+  } else if (warp == kWorkers) {
+    coordinator(a, sh);
+  } else {
+    decider(a, sh);
+  }
+  grid_dep_wait();
+}
+
+// ---------------------------------------------------------------- host side
+
+namespace {
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+int sub_chunks(int V) { return (V + kSub - 1) / kSub; }
+int max_chunks(int V) { return (sub_chunks(V) + kWorkers - 1) / kWorkers; }  // slices of one sub-chunk
+long long env_int(const char *name, long long dflt) {
+  const char *v = getenv(name);
+  return v && *v ? atoll(v) : dflt;
+}
+}  // namespace
+
+size_t verify_state_bytes(int B, int k, int V) {
+  size_t n = 256;                                           // claim / exit counters
+  n += 3 * up256((size_t)B * 4);                            // tickets and flags
+  n += up256((size_t)B * sizeof(VerifyDecision));           // decisions
+  n += up256((size_t)B * (2 * k + 1) * max_chunks(V) * 8);  // published partials
+  n += up256((size_t)B * sub_chunks(V) * 8);                // published masses
   return n;
 }
 
-cudaError_t launch_verify(const VerifyArgs &a, int cluster, cudaStream_t s, bool pdl) {
-  const int nclusters = verify_clusters(a.B);  // persistent: each loops over B / 64 sequences
+void verify_bind_state(VerifyArgs &a, void *state) {
+  char *p = static_cast<char *>(state);
+  const int B = a.B, k = a.k, V = a.V;
+  a.ctl = reinterpret_cast<unsigned *>(p);
+  p += 256;
+  a.cnt1 = reinterpret_cast<unsigned *>(p);
+  p += up256((size_t)B * 4);
+  a.cnt2 = reinterpret_cast<unsigned *>(p);
+  p += up256((size_t)B * 4);
+  a.flag = reinterpret_cast<unsigned *>(p);
+  p += up256((size_t)B * 4);
+  a.dec = reinterpret_cast<VerifyDecision *>(p);
+  p += up256((size_t)B * sizeof(VerifyDecision));
+  a.part1 = reinterpret_cast<float2 *>(p);
+  p += up256((size_t)B * (2 * k + 1) * max_chunks(V) * 8);
+  a.mass2 = reinterpret_cast<float2 *>(p);
+}
+
+bool plan_verify(int B, int k, int V, int mode, int num_sms, int blocks_per_sm, VerifyPlan *p) {
+  VerifyPlan q{};
+  const bool stoch = mode == 1;
+  q.nrows = stoch ? 2 * k + 1 : k + 1;
+  q.NS = sub_chunks(V);
+  const long long ctas = (long long)num_sms * blocks_per_sm;
+  // the widest slice (8 sub-chunks, down to 1) that
+  // still gives every CTA about four items
+  int m = (int)env_int(stoch ? "MTP_VERIFY_SM" : "MTP_VERIFY_GM", 8);
+  m = std::max(1, std::min(kMaxM, m));
+  for (;;) {
+    q.U = (q.NS + kWorkers * m - 1) / (kWorkers * m);
+    if (m <= 1 || (long long)B * q.nrows * q.U >= 4 * ctas) break;
+    m /= 2;
+  }
+  q.m = m;
+  q.n1 = q.nrows * q.U;
+  q.pol = (int)env_int("MTP_VERIFY_POL", 0);
+  const long long total = (long long)B * q.n1;
+  if (total >= (1ll << 31)) return false;
+  q.total = (unsigned)total;
+  q.grid = (int)std::max<long long>(1, std::min<long long>(ctas, total));
+  *p = q;
+  return true;
+}
+
+cudaError_t verify_set_attributes() {
+  return cudaFuncSetAttribute(verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+}
+
+int verify_blocks_per_sm() {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, verify_kernel, kVerifyThreads, kSmemBytes) != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
+  return n < 1 ? 1 : n;
+}
+
+cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(nclusters * cluster);
+  cfg.gridDim = dim3(a.p.grid);
   cfg.blockDim = dim3(kVerifyThreads);
-  cfg.dynamicSmemBytes = layout(a.V, cluster).bytes;
+  cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 2 : 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   note_launch();
   return cudaLaunchKernelEx(&cfg, verify_kernel, a);
 }
