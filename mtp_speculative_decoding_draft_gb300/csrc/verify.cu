@@ -47,6 +47,7 @@ namespace {
 
 constexpr int kWorkers = 8;      // worker warps; then the coordinator and the decider warp
 constexpr int kDQ = 64;          // published items waiting for their tickets
+constexpr int kScr = 1024;       // decider scratch: published words gathered at once
 constexpr int kStages = 3;       // ring stages per worker
 #ifndef MTP_VERIFY_STAGE
 #define MTP_VERIFY_STAGE 1024
@@ -79,6 +80,7 @@ struct Shared {
   int dq_b[kDQ], dq_pass[kDQ];
   unsigned dq_tail, dq_head;
   int coord_done;
+  unsigned long long scr[kScr];  // decider: a sequence's partials or masses
 };
 
 constexpr size_t kHdr = (sizeof(Shared) + 127) / 128 * 128;
@@ -335,17 +337,69 @@ __device__ void clear_part1(const VerifyArgs &a, int b) {
   }
 }
 
+// Gather n <= kScr published words into scratch: all loads of a round (16
+// per lane) are issued before any is looked at, then late ones are polled.
+__device__ void gather(const unsigned long long *src, int n, unsigned long long *scr, int *status) {
+  const int lane = threadIdx.x & 31;
+  for (int i0 = 0; i0 < n; i0 += 512) {
+    unsigned long long w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int e = i0 + lane + 32 * i;
+      w[i] = e < n ? ld_relaxed64(src + e) : 1ull;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int e = i0 + lane + 32 * i;
+      if (e < n) scr[e] = w[i] ? w[i] : poll64(src + e, status);
+    }
+  }
+  __syncwarp();
+}
+
+// Row statistics from gathered partials (entries r*U .. r*U+U-1).
+__device__ void scr_row_lse(const unsigned long long *scr, int U, int r, float c, float &M, double &Z) {
+  const int lane = threadIdx.x & 31;
+  float m = -INFINITY;
+  for (int u = lane; u < U; u += 32) m = fmaxf(m, lo_f(scr[r * U + u]));
+  M = warp_max(m);
+  double z = 0.0;
+  if (M != -INFINITY)
+    for (int u = lane; u < U; u += 32) {
+      const unsigned long long w = scr[r * U + u];
+      if (lo_f(w) != -INFINITY) z += (double)hi_f(w) * (double)ex2((lo_f(w) - M) * c);
+    }
+  Z = warp_sum_d(z);
+}
+
+__device__ void scr_row_argmax(const unsigned long long *scr, int U, int r, float &M, int &I) {
+  const int lane = threadIdx.x & 31;
+  M = -INFINITY;
+  I = 0x7fffffff;
+  for (int u = lane; u < U; u += 32) argmax_merge(M, I, lo_f(scr[r * U + u]), dec_greedy_idx(scr[r * U + u]));
+  warp_argmax(M, I);
+}
+
+// Zero n gathered (so landed) published words for the next call.
+__device__ void zero_words(unsigned long long *dst, int n) {
+  for (int i = threadIdx.x & 31; i < n; i += 32) st_relaxed64(dst + i, 0ull);
+}
+
 // Greedy decision of sequence b (warp-collective): accept drafts while they
 // equal the target argmax, then emit the argmax of the first disagreeing row.
-__device__ void decide_greedy(const VerifyArgs &a, int b) {
-  const int k = a.k, V = a.V, lane = threadIdx.x & 31;
+__device__ void decide_greedy(const VerifyArgs &a, int b, unsigned long long *scr) {
+  const int k = a.k, V = a.V, lane = threadIdx.x & 31, U = a.p.U, n = a.p.nrows * U;
   grid_dep_wait();  // the drafts come from the drafter
   const int my = lane < k ? __ldcg(&a.draft_tok[(size_t)b * k + lane]) : 0;
+  unsigned long long *src = reinterpret_cast<unsigned long long *>(a.part1) + (size_t)b * n;
+  const bool gathered = n <= kScr;
+  if (gathered) gather(src, n, scr, a.status);
   int acc_n = 0;
   float M;
   int I;
   for (;;) {
-    row_argmax(a, b, trow(0, k, acc_n), M, I);
+    if (gathered) scr_row_argmax(scr, U, trow(0, k, acc_n), M, I);
+    else row_argmax(a, b, trow(0, k, acc_n), M, I);
     if (acc_n == k) break;
     const int d = __shfl_sync(kFull, my, acc_n);
     if (d < 0 || d >= V) {
@@ -363,13 +417,14 @@ __device__ void decide_greedy(const VerifyArgs &a, int b) {
     a.num_accepted[b] = acc_n;
     a.cnt1[b] = 0u;
   }
-  clear_part1(a, b);
+  if (gathered) zero_words(src, n);
+  else clear_part1(a, b);
 }
 
 // Stochastic decision of sequence b (warp-collective): the ratio tests in
 // position order; publishes the sampling task for the pass-2 items.
-__device__ void decide_stochastic(const VerifyArgs &a, int b, float c) {
-  const int k = a.k, V = a.V, lane = threadIdx.x & 31;
+__device__ void decide_stochastic(const VerifyArgs &a, int b, float c, unsigned long long *scr) {
+  const int k = a.k, V = a.V, lane = threadIdx.x & 31, U = a.p.U, n = a.p.nrows * U;
   grid_dep_wait();
   // lanes 0-7: target logit at drafted token j; 8-15: draft logit at it;
   // 16-23: u_accept; lane 24: u_final
@@ -381,6 +436,13 @@ __device__ void decide_stochastic(const VerifyArgs &a, int b, float c) {
   if (g == 1 && j < k && valid) val = __ldcg(&a.draft[((size_t)b * k + j) * V + dj]);
   if (g == 2 && j < k) val = __ldg(&a.u_accept[(size_t)b * k + j]);
   if (lane == 24) val = __ldg(&a.u_final[b]);
+  unsigned long long *src = reinterpret_cast<unsigned long long *>(a.part1) + (size_t)b * n;
+  const bool gathered = n <= kScr;
+  if (gathered) gather(src, n, scr, a.status);
+  auto stats = [&](int r, float &M, double &Z) {
+    if (gathered) scr_row_lse(scr, U, r, c, M, Z);
+    else row_lse(a, b, r, c, M, Z);
+  };
   int acc_n = 0, rej = k;
   float Mt = 0.f, Ml = 0.f;
   double Zt = 1.0, Zl = 1.0;
@@ -389,8 +451,8 @@ __device__ void decide_stochastic(const VerifyArgs &a, int b, float c) {
     const float td = __shfl_sync(kFull, val, q), ld = __shfl_sync(kFull, val, 8 + q);
     const float ua = __shfl_sync(kFull, val, 16 + q);
     bool accept = false;
-    row_lse(a, b, trow(1, k, q), c, Mt, Zt);
-    row_lse(a, b, drow(k, q), c, Ml, Zl);
+    stats(trow(1, k, q), Mt, Zt);
+    stats(drow(k, q), Ml, Zl);
     if (d < 0 || d >= V) {
       if (lane == 0) set_status(a.status, kStatusBadToken);
     } else {
@@ -405,9 +467,10 @@ __device__ void decide_stochastic(const VerifyArgs &a, int b, float c) {
     }
     ++acc_n;
   }
-  if (rej == k) row_lse(a, b, trow(1, k, k), c, Mt, Zt);  // bonus token from target row k
+  if (rej == k) stats(trow(1, k, k), Mt, Zt);  // bonus token from target row k
   const float uf = __shfl_sync(kFull, val, 24);
-  clear_part1(a, b);
+  if (gathered) zero_words(src, n);
+  else clear_part1(a, b);
   if (lane == 0) {
     VerifyDecision &dd = a.dec[b];
     dd.acc_n = acc_n;
@@ -426,29 +489,27 @@ __device__ void decide_stochastic(const VerifyArgs &a, int b, float c) {
 // Final sampling of sequence b (warp-collective): locate the sub-chunk holding
 // the inverse-CDF crossing from the per-sub-chunk masses, rescan it in
 // float64, write the outputs.
-__device__ void sample_final(const VerifyArgs &a, int b, const VerifyDecision &dd, float c) {
+__device__ void sample_final(const VerifyArgs &a, int b, const VerifyDecision &dd, float c,
+                             unsigned long long *scr) {
   const int k = a.k, V = a.V, lane = threadIdx.x & 31;
   grid_dep_wait();
+  const int my = lane < dd.acc_n ? __ldcg(&a.draft_tok[(size_t)b * k + lane]) : 0;
   const int NS = a.p.NS;
-  unsigned long long *ms = reinterpret_cast<unsigned long long *>(a.mass2) + (size_t)b * NS;
+  unsigned long long *msg = reinterpret_cast<unsigned long long *>(a.mass2) + (size_t)b * NS;
+  const bool gathered = NS <= kScr;
+  if (gathered) gather(msg, NS, scr, a.status);
+  const unsigned long long *ms = gathered ? scr : msg;
   const int per = (NS + 31) / 32;
   const int s0 = min(NS, lane * per), s1 = min(NS, s0 + per);
   double lr = 0.0, lp = 0.0;
   int lastR = -1, lastP = -1;
-  for (int q0 = s0; q0 < s1; q0 += kBatch) {  // this lane's run, kBatch loads at a time
-    unsigned long long w[kBatch];
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) w[i] = q0 + i < s1 ? ld_relaxed64(ms + q0 + i) : 1ull;
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      if (q0 + i >= s1) continue;
-      if (w[i] == 0ull) w[i] = poll64(ms + q0 + i, a.status);
-      const float mr = fabsf(lo_f(w[i])), mp = fabsf(hi_f(w[i]));
-      lr += (double)mr;
-      lp += (double)mp;
-      if (mr > 0.f) lastR = q0 + i;
-      if (mp > 0.f) lastP = q0 + i;
-    }
+  for (int s = s0; s < s1; ++s) {
+    const unsigned long long w = gathered ? ms[s] : poll64(msg + s, a.status);
+    const float mr = fabsf(lo_f(w)), mp = fabsf(hi_f(w));
+    lr += (double)mr;
+    lp += (double)mp;
+    if (mr > 0.f) lastR = s;
+    if (mp > 0.f) lastP = s;
   }
   const double SR = warp_sum_d(lr);
   const double SP = warp_sum_d(lp);
@@ -471,7 +532,7 @@ __device__ void sample_final(const VerifyArgs &a, int b, const VerifyDecision &d
     if (lane == cl) {
       double cum = incl - own;
       for (int s = s0; s < s1; ++s) {
-        const unsigned long long w = ld_relaxed64(ms + s);
+        const unsigned long long w = gathered ? ms[s] : ld_relaxed64(msg + s);
         const double m = use_p ? (double)fabsf(hi_f(w)) : (double)fabsf(lo_f(w));
         if (cum + m > tgt) {
           sstar = s;
@@ -539,10 +600,9 @@ __device__ void sample_final(const VerifyArgs &a, int b, const VerifyDecision &d
     chosen = 0;
   }
   int *o = a.out_tok + (size_t)b * (k + 1);
-  if (lane <= k)
-    o[lane] = lane < dd.acc_n ? __ldcg(&a.draft_tok[(size_t)b * k + lane]) : (lane == dd.acc_n ? chosen : -1);
+  if (lane <= k) o[lane] = lane < dd.acc_n ? my : (lane == dd.acc_n ? chosen : -1);
   // every mass was read above, so it has landed: zero them for the next call
-  for (int s = s0; s < s1; ++s) st_relaxed64(ms + s, 0ull);
+  zero_words(msg, NS);
   if (lane == 0) {
     a.accept_len[b] = dd.acc_n + 1;
     a.num_accepted[b] = dd.acc_n;
@@ -1075,8 +1135,8 @@ __device__ void decider(const VerifyArgs &a, Shared &sh) {
       mask &= mask - 1;
       const int bj = __shfl_sync(kFull, b, j), pj = __shfl_sync(kFull, pass, j);
       if (pj == 1) {
-        if (stoch) decide_stochastic(a, bj, c);
-        else decide_greedy(a, bj);
+        if (stoch) decide_stochastic(a, bj, c, sh.scr);
+        else decide_greedy(a, bj, sh.scr);
       } else {
         VerifyDecision dd;
         const VerifyDecision *g = &a.dec[bj];
@@ -1088,7 +1148,7 @@ __device__ void decider(const VerifyArgs &a, Shared &sh) {
         dd.Ml = __ldcg(&g->Ml);
         dd.iZt = __ldcg(&g->iZt);
         dd.iZl = __ldcg(&g->iZl);
-        sample_final(a, bj, dd, c);
+        sample_final(a, bj, dd, c, sh.scr);
       }
     }
   }
