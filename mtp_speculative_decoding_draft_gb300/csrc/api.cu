@@ -39,6 +39,7 @@ int device_info(DevInfo *out) {
     if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MTP_ERR_CUDA;
     di.max_cluster = 8;
     if (verify_set_attributes() != cudaSuccess) return MTP_ERR_CUDA;
+    if (tc_set_attributes() != cudaSuccess) return MTP_ERR_CUDA;
     di.verify_bps = verify_blocks_per_sm();
     di.init = true;
   }
@@ -63,8 +64,12 @@ int check_dims(const MtpDims *d, int k) {
 }
 
 struct WsLayout {
-  size_t status, lm_cnt, x0, x1, x2, q, o, act, lm_part, logits, vstate, total;
+  size_t status, lm_cnt, x0, x1, x2, q, o, act, lm_part, logits, vstate, tc_a[3], tc_part, total;
+  bool tc;
+  TcSizes tz;
 };
+
+MtpShape shape_of(const MtpDims &d) { return MtpShape{d.B, d.d, d.Hq, d.Hkv, d.Dh, d.F, d.V}; }
 
 WsLayout draft_layout(const MtpDims &d, int k) {
   WsLayout L{};
@@ -91,6 +96,16 @@ WsLayout draft_layout(const MtpDims &d, int k) {
   off += up((size_t)d.B * k * d.V * 4);
   L.vstate = off;
   off += up(verify_state_bytes(d.B, k, d.V));
+  L.tc = tc_shape_ok(shape_of(d));
+  if (L.tc) {
+    L.tz = tc_sizes(shape_of(d));
+    for (int t = 0; t < 3; ++t) {
+      L.tc_a[t] = off;
+      off += up((size_t)L.tz.rows * L.tz.kmax * 2);
+    }
+    L.tc_part = off;
+    off += up(L.tz.part_floats * 4);
+  }
   L.total = off;
   return L;
 }
@@ -128,6 +143,8 @@ struct Draft {
   DraftCtx c;
   GemvPlan fc, qkv, wo, gateup, down, lm;
   int attn_cluster;
+  bool tc;   // tensor-core path
+  TcBufs t;
 };
 
 int prepare_draft(const MtpDims *dims, const MtpWeights *w, const void *h, const int32_t *last_tok, void *k_cache,
@@ -177,7 +194,7 @@ int prepare_draft(const MtpDims *dims, const MtpWeights *w, const void *h, const
   c.o = reinterpret_cast<float *>(base + L.o);
   c.act = reinterpret_cast<float *>(base + L.act);
   c.lm_part = reinterpret_cast<float *>(base + L.lm_part);
-  out->attn_cluster = attention_cluster_size(d.Lmax, di.max_cluster);
+  out->attn_cluster = attention_cluster_size(d.Lmax, d.B * d.Hkv, di.sms, di.max_cluster);
 
   out->fc = plan_gemv(OP_FC, d.d, 2 * d.d, d.B, di.sms);
   out->qkv = plan_gemv(OP_QKV, (d.Hq + 2 * d.Hkv) * d.Dh, d.d, d.B, di.sms);
@@ -188,6 +205,14 @@ int prepare_draft(const MtpDims *dims, const MtpWeights *w, const void *h, const
   if (out->lm.grid > kMaxLmGrid) return MTP_ERR_UNSUPPORTED_SHAPE;
   c.lm_grid = out->lm.grid;
   c.lm_rpc = out->lm.rows_per_cta;
+  out->tc = L.tc && tc_available();
+  if (out->tc) {
+    for (int t = 0; t < 3; ++t) out->t.a[t] = reinterpret_cast<uint16_t *>(base + L.tc_a[t]);
+    out->t.rows = L.tz.rows;
+    out->t.kmax = L.tz.kmax;
+    out->t.part = reinterpret_cast<float *>(base + L.tc_part);
+    out->t.part_floats = L.tz.part_floats;
+  }
   return MTP_OK;
 }
 
@@ -205,6 +230,13 @@ cudaError_t run_draft(Draft &D, cudaStream_t s) {
     DraftCtx c = D.c;
     c.j = j;
     c.zero_counters = j == 0;
+    if (D.tc) {  // tensor-core path
+      if ((e = timed(MTP_KC_GEMV, s, [&] { return run_block_pre_tc(c, D.t, s, pdl); }))) break;
+      if ((e = timed(MTP_KC_ATTN, s, [&] { return launch_attention(c, D.attn_cluster, s, pdl); }))) break;
+      if ((e = timed(MTP_KC_GEMV, s, [&] { return run_block_post_tc(c, D.t, s, pdl); }))) break;
+      if ((e = timed(MTP_KC_LMHEAD, s, [&] { return run_lmhead_tc(c, D.t, s, pdl); }))) break;
+      continue;
+    }
     if ((e = timed(MTP_KC_GEMV, s, [&] { return launch_gemv(c, D.fc, s, pdl); }))) break;
     if ((e = timed(MTP_KC_GEMV, s, [&] { return launch_gemv(c, D.qkv, s, pdl); }))) break;
     if ((e = timed(MTP_KC_ATTN, s, [&] { return launch_attention(c, D.attn_cluster, s, pdl); }))) break;

@@ -83,6 +83,29 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *s
   }
 }
 
+// The same bounded wait, parking the warp between tries (suspend-time hint):
+// the hardware wakes it when the phase completes, and a warp that waits for
+// data does not take issue slots from the warps computing.
+__device__ __forceinline__ bool mbar_sleep_wait(uint64_t *bar, uint32_t parity, int *status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
+        : "memory");
+    if (done) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      set_status(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
 // Cross-CTA flavour: acquire at cluster scope, so stores other CTAs of the
 // cluster made before their (release) arrivals are visible afterwards.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {

@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(DraftCtx c, GemvPlan
     }
     for (int u = 0; u < units_per_group && ncols > 0; ++u, ++n) {
       const int stage = n % S;
-      if (ok) ok = mbar_wait(&bars[stage], (uint32_t)(n / S) & 1u, c.status);
+      if (ok) ok = mbar_sleep_wait(&bars[stage], (uint32_t)(n / S) & 1u, c.status);
       ok = __all_sync(0xffffffffu, ok);
       float acc[BG];
 #pragma unroll
@@ -336,12 +336,21 @@ cudaError_t launch_gemv(const DraftCtx &c, const GemvPlan &g, cudaStream_t s, bo
 // loop.  Warps are merged through shared memory, CTAs through distributed
 // shared memory (each CTA finalises a slice of the output).
 
-constexpr int kAttnUnroll = 4;   // row pairs per batch and warp
+constexpr int kAttnWarps = 8;    // compute warps; warp kAttnWarps streams K/V
+constexpr int kAttnTile = 64;    // rows per ring stage, at most
+constexpr int kAttnStages = 3;
+// row pairs per warp and tile: 4, or 1 for groups of more than four heads
+// (their per-head state takes the registers)
+__host__ __device__ constexpr int attn_unroll(int gm) { return gm > 4 ? 1 : 4; }
 
+// Shared memory: [K/V ring: S x (K tile, V tile)][per-warp (max, sum, output)]
+// [q, then the CTA's output][CTA (max, sum)][mbarriers]
 size_t attention_smem_bytes(int Dh) {
-  return (size_t)kAttnThreads / 32 * kMaxGroup * (Dh + 2) * 4   // per-warp (max, sum, output)
-         + (size_t)kMaxGroup * Dh * 4                           // q, then the CTA's output
-         + (size_t)kMaxGroup * 2 * 4 + 16;                      // CTA (max, sum)
+  return (size_t)kAttnStages * 2 * kAttnTile * Dh * 2            // K/V ring
+         + (size_t)kAttnWarps * kMaxGroup * (Dh + 2) * 4          // per-warp (max, sum, output)
+         + (size_t)kMaxGroup * Dh * 4                             // q, then the CTA's output
+         + (size_t)kMaxGroup * 2 * 4                              // CTA (max, sum)
+         + (size_t)2 * kAttnStages * (kAttnTile / 16) * 8 + 16;   // mbarriers (up to 12 stages)
 }
 
 template <int DPL>
@@ -354,11 +363,11 @@ template <>
 struct RowVec<8> { uint4 x; };
 
 template <int DPL>
-__device__ __forceinline__ RowVec<DPL> load_row(const uint16_t *p) {
+__device__ __forceinline__ RowVec<DPL> load_row_smem(const uint16_t *p) {
   RowVec<DPL> r;
-  if constexpr (DPL == 2) r.x = __ldcg(reinterpret_cast<const unsigned int *>(p));
-  else if constexpr (DPL == 4) r.x = __ldcg(reinterpret_cast<const uint2 *>(p));
-  else r.x = __ldcg(reinterpret_cast<const uint4 *>(p));
+  if constexpr (DPL == 2) r.x = *reinterpret_cast<const unsigned int *>(p);
+  else if constexpr (DPL == 4) r.x = *reinterpret_cast<const uint2 *>(p);
+  else r.x = *reinterpret_cast<const uint4 *>(p);
   return r;
 }
 
@@ -372,14 +381,30 @@ __device__ __forceinline__ void unpack_row(const RowVec<DPL> &r, float *out) {
   }
 }
 
+// Decode attention of one (sequence, kv head) over its cache rows 0 .. L+j,
+// split over a cluster of C CTAs (CTA r takes a contiguous range of rows).
+// Warp kAttnWarps streams the CTA's K and V rows in tiles of 64 through a ring
+// of shared-memory stages with 1-D TMA bulk copies (a sequence's rows are
+// contiguous); tiles of context rows only -- written by the caller -- are
+// requested before the previous kernel of the chain has finished.  Each
+// compute warp takes 2U rows of every tile, a half-warp per row: scores for all
+// heads of the GQA group, then one online-softmax update per head for the
+// warp's rows.  Warps merge through shared memory, the cluster's CTAs through
+// distributed shared memory.
 template <int DH, int GM>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(DraftCtx c) {
-  constexpr int DPL = DH / 16, NW = kAttnThreads / 32, U = kAttnUnroll;
+  constexpr int DPL = DH / 16, NW = kAttnWarps, U = attn_unroll(GM);
+  constexpr int TT = 2 * U * NW;        // rows per tile
+  constexpr int TILE = TT * DH;         // elements of one K (or V) tile
+  constexpr int NS = kAttnStages * kAttnTile / TT;  // stages: the ring holds 3 x 64 rows
   extern __shared__ __align__(128) unsigned char smem[];
-  float *wst = reinterpret_cast<float *>(smem);           // [NW][GM][DH+2]: max, sum, output
+  uint16_t *ring = reinterpret_cast<uint16_t *>(smem);                  // [S][K tile, V tile]
+  float *wst = reinterpret_cast<float *>(ring + (size_t)NS * 2 * TILE);  // [NW][GM][DH+2]
   float *qo = wst + NW * kMaxGroup * (DH + 2);            // [GM][DH]
   float *mrun = qo + kMaxGroup * DH;                      // [GM]
   float *lrun = mrun + kMaxGroup;                         // [GM]
+  uint64_t *full = reinterpret_cast<uint64_t *>(lrun + kMaxGroup);
+  uint64_t *empty = full + NS;
 
   const int g = blockIdx.y, b = blockIdx.z;
   const int C = (int)cluster_size(), rank = (int)cluster_rank();
@@ -391,134 +416,158 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(DraftCtx c) {
   const int ntok = L + c.j + 1;
   const int T = (ntok + C - 1) / C;
   const int r0 = min(ntok, rank * T), r1 = min(ntok, r0 + T);
-  const int Tw = (r1 - r0 + NW - 1) / NW;
-  const int w0 = min(r1, r0 + warp * Tw), w1 = min(r1, w0 + Tw);
-  const int npairs = (w1 - w0 + 1) / 2;
-  const int nbatch = (npairs + U - 1) / U;
-  const size_t base = ((size_t)b * c.Hkv + g) * c.Lmax * DH + hl * DPL;
-  const uint16_t *kb = c.kc + base;
-  const uint16_t *vb = c.vc + base;
+  const int ntiles = (r1 - r0 + TT - 1) / TT;
+  const size_t base = ((size_t)b * c.Hkv + g) * c.Lmax * DH;
 
-  RowVec<DPL> kbuf[U], vbuf[U];
-  auto load_batch = [&](int bi) {
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int t = min(w0 + 2 * (bi * U + u) + half, max(w1 - 1, 0));
-      kbuf[u] = load_row<DPL>(kb + (size_t)t * DH);
-      vbuf[u] = load_row<DPL>(vb + (size_t)t * DH);
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NW);
     }
-  };
-  // the first batch can be fetched before the previous kernel finishes when it
-  // holds only context rows, which the caller wrote
-  const bool early = nbatch > 0 && w0 + 2 * U <= L;
-  if (early) load_batch(0);
-  grid_dep_wait();
-  grid_dep_launch();
-  if (nbatch > 0 && !early) load_batch(0);
-
-  const int nq = c.Hq * DH;
-  float q[GM][DPL];
-#pragma unroll
-  for (int h = 0; h < GM; ++h)
-#pragma unroll
-    for (int e = 0; e < DPL; ++e)
-      q[h][e] = h < group ? __ldcg(&c.q[(size_t)b * nq + ((size_t)g * group + h) * DH + hl * DPL + e]) : 0.f;
-  float m[GM], l[GM], acc[GM][DPL];
-#pragma unroll
-  for (int h = 0; h < GM; ++h) {
-    m[h] = -INFINITY;
-    l[h] = 0.f;
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) acc[h][e] = 0.f;
+    fence_barrier_init();
   }
-  const float scale = rsqrtf((float)DH) * kLog2e;
+  __syncthreads();
 
-  for (int bi = 0; bi < nbatch; ++bi) {
-    RowVec<DPL> kc_[U], vc_[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      kc_[u] = kbuf[u];
-      vc_[u] = vbuf[u];
+  bool ok = true;
+  if (warp == NW) {
+    // ------------------------------------------------ K/V producer
+    if (lane == 0) {
+      bool waited = false;
+      for (int i = 0; i < ntiles && ok; ++i) {
+        const int s = i % NS;
+        if (i >= NS) ok = mbar_wait(&empty[s], (uint32_t)((i / NS) - 1) & 1u, c.status);
+        if (!ok) break;
+        const int t0 = r0 + i * TT, n = min(TT, r1 - t0);
+        if (!waited && t0 + n > L) {  // rows L.. are appended by this chain
+          grid_dep_wait();
+          waited = true;
+        }
+        const uint32_t bytes = (uint32_t)n * DH * 2;
+        mbar_arrive_expect_tx(&full[s], 2 * bytes);
+        bulk_g2s(ring + (size_t)s * 2 * TILE, c.kc + base + (size_t)t0 * DH, bytes, &full[s]);
+        bulk_g2s(ring + (size_t)s * 2 * TILE + TILE, c.vc + base + (size_t)t0 * DH, bytes, &full[s]);
+      }
+      if (!waited) grid_dep_wait();
     }
-    if (bi + 1 < nbatch) load_batch(bi + 1);
-    // scores of the batch's U rows (one per pair and half-warp), all heads
-    float sc[U][GM];
+    grid_dep_launch();
+  } else {
+    // ------------------------------------------------ compute warps
+    grid_dep_wait();  // q comes from this depth's projection
+    grid_dep_launch();
+    const int nq = c.Hq * DH;
+    float q[GM][DPL];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const bool live = w0 + 2 * (bi * U + u) + half < w1;
-      float kv[DPL];
-      unpack_row<DPL>(kc_[u], kv);
+    for (int h = 0; h < GM; ++h)
+#pragma unroll
+      for (int e = 0; e < DPL; ++e)
+        q[h][e] = h < group ? __ldcg(&c.q[(size_t)b * nq + ((size_t)g * group + h) * DH + hl * DPL + e]) : 0.f;
+    float m[GM], l[GM], acc[GM][DPL];
+#pragma unroll
+    for (int h = 0; h < GM; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) acc[h][e] = 0.f;
+    }
+    const float scale = rsqrtf((float)DH) * kLog2e;
+
+    for (int i = 0; i < ntiles; ++i) {
+      const int s = i % NS;
+      if (ok) ok = mbar_wait(&full[s], (uint32_t)(i / NS) & 1u, c.status);
+      ok = __all_sync(0xffffffffu, ok);
+      const int t0 = r0 + i * TT;
+      const uint16_t *kt = ring + (size_t)s * 2 * TILE;
+      const uint16_t *vt = kt + TILE;
+      // this warp's rows of the tile: 2 U w + 2 u + half
+      float sc[U][GM];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int rl = 2 * U * warp + 2 * u + half;
+        const bool live = t0 + rl < r1;
+        float kv[DPL];
+        unpack_row<DPL>(load_row_smem<DPL>(kt + (size_t)rl * DH + hl * DPL), kv);
+#pragma unroll
+        for (int h = 0; h < GM; ++h) {
+          float sdot = 0.f;
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) sdot = fmaf(q[h][e], kv[e], sdot);
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) sdot += __shfl_xor_sync(0xffffffffu, sdot, o);
+          sc[u][h] = live ? sdot * scale : -INFINITY;
+        }
+      }
+      float vv[U][DPL];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int rl = 2 * U * warp + 2 * u + half;
+        if (t0 + rl < r1) unpack_row<DPL>(load_row_smem<DPL>(vt + (size_t)rl * DH + hl * DPL), vv[u]);
+        else {
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) vv[u][e] = 0.f;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
+      // one online-softmax update per head for the warp's rows
 #pragma unroll
       for (int h = 0; h < GM; ++h) {
-        float sdot = 0.f;
+        if (h < group) {
+          float bm = sc[0][h];
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) sdot = fmaf(q[h][e], kv[e], sdot);
+          for (int u = 1; u < U; ++u) bm = fmaxf(bm, sc[u][h]);
+          const float mn = fmaxf(m[h], bm);
+          if (mn != -INFINITY) {
+            const float f = exp2f(m[h] - mn);   // 0 while m is -inf
+            float pw[U], ps = 0.f;
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) sdot += __shfl_xor_sync(0xffffffffu, sdot, o);
-        sc[u][h] = live ? sdot * scale : -INFINITY;
+            for (int u = 0; u < U; ++u) {
+              pw[u] = exp2f(sc[u][h] - mn);
+              ps += pw[u];
+            }
+            l[h] = l[h] * f + ps;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) {
+              float a = acc[h][e] * f;
+#pragma unroll
+              for (int u = 0; u < U; ++u) a = fmaf(pw[u], vv[u][e], a);
+              acc[h][e] = a;
+            }
+            m[h] = mn;
+          }
+        }
       }
     }
-    // one online-softmax update per head for the whole batch
-    float vv[U][DPL];
-#pragma unroll
-    for (int u = 0; u < U; ++u) unpack_row<DPL>(vc_[u], vv[u]);
+
+    // merge the two half-warps into the warp's slot
 #pragma unroll
     for (int h = 0; h < GM; ++h) {
       if (h < group) {
-        float bm = sc[0][h];
+        const float m2 = __shfl_xor_sync(0xffffffffu, m[h], 16);
+        const float l2 = __shfl_xor_sync(0xffffffffu, l[h], 16);
+        const float M = fmaxf(m[h], m2);
+        const float f1 = m[h] == -INFINITY ? 0.f : exp2f(m[h] - M);
+        const float f2 = m2 == -INFINITY ? 0.f : exp2f(m2 - M);
 #pragma unroll
-        for (int u = 1; u < U; ++u) bm = fmaxf(bm, sc[u][h]);
-        const float mn = fmaxf(m[h], bm);
-        if (mn != -INFINITY) {
-          const float f = exp2f(m[h] - mn);   // 0 while m is -inf
-          float pw[U], ps = 0.f;
-#pragma unroll
-          for (int u = 0; u < U; ++u) {
-            pw[u] = exp2f(sc[u][h] - mn);
-            ps += pw[u];
-          }
-          l[h] = l[h] * f + ps;
-#pragma unroll
-          for (int e = 0; e < DPL; ++e) {
-            float a = acc[h][e] * f;
-#pragma unroll
-            for (int u = 0; u < U; ++u) a = fmaf(pw[u], vv[u][e], a);
-            acc[h][e] = a;
-          }
-          m[h] = mn;
+        for (int e = 0; e < DPL; ++e) {
+          const float a2 = __shfl_xor_sync(0xffffffffu, acc[h][e], 16);
+          acc[h][e] = acc[h][e] * f1 + a2 * f2;
         }
-      }
-    }
-  }
-
-  // merge the two half-warps, then the warps of the CTA
+        l[h] = l[h] * f1 + l2 * f2;
+        m[h] = M;
+        if (half == 0) {
+          float *ws = wst + ((size_t)warp * kMaxGroup + h) * (DH + 2);
+          if (hl == 0) {
+            ws[0] = m[h];
+            ws[1] = l[h];
+          }
 #pragma unroll
-  for (int h = 0; h < GM; ++h) {
-    if (h < group) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m[h], 16);
-      const float l2 = __shfl_xor_sync(0xffffffffu, l[h], 16);
-      const float M = fmaxf(m[h], m2);
-      const float f1 = m[h] == -INFINITY ? 0.f : exp2f(m[h] - M);
-      const float f2 = m2 == -INFINITY ? 0.f : exp2f(m2 - M);
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) {
-        const float a2 = __shfl_xor_sync(0xffffffffu, acc[h][e], 16);
-        acc[h][e] = acc[h][e] * f1 + a2 * f2;
-      }
-      l[h] = l[h] * f1 + l2 * f2;
-      m[h] = M;
-      if (half == 0) {
-        float *ws = wst + ((size_t)warp * kMaxGroup + h) * (DH + 2);
-        if (hl == 0) {
-          ws[0] = m[h];
-          ws[1] = l[h];
+          for (int e = 0; e < DPL; ++e) ws[2 + hl * DPL + e] = acc[h][e];
         }
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) ws[2 + hl * DPL + e] = acc[h][e];
       }
     }
   }
   __syncthreads();
+  // merge the warps of the CTA
   for (int idx = tid; idx < group * DH; idx += kAttnThreads) {
     const int h = idx / DH, e = idx % DH;
     float M = -INFINITY;
@@ -539,8 +588,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(DraftCtx c) {
       lrun[h] = Ls;
     }
   }
-
   // combine across the cluster: CTA r finalises pairs (h, e) r, r + C, ...
+  const int nq = c.Hq * DH;
   cluster_sync();
   for (int idx = rank + C * tid; idx < group * DH; idx += C * kAttnThreads) {
     const int h = idx / DH, e = idx % DH;
@@ -571,12 +620,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(DraftCtx c) {
   cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
 }
 
-int attention_cluster_size(int ctx_max, int max_cluster) {
+int attention_cluster_size(int ctx_max, int pairs, int num_sms, int max_cluster) {
   const int forced = env_int("MTP_ATTN_CLUSTER", 0);
   if (forced > 0) return forced < max_cluster ? forced : max_cluster;
-  // up to 8 CTAs per (sequence, kv head): a 16-CTA cluster of one-CTA-per-SM
-  // kernels does not fit every GPC at once
-  int C = (ctx_max + 255) / 256;
+  // CTAs per (sequence, kv head): one per 512 context rows, at most 8 (a
+  // 16-CTA cluster of one-CTA-per-SM kernels does not fit every GPC at once),
+  // and no more than about four CTAs per SM in all
+  int C = (ctx_max + 511) / 512;
+  const int by_sms = (4 * num_sms + pairs - 1) / (pairs > 0 ? pairs : 1);
+  if (C > by_sms) C = by_sms;
   const int cap = max_cluster < 8 ? max_cluster : 8;
   return C < 1 ? 1 : (C > cap ? cap : C);
 }

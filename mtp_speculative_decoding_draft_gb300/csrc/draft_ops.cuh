@@ -160,7 +160,7 @@ __device__ __forceinline__ float silu_f(float z) { return z / (1.f + __expf(-z))
 // Greedy: the argmax, lowest index on ties.  Stochastic: the inverse CDF of
 // softmax(logits / T) at u_draft[b, j] -- walk the per-CTA masses in vocabulary
 // order, then rescan the CTA that holds the crossing in float64.
-__device__ void lm_select_warp(const DraftCtx &c, int G, int rpc) {
+__device__ inline void lm_select_warp(const DraftCtx &c, int G, int rpc) {
   const int lane = threadIdx.x & 31;
   const float cT = kLog2e / c.T;
   for (int b = 0; b < c.B; ++b) {

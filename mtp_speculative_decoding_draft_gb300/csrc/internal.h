@@ -58,14 +58,37 @@ struct GemvPlan {
 
 constexpr int kGemvWarps = 8;
 constexpr int kGemvThreads = kGemvWarps * 32;
-constexpr int kAttnThreads = 256;
+constexpr int kAttnThreads = 288;  // 8 compute warps and a K/V streaming warp
 constexpr int kMaxGroup = 8;        // Hq / Hkv
 
 GemvPlan plan_gemv(int op, int N, int K, int B, int num_sms);
 cudaError_t launch_gemv(const DraftCtx &c, const GemvPlan &g, cudaStream_t s, bool pdl);
 cudaError_t launch_attention(const DraftCtx &c, int cluster, cudaStream_t s, bool pdl);
 size_t attention_smem_bytes(int Dh);
-int attention_cluster_size(int ctx_max, int max_cluster);
+int attention_cluster_size(int ctx_max, int pairs, int num_sms, int max_cluster);
+
+// Tensor-core path of the draft chain (batches of several sequences).
+struct MtpShape {
+  int B, d, Hq, Hkv, Dh, F, V;
+};
+struct TcSizes {
+  int rows;            // activation rows: the batch padded to the MMA N
+  int kmax;            // activation row length: max K over the GEMMs
+  size_t part_floats;  // split-K partials / LM-head logits scratch
+};
+struct TcBufs {
+  uint16_t *a[3];  // [rows, kmax] bf16 terms hi, mid, lo of the next GEMM's input
+  int rows, kmax;
+  float *part;
+  size_t part_floats;
+};
+bool tc_shape_ok(const MtpShape &s);  // the workspace holds the tensor-core buffers
+bool tc_available();                  // the driver can encode tensor maps
+TcSizes tc_sizes(const MtpShape &s);
+cudaError_t tc_set_attributes();
+cudaError_t run_block_pre_tc(const DraftCtx &c, const TcBufs &t, cudaStream_t s, bool pdl);
+cudaError_t run_block_post_tc(const DraftCtx &c, const TcBufs &t, cudaStream_t s, bool pdl);
+cudaError_t run_lmhead_tc(const DraftCtx &c, const TcBufs &t, cudaStream_t s, bool pdl);
 
 // Verification launch.
 struct VerifyPlan {

@@ -1,0 +1,724 @@
+// The draft chain for batches of several sequences on the fifth-generation
+// tensor cores.  A weight-streaming GEMV reads every weight matrix once per
+// couple of sequences; here each depth reads it once for the whole batch:
+//
+//   out[b, n] = sum_k W[n, k] a[b, k]         (fp32 accumulation in TMEM)
+//
+// with the fp32 activation a split into three bf16 terms a = hi + mid + lo
+// (hi = bf16(a), mid = bf16(a - hi), lo = bf16(a - hi - mid)): three
+// tcgen05.mma per k-step keep the activation's 24 significant bits, so the
+// products match an fp32 GEMV ("The Tiny Draft Model Hidden Inside
+// Qwen", opening section: the module is one full-attention block; the same
+// module is applied k times, "One step deeper than the main model").
+//
+// Per depth: prep(FC input) -> GEMM FC -> mid(x0, QKV input) -> GEMM QKV ->
+// mid(q, K/V append) -> attention -> prep(WO input) -> GEMM WO -> mid(x1,
+// gate/up input) -> GEMM gate/up -> mid(SwiGLU, down input) -> GEMM down ->
+// mid(x2, LM-head input) -> GEMM LM head -> draft-token selection.  The GEMM
+// is split over K where the output has few 128-row tiles; the mid kernels (one
+// CTA per sequence) sum the split-K partials and apply the same epilogues as
+// the GEMV path (residual adds, SwiGLU, bf16 K/V append) before writing the
+// next GEMM's bf16 terms.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <stdlib.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "draft_ops.cuh"
+#include "internal.h"
+#include "tcgen05.cuh"
+
+namespace mtp {
+
+namespace {
+
+constexpr int kTcThreads = 192;  // warp 0 TMA, warp 1 MMA and TMEM, warps 2-5 read TMEM back
+constexpr int kTileM = 128;      // output rows per tile (MMA M)
+constexpr int kBK = 64;          // K per stage: one 128-byte swizzle row of bf16
+constexpr uint32_t kWTileBytes = kTileM * kBK * 2;
+constexpr int kSmemBudget = 200 * 1024;
+constexpr int kTargetCtas = 296;  // split K until about this many CTAs (two per SM)
+constexpr int kMaxSplits = 16;
+constexpr int kPrepThreads = 256;
+
+struct TcMaps {
+  CUtensorMap w[3];  // weight row blocks (QKV: wq, wk, wv; gate/up: wgate, wup)
+  CUtensorMap a[3];  // activation terms hi, mid, lo
+};
+
+struct TcGemmArgs {
+  int nmaps, mt;                   // weight maps; 128-row tiles per CTA (sharing each activation stage)
+  int rows[3], groups[3], base[3];  // rows and mt-tile groups of each map; its first output row
+  int ks, kb_per, kbs;             // K splits, 64-wide k-blocks per split and in all
+  int nb, stages;                  // MMA N (padded batch rows), pipeline depth
+  int B, arow0;                    // batch rows, first batch row of this group
+  float *out;                      // element (split s, batch b, row n) at out + s*sstride + b*bstride + n
+  size_t sstride, bstride;
+  int *status;
+};
+
+__host__ __device__ inline uint32_t a_tile_bytes(int nb) { return (uint32_t)nb * kBK * 2; }
+constexpr int kTerms = 3;
+__host__ __device__ inline uint32_t stage_bytes(int nb, int mt) {
+  return (uint32_t)mt * kWTileBytes + kTerms * a_tile_bytes(nb);
+}
+__host__ __device__ inline int tmem_cols(int nb, int mt) {
+  int n = 32;
+  while (n < nb * mt) n *= 2;
+  return n;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- GEMM kernel
+
+__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ TcMaps maps,
+                                                                  const TcGemmArgs g) {
+  extern __shared__ unsigned char smem_raw[];
+  // SW128 tiles need 1024-byte alignment
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  unsigned char *sm = smem_raw + pad;
+  const int S = g.stages;
+  const int MT = g.mt;
+  const uint32_t ab = a_tile_bytes(g.nb), sb = stage_bytes(g.nb, MT), wb = (uint32_t)MT * kWTileBytes;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sm + (size_t)S * sb);
+  uint64_t *empty = full + S;
+  uint64_t *done = empty + S;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ncols = tmem_cols(g.nb, MT);
+
+  const int split = blockIdx.x % g.ks;
+  int grp = blockIdx.x / g.ks, m = 0;
+  while (m < g.nmaps - 1 && grp >= g.groups[m]) {
+    grp -= g.groups[m];
+    ++m;
+  }
+  const int row0 = grp * MT * kTileM;  // within map m
+  const int kb0 = split * g.kb_per;
+  const int nkb = max(0, min(g.kb_per, g.kbs - kb0));
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, (uint32_t)ncols);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  grid_dep_launch();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // Weights do not depend on the previous kernel: the first stages are
+      // requested before waiting for it; the activations only after.
+      const uint64_t pol_w = l2_policy_evict_first(), pol_a = l2_policy_evict_last();
+      const int pre = min(S, nkb);
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], sb);
+        for (int t = 0; t < MT; ++t)
+          tma_load_2d(sm + (size_t)i * sb + t * kWTileBytes, &maps.w[m], (kb0 + i) * kBK, row0 + t * kTileM,
+                      &full[i], pol_w);
+      }
+      grid_dep_wait();
+      bool ok = true;
+      for (int i = 0; i < nkb && ok; ++i) {
+        const int s = i % S;
+        unsigned char *st = sm + (size_t)s * sb;
+        const int x = (kb0 + i) * kBK;
+        if (i >= pre) {
+          ok = mbar_wait(&empty[s], (uint32_t)((i / S) - 1) & 1u, g.status);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&full[s], sb);
+          for (int t = 0; t < MT; ++t)
+            tma_load_2d(st + t * kWTileBytes, &maps.w[m], x, row0 + t * kTileM, &full[s], pol_w);
+        }
+#pragma unroll
+        for (int tt = 0; tt < kTerms; ++tt)
+          tma_load_2d(st + wb + tt * ab, &maps.a[tt], x, g.arow0, &full[s], pol_a);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kTileM, g.nb);
+      bool ok = true;
+      for (int i = 0; i < nkb && ok; ++i) {
+        const int s = i % S;
+        ok = mbar_wait(&full[s], (uint32_t)(i / S) & 1u, g.status);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t st = smem_u32(sm + (size_t)s * sb);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)  // 16 bf16 = 32 bytes: +2 in the >>4 address field
+          for (int t = 0; t < MT; ++t) {  // tile t accumulates in TMEM columns [t nb, (t + 1) nb)
+            const uint64_t dw = sw128_kmajor_desc(st + t * kWTileBytes) + 2 * kk;
+#pragma unroll
+            for (int tt = 0; tt < kTerms; ++tt)
+              mma_bf16(tmem + (uint32_t)(t * g.nb), dw, sw128_kmajor_desc(st + wb + tt * ab) + 2 * kk, idesc,
+                       (i | kk | tt) != 0 ? 1u : 0u);
+          }
+        mma_commit(&empty[s]);  // the stage is free once these MMAs have read it
+      }
+      mma_commit(done);
+    }
+  } else {
+    // read the accumulator back: warp w reads TMEM lanes 32 (w % 4) .. + 31
+    const int q = warp & 3;
+    const bool ok = mbar_wait(done, 0u, g.status) && nkb > 0;
+    tc_fence_after();
+    for (int t = 0; t < MT; ++t) {
+      const int row = row0 + t * kTileM + q * 32 + lane;
+      const bool valid = ok && row < g.rows[m];
+      float *o = g.out + (size_t)split * g.sstride + (size_t)g.base[m] + row;
+      for (int c0 = 0; c0 < g.nb; c0 += 32) {
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(t * g.nb + c0), v);
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int b = g.arow0 + c0 + i;
+            if (b < g.B) o[(size_t)b * g.bstride] = v[i];
+          }
+        }
+      }
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, (uint32_t)ncols);
+  }
+}
+
+// ---------------------------------------------------------------- per-sequence kernels
+
+namespace {
+
+// Eight values into the three bf16 terms of activation row b at column col.
+__device__ __forceinline__ void store_split8(const TcBufs &t, int b, int col, const float *v) {
+  uint32_t w[kTerms][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float r0 = v[2 * i], r1 = v[2 * i + 1];
+#pragma unroll
+    for (int tt = 0; tt < kTerms; ++tt) {
+      const __nv_bfloat16 h0 = __float2bfloat16_rn(r0), h1 = __float2bfloat16_rn(r1);
+      w[tt][i] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+      r0 -= __bfloat162float(h0);
+      r1 -= __bfloat162float(h1);
+    }
+  }
+  const size_t off = (size_t)b * t.kmax + col;
+#pragma unroll
+  for (int tt = 0; tt < kTerms; ++tt)
+    *reinterpret_cast<uint4 *>(t.a[tt] + off) = make_uint4(w[tt][0], w[tt][1], w[tt][2], w[tt][3]);
+}
+
+// Sum over the K splits of eight consecutive outputs (row n) of sequence b.
+__device__ __forceinline__ void sum8(const float *part, int ks, size_t sstride, size_t boff, float *y) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) y[i] = 0.f;
+  for (int s = 0; s < ks; ++s) {
+    float v[8];
+    load8_f32(part + s * sstride + boff, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] += v[i];
+  }
+}
+
+__device__ __forceinline__ float sumsq8(const float *v, float acc) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc = fmaf(v[i], v[i], acc);
+  return acc;
+}
+
+}  // namespace
+
+// Input of the input projection: [rms(E[tok]) g_emb ; rms(x) g_hid], x = h at
+// depth 0, else the previous depth's x2.
+__global__ void __launch_bounds__(kPrepThreads) tc_prep_fc_kernel(DraftCtx c, TcBufs t) {
+  __shared__ float red[2 * kGemvWarps];
+  const int b = blockIdx.x, d = c.d;
+  grid_dep_wait();
+  grid_dep_launch();
+  const int tok = depth_token(c, b);
+  const uint16_t *e = c.E + (size_t)tok * d;
+  float s0 = 0.f, s1 = 0.f;
+  for (int i = threadIdx.x * 8; i < d; i += kPrepThreads * 8) {
+    float v[8], x[8];
+    load8_bf16(e + i, v);
+    if (c.j == 0) load8_bf16(c.h + (size_t)b * d + i, x);
+    else load8_f32(c.x2 + (size_t)b * d + i, x);
+    s0 = sumsq8(v, s0);
+    s1 = sumsq8(x, s1);
+  }
+  s0 = block_sum_256(s0, red);
+  s1 = block_sum_256(s1, red + kGemvWarps);
+  const float r0 = rsqrtf(s0 / (float)d + c.eps), r1 = rsqrtf(s1 / (float)d + c.eps);
+  for (int i = threadIdx.x * 8; i < d; i += kPrepThreads * 8) {
+    float v[8], x[8], g[8];
+    load8_bf16(e + i, v);
+    load8_bf16(c.g_emb + i, g);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = v[q] * r0 * g[q];
+    store_split8(t, b, i, v);
+    if (c.j == 0) load8_bf16(c.h + (size_t)b * d + i, x);
+    else load8_f32(c.x2 + (size_t)b * d + i, x);
+    load8_bf16(c.g_hid + i, g);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) x[q] = x[q] * r1 * g[q];
+    store_split8(t, b, d + i, x);
+  }
+}
+
+// Input of the output projection: the attention output as is.
+__global__ void __launch_bounds__(kPrepThreads) tc_prep_wo_kernel(DraftCtx c, TcBufs t) {
+  const int b = blockIdx.x, n = c.Hq * c.Dh;
+  grid_dep_wait();
+  grid_dep_launch();
+  for (int i = threadIdx.x * 8; i < n; i += kPrepThreads * 8) {
+    float v[8];
+    load8_f32(c.o + (size_t)b * n + i, v);
+    store_split8(t, b, i, v);
+  }
+}
+
+// Sum the split-K partials of OP for sequence b, apply OP's epilogue and
+// write the next GEMM's input halves.
+template <int OP>
+__global__ void __launch_bounds__(kPrepThreads) tc_mid_kernel(DraftCtx c, TcBufs t, int ks, int N) {
+  __shared__ float red[kGemvWarps];
+  const int b = blockIdx.x, d = c.d;
+  const size_t sstride = (size_t)c.B * N, boff = (size_t)b * N;
+  grid_dep_wait();
+  grid_dep_launch();
+  if (OP == OP_QKV) {
+    const int nq = c.Hq * c.Dh, nkv = c.Hkv * c.Dh;
+    int L = __ldg(&c.ctx_len[b]);
+    if (L < 0 || L + c.k > c.Lmax) {
+      if (threadIdx.x == 0) set_status(c.status, kStatusBadCtx);
+      L = min(max(L, 0), c.Lmax - c.k);
+    }
+    for (int i = threadIdx.x * 8; i < N; i += kPrepThreads * 8) {
+      float y[8];
+      sum8(t.part, ks, sstride, boff + i, y);
+      if (i < nq) {
+        *reinterpret_cast<float4 *>(c.q + (size_t)b * nq + i) = make_float4(y[0], y[1], y[2], y[3]);
+        *reinterpret_cast<float4 *>(c.q + (size_t)b * nq + i + 4) = make_float4(y[4], y[5], y[6], y[7]);
+      } else {
+        int r = i - nq;
+        uint16_t *cache = r < nkv ? c.kc : c.vc;
+        if (r >= nkv) r -= nkv;
+        const int kvh = r / c.Dh, dd = r % c.Dh;  // 8 | Dh: the eight stay in one head
+        uint16_t *dst = cache + (((size_t)b * c.Hkv + kvh) * c.Lmax + L + c.j) * c.Dh + dd;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) dst[q] = __bfloat16_as_ushort(__float2bfloat16_rn(y[q]));
+      }
+    }
+    return;
+  }
+  if (OP == OP_GATEUP) {  // SwiGLU: gate rows [0, F), up rows [F, 2F)
+    const int F = c.F;
+    for (int i = threadIdx.x * 8; i < F; i += kPrepThreads * 8) {
+      float gt[8], up[8];
+      sum8(t.part, ks, sstride, boff + i, gt);
+      sum8(t.part, ks, sstride, boff + F + i, up);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) gt[q] = silu_f(gt[q]) * up[q];
+      store_split8(t, b, i, gt);
+    }
+    return;
+  }
+  // FC -> x0, WO -> x1 = x0 + y, DOWN -> x2 = x1 + y; then the next input rms(x) g
+  float *xo = OP == OP_FC ? c.x0 : (OP == OP_WO ? c.x1 : c.x2);
+  const float *xr = OP == OP_WO ? c.x0 : c.x1;
+  const uint16_t *gain = OP == OP_FC ? c.g_attn : (OP == OP_WO ? c.g_mlp : c.g_final);
+  float ss = 0.f;
+  for (int i = threadIdx.x * 8; i < d; i += kPrepThreads * 8) {
+    float y[8];
+    sum8(t.part, ks, sstride, boff + i, y);
+    if (OP != OP_FC) {
+      float r[8];
+      load8_f32(xr + (size_t)b * d + i, r);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) y[q] += r[q];
+    }
+    *reinterpret_cast<float4 *>(xo + (size_t)b * d + i) = make_float4(y[0], y[1], y[2], y[3]);
+    *reinterpret_cast<float4 *>(xo + (size_t)b * d + i + 4) = make_float4(y[4], y[5], y[6], y[7]);
+    ss = sumsq8(y, ss);
+  }
+  ss = block_sum_256(ss, red);
+  const float rs = rsqrtf(ss / (float)d + c.eps);
+  __syncthreads();  // this CTA's x writes are visible to its own re-reads below
+  for (int i = threadIdx.x * 8; i < d; i += kPrepThreads * 8) {
+    float y[8], g[8];
+    load8_f32(xo + (size_t)b * d + i, y);
+    load8_bf16(gain + i, g);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) y[q] = y[q] * rs * g[q];
+    store_split8(t, b, i, y);
+  }
+}
+
+// Draft-token selection of sequence b at depth j from its logits row: argmax
+// (lowest index on ties), or the inverse CDF of softmax(logits / T) at
+// u_draft[b, j].  All passes read the row lane-strided (coalesced): warp w
+// owns a contiguous segment, the segments' masses are scanned in float64 in
+// vocabulary order and the warp holding the crossing rescans its segment 32
+// elements at a time with a float64 warp scan.
+constexpr int kSelThreads = 512;
+__global__ void __launch_bounds__(kSelThreads) tc_select_kernel(DraftCtx c, const float *logits, size_t bstride) {
+  constexpr int NW = kSelThreads / 32;
+  __shared__ float sv[NW];
+  __shared__ int si[NW];
+  __shared__ double sd[NW];
+  __shared__ int s_last[NW];
+  const int b = blockIdx.x, V = c.V, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  grid_dep_wait();
+  grid_dep_launch();
+  const float *row = logits + (size_t)b * bstride;
+  float M = -INFINITY;
+  int I = 0x7fffffff;
+  for (int i = tid; i < V; i += kSelThreads) {
+    const float x = __ldcg(row + i);
+    if (x > M) {  // ascending i per thread: the first maximum is the lowest index
+      M = x;
+      I = i;
+    }
+  }
+  warp_argmax(M, I);
+  if (lane == 0) {
+    sv[warp] = M;
+    si[warp] = I;
+  }
+  __syncthreads();
+  M = -INFINITY;
+  I = 0x7fffffff;
+  for (int w = 0; w < NW; ++w) argmax_merge(M, I, sv[w], si[w]);
+  int tok = I;
+  if (M == -INFINITY || !(M == M)) {
+    if (tid == 0) set_status(c.status, kStatusNonFinite);
+    tok = 0;
+  } else if (c.mode == 1) {
+    const float cT = kLog2e / c.T;
+    const int seg = ((V + NW - 1) / NW + 31) / 32 * 32;
+    const int s0 = min(V, warp * seg), s1 = min(V, s0 + seg);
+    float own = 0.f;
+    int lastpos = -1;
+    for (int i = s0 + lane; i < s1; i += 32) {
+      const float w = exp2f((__ldcg(row + i) - M) * cT);
+      own += w;
+      if (w > 0.f) lastpos = i;
+    }
+    const double segsum = warp_sum_d((double)own);
+    int lp = lastpos;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
+    if (lane == 0) {
+      sd[warp] = segsum;
+      s_last[warp] = lp;
+    }
+    __syncthreads();
+    double Z = 0.0;
+    int last = -1;
+    for (int w = 0; w < NW; ++w) {
+      Z += sd[w];
+      last = max(last, s_last[w]);
+    }
+    const double target = (double)__ldg(&c.u_draft[b * c.k + c.j]) * Z;
+    double before = 0.0;
+    int wstar = -1;
+    for (int w = 0; w < NW; ++w) {
+      if (wstar < 0 && before + sd[w] > target) wstar = w;
+      if (wstar < 0) before += sd[w];
+    }
+    __shared__ int s_found;
+    if (tid == 0) s_found = 0x7fffffff;
+    __syncthreads();
+    if (warp == wstar) {
+      double cum = before;
+      bool hit_any = false;
+      for (int i0 = s0; i0 < s1; i0 += 32) {
+        const int i = i0 + lane;
+        const double w = i < s1 ? (double)exp2f((__ldcg(row + i) - M) * cT) : 0.0;
+        double incl = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const double v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, i < s1 && cum + incl > target);
+        if (hit) {
+          if (lane == 0) s_found = i0 + __ffs(hit) - 1;
+          hit_any = true;
+          break;
+        }
+        cum += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      // rounding left the crossing past this segment's rescan: its last positive index
+      if (!hit_any && lane == 0) s_found = s_last[warp] >= 0 ? s_last[warp] : 0x7fffffff;
+    }
+    __syncthreads();
+    tok = s_found != 0x7fffffff ? s_found : (last >= 0 ? last : I);
+  }
+  if (tid == 0) c.draft_tok[b * c.k + c.j] = tok;
+}
+
+// ---------------------------------------------------------------- host side
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 map over a row-major [rows, cols] matrix with row stride ld
+// (elements), boxes of box_rows x 64 columns, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t ld, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {ld * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct OpShape {
+  int nmaps;
+  const uint16_t *w[3];
+  int rows[3];
+  int K;
+};
+
+OpShape op_shape(const DraftCtx &c, int op) {
+  OpShape s{};
+  s.nmaps = 1;
+  switch (op) {
+    case OP_FC: s.w[0] = c.fc; s.rows[0] = c.d; s.K = 2 * c.d; break;
+    case OP_QKV:
+      s.nmaps = 3;
+      s.w[0] = c.wq; s.rows[0] = c.Hq * c.Dh;
+      s.w[1] = c.wk; s.rows[1] = c.Hkv * c.Dh;
+      s.w[2] = c.wv; s.rows[2] = c.Hkv * c.Dh;
+      s.K = c.d;
+      break;
+    case OP_WO: s.w[0] = c.wo; s.rows[0] = c.d; s.K = c.Hq * c.Dh; break;
+    case OP_GATEUP:
+      s.nmaps = 2;
+      s.w[0] = c.wgate; s.rows[0] = c.F;
+      s.w[1] = c.wup; s.rows[1] = c.F;
+      s.K = c.d;
+      break;
+    case OP_DOWN: s.w[0] = c.wdown; s.rows[0] = c.d; s.K = c.F; break;
+    default: s.w[0] = c.E; s.rows[0] = c.V; s.K = c.d; break;
+  }
+  return s;
+}
+
+int op_rows(const OpShape &s) {
+  int n = 0;
+  for (int i = 0; i < s.nmaps; ++i) n += s.rows[i];
+  return n;
+}
+
+int op_groups(const OpShape &s, int mt) {
+  int n = 0;
+  for (int i = 0; i < s.nmaps; ++i) n += ((s.rows[i] + kTileM - 1) / kTileM + mt - 1) / mt;
+  return n;
+}
+
+// K splits: about kTargetCtas CTAs, whole k-blocks per split.
+void op_splits(int tiles, int K, int *ks, int *kb_per) {
+  const int kbs = K / kBK;
+  int s = (kTargetCtas + tiles - 1) / tiles;
+  s = s < 1 ? 1 : (s > kMaxSplits ? kMaxSplits : s);
+  if (s > kbs) s = kbs;
+  *kb_per = (kbs + s - 1) / s;
+  *ks = (kbs + *kb_per - 1) / *kb_per;
+}
+
+int batch_nb(int B) { return B <= 32 ? 32 : (B <= 64 ? 64 : 128); }
+
+// 128-row weight tiles per CTA: each activation stage in shared memory serves
+// mt tiles, so the activations are re-read from L2 once per mt tiles.  Two
+// pipeline stages at least must fit.  MTP_TC_MT overrides.
+int op_mt(int nb) {
+  const char *v = getenv("MTP_TC_MT");
+  int mt = v && *v ? atoi(v) : (nb <= 64 ? 4 : 2);
+  if (mt < 1) mt = 1;
+  while (mt > 1 && (2 * stage_bytes(nb, mt) > (uint32_t)kSmemBudget || nb * mt > 512)) --mt;
+  return mt;
+}
+
+template <class K, class... Args>
+cudaError_t launch(K kern, dim3 grid, int threads, size_t smem, cudaStream_t s, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  note_launch();
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+}  // namespace
+
+// The tensor-core path needs K % 64 == 0 for every GEMM and weight blocks of
+// at least one tile; it pays off from a handful of sequences up (the GEMV
+// re-reads the weights once per couple of sequences).  MTP_TC_MIN_B overrides
+// the threshold (0 turns the path off).
+bool tc_shape_ok(const MtpShape &s) {
+  if (s.d % kBK || (s.Hq * s.Dh) % kBK || s.F % kBK) return false;
+  if (s.d < kTileM || s.F < kTileM || s.Hkv * s.Dh < kTileM || s.V < kTileM) return false;
+  const char *v = getenv("MTP_TC_MIN_B");
+  const int min_b = v && *v ? atoi(v) : 5;
+  return min_b > 0 && s.B >= min_b;
+}
+
+bool tc_available() { return encode_fn() != nullptr; }
+
+TcSizes tc_sizes(const MtpShape &s) {
+  TcSizes z{};
+  const int nb = batch_nb(s.B);
+  z.rows = (s.B + nb - 1) / nb * nb;
+  z.kmax = 2 * s.d;
+  if (s.Hq * s.Dh > z.kmax) z.kmax = s.Hq * s.Dh;
+  if (s.F > z.kmax) z.kmax = s.F;
+  DraftCtx c{};
+  c.d = s.d; c.Hq = s.Hq; c.Hkv = s.Hkv; c.Dh = s.Dh; c.F = s.F; c.V = s.V;
+  size_t part = (size_t)s.B * s.V;  // LM-head logits when the caller keeps none
+  for (int op = OP_FC; op <= OP_DOWN; ++op) {
+    const OpShape sh = op_shape(c, op);
+    int ks, kb_per;
+    op_splits(op_groups(sh, op_mt(batch_nb(s.B))), sh.K, &ks, &kb_per);
+    const size_t n = (size_t)ks * s.B * op_rows(sh);
+    if (n > part) part = n;
+  }
+  z.part_floats = part;
+  return z;
+}
+
+cudaError_t tc_set_attributes() {
+  return cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget + 2048);
+}
+
+namespace {
+
+// One GEMM: out[s][b][n] = W[n, K-range s] . a[b, K-range s] for every
+// 128-row tile of the op's weight blocks and every K split.
+cudaError_t run_gemm(const DraftCtx &c, const TcBufs &t, int op, float *out, size_t bstride, cudaStream_t s,
+                     bool pdl, int *ks_out) {
+  const OpShape sh = op_shape(c, op);
+  TcMaps maps{};
+  TcGemmArgs g{};
+  g.nmaps = sh.nmaps;
+  const int nb = batch_nb(c.B);
+  g.mt = op_mt(nb);
+  int base = 0, groups = 0;
+  for (int i = 0; i < sh.nmaps; ++i) {
+    if (!make_map(&maps.w[i], sh.w[i], (uint64_t)sh.K, (uint64_t)sh.rows[i], (uint64_t)sh.K, kTileM))
+      return cudaErrorInvalidValue;
+    g.rows[i] = sh.rows[i];
+    g.groups[i] = ((sh.rows[i] + kTileM - 1) / kTileM + g.mt - 1) / g.mt;
+    g.base[i] = base;
+    base += sh.rows[i];
+    groups += g.groups[i];
+  }
+  for (int tt = 0; tt < kTerms; ++tt)
+    if (!make_map(&maps.a[tt], t.a[tt], (uint64_t)sh.K, (uint64_t)t.rows, (uint64_t)t.kmax, (uint32_t)nb))
+      return cudaErrorInvalidValue;
+  int ks = 1, kb_per = sh.K / kBK;
+  if (op != OP_LMHEAD) {
+    op_splits(groups, sh.K, &ks, &kb_per);
+    while (ks > 1 && (size_t)ks * c.B * base > t.part_floats) {  // what the workspace holds
+      kb_per = (sh.K / kBK + ks - 2) / (ks - 1);
+      ks = (sh.K / kBK + kb_per - 1) / kb_per;
+    }
+  }
+  g.ks = ks;
+  g.kb_per = kb_per;
+  g.kbs = sh.K / kBK;
+  g.nb = nb;
+  g.stages = (int)(kSmemBudget / stage_bytes(nb, g.mt));
+  if (g.stages > 8) g.stages = 8;
+  g.B = c.B;
+  g.out = out;
+  g.sstride = (size_t)c.B * base;
+  g.bstride = bstride;
+  g.status = c.status;
+  const size_t smem = (size_t)g.stages * stage_bytes(nb, g.mt) + (size_t)(2 * g.stages + 1) * 8 + 16 + 1024;
+  *ks_out = ks;
+  cudaError_t e = cudaSuccess;
+  for (int r0 = 0; r0 < c.B && e == cudaSuccess; r0 += nb) {  // batch groups of nb rows
+    g.arow0 = r0;
+    e = launch(tc_gemm_kernel, dim3(groups * ks), kTcThreads, smem, s, pdl, maps, g);
+  }
+  return e;
+}
+
+}  // namespace
+
+// One depth in three phases (the caller times them separately): the block up
+// to the attention inputs, the block after the attention, the LM head with
+// the draft-token selection.
+cudaError_t run_block_pre_tc(const DraftCtx &c, const TcBufs &t, cudaStream_t s, bool pdl) {
+  const dim3 gb(c.B);
+  cudaError_t e;
+  int ks = 1;
+  const int nqkv = (c.Hq + 2 * c.Hkv) * c.Dh;
+  if ((e = launch(tc_prep_fc_kernel, gb, kPrepThreads, 0, s, pdl, c, t))) return e;
+  if ((e = run_gemm(c, t, OP_FC, t.part, (size_t)c.d, s, pdl, &ks))) return e;
+  if ((e = launch(tc_mid_kernel<OP_FC>, gb, kPrepThreads, 0, s, pdl, c, t, ks, c.d))) return e;
+  if ((e = run_gemm(c, t, OP_QKV, t.part, (size_t)nqkv, s, pdl, &ks))) return e;
+  return launch(tc_mid_kernel<OP_QKV>, gb, kPrepThreads, 0, s, pdl, c, t, ks, nqkv);
+}
+
+cudaError_t run_block_post_tc(const DraftCtx &c, const TcBufs &t, cudaStream_t s, bool pdl) {
+  const dim3 gb(c.B);
+  cudaError_t e;
+  int ks = 1;
+  if ((e = launch(tc_prep_wo_kernel, gb, kPrepThreads, 0, s, pdl, c, t))) return e;
+  if ((e = run_gemm(c, t, OP_WO, t.part, (size_t)c.d, s, pdl, &ks))) return e;
+  if ((e = launch(tc_mid_kernel<OP_WO>, gb, kPrepThreads, 0, s, pdl, c, t, ks, c.d))) return e;
+  if ((e = run_gemm(c, t, OP_GATEUP, t.part, (size_t)(2 * c.F), s, pdl, &ks))) return e;
+  if ((e = launch(tc_mid_kernel<OP_GATEUP>, gb, kPrepThreads, 0, s, pdl, c, t, ks, 2 * c.F))) return e;
+  if ((e = run_gemm(c, t, OP_DOWN, t.part, (size_t)c.d, s, pdl, &ks))) return e;
+  return launch(tc_mid_kernel<OP_DOWN>, gb, kPrepThreads, 0, s, pdl, c, t, ks, c.d);
+}
+
+cudaError_t run_lmhead_tc(const DraftCtx &c, const TcBufs &t, cudaStream_t s, bool pdl) {
+  // straight into the caller's logits when it keeps them
+  float *lg = c.logits ? c.logits + (size_t)c.j * c.V : t.part;
+  const size_t lstride = c.logits ? (size_t)c.k * c.V : (size_t)c.V;
+  int ks = 1;
+  cudaError_t e = run_gemm(c, t, OP_LMHEAD, lg, lstride, s, pdl, &ks);
+  if (e) return e;
+  return launch(tc_select_kernel, dim3(c.B), kSelThreads, 0, s, pdl, c, (const float *)lg, lstride);
+}
+
+}  // namespace mtp

@@ -171,28 +171,6 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait on an mbarrier phase that parks the warp (suspend-time hint)
-// instead of spinning; the hardware wakes it when the phase completes.
-__device__ __forceinline__ bool mbar_sleep_wait(uint64_t *bar, uint32_t parity, int *status) {
-  if (mbar_test(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (;;) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
-        : "memory");
-    if (ok) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      set_status(status, kStatusTimeout);
-      return false;
-    }
-  }
-}
-
 // 2^x, hardware approximation (relative error about 2^-22; -inf gives +0).
 __device__ __forceinline__ float ex2(float x) {
   float y;
