@@ -101,6 +101,7 @@ struct VerifyPlan {
   int grid;        // CTAs
   int pol;         // L2 policy of rows a rejection may re-read: 0 evict-last on
                    // position 0, 1 evict-normal on all, 2 evict-last on all
+  int p2_first;    // queue pass-2 items as soon as decided (else after the pass-1 claims)
 };
 
 // A stochastic sequence's decision, published for its pass-2 items.

@@ -1012,6 +1012,10 @@ __device__ void coordinator(const VerifyArgs &a, Shared &sh) {
     __syncwarp();
   };
 
+  // Pass-2 items normally wait until the pass-1 claims run out: they then fill
+  // the time the last sequences' decisions take instead of leaving it idle.
+  // MTP_VERIFY_P2_FIRST=1 queues them as soon as their sequence is decided.
+  const bool p2_first = a.p.p2_first != 0;
   uint32_t fill = 0, drain = 0;
   uint64_t idle_since = 0;
   for (;;) {
@@ -1032,7 +1036,7 @@ __device__ void coordinator(const VerifyArgs &a, Shared &sh) {
     }
     probe();
     if (fill - drain < (uint32_t)kQ) {
-      if (p2 == 2 && clock64() >= p2_at) {  // an owned pass-2 item whose sequence is decided goes first
+      if (p2 == 2 && clock64() >= p2_at && (claims_done || p2_first)) {  // a decided owned pass-2 item
         enqueue(fill, Item{2, owned_b(), 0, owned_u()});
         ++fill;
         ++t2;
@@ -1228,6 +1232,7 @@ bool plan_verify(int B, int k, int V, int mode, int num_sms, int blocks_per_sm, 
   q.m = m;
   q.n1 = q.nrows * q.U;
   q.pol = (int)env_int("MTP_VERIFY_POL", 0);
+  q.p2_first = (int)env_int("MTP_VERIFY_P2_FIRST", 0);
   const long long total = (long long)B * q.n1;
   if (total >= (1ll << 31)) return false;
   q.total = (unsigned)total;
