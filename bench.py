@@ -55,11 +55,18 @@ def lmhead_bytes(w, logits_out):
 # are unchanged; the summaries of the captures are kept under profiles/.
 NCU_TRAFFIC = {
     ("lm_head_gemv", "single_greedy_b1_d4096_v151936_ctx4096"): {
-        "bytes": 1244746240 + 2924800,
+        "bytes": 1244783104 + 3415296,
         "sources": {
-            "csrc/draft.cu": "79780104dbc932848f791ad1fc2472422a3f9590b82cf6fa3caf919609e8e453",
-            "csrc/draft_ops.cuh": "ee49d719a429f452c36d9668dfe63f0e031b4af814a8cad66a458d8eba41d1c3",
-            "csrc/common.cuh": "b0c0558dd02abe592f024b86032afd9c52bdeb68988177d7046fef9e10f74863",
+            "csrc/draft.cu": "7423ff25b2c3d53aa90b9ed37469d0bed9f9262144376e7cb33f369fb6a550ca",
+            "csrc/draft_ops.cuh": "5521f139698822af7da637dfe7303059c64bec5fd546cc7ae246193f2a491186",
+            "csrc/common.cuh": "fcd7bd8f56df32fc490b2c47f2fbc0f7f37047c578430d777438202c9279de66",
+        },
+    },
+    ("verify_kernel", "verify_sweep_b256_v151936_k3/greedy"): {
+        "bytes": 622444032 + 3472384,
+        "sources": {
+            "csrc/verify.cu": "297ef16365eabba513afa2d6433f63c98bee8f9829560493ca3a4d8017fc2291",
+            "csrc/common.cuh": "fcd7bd8f56df32fc490b2c47f2fbc0f7f37047c578430d777438202c9279de66",
         },
     },
 }
@@ -263,7 +270,9 @@ def run_verify_only(args, w):
             "vs_baseline": None, "dtype": "f32 logits", "data": "synthetic (seeded)", "config": config_of(w, args),
             "accept_len_mean": float(L.mean()),
             "roofline": {"bound": "hbm", "kernel": "verify_kernel", "achieved": ach, "peak": peak, "unit": "GB/s",
-                         "frac": ach / peak, "peak_kind": peak_kind, "traffic": None, "bytes_per_launch": vb,
+                         "frac": ach / peak, "peak_kind": peak_kind,
+                         "traffic": ncu_traffic("verify_kernel", f"{w.name}/{'greedy' if w.mode == W.GREEDY else 'stochastic'}"),
+                         "bytes_per_launch": vb,
                          "avg_launch_ms": ms, "launches": args.steps},
             "gpu_launches": int(launches), "clocks": clk}
     print(json.dumps(line), flush=True)
