@@ -25,7 +25,6 @@ struct DevInfo {
   bool init = false;
   int sms = 0;
   int max_cluster = 8;
-  int verify_bps = 1;  // verifier CTAs resident per SM
 };
 std::mutex g_mu;
 DevInfo g_dev[64];
@@ -40,7 +39,6 @@ int device_info(DevInfo *out) {
     di.max_cluster = 8;
     if (verify_set_attributes() != cudaSuccess) return MTP_ERR_CUDA;
     if (tc_set_attributes() != cudaSuccess) return MTP_ERR_CUDA;
-    di.verify_bps = verify_blocks_per_sm();
     di.init = true;
   }
   *out = di;
@@ -270,7 +268,7 @@ int prepare_verify(int B, int k, int V, float T, int mode, const float *target, 
   a->B = B; a->k = k; a->V = V; a->mode = mode; a->T = mode == MTP_STOCHASTIC ? T : 1.f;
   a->target = target; a->draft = draft; a->draft_tok = draft_tok; a->u_accept = u_accept; a->u_final = u_final;
   a->out_tok = out_tok; a->accept_len = accept_len; a->num_accepted = num_accepted;
-  if (!plan_verify(B, k, V, mode, di.sms, di.verify_bps, &a->p)) return MTP_ERR_UNSUPPORTED_SHAPE;
+  if (!plan_verify(B, k, V, &a->p)) return MTP_ERR_UNSUPPORTED_SHAPE;
   verify_bind_state(*a, state);
   return MTP_OK;
 }

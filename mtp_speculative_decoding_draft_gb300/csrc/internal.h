@@ -93,22 +93,10 @@ cudaError_t run_lmhead_tc(const DraftCtx &c, const TcBufs &t, cudaStream_t s, bo
 // Verification launch.
 struct VerifyPlan {
   int NS;          // 512-element sub-chunks per logit row
-  int m;           // sub-chunks per worker-warp slice of a chunk
-  int U;           // chunks (8 slices) per logit row
-  int nrows;       // logit rows per sequence: k+1 (greedy) or 2k+1 (stochastic)
-  int n1;          // work items per sequence (one per row and chunk)
-  unsigned total;  // work items
-  int grid;        // CTAs
-  int pol;         // L2 policy of rows a rejection may re-read: 0 evict-last on
-                   // position 0, 1 evict-normal on all, 2 evict-last on all
-  int p2_first;    // queue pass-2 items as soon as decided (else after the pass-1 claims)
-};
-
-// A stochastic sequence's decision, published for its pass-2 items.
-struct VerifyDecision {
-  int acc_n, rej, kind;  // kind 0: residual at rej; 2: bonus draw from row k
-  float uf;
-  float Mt, Ml, iZt, iZl;  // row maxima and reciprocal partition sums
+  int C;           // CTAs per cluster: each owns C-th of every row's sub-chunks
+  int G;           // clusters
+  int lookahead;   // items a cluster claims ahead of the one it streams
+  unsigned total;  // work items: one per position of one sequence
 };
 
 struct VerifyArgs {
@@ -124,23 +112,19 @@ struct VerifyArgs {
   int *num_accepted;     // [B]
   int *status;
   // state in the workspace: zero before the first call, left zero by each call
-  unsigned *ctl;          // [0] claim counter, [1] CTAs finished
-  unsigned *cnt1, *cnt2;  // [B] pass-1 / pass-2 tickets
-  unsigned *flag;         // [B] decision published
-  VerifyDecision *dec;    // [B]
-  float2 *part1;          // [B][nrows][U] published per-chunk partials
-  float2 *mass2;          // [B][NS] published sub-chunk sampling masses
+  unsigned *ctl;         // [0] claim counter, [1] CTAs finished
+  unsigned *hint;        // [B] k + 1 - (earliest position known to reject), or 0
+  unsigned long long *rec;  // [B, k+1] per position: flags | token << 32, 0 until written
   VerifyPlan p;
 };
 
-constexpr int kVerifyThreads = 320;  // 8 streaming worker warps, a coordinator and a decider warp
+constexpr int kVerifyThreads = 320;  // 4 streaming warps, a producer, a claimer and 4 decider warps
 
 size_t verify_state_bytes(int B, int k, int V);
 void verify_bind_state(VerifyArgs &a, void *state);
-bool plan_verify(int B, int k, int V, int mode, int num_sms, int blocks_per_sm, VerifyPlan *p);
+bool plan_verify(int B, int k, int V, VerifyPlan *p);
 cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s, bool pdl);
 cudaError_t verify_set_attributes();
-int verify_blocks_per_sm();
 
 // bookkeeping shared with api.cu
 void note_launch();
