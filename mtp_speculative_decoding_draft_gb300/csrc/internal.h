@@ -118,8 +118,6 @@ struct VerifyArgs {
   VerifyPlan p;
 };
 
-constexpr int kVerifyThreads = 320;  // 4 streaming warps, a producer, a claimer and 4 decider warps
-
 size_t verify_state_bytes(int B, int k, int V);
 void verify_bind_state(VerifyArgs &a, void *state);
 bool plan_verify(int B, int k, int V, VerifyPlan *p);

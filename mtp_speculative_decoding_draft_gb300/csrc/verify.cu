@@ -5,7 +5,7 @@
 //
 // Work items, one per position of one sequence, in position-major order:
 //  greedy      row t_j, j = 0..k            -> its (max, lowest argmax);
-//  stochastic  the bonus row t_k first, then the pair (t_j, q_j), j < k.
+//  stochastic  the pair (t_j, q_j), j < k, then the bonus row t_k.
 //              A pair yields the ratio test at j and, when the test rejects,
 //              the inverse-CDF draw from max(0, p_j - q_j); the bonus row
 //              yields the draw from p_k.
@@ -17,18 +17,20 @@
 // items raise); the item of the position claimed last gathers the
 // positions' records, picks the first rejection and writes the outputs.
 //
-// Inside a CTA: a producer lane streams the CTA's sub-chunks through a ring of
-// 4 KB shared-memory stages with 1-D bulk copies; four worker warps reduce
-// each stage (per sub-chunk max and sum of exp2, or argmax) and, for a
-// rejecting pair, re-read the pair -- still in L2, a few microseconds after
-// the first read -- for the per-sub-chunk sampling weights; four decider
-// warps, item n going to decider n mod 4, combine the sub-chunks, exchange
-// the CTA partials with the other CTAs of the cluster through distributed
-// shared memory (a remote store and a remote mbarrier arrive per peer), take
-// the decision and, for a draw, locate the crossing CTA, sub-chunk and
-// element (the last 512 elements rescanned in float64).  A claimer warp of
-// the cluster's first CTA takes items from one global counter, a few ahead
-// of its producer, and hands them to every CTA of the cluster.
+// Inside a CTA: a producer warp streams the CTA's sub-chunks through a ring
+// of 8 KB shared-memory stages with 1-D bulk copies (up to eight stages at a
+// time, one per lane; a row piece is 4 sub-chunks of one row in one copy);
+// five worker warps take the stages round-robin and reduce them (per
+// sub-chunk max and sum of exp2, or argmax) and, for a rejecting pair,
+// re-read the pair -- a few microseconds after the first read, partly from
+// L2 -- for the per-sub-chunk sampling weights; three decider warps, item n
+// going to decider n mod 3, combine the sub-chunks, exchange the CTA partials
+// with the other CTAs of the cluster through distributed shared memory (a
+// remote store and a remote mbarrier arrive per peer), take the decision and,
+// for a draw, locate the crossing CTA, sub-chunk and element (the last 512
+// elements rescanned in float64).  A claimer warp of the cluster's first CTA
+// takes items from one global counter, a few ahead of its producer, and hands
+// them to every CTA of the cluster.
 //
 // No result depends on which cluster ran which item.  Every wait is bounded
 // and gives up (flagging the status word) once any thread has timed out.
@@ -45,13 +47,22 @@ namespace mtp {
 namespace {
 
 constexpr int kSub = 512;        // sub-chunk: elements of one stage part
-constexpr int kWorkers = 4;      // streaming warps
-constexpr int kDeciders = 4;     // decision warps
+#ifndef MTP_VERIFY_WORKERS
+#define MTP_VERIFY_WORKERS 5
+#endif
+constexpr int kWorkers = MTP_VERIFY_WORKERS;  // streaming warps
+#ifndef MTP_VERIFY_DECIDERS
+#define MTP_VERIFY_DECIDERS 3
+#endif
+constexpr int kDeciders = MTP_VERIFY_DECIDERS;  // decision warps
 constexpr int kProducerWarp = kWorkers;
 constexpr int kClaimerWarp = kWorkers + 1;
 constexpr int kFirstDecider = kWorkers + 2;
-static_assert(kVerifyThreads == 32 * (kWorkers + 2 + kDeciders), "warp roles");
-constexpr int kQD = 8;           // item slots per CTA
+constexpr int kVerifyThreads = 32 * (kWorkers + 2 + kDeciders);
+#ifndef MTP_VERIFY_QD
+#define MTP_VERIFY_QD 9
+#endif
+constexpr int kQD = MTP_VERIFY_QD;  // item slots per CTA
 static_assert(kQD % kDeciders == 0, "a slot always goes to the same decider");
 #ifndef MTP_VERIFY_STAGES
 #define MTP_VERIFY_STAGES 11
@@ -60,12 +71,15 @@ constexpr int kStages = MTP_VERIFY_STAGES;  // ring stages
 constexpr int kStageF = 4 * kSub;           // floats per stage (8 KB)
 constexpr int kRowSubs = 4;                 // sub-chunks of one row per stage
 constexpr int kPairSubs = 2;                // sub-chunks of each of two rows per stage
-constexpr int kMaxP = 64;        // sub-chunks per CTA slice, at most
+#ifndef MTP_VERIFY_MAXP
+#define MTP_VERIFY_MAXP 64
+#endif
+constexpr int kMaxP = MTP_VERIFY_MAXP;  // sub-chunks per CTA slice, at most
 constexpr int kMaxC = 16;        // CTAs per cluster, at most
 constexpr unsigned kFull = 0xffffffffu;
 
 enum : int { kItemStop = 0, kItemGreedy = 1, kItemPair = 2, kItemBonus = 3 };
-enum : int { kPieceStop = 0, kPieceRow = 1, kPiecePair = 2, kPieceWeights = 3 };
+enum : int { kPieceStop = 0, kPieceRow = 1, kPieceRowDraft = 2, kPieceWeights = 3 };
 // bits of a position's record word
 constexpr int kRecAccept = 1, kRecBadToken = 2, kRecNonFinite = 4, kRecWritten = 8;
 
@@ -80,9 +94,9 @@ struct Xchg {
   int i0, i1;     // argmax, rejection hint, or last sub-chunk with positive weight
 };
 
-// What one ring stage holds: local sub-chunks p .. p+np-1 of the item's row (a
-// row piece, up to 4), or of its target and draft rows (a pair or weight
-// piece, up to 2 of each, the draft span in the stage's second half).  Each
+// What one ring stage holds: local sub-chunks p .. p+np-1 (up to 4) of the
+// item's target or draft row (a row piece), or of both rows (a weight piece,
+// up to 2 of each, the draft span in the stage's second half).  Each
 // span's 16-byte aligned body arrives by one bulk copy; an unaligned head or
 // tail is read from global memory by the worker.
 struct Tag {
@@ -94,8 +108,9 @@ struct Tag {
 struct SlotState {
   ItemInfo info;           // written by the cluster's first CTA
   float Mt, Ml, iZt, iZl;  // normalisers of the sampling weights
-  float4 stats[kMaxP];     // per sub-chunk: (max, sum | argmax) of rows 0 and 1
-  float2 mass[kMaxP];      // per sub-chunk: residual and target weight sums
+  // per sub-chunk: (max, sum | argmax) of rows 0 and 1; once a pair's
+  // statistics are combined, .xy takes its residual and target weight sums
+  float4 stats[kMaxP];
   Xchg x1[kMaxC], x2[kMaxC];
 };
 
@@ -234,10 +249,13 @@ struct Span {
 __device__ __forceinline__ Span stage_span(const VerifyArgs &a, const ItemInfo &it, int kind, int s0, int p, int np,
                                            int q) {
   Span sp{nullptr, 0, 0, 0, 0};
-  if (kind == kPiecePair || kind == kPieceWeights)
-    sp.row = q == 0 ? a.target + ((size_t)it.b * (a.k + 1) + it.j) * a.V : a.draft + ((size_t)it.b * a.k + it.j) * a.V;
+  const float *trow = a.target + ((size_t)it.b * (a.k + 1) + it.j) * a.V;
+  if (kind == kPieceWeights)
+    sp.row = q == 0 ? trow : a.draft + ((size_t)it.b * a.k + it.j) * a.V;
   else if (kind == kPieceRow && q == 0)
-    sp.row = a.target + ((size_t)it.b * (a.k + 1) + it.j) * a.V;
+    sp.row = trow;
+  else if (kind == kPieceRowDraft && q == 0)
+    sp.row = a.draft + ((size_t)it.b * a.k + it.j) * a.V;
   if (sp.row) {
     sp.e0 = (s0 + p) * kSub;
     sp.n = min(np * kSub, a.V - sp.e0);
@@ -270,6 +288,10 @@ __device__ __forceinline__ void load_sub(const float *buf, const Span &sp, int i
       x[m] = e >= sp.n ? fill : (e < h || e >= h + L) ? __ldcg(row + e) : buf[e - h];
     }
   }
+}
+
+__device__ __forceinline__ void mbar_arrive_n(uint64_t *bar, uint32_t n) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(n) : "memory");
 }
 
 // Warp maximum of a float in one instruction (-inf for an empty warp maximum).
@@ -321,6 +343,18 @@ __device__ __forceinline__ void part_lse2(const float (&x)[16], const float (&y)
   ry = make_float2(my, sy);
 }
 
+// Four warp sums with their shuffle rounds interleaved.
+__device__ __forceinline__ void warp_sum4(float (&v)[4]) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float t[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) t[q] = __shfl_xor_sync(kFull, v[q], o);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] += t[q];
+  }
+}
+
 // (max, lowest index) of a part over the warp; e0 is the part's first element.
 __device__ __forceinline__ float2 part_argmax(const float (&x)[16], int e0) {
   const int lane = threadIdx.x & 31;
@@ -340,24 +374,15 @@ __device__ __forceinline__ const float *draft_row(const VerifyArgs &a, int b, in
   return a.draft + ((size_t)b * a.k + j) * a.V;
 }
 
-// Item idx in position-major order.
+// Item idx in position-major order: position j = idx / B of sequence idx % B;
+// in stochastic mode positions 0..k-1 are pairs and position k the bonus row.
 __device__ __forceinline__ ItemInfo decode(const VerifyArgs &a, unsigned idx) {
   ItemInfo it{kItemStop, 0, 0, 0};
   if (idx >= a.p.total) return it;
   const unsigned B = (unsigned)a.B;
-  if (a.mode == 0) {
-    it.kind = kItemGreedy;
-    it.j = (int)(idx / B);
-    it.b = (int)(idx % B);
-  } else if (idx < B) {
-    it.kind = kItemBonus;
-    it.b = (int)idx;
-    it.j = a.k;
-  } else {
-    it.kind = kItemPair;
-    it.j = (int)((idx - B) / B);
-    it.b = (int)((idx - B) % B);
-  }
+  it.j = (int)(idx / B);
+  it.b = (int)(idx % B);
+  it.kind = a.mode == 0 ? kItemGreedy : (it.j < a.k ? kItemPair : kItemBonus);
   return it;
 }
 
@@ -373,7 +398,7 @@ __device__ void producer(const VerifyArgs &a, Shared &sh, float *ring, int s0, i
   uint32_t g = 0, n = 0, bq_head = 0;
   bool ok = true, have = false, stopped = false, dep = false;
   ItemInfo it{};
-  int pn = 0;
+  int pn = 0, half = 0;  // next sub-chunk of the current row; 1 on a pair's draft row
   uint64_t t_idle = 0;
 
   // m pieces of one kind: piece i covers local sub-chunks pbase + i * pstep
@@ -435,6 +460,7 @@ __device__ void producer(const VerifyArgs &a, Shared &sh, float *ring, int s0, i
           }
           have = true;
           pn = 0;
+          half = 0;
           if (it.kind == kItemPair && !dep) {
             grid_dep_wait();  // the draft rows come from the drafter
             dep = true;
@@ -457,15 +483,20 @@ __device__ void producer(const VerifyArgs &a, Shared &sh, float *ring, int s0, i
         continue;
       }
     }
+    // a pair streams its target row, then its draft row
     const int slot = (int)(n % kQD);
     const bool pair = it.kind == kItemPair;
-    const int step = pair ? kPairSubs : kRowSubs;
-    const int m = min(kBatch, (P - pn + step - 1) / step);
-    ok = issue_batch(m, pair ? kPiecePair : kPieceRow, slot, it, pn, step, pair ? pol_norm : pol_first);
-    pn += m * step;
+    const int m = min(kBatch, (P - pn + kRowSubs - 1) / kRowSubs);
+    ok = issue_batch(m, half ? kPieceRowDraft : kPieceRow, slot, it, pn, kRowSubs, pair ? pol_norm : pol_first);
+    pn += m * kRowSubs;
     if (pn >= P) {
-      have = false;
-      ++n;
+      if (pair && half == 0) {
+        half = 1;
+        pn = 0;
+      } else {
+        have = false;
+        ++n;
+      }
     }
   }
   if (ok) ok = issue_batch(kWorkers, kPieceStop, 0, it, 0, 0, 0);
@@ -517,27 +548,38 @@ __device__ void worker(const VerifyArgs &a, Shared &sh, const float *ring, int w
     SlotState &ss = sh.slot[t.slot];
     const ItemInfo inf = ss.info;
     const Span s0p = stage_span(a, inf, t.kind, s0, t.p, t.np, 0);
-    if (t.kind == kPieceRow) {
-      // sub-chunks two at a time, their reductions interleaved
-      for (int i = 0; i < t.np; i += 2) {
-        float x[16], y[16];
-        load_sub(buf, s0p, i, -INFINITY, x);
-        load_sub(buf, s0p, i + 1, -INFINITY, y);  // all -inf past the piece's end
-        float2 r0, r1;
-        if (greedy) {
-          r0 = part_argmax(x, s0p.e0 + i * kSub);
-          r1 = part_argmax(y, s0p.e0 + (i + 1) * kSub);
-        } else {
-          part_lse2(x, y, c, r0, r1);
-        }
-        if (lane == 0) {
-          ss.stats[t.p + i] = make_float4(r0.x, r0.y, 0.f, 0.f);
-          mbar_arrive(&sh.adone[t.slot]);
-          if (i + 1 < t.np) {
-            ss.stats[t.p + i + 1] = make_float4(r1.x, r1.y, 0.f, 0.f);
-            mbar_arrive(&sh.adone[t.slot]);
+    if (t.kind == kPieceRow || t.kind == kPieceRowDraft) {
+      // a row's sub-chunks two at a time, their reductions interleaved; the
+      // first-pass barrier counts two arrivals per sub-chunk: one per row of a
+      // pair, two for a lone row
+      const int half = t.kind == kPieceRowDraft ? 1 : 0;
+      const uint32_t cnt = inf.kind == kItemPair ? 1u : 2u;
+      // all four sub-chunks at once (past the piece's end: -inf), so that
+      // their reductions overlap
+      float x[4][16];
+#pragma unroll
+      for (int i = 0; i < kRowSubs; ++i) load_sub(buf, s0p, i, -INFINITY, x[i]);
+      float2 r[4];
+      if (greedy) {
+#pragma unroll
+        for (int i = 0; i < kRowSubs; ++i) r[i] = part_argmax(x[i], s0p.e0 + i * kSub);
+      } else {
+        float m[4], sm[4];
+#pragma unroll
+        for (int i = 0; i < kRowSubs; ++i) m[i] = redux_max(lane_max16(x[i]));
+#pragma unroll
+        for (int i = 0; i < kRowSubs; ++i) sm[i] = lane_sumexp16(x[i], m[i], c);
+        warp_sum4(sm);
+#pragma unroll
+        for (int i = 0; i < kRowSubs; ++i) r[i] = make_float2(m[i], sm[i]);
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < kRowSubs; ++i)
+          if (i < t.np) {
+            reinterpret_cast<float2 *>(&ss.stats[t.p + i])[half] = r[i];
+            mbar_arrive_n(&sh.adone[t.slot], cnt);
           }
-        }
       }
     } else {
       const Span s1p = stage_span(a, inf, t.kind, s0, t.p, t.np, 1);
@@ -547,25 +589,16 @@ __device__ void worker(const VerifyArgs &a, Shared &sh, const float *ring, int w
         float x[16], y[16];
         load_sub(buf, s0p, i, -INFINITY, x);
         load_sub(buf1, s1p, i, -INFINITY, y);
-        if (t.kind == kPiecePair) {
-          float2 rt, rl;
-          part_lse2(x, y, c, rt, rl);
-          if (lane == 0) {
-            ss.stats[t.p + i] = make_float4(rt.x, rt.y, rl.x, rl.y);
-            mbar_arrive(&sh.adone[t.slot]);
-          }
-        } else {
-          float sr = 0.f, sp = 0.f;
+        float sr = 0.f, sp = 0.f;
 #pragma unroll
-          for (int m = 0; m < 16; ++m) {
-            sr += weight(0, x[m], y[m], Mt, Ml, iZt, iZl, c);
-            sp += weight(1, x[m], y[m], Mt, Ml, iZt, iZl, c);
-          }
-          warp_sum2(sr, sp);
-          if (lane == 0) {
-            ss.mass[t.p + i] = make_float2(sr, sp);
-            mbar_arrive(&sh.bdone[t.slot]);
-          }
+        for (int m = 0; m < 16; ++m) {
+          sr += weight(0, x[m], y[m], Mt, Ml, iZt, iZl, c);
+          sp += weight(1, x[m], y[m], Mt, Ml, iZt, iZl, c);
+        }
+        warp_sum2(sr, sp);
+        if (lane == 0) {
+          reinterpret_cast<float2 *>(&ss.stats[t.p + i])[0] = make_float2(sr, sp);
+          mbar_arrive(&sh.bdone[t.slot]);
         }
       }
     }
@@ -721,9 +754,8 @@ __device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned l
   asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-// The position of a sequence claimed last: the bonus rows come first in
-// stochastic mode, so it is k-1 there and k in greedy mode.
-__device__ __forceinline__ int last_position(const VerifyArgs &a) { return a.mode == 0 ? a.k : a.k - 1; }
+// The position of a sequence claimed last: k (the bonus row in stochastic mode).
+__device__ __forceinline__ int last_position(const VerifyArgs &a) { return a.k; }
 
 // Record position j's outcome (flags, token) as one 64-bit word.  The item of
 // the position claimed last also gathers the other positions' words (lane l
@@ -908,8 +940,8 @@ __device__ void decider(const VerifyArgs &a, Shared &sh, int d, int rank, int C,
       ok = wait_phase<false>(&sh.bdone[s], (bpar >> s) & 1u, a.status);
       bpar ^= 1u << s;
       if (!__all_sync(kFull, ok)) break;
-      const double r0 = p0 < P ? (double)ss.mass[p0].x : 0.0, r1 = p1 < P ? (double)ss.mass[p1].x : 0.0;
-      const double q0 = p0 < P ? (double)ss.mass[p0].y : 0.0, q1 = p1 < P ? (double)ss.mass[p1].y : 0.0;
+      const double r0 = p0 < P ? (double)ss.stats[p0].x : 0.0, r1 = p1 < P ? (double)ss.stats[p1].x : 0.0;
+      const double q0 = p0 < P ? (double)ss.stats[p0].y : 0.0, q1 = p1 < P ? (double)ss.stats[p1].y : 0.0;
       mine2.z0 = __shfl_sync(kFull, warp_incl_scan_d(r0 + r1), 31);
       mine2.z1 = __shfl_sync(kFull, warp_incl_scan_d(q0 + q1), 31);
       mine2.i0 = warp_max_i(r1 > 0.0 ? s0 + p1 : (r0 > 0.0 ? s0 + p0 : -1));
@@ -949,10 +981,10 @@ __device__ void decider(const VerifyArgs &a, Shared &sh, int d, int rank, int C,
         chosen = draw_in_slice(a, bonus_mass, P, s0, cross != 0u, before, tgt, slast, wk, rt, rl, Mt, Ml, iZt, iZl,
                                c);
       } else if (use_p) {
-        auto pm = [&](int p) -> double { return (double)ss.mass[p].y; };
+        auto pm = [&](int p) -> double { return (double)ss.stats[p].y; };
         chosen = draw_in_slice(a, pm, P, s0, cross != 0u, before, tgt, slast, wk, rt, rl, Mt, Ml, iZt, iZl, c);
       } else {
-        auto rm = [&](int p) -> double { return (double)ss.mass[p].x; };
+        auto rm = [&](int p) -> double { return (double)ss.stats[p].x; };
         chosen = draw_in_slice(a, rm, P, s0, cross != 0u, before, tgt, slast, wk, rt, rl, Mt, Ml, iZt, iZl, c);
       }
       if (chosen < 0) {
@@ -990,7 +1022,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(VerifyArgs a)
     for (int i = 0; i < kQD; ++i) {
       mbar_init(&sh.item_full[i], 1);
       mbar_init(&sh.item_empty[i], C);
-      mbar_init(&sh.adone[i], P);
+      mbar_init(&sh.adone[i], 2 * P);
       mbar_init(&sh.bdone[i], P);
       mbar_init(&sh.x1bar[i], C);
       mbar_init(&sh.x2bar[i], C);
@@ -1080,7 +1112,7 @@ void verify_bind_state(VerifyArgs &a, void *state) {
 bool plan_verify(int B, int k, int V, VerifyPlan *p) {
   VerifyPlan q{};
   q.NS = sub_chunks(V);
-  int C = (int)env_int("MTP_VERIFY_C", 8);
+  int C = (int)env_int("MTP_VERIFY_C", 6);
   C = std::max(1, std::min(kMaxC, C));
   while (C < kMaxC && (q.NS + C - 1) / C > kMaxP) ++C;
   C = std::min(C, q.NS);
