@@ -63,9 +63,16 @@ NCU_TRAFFIC = {
         },
     },
     ("verify_kernel", "verify_sweep_b256_v151936_k3/greedy"): {
-        "bytes": 622444032 + 3472384,
+        "bytes": 622490880 + 3303680,
         "sources": {
-            "csrc/verify.cu": "297ef16365eabba513afa2d6433f63c98bee8f9829560493ca3a4d8017fc2291",
+            "csrc/verify.cu": "4f9309d361b99df630507ea36fb54694c9eba1421090f06589088e4d4c20f9cd",
+            "csrc/common.cuh": "fcd7bd8f56df32fc490b2c47f2fbc0f7f37047c578430d777438202c9279de66",
+        },
+    },
+    ("verify_kernel", "verify_sweep_b256_v151936_k3/stochastic"): {
+        "bytes": 1297813760 + 3417088,
+        "sources": {
+            "csrc/verify.cu": "4f9309d361b99df630507ea36fb54694c9eba1421090f06589088e4d4c20f9cd",
             "csrc/common.cuh": "fcd7bd8f56df32fc490b2c47f2fbc0f7f37047c578430d777438202c9279de66",
         },
     },
