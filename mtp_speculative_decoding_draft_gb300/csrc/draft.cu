@@ -672,6 +672,7 @@ static cudaError_t launch_attn_g(const DraftCtx &c, int cluster, cudaStream_t s,
 }
 
 cudaError_t launch_attention(const DraftCtx &c, int cluster, cudaStream_t s, bool pdl) {
+  if (attention_tc_shape_ok(c)) return launch_attention_tc(c, cluster, s, pdl);
   switch (c.Dh) {
     case 32: return launch_attn_g<32>(c, cluster, s, pdl);
     case 64: return launch_attn_g<64>(c, cluster, s, pdl);

@@ -66,6 +66,9 @@ cudaError_t launch_gemv(const DraftCtx &c, const GemvPlan &g, cudaStream_t s, bo
 cudaError_t launch_attention(const DraftCtx &c, int cluster, cudaStream_t s, bool pdl);
 size_t attention_smem_bytes(int Dh);
 int attention_cluster_size(int ctx_max, int pairs, int num_sms, int max_cluster);
+// Tensor-core decode attention (GQA groups of 2..16, head size 64 or 128).
+bool attention_tc_shape_ok(const DraftCtx &c);
+cudaError_t launch_attention_tc(const DraftCtx &c, int cluster, cudaStream_t s, bool pdl);
 
 // Tensor-core path of the draft chain (batches of several sequences).
 struct MtpShape {

@@ -475,6 +475,14 @@ __global__ void __launch_bounds__(kSelThreads) tc_select_kernel(DraftCtx c, cons
 
 namespace {
 
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
+
+}  // namespace
+
+bool make_bf16_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t ld, uint32_t box_rows);
+
+namespace {
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -489,9 +497,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+bool make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t ld, uint32_t box_rows) {
+  return make_bf16_map(m, base, cols, rows, ld, box_rows);
+}
+
+}  // namespace
+
 // 2-D bf16 map over a row-major [rows, cols] matrix with row stride ld
 // (elements), boxes of box_rows x 64 columns, 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t ld, uint32_t box_rows) {
+bool make_bf16_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t ld, uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {cols, rows};
@@ -502,6 +516,8 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, ui
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 struct OpShape {
   int nmaps;

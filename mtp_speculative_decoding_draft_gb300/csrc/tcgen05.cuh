@@ -9,6 +9,11 @@
 
 namespace mtp {
 
+// Host: a 2-D bf16 tensor map over a row-major [rows, cols] matrix with row
+// stride ld (elements), boxes of box_rows x 64 columns, 128-byte swizzle;
+// false if the driver's encoder is unavailable or rejects the shape.
+bool make_bf16_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t ld, uint32_t box_rows);
+
 // 2-D tiled TMA load of box {x .. x+box0, y .. y+box1} into shared memory,
 // completing on `bar`; x is the innermost (contiguous) coordinate in elements.
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
