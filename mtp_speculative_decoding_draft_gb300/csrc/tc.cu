@@ -373,102 +373,167 @@ __global__ void __launch_bounds__(kPrepThreads) tc_mid_kernel(DraftCtx c, TcBufs
 // owns a contiguous segment, the segments' masses are scanned in float64 in
 // vocabulary order and the warp holding the crossing rescans its segment 32
 // elements at a time with a float64 warp scan.
-constexpr int kSelThreads = 512;
-__global__ void __launch_bounds__(kSelThreads) tc_select_kernel(DraftCtx c, const float *logits, size_t bstride) {
-  constexpr int NW = kSelThreads / 32;
-  __shared__ float sv[NW];
-  __shared__ int si[NW];
-  __shared__ double sd[NW];
-  __shared__ int s_last[NW];
-  const int b = blockIdx.x, V = c.V, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// Draft-token selection over the batch's logits rows, in two launches.
+// tc_select_part_kernel: one CTA per 4096 elements of a row, a warp per
+// 1024-element sub-segment: its (max, lowest argmax) and, in stochastic mode,
+// sum exp2((x - max) c).  tc_select_fin_kernel: one warp per sequence
+// combines the sub-segments in order -- the argmax, or the inverse CDF of
+// softmax(x / T) at u_draft: float64 sub-segment masses, the crossing
+// sub-segment rescanned in float64 (each lane a contiguous run of 32).
+constexpr int kSelSub = 1024;
+constexpr int kSelWarps = 4;
+constexpr int kSelThreads = 32 * kSelWarps;
+
+__host__ __device__ inline int sel_subs(int V) { return (V + kSelSub - 1) / kSelSub; }
+
+__global__ void __launch_bounds__(kSelThreads) tc_select_part_kernel(DraftCtx c, const float *logits, size_t bstride,
+                                                                     float4 *part) {
+  const int b = blockIdx.y, V = c.V, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int q = blockIdx.x * kSelWarps + warp, nq = sel_subs(V);
   grid_dep_wait();
   grid_dep_launch();
+  if (q >= nq) return;
   const float *row = logits + (size_t)b * bstride;
+  const int e0 = q * kSelSub, n = min(kSelSub, V - e0);
+  float x[32];
+  if ((reinterpret_cast<uintptr_t>(row + e0) & 15u) == 0 && n == kSelSub) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 v = __ldcg(reinterpret_cast<const float4 *>(row + e0) + lane + 32 * i);
+      x[4 * i] = v.x;
+      x[4 * i + 1] = v.y;
+      x[4 * i + 2] = v.z;
+      x[4 * i + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = 4 * (lane + 32 * i) + u;
+        x[4 * i + u] = e < n ? __ldcg(row + e0 + e) : -INFINITY;
+      }
+  }
+  // element 4 (lane + 32 i) + u of the sub-segment is x[4 i + u]
   float M = -INFINITY;
   int I = 0x7fffffff;
-  for (int i = tid; i < V; i += kSelThreads) {
-    const float x = __ldcg(row + i);
-    if (x > M) {  // ascending i per thread: the first maximum is the lowest index
-      M = x;
-      I = i;
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (x[i] > M) {  // ascending element order per lane: the first maximum stays
+      M = x[i];
+      I = e0 + 4 * (lane + 32 * (i >> 2)) + (i & 3);
     }
-  }
   warp_argmax(M, I);
-  if (lane == 0) {
-    sv[warp] = M;
-    si[warp] = I;
+  float sum = 0.f;
+  if (c.mode == 1 && M != -INFINITY) {
+    const float cT = kLog2e / c.T, mc = M * cT;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) sum += exp2f(fmaf(x[i], cT, -mc));
+    sum = warp_sum(sum);
   }
-  __syncthreads();
-  M = -INFINITY;
-  I = 0x7fffffff;
-  for (int w = 0; w < NW; ++w) argmax_merge(M, I, sv[w], si[w]);
+  if (lane == 0) part[(size_t)b * nq + q] = make_float4(M, __int_as_float(I), sum, 0.f);
+}
+
+__global__ void __launch_bounds__(32) tc_select_fin_kernel(DraftCtx c, const float *logits, size_t bstride,
+                                                           const float4 *part) {
+  const int b = blockIdx.x, V = c.V, lane = threadIdx.x, nq = sel_subs(V);
+  grid_dep_wait();
+  grid_dep_launch();
+  const float4 *pp = part + (size_t)b * nq;
+  // lane l owns sub-segments [l per, (l+1) per) in order
+  const int per = (nq + 31) / 32, q0 = min(nq, lane * per), q1 = min(nq, q0 + per);
+  float M = -INFINITY;
+  int I = 0x7fffffff;
+  for (int q = q0; q < q1; ++q) argmax_merge(M, I, pp[q].x, __float_as_int(pp[q].y));
+  warp_argmax(M, I);
   int tok = I;
   if (M == -INFINITY || !(M == M)) {
-    if (tid == 0) set_status(c.status, kStatusNonFinite);
+    if (lane == 0) set_status(c.status, kStatusNonFinite);
     tok = 0;
   } else if (c.mode == 1) {
     const float cT = kLog2e / c.T;
-    const int seg = ((V + NW - 1) / NW + 31) / 32 * 32;
-    const int s0 = min(V, warp * seg), s1 = min(V, s0 + seg);
-    float own = 0.f;
-    int lastpos = -1;
-    for (int i = s0 + lane; i < s1; i += 32) {
-      const float w = exp2f((__ldcg(row + i) - M) * cT);
-      own += w;
-      if (w > 0.f) lastpos = i;
+    double own = 0.0;
+    int lastq = -1;
+    for (int q = q0; q < q1; ++q) {
+      const float4 v = pp[q];
+      const double m = v.x == -INFINITY ? 0.0 : (double)v.z * (double)exp2f((v.x - M) * cT);
+      own += m;
+      if (m > 0.0) lastq = q;
     }
-    const double segsum = warp_sum_d((double)own);
-    int lp = lastpos;
+    double incl = own;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
-    if (lane == 0) {
-      sd[warp] = segsum;
-      s_last[warp] = lp;
+    for (int o = 1; o < 32; o <<= 1) {
+      const double t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
     }
-    __syncthreads();
-    double Z = 0.0;
-    int last = -1;
-    for (int w = 0; w < NW; ++w) {
-      Z += sd[w];
-      last = max(last, s_last[w]);
-    }
+    const double Z = __shfl_sync(0xffffffffu, incl, 31);
     const double target = (double)__ldg(&c.u_draft[b * c.k + c.j]) * Z;
+    int qs = -1;
     double before = 0.0;
-    int wstar = -1;
-    for (int w = 0; w < NW; ++w) {
-      if (wstar < 0 && before + sd[w] > target) wstar = w;
-      if (wstar < 0) before += sd[w];
-    }
-    __shared__ int s_found;
-    if (tid == 0) s_found = 0x7fffffff;
-    __syncthreads();
-    if (warp == wstar) {
-      double cum = before;
-      bool hit_any = false;
-      for (int i0 = s0; i0 < s1; i0 += 32) {
-        const int i = i0 + lane;
-        const double w = i < s1 ? (double)exp2f((__ldcg(row + i) - M) * cT) : 0.0;
-        double incl = w;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const double v = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += v;
+    const unsigned cross = __ballot_sync(0xffffffffu, q1 > q0 && incl > target);
+    if (cross) {
+      const int cl = __ffs(cross) - 1;
+      if (lane == cl) {
+        double cum = incl - own;
+        for (int q = q0; q < q1; ++q) {
+          const float4 v = pp[q];
+          const double m = v.x == -INFINITY ? 0.0 : (double)v.z * (double)exp2f((v.x - M) * cT);
+          if (cum + m > target) {
+            qs = q;
+            before = cum;
+            break;
+          }
+          cum += m;
         }
-        const unsigned hit = __ballot_sync(0xffffffffu, i < s1 && cum + incl > target);
-        if (hit) {
-          if (lane == 0) s_found = i0 + __ffs(hit) - 1;
-          hit_any = true;
-          break;
-        }
-        cum += __shfl_sync(0xffffffffu, incl, 31);
       }
-      // rounding left the crossing past this segment's rescan: its last positive index
-      if (!hit_any && lane == 0) s_found = s_last[warp] >= 0 ? s_last[warp] : 0x7fffffff;
+      qs = __shfl_sync(0xffffffffu, qs, cl);
+      before = __shfl_sync(0xffffffffu, before, cl);
     }
-    __syncthreads();
-    tok = s_found != 0x7fffffff ? s_found : (last >= 0 ? last : I);
+    int ql = lastq;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ql = max(ql, __shfl_xor_sync(0xffffffffu, ql, o));
+    const bool crossing = qs >= 0;
+    const int qr = crossing ? qs : ql;
+    int found = 0x7fffffff, lastpos = -1;
+    if (qr >= 0) {
+      // rescan sub-segment qr: lane l takes elements [32 l, 32 l + 32), float64
+      const float *row = logits + (size_t)b * bstride;
+      const int e0 = qr * kSelSub, n = min(kSelSub, V - e0);
+      float w[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int e = 32 * lane + i;
+        w[i] = e < n ? exp2f((__ldcg(row + e0 + e) - M) * cT) : 0.f;
+      }
+      double ls = 0.0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        ls += (double)w[i];
+        if (w[i] > 0.f) lastpos = e0 + 32 * lane + i;
+      }
+      double inc = ls;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+      }
+      if (crossing && before + inc > target) {
+        double run = before + (inc - ls);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          run += (double)w[i];
+          if (found == 0x7fffffff && run > target && 32 * lane + i < n) found = e0 + 32 * lane + i;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        found = min(found, __shfl_xor_sync(0xffffffffu, found, o));
+        lastpos = max(lastpos, __shfl_xor_sync(0xffffffffu, lastpos, o));
+      }
+    }
+    tok = found != 0x7fffffff ? found : (lastpos >= 0 ? lastpos : I);
   }
-  if (tid == 0) c.draft_tok[b * c.k + c.j] = tok;
+  if (lane == 0) c.draft_tok[b * c.k + c.j] = tok;
 }
 
 // ---------------------------------------------------------------- host side
@@ -627,7 +692,8 @@ TcSizes tc_sizes(const MtpShape &s) {
   if (s.F > z.kmax) z.kmax = s.F;
   DraftCtx c{};
   c.d = s.d; c.Hq = s.Hq; c.Hkv = s.Hkv; c.Dh = s.Dh; c.F = s.F; c.V = s.V;
-  size_t part = (size_t)s.B * s.V;  // LM-head logits when the caller keeps none
+  // LM-head logits when the caller keeps none, then the selection's partials
+  size_t part = ((size_t)s.B * s.V + 3) / 4 * 4 + (size_t)s.B * sel_subs(s.V) * 4;
   for (int op = OP_FC; op <= OP_DOWN; ++op) {
     const OpShape sh = op_shape(c, op);
     int ks, kb_per;
@@ -734,7 +800,12 @@ cudaError_t run_lmhead_tc(const DraftCtx &c, const TcBufs &t, cudaStream_t s, bo
   int ks = 1;
   cudaError_t e = run_gemm(c, t, OP_LMHEAD, lg, lstride, s, pdl, &ks);
   if (e) return e;
-  return launch(tc_select_kernel, dim3(c.B), kSelThreads, 0, s, pdl, c, (const float *)lg, lstride);
+  // past the logits, on a 16-byte boundary
+  float4 *sel = reinterpret_cast<float4 *>(t.part + ((size_t)c.B * c.V + 3) / 4 * 4);
+  e = launch(tc_select_part_kernel, dim3((sel_subs(c.V) + kSelWarps - 1) / kSelWarps, c.B), kSelThreads, 0, s, pdl,
+             c, (const float *)lg, lstride, sel);
+  if (e) return e;
+  return launch(tc_select_fin_kernel, dim3(c.B), 32, 0, s, pdl, c, (const float *)lg, lstride, (const float4 *)sel);
 }
 
 }  // namespace mtp
