@@ -54,6 +54,7 @@ struct TcGemmArgs {
   int ks, kb_per, kbs;             // K splits, 64-wide k-blocks per split and in all
   int nb, stages;                  // MMA N (padded batch rows), pipeline depth
   int B, arow0;                    // batch rows, first batch row of this group
+  int nunits;                      // (row group, K split) units, taken by the CTAs in turn
   float *out;                      // element (split s, batch b, row n) at out + s*sstride + b*bstride + n
   size_t sstride, bstride;
   int *status;
@@ -74,6 +75,29 @@ __host__ __device__ inline int tmem_cols(int nb, int mt) {
 
 // ---------------------------------------------------------------- GEMM kernel
 
+// A unit of work: one group of MT row tiles of map m and one K split.
+struct TcUnit {
+  int m, row0, split, kb0, nkb;
+};
+
+__device__ __forceinline__ TcUnit tc_unit(const TcGemmArgs &g, int u) {
+  TcUnit w;
+  w.split = u % g.ks;
+  int grp = u / g.ks, m = 0;
+  while (m < g.nmaps - 1 && grp >= g.groups[m]) {
+    grp -= g.groups[m];
+    ++m;
+  }
+  w.m = m;
+  w.row0 = grp * g.mt * kTileM;  // within map m
+  w.kb0 = w.split * g.kb_per;
+  w.nkb = max(0, min(g.kb_per, g.kbs - w.kb0));
+  return w;
+}
+
+// Persistent: CTA c takes units c, c + gridDim.x, ...  The stage ring runs on
+// across units; the accumulator is double-buffered in TMEM (when two fit), so
+// that the epilogue of one unit overlaps the MMAs of the next.
 __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ TcMaps maps,
                                                                   const TcGemmArgs g) {
   extern __shared__ unsigned char smem_raw[];
@@ -85,30 +109,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   const uint32_t ab = a_tile_bytes(g.nb), sb = stage_bytes(g.nb, MT), wb = (uint32_t)MT * kWTileBytes;
   uint64_t *full = reinterpret_cast<uint64_t *>(sm + (size_t)S * sb);
   uint64_t *empty = full + S;
-  uint64_t *done = empty + S;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+  uint64_t *done = empty + S;   // [2] accumulator buffer ready for the epilogue
+  uint64_t *tfree = done + 2;   // [2] accumulator buffer read back
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tfree + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ncols = tmem_cols(g.nb, MT);
-
-  const int split = blockIdx.x % g.ks;
-  int grp = blockIdx.x / g.ks, m = 0;
-  while (m < g.nmaps - 1 && grp >= g.groups[m]) {
-    grp -= g.groups[m];
-    ++m;
-  }
-  const int row0 = grp * MT * kTileM;  // within map m
-  const int kb0 = split * g.kb_per;
-  const int nkb = max(0, min(g.kb_per, g.kbs - kb0));
+  const int nbuf = 2 * ncols <= 512 ? 2 : 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(done, 1);
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&done[q], 1);
+      mbar_init(&tfree[q], 4);
+    }
     fence_barrier_init();
   }
-  if (warp == 1) tmem_alloc(tmem_slot, (uint32_t)ncols);
+  if (warp == 1) tmem_alloc(tmem_slot, (uint32_t)(nbuf * ncols));
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
@@ -116,84 +135,111 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
 
   if (warp == 0) {
     if (lane == 0) {
-      // Weights do not depend on the previous kernel: the first stages are
-      // requested before waiting for it; the activations only after.
+      // Weights do not depend on the previous kernel: the first unit's first
+      // stages are requested before waiting for it; activations only after.
       const uint64_t pol_w = l2_policy_evict_first(), pol_a = l2_policy_evict_last();
-      const int pre = min(S, nkb);
+      const TcUnit u0 = tc_unit(g, blockIdx.x);
+      const int pre = (int)blockIdx.x < g.nunits ? min(S, u0.nkb) : 0;
       for (int i = 0; i < pre; ++i) {
         mbar_arrive_expect_tx(&full[i], sb);
         for (int t = 0; t < MT; ++t)
-          tma_load_2d(sm + (size_t)i * sb + t * kWTileBytes, &maps.w[m], (kb0 + i) * kBK, row0 + t * kTileM,
-                      &full[i], pol_w);
+          tma_load_2d(sm + (size_t)i * sb + t * kWTileBytes, &maps.w[u0.m], (u0.kb0 + i) * kBK,
+                      u0.row0 + t * kTileM, &full[i], pol_w);
       }
       grid_dep_wait();
       bool ok = true;
-      for (int i = 0; i < nkb && ok; ++i) {
-        const int s = i % S;
-        unsigned char *st = sm + (size_t)s * sb;
-        const int x = (kb0 + i) * kBK;
-        if (i >= pre) {
-          ok = mbar_wait(&empty[s], (uint32_t)((i / S) - 1) & 1u, g.status);
-          if (!ok) break;
-          mbar_arrive_expect_tx(&full[s], sb);
-          for (int t = 0; t < MT; ++t)
-            tma_load_2d(st + t * kWTileBytes, &maps.w[m], x, row0 + t * kTileM, &full[s], pol_w);
-        }
+      uint32_t i = 0;  // k-blocks issued by this CTA
+      for (int u = blockIdx.x, n = 0; u < g.nunits && ok; u += gridDim.x, ++n) {
+        const TcUnit w = tc_unit(g, u);
+        for (int kb = 0; kb < w.nkb && ok; ++kb, ++i) {
+          const int s = (int)(i % S);
+          unsigned char *st = sm + (size_t)s * sb;
+          const int x = (w.kb0 + kb) * kBK;
+          if (!(n == 0 && kb < pre)) {
+            if (i >= (uint32_t)S) ok = mbar_wait(&empty[s], ((i / S) - 1u) & 1u, g.status);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&full[s], sb);
+            for (int t = 0; t < MT; ++t)
+              tma_load_2d(st + t * kWTileBytes, &maps.w[w.m], x, w.row0 + t * kTileM, &full[s], pol_w);
+          }
 #pragma unroll
-        for (int tt = 0; tt < kTerms; ++tt)
-          tma_load_2d(st + wb + tt * ab, &maps.a[tt], x, g.arow0, &full[s], pol_a);
+          for (int tt = 0; tt < kTerms; ++tt)
+            tma_load_2d(st + wb + tt * ab, &maps.a[tt], x, g.arow0, &full[s], pol_a);
+        }
       }
+      if (!ok)  // let copies still in flight land before the CTA exits
+        for (uint32_t q = i > (uint32_t)S ? i - S : 0u; q < i; ++q)
+          if (!mbar_wait(&full[q % S], (q / S) & 1u, g.status)) break;
     }
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kTileM, g.nb);
       bool ok = true;
-      for (int i = 0; i < nkb && ok; ++i) {
-        const int s = i % S;
-        ok = mbar_wait(&full[s], (uint32_t)(i / S) & 1u, g.status);
+      uint32_t i = 0;  // k-blocks consumed
+      for (int u = blockIdx.x, n = 0; u < g.nunits && ok; u += gridDim.x, ++n) {
+        const TcUnit w = tc_unit(g, u);
+        const int buf = n % nbuf;
+        if (n >= nbuf) ok = mbar_wait(&tfree[buf], (uint32_t)((n / nbuf) - 1) & 1u, g.status);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t st = smem_u32(sm + (size_t)s * sb);
+        const uint32_t acc = tmem + (uint32_t)(buf * ncols);
+        for (int kb = 0; kb < w.nkb && ok; ++kb, ++i) {
+          const int s = (int)(i % S);
+          ok = mbar_wait(&full[s], (i / S) & 1u, g.status);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t st = smem_u32(sm + (size_t)s * sb);
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)  // 16 bf16 = 32 bytes: +2 in the >>4 address field
-          for (int t = 0; t < MT; ++t) {  // tile t accumulates in TMEM columns [t nb, (t + 1) nb)
-            const uint64_t dw = sw128_kmajor_desc(st + t * kWTileBytes) + 2 * kk;
+          for (int kk = 0; kk < kBK / 16; ++kk)  // 16 bf16 = 32 bytes: +2 in the >>4 address field
+            for (int t = 0; t < MT; ++t) {  // tile t accumulates in columns [t nb, (t + 1) nb)
+              const uint64_t dw = sw128_kmajor_desc(st + t * kWTileBytes) + 2 * kk;
 #pragma unroll
-            for (int tt = 0; tt < kTerms; ++tt)
-              mma_bf16(tmem + (uint32_t)(t * g.nb), dw, sw128_kmajor_desc(st + wb + tt * ab) + 2 * kk, idesc,
-                       (i | kk | tt) != 0 ? 1u : 0u);
-          }
-        mma_commit(&empty[s]);  // the stage is free once these MMAs have read it
+              for (int tt = 0; tt < kTerms; ++tt)
+                mma_bf16(acc + (uint32_t)(t * g.nb), dw, sw128_kmajor_desc(st + wb + tt * ab) + 2 * kk, idesc,
+                         (kb | kk | tt) != 0 ? 1u : 0u);
+            }
+          mma_commit(&empty[s]);  // the stage is free once these MMAs have read it
+        }
+        mma_commit(&done[buf]);
       }
-      mma_commit(done);
     }
   } else {
-    // read the accumulator back: warp w reads TMEM lanes 32 (w % 4) .. + 31
+    // read the accumulators back: warp w reads TMEM lanes 32 (w % 4) .. + 31
     const int q = warp & 3;
-    const bool ok = mbar_wait(done, 0u, g.status) && nkb > 0;
-    tc_fence_after();
-    for (int t = 0; t < MT; ++t) {
-      const int row = row0 + t * kTileM + q * 32 + lane;
-      const bool valid = ok && row < g.rows[m];
-      float *o = g.out + (size_t)split * g.sstride + (size_t)g.base[m] + row;
-      for (int c0 = 0; c0 < g.nb; c0 += 32) {
-        float v[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(t * g.nb + c0), v);
-        if (valid) {
+    bool ok = true;
+    for (int u = blockIdx.x, n = 0; u < g.nunits && ok; u += gridDim.x, ++n) {
+      const TcUnit w = tc_unit(g, u);
+      const int buf = n % nbuf;
+      ok = mbar_wait(&done[buf], (uint32_t)(n / nbuf) & 1u, g.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t acc = tmem + (uint32_t)(buf * ncols);
+      for (int t = 0; t < MT; ++t) {
+        const int row = w.row0 + t * kTileM + q * 32 + lane;
+        const bool valid = w.nkb > 0 && row < g.rows[w.m];
+        float *o = g.out + (size_t)w.split * g.sstride + (size_t)g.base[w.m] + row;
+        for (int c0 = 0; c0 < g.nb; c0 += 32) {
+          float v[32];
+          tmem_ld32(acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(t * g.nb + c0), v);
+          if (valid) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int b = g.arow0 + c0 + i;
-            if (b < g.B) o[(size_t)b * g.bstride] = v[i];
+            for (int i = 0; i < 32; ++i) {
+              const int b = g.arow0 + c0 + i;
+              if (b < g.B) o[(size_t)b * g.bstride] = v[i];
+            }
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tfree[buf]);
     }
-    tc_fence_before();
   }
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, (uint32_t)ncols);
+    tmem_dealloc(tmem, (uint32_t)(nbuf * ncols));
   }
 }
 
@@ -753,12 +799,16 @@ cudaError_t run_gemm(const DraftCtx &c, const TcBufs &t, int op, float *out, siz
   g.sstride = (size_t)c.B * base;
   g.bstride = bstride;
   g.status = c.status;
-  const size_t smem = (size_t)g.stages * stage_bytes(nb, g.mt) + (size_t)(2 * g.stages + 1) * 8 + 16 + 1024;
+  const size_t smem = (size_t)g.stages * stage_bytes(nb, g.mt) + (size_t)(2 * g.stages + 4) * 8 + 16 + 1024;
+  g.nunits = groups * ks;
+  static int sms = 0;
+  if (!sms && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0) != cudaSuccess) sms = 148;
+  const int grid = g.nunits < sms ? g.nunits : sms;
   *ks_out = ks;
   cudaError_t e = cudaSuccess;
   for (int r0 = 0; r0 < c.B && e == cudaSuccess; r0 += nb) {  // batch groups of nb rows
     g.arow0 = r0;
-    e = launch(tc_gemm_kernel, dim3(groups * ks), kTcThreads, smem, s, pdl, maps, g);
+    e = launch(tc_gemm_kernel, dim3(grid), kTcThreads, smem, s, pdl, maps, g);
   }
   return e;
 }
