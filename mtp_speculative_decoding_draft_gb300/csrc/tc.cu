@@ -39,7 +39,7 @@ constexpr int kTileM = 128;      // output rows per tile (MMA M)
 constexpr int kBK = 64;          // K per stage: one 128-byte swizzle row of bf16
 constexpr uint32_t kWTileBytes = kTileM * kBK * 2;
 constexpr int kSmemBudget = 200 * 1024;
-constexpr int kTargetCtas = 296;  // split K until about this many CTAs (two per SM)
+constexpr int kTargetUnits = 152;  // split K until about this many units (one per SM)
 constexpr int kMaxSplits = 16;
 constexpr int kPrepThreads = 256;
 
@@ -336,33 +336,38 @@ __global__ void __launch_bounds__(kPrepThreads) tc_prep_wo_kernel(DraftCtx c, Tc
   }
 }
 
-// Sum the split-K partials of OP for sequence b, apply OP's epilogue and
-// write the next GEMM's input halves.
+// Sum the split-K partials of OP for sequence b (CTA r of the sequence's
+// cluster takes the r-th share of the columns), apply OP's epilogue and write
+// the next GEMM's input terms.
 template <int OP>
 __global__ void __launch_bounds__(kPrepThreads) tc_mid_kernel(DraftCtx c, TcBufs t, int ks, int N) {
   __shared__ float red[kGemvWarps];
-  const int b = blockIdx.x, d = c.d;
+  __shared__ float css;  // this CTA's sum of squares, read by the cluster's other CTAs
+  const int b = blockIdx.y, d = c.d, NC = (int)gridDim.x, r = (int)blockIdx.x;
   const size_t sstride = (size_t)c.B * N, boff = (size_t)b * N;
+  // this CTA's share of the op's columns, in whole groups of eight
+  const int ncol = OP == OP_QKV ? N : (OP == OP_GATEUP ? c.F : d);
+  const int g8 = ncol / 8, c0 = 8 * (int)(((long long)r * g8) / NC), c1 = 8 * (int)(((long long)(r + 1) * g8) / NC);
   grid_dep_wait();
   grid_dep_launch();
   if (OP == OP_QKV) {
     const int nq = c.Hq * c.Dh, nkv = c.Hkv * c.Dh;
     int L = __ldg(&c.ctx_len[b]);
     if (L < 0 || L + c.k > c.Lmax) {
-      if (threadIdx.x == 0) set_status(c.status, kStatusBadCtx);
+      if (threadIdx.x == 0 && r == 0) set_status(c.status, kStatusBadCtx);
       L = min(max(L, 0), c.Lmax - c.k);
     }
-    for (int i = threadIdx.x * 8; i < N; i += kPrepThreads * 8) {
+    for (int i = c0 + threadIdx.x * 8; i < c1; i += kPrepThreads * 8) {
       float y[8];
       sum8(t.part, ks, sstride, boff + i, y);
       if (i < nq) {
         *reinterpret_cast<float4 *>(c.q + (size_t)b * nq + i) = make_float4(y[0], y[1], y[2], y[3]);
         *reinterpret_cast<float4 *>(c.q + (size_t)b * nq + i + 4) = make_float4(y[4], y[5], y[6], y[7]);
       } else {
-        int r = i - nq;
-        uint16_t *cache = r < nkv ? c.kc : c.vc;
-        if (r >= nkv) r -= nkv;
-        const int kvh = r / c.Dh, dd = r % c.Dh;  // 8 | Dh: the eight stay in one head
+        int rr = i - nq;
+        uint16_t *cache = rr < nkv ? c.kc : c.vc;
+        if (rr >= nkv) rr -= nkv;
+        const int kvh = rr / c.Dh, dd = rr % c.Dh;  // 8 | Dh: the eight stay in one head
         uint16_t *dst = cache + (((size_t)b * c.Hkv + kvh) * c.Lmax + L + c.j) * c.Dh + dd;
 #pragma unroll
         for (int q = 0; q < 8; ++q) dst[q] = __bfloat16_as_ushort(__float2bfloat16_rn(y[q]));
@@ -372,7 +377,7 @@ __global__ void __launch_bounds__(kPrepThreads) tc_mid_kernel(DraftCtx c, TcBufs
   }
   if (OP == OP_GATEUP) {  // SwiGLU: gate rows [0, F), up rows [F, 2F)
     const int F = c.F;
-    for (int i = threadIdx.x * 8; i < F; i += kPrepThreads * 8) {
+    for (int i = c0 + threadIdx.x * 8; i < c1; i += kPrepThreads * 8) {
       float gt[8], up[8];
       sum8(t.part, ks, sstride, boff + i, gt);
       sum8(t.part, ks, sstride, boff + F + i, up);
@@ -382,28 +387,32 @@ __global__ void __launch_bounds__(kPrepThreads) tc_mid_kernel(DraftCtx c, TcBufs
     }
     return;
   }
-  // FC -> x0, WO -> x1 = x0 + y, DOWN -> x2 = x1 + y; then the next input rms(x) g
+  // FC -> x0, WO -> x1 = x0 + y, DOWN -> x2 = x1 + y; then the next input
+  // rms(x) g, the sum of squares added over the cluster's CTAs in rank order
   float *xo = OP == OP_FC ? c.x0 : (OP == OP_WO ? c.x1 : c.x2);
   const float *xr = OP == OP_WO ? c.x0 : c.x1;
   const uint16_t *gain = OP == OP_FC ? c.g_attn : (OP == OP_WO ? c.g_mlp : c.g_final);
   float ss = 0.f;
-  for (int i = threadIdx.x * 8; i < d; i += kPrepThreads * 8) {
+  for (int i = c0 + threadIdx.x * 8; i < c1; i += kPrepThreads * 8) {
     float y[8];
     sum8(t.part, ks, sstride, boff + i, y);
     if (OP != OP_FC) {
-      float r[8];
-      load8_f32(xr + (size_t)b * d + i, r);
+      float rv[8];
+      load8_f32(xr + (size_t)b * d + i, rv);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) y[q] += r[q];
+      for (int q = 0; q < 8; ++q) y[q] += rv[q];
     }
     *reinterpret_cast<float4 *>(xo + (size_t)b * d + i) = make_float4(y[0], y[1], y[2], y[3]);
     *reinterpret_cast<float4 *>(xo + (size_t)b * d + i + 4) = make_float4(y[4], y[5], y[6], y[7]);
     ss = sumsq8(y, ss);
   }
   ss = block_sum_256(ss, red);
-  const float rs = rsqrtf(ss / (float)d + c.eps);
-  __syncthreads();  // this CTA's x writes are visible to its own re-reads below
-  for (int i = threadIdx.x * 8; i < d; i += kPrepThreads * 8) {
+  if (threadIdx.x == 0) css = ss;
+  cluster_sync();  // every CTA's sum is in place; this CTA's x writes are visible to it
+  float tot = 0.f;
+  for (int q = 0; q < NC; ++q) tot += *dsmem_ptr(&css, (uint32_t)q);
+  const float rs = rsqrtf(tot / (float)d + c.eps);
+  for (int i = c0 + threadIdx.x * 8; i < c1; i += kPrepThreads * 8) {
     float y[8], g[8];
     load8_f32(xo + (size_t)b * d + i, y);
     load8_bf16(gain + i, g);
@@ -411,14 +420,9 @@ __global__ void __launch_bounds__(kPrepThreads) tc_mid_kernel(DraftCtx c, TcBufs
     for (int q = 0; q < 8; ++q) y[q] = y[q] * rs * g[q];
     store_split8(t, b, i, y);
   }
+  cluster_sync();  // no CTA leaves before its peers have read its sum
 }
 
-// Draft-token selection of sequence b at depth j from its logits row: argmax
-// (lowest index on ties), or the inverse CDF of softmax(logits / T) at
-// u_draft[b, j].  All passes read the row lane-strided (coalesced): warp w
-// owns a contiguous segment, the segments' masses are scanned in float64 in
-// vocabulary order and the warp holding the crossing rescans its segment 32
-// elements at a time with a float64 warp scan.
 // Draft-token selection over the batch's logits rows, in two launches.
 // tc_select_part_kernel: one CTA per 4096 elements of a row, a warp per
 // 1024-element sub-segment: its (max, lowest argmax) and, in stochastic mode,
@@ -674,10 +678,13 @@ int op_groups(const OpShape &s, int mt) {
   return n;
 }
 
-// K splits: about kTargetCtas CTAs, whole k-blocks per split.
+// K splits: about one unit per SM (the kernel is persistent), whole k-blocks
+// per split.  MTP_TC_UNITS overrides the target.
 void op_splits(int tiles, int K, int *ks, int *kb_per) {
   const int kbs = K / kBK;
-  int s = (kTargetCtas + tiles - 1) / tiles;
+  const char *v = getenv("MTP_TC_UNITS");
+  const int target = v && *v ? atoi(v) : kTargetUnits;
+  int s = (target + tiles - 1) / tiles;
   s = s < 1 ? 1 : (s > kMaxSplits ? kMaxSplits : s);
   if (s > kbs) s = kbs;
   *kb_per = (kbs + s - 1) / s;
@@ -686,12 +693,16 @@ void op_splits(int tiles, int K, int *ks, int *kb_per) {
 
 int batch_nb(int B) { return B <= 32 ? 32 : (B <= 64 ? 64 : 128); }
 
-// 128-row weight tiles per CTA: each activation stage in shared memory serves
-// mt tiles, so the activations are re-read from L2 once per mt tiles.  Two
-// pipeline stages at least must fit.  MTP_TC_MT overrides.
-int op_mt(int nb) {
-  const char *v = getenv("MTP_TC_MT");
-  int mt = v && *v ? atoi(v) : (nb <= 64 ? 4 : 2);
+// 128-row weight tiles per unit: each activation stage in shared memory serves
+// mt tiles, so the activations are re-read from L2 once per mt tiles.  The
+// LM head takes 4 (2 for 128-row batches); the block's GEMMs take 2: smaller
+// stages keep more of their few k-blocks in flight (measured: 2 beats 1 and
+// 4 over the batch-of-64 and deep-chain workloads).  Two pipeline stages at
+// least must fit.
+// MTP_TC_MT and MTP_TC_MT_BLOCK override.
+int op_mt(int nb, int op) {
+  const char *v = getenv(op == OP_LMHEAD ? "MTP_TC_MT" : "MTP_TC_MT_BLOCK");
+  int mt = v && *v ? atoi(v) : (op == OP_LMHEAD ? (nb <= 64 ? 4 : 2) : 2);
   if (mt < 1) mt = 1;
   while (mt > 1 && (2 * stage_bytes(nb, mt) > (uint32_t)kSmemBudget || nb * mt > 512)) --mt;
   return mt;
@@ -711,6 +722,30 @@ cudaError_t launch(K kern, dim3 grid, int threads, size_t smem, cudaStream_t s, 
   cfg.numAttrs = pdl ? 1 : 0;
   note_launch();
   return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// The mid kernels: one cluster of nc CTAs per sequence, each CTA a share of
+// the columns (about 1024 of them, at most 8 CTAs).
+template <int OP>
+cudaError_t launch_mid(const DraftCtx &c, const TcBufs &t, int ks, int N, cudaStream_t s, bool pdl) {
+  const int ncol = OP == OP_QKV ? N : (OP == OP_GATEUP ? c.F : c.d);
+  int nc = ncol / 1024;
+  nc = nc < 1 ? 1 : (nc > 8 ? 8 : nc);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(nc, c.B);
+  cfg.blockDim = dim3(kPrepThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)nc;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  note_launch();
+  return cudaLaunchKernelEx(&cfg, tc_mid_kernel<OP>, c, t, ks, N);
 }
 
 }  // namespace
@@ -743,7 +778,7 @@ TcSizes tc_sizes(const MtpShape &s) {
   for (int op = OP_FC; op <= OP_DOWN; ++op) {
     const OpShape sh = op_shape(c, op);
     int ks, kb_per;
-    op_splits(op_groups(sh, op_mt(batch_nb(s.B))), sh.K, &ks, &kb_per);
+    op_splits(op_groups(sh, op_mt(batch_nb(s.B), op)), sh.K, &ks, &kb_per);
     const size_t n = (size_t)ks * s.B * op_rows(sh);
     if (n > part) part = n;
   }
@@ -766,7 +801,7 @@ cudaError_t run_gemm(const DraftCtx &c, const TcBufs &t, int op, float *out, siz
   TcGemmArgs g{};
   g.nmaps = sh.nmaps;
   const int nb = batch_nb(c.B);
-  g.mt = op_mt(nb);
+  g.mt = op_mt(nb, op);
   int base = 0, groups = 0;
   for (int i = 0; i < sh.nmaps; ++i) {
     if (!make_map(&maps.w[i], sh.w[i], (uint64_t)sh.K, (uint64_t)sh.rows[i], (uint64_t)sh.K, kTileM))
@@ -825,9 +860,9 @@ cudaError_t run_block_pre_tc(const DraftCtx &c, const TcBufs &t, cudaStream_t s,
   const int nqkv = (c.Hq + 2 * c.Hkv) * c.Dh;
   if ((e = launch(tc_prep_fc_kernel, gb, kPrepThreads, 0, s, pdl, c, t))) return e;
   if ((e = run_gemm(c, t, OP_FC, t.part, (size_t)c.d, s, pdl, &ks))) return e;
-  if ((e = launch(tc_mid_kernel<OP_FC>, gb, kPrepThreads, 0, s, pdl, c, t, ks, c.d))) return e;
+  if ((e = launch_mid<OP_FC>(c, t, ks, c.d, s, pdl))) return e;
   if ((e = run_gemm(c, t, OP_QKV, t.part, (size_t)nqkv, s, pdl, &ks))) return e;
-  return launch(tc_mid_kernel<OP_QKV>, gb, kPrepThreads, 0, s, pdl, c, t, ks, nqkv);
+  return launch_mid<OP_QKV>(c, t, ks, nqkv, s, pdl);
 }
 
 cudaError_t run_block_post_tc(const DraftCtx &c, const TcBufs &t, cudaStream_t s, bool pdl) {
@@ -836,11 +871,11 @@ cudaError_t run_block_post_tc(const DraftCtx &c, const TcBufs &t, cudaStream_t s
   int ks = 1;
   if ((e = launch(tc_prep_wo_kernel, gb, kPrepThreads, 0, s, pdl, c, t))) return e;
   if ((e = run_gemm(c, t, OP_WO, t.part, (size_t)c.d, s, pdl, &ks))) return e;
-  if ((e = launch(tc_mid_kernel<OP_WO>, gb, kPrepThreads, 0, s, pdl, c, t, ks, c.d))) return e;
+  if ((e = launch_mid<OP_WO>(c, t, ks, c.d, s, pdl))) return e;
   if ((e = run_gemm(c, t, OP_GATEUP, t.part, (size_t)(2 * c.F), s, pdl, &ks))) return e;
-  if ((e = launch(tc_mid_kernel<OP_GATEUP>, gb, kPrepThreads, 0, s, pdl, c, t, ks, 2 * c.F))) return e;
+  if ((e = launch_mid<OP_GATEUP>(c, t, ks, 2 * c.F, s, pdl))) return e;
   if ((e = run_gemm(c, t, OP_DOWN, t.part, (size_t)c.d, s, pdl, &ks))) return e;
-  return launch(tc_mid_kernel<OP_DOWN>, gb, kPrepThreads, 0, s, pdl, c, t, ks, c.d);
+  return launch_mid<OP_DOWN>(c, t, ks, c.d, s, pdl);
 }
 
 cudaError_t run_lmhead_tc(const DraftCtx &c, const TcBufs &t, cudaStream_t s, bool pdl) {
