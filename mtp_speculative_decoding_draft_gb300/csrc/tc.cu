@@ -695,14 +695,16 @@ int batch_nb(int B) { return B <= 32 ? 32 : (B <= 64 ? 64 : 128); }
 
 // 128-row weight tiles per unit: each activation stage in shared memory serves
 // mt tiles, so the activations are re-read from L2 once per mt tiles.  The
-// LM head takes 4 (2 for 128-row batches); the block's GEMMs take 2: smaller
+// LM head takes 3 for batches of up to 32 (three stages fit), 4 up to 64 and
+// 2 for 128-row batches (measured best on the deep-chain and batch-of-64
+// workloads); the block's GEMMs take 2: smaller
 // stages keep more of their few k-blocks in flight (measured: 2 beats 1 and
 // 4 over the batch-of-64 and deep-chain workloads).  Two pipeline stages at
 // least must fit.
 // MTP_TC_MT and MTP_TC_MT_BLOCK override.
 int op_mt(int nb, int op) {
   const char *v = getenv(op == OP_LMHEAD ? "MTP_TC_MT" : "MTP_TC_MT_BLOCK");
-  int mt = v && *v ? atoi(v) : (op == OP_LMHEAD ? (nb <= 64 ? 4 : 2) : 2);
+  int mt = v && *v ? atoi(v) : (op == OP_LMHEAD ? (nb <= 32 ? 3 : (nb <= 64 ? 4 : 2)) : 2);
   if (mt < 1) mt = 1;
   while (mt > 1 && (2 * stage_bytes(nb, mt) > (uint32_t)kSmemBudget || nb * mt > 512)) --mt;
   return mt;
