@@ -5,11 +5,13 @@
 //   out[b, n] = sum_k W[n, k] a[b, k]         (fp32 accumulation in TMEM)
 //
 // with the fp32 activation a split into three bf16 terms a = hi + mid + lo
-// (hi = bf16(a), mid = bf16(a - hi), lo = bf16(a - hi - mid)): three
-// tcgen05.mma per k-step keep the activation's 24 significant bits, so the
-// products match an fp32 GEMV ("The Tiny Draft Model Hidden Inside
-// Qwen", opening section: the module is one full-attention block; the same
-// module is applied k times, "One step deeper than the main model").
+// (hi = bf16(a), mid = bf16(a - hi), lo = bf16(a - hi - mid)): the three
+// terms' products keep the activation's 24 significant bits (for batches of
+// up to 64 one tcgen05.mma of N = 3 nb per k-step, the terms side by side in
+// N; beyond, three of N = nb), so the products match an fp32 GEMV ("The Tiny
+// Draft Model Hidden Inside Qwen", opening section: the module is one
+// full-attention block; the same module is applied k times, "One step deeper
+// than the main model").
 //
 // Per depth: prep(FC input) -> GEMM FC -> mid(x0, QKV input) -> GEMM QKV ->
 // mid(q, K/V append) -> attention -> prep(WO input) -> GEMM WO -> mid(x1,
@@ -38,9 +40,10 @@ constexpr int kTcThreads = 192;  // warp 0 TMA, warp 1 MMA and TMEM, warps 2-5 r
 constexpr int kTileM = 128;      // output rows per tile (MMA M)
 constexpr int kBK = 64;          // K per stage: one 128-byte swizzle row of bf16
 constexpr uint32_t kWTileBytes = kTileM * kBK * 2;
-constexpr int kSmemBudget = 200 * 1024;
-constexpr int kTargetUnits = 152;  // split K until about this many units (one per SM)
-constexpr int kMaxSplits = 16;
+// stage ring budget: the 227 KB a CTA may hold, less the 1024-byte alignment
+// pad and the barriers
+constexpr int kSmemBudget = 227 * 1024 - 1024 - 256;
+constexpr int kMaxSplits = 32;
 constexpr int kPrepThreads = 256;
 
 struct TcMaps {
@@ -52,7 +55,7 @@ struct TcGemmArgs {
   int nmaps, mt;                   // weight maps; 128-row tiles per CTA (sharing each activation stage)
   int rows[3], groups[3], base[3];  // rows and mt-tile groups of each map; its first output row
   int ks, kb_per, kbs;             // K splits, 64-wide k-blocks per split and in all
-  int nb, stages;                  // MMA N (padded batch rows), pipeline depth
+  int nb, stages;                  // padded batch rows, pipeline depth
   int B, arow0;                    // batch rows, first batch row of this group
   int nunits;                      // (row group, K split) units, taken by the CTAs in turn
   float *out;                      // element (split s, batch b, row n) at out + s*sstride + b*bstride + n
@@ -65,9 +68,10 @@ constexpr int kTerms = 3;
 __host__ __device__ inline uint32_t stage_bytes(int nb, int mt) {
   return (uint32_t)mt * kWTileBytes + kTerms * a_tile_bytes(nb);
 }
-__host__ __device__ inline int tmem_cols(int nb, int mt) {
+// TMEM columns of one accumulator buffer: mt tiles of N columns each
+__host__ __device__ inline int tmem_cols(int n_mma, int mt) {
   int n = 32;
-  while (n < nb * mt) n *= 2;
+  while (n < n_mma * mt) n *= 2;
   return n;
 }
 
@@ -98,6 +102,11 @@ __device__ __forceinline__ TcUnit tc_unit(const TcGemmArgs &g, int u) {
 // Persistent: CTA c takes units c, c + gridDim.x, ...  The stage ring runs on
 // across units; the accumulator is double-buffered in TMEM (when two fit), so
 // that the epilogue of one unit overlaps the MMAs of the next.
+// FUSE: the three activation terms lie back to back in a stage, one K-major
+// operand of 3 nb rows, so one MMA of N = 3 nb per k-step and tile reads the
+// weight tile once (three MMAs of N = nb would read it three times); each
+// term accumulates in its own block of nb columns and the epilogue adds them.
+template <bool FUSE>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ TcMaps maps,
                                                                   const TcGemmArgs g) {
   extern __shared__ unsigned char smem_raw[];
@@ -113,7 +122,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   uint64_t *tfree = done + 2;   // [2] accumulator buffer read back
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tfree + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ncols = tmem_cols(g.nb, MT);
+  const int nmma = FUSE ? kTerms * g.nb : g.nb;  // accumulator columns of one tile
+  const int ncols = tmem_cols(nmma, MT);
   const int nbuf = 2 * ncols <= 512 ? 2 : 1;
 
   if (threadIdx.x == 0) {
@@ -173,7 +183,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kTileM, g.nb);
+      const uint32_t idesc = idesc_bf16_f32(kTileM, nmma);
       bool ok = true;
       uint32_t i = 0;  // k-blocks consumed
       for (int u = blockIdx.x, n = 0; u < g.nunits && ok; u += gridDim.x, ++n) {
@@ -191,12 +201,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
           const uint32_t st = smem_u32(sm + (size_t)s * sb);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)  // 16 bf16 = 32 bytes: +2 in the >>4 address field
-            for (int t = 0; t < MT; ++t) {  // tile t accumulates in columns [t nb, (t + 1) nb)
+            for (int t = 0; t < MT; ++t) {  // tile t accumulates in columns [t nmma, (t + 1) nmma)
               const uint64_t dw = sw128_kmajor_desc(st + t * kWTileBytes) + 2 * kk;
+              if (FUSE) {
+                mma_bf16(acc + (uint32_t)(t * nmma), dw, sw128_kmajor_desc(st + wb) + 2 * kk, idesc,
+                         (kb | kk) != 0 ? 1u : 0u);
+              } else {
 #pragma unroll
-              for (int tt = 0; tt < kTerms; ++tt)
-                mma_bf16(acc + (uint32_t)(t * g.nb), dw, sw128_kmajor_desc(st + wb + tt * ab) + 2 * kk, idesc,
-                         (kb | kk | tt) != 0 ? 1u : 0u);
+                for (int tt = 0; tt < kTerms; ++tt)
+                  mma_bf16(acc + (uint32_t)(t * nmma), dw, sw128_kmajor_desc(st + wb + tt * ab) + 2 * kk, idesc,
+                           (kb | kk | tt) != 0 ? 1u : 0u);
+              }
             }
           mma_commit(&empty[s]);  // the stage is free once these MMAs have read it
         }
@@ -221,7 +236,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         float *o = g.out + (size_t)w.split * g.sstride + (size_t)g.base[w.m] + row;
         for (int c0 = 0; c0 < g.nb; c0 += 32) {
           float v[32];
-          tmem_ld32(acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(t * g.nb + c0), v);
+          const uint32_t ta = acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(t * nmma + c0);
+          tmem_ld32(ta, v);
+          if (FUSE) {  // hi + mid + lo products
+            float v1[32];
+            tmem_ld32(ta + (uint32_t)g.nb, v1);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] += v1[i];
+            tmem_ld32(ta + (uint32_t)(2 * g.nb), v1);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] += v1[i];
+          }
           if (valid) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -678,35 +703,84 @@ int op_groups(const OpShape &s, int mt) {
   return n;
 }
 
-// K splits: about one unit per SM (the kernel is persistent), whole k-blocks
-// per split.  MTP_TC_UNITS overrides the target.
-void op_splits(int tiles, int K, int *ks, int *kb_per) {
+int num_sms() {
+  static int sms = 0;
+  if (sms <= 0 && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0) != cudaSuccess) sms = 0;
+  return sms > 0 ? sms : 152;
+}
+
+// K splits of an op with `groups` row groups, whole k-blocks per split.  The
+// persistent CTAs take the (group, split) units in turn, so the busiest CTA
+// runs ceil(units / SMs) units of kb_per k-blocks each, plus a little per
+// unit (the accumulator read-back and the turn to the next unit; half a
+// k-block here).  The split count minimises that; a larger count must gain
+// 5% over a smaller one, since it leaves more partials to sum.  (A unit count
+// just above the SM count would run a second wave of a few units.)
+// MTP_TC_SPLITS fixes the count.
+void op_splits(int groups, int K, int sms, int *ks, int *kb_per) {
   const int kbs = K / kBK;
-  const char *v = getenv("MTP_TC_UNITS");
-  const int target = v && *v ? atoi(v) : kTargetUnits;
-  int s = (target + tiles - 1) / tiles;
-  s = s < 1 ? 1 : (s > kMaxSplits ? kMaxSplits : s);
-  if (s > kbs) s = kbs;
-  *kb_per = (kbs + s - 1) / s;
-  *ks = (kbs + *kb_per - 1) / *kb_per;
+  const char *v = getenv("MTP_TC_SPLITS");
+  if (v && *v) {
+    int s = atoi(v);
+    s = s < 1 ? 1 : (s > kMaxSplits ? kMaxSplits : (s > kbs ? kbs : s));
+    *kb_per = (kbs + s - 1) / s;
+    *ks = (kbs + *kb_per - 1) / *kb_per;
+    return;
+  }
+  long best = -1;
+  *ks = 1;
+  *kb_per = kbs;
+  for (int s = 1; s <= kMaxSplits && s <= kbs; ++s) {
+    const int kb = (kbs + s - 1) / s;
+    if ((kbs + kb - 1) / kb != s) continue;  // the same split as a smaller count
+    const long waves = ((long)groups * s + sms - 1) / sms;
+    const long cost = waves * (2L * kb + 1);
+    if (best < 0 || 20 * cost < 19 * best) {
+      best = cost;
+      *ks = s;
+      *kb_per = kb;
+    }
+  }
 }
 
 int batch_nb(int B) { return B <= 32 ? 32 : (B <= 64 ? 64 : 128); }
 
+// Shared memory for the stage ring; MTP_TC_SMEM_KB lowers it.
+int smem_budget() {
+  const char *v = getenv("MTP_TC_SMEM_KB");
+  const int kb = v && *v ? atoi(v) : 0;
+  return kb > 0 && kb * 1024 < kSmemBudget ? kb * 1024 : kSmemBudget;
+}
+
+// One MMA of N = 3 nb per k-step and tile instead of three of N = nb: the
+// weight tile is then read from shared memory once per k-step, not three
+// times.  N is at most 256, so batches of up to 64 rows.  MTP_TC_FUSE=0 turns
+// it off.
+bool use_fuse(int nb) {
+  const char *v = getenv("MTP_TC_FUSE");
+  return kTerms * nb <= 256 && !(v && *v == '0');
+}
+
 // 128-row weight tiles per unit: each activation stage in shared memory serves
-// mt tiles, so the activations are re-read from L2 once per mt tiles.  The
-// LM head takes 3 for batches of up to 32 (three stages fit), 4 up to 64 and
-// 2 for 128-row batches (measured best on the deep-chain and batch-of-64
-// workloads); the block's GEMMs take 2: smaller
-// stages keep more of their few k-blocks in flight (measured: 2 beats 1 and
-// 4 over the batch-of-64 and deep-chain workloads).  Two pipeline stages at
-// least must fit.
+// mt tiles, so the activations are re-read from L2 once per mt tiles.  With
+// three MMAs per tile the LM head takes 3 for batches of up to 32, 4 up to 64
+// and 2 for 128-row batches (measured best on the deep-chain and batch-of-64
+// workloads); the block's GEMMs take 2: smaller stages keep more of their few
+// k-blocks in flight (measured: 2 beats 1 and 4 over the same workloads).
+// With the fused MMA a tile's accumulator takes 3 nb TMEM columns: the LM head
+// takes 3 tiles for batches of up to 32 (288 columns; three 60 KB stages fit)
+// and 2 for 64 (384 columns), the block's GEMMs 2 (measured on the same
+// workloads: 4 tiles at a batch of 32 leave room for two stages only, 1 tile
+// re-reads the activations too often).  Two pipeline stages at least must fit.
 // MTP_TC_MT and MTP_TC_MT_BLOCK override.
-int op_mt(int nb, int op) {
+int op_mt(int nb, int op, bool fuse) {
   const char *v = getenv(op == OP_LMHEAD ? "MTP_TC_MT" : "MTP_TC_MT_BLOCK");
-  int mt = v && *v ? atoi(v) : (op == OP_LMHEAD ? (nb <= 32 ? 3 : (nb <= 64 ? 4 : 2)) : 2);
+  int mt = 2;
+  if (v && *v) mt = atoi(v);
+  else if (op == OP_LMHEAD) mt = nb <= 32 ? 3 : (nb <= 64 && !fuse ? 4 : 2);
   if (mt < 1) mt = 1;
-  while (mt > 1 && (2 * stage_bytes(nb, mt) > (uint32_t)kSmemBudget || nb * mt > 512)) --mt;
+  const int nmma = fuse ? kTerms * nb : nb;
+  while (mt > 1 && (2 * stage_bytes(nb, mt) > (uint32_t)kSmemBudget || nmma * mt > 512)) --mt;
   return mt;
 }
 
@@ -780,7 +854,8 @@ TcSizes tc_sizes(const MtpShape &s) {
   for (int op = OP_FC; op <= OP_DOWN; ++op) {
     const OpShape sh = op_shape(c, op);
     int ks, kb_per;
-    op_splits(op_groups(sh, op_mt(batch_nb(s.B), op)), sh.K, &ks, &kb_per);
+    const int nb = batch_nb(s.B);
+    op_splits(op_groups(sh, op_mt(nb, op, use_fuse(nb))), sh.K, num_sms(), &ks, &kb_per);
     const size_t n = (size_t)ks * s.B * op_rows(sh);
     if (n > part) part = n;
   }
@@ -788,8 +863,14 @@ TcSizes tc_sizes(const MtpShape &s) {
   return z;
 }
 
+// The GEMM's shared-memory ceiling: what the largest stage ring needs (the
+// ring budget with its alignment pad and barriers), or the ring budget that
+// MTP_TC_SMEM_KB sets.
 cudaError_t tc_set_attributes() {
-  return cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget + 2048);
+  const int bytes = smem_budget() + 1024 + 256;
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(tc_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 namespace {
@@ -803,7 +884,8 @@ cudaError_t run_gemm(const DraftCtx &c, const TcBufs &t, int op, float *out, siz
   TcGemmArgs g{};
   g.nmaps = sh.nmaps;
   const int nb = batch_nb(c.B);
-  g.mt = op_mt(nb, op);
+  const bool fuse = use_fuse(nb);
+  g.mt = op_mt(nb, op, fuse);
   int base = 0, groups = 0;
   for (int i = 0; i < sh.nmaps; ++i) {
     if (!make_map(&maps.w[i], sh.w[i], (uint64_t)sh.K, (uint64_t)sh.rows[i], (uint64_t)sh.K, kTileM))
@@ -819,7 +901,7 @@ cudaError_t run_gemm(const DraftCtx &c, const TcBufs &t, int op, float *out, siz
       return cudaErrorInvalidValue;
   int ks = 1, kb_per = sh.K / kBK;
   if (op != OP_LMHEAD) {
-    op_splits(groups, sh.K, &ks, &kb_per);
+    op_splits(groups, sh.K, num_sms(), &ks, &kb_per);
     while (ks > 1 && (size_t)ks * c.B * base > t.part_floats) {  // what the workspace holds
       kb_per = (sh.K / kBK + ks - 2) / (ks - 1);
       ks = (sh.K / kBK + kb_per - 1) / kb_per;
@@ -829,7 +911,8 @@ cudaError_t run_gemm(const DraftCtx &c, const TcBufs &t, int op, float *out, siz
   g.kb_per = kb_per;
   g.kbs = sh.K / kBK;
   g.nb = nb;
-  g.stages = (int)(kSmemBudget / stage_bytes(nb, g.mt));
+  g.stages = (int)(smem_budget() / stage_bytes(nb, g.mt));
+  if (g.stages < 2) g.stages = 2;
   if (g.stages > 8) g.stages = 8;
   g.B = c.B;
   g.out = out;
@@ -838,14 +921,14 @@ cudaError_t run_gemm(const DraftCtx &c, const TcBufs &t, int op, float *out, siz
   g.status = c.status;
   const size_t smem = (size_t)g.stages * stage_bytes(nb, g.mt) + (size_t)(2 * g.stages + 4) * 8 + 16 + 1024;
   g.nunits = groups * ks;
-  static int sms = 0;
-  if (!sms && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0) != cudaSuccess) sms = 148;
+  const int sms = num_sms();
   const int grid = g.nunits < sms ? g.nunits : sms;
   *ks_out = ks;
   cudaError_t e = cudaSuccess;
   for (int r0 = 0; r0 < c.B && e == cudaSuccess; r0 += nb) {  // batch groups of nb rows
     g.arow0 = r0;
-    e = launch(tc_gemm_kernel, dim3(grid), kTcThreads, smem, s, pdl, maps, g);
+    e = fuse ? launch(tc_gemm_kernel<true>, dim3(grid), kTcThreads, smem, s, pdl, maps, g)
+             : launch(tc_gemm_kernel<false>, dim3(grid), kTcThreads, smem, s, pdl, maps, g);
   }
   return e;
 }
