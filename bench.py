@@ -33,13 +33,15 @@ def block_elements(w):
     return (w.d * 2 * w.d + (w.Hq + 2 * w.Hkv) * w.Dh * w.d + w.d * w.Hq * w.Dh + 3 * w.d * w.F + 5 * w.d)
 
 
-def step_bytes(w, ctx_len, logits_out):
+def step_bytes(w, ctx_len, logits_out, n_modules=1):
     """Algorithmic HBM bytes of one spec_step: weights re-streamed at every
     depth, the visible KV rows read once per depth, target logits read once,
-    draft logits written and read once when they are materialised."""
+    draft logits written and read once when they are materialised.  With
+    distinct modules depth j runs module min(j, n - 1) and sees that module's
+    context plus the rows earlier depths appended to the same cache."""
     k = w.k
     weights = k * (block_elements(w) + w.V * w.d) * 2
-    kv = sum(int(L) + j + 1 for L in ctx_len for j in range(k)) * w.Hkv * w.Dh * 2 * 2
+    kv = sum(int(L) + j - min(j, n_modules - 1) + 1 for L in ctx_len for j in range(k)) * w.Hkv * w.Dh * 2 * 2
     target = w.B * (k + 1) * w.V * 4
     draft = 2 * w.B * k * w.V * 4 if logits_out else 0
     return weights + kv + target + draft
@@ -215,7 +217,8 @@ def run_reference(args):
 
 
 def config_of(w, args):
-    return {"workload": w.name, "B": w.B, "k": w.k, "d": w.d, "Hq": w.Hq, "Hkv": w.Hkv, "Dh": w.Dh, "F": w.F,
+    mods = getattr(args, "modules", 1)
+    return {"workload": w.name + ("_modules%d" % mods if mods > 1 else ""), "modules": mods, "B": w.B, "k": w.k, "d": w.d, "Hq": w.Hq, "Hkv": w.Hkv, "Dh": w.Dh, "F": w.F,
             "V": w.V, "ctx": w.ctx if not isinstance(w.ctx, tuple) else list(w.ctx),
             "mode": "greedy" if w.mode == 0 else "stochastic", "T": w.T,
             "parallelism": "replicas%d" % args.gpus, "l2": "inputs larger than L2 (weights %.2f GB re-streamed per depth)"
@@ -314,8 +317,11 @@ def run_ours(args):
     wts = W.make_weights(w)
     ctx = W.make_context(w)
     u = W.make_uniforms(w)
-    m = DraftModule(w, wts)
-    m.set_context(ctx)
+    nm = max(1, min(args.modules, w.k))
+    extra = [W.make_module_weights(w, i, E=wts["E"]) for i in range(1, nm)]
+    caches = [W.make_module_cache(w, i) for i in range(1, nm)]
+    m = DraftModule(w, wts, extra_modules=extra)
+    m.set_context(ctx, caches)
     if w.mode == 1:
         # target = the module's own draft logits + noise growing with position
         m.draft(w.T, w.mode, to_device(u["u_draft"]), logits=True)
@@ -326,7 +332,7 @@ def run_ours(args):
                                w.k + 1)
         for j in range(w.k + 1):
             target[:, j] += dl[:, min(j, w.k - 1)]
-        m.set_context(ctx)
+        m.set_context(ctx, caches)
     else:
         target = W.target_logits(w)
     target_d = to_device(target)
@@ -428,7 +434,7 @@ def run_ours(args):
         return
 
     peak, peak_kind = measured_peaks()
-    sb = step_bytes(w, ctx["ctx_len"], logits_out)
+    sb = step_bytes(w, ctx["ctx_len"], logits_out, nm)
     steps_s = 1e3 / ms * world
     tokens_per_step = float(L.sum())
     lm_avg = lm_ms / max(lm_n, 1)
@@ -480,6 +486,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--k", type=int, default=0, help="draft depth for the verify sweep (1..5)")
     ap.add_argument("--greedy", action="store_true", help="greedy verification for the verify sweep")
+    ap.add_argument("--modules", type=int, default=1,
+                    help="distinct draft modules (depth j runs module min(j, modules-1)); 1 = one reused module")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -214,6 +214,48 @@ int spec_step(const MtpDims *dims, const MtpWeights *w, const void *h,
               int32_t *out_tok, int32_t *accept_len, int32_t *num_accepted,
               void *ws, size_t ws_bytes, mtp_stream_t stream);
 
+/*
+ * Distinct modules per depth.  [P1] "What is multi-token prediction?": a
+ * model trained with MTP carries D sequential modules, one per additional
+ * future token, chained so that each takes the previous one's output hidden
+ * state; every module has its own transformer block and input projection and
+ * shares the embedding and the output head with the main model.  [P1] "Why
+ * fine-tune a single MTP head": DeepSeek-V3 trains D distinct modules, while
+ * engines usually keep one and reuse it -- mtp_draft's case.
+ *
+ * One module: its weights and its own K/V cache (its block has its own
+ * attention).  `modules` is a HOST array of n_modules such structs, 1 <=
+ * n_modules <= k; every pointer inside is a device pointer as for mtp_draft.
+ * Depth j runs module m = min(j, n_modules - 1): n_modules = 1 is mtp_draft's
+ * single module applied k times, n_modules = k gives every depth its own
+ * module, and in between the last module serves the remaining depths.  Depth j
+ * stores its K/V row at position ctx_len[b] + jc of module m's cache and
+ * attends over that cache's positions 0 .. ctx_len[b] + jc, where jc = j - m
+ * is the number of earlier depths of this call that ran module m (jc = j with
+ * one module, 0 with one module per depth).  Each module's E is its embedding
+ * and vocabulary head; pass the same E in every module for the shared head of
+ * the pages.  Everything else, the outputs and the workspace
+ * (mtp_workspace_size(dims, k)) are as for mtp_draft / spec_step.
+ */
+typedef struct {
+    MtpWeights w;
+    void *k_cache, *v_cache; /* [B, Hkv, Lmax, Dh] bf16, this module's own */
+} MtpModule;
+
+int mtp_draft_modules(const MtpDims *dims, const MtpModule *modules, int n_modules,
+                      const void *h, const int32_t *last_tok, const int32_t *ctx_len,
+                      int k, float T, int mode, const float *u_draft,
+                      int32_t *draft_tok, float *draft_logits,
+                      void *ws, size_t ws_bytes, mtp_stream_t stream);
+
+int spec_step_modules(const MtpDims *dims, const MtpModule *modules, int n_modules,
+                      const void *h, const int32_t *last_tok, const int32_t *ctx_len,
+                      int k, float T, int mode, const float *u_draft,
+                      const float *target_logits, const float *u_accept,
+                      const float *u_final, int32_t *draft_tok, float *draft_logits,
+                      int32_t *out_tok, int32_t *accept_len, int32_t *num_accepted,
+                      void *ws, size_t ws_bytes, mtp_stream_t stream);
+
 /* Wait for the stream, then copy the workspace's status word (MTP_STATUS_* bits)
  * to *status.  Returns MTP_OK or MTP_ERR_*. */
 int mtp_get_status(const void *ws, mtp_stream_t stream, int32_t *status);

@@ -44,6 +44,10 @@ class MtpWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_FIELDS]
 
 
+class MtpModule(ctypes.Structure):
+    _fields_ = [("w", MtpWeights), ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p)]
+
+
 _LIB = None
 
 
@@ -69,6 +73,12 @@ def _lib():
         L.spec_step.argtypes = [ctypes.POINTER(MtpDims), ctypes.POINTER(MtpWeights), P, P, P, P, P, I, F, I,
                                 P, P, P, P, P, P, P, P, P, P, Z, P]
         L.spec_step.restype = I
+        L.mtp_draft_modules.argtypes = [ctypes.POINTER(MtpDims), ctypes.POINTER(MtpModule), I, P, P, P, I, F, I,
+                                        P, P, P, P, Z, P]
+        L.mtp_draft_modules.restype = I
+        L.spec_step_modules.argtypes = [ctypes.POINTER(MtpDims), ctypes.POINTER(MtpModule), I, P, P, P, I, F, I,
+                                        P, P, P, P, P, P, P, P, P, P, Z, P]
+        L.spec_step_modules.restype = I
         L.mtp_get_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
         L.mtp_get_status.restype = I
         L.mtp_clear_status.argtypes = [P, P]
@@ -119,6 +129,16 @@ def make_dims(B, d, Hq, Hkv, Dh, F, V, Lmax, eps=1e-6):
 def make_weights(w):
     """MtpWeights from a dict of bf16 CUDA tensors keyed by WEIGHT_FIELDS."""
     return MtpWeights(*[_ptr(w[n], n, torch.bfloat16) for n in WEIGHT_FIELDS])
+
+
+def make_modules(modules):
+    """A ctypes array of MtpModule from (weights dict, k_cache, v_cache) triples;
+    the caches are bf16 CUDA tensors [B, Hkv, Lmax, Dh]."""
+    arr = (MtpModule * len(modules))()
+    for i, (w, kc, vc) in enumerate(modules):
+        arr[i] = MtpModule(make_weights(w), _ptr(kc, "k_cache", torch.bfloat16),
+                           _ptr(vc, "v_cache", torch.bfloat16))
+    return arr
 
 
 def workspace_size(dims, k):
@@ -198,6 +218,41 @@ def spec_step(dims, weights, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode,
         _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
     if rc != 0:
         raise MtpError(rc, "spec_step")
+
+
+def mtp_draft_modules(dims, modules, h, last_tok, ctx_len, k, T, mode, u_draft, draft_tok, draft_logits,
+                      ws, stream=None):
+    """mtp_draft over distinct modules: `modules` from make_modules(); depth j
+    runs module min(j, len(modules) - 1)."""
+    B, V = dims.B, dims.V
+    rc = _lib().mtp_draft_modules(
+        ctypes.byref(dims), modules, len(modules), _ptr(h, "h", torch.bfloat16, B * dims.d),
+        _ptr(last_tok, "last_tok", torch.int32, B), _ptr(ctx_len, "ctx_len", torch.int32, B), int(k),
+        float(T), int(mode), _ptr(u_draft, "u_draft", torch.float32, B * k),
+        _ptr(draft_tok, "draft_tok", torch.int32, B * k),
+        _ptr(draft_logits, "draft_logits", torch.float32, B * k * V),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
+    if rc != 0:
+        raise MtpError(rc, "mtp_draft_modules")
+
+
+def spec_step_modules(dims, modules, h, last_tok, ctx_len, k, T, mode, u_draft, target_logits, u_accept,
+                      u_final, draft_tok, draft_logits, out_tok, accept_len, num_accepted, ws, stream=None):
+    """spec_step over distinct modules (see mtp_draft_modules)."""
+    B, V = dims.B, dims.V
+    rc = _lib().spec_step_modules(
+        ctypes.byref(dims), modules, len(modules), _ptr(h, "h", torch.bfloat16, B * dims.d),
+        _ptr(last_tok, "last_tok", torch.int32, B), _ptr(ctx_len, "ctx_len", torch.int32, B), int(k),
+        float(T), int(mode), _ptr(u_draft, "u_draft", torch.float32, B * k),
+        _ptr(target_logits, "target_logits", torch.float32, B * (k + 1) * V),
+        _ptr(u_accept, "u_accept", torch.float32, B * k), _ptr(u_final, "u_final", torch.float32, B),
+        _ptr(draft_tok, "draft_tok", torch.int32, B * k),
+        _ptr(draft_logits, "draft_logits", torch.float32, B * k * V),
+        _ptr(out_tok, "out_tok", torch.int32, B * (k + 1)), _ptr(accept_len, "accept_len", torch.int32, B),
+        _ptr(num_accepted, "num_accepted", torch.int32, B),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
+    if rc != 0:
+        raise MtpError(rc, "spec_step_modules")
 
 
 def get_status(ws, stream=None):

@@ -137,26 +137,45 @@ cudaError_t timed(int kc, cudaStream_t s, F &&launch) {
   return e;
 }
 
+constexpr int kMaxModules = 8;  // one per depth at most
+
 struct Draft {
   DraftCtx c;
   GemvPlan fc, qkv, wo, gateup, down, lm;
   int attn_cluster;
   bool tc;   // tensor-core path
   TcBufs t;
+  MtpModule mods[kMaxModules];
+  int nmod;
 };
 
-int prepare_draft(const MtpDims *dims, const MtpWeights *w, const void *h, const int32_t *last_tok, void *k_cache,
-                  void *v_cache, const int32_t *ctx_len, int k, float T, int mode, const float *u_draft,
-                  int32_t *draft_tok, float *draft_logits, void *ws, size_t ws_bytes, bool logits_in_ws,
-                  Draft *out) {
+// Point the context at module m's weights and K/V cache.
+void use_module(DraftCtx &c, const MtpModule &m) {
+  auto bf = [](const void *p) { return static_cast<const uint16_t *>(p); };
+  const MtpWeights *w = &m.w;
+  c.E = bf(w->E); c.fc = bf(w->fc); c.wq = bf(w->wq); c.wk = bf(w->wk); c.wv = bf(w->wv); c.wo = bf(w->wo);
+  c.wgate = bf(w->wgate); c.wup = bf(w->wup); c.wdown = bf(w->wdown);
+  c.g_emb = bf(w->g_emb); c.g_hid = bf(w->g_hid); c.g_attn = bf(w->g_attn); c.g_mlp = bf(w->g_mlp);
+  c.g_final = bf(w->g_final);
+  c.kc = static_cast<uint16_t *>(m.k_cache); c.vc = static_cast<uint16_t *>(m.v_cache);
+}
+
+int prepare_draft(const MtpDims *dims, const MtpModule *mods, int nmod, const void *h, const int32_t *last_tok,
+                  const int32_t *ctx_len, int k, float T, int mode, const float *u_draft, int32_t *draft_tok,
+                  float *draft_logits, void *ws, size_t ws_bytes, bool logits_in_ws, Draft *out) {
   int rc = check_dims(dims, k);
   if (rc) return rc;
-  if (!w) return MTP_ERR_INVALID_ARG;
+  if (!mods || nmod < 1 || nmod > k) return MTP_ERR_INVALID_ARG;
   if (mode != MTP_GREEDY && mode != MTP_STOCHASTIC) return MTP_ERR_INVALID_ARG;
   if (mode == MTP_STOCHASTIC && !(T > 0.f && T < 1e30f)) return MTP_ERR_INVALID_ARG;
-  const void *ptrs[] = {w->E, w->fc, w->wq, w->wk, w->wv, w->wo, w->wgate, w->wup, w->wdown, w->g_emb,
-                        w->g_hid, w->g_attn, w->g_mlp, w->g_final, h, last_tok, k_cache, v_cache, ctx_len,
-                        draft_tok, ws};
+  for (int m = 0; m < nmod; ++m) {
+    const MtpWeights *w = &mods[m].w;
+    const void *wp[] = {w->E, w->fc, w->wq, w->wk, w->wv, w->wo, w->wgate, w->wup, w->wdown, w->g_emb,
+                        w->g_hid, w->g_attn, w->g_mlp, w->g_final, mods[m].k_cache, mods[m].v_cache};
+    for (const void *p : wp)
+      if (!aligned16(p)) return MTP_ERR_INVALID_ARG;
+  }
+  const void *ptrs[] = {h, last_tok, ctx_len, draft_tok, ws};
   for (const void *p : ptrs)
     if (!aligned16(p)) return MTP_ERR_INVALID_ARG;
   if (mode == MTP_STOCHASTIC && !aligned16(u_draft)) return MTP_ERR_INVALID_ARG;
@@ -172,14 +191,11 @@ int prepare_draft(const MtpDims *dims, const MtpWeights *w, const void *h, const
   DraftCtx &c = out->c;
   c = DraftCtx{};
   c.B = d.B; c.d = d.d; c.Hq = d.Hq; c.Hkv = d.Hkv; c.Dh = d.Dh; c.F = d.F; c.V = d.V; c.Lmax = d.Lmax;
-  c.k = k; c.j = 0; c.mode = mode; c.eps = d.rms_eps; c.T = mode == MTP_STOCHASTIC ? T : 1.f;
-  auto bf = [](const void *p) { return static_cast<const uint16_t *>(p); };
-  c.E = bf(w->E); c.fc = bf(w->fc); c.wq = bf(w->wq); c.wk = bf(w->wk); c.wv = bf(w->wv); c.wo = bf(w->wo);
-  c.wgate = bf(w->wgate); c.wup = bf(w->wup); c.wdown = bf(w->wdown);
-  c.g_emb = bf(w->g_emb); c.g_hid = bf(w->g_hid); c.g_attn = bf(w->g_attn); c.g_mlp = bf(w->g_mlp);
-  c.g_final = bf(w->g_final);
-  c.h = bf(h); c.last_tok = last_tok; c.ctx_len = ctx_len; c.u_draft = u_draft;
-  c.kc = static_cast<uint16_t *>(k_cache); c.vc = static_cast<uint16_t *>(v_cache);
+  c.k = k; c.j = 0; c.jc = 0; c.mode = mode; c.eps = d.rms_eps; c.T = mode == MTP_STOCHASTIC ? T : 1.f;
+  use_module(c, mods[0]);
+  for (int m = 0; m < nmod; ++m) out->mods[m] = mods[m];
+  out->nmod = nmod;
+  c.h = static_cast<const uint16_t *>(h); c.last_tok = last_tok; c.ctx_len = ctx_len; c.u_draft = u_draft;
   c.draft_tok = draft_tok;
   char *base = static_cast<char *>(ws);
   c.logits = draft_logits ? draft_logits : (logits_in_ws ? reinterpret_cast<float *>(base + L.logits) : nullptr);
@@ -226,7 +242,11 @@ cudaError_t run_draft(Draft &D, cudaStream_t s) {
   const bool pdl = use_pdl();
   for (int j = 0; j < D.c.k && e == cudaSuccess; ++j) {
     DraftCtx c = D.c;
+    // depth j runs module min(j, nmod - 1), at the next row of that module's cache
+    const int m = j < D.nmod ? j : D.nmod - 1;
+    use_module(c, D.mods[m]);
     c.j = j;
+    c.jc = j - m;
     c.zero_counters = j == 0;
     if (D.tc) {  // tensor-core path
       if ((e = timed(MTP_KC_GEMV, s, [&] { return run_block_pre_tc(c, D.t, s, pdl); }))) break;
@@ -317,17 +337,27 @@ size_t mtp_workspace_size(const MtpDims *dims, int k) {
   return draft_layout(*dims, k).total;
 }
 
-int mtp_draft(const MtpDims *dims, const MtpWeights *w, const void *h, const int32_t *last_tok, void *k_cache,
-              void *v_cache, const int32_t *ctx_len, int k, float T, int mode, const float *u_draft,
-              int32_t *draft_tok, float *draft_logits, void *ws, size_t ws_bytes, mtp_stream_t stream) {
+int mtp_draft_modules(const MtpDims *dims, const MtpModule *modules, int n_modules, const void *h,
+                      const int32_t *last_tok, const int32_t *ctx_len, int k, float T, int mode,
+                      const float *u_draft, int32_t *draft_tok, float *draft_logits, void *ws, size_t ws_bytes,
+                      mtp_stream_t stream) {
   Draft D;
-  int rc = prepare_draft(dims, w, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode, u_draft, draft_tok,
+  int rc = prepare_draft(dims, modules, n_modules, h, last_tok, ctx_len, k, T, mode, u_draft, draft_tok,
                          draft_logits, ws, ws_bytes, false, &D);
   if (rc) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = run_draft(D, s);
   if (e == cudaSuccess) e = cudaGetLastError();
   return cuda_rc(e);
+}
+
+int mtp_draft(const MtpDims *dims, const MtpWeights *w, const void *h, const int32_t *last_tok, void *k_cache,
+              void *v_cache, const int32_t *ctx_len, int k, float T, int mode, const float *u_draft,
+              int32_t *draft_tok, float *draft_logits, void *ws, size_t ws_bytes, mtp_stream_t stream) {
+  if (!w) return MTP_ERR_INVALID_ARG;
+  const MtpModule one{*w, k_cache, v_cache};
+  return mtp_draft_modules(dims, &one, 1, h, last_tok, ctx_len, k, T, mode, u_draft, draft_tok, draft_logits, ws,
+                           ws_bytes, stream);
 }
 
 int mtp_draft_noalloc(const MtpDims *dims, const MtpWeights *w, const void *h, const int32_t *last_tok,
@@ -338,11 +368,13 @@ int mtp_draft_noalloc(const MtpDims *dims, const MtpWeights *w, const void *h, c
   if (rc) return rc;
   if (draft_layout(*dims, k).total > MTP_STATIC_SCRATCH_BYTES) return MTP_ERR_SCRATCH_LIMIT;
   if (status && (reinterpret_cast<uintptr_t>(status) & 3u) != 0) return MTP_ERR_INVALID_ARG;
+  if (!w) return MTP_ERR_INVALID_ARG;
   void *scratch = nullptr;
   if ((rc = static_scratch(&scratch))) return rc;
+  const MtpModule one{*w, k_cache, v_cache};
   Draft D;
-  rc = prepare_draft(dims, w, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode, u_draft, draft_tok, draft_logits,
-                     scratch, MTP_STATIC_SCRATCH_BYTES, false, &D);
+  rc = prepare_draft(dims, &one, 1, h, last_tok, ctx_len, k, T, mode, u_draft, draft_tok, draft_logits, scratch,
+                     MTP_STATIC_SCRATCH_BYTES, false, &D);
   if (rc) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the status word and the LM-head ticket counter (the first two aligned
@@ -376,13 +408,13 @@ int spec_verify(int B, int k, int V, float T, int mode, const float *target_logi
   return cuda_rc(e);
 }
 
-int spec_step(const MtpDims *dims, const MtpWeights *w, const void *h, const int32_t *last_tok, void *k_cache,
-              void *v_cache, const int32_t *ctx_len, int k, float T, int mode, const float *u_draft,
-              const float *target_logits, const float *u_accept, const float *u_final, int32_t *draft_tok,
-              float *draft_logits, int32_t *out_tok, int32_t *accept_len, int32_t *num_accepted, void *ws,
-              size_t ws_bytes, mtp_stream_t stream) {
+int spec_step_modules(const MtpDims *dims, const MtpModule *modules, int n_modules, const void *h,
+                      const int32_t *last_tok, const int32_t *ctx_len, int k, float T, int mode,
+                      const float *u_draft, const float *target_logits, const float *u_accept,
+                      const float *u_final, int32_t *draft_tok, float *draft_logits, int32_t *out_tok,
+                      int32_t *accept_len, int32_t *num_accepted, void *ws, size_t ws_bytes, mtp_stream_t stream) {
   Draft D;
-  int rc = prepare_draft(dims, w, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode, u_draft, draft_tok,
+  int rc = prepare_draft(dims, modules, n_modules, h, last_tok, ctx_len, k, T, mode, u_draft, draft_tok,
                          draft_logits, ws, ws_bytes, mode == MTP_STOCHASTIC, &D);
   if (rc) return rc;
   VerifyArgs a{};
@@ -396,6 +428,17 @@ int spec_step(const MtpDims *dims, const MtpWeights *w, const void *h, const int
   if (e == cudaSuccess) e = timed(MTP_KC_VERIFY, s, [&] { return launch_verify(a, s, use_pdl()); });
   if (e == cudaSuccess) e = cudaGetLastError();
   return cuda_rc(e);
+}
+
+int spec_step(const MtpDims *dims, const MtpWeights *w, const void *h, const int32_t *last_tok, void *k_cache,
+              void *v_cache, const int32_t *ctx_len, int k, float T, int mode, const float *u_draft,
+              const float *target_logits, const float *u_accept, const float *u_final, int32_t *draft_tok,
+              float *draft_logits, int32_t *out_tok, int32_t *accept_len, int32_t *num_accepted, void *ws,
+              size_t ws_bytes, mtp_stream_t stream) {
+  if (!w) return MTP_ERR_INVALID_ARG;
+  const MtpModule one{*w, k_cache, v_cache};
+  return spec_step_modules(dims, &one, 1, h, last_tok, ctx_len, k, T, mode, u_draft, target_logits, u_accept,
+                           u_final, draft_tok, draft_logits, out_tok, accept_len, num_accepted, ws, ws_bytes, stream);
 }
 
 int mtp_get_status(const void *ws, mtp_stream_t stream, int32_t *status) {

@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) attn_tc_kernel(const __grid_con
   const int group = c.Hq / c.Hkv;
   int L = __ldg(&c.ctx_len[b]);
   L = min(max(L, 0), c.Lmax - c.k);
-  const int ntok = L + c.j + 1;
+  const int ntok = L + c.jc + 1;
   const int T = (ntok + C - 1) / C;
   const int r0 = min(ntok, rank * T), r1 = min(ntok, r0 + T);
   const int ntiles = (r1 - r0 + kTcRows - 1) / kTcRows;

@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(DraftCtx c, GemvPlan
             int L = __ldg(&c.ctx_len[b]);
             if (L < 0 || L + c.k > c.Lmax) set_status(c.status, kStatusBadCtx);
             L = min(max(L, 0), c.Lmax - c.k);
-            const size_t idx = (((size_t)b * c.Hkv + kvh) * c.Lmax + L + c.j) * c.Dh + dd;
+            const size_t idx = (((size_t)b * c.Hkv + kvh) * c.Lmax + L + c.jc) * c.Dh + dd;
             cache[idx] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
           }
         } else if (OP == OP_WO) {
@@ -413,7 +413,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(DraftCtx c) {
   const int group = c.Hq / c.Hkv;
   int L = __ldg(&c.ctx_len[b]);
   L = min(max(L, 0), c.Lmax - c.k);
-  const int ntok = L + c.j + 1;
+  const int ntok = L + c.jc + 1;
   const int T = (ntok + C - 1) / C;
   const int r0 = min(ntok, rank * T), r1 = min(ntok, r0 + T);
   const int ntiles = (r1 - r0 + TT - 1) / TT;

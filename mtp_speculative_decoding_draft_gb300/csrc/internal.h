@@ -13,6 +13,8 @@ namespace mtp {
 struct DraftCtx {
   // shape
   int B, d, Hq, Hkv, Dh, F, V, Lmax, k, j, mode;
+  int jc;                 // this depth's cache row past ctx_len: depths of this call
+                          // that ran the same module before it (j with one module)
   float eps, T;
   // weights (bf16)
   const uint16_t *E, *fc, *wq, *wk, *wv, *wo, *wgate, *wup, *wdown;

@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(kPrepThreads) tc_mid_kernel(DraftCtx c, TcBufs
         uint16_t *cache = rr < nkv ? c.kc : c.vc;
         if (rr >= nkv) rr -= nkv;
         const int kvh = rr / c.Dh, dd = rr % c.Dh;  // 8 | Dh: the eight stay in one head
-        uint16_t *dst = cache + (((size_t)b * c.Hkv + kvh) * c.Lmax + L + c.j) * c.Dh + dd;
+        uint16_t *dst = cache + (((size_t)b * c.Hkv + kvh) * c.Lmax + L + c.jc) * c.Dh + dd;
 #pragma unroll
         for (int q = 0; q < 8; ++q) dst[q] = __bfloat16_as_ushort(__float2bfloat16_rn(y[q]));
       }

@@ -20,13 +20,24 @@ def to_device(x, device="cuda"):
 
 
 class DraftModule:
-    """The MTP module's weights on the device plus the per-step buffers."""
+    """The MTP module's weights on the device plus the per-step buffers.
 
-    def __init__(self, w, weights_bits, device="cuda", k=None):
+    extra_modules: weights (bf16 bits) of further distinct modules for depths 1,
+    2, ... (the chain then runs mtp_draft_modules / spec_step_modules); their E
+    is not uploaded again, every module uses this one's.
+    """
+
+    def __init__(self, w, weights_bits, device="cuda", k=None, extra_modules=()):
         self.w = w
         self.k = w.k if k is None else k
         self.device = device
         self.weights = {n: to_device_bf16(weights_bits[n], device) for n in bd.WEIGHT_FIELDS}
+        self.extra = []
+        for bits in extra_modules:
+            wd = {n: to_device_bf16(bits[n], device) for n in bd.WEIGHT_FIELDS if n != "E"}
+            wd["E"] = self.weights["E"]
+            self.extra.append(wd)
+        self.mods = None
         self.dims = bd.make_dims(w.B, w.d, w.Hq, w.Hkv, w.Dh, w.F, w.V, w.ctx_max + self.k, w.eps)
         self.wptr = bd.make_weights(self.weights)
         self.ws = bd.alloc_workspace(bd.workspace_size(self.dims, self.k), device)
@@ -37,25 +48,42 @@ class DraftModule:
         self.accept_len = torch.zeros(B, dtype=torch.int32, device=device)
         self.num_accepted = torch.zeros(B, dtype=torch.int32, device=device)
 
-    def set_context(self, ctx):
-        """Upload h, last_tok, ctx_len and the K/V caches (numpy from workloads)."""
+    def set_context(self, ctx, extra_caches=()):
+        """Upload h, last_tok, ctx_len and the K/V caches (numpy from workloads);
+        extra_caches: (k_cache, v_cache) of each extra module."""
         self.h = to_device_bf16(ctx["h"], self.device)
         self.last_tok = to_device(ctx["last_tok"].astype(np.int32), self.device)
         self.ctx_len = to_device(ctx["ctx_len"].astype(np.int32), self.device)
         self.k_cache = to_device_bf16(ctx["k_cache"], self.device)
         self.v_cache = to_device_bf16(ctx["v_cache"], self.device)
+        if self.extra:
+            if len(extra_caches) != len(self.extra):
+                raise ValueError("one (k_cache, v_cache) pair per extra module")
+            self.extra_caches = [(to_device_bf16(kc, self.device), to_device_bf16(vc, self.device))
+                                 for kc, vc in extra_caches]
+            self.mods = bd.make_modules([(self.weights, self.k_cache, self.v_cache)] +
+                                        [(wd, kc, vc) for wd, (kc, vc) in zip(self.extra, self.extra_caches)])
 
     def draft(self, T, mode, u_draft=None, logits=True, stream=None):
+        lg = self.draft_logits if logits else None
+        if self.mods is not None:
+            bd.mtp_draft_modules(self.dims, self.mods, self.h, self.last_tok, self.ctx_len, self.k, T, mode,
+                                 u_draft, self.draft_tok, lg, self.ws, stream)
+            return
         bd.mtp_draft(self.dims, self.wptr, self.h, self.last_tok, self.k_cache, self.v_cache,
-                     self.ctx_len, self.k, T, mode, u_draft, self.draft_tok,
-                     self.draft_logits if logits else None, self.ws, stream)
+                     self.ctx_len, self.k, T, mode, u_draft, self.draft_tok, lg, self.ws, stream)
 
     def step(self, T, mode, target_logits, u_draft=None, u_accept=None, u_final=None,
              logits=True, stream=None):
+        lg = self.draft_logits if logits else None
+        if self.mods is not None:
+            bd.spec_step_modules(self.dims, self.mods, self.h, self.last_tok, self.ctx_len, self.k, T, mode,
+                                 u_draft, target_logits, u_accept, u_final, self.draft_tok, lg, self.out_tok,
+                                 self.accept_len, self.num_accepted, self.ws, stream)
+            return
         bd.spec_step(self.dims, self.wptr, self.h, self.last_tok, self.k_cache, self.v_cache,
                      self.ctx_len, self.k, T, mode, u_draft, target_logits, u_accept, u_final,
-                     self.draft_tok, self.draft_logits if logits else None, self.out_tok,
-                     self.accept_len, self.num_accepted, self.ws, stream)
+                     self.draft_tok, lg, self.out_tok, self.accept_len, self.num_accepted, self.ws, stream)
 
     def status(self, stream=None):
         return bd.get_status(self.ws, stream)

@@ -190,6 +190,35 @@ def make_weights(w, master=False):
     return (bits, full) if master else bits
 
 
+def make_module_weights(w, m, E=None):
+    """Weights of module m of a chain of distinct modules, as bf16 bits.
+
+    Module 0 is make_weights' module.  Module m >= 1 draws its own input
+    projection, block and gains from streams named "w<m>.<name>"; the embedding
+    and vocabulary head E is shared, so every module returns module 0's E (drawn
+    again unless the caller passes it in).
+    """
+    if m == 0:
+        return make_weights(w)
+    if E is None:
+        E = to_bf16_bits(normal(w.seed, "w.E", weight_shapes(w)["E"], std=w.w_std))
+    bits = {"E": E}
+    for name, shape in weight_shapes(w).items():
+        if name != "E":
+            bits[name] = to_bf16_bits(normal(w.seed, "w%d.%s" % (m, name), shape, std=w.w_std))
+    for name in GAIN_NAMES:
+        bits[name] = to_bf16_bits(normal(w.seed, "w%d.%s" % (m, name), (w.d,), std=w.w_std, mean=1.0))
+    return bits
+
+
+def make_module_cache(w, m):
+    """K/V caches [B, Hkv, Lmax, Dh] bf16 N(0,1) of module m (m = 0: make_context's)."""
+    shape = (w.B, w.Hkv, w.Lmax, w.Dh)
+    suffix = "" if m == 0 else str(m)
+    return (to_bf16_bits(normal(w.seed, "k_cache" + suffix, shape)),
+            to_bf16_bits(normal(w.seed, "v_cache" + suffix, shape)))
+
+
 def make_context(w):
     """Per-step inputs of the drafter.
 

@@ -175,12 +175,40 @@ def mtp_draft(W, dims, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode,
     Returns a dict with draft_tok [n,k], draft_logits [n,k,V] (float32 values),
     hidden [n,k,d] (x2 of every depth), k_new / v_new [n,k,Hkv,Dh] (bf16 values).
     """
+    return mtp_draft_modules([(W, k_cache, v_cache)], dims, h, last_tok, ctx_len, k, T, mode,
+                             u_draft, seqs)
+
+
+def module_of_depth(j, n_modules):
+    """The module depth j runs when a chain has n_modules distinct modules: its
+    own while there are enough (DeepSeek-V3's one module per future token,
+    "Optimize vLLM speculative decoding with FastMTP heads", sections "What is
+    multi-token prediction?" and "Why fine-tune a single MTP head"), else the
+    last one again (one module reused at every depth when n_modules = 1)."""
+    return min(j, n_modules - 1)
+
+
+def mtp_draft_modules(modules, dims, h, last_tok, ctx_len, k, T, mode, u_draft=None, seqs=None):
+    """The chain over distinct modules.
+
+    modules  list of (W, k_cache, v_cache): each module's weights and its own
+             K/V cache (each module has its own attention).  Depth j runs module
+             m = module_of_depth(j, len(modules)); it attends over module m's
+             context rows [0, ctx_len[b]) plus the rows this call appended to
+             that cache, its own last, so its row lands at position ctx_len[b] +
+             (number of earlier depths that ran module m).
+    Other arguments and the returned dict as ``mtp_draft``; the dict also holds
+    module [k] (the module of each depth) and row [n, k] (the cache position of
+    each depth's K/V row in its module's cache).
+    """
     seqs = list(range(np.asarray(last_tok).shape[0])) if seqs is None else list(seqs)
     n = len(seqs)
     x = as_f64(np.asarray(h)[seqs])
     tok = np.asarray(last_tok)[seqs].astype(np.int64)
-    keys = [as_f64(np.asarray(k_cache)[b, :, :int(ctx_len[b]), :]) for b in seqs]
-    values = [as_f64(np.asarray(v_cache)[b, :, :int(ctx_len[b]), :]) for b in seqs]
+    keys, values = [], []
+    for (_, kc, vc) in modules:
+        keys.append([as_f64(np.asarray(kc)[b, :, :int(ctx_len[b]), :]) for b in seqs])
+        values.append([as_f64(np.asarray(vc)[b, :, :int(ctx_len[b]), :]) for b in seqs])
 
     out = {
         "draft_tok": np.zeros((n, k), dtype=np.int64),
@@ -188,18 +216,25 @@ def mtp_draft(W, dims, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode,
         "hidden": np.zeros((n, k, dims.d), dtype=np.float64),
         "k_new": np.zeros((n, k, dims.Hkv, dims.Dh), dtype=np.float64),
         "v_new": np.zeros((n, k, dims.Hkv, dims.Dh), dtype=np.float64),
+        "module": np.zeros(k, dtype=np.int64),
+        "row": np.zeros((n, k), dtype=np.int64),
     }
     for j in range(k):
-        x, logits, k_new, v_new = draft_depth(W, dims, x, tok, keys, values)
+        m = module_of_depth(j, len(modules))
+        W = modules[m][0]
+        for i in range(n):
+            out["row"][i, j] = keys[m][i].shape[1]
+        x, logits, k_new, v_new = draft_depth(W, dims, x, tok, keys[m], values[m])
         logits = round_f32(logits)
         for i, b in enumerate(seqs):
             u = None if mode == GREEDY else float(u_draft[b][j])
             out["draft_tok"][i, j] = select_token(logits[i], mode, T, u)
-            keys[i] = np.concatenate([keys[i], k_new[i][:, None, :]], axis=1)
-            values[i] = np.concatenate([values[i], v_new[i][:, None, :]], axis=1)
+            keys[m][i] = np.concatenate([keys[m][i], k_new[i][:, None, :]], axis=1)
+            values[m][i] = np.concatenate([values[m][i], v_new[i][:, None, :]], axis=1)
         out["draft_logits"][:, j] = logits
         out["hidden"][:, j] = x
         out["k_new"][:, j] = k_new
         out["v_new"][:, j] = v_new
+        out["module"][j] = m
         tok = out["draft_tok"][:, j].copy()
     return out

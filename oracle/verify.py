@@ -106,9 +106,16 @@ def spec_step(W, dims, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode,
     Returns (draft result dict from ``block.mtp_draft``, out_tok, accept_len,
     num_accepted) for the sequences in ``seqs``.
     """
-    from .block import mtp_draft
+    return spec_step_modules([(W, k_cache, v_cache)], dims, h, last_tok, ctx_len, k, T, mode,
+                             target_logits, u_draft, u_accept, u_final, seqs)
+
+
+def spec_step_modules(modules, dims, h, last_tok, ctx_len, k, T, mode, target_logits,
+                      u_draft=None, u_accept=None, u_final=None, seqs=None):
+    """``spec_step`` over a chain of distinct modules (``block.mtp_draft_modules``)."""
+    from .block import mtp_draft_modules
     seqs = list(range(np.asarray(last_tok).shape[0])) if seqs is None else list(seqs)
-    dr = mtp_draft(W, dims, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode, u_draft, seqs)
+    dr = mtp_draft_modules(modules, dims, h, last_tok, ctx_len, k, T, mode, u_draft, seqs)
     tl = np.asarray(target_logits)[seqs]
     ua = None if u_accept is None else np.asarray(u_accept)[seqs]
     uf = None if u_final is None else np.asarray(u_final)[seqs]

@@ -28,3 +28,15 @@ def test_tc_batch_of_20(mode):
 def test_tc_two_batch_groups(mode):
     r = run_draft_parity(TC150, mode, TC150.T, seqs=[0, 63, 127, 128, 149])
     print("tc150 mode=%d max rel L2 %.3g excused %d" % (mode, max(r["rel_l2"]), r["excused"]))
+
+
+# Batch of 40: MMA columns padded to 64, the three activation terms side by side
+# in one MMA of N = 192.
+TC40 = W.Workload("tc_b40_d384_v4099", B=40, k=3, V=4099, d=384, Hq=6, Hkv=2, Dh=64, F=1152,
+                  ctx=(1, 150), T=0.9, seed=2005)
+
+
+@pytest.mark.parametrize("mode", [GREEDY, STOCH])
+def test_tc_batch_of_40(mode):
+    r = run_draft_parity(TC40, mode, TC40.T, seqs=[0, 17, 31, 32, 39])
+    print("tc40 mode=%d max rel L2 %.3g excused %d" % (mode, max(r["rel_l2"]), r["excused"]))
