@@ -64,6 +64,15 @@ NCU_TRAFFIC = {
             "csrc/common.cuh": "fcd7bd8f56df32fc490b2c47f2fbc0f7f37047c578430d777438202c9279de66",
         },
     },
+    ("tc_gemm_kernel(LM head)", "batched_stochastic_b64_d4096_v151936_ctx1024-8192"): {
+        "bytes": 1248202496 + 8034560,
+        "sources": {
+            "csrc/tc.cu": "3d947329414032c4b0d4b009ab2a06f7151e432ae1bab6231c28f36531157949",
+            "csrc/tcgen05.cuh": "e128ff6d7c8451d618848063024b7cd0a98c722dd1b86ef0d04e6a07a9070ee7",
+            "csrc/common.cuh": "fcd7bd8f56df32fc490b2c47f2fbc0f7f37047c578430d777438202c9279de66",
+            "csrc/internal.h": "f3fa200359aee7e9705348b45c4914b9e60226a11e00a6c5c83253788e3a260c",
+        },
+    },
     ("verify_kernel", "verify_sweep_b256_v151936_k3/greedy"): {
         "bytes": 622490880 + 3303680,
         "sources": {
