@@ -161,6 +161,36 @@ def select_token(logits, mode, T, u):
     return inverse_cdf(np.exp((z - np.max(z)) / T), u)
 
 
+def draft_confidence(logits, mode, T):
+    """The draft's largest probability at one depth: max_i q(i), with q the
+    distribution the draft token is taken from -- softmax(logits / T) when
+    stochastic, softmax(logits) when greedy.  Written as 1 / sum_i exp((l_i -
+    max) / T), in float64."""
+    z = np.asarray(logits, dtype=np.float64)
+    t = T if mode == STOCHASTIC else 1.0
+    return 1.0 / float(np.sum(np.exp((z - np.max(z)) / t)))
+
+
+def dynamic_depths(draft_logits, mode, T, stop_p):
+    """Drafts each sequence keeps under a dynamic draft length ("Faster
+    Rollouts with MTP Speculative Decoding", section "What's Next", names
+    dynamic draft length without a rule; the reading taken here): the chain of
+    sequence b stops at the first depth j whose draft confidence is below
+    stop_p, keeping the j drafts before it; k if no depth falls below.
+
+    draft_logits [n, k, V] (float32 values).  Returns k_eff [n] in 0..k.
+    """
+    dl = np.asarray(draft_logits)
+    n, k = dl.shape[0], dl.shape[1]
+    out = np.full(n, k, dtype=np.int64)
+    for i in range(n):
+        for j in range(k):
+            if draft_confidence(dl[i, j], mode, T) < stop_p:
+                out[i] = j
+                break
+    return out
+
+
 def mtp_draft(W, dims, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode,
               u_draft=None, seqs=None):
     """Run the module k times in a chain and return the drafts.

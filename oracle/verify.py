@@ -71,11 +71,14 @@ def verify_stochastic_one(target, draft, draft_tok, u_accept, u_final, T):
 
 
 def spec_verify(target_logits, draft_logits, draft_tok, mode, T=1.0,
-                u_accept=None, u_final=None, seqs=None):
+                u_accept=None, u_final=None, seqs=None, k_eff=None):
     """Batched verification.
 
     target_logits [B, k+1, V]; draft_logits [B, k, V] (unused when greedy);
-    draft_tok [B, k]; u_accept [B, k]; u_final [B].
+    draft_tok [B, k]; u_accept [B, k]; u_final [B]; k_eff [B] (optional): the
+    drafts sequence b keeps (a dynamic draft length, ``block.dynamic_depths``);
+    its verification then sees only drafts 0..k_eff-1 and target rows
+    0..k_eff, the bonus row being row k_eff.
     Returns out_tok [n, k+1] (padded with -1), accept_len [n] (= a + 1) and
     num_accepted [n] (= a) for the sequences in ``seqs`` (all by default).
     """
@@ -87,12 +90,13 @@ def spec_verify(target_logits, draft_logits, draft_tok, mode, T=1.0,
     accept_len = np.zeros(len(seqs), dtype=np.int64)
     num_accepted = np.zeros(len(seqs), dtype=np.int64)
     for i, b in enumerate(seqs):
-        t = target_logits[b].astype(np.float64)
+        kb = k if k_eff is None else int(k_eff[b])
+        t = target_logits[b, :kb + 1].astype(np.float64)
         if mode == GREEDY:
-            toks, a = verify_greedy_one(t, draft_tok[b])
+            toks, a = verify_greedy_one(t, draft_tok[b][:kb])
         else:
-            toks, a = verify_stochastic_one(t, np.asarray(draft_logits[b], np.float64),
-                                            draft_tok[b], u_accept[b], float(u_final[b]), T)
+            toks, a = verify_stochastic_one(t, np.asarray(draft_logits[b][:kb], np.float64),
+                                            draft_tok[b][:kb], u_accept[b][:kb], float(u_final[b]), T)
         out_tok[i, :len(toks)] = toks
         accept_len[i] = a + 1
         num_accepted[i] = a
@@ -100,24 +104,31 @@ def spec_verify(target_logits, draft_logits, draft_tok, mode, T=1.0,
 
 
 def spec_step(W, dims, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode,
-              target_logits, u_draft=None, u_accept=None, u_final=None, seqs=None):
-    """Draft k tokens with the chained module, then verify them.
+              target_logits, u_draft=None, u_accept=None, u_final=None, seqs=None, stop_p=None):
+    """Draft k tokens with the chained module, then verify them.  With stop_p,
+    each sequence keeps the drafts before its first depth of confidence below
+    stop_p (``block.dynamic_depths``; the result dict then holds k_eff).
 
     Returns (draft result dict from ``block.mtp_draft``, out_tok, accept_len,
     num_accepted) for the sequences in ``seqs``.
     """
     return spec_step_modules([(W, k_cache, v_cache)], dims, h, last_tok, ctx_len, k, T, mode,
-                             target_logits, u_draft, u_accept, u_final, seqs)
+                             target_logits, u_draft, u_accept, u_final, seqs, stop_p)
 
 
 def spec_step_modules(modules, dims, h, last_tok, ctx_len, k, T, mode, target_logits,
-                      u_draft=None, u_accept=None, u_final=None, seqs=None):
+                      u_draft=None, u_accept=None, u_final=None, seqs=None, stop_p=None):
     """``spec_step`` over a chain of distinct modules (``block.mtp_draft_modules``)."""
-    from .block import mtp_draft_modules
+    from .block import dynamic_depths, mtp_draft_modules
     seqs = list(range(np.asarray(last_tok).shape[0])) if seqs is None else list(seqs)
     dr = mtp_draft_modules(modules, dims, h, last_tok, ctx_len, k, T, mode, u_draft, seqs)
     tl = np.asarray(target_logits)[seqs]
     ua = None if u_accept is None else np.asarray(u_accept)[seqs]
     uf = None if u_final is None else np.asarray(u_final)[seqs]
-    out_tok, accept_len, num_acc = spec_verify(tl, dr["draft_logits"], dr["draft_tok"], mode, T, ua, uf)
+    k_eff = None
+    if stop_p is not None:
+        k_eff = dynamic_depths(dr["draft_logits"], mode, T, stop_p)
+        dr["k_eff"] = k_eff
+    out_tok, accept_len, num_acc = spec_verify(tl, dr["draft_logits"], dr["draft_tok"], mode, T, ua, uf,
+                                               k_eff=k_eff)
     return dr, out_tok, accept_len, num_acc
