@@ -33,15 +33,16 @@ def block_elements(w):
     return (w.d * 2 * w.d + (w.Hq + 2 * w.Hkv) * w.Dh * w.d + w.d * w.Hq * w.Dh + 3 * w.d * w.F + 5 * w.d)
 
 
-def step_bytes(w, ctx_len, logits_out, n_modules=1):
+def step_bytes(w, ctx_len, logits_out, n_modules=1, depths=None):
     """Algorithmic HBM bytes of one spec_step: weights re-streamed at every
     depth, the visible KV rows read once per depth, target logits read once,
     draft logits written and read once when they are materialised.  With
     distinct modules depth j runs module min(j, n - 1) and sees that module's
     context plus the rows earlier depths appended to the same cache."""
     k = w.k
-    weights = k * (block_elements(w) + w.V * w.d) * 2
-    kv = sum(int(L) + j - min(j, n_modules - 1) + 1 for L in ctx_len for j in range(k)) * w.Hkv * w.Dh * 2 * 2
+    kd = k if depths is None else depths  # depths whose weights are streamed (a stopped chain skips the rest)
+    weights = kd * (block_elements(w) + w.V * w.d) * 2
+    kv = sum(int(L) + j - min(j, n_modules - 1) + 1 for L in ctx_len for j in range(kd)) * w.Hkv * w.Dh * 2 * 2
     target = w.B * (k + 1) * w.V * 4
     draft = 2 * w.B * k * w.V * 4 if logits_out else 0
     return weights + kv + target + draft
@@ -227,7 +228,10 @@ def run_reference(args):
 
 def config_of(w, args):
     mods = getattr(args, "modules", 1)
-    return {"workload": w.name + ("_modules%d" % mods if mods > 1 else ""), "modules": mods, "B": w.B, "k": w.k, "d": w.d, "Hq": w.Hq, "Hkv": w.Hkv, "Dh": w.Dh, "F": w.F,
+    sp = getattr(args, "stop_p", None)
+    name = w.name + ("_modules%d" % mods if mods > 1 else "") + ("_stop%g" % sp if sp is not None else "")
+    return {"workload": name, "modules": mods, "stop_p": sp, "B": w.B, "k": w.k, "d": w.d, "Hq": w.Hq, "Hkv": w.Hkv,
+            "Dh": w.Dh, "F": w.F,
             "V": w.V, "ctx": w.ctx if not isinstance(w.ctx, tuple) else list(w.ctx),
             "mode": "greedy" if w.mode == 0 else "stochastic", "T": w.T,
             "parallelism": "replicas%d" % args.gpus, "l2": "inputs larger than L2 (weights %.2f GB re-streamed per depth)"
@@ -327,6 +331,8 @@ def run_ours(args):
     ctx = W.make_context(w)
     u = W.make_uniforms(w)
     nm = max(1, min(args.modules, w.k))
+    if args.stop_p is not None and nm > 1:
+        raise SystemExit("--stop-p runs one module (spec_step_dynamic); drop --modules")
     extra = [W.make_module_weights(w, i, E=wts["E"]) for i in range(1, nm)]
     caches = [W.make_module_cache(w, i) for i in range(1, nm)]
     m = DraftModule(w, wts, extra_modules=extra)
@@ -351,7 +357,10 @@ def run_ours(args):
     logits_out = stoch
 
     def step(stream=None):
-        m.step(w.T, w.mode, target_d, ud, ua, uf, logits=logits_out, stream=stream)
+        if args.stop_p is not None:
+            m.step_dynamic(w.T, w.mode, args.stop_p, target_d, ud, ua, uf, logits=logits_out, stream=stream)
+        else:
+            m.step(w.T, w.mode, target_d, ud, ua, uf, logits=logits_out, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -443,7 +452,12 @@ def run_ours(args):
         return
 
     peak, peak_kind = measured_peaks()
-    sb = step_bytes(w, ctx["ctx_len"], logits_out, nm)
+    depths = None
+    if args.stop_p is not None:
+        ke = m.k_eff.cpu().numpy()
+        # weight-streaming launches of batches of up to 4 return once every sequence has stopped
+        depths = min(w.k, int(ke.max()) + 1) if w.B <= 4 else w.k
+    sb = step_bytes(w, ctx["ctx_len"], logits_out, nm, depths)
     steps_s = 1e3 / ms * world
     tokens_per_step = float(L.sum())
     lm_avg = lm_ms / max(lm_n, 1)
@@ -458,6 +472,7 @@ def run_ours(args):
         "config": config_of(w, args),
         "accepted_tok_s": steps_s * tokens_per_step,
         "accept_len_mean": float(L.mean()),
+        "k_eff_mean": float(m.k_eff.float().mean().item()) if args.stop_p is not None else None,
         "hbm_bytes_per_step": sb,
         "hbm_roofline_frac": sb / (ms * 1e-3) / 1e9 / peak,
         "roofline": {"bound": "hbm", "kernel": lm_kernel, "achieved": ach, "peak": peak, "unit": "GB/s",
@@ -495,6 +510,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--k", type=int, default=0, help="draft depth for the verify sweep (1..5)")
     ap.add_argument("--greedy", action="store_true", help="greedy verification for the verify sweep")
+    ap.add_argument("--stop-p", type=float, default=None,
+                    help="dynamic draft length: stop a sequence's chain at its first depth of draft confidence "
+                         "below this (spec_step_dynamic)")
     ap.add_argument("--modules", type=int, default=1,
                     help="distinct draft modules (depth j runs module min(j, modules-1)); 1 = one reused module")
     args = ap.parse_args()

@@ -256,6 +256,52 @@ int spec_step_modules(const MtpDims *dims, const MtpModule *modules, int n_modul
                       int32_t *out_tok, int32_t *accept_len, int32_t *num_accepted,
                       void *ws, size_t ws_bytes, mtp_stream_t stream);
 
+/*
+ * Dynamic draft length.  [P2] "Faster Rollouts with MTP Speculative
+ * Decoding", section "What's Next", names it without a rule; the rule here:
+ * the draft confidence of depth j is the largest probability of the
+ * distribution its token is taken from (softmax(logits / T) when stochastic,
+ * softmax(logits) when greedy).  Sequence b keeps the drafts before its first
+ * depth j whose confidence is below stop_p: k_eff[b] = j, or k if none is
+ * (stop_p = 0 never stops; stop_p > 1 stops at depth 0, a plain decoding
+ * step).  The stop depends only on the draft, so the stochastic output keeps
+ * the target's distribution exactly.
+ *
+ * mtp_draft_dynamic: mtp_draft plus k_eff [B] int32 (device, output).  Drafts
+ *   and logits at depths >= k_eff[b] are unspecified.  Once every sequence of
+ *   the batch has stopped, the later depths' weight-streaming kernels (batches
+ *   of up to 4) return after their first copies land, so a stopped chain does
+ *   not stream the remaining depths' weights.
+ * spec_verify_dynamic: spec_verify where sequence b is verified over its
+ *   drafts 0 .. k_eff[b]-1 only, the bonus row being target row k_eff[b];
+ *   k_eff [B] int32 (device, input; clamped to 0..k; NULL: k for all).
+ *   accept_len[b] is then in 1 .. k_eff[b]+1.
+ * spec_step_dynamic: the two in one call, k_eff written by the draft and read
+ *   by the verification.
+ * stop_p must be finite and >= 0 (else MTP_ERR_INVALID_ARG).
+ */
+int mtp_draft_dynamic(const MtpDims *dims, const MtpWeights *w, const void *h,
+                      const int32_t *last_tok, void *k_cache, void *v_cache,
+                      const int32_t *ctx_len, int k, float T, int mode, float stop_p,
+                      const float *u_draft, int32_t *draft_tok, float *draft_logits,
+                      int32_t *k_eff, void *ws, size_t ws_bytes, mtp_stream_t stream);
+
+int spec_verify_dynamic(int B, int k, int V, float T, int mode,
+                        const float *target_logits, const float *draft_logits,
+                        const int32_t *draft_tok, const int32_t *k_eff,
+                        const float *u_accept, const float *u_final,
+                        int32_t *out_tok, int32_t *accept_len, int32_t *num_accepted,
+                        void *ws, size_t ws_bytes, mtp_stream_t stream);
+
+int spec_step_dynamic(const MtpDims *dims, const MtpWeights *w, const void *h,
+                      const int32_t *last_tok, void *k_cache, void *v_cache,
+                      const int32_t *ctx_len, int k, float T, int mode, float stop_p,
+                      const float *u_draft, const float *target_logits,
+                      const float *u_accept, const float *u_final,
+                      int32_t *draft_tok, float *draft_logits, int32_t *k_eff,
+                      int32_t *out_tok, int32_t *accept_len, int32_t *num_accepted,
+                      void *ws, size_t ws_bytes, mtp_stream_t stream);
+
 /* Wait for the stream, then copy the workspace's status word (MTP_STATUS_* bits)
  * to *status.  Returns MTP_OK or MTP_ERR_*. */
 int mtp_get_status(const void *ws, mtp_stream_t stream, int32_t *status);

@@ -79,6 +79,14 @@ def _lib():
         L.spec_step_modules.argtypes = [ctypes.POINTER(MtpDims), ctypes.POINTER(MtpModule), I, P, P, P, I, F, I,
                                         P, P, P, P, P, P, P, P, P, P, Z, P]
         L.spec_step_modules.restype = I
+        L.mtp_draft_dynamic.argtypes = [ctypes.POINTER(MtpDims), ctypes.POINTER(MtpWeights), P, P, P, P, P, I, F,
+                                        I, F, P, P, P, P, P, Z, P]
+        L.mtp_draft_dynamic.restype = I
+        L.spec_verify_dynamic.argtypes = [I, I, I, F, I, P, P, P, P, P, P, P, P, P, P, Z, P]
+        L.spec_verify_dynamic.restype = I
+        L.spec_step_dynamic.argtypes = [ctypes.POINTER(MtpDims), ctypes.POINTER(MtpWeights), P, P, P, P, P, I, F,
+                                        I, F, P, P, P, P, P, P, P, P, P, P, P, Z, P]
+        L.spec_step_dynamic.restype = I
         L.mtp_get_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
         L.mtp_get_status.restype = I
         L.mtp_clear_status.argtypes = [P, P]
@@ -253,6 +261,60 @@ def spec_step_modules(dims, modules, h, last_tok, ctx_len, k, T, mode, u_draft, 
         _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
     if rc != 0:
         raise MtpError(rc, "spec_step_modules")
+
+
+def mtp_draft_dynamic(dims, weights, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode, stop_p, u_draft,
+                      draft_tok, draft_logits, k_eff, ws, stream=None):
+    """mtp_draft with the dynamic draft length: k_eff [B] int32 receives the
+    drafts each sequence keeps (its first depth of confidence below stop_p)."""
+    B, V = dims.B, dims.V
+    rc = _lib().mtp_draft_dynamic(
+        ctypes.byref(dims), ctypes.byref(weights), _ptr(h, "h", torch.bfloat16, B * dims.d),
+        _ptr(last_tok, "last_tok", torch.int32, B), _ptr(k_cache, "k_cache", torch.bfloat16),
+        _ptr(v_cache, "v_cache", torch.bfloat16), _ptr(ctx_len, "ctx_len", torch.int32, B), int(k),
+        float(T), int(mode), float(stop_p), _ptr(u_draft, "u_draft", torch.float32, B * k),
+        _ptr(draft_tok, "draft_tok", torch.int32, B * k),
+        _ptr(draft_logits, "draft_logits", torch.float32, B * k * V), _ptr(k_eff, "k_eff", torch.int32, B),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
+    if rc != 0:
+        raise MtpError(rc, "mtp_draft_dynamic")
+
+
+def spec_verify_dynamic(B, k, V, T, mode, target_logits, draft_logits, draft_tok, k_eff, u_accept, u_final,
+                        out_tok, accept_len, num_accepted, ws, stream=None):
+    """spec_verify over each sequence's kept drafts (k_eff [B] int32, or None for k)."""
+    rc = _lib().spec_verify_dynamic(
+        int(B), int(k), int(V), float(T), int(mode),
+        _ptr(target_logits, "target_logits", torch.float32, B * (k + 1) * V),
+        _ptr(draft_logits, "draft_logits", torch.float32, B * k * V),
+        _ptr(draft_tok, "draft_tok", torch.int32, B * k), _ptr(k_eff, "k_eff", torch.int32, B),
+        _ptr(u_accept, "u_accept", torch.float32, B * k), _ptr(u_final, "u_final", torch.float32, B),
+        _ptr(out_tok, "out_tok", torch.int32, B * (k + 1)), _ptr(accept_len, "accept_len", torch.int32, B),
+        _ptr(num_accepted, "num_accepted", torch.int32, B),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
+    if rc != 0:
+        raise MtpError(rc, "spec_verify_dynamic")
+
+
+def spec_step_dynamic(dims, weights, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode, stop_p, u_draft,
+                      target_logits, u_accept, u_final, draft_tok, draft_logits, k_eff, out_tok, accept_len,
+                      num_accepted, ws, stream=None):
+    """spec_step with the dynamic draft length (see mtp_draft_dynamic)."""
+    B, V = dims.B, dims.V
+    rc = _lib().spec_step_dynamic(
+        ctypes.byref(dims), ctypes.byref(weights), _ptr(h, "h", torch.bfloat16, B * dims.d),
+        _ptr(last_tok, "last_tok", torch.int32, B), _ptr(k_cache, "k_cache", torch.bfloat16),
+        _ptr(v_cache, "v_cache", torch.bfloat16), _ptr(ctx_len, "ctx_len", torch.int32, B), int(k),
+        float(T), int(mode), float(stop_p), _ptr(u_draft, "u_draft", torch.float32, B * k),
+        _ptr(target_logits, "target_logits", torch.float32, B * (k + 1) * V),
+        _ptr(u_accept, "u_accept", torch.float32, B * k), _ptr(u_final, "u_final", torch.float32, B),
+        _ptr(draft_tok, "draft_tok", torch.int32, B * k),
+        _ptr(draft_logits, "draft_logits", torch.float32, B * k * V), _ptr(k_eff, "k_eff", torch.int32, B),
+        _ptr(out_tok, "out_tok", torch.int32, B * (k + 1)), _ptr(accept_len, "accept_len", torch.int32, B),
+        _ptr(num_accepted, "num_accepted", torch.int32, B),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
+    if rc != 0:
+        raise MtpError(rc, "spec_step_dynamic")
 
 
 def get_status(ws, stream=None):

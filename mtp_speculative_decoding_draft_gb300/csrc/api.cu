@@ -162,9 +162,11 @@ void use_module(DraftCtx &c, const MtpModule &m) {
 
 int prepare_draft(const MtpDims *dims, const MtpModule *mods, int nmod, const void *h, const int32_t *last_tok,
                   const int32_t *ctx_len, int k, float T, int mode, const float *u_draft, int32_t *draft_tok,
-                  float *draft_logits, void *ws, size_t ws_bytes, bool logits_in_ws, Draft *out) {
+                  float *draft_logits, void *ws, size_t ws_bytes, bool logits_in_ws, float stop_p, int32_t *k_eff,
+                  Draft *out) {
   int rc = check_dims(dims, k);
   if (rc) return rc;
+  if (k_eff && (!aligned16(k_eff) || !(stop_p >= 0.f && stop_p < 1e30f))) return MTP_ERR_INVALID_ARG;
   if (!mods || nmod < 1 || nmod > k) return MTP_ERR_INVALID_ARG;
   if (mode != MTP_GREEDY && mode != MTP_STOCHASTIC) return MTP_ERR_INVALID_ARG;
   if (mode == MTP_STOCHASTIC && !(T > 0.f && T < 1e30f)) return MTP_ERR_INVALID_ARG;
@@ -197,10 +199,13 @@ int prepare_draft(const MtpDims *dims, const MtpModule *mods, int nmod, const vo
   out->nmod = nmod;
   c.h = static_cast<const uint16_t *>(h); c.last_tok = last_tok; c.ctx_len = ctx_len; c.u_draft = u_draft;
   c.draft_tok = draft_tok;
+  c.k_eff = k_eff;
+  c.stop_p = stop_p;
   char *base = static_cast<char *>(ws);
   c.logits = draft_logits ? draft_logits : (logits_in_ws ? reinterpret_cast<float *>(base + L.logits) : nullptr);
   c.status = reinterpret_cast<int *>(base + L.status);
   c.lm_cnt = reinterpret_cast<unsigned *>(base + L.lm_cnt);
+  c.n_active = k_eff ? c.lm_cnt + 1 : nullptr;  // same 256-byte slot as the ticket counter
   c.x0 = reinterpret_cast<float *>(base + L.x0);
   c.x1 = reinterpret_cast<float *>(base + L.x1);
   c.x2 = reinterpret_cast<float *>(base + L.x2);
@@ -269,7 +274,8 @@ cudaError_t run_draft(Draft &D, cudaStream_t s) {
 int prepare_verify(int B, int k, int V, float T, int mode, const float *target, const float *draft,
                    const int32_t *draft_tok, const float *u_accept, const float *u_final, int32_t *out_tok,
                    int32_t *accept_len, int32_t *num_accepted, void *state, size_t state_bytes, bool draft_check,
-                   VerifyArgs *a) {
+                   const int32_t *k_eff, VerifyArgs *a) {
+  if (k_eff && !aligned16(k_eff)) return MTP_ERR_INVALID_ARG;
   if (B < 1 || k < 1 || k > 8 || V < 1 || V > (1 << 30) || B > (1 << 20)) return MTP_ERR_INVALID_ARG;
   if (mode != MTP_GREEDY && mode != MTP_STOCHASTIC) return MTP_ERR_INVALID_ARG;
   if (mode == MTP_STOCHASTIC && !(T > 0.f && T < 1e30f)) return MTP_ERR_INVALID_ARG;
@@ -288,6 +294,7 @@ int prepare_verify(int B, int k, int V, float T, int mode, const float *target, 
   a->B = B; a->k = k; a->V = V; a->mode = mode; a->T = mode == MTP_STOCHASTIC ? T : 1.f;
   a->target = target; a->draft = draft; a->draft_tok = draft_tok; a->u_accept = u_accept; a->u_final = u_final;
   a->out_tok = out_tok; a->accept_len = accept_len; a->num_accepted = num_accepted;
+  a->k_eff = k_eff;
   if (!plan_verify(B, k, V, &a->p)) return MTP_ERR_UNSUPPORTED_SHAPE;
   verify_bind_state(*a, state);
   return MTP_OK;
@@ -343,7 +350,7 @@ int mtp_draft_modules(const MtpDims *dims, const MtpModule *modules, int n_modul
                       mtp_stream_t stream) {
   Draft D;
   int rc = prepare_draft(dims, modules, n_modules, h, last_tok, ctx_len, k, T, mode, u_draft, draft_tok,
-                         draft_logits, ws, ws_bytes, false, &D);
+                         draft_logits, ws, ws_bytes, false, 0.f, nullptr, &D);
   if (rc) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = run_draft(D, s);
@@ -360,6 +367,22 @@ int mtp_draft(const MtpDims *dims, const MtpWeights *w, const void *h, const int
                            ws_bytes, stream);
 }
 
+int mtp_draft_dynamic(const MtpDims *dims, const MtpWeights *w, const void *h, const int32_t *last_tok,
+                      void *k_cache, void *v_cache, const int32_t *ctx_len, int k, float T, int mode, float stop_p,
+                      const float *u_draft, int32_t *draft_tok, float *draft_logits, int32_t *k_eff, void *ws,
+                      size_t ws_bytes, mtp_stream_t stream) {
+  if (!w || !k_eff) return MTP_ERR_INVALID_ARG;
+  const MtpModule one{*w, k_cache, v_cache};
+  Draft D;
+  int rc = prepare_draft(dims, &one, 1, h, last_tok, ctx_len, k, T, mode, u_draft, draft_tok, draft_logits, ws,
+                         ws_bytes, false, stop_p, k_eff, &D);
+  if (rc) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = run_draft(D, s);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return cuda_rc(e);
+}
+
 int mtp_draft_noalloc(const MtpDims *dims, const MtpWeights *w, const void *h, const int32_t *last_tok,
                       void *k_cache, void *v_cache, const int32_t *ctx_len, int k, float T, int mode,
                       const float *u_draft, int32_t *draft_tok, float *draft_logits, int32_t *status,
@@ -374,7 +397,7 @@ int mtp_draft_noalloc(const MtpDims *dims, const MtpWeights *w, const void *h, c
   const MtpModule one{*w, k_cache, v_cache};
   Draft D;
   rc = prepare_draft(dims, &one, 1, h, last_tok, ctx_len, k, T, mode, u_draft, draft_tok, draft_logits, scratch,
-                     MTP_STATIC_SCRATCH_BYTES, false, &D);
+                     MTP_STATIC_SCRATCH_BYTES, false, 0.f, nullptr, &D);
   if (rc) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the status word and the LM-head ticket counter (the first two aligned
@@ -392,18 +415,51 @@ size_t spec_verify_workspace_size(int B, int k, int V) {
   return kAlign + up(verify_state_bytes(B, k, V));
 }
 
-int spec_verify(int B, int k, int V, float T, int mode, const float *target_logits, const float *draft_logits,
-                const int32_t *draft_tok, const float *u_accept, const float *u_final, int32_t *out_tok,
-                int32_t *accept_len, int32_t *num_accepted, void *ws, size_t ws_bytes, mtp_stream_t stream) {
+int spec_verify_dynamic(int B, int k, int V, float T, int mode, const float *target_logits,
+                        const float *draft_logits, const int32_t *draft_tok, const int32_t *k_eff,
+                        const float *u_accept, const float *u_final, int32_t *out_tok, int32_t *accept_len,
+                        int32_t *num_accepted, void *ws, size_t ws_bytes, mtp_stream_t stream) {
   VerifyArgs a{};
   if (!aligned16(ws) || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MTP_ERR_INVALID_ARG;
   if (ws_bytes < kAlign) return MTP_ERR_WORKSPACE;
   int rc = prepare_verify(B, k, V, T, mode, target_logits, draft_logits, draft_tok, u_accept, u_final, out_tok,
-                          accept_len, num_accepted, static_cast<char *>(ws) + kAlign, ws_bytes - kAlign, true, &a);
+                          accept_len, num_accepted, static_cast<char *>(ws) + kAlign, ws_bytes - kAlign, true, k_eff,
+                          &a);
   if (rc) return rc;
   a.status = static_cast<int *>(ws);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = timed(MTP_KC_VERIFY, s, [&] { return launch_verify(a, s, false); });
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return cuda_rc(e);
+}
+
+int spec_verify(int B, int k, int V, float T, int mode, const float *target_logits, const float *draft_logits,
+                const int32_t *draft_tok, const float *u_accept, const float *u_final, int32_t *out_tok,
+                int32_t *accept_len, int32_t *num_accepted, void *ws, size_t ws_bytes, mtp_stream_t stream) {
+  return spec_verify_dynamic(B, k, V, T, mode, target_logits, draft_logits, draft_tok, nullptr, u_accept, u_final,
+                             out_tok, accept_len, num_accepted, ws, ws_bytes, stream);
+}
+
+// spec_step over modules, with the dynamic draft length when k_eff is given.
+static int step_call(const MtpDims *dims, const MtpModule *modules, int n_modules, const void *h,
+                     const int32_t *last_tok, const int32_t *ctx_len, int k, float T, int mode, float stop_p,
+                     const float *u_draft, const float *target_logits, const float *u_accept, const float *u_final,
+                     int32_t *draft_tok, float *draft_logits, int32_t *k_eff, int32_t *out_tok,
+                     int32_t *accept_len, int32_t *num_accepted, void *ws, size_t ws_bytes, mtp_stream_t stream) {
+  Draft D;
+  int rc = prepare_draft(dims, modules, n_modules, h, last_tok, ctx_len, k, T, mode, u_draft, draft_tok,
+                         draft_logits, ws, ws_bytes, mode == MTP_STOCHASTIC, stop_p, k_eff, &D);
+  if (rc) return rc;
+  VerifyArgs a{};
+  const WsLayout L = draft_layout(*dims, k);
+  rc = prepare_verify(dims->B, k, dims->V, T, mode, target_logits, D.c.logits, draft_tok, u_accept, u_final, out_tok,
+                      accept_len, num_accepted, static_cast<char *>(ws) + L.vstate, L.total - L.vstate, false, k_eff,
+                      &a);
+  if (rc) return rc;
+  a.status = D.c.status;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = run_draft(D, s);
+  if (e == cudaSuccess) e = timed(MTP_KC_VERIFY, s, [&] { return launch_verify(a, s, use_pdl()); });
   if (e == cudaSuccess) e = cudaGetLastError();
   return cuda_rc(e);
 }
@@ -413,21 +469,21 @@ int spec_step_modules(const MtpDims *dims, const MtpModule *modules, int n_modul
                       const float *u_draft, const float *target_logits, const float *u_accept,
                       const float *u_final, int32_t *draft_tok, float *draft_logits, int32_t *out_tok,
                       int32_t *accept_len, int32_t *num_accepted, void *ws, size_t ws_bytes, mtp_stream_t stream) {
-  Draft D;
-  int rc = prepare_draft(dims, modules, n_modules, h, last_tok, ctx_len, k, T, mode, u_draft, draft_tok,
-                         draft_logits, ws, ws_bytes, mode == MTP_STOCHASTIC, &D);
-  if (rc) return rc;
-  VerifyArgs a{};
-  const WsLayout L = draft_layout(*dims, k);
-  rc = prepare_verify(dims->B, k, dims->V, T, mode, target_logits, D.c.logits, draft_tok, u_accept, u_final, out_tok,
-                      accept_len, num_accepted, static_cast<char *>(ws) + L.vstate, L.total - L.vstate, false, &a);
-  if (rc) return rc;
-  a.status = D.c.status;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = run_draft(D, s);
-  if (e == cudaSuccess) e = timed(MTP_KC_VERIFY, s, [&] { return launch_verify(a, s, use_pdl()); });
-  if (e == cudaSuccess) e = cudaGetLastError();
-  return cuda_rc(e);
+  return step_call(dims, modules, n_modules, h, last_tok, ctx_len, k, T, mode, 0.f, u_draft, target_logits,
+                   u_accept, u_final, draft_tok, draft_logits, nullptr, out_tok, accept_len, num_accepted, ws,
+                   ws_bytes, stream);
+}
+
+int spec_step_dynamic(const MtpDims *dims, const MtpWeights *w, const void *h, const int32_t *last_tok,
+                      void *k_cache, void *v_cache, const int32_t *ctx_len, int k, float T, int mode, float stop_p,
+                      const float *u_draft, const float *target_logits, const float *u_accept,
+                      const float *u_final, int32_t *draft_tok, float *draft_logits, int32_t *k_eff,
+                      int32_t *out_tok, int32_t *accept_len, int32_t *num_accepted, void *ws, size_t ws_bytes,
+                      mtp_stream_t stream) {
+  if (!w || !k_eff) return MTP_ERR_INVALID_ARG;
+  const MtpModule one{*w, k_cache, v_cache};
+  return step_call(dims, &one, 1, h, last_tok, ctx_len, k, T, mode, stop_p, u_draft, target_logits, u_accept,
+                   u_final, draft_tok, draft_logits, k_eff, out_tok, accept_len, num_accepted, ws, ws_bytes, stream);
 }
 
 int spec_step(const MtpDims *dims, const MtpWeights *w, const void *h, const int32_t *last_tok, void *k_cache,

@@ -80,7 +80,23 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(DraftCtx c, GemvPlan
   grid_dep_wait();
   grid_dep_launch();
 
-  if (OP == OP_FC && c.zero_counters && blockIdx.x == 0 && threadIdx.x == 0) *c.lm_cnt = 0u;
+  // Dynamic draft length: once every sequence has stopped drafting, the later
+  // depths have nothing to do -- let the weight copies already issued land and
+  // leave (the flag is written only by earlier launches, so every CTA reads the
+  // same value).
+  if (c.n_active && c.j > 0 && *reinterpret_cast<volatile unsigned *>(c.n_active) == 0u) {
+    if (lane == 0)
+      for (int n = 0; n < min(S, total_units); ++n)
+        if (!mbar_sleep_wait(&bars[n], 0u, c.status)) break;
+    return;
+  }
+  if (OP == OP_FC && c.zero_counters && blockIdx.x == 0) {
+    if (threadIdx.x == 0) *c.lm_cnt = 0u;
+    if (c.k_eff) {
+      for (int b = threadIdx.x; b < c.B; b += kGemvThreads) c.k_eff[b] = c.k;
+      if (threadIdx.x == 0) *c.n_active = (unsigned)c.B;
+    }
+  }
   compute_scales<OP>(c, scales, red);
 
   int n = 0;
@@ -195,7 +211,7 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(DraftCtx c, GemvPlan
         int mi = 0x7fffffff;
         for (int w = 0; w < kGemvWarps; ++w) argmax_merge(m, mi, red[w], __float_as_int(red[kGemvWarps + w]));
         float s = 0.f;
-        if (c.mode == 1 && m != -INFINITY)
+        if ((c.mode == 1 || c.k_eff) && m != -INFINITY)
           for (int rl = threadIdx.x; rl < nrows; rl += kGemvThreads) s += exp2f((ys[(size_t)rl * BG + bb] - m) * cT);
         s = block_sum_256(s, red + 2 * kGemvWarps);
         if (threadIdx.x == 0) {

@@ -153,6 +153,16 @@ __device__ __forceinline__ const uint16_t *weight_row(const DraftCtx &c, int row
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + __expf(-z)); }
 
 
+// Dynamic draft length: a sequence still drafting stops at this depth when the
+// draft's largest probability (1 / the partition sum relative to the largest
+// term) is below stop_p; it keeps the c.j drafts before this one.
+__device__ __forceinline__ void stop_check(const DraftCtx &c, int b, double conf) {
+  if (conf < (double)c.stop_p && c.k_eff[b] == c.k) {
+    c.k_eff[b] = c.j;
+    atomicSub(c.n_active, 1u);
+  }
+}
+
 // Draft-token selection over the vocabulary, run by one warp after every
 // LM-head CTA has written its per-sequence partials lm_part[b][cta] =
 // (max, sum of exp2((logit - max) * log2e / T), argmax).  CTA cta owns the
@@ -170,20 +180,31 @@ __device__ inline void lm_select_warp(const DraftCtx &c, int G, int rpc) {
     for (int cta = lane; cta < G; cta += 32) argmax_merge(M, Mi, __ldcg(&pb[cta * 4]), __float_as_int(__ldcg(&pb[cta * 4 + 2])));
     warp_argmax(M, Mi);
     int tok = Mi;
-    if (M == -INFINITY || !(M == M)) {
-      if (lane == 0) set_status(c.status, kStatusNonFinite);
-      tok = 0;
-    } else if (c.mode == 1) {
-      // Inverse CDF of softmax(logits / T) at u: walk the per-CTA masses in
-      // vocabulary order, then rescan the CTA that holds the crossing.
-      const double u = (double)__ldg(&c.u_draft[b * c.k + c.j]);
-      double Z = 0.0;
+    const bool finite = !(M == -INFINITY || !(M == M));
+    // the partition sum of softmax(logits / T) relative to its largest term
+    double Z = 0.0;
+    if (finite && c.mode == 1) {  // in vocabulary order, as the walk below adds them up
       if (lane == 0)
         for (int cta = 0; cta < G; ++cta) {
           const float mc = __ldcg(&pb[cta * 4]);
           if (mc != -INFINITY) Z += (double)__ldcg(&pb[cta * 4 + 1]) * (double)exp2f((mc - M) * cT);
         }
       Z = __shfl_sync(0xffffffffu, Z, 0);
+    } else if (finite && c.k_eff) {  // greedy: only the total, over the lanes
+      for (int cta = lane; cta < G; cta += 32) {
+        const float mc = __ldcg(&pb[cta * 4]);
+        if (mc != -INFINITY) Z += (double)__ldcg(&pb[cta * 4 + 1]) * (double)exp2f((mc - M) * cT);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
+    }
+    if (!finite) {
+      if (lane == 0) set_status(c.status, kStatusNonFinite);
+      tok = 0;
+    } else if (c.mode == 1) {
+      // Inverse CDF of softmax(logits / T) at u: walk the per-CTA masses in
+      // vocabulary order, then rescan the CTA that holds the crossing.
+      const double u = (double)__ldg(&c.u_draft[b * c.k + c.j]);
       const double target = u * Z;
       int cstar = -1, clast = -1;
       double before = 0.0;
@@ -246,6 +267,7 @@ __device__ inline void lm_select_warp(const DraftCtx &c, int G, int rpc) {
       tok = found != 0x7fffffff ? found : (lp >= 0 ? lp : Mi);
     }
     if (lane == 0) c.draft_tok[b * c.k + c.j] = tok;
+    if (lane == 0 && c.k_eff && finite) stop_check(c, b, 1.0 / Z);
   }
   if (lane == 0) *c.lm_cnt = 0u;
 }

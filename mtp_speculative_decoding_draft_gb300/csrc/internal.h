@@ -28,6 +28,11 @@ struct DraftCtx {
   // outputs
   int *draft_tok;         // [B, k]
   float *logits;          // [B, k, V] or null (greedy without logits)
+  // dynamic draft length (null k_eff: off): sequence b keeps the drafts before
+  // its first depth whose draft confidence is below stop_p
+  int *k_eff;             // [B] drafts kept (k until the sequence stops)
+  unsigned *n_active;     // sequences still drafting (workspace)
+  float stop_p;
   // workspace
   int *status;
   unsigned *lm_cnt;       // 1 ticket counter
@@ -110,6 +115,7 @@ struct VerifyArgs {
   const float *target;   // [B, k+1, V]
   const float *draft;    // [B, k, V]
   const int *draft_tok;  // [B, k]
+  const int *k_eff;      // [B] drafts kept per sequence, or null (all k)
   const float *u_accept; // [B, k]
   const float *u_final;  // [B]
   int *out_tok;          // [B, k+1]

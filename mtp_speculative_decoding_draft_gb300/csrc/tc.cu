@@ -319,6 +319,10 @@ __global__ void __launch_bounds__(kPrepThreads) tc_prep_fc_kernel(DraftCtx c, Tc
   const int b = blockIdx.x, d = c.d;
   grid_dep_wait();
   grid_dep_launch();
+  if (c.k_eff && c.j == 0 && threadIdx.x == 0) {  // dynamic draft length: every sequence drafting
+    c.k_eff[b] = c.k;
+    if (b == 0) *c.n_active = (unsigned)c.B;
+  }
   const int tok = depth_token(c, b);
   const uint16_t *e = c.E + (size_t)tok * d;
   float s0 = 0.f, s1 = 0.f;
@@ -500,7 +504,7 @@ __global__ void __launch_bounds__(kSelThreads) tc_select_part_kernel(DraftCtx c,
     }
   warp_argmax(M, I);
   float sum = 0.f;
-  if (c.mode == 1 && M != -INFINITY) {
+  if ((c.mode == 1 || c.k_eff) && M != -INFINITY) {
     const float cT = kLog2e / c.T, mc = M * cT;
 #pragma unroll
     for (int i = 0; i < 32; ++i) sum += exp2f(fmaf(x[i], cT, -mc));
@@ -522,26 +526,31 @@ __global__ void __launch_bounds__(32) tc_select_fin_kernel(DraftCtx c, const flo
   for (int q = q0; q < q1; ++q) argmax_merge(M, I, pp[q].x, __float_as_int(pp[q].y));
   warp_argmax(M, I);
   int tok = I;
-  if (M == -INFINITY || !(M == M)) {
-    if (lane == 0) set_status(c.status, kStatusNonFinite);
-    tok = 0;
-  } else if (c.mode == 1) {
-    const float cT = kLog2e / c.T;
-    double own = 0.0;
-    int lastq = -1;
+  const bool finite = !(M == -INFINITY || !(M == M));
+  const float cT = kLog2e / c.T;
+  // float64 masses of this lane's sub-segments, their inclusive scan and the
+  // partition sum relative to the largest term
+  double own = 0.0, incl = 0.0, Z = 0.0;
+  int lastq = -1;
+  if (finite && (c.mode == 1 || c.k_eff)) {
     for (int q = q0; q < q1; ++q) {
       const float4 v = pp[q];
       const double m = v.x == -INFINITY ? 0.0 : (double)v.z * (double)exp2f((v.x - M) * cT);
       own += m;
       if (m > 0.0) lastq = q;
     }
-    double incl = own;
+    incl = own;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const double t = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += t;
     }
-    const double Z = __shfl_sync(0xffffffffu, incl, 31);
+    Z = __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (!finite) {
+    if (lane == 0) set_status(c.status, kStatusNonFinite);
+    tok = 0;
+  } else if (c.mode == 1) {
     const double target = (double)__ldg(&c.u_draft[b * c.k + c.j]) * Z;
     int qs = -1;
     double before = 0.0;
@@ -609,6 +618,7 @@ __global__ void __launch_bounds__(32) tc_select_fin_kernel(DraftCtx c, const flo
     tok = found != 0x7fffffff ? found : (lastpos >= 0 ? lastpos : I);
   }
   if (lane == 0) c.draft_tok[b * c.k + c.j] = tok;
+  if (lane == 0 && c.k_eff && finite) stop_check(c, b, 1.0 / Z);
 }
 
 // ---------------------------------------------------------------- host side

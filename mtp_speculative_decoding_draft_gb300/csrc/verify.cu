@@ -84,7 +84,7 @@ enum : int { kPieceStop = 0, kPieceRow = 1, kPieceRowDraft = 2, kPieceWeights = 
 constexpr int kRecAccept = 1, kRecBadToken = 2, kRecNonFinite = 4, kRecWritten = 8;
 
 struct ItemInfo {
-  int kind, b, j, pad;
+  int kind, b, j, kb;  // kb: drafts sequence b keeps (k unless the draft length is dynamic)
 };
 
 // A CTA's partial of one item, sent to every CTA of the cluster (32 bytes).
@@ -375,14 +375,20 @@ __device__ __forceinline__ const float *draft_row(const VerifyArgs &a, int b, in
 }
 
 // Item idx in position-major order: position j = idx / B of sequence idx % B;
-// in stochastic mode positions 0..k-1 are pairs and position k the bonus row.
+// in stochastic mode positions 0..kb-1 are pairs and position kb the bonus
+// row.  With a dynamic draft length (kb < k) the positions past kb carry no
+// draft: their items take the plain one-row form (read, recorded, ignored by
+// the gather), so every item still runs the same barrier protocol.
 __device__ __forceinline__ ItemInfo decode(const VerifyArgs &a, unsigned idx) {
   ItemInfo it{kItemStop, 0, 0, 0};
   if (idx >= a.p.total) return it;
   const unsigned B = (unsigned)a.B;
   it.j = (int)(idx / B);
   it.b = (int)(idx % B);
-  it.kind = a.mode == 0 ? kItemGreedy : (it.j < a.k ? kItemPair : kItemBonus);
+  it.kb = a.k;
+  if (a.k_eff) it.kb = min(max(__ldcg(&a.k_eff[it.b]), 0), a.k);
+  if (a.mode == 0 || it.j > it.kb) it.kind = kItemGreedy;
+  else it.kind = it.j < it.kb ? kItemPair : kItemBonus;
   return it;
 }
 
@@ -616,6 +622,7 @@ __device__ void claimer(const VerifyArgs &a, Shared &sh, int C) {
   const int lane = threadIdx.x & 31;
   int stops = 0;
   bool ok = true;
+  if (a.k_eff) grid_dep_wait();  // the drafts kept come from the drafter
   for (uint32_t n = 0; stops < kDeciders && ok; ++n) {
     const int s = (int)(n % kQD);
     if (stops == 0) {
@@ -650,7 +657,7 @@ __device__ void claimer(const VerifyArgs &a, Shared &sh, int C) {
     if (it.kind == kItemStop) ++stops;
     if (lane < C) {
       int4 *dst = dsmem_ptr_mut(reinterpret_cast<int4 *>(&sh.slot[s].info), (uint32_t)lane);
-      *dst = make_int4(it.kind, it.b, it.j, 0);
+      *dst = make_int4(it.kind, it.b, it.j, it.kb);
       mbar_arrive_remote(&sh.item_full[s], (uint32_t)lane);
     }
   }
@@ -762,7 +769,7 @@ __device__ __forceinline__ int last_position(const VerifyArgs &a) { return a.k; 
 // holds position l's word in `pre`, loaded when the item started; missing ones
 // are polled, bounded), picks the first rejection, writes the outputs and
 // resets the sequence's state (warp-collective).
-__device__ void record(const VerifyArgs &a, int b, int j, int word, int tok, unsigned long long pre) {
+__device__ void record(const VerifyArgs &a, int b, int j, int kb, int word, int tok, unsigned long long pre) {
   const int lane = threadIdx.x & 31, k = a.k, V = a.V;
   unsigned long long *rb = a.rec + (size_t)b * (k + 1);
   const unsigned long long mine = ((unsigned long long)(unsigned)tok << 32) | (unsigned)(word | kRecWritten);
@@ -786,13 +793,13 @@ __device__ void record(const VerifyArgs &a, int b, int j, int word, int tok, uns
   }
   const int rw = (int)(unsigned)r, rt = (int)(unsigned)(r >> 32);
   int d = 0;
-  if (lane < k) d = __ldcg(&a.draft_tok[(size_t)b * k + lane]);
-  const bool bad = lane < k && (d < 0 || d >= V);
+  if (lane < kb) d = __ldcg(&a.draft_tok[(size_t)b * k + lane]);
+  const bool bad = lane < kb && (d < 0 || d >= V);
   bool acc;
-  if (a.mode == 0) acc = lane < k && !bad && rt == d;
-  else acc = lane < k && !bad && (rw & kRecAccept) != 0;
-  const unsigned rejm = __ballot_sync(kFull, lane < k && !acc);
-  const int n_acc = rejm ? __ffs(rejm) - 1 : k;
+  if (a.mode == 0) acc = lane < kb && !bad && rt == d;
+  else acc = lane < kb && !bad && (rw & kRecAccept) != 0;
+  const unsigned rejm = __ballot_sync(kFull, lane < kb && !acc);
+  const int n_acc = rejm ? __ffs(rejm) - 1 : kb;
   const int tok_out = __shfl_sync(kFull, rt, n_acc);
   // flags of the positions the chain reached
   int flags = lane <= n_acc ? (rw & (kRecBadToken | kRecNonFinite)) : 0;
@@ -884,7 +891,7 @@ __device__ void decider(const VerifyArgs &a, Shared &sh, int d, int rank, int C,
       int idx = xr.i0;
       warp_argmax(m, idx);
       if (lane == 0) mbar_arrive_remote(&sh.item_empty[s], 0u);
-      if (rank == 0) record(a, b, j, m > -INFINITY ? 0 : kRecNonFinite, idx == 0x7fffffff ? 0 : idx, pre);
+      if (rank == 0) record(a, b, j, it.kb, m > -INFINITY ? 0 : kRecNonFinite, idx == 0x7fffffff ? 0 : idx, pre);
       continue;
     }
     const float M0 = warp_max(xr.m0), M1 = warp_max(xr.m1);
@@ -914,7 +921,7 @@ __device__ void decider(const VerifyArgs &a, Shared &sh, int d, int rank, int C,
     }
     if (!draw) {
       if (lane == 0) mbar_arrive_remote(&sh.item_empty[s], 0u);
-      if (rank == 0) record(a, b, j, word, 0, pre);
+      if (rank == 0) record(a, b, j, it.kb, word, 0, pre);
       continue;
     }
     const float Mt = M0, Ml = M1;
@@ -993,7 +1000,7 @@ __device__ void decider(const VerifyArgs &a, Shared &sh, int d, int rank, int C,
       }
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(&sh.item_empty[s], 0u);
-      record(a, b, j, word, chosen, pre);
+      record(a, b, j, it.kb, word, chosen, pre);
     } else if (lane == 0) {
       mbar_arrive_remote(&sh.item_empty[s], 0u);
     }

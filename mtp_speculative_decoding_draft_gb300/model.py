@@ -85,6 +85,16 @@ class DraftModule:
                      self.ctx_len, self.k, T, mode, u_draft, target_logits, u_accept, u_final,
                      self.draft_tok, lg, self.out_tok, self.accept_len, self.num_accepted, self.ws, stream)
 
+    def step_dynamic(self, T, mode, stop_p, target_logits, u_draft=None, u_accept=None, u_final=None,
+                     logits=True, stream=None):
+        """spec_step with the dynamic draft length; self.k_eff receives the drafts kept."""
+        if not hasattr(self, "k_eff"):
+            self.k_eff = torch.zeros(self.w.B, dtype=torch.int32, device=self.device)
+        bd.spec_step_dynamic(self.dims, self.wptr, self.h, self.last_tok, self.k_cache, self.v_cache,
+                             self.ctx_len, self.k, T, mode, stop_p, u_draft, target_logits, u_accept, u_final,
+                             self.draft_tok, self.draft_logits if logits else None, self.k_eff, self.out_tok,
+                             self.accept_len, self.num_accepted, self.ws, stream)
+
     def status(self, stream=None):
         return bd.get_status(self.ws, stream)
 
