@@ -33,7 +33,7 @@ def block_elements(w):
     return (w.d * 2 * w.d + (w.Hq + 2 * w.Hkv) * w.Dh * w.d + w.d * w.Hq * w.Dh + 3 * w.d * w.F + 5 * w.d)
 
 
-def step_bytes(w, ctx_len, logits_out, n_modules=1, depths=None):
+def step_bytes(w, ctx_len, logits_out, n_modules=1, depths=None, head_rows=None):
     """Algorithmic HBM bytes of one spec_step: weights re-streamed at every
     depth, the visible KV rows read once per depth, target logits read once,
     draft logits written and read once when they are materialised.  With
@@ -41,15 +41,15 @@ def step_bytes(w, ctx_len, logits_out, n_modules=1, depths=None):
     context plus the rows earlier depths appended to the same cache."""
     k = w.k
     kd = k if depths is None else depths  # depths whose weights are streamed (a stopped chain skips the rest)
-    weights = kd * (block_elements(w) + w.V * w.d) * 2
+    weights = kd * (block_elements(w) + (w.V if head_rows is None else head_rows) * w.d) * 2
     kv = sum(int(L) + j - min(j, n_modules - 1) + 1 for L in ctx_len for j in range(kd)) * w.Hkv * w.Dh * 2 * 2
     target = w.B * (k + 1) * w.V * 4
     draft = 2 * w.B * k * w.V * 4 if logits_out else 0
     return weights + kv + target + draft
 
 
-def lmhead_bytes(w, logits_out):
-    return w.V * w.d * 2 + (w.B * w.V * 4 if logits_out else 0)
+def lmhead_bytes(w, logits_out, head_rows=None):
+    return (w.V if head_rows is None else head_rows) * w.d * 2 + (w.B * w.V * 4 if logits_out else 0)
 
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a
@@ -58,20 +58,21 @@ def lmhead_bytes(w, logits_out):
 # are unchanged; the summaries of the captures are kept under profiles/.
 NCU_TRAFFIC = {
     ("lm_head_gemv", "single_greedy_b1_d4096_v151936_ctx4096"): {
-        "bytes": 1244783104 + 3415296,
+        "bytes": 1244775424 + 3031808,
         "sources": {
-            "csrc/draft.cu": "7423ff25b2c3d53aa90b9ed37469d0bed9f9262144376e7cb33f369fb6a550ca",
-            "csrc/draft_ops.cuh": "5521f139698822af7da637dfe7303059c64bec5fd546cc7ae246193f2a491186",
+            "csrc/draft.cu": "13e1c2b716cefe9a649e8aae88bd225b4a0f9ac86dc8cece6ee2afc2eb123ece",
+            "csrc/draft_ops.cuh": "3067b6cc411842aa64b55c5c50ad63b20034f1eb2bdba96dc444c1983d92c325",
             "csrc/common.cuh": "fcd7bd8f56df32fc490b2c47f2fbc0f7f37047c578430d777438202c9279de66",
+            "csrc/internal.h": "d53bd2440af30e46859baefc729772cd592b6e5b2ae32e84da3001f7c8da4104",
         },
     },
     ("tc_gemm_kernel(LM head)", "batched_stochastic_b64_d4096_v151936_ctx1024-8192"): {
-        "bytes": 1248202496 + 8034560,
+        "bytes": 1248388096 + 7836416,
         "sources": {
-            "csrc/tc.cu": "3d947329414032c4b0d4b009ab2a06f7151e432ae1bab6231c28f36531157949",
+            "csrc/tc.cu": "bbf936c6286eab81ddd55dcbb75b7fa5ce319eb13fd25fb9147e60d0c7e49da8",
             "csrc/tcgen05.cuh": "e128ff6d7c8451d618848063024b7cd0a98c722dd1b86ef0d04e6a07a9070ee7",
             "csrc/common.cuh": "fcd7bd8f56df32fc490b2c47f2fbc0f7f37047c578430d777438202c9279de66",
-            "csrc/internal.h": "f3fa200359aee7e9705348b45c4914b9e60226a11e00a6c5c83253788e3a260c",
+            "csrc/internal.h": "d53bd2440af30e46859baefc729772cd592b6e5b2ae32e84da3001f7c8da4104",
         },
     },
     ("verify_kernel", "verify_sweep_b256_v151936_k3/greedy"): {
@@ -229,8 +230,10 @@ def run_reference(args):
 def config_of(w, args):
     mods = getattr(args, "modules", 1)
     sp = getattr(args, "stop_p", None)
-    name = w.name + ("_modules%d" % mods if mods > 1 else "") + ("_stop%g" % sp if sp is not None else "")
-    return {"workload": name, "modules": mods, "stop_p": sp, "B": w.B, "k": w.k, "d": w.d, "Hq": w.Hq, "Hkv": w.Hkv,
+    dv = getattr(args, "draft_vocab", 0)
+    name = (w.name + ("_modules%d" % mods if mods > 1 else "") + ("_stop%g" % sp if sp is not None else "")
+            + ("_draftvocab%d" % dv if dv else ""))
+    return {"workload": name, "modules": mods, "stop_p": sp, "draft_vocab": dv or None, "B": w.B, "k": w.k, "d": w.d, "Hq": w.Hq, "Hkv": w.Hkv,
             "Dh": w.Dh, "F": w.F,
             "V": w.V, "ctx": w.ctx if not isinstance(w.ctx, tuple) else list(w.ctx),
             "mode": "greedy" if w.mode == 0 else "stochastic", "T": w.T,
@@ -331,8 +334,10 @@ def run_ours(args):
     ctx = W.make_context(w)
     u = W.make_uniforms(w)
     nm = max(1, min(args.modules, w.k))
-    if args.stop_p is not None and nm > 1:
-        raise SystemExit("--stop-p runs one module (spec_step_dynamic); drop --modules")
+    if (args.stop_p is not None or args.draft_vocab) and nm > 1:
+        raise SystemExit("--stop-p and --draft-vocab run one module; drop --modules")
+    if args.stop_p is not None and args.draft_vocab:
+        raise SystemExit("--stop-p and --draft-vocab are separate calls; give one")
     extra = [W.make_module_weights(w, i, E=wts["E"]) for i in range(1, nm)]
     caches = [W.make_module_cache(w, i) for i in range(1, nm)]
     m = DraftModule(w, wts, extra_modules=extra)
@@ -356,8 +361,14 @@ def run_ours(args):
     uf = to_device(u["u_final"]) if stoch else None
     logits_out = stoch
 
+    if args.draft_vocab:
+        vmap, head = W.make_draft_vocab(w, args.draft_vocab)
+        m.set_draft_vocab(vmap, head)
+
     def step(stream=None):
-        if args.stop_p is not None:
+        if args.draft_vocab:
+            m.step_reduced(w.T, w.mode, target_d, ud, ua, uf, logits=logits_out, stream=stream)
+        elif args.stop_p is not None:
             m.step_dynamic(w.T, w.mode, args.stop_p, target_d, ud, ua, uf, logits=logits_out, stream=stream)
         else:
             m.step(w.T, w.mode, target_d, ud, ua, uf, logits=logits_out, stream=stream)
@@ -457,11 +468,12 @@ def run_ours(args):
         ke = m.k_eff.cpu().numpy()
         # weight-streaming launches of batches of up to 4 return once every sequence has stopped
         depths = min(w.k, int(ke.max()) + 1) if w.B <= 4 else w.k
-    sb = step_bytes(w, ctx["ctx_len"], logits_out, nm, depths)
+    hr = args.draft_vocab or None
+    sb = step_bytes(w, ctx["ctx_len"], logits_out, nm, depths, hr)
     steps_s = 1e3 / ms * world
     tokens_per_step = float(L.sum())
     lm_avg = lm_ms / max(lm_n, 1)
-    lm_b = lmhead_bytes(w, logits_out)
+    lm_b = lmhead_bytes(w, logits_out, hr)
     ach = lm_b / (lm_avg * 1e-3) / 1e9
     # Batches of five or more run the LM head as a tensor-core GEMM; smaller ones as the GEMV.
     lm_kernel = "tc_gemm_kernel(LM head)" if w.B >= 5 and w.d % 64 == 0 else "lm_head_gemv"
@@ -513,6 +525,8 @@ def main():
     ap.add_argument("--stop-p", type=float, default=None,
                     help="dynamic draft length: stop a sequence's chain at its first depth of draft confidence "
                          "below this (spec_step_dynamic)")
+    ap.add_argument("--draft-vocab", type=int, default=0,
+                    help="reduced draft vocabulary of this many ids (spec_step_reduced); 0 = the full head")
     ap.add_argument("--modules", type=int, default=1,
                     help="distinct draft modules (depth j runs module min(j, modules-1)); 1 = one reused module")
     args = ap.parse_args()

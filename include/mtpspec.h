@@ -302,6 +302,43 @@ int spec_step_dynamic(const MtpDims *dims, const MtpWeights *w, const void *h,
                       int32_t *out_tok, int32_t *accept_len, int32_t *num_accepted,
                       void *ws, size_t ws_bytes, mtp_stream_t stream);
 
+/*
+ * Reduced draft vocabulary.  [P1] "How FastMTP-style fine-tuning works in
+ * Speculators" (its note on the full-vocabulary head) and "What's next?" name
+ * FR-Spec-style frequency-ranked draft-vocabulary reduction, to shrink the cost
+ * of each recursive step, without a rule.  The
+ * rule here: the draft head is N rows of E chosen by the caller (in FR-Spec,
+ * the N most frequent tokens).
+ *   head_rows  [N, d] bf16: those rows, gathered once by the caller
+ *              (head_rows[i] = E[vocab_map[i]])
+ *   vocab_map  [N] int32: the vocabulary id of each head row; distinct ids in
+ *              [0, V) (an id outside it sets MTP_STATUS_BAD_TOKEN)
+ *   n_draft_vocab = N, 128 <= N <= V
+ * The draft distribution is q = softmax over the N head logits (zero outside
+ * the N ids); the draft token is vocab_map of the argmax / inverse-CDF draw
+ * over the N rows in row order.  The token embedding still reads E.
+ * draft_logits [B, k, V] stays in full-vocabulary layout: the N logits at
+ * their ids and -inf at every other id, so spec_verify (q = 0 there) needs
+ * nothing new and stays exact.  Everything else is as for mtp_draft /
+ * spec_step.
+ */
+int mtp_draft_reduced(const MtpDims *dims, const MtpWeights *w,
+                      const void *head_rows, const int32_t *vocab_map, int n_draft_vocab,
+                      const void *h, const int32_t *last_tok, void *k_cache, void *v_cache,
+                      const int32_t *ctx_len, int k, float T, int mode,
+                      const float *u_draft, int32_t *draft_tok, float *draft_logits,
+                      void *ws, size_t ws_bytes, mtp_stream_t stream);
+
+int spec_step_reduced(const MtpDims *dims, const MtpWeights *w,
+                      const void *head_rows, const int32_t *vocab_map, int n_draft_vocab,
+                      const void *h, const int32_t *last_tok, void *k_cache, void *v_cache,
+                      const int32_t *ctx_len, int k, float T, int mode,
+                      const float *u_draft, const float *target_logits,
+                      const float *u_accept, const float *u_final,
+                      int32_t *draft_tok, float *draft_logits,
+                      int32_t *out_tok, int32_t *accept_len, int32_t *num_accepted,
+                      void *ws, size_t ws_bytes, mtp_stream_t stream);
+
 /* Wait for the stream, then copy the workspace's status word (MTP_STATUS_* bits)
  * to *status.  Returns MTP_OK or MTP_ERR_*. */
 int mtp_get_status(const void *ws, mtp_stream_t stream, int32_t *status);

@@ -87,6 +87,12 @@ def _lib():
         L.spec_step_dynamic.argtypes = [ctypes.POINTER(MtpDims), ctypes.POINTER(MtpWeights), P, P, P, P, P, I, F,
                                         I, F, P, P, P, P, P, P, P, P, P, P, P, Z, P]
         L.spec_step_dynamic.restype = I
+        L.mtp_draft_reduced.argtypes = [ctypes.POINTER(MtpDims), ctypes.POINTER(MtpWeights), P, P, I, P, P, P, P,
+                                        P, I, F, I, P, P, P, P, Z, P]
+        L.mtp_draft_reduced.restype = I
+        L.spec_step_reduced.argtypes = [ctypes.POINTER(MtpDims), ctypes.POINTER(MtpWeights), P, P, I, P, P, P, P,
+                                        P, I, F, I, P, P, P, P, P, P, P, P, P, P, Z, P]
+        L.spec_step_reduced.restype = I
         L.mtp_get_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
         L.mtp_get_status.restype = I
         L.mtp_clear_status.argtypes = [P, P]
@@ -315,6 +321,46 @@ def spec_step_dynamic(dims, weights, h, last_tok, k_cache, v_cache, ctx_len, k, 
         _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
     if rc != 0:
         raise MtpError(rc, "spec_step_dynamic")
+
+
+def mtp_draft_reduced(dims, weights, head_rows, vocab_map, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode,
+                      u_draft, draft_tok, draft_logits, ws, stream=None):
+    """mtp_draft over a reduced draft vocabulary: head_rows [N, d] bf16 (rows
+    vocab_map of E), vocab_map [N] int32."""
+    B, V, N = dims.B, dims.V, int(vocab_map.numel())
+    rc = _lib().mtp_draft_reduced(
+        ctypes.byref(dims), ctypes.byref(weights), _ptr(head_rows, "head_rows", torch.bfloat16, N * dims.d),
+        _ptr(vocab_map, "vocab_map", torch.int32, N), N, _ptr(h, "h", torch.bfloat16, B * dims.d),
+        _ptr(last_tok, "last_tok", torch.int32, B), _ptr(k_cache, "k_cache", torch.bfloat16),
+        _ptr(v_cache, "v_cache", torch.bfloat16), _ptr(ctx_len, "ctx_len", torch.int32, B), int(k),
+        float(T), int(mode), _ptr(u_draft, "u_draft", torch.float32, B * k),
+        _ptr(draft_tok, "draft_tok", torch.int32, B * k),
+        _ptr(draft_logits, "draft_logits", torch.float32, B * k * V),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
+    if rc != 0:
+        raise MtpError(rc, "mtp_draft_reduced")
+
+
+def spec_step_reduced(dims, weights, head_rows, vocab_map, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode,
+                      u_draft, target_logits, u_accept, u_final, draft_tok, draft_logits, out_tok, accept_len,
+                      num_accepted, ws, stream=None):
+    """spec_step over a reduced draft vocabulary (see mtp_draft_reduced)."""
+    B, V, N = dims.B, dims.V, int(vocab_map.numel())
+    rc = _lib().spec_step_reduced(
+        ctypes.byref(dims), ctypes.byref(weights), _ptr(head_rows, "head_rows", torch.bfloat16, N * dims.d),
+        _ptr(vocab_map, "vocab_map", torch.int32, N), N, _ptr(h, "h", torch.bfloat16, B * dims.d),
+        _ptr(last_tok, "last_tok", torch.int32, B), _ptr(k_cache, "k_cache", torch.bfloat16),
+        _ptr(v_cache, "v_cache", torch.bfloat16), _ptr(ctx_len, "ctx_len", torch.int32, B), int(k),
+        float(T), int(mode), _ptr(u_draft, "u_draft", torch.float32, B * k),
+        _ptr(target_logits, "target_logits", torch.float32, B * (k + 1) * V),
+        _ptr(u_accept, "u_accept", torch.float32, B * k), _ptr(u_final, "u_final", torch.float32, B),
+        _ptr(draft_tok, "draft_tok", torch.int32, B * k),
+        _ptr(draft_logits, "draft_logits", torch.float32, B * k * V),
+        _ptr(out_tok, "out_tok", torch.int32, B * (k + 1)), _ptr(accept_len, "accept_len", torch.int32, B),
+        _ptr(num_accepted, "num_accepted", torch.int32, B),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
+    if rc != 0:
+        raise MtpError(rc, "spec_step_reduced")
 
 
 def get_status(ws, stream=None):

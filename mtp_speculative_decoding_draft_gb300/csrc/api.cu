@@ -158,15 +158,28 @@ void use_module(DraftCtx &c, const MtpModule &m) {
   c.g_emb = bf(w->g_emb); c.g_hid = bf(w->g_hid); c.g_attn = bf(w->g_attn); c.g_mlp = bf(w->g_mlp);
   c.g_final = bf(w->g_final);
   c.kc = static_cast<uint16_t *>(m.k_cache); c.vc = static_cast<uint16_t *>(m.v_cache);
+  if (!c.vmap) c.head = c.E;  // a reduced head stays as set
 }
+
+// Options beyond the plain chain: the dynamic draft length (k_eff non-null)
+// and a reduced draft vocabulary (vmap non-null).
+struct DraftOpts {
+  float stop_p = 0.f;
+  int32_t *k_eff = nullptr;
+  const void *head = nullptr;     // [Vd, d] bf16
+  const int32_t *vmap = nullptr;  // [Vd]
+  int Vd = 0;
+};
 
 int prepare_draft(const MtpDims *dims, const MtpModule *mods, int nmod, const void *h, const int32_t *last_tok,
                   const int32_t *ctx_len, int k, float T, int mode, const float *u_draft, int32_t *draft_tok,
-                  float *draft_logits, void *ws, size_t ws_bytes, bool logits_in_ws, float stop_p, int32_t *k_eff,
+                  float *draft_logits, void *ws, size_t ws_bytes, bool logits_in_ws, const DraftOpts &o,
                   Draft *out) {
   int rc = check_dims(dims, k);
   if (rc) return rc;
-  if (k_eff && (!aligned16(k_eff) || !(stop_p >= 0.f && stop_p < 1e30f))) return MTP_ERR_INVALID_ARG;
+  if (o.k_eff && (!aligned16(o.k_eff) || !(o.stop_p >= 0.f && o.stop_p < 1e30f))) return MTP_ERR_INVALID_ARG;
+  if (o.vmap && (!aligned16(o.vmap) || !aligned16(o.head) || o.Vd < 128 || o.Vd > dims->V))
+    return MTP_ERR_INVALID_ARG;
   if (!mods || nmod < 1 || nmod > k) return MTP_ERR_INVALID_ARG;
   if (mode != MTP_GREEDY && mode != MTP_STOCHASTIC) return MTP_ERR_INVALID_ARG;
   if (mode == MTP_STOCHASTIC && !(T > 0.f && T < 1e30f)) return MTP_ERR_INVALID_ARG;
@@ -194,18 +207,21 @@ int prepare_draft(const MtpDims *dims, const MtpModule *mods, int nmod, const vo
   c = DraftCtx{};
   c.B = d.B; c.d = d.d; c.Hq = d.Hq; c.Hkv = d.Hkv; c.Dh = d.Dh; c.F = d.F; c.V = d.V; c.Lmax = d.Lmax;
   c.k = k; c.j = 0; c.jc = 0; c.mode = mode; c.eps = d.rms_eps; c.T = mode == MTP_STOCHASTIC ? T : 1.f;
+  c.vmap = o.vmap;
+  c.head = static_cast<const uint16_t *>(o.head);
   use_module(c, mods[0]);
   for (int m = 0; m < nmod; ++m) out->mods[m] = mods[m];
   out->nmod = nmod;
   c.h = static_cast<const uint16_t *>(h); c.last_tok = last_tok; c.ctx_len = ctx_len; c.u_draft = u_draft;
   c.draft_tok = draft_tok;
-  c.k_eff = k_eff;
-  c.stop_p = stop_p;
+  c.k_eff = o.k_eff;
+  c.stop_p = o.stop_p;
+  c.Vd = o.vmap ? o.Vd : d.V;
   char *base = static_cast<char *>(ws);
   c.logits = draft_logits ? draft_logits : (logits_in_ws ? reinterpret_cast<float *>(base + L.logits) : nullptr);
   c.status = reinterpret_cast<int *>(base + L.status);
   c.lm_cnt = reinterpret_cast<unsigned *>(base + L.lm_cnt);
-  c.n_active = k_eff ? c.lm_cnt + 1 : nullptr;  // same 256-byte slot as the ticket counter
+  c.n_active = o.k_eff ? c.lm_cnt + 1 : nullptr;  // same 256-byte slot as the ticket counter
   c.x0 = reinterpret_cast<float *>(base + L.x0);
   c.x1 = reinterpret_cast<float *>(base + L.x1);
   c.x2 = reinterpret_cast<float *>(base + L.x2);
@@ -220,7 +236,7 @@ int prepare_draft(const MtpDims *dims, const MtpModule *mods, int nmod, const vo
   out->wo = plan_gemv(OP_WO, d.d, d.Hq * d.Dh, d.B, di.sms);
   out->gateup = plan_gemv(OP_GATEUP, 2 * d.F, d.d, d.B, di.sms);
   out->down = plan_gemv(OP_DOWN, d.d, d.F, d.B, di.sms);
-  out->lm = plan_gemv(OP_LMHEAD, d.V, d.d, d.B, di.sms);
+  out->lm = plan_gemv(OP_LMHEAD, c.Vd, d.d, d.B, di.sms);
   if (out->lm.grid > kMaxLmGrid) return MTP_ERR_UNSUPPORTED_SHAPE;
   c.lm_grid = out->lm.grid;
   c.lm_rpc = out->lm.rows_per_cta;
@@ -245,6 +261,10 @@ bool use_pdl() {
 cudaError_t run_draft(Draft &D, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
   const bool pdl = use_pdl();
+  if (D.c.vmap && D.c.logits) {  // a reduced head writes only its ids: the rest of each row is -inf
+    e = launch_fill(D.c.logits, (size_t)D.c.B * D.c.k * D.c.V, -INFINITY, s, pdl);
+    if (e) return e;
+  }
   for (int j = 0; j < D.c.k && e == cudaSuccess; ++j) {
     DraftCtx c = D.c;
     // depth j runs module min(j, nmod - 1), at the next row of that module's cache
@@ -350,7 +370,7 @@ int mtp_draft_modules(const MtpDims *dims, const MtpModule *modules, int n_modul
                       mtp_stream_t stream) {
   Draft D;
   int rc = prepare_draft(dims, modules, n_modules, h, last_tok, ctx_len, k, T, mode, u_draft, draft_tok,
-                         draft_logits, ws, ws_bytes, false, 0.f, nullptr, &D);
+                         draft_logits, ws, ws_bytes, false, DraftOpts{}, &D);
   if (rc) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = run_draft(D, s);
@@ -367,6 +387,26 @@ int mtp_draft(const MtpDims *dims, const MtpWeights *w, const void *h, const int
                            ws_bytes, stream);
 }
 
+int mtp_draft_reduced(const MtpDims *dims, const MtpWeights *w, const void *head_rows, const int32_t *vocab_map,
+                      int n_draft_vocab, const void *h, const int32_t *last_tok, void *k_cache, void *v_cache,
+                      const int32_t *ctx_len, int k, float T, int mode, const float *u_draft, int32_t *draft_tok,
+                      float *draft_logits, void *ws, size_t ws_bytes, mtp_stream_t stream) {
+  if (!w || !vocab_map) return MTP_ERR_INVALID_ARG;
+  const MtpModule one{*w, k_cache, v_cache};
+  DraftOpts o;
+  o.head = head_rows;
+  o.vmap = vocab_map;
+  o.Vd = n_draft_vocab;
+  Draft D;
+  int rc = prepare_draft(dims, &one, 1, h, last_tok, ctx_len, k, T, mode, u_draft, draft_tok, draft_logits, ws,
+                         ws_bytes, false, o, &D);
+  if (rc) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = run_draft(D, s);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return cuda_rc(e);
+}
+
 int mtp_draft_dynamic(const MtpDims *dims, const MtpWeights *w, const void *h, const int32_t *last_tok,
                       void *k_cache, void *v_cache, const int32_t *ctx_len, int k, float T, int mode, float stop_p,
                       const float *u_draft, int32_t *draft_tok, float *draft_logits, int32_t *k_eff, void *ws,
@@ -374,8 +414,11 @@ int mtp_draft_dynamic(const MtpDims *dims, const MtpWeights *w, const void *h, c
   if (!w || !k_eff) return MTP_ERR_INVALID_ARG;
   const MtpModule one{*w, k_cache, v_cache};
   Draft D;
+  DraftOpts o;
+  o.stop_p = stop_p;
+  o.k_eff = k_eff;
   int rc = prepare_draft(dims, &one, 1, h, last_tok, ctx_len, k, T, mode, u_draft, draft_tok, draft_logits, ws,
-                         ws_bytes, false, stop_p, k_eff, &D);
+                         ws_bytes, false, o, &D);
   if (rc) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = run_draft(D, s);
@@ -397,7 +440,7 @@ int mtp_draft_noalloc(const MtpDims *dims, const MtpWeights *w, const void *h, c
   const MtpModule one{*w, k_cache, v_cache};
   Draft D;
   rc = prepare_draft(dims, &one, 1, h, last_tok, ctx_len, k, T, mode, u_draft, draft_tok, draft_logits, scratch,
-                     MTP_STATIC_SCRATCH_BYTES, false, 0.f, nullptr, &D);
+                     MTP_STATIC_SCRATCH_BYTES, false, DraftOpts{}, &D);
   if (rc) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the status word and the LM-head ticket counter (the first two aligned
@@ -442,18 +485,18 @@ int spec_verify(int B, int k, int V, float T, int mode, const float *target_logi
 
 // spec_step over modules, with the dynamic draft length when k_eff is given.
 static int step_call(const MtpDims *dims, const MtpModule *modules, int n_modules, const void *h,
-                     const int32_t *last_tok, const int32_t *ctx_len, int k, float T, int mode, float stop_p,
+                     const int32_t *last_tok, const int32_t *ctx_len, int k, float T, int mode, const DraftOpts &o,
                      const float *u_draft, const float *target_logits, const float *u_accept, const float *u_final,
-                     int32_t *draft_tok, float *draft_logits, int32_t *k_eff, int32_t *out_tok,
-                     int32_t *accept_len, int32_t *num_accepted, void *ws, size_t ws_bytes, mtp_stream_t stream) {
+                     int32_t *draft_tok, float *draft_logits, int32_t *out_tok, int32_t *accept_len,
+                     int32_t *num_accepted, void *ws, size_t ws_bytes, mtp_stream_t stream) {
   Draft D;
   int rc = prepare_draft(dims, modules, n_modules, h, last_tok, ctx_len, k, T, mode, u_draft, draft_tok,
-                         draft_logits, ws, ws_bytes, mode == MTP_STOCHASTIC, stop_p, k_eff, &D);
+                         draft_logits, ws, ws_bytes, mode == MTP_STOCHASTIC, o, &D);
   if (rc) return rc;
   VerifyArgs a{};
   const WsLayout L = draft_layout(*dims, k);
   rc = prepare_verify(dims->B, k, dims->V, T, mode, target_logits, D.c.logits, draft_tok, u_accept, u_final, out_tok,
-                      accept_len, num_accepted, static_cast<char *>(ws) + L.vstate, L.total - L.vstate, false, k_eff,
+                      accept_len, num_accepted, static_cast<char *>(ws) + L.vstate, L.total - L.vstate, false, o.k_eff,
                       &a);
   if (rc) return rc;
   a.status = D.c.status;
@@ -469,9 +512,25 @@ int spec_step_modules(const MtpDims *dims, const MtpModule *modules, int n_modul
                       const float *u_draft, const float *target_logits, const float *u_accept,
                       const float *u_final, int32_t *draft_tok, float *draft_logits, int32_t *out_tok,
                       int32_t *accept_len, int32_t *num_accepted, void *ws, size_t ws_bytes, mtp_stream_t stream) {
-  return step_call(dims, modules, n_modules, h, last_tok, ctx_len, k, T, mode, 0.f, u_draft, target_logits,
-                   u_accept, u_final, draft_tok, draft_logits, nullptr, out_tok, accept_len, num_accepted, ws,
-                   ws_bytes, stream);
+  return step_call(dims, modules, n_modules, h, last_tok, ctx_len, k, T, mode, DraftOpts{}, u_draft, target_logits,
+                   u_accept, u_final, draft_tok, draft_logits, out_tok, accept_len, num_accepted, ws, ws_bytes,
+                   stream);
+}
+
+int spec_step_reduced(const MtpDims *dims, const MtpWeights *w, const void *head_rows, const int32_t *vocab_map,
+                      int n_draft_vocab, const void *h, const int32_t *last_tok, void *k_cache, void *v_cache,
+                      const int32_t *ctx_len, int k, float T, int mode, const float *u_draft,
+                      const float *target_logits, const float *u_accept, const float *u_final, int32_t *draft_tok,
+                      float *draft_logits, int32_t *out_tok, int32_t *accept_len, int32_t *num_accepted, void *ws,
+                      size_t ws_bytes, mtp_stream_t stream) {
+  if (!w || !vocab_map) return MTP_ERR_INVALID_ARG;
+  const MtpModule one{*w, k_cache, v_cache};
+  DraftOpts o;
+  o.head = head_rows;
+  o.vmap = vocab_map;
+  o.Vd = n_draft_vocab;
+  return step_call(dims, &one, 1, h, last_tok, ctx_len, k, T, mode, o, u_draft, target_logits, u_accept, u_final,
+                   draft_tok, draft_logits, out_tok, accept_len, num_accepted, ws, ws_bytes, stream);
 }
 
 int spec_step_dynamic(const MtpDims *dims, const MtpWeights *w, const void *h, const int32_t *last_tok,
@@ -482,8 +541,11 @@ int spec_step_dynamic(const MtpDims *dims, const MtpWeights *w, const void *h, c
                       mtp_stream_t stream) {
   if (!w || !k_eff) return MTP_ERR_INVALID_ARG;
   const MtpModule one{*w, k_cache, v_cache};
-  return step_call(dims, &one, 1, h, last_tok, ctx_len, k, T, mode, stop_p, u_draft, target_logits, u_accept,
-                   u_final, draft_tok, draft_logits, k_eff, out_tok, accept_len, num_accepted, ws, ws_bytes, stream);
+  DraftOpts o;
+  o.stop_p = stop_p;
+  o.k_eff = k_eff;
+  return step_call(dims, &one, 1, h, last_tok, ctx_len, k, T, mode, o, u_draft, target_logits, u_accept, u_final,
+                   draft_tok, draft_logits, out_tok, accept_len, num_accepted, ws, ws_bytes, stream);
 }
 
 int spec_step(const MtpDims *dims, const MtpWeights *w, const void *h, const int32_t *last_tok, void *k_cache,

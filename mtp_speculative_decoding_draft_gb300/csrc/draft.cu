@@ -185,7 +185,10 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(DraftCtx c, GemvPlan
         } else if (OP == OP_DOWN) {
           c.x2[(size_t)b * c.d + row] = __ldcg(&c.x1[(size_t)b * c.d + row]) + y;
         } else {  // LM head
-          if (c.logits) c.logits[((size_t)b * c.k + c.j) * c.V + row] = y;
+          if (c.logits) {
+            const int v = vocab_id(c, row);
+            if (v >= 0) c.logits[((size_t)b * c.k + c.j) * c.V + v] = y;
+          }
           ys[(size_t)rl * BG + bb] = y;
         }
       }
@@ -634,6 +637,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(DraftCtx c) {
     c.o[(size_t)b * nq + ((size_t)g * group + h) * DH + e] = O / Ls;
   }
   cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
+}
+
+__global__ void __launch_bounds__(256) fill_kernel(float *p, size_t n, float v) {
+  grid_dep_wait();  // the previous call may still read these
+  grid_dep_launch();
+  for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (size_t)gridDim.x * 256) p[i] = v;
+}
+
+cudaError_t launch_fill(float *p, size_t n, float v, cudaStream_t s, bool pdl) {
+  cudaLaunchConfig_t cfg{};
+  const size_t blocks = (n + 255) / 256;
+  cfg.gridDim = dim3((unsigned)(blocks < 4096 ? (blocks > 0 ? blocks : 1) : 4096));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  note_launch();
+  return cudaLaunchKernelEx(&cfg, fill_kernel, p, n, v);
 }
 
 int attention_cluster_size(int ctx_max, int pairs, int num_sms, int max_cluster) {

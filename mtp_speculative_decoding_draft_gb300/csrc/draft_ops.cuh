@@ -48,6 +48,18 @@ __device__ __forceinline__ int depth_token(const DraftCtx &c, int b) {
   return t;
 }
 
+// Full-vocabulary id of draft-head row i (a reduced draft vocabulary maps its
+// rows; an id outside [0, V) flags a bad token and reads as -1).
+__device__ __forceinline__ int vocab_id(const DraftCtx &c, int i) {
+  if (!c.vmap) return i;
+  const int v = __ldg(&c.vmap[i]);
+  if (v < 0 || v >= c.V) {
+    set_status(c.status, kStatusBadToken);
+    return -1;
+  }
+  return v;
+}
+
 __device__ __forceinline__ int clamped_ctx(const DraftCtx &c, int b) {
   int L = __ldg(&c.ctx_len[b]);
   return min(max(L, 0), c.Lmax - c.k);
@@ -147,7 +159,7 @@ __device__ __forceinline__ const uint16_t *weight_row(const DraftCtx &c, int row
   if (OP == OP_WO) return c.wo + (size_t)row * K;
   if (OP == OP_GATEUP) return ((row & 1) ? c.wup : c.wgate) + (size_t)(row >> 1) * K;
   if (OP == OP_DOWN) return c.wdown + (size_t)row * K;
-  return c.E + (size_t)row * K;
+  return c.head + (size_t)row * K;
 }
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + __expf(-z)); }
@@ -229,14 +241,18 @@ __device__ inline void lm_select_warp(const DraftCtx &c, int G, int rpc) {
       cstar = __shfl_sync(0xffffffffu, cstar, 0);
       before = __shfl_sync(0xffffffffu, before, 0);
       // rows of CTA cstar (same split as the launch)
-      const int lo = cstar * rpc, hi = min(c.V, lo + rpc);
-      const float *lg = c.logits + ((size_t)b * c.k + c.j) * c.V;
+      const int lo = cstar * rpc, hi = min(c.Vd, lo + rpc);
+      const float *lg = c.logits + ((size_t)b * c.k + c.j) * c.V;  // head row i at vocab_id(i)
       const int per = (hi - lo + 31) / 32;
       const int a0 = lo + lane * per, a1 = min(hi, a0 + per);
+      auto logit = [&](int i) {
+        const int v = vocab_id(c, i);
+        return v < 0 ? -INFINITY : __ldcg(&lg[v]);
+      };
       double ls = 0.0;
       int lastpos = -1;
       for (int i = a0; i < a1; ++i) {
-        const float w = exp2f((__ldcg(&lg[i]) - M) * cT);
+        const float w = exp2f((logit(i) - M) * cT);
         ls += (double)w;
         if (w > 0.f) lastpos = i;
       }
@@ -252,7 +268,7 @@ __device__ inline void lm_select_warp(const DraftCtx &c, int G, int rpc) {
       if (before >= 0.0 && before + incl > target) {
         double cum = before + excl;
         for (int i = a0; i < a1; ++i) {
-          cum += (double)exp2f((__ldcg(&lg[i]) - M) * cT);
+          cum += (double)exp2f((logit(i) - M) * cT);
           if (cum > target) {
             found = i;
             break;
@@ -266,6 +282,7 @@ __device__ inline void lm_select_warp(const DraftCtx &c, int G, int rpc) {
       for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
       tok = found != 0x7fffffff ? found : (lp >= 0 ? lp : Mi);
     }
+    if (finite) tok = vocab_id(c, tok);  // head row -> vocabulary id
     if (lane == 0) c.draft_tok[b * c.k + c.j] = tok;
     if (lane == 0 && c.k_eff && finite) stop_check(c, b, 1.0 / Z);
   }

@@ -19,6 +19,11 @@ struct DraftCtx {
   // weights (bf16)
   const uint16_t *E, *fc, *wq, *wk, *wv, *wo, *wgate, *wup, *wdown;
   const uint16_t *g_emb, *g_hid, *g_attn, *g_mlp, *g_final;
+  // the draft's vocabulary head: E itself, or the Vd rows of a reduced draft
+  // vocabulary with the full-vocabulary id of each (vmap null: head = E, Vd = V)
+  const uint16_t *head;
+  const int *vmap;
+  int Vd;
   // caller inputs
   const uint16_t *h;      // [B, d] trunk hidden state
   const int *last_tok;    // [B]
@@ -71,6 +76,8 @@ constexpr int kMaxGroup = 8;        // Hq / Hkv
 GemvPlan plan_gemv(int op, int N, int K, int B, int num_sms);
 cudaError_t launch_gemv(const DraftCtx &c, const GemvPlan &g, cudaStream_t s, bool pdl);
 cudaError_t launch_attention(const DraftCtx &c, int cluster, cudaStream_t s, bool pdl);
+// p[0 .. n) = v (a reduced draft vocabulary's logits: -inf at the other ids)
+cudaError_t launch_fill(float *p, size_t n, float v, cudaStream_t s, bool pdl);
 size_t attention_smem_bytes(int Dh);
 int attention_cluster_size(int ctx_max, int pairs, int num_sms, int max_cluster);
 // Tensor-core decode attention (GQA groups of 2..16, head size 64 or 128).

@@ -467,7 +467,7 @@ __host__ __device__ inline int sel_subs(int V) { return (V + kSelSub - 1) / kSel
 
 __global__ void __launch_bounds__(kSelThreads) tc_select_part_kernel(DraftCtx c, const float *logits, size_t bstride,
                                                                      float4 *part) {
-  const int b = blockIdx.y, V = c.V, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int b = blockIdx.y, V = c.Vd, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int q = blockIdx.x * kSelWarps + warp, nq = sel_subs(V);
   grid_dep_wait();
   grid_dep_launch();
@@ -515,7 +515,7 @@ __global__ void __launch_bounds__(kSelThreads) tc_select_part_kernel(DraftCtx c,
 
 __global__ void __launch_bounds__(32) tc_select_fin_kernel(DraftCtx c, const float *logits, size_t bstride,
                                                            const float4 *part) {
-  const int b = blockIdx.x, V = c.V, lane = threadIdx.x, nq = sel_subs(V);
+  const int b = blockIdx.x, V = c.Vd, lane = threadIdx.x, nq = sel_subs(V);
   grid_dep_wait();
   grid_dep_launch();
   const float4 *pp = part + (size_t)b * nq;
@@ -617,8 +617,22 @@ __global__ void __launch_bounds__(32) tc_select_fin_kernel(DraftCtx c, const flo
     }
     tok = found != 0x7fffffff ? found : (lastpos >= 0 ? lastpos : I);
   }
+  if (finite) tok = vocab_id(c, tok);  // head row -> vocabulary id
   if (lane == 0) c.draft_tok[b * c.k + c.j] = tok;
   if (lane == 0 && c.k_eff && finite) stop_check(c, b, 1.0 / Z);
+}
+
+// A reduced draft vocabulary: head row i's logit to its vocabulary id in the
+// caller's full-vocabulary logits (the other ids hold -inf from the start of
+// the call).
+__global__ void __launch_bounds__(256) tc_scatter_logits_kernel(DraftCtx c, const float *lg) {
+  const int b = blockIdx.y;
+  grid_dep_wait();
+  grid_dep_launch();
+  for (int i = blockIdx.x * 256 + threadIdx.x; i < c.Vd; i += gridDim.x * 256) {
+    const int v = vocab_id(c, i);
+    if (v >= 0) c.logits[((size_t)b * c.k + c.j) * c.V + v] = __ldcg(&lg[(size_t)b * c.Vd + i]);
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -696,7 +710,7 @@ OpShape op_shape(const DraftCtx &c, int op) {
       s.K = c.d;
       break;
     case OP_DOWN: s.w[0] = c.wdown; s.rows[0] = c.d; s.K = c.F; break;
-    default: s.w[0] = c.E; s.rows[0] = c.V; s.K = c.d; break;
+    default: s.w[0] = c.head; s.rows[0] = c.Vd; s.K = c.d; break;
   }
   return s;
 }
@@ -974,18 +988,24 @@ cudaError_t run_block_post_tc(const DraftCtx &c, const TcBufs &t, cudaStream_t s
 }
 
 cudaError_t run_lmhead_tc(const DraftCtx &c, const TcBufs &t, cudaStream_t s, bool pdl) {
-  // straight into the caller's logits when it keeps them
-  float *lg = c.logits ? c.logits + (size_t)c.j * c.V : t.part;
-  const size_t lstride = c.logits ? (size_t)c.k * c.V : (size_t)c.V;
+  // straight into the caller's logits when it keeps them (and the head is
+  // the full vocabulary); a reduced head's Vd logits go to the workspace and
+  // are scattered to their vocabulary ids after the selection
+  const bool direct = c.logits && !c.vmap;
+  float *lg = direct ? c.logits + (size_t)c.j * c.V : t.part;
+  const size_t lstride = direct ? (size_t)c.k * c.V : (size_t)c.Vd;
   int ks = 1;
   cudaError_t e = run_gemm(c, t, OP_LMHEAD, lg, lstride, s, pdl, &ks);
   if (e) return e;
   // past the logits, on a 16-byte boundary
   float4 *sel = reinterpret_cast<float4 *>(t.part + ((size_t)c.B * c.V + 3) / 4 * 4);
-  e = launch(tc_select_part_kernel, dim3((sel_subs(c.V) + kSelWarps - 1) / kSelWarps, c.B), kSelThreads, 0, s, pdl,
-             c, (const float *)lg, lstride, sel);
+  e = launch(tc_select_part_kernel, dim3((sel_subs(c.Vd) + kSelWarps - 1) / kSelWarps, c.B), kSelThreads, 0, s,
+             pdl, c, (const float *)lg, lstride, sel);
   if (e) return e;
-  return launch(tc_select_fin_kernel, dim3(c.B), 32, 0, s, pdl, c, (const float *)lg, lstride, (const float4 *)sel);
+  e = launch(tc_select_fin_kernel, dim3(c.B), 32, 0, s, pdl, c, (const float *)lg, lstride, (const float4 *)sel);
+  if (e || direct || !c.logits) return e;
+  return launch(tc_scatter_logits_kernel, dim3((c.Vd + 255) / 256 < 64 ? (c.Vd + 255) / 256 : 64, c.B), 256, 0, s,
+                pdl, c, (const float *)lg);
 }
 
 }  // namespace mtp

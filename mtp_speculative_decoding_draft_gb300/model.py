@@ -95,6 +95,18 @@ class DraftModule:
                              self.draft_tok, self.draft_logits if logits else None, self.k_eff, self.out_tok,
                              self.accept_len, self.num_accepted, self.ws, stream)
 
+    def set_draft_vocab(self, vmap, head_bits):
+        """Draft over a reduced vocabulary from now on: vmap [N] ids, head [N, d] bf16 bits."""
+        self.vmap = to_device(np.asarray(vmap, dtype=np.int32), self.device)
+        self.head = to_device_bf16(head_bits, self.device)
+
+    def step_reduced(self, T, mode, target_logits, u_draft=None, u_accept=None, u_final=None, logits=True,
+                     stream=None):
+        bd.spec_step_reduced(self.dims, self.wptr, self.head, self.vmap, self.h, self.last_tok, self.k_cache,
+                             self.v_cache, self.ctx_len, self.k, T, mode, u_draft, target_logits, u_accept,
+                             u_final, self.draft_tok, self.draft_logits if logits else None, self.out_tok,
+                             self.accept_len, self.num_accepted, self.ws, stream)
+
     def status(self, stream=None):
         return bd.get_status(self.ws, stream)
 

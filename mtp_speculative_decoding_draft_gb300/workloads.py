@@ -211,6 +211,17 @@ def make_module_weights(w, m, E=None):
     return bits
 
 
+def make_draft_vocab(w, n):
+    """A reduced draft vocabulary of n distinct ids in [0, V), in a seeded random
+    order (the order of the draft head's rows), and the head: those rows of E,
+    as bf16 bits.  Stands in for FR-Spec's most frequent tokens: synthetic
+    weights have no token frequencies."""
+    g = _stream(w.seed, "draft_vocab", 0)
+    vmap = g.permutation(w.V)[:n].astype(np.int32)
+    E = to_bf16_bits(normal(w.seed, "w.E", weight_shapes(w)["E"], std=w.w_std))
+    return vmap, np.ascontiguousarray(E[vmap])
+
+
 def make_module_cache(w, m):
     """K/V caches [B, Hkv, Lmax, Dh] bf16 N(0,1) of module m (m = 0: make_context's)."""
     shape = (w.B, w.Hkv, w.Lmax, w.Dh)

@@ -143,7 +143,8 @@ def draft_depth(W, dims, x, tok, keys, values):
     act = silu(linear(W["wgate"], nrm2)) * linear(W["wup"], nrm2)
     x2 = x1 + linear(W["wdown"], act)
 
-    logits = linear(W["E"], rmsnorm(x2, W["g_final"], eps))
+    # the vocabulary head: E, or the rows of a reduced draft vocabulary
+    logits = linear(W.get("head", W["E"]), rmsnorm(x2, W["g_final"], eps))
     return x2, logits, k_new, v_new
 
 
@@ -192,7 +193,7 @@ def dynamic_depths(draft_logits, mode, T, stop_p):
 
 
 def mtp_draft(W, dims, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode,
-              u_draft=None, seqs=None):
+              u_draft=None, seqs=None, vocab_map=None):
     """Run the module k times in a chain and return the drafts.
 
     h        [B, d] trunk hidden states (bf16 bits or reals).
@@ -206,7 +207,7 @@ def mtp_draft(W, dims, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode,
     hidden [n,k,d] (x2 of every depth), k_new / v_new [n,k,Hkv,Dh] (bf16 values).
     """
     return mtp_draft_modules([(W, k_cache, v_cache)], dims, h, last_tok, ctx_len, k, T, mode,
-                             u_draft, seqs)
+                             u_draft, seqs, vocab_map)
 
 
 def module_of_depth(j, n_modules):
@@ -218,7 +219,8 @@ def module_of_depth(j, n_modules):
     return min(j, n_modules - 1)
 
 
-def mtp_draft_modules(modules, dims, h, last_tok, ctx_len, k, T, mode, u_draft=None, seqs=None):
+def mtp_draft_modules(modules, dims, h, last_tok, ctx_len, k, T, mode, u_draft=None, seqs=None,
+                      vocab_map=None):
     """The chain over distinct modules.
 
     modules  list of (W, k_cache, v_cache): each module's weights and its own
@@ -230,6 +232,15 @@ def mtp_draft_modules(modules, dims, h, last_tok, ctx_len, k, T, mode, u_draft=N
     Other arguments and the returned dict as ``mtp_draft``; the dict also holds
     module [k] (the module of each depth) and row [n, k] (the cache position of
     each depth's K/V row in its module's cache).
+
+    vocab_map  [N] (optional): a reduced draft vocabulary ("Optimize vLLM
+    speculative decoding with FastMTP heads", sections "How FastMTP-style
+    fine-tuning works in Speculators" and "What's next?", name FR-Spec-style
+    reduction; the rule is this build's reading).  The weights then carry
+    "head" [N, d], the rows vocab_map of E; the draft distribution is the
+    softmax over those N logits, the draft token vocab_map of the choice among
+    them, and draft_logits hold the N logits at their ids and -inf elsewhere
+    (q = 0 outside the reduced vocabulary).
     """
     seqs = list(range(np.asarray(last_tok).shape[0])) if seqs is None else list(seqs)
     n = len(seqs)
@@ -258,10 +269,15 @@ def mtp_draft_modules(modules, dims, h, last_tok, ctx_len, k, T, mode, u_draft=N
         logits = round_f32(logits)
         for i, b in enumerate(seqs):
             u = None if mode == GREEDY else float(u_draft[b][j])
-            out["draft_tok"][i, j] = select_token(logits[i], mode, T, u)
+            choice = select_token(logits[i], mode, T, u)
+            out["draft_tok"][i, j] = choice if vocab_map is None else int(vocab_map[choice])
             keys[m][i] = np.concatenate([keys[m][i], k_new[i][:, None, :]], axis=1)
             values[m][i] = np.concatenate([values[m][i], v_new[i][:, None, :]], axis=1)
-        out["draft_logits"][:, j] = logits
+        if vocab_map is None:
+            out["draft_logits"][:, j] = logits
+        else:
+            out["draft_logits"][:, j] = -np.inf
+            out["draft_logits"][:, j][:, np.asarray(vocab_map)] = logits
         out["hidden"][:, j] = x
         out["k_new"][:, j] = k_new
         out["v_new"][:, j] = v_new

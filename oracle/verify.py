@@ -104,7 +104,8 @@ def spec_verify(target_logits, draft_logits, draft_tok, mode, T=1.0,
 
 
 def spec_step(W, dims, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode,
-              target_logits, u_draft=None, u_accept=None, u_final=None, seqs=None, stop_p=None):
+              target_logits, u_draft=None, u_accept=None, u_final=None, seqs=None, stop_p=None,
+              vocab_map=None):
     """Draft k tokens with the chained module, then verify them.  With stop_p,
     each sequence keeps the drafts before its first depth of confidence below
     stop_p (``block.dynamic_depths``; the result dict then holds k_eff).
@@ -113,15 +114,15 @@ def spec_step(W, dims, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode,
     num_accepted) for the sequences in ``seqs``.
     """
     return spec_step_modules([(W, k_cache, v_cache)], dims, h, last_tok, ctx_len, k, T, mode,
-                             target_logits, u_draft, u_accept, u_final, seqs, stop_p)
+                             target_logits, u_draft, u_accept, u_final, seqs, stop_p, vocab_map)
 
 
 def spec_step_modules(modules, dims, h, last_tok, ctx_len, k, T, mode, target_logits,
-                      u_draft=None, u_accept=None, u_final=None, seqs=None, stop_p=None):
+                      u_draft=None, u_accept=None, u_final=None, seqs=None, stop_p=None, vocab_map=None):
     """``spec_step`` over a chain of distinct modules (``block.mtp_draft_modules``)."""
     from .block import dynamic_depths, mtp_draft_modules
     seqs = list(range(np.asarray(last_tok).shape[0])) if seqs is None else list(seqs)
-    dr = mtp_draft_modules(modules, dims, h, last_tok, ctx_len, k, T, mode, u_draft, seqs)
+    dr = mtp_draft_modules(modules, dims, h, last_tok, ctx_len, k, T, mode, u_draft, seqs, vocab_map)
     tl = np.asarray(target_logits)[seqs]
     ua = None if u_accept is None else np.asarray(u_accept)[seqs]
     uf = None if u_final is None else np.asarray(u_final)[seqs]

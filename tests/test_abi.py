@@ -65,5 +65,7 @@ def test_host_side_validation_without_gpu(lib):
                                None, None, None, 0, None) == -1       # no weights, no k_eff
     assert L.spec_verify_dynamic(4, 0, 100, 1.0, 0, None, None, None, None, None, None, None, None, None, None, 0,
                                  None) == -1
+    assert L.mtp_draft_reduced(ctypes.byref(dims), None, None, None, 0, None, None, None, None, None, 3, 1.0, 0,
+                               None, None, None, None, 0, None) == -1   # no weights, no map
     assert L.mtp_error_string(-3) == b"workspace too small"
     assert L.spec_verify_workspace_size(4, 3, 100) >= 4
