@@ -62,7 +62,7 @@ int check_dims(const MtpDims *d, int k) {
 }
 
 struct WsLayout {
-  size_t status, lm_cnt, x0, x1, x2, q, o, act, lm_part, logits, vstate, tc_a[3], tc_part, total;
+  size_t status, lm_cnt, x0, x1, x2, q, o, act, lm_part, logits, vstate, tc_a[3], tc_part, order, total;
   bool tc;
   TcSizes tz;
 };
@@ -103,6 +103,8 @@ WsLayout draft_layout(const MtpDims &d, int k) {
     }
     L.tc_part = off;
     off += up(L.tz.part_floats * 4);
+    L.order = off;
+    off += up((size_t)d.B * 4);
   }
   L.total = off;
   return L;
@@ -246,6 +248,7 @@ int prepare_draft(const MtpDims *dims, const MtpModule *mods, int nmod, const vo
     out->t.rows = L.tz.rows;
     out->t.kmax = L.tz.kmax;
     out->t.part = reinterpret_cast<float *>(base + L.tc_part);
+    c.seq_order = reinterpret_cast<int *>(base + L.order);
     out->t.part_floats = L.tz.part_floats;
   }
   return MTP_OK;

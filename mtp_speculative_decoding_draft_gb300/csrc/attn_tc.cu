@@ -110,7 +110,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) attn_tc_kernel(const __grid_con
   float *qo = wst + kTcWarps * 16 * (DH + 2);                           // [16][DH], after the loop
 
   const DraftCtx &c = p.c;
-  const int g = blockIdx.y, b = blockIdx.z;
+  // longest contexts first, so that the last clusters to be scheduled are short
+  const int g = blockIdx.y, b = c.seq_order ? __ldg(&c.seq_order[blockIdx.z]) : (int)blockIdx.z;
   const int C = (int)cluster_size(), rank = (int)cluster_rank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int group = c.Hq / c.Hkv;

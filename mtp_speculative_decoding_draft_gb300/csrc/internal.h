@@ -48,6 +48,9 @@ struct DraftCtx {
   int lm_grid;            // CTAs of the LM-head launch
   int lm_rpc;             // vocabulary rows per LM-head CTA
   int zero_counters;      // this launch clears the ticket counters first
+  // sequences longest context first (batches on the tensor-core path; null:
+  // index order): the attention's clusters are scheduled in this order
+  int *seq_order;         // [B]
 };
 
 enum GemvOp { OP_FC = 0, OP_QKV = 1, OP_WO = 2, OP_GATEUP = 3, OP_DOWN = 4, OP_LMHEAD = 5 };

@@ -323,6 +323,18 @@ __global__ void __launch_bounds__(kPrepThreads) tc_prep_fc_kernel(DraftCtx c, Tc
     c.k_eff[b] = c.k;
     if (b == 0) *c.n_active = (unsigned)c.B;
   }
+  if (c.seq_order && c.j == 0) {
+    // this sequence's place in the longest-context-first order (ties by index)
+    const int L = __ldg(&c.ctx_len[b]);
+    int before = 0;
+    for (int o = threadIdx.x; o < c.B; o += kPrepThreads) {
+      const int Lo = __ldg(&c.ctx_len[o]);
+      before += (Lo > L || (Lo == L && o < b)) ? 1 : 0;
+    }
+    before = (int)block_sum_256((float)before, red);
+    if (threadIdx.x == 0) c.seq_order[before] = b;
+    __syncthreads();
+  }
   const int tok = depth_token(c, b);
   const uint16_t *e = c.E + (size_t)tok * d;
   float s0 = 0.f, s1 = 0.f;
