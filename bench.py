@@ -58,21 +58,21 @@ def lmhead_bytes(w, logits_out, head_rows=None):
 # are unchanged; the summaries of the captures are kept under profiles/.
 NCU_TRAFFIC = {
     ("lm_head_gemv", "single_greedy_b1_d4096_v151936_ctx4096"): {
-        "bytes": 1244775424 + 3031808,
+        "bytes": 1244773888 + 2982656,
         "sources": {
-            "csrc/draft.cu": "13e1c2b716cefe9a649e8aae88bd225b4a0f9ac86dc8cece6ee2afc2eb123ece",
+            "csrc/draft.cu": "2d187302ba21e967a2a538b7d5f44a9876b2ebac216babfa86527f46a3cc322c",
             "csrc/draft_ops.cuh": "3067b6cc411842aa64b55c5c50ad63b20034f1eb2bdba96dc444c1983d92c325",
             "csrc/common.cuh": "fcd7bd8f56df32fc490b2c47f2fbc0f7f37047c578430d777438202c9279de66",
-            "csrc/internal.h": "d53bd2440af30e46859baefc729772cd592b6e5b2ae32e84da3001f7c8da4104",
+            "csrc/internal.h": "b43fd6a70993fe8eec8ad2b42064359652d9ada36507a33922564512b9f7169a",
         },
     },
     ("tc_gemm_kernel(LM head)", "batched_stochastic_b64_d4096_v151936_ctx1024-8192"): {
-        "bytes": 1248388096 + 7836416,
+        "bytes": 1248019712 + 7777280,
         "sources": {
-            "csrc/tc.cu": "bbf936c6286eab81ddd55dcbb75b7fa5ce319eb13fd25fb9147e60d0c7e49da8",
+            "csrc/tc.cu": "792cfe0e73815f8f7c27b8c8f32d9d2114544f1648f6d41af10c810afcce54fc",
             "csrc/tcgen05.cuh": "e128ff6d7c8451d618848063024b7cd0a98c722dd1b86ef0d04e6a07a9070ee7",
             "csrc/common.cuh": "fcd7bd8f56df32fc490b2c47f2fbc0f7f37047c578430d777438202c9279de66",
-            "csrc/internal.h": "d53bd2440af30e46859baefc729772cd592b6e5b2ae32e84da3001f7c8da4104",
+            "csrc/internal.h": "b43fd6a70993fe8eec8ad2b42064359652d9ada36507a33922564512b9f7169a",
         },
     },
     ("verify_kernel", "verify_sweep_b256_v151936_k3/greedy"): {

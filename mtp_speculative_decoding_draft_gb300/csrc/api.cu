@@ -36,7 +36,7 @@ int device_info(DevInfo *out) {
   DevInfo &di = g_dev[dev];
   if (!di.init) {
     if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MTP_ERR_CUDA;
-    di.max_cluster = 8;
+    di.max_cluster = 16;  // the non-portable size; the automatic choice stays at 8 or less
     if (verify_set_attributes() != cudaSuccess) return MTP_ERR_CUDA;
     if (tc_set_attributes() != cudaSuccess) return MTP_ERR_CUDA;
     di.init = true;
@@ -231,7 +231,8 @@ int prepare_draft(const MtpDims *dims, const MtpModule *mods, int nmod, const vo
   c.o = reinterpret_cast<float *>(base + L.o);
   c.act = reinterpret_cast<float *>(base + L.act);
   c.lm_part = reinterpret_cast<float *>(base + L.lm_part);
-  out->attn_cluster = attention_cluster_size(d.Lmax, d.B * d.Hkv, di.sms, di.max_cluster);
+  out->attn_cluster =
+      attention_cluster_size(d.Lmax, d.B * d.Hkv, di.sms, di.max_cluster, attention_tc_shape_ok(c));
 
   out->fc = plan_gemv(OP_FC, d.d, 2 * d.d, d.B, di.sms);
   out->qkv = plan_gemv(OP_QKV, (d.Hq + 2 * d.Hkv) * d.Dh, d.d, d.B, di.sms);

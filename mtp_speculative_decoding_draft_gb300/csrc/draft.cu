@@ -660,16 +660,20 @@ cudaError_t launch_fill(float *p, size_t n, float v, cudaStream_t s, bool pdl) {
   return cudaLaunchKernelEx(&cfg, fill_kernel, p, n, v);
 }
 
-int attention_cluster_size(int ctx_max, int pairs, int num_sms, int max_cluster) {
+int attention_cluster_size(int ctx_max, int pairs, int num_sms, int max_cluster, bool tc) {
   const int forced = env_int("MTP_ATTN_CLUSTER", 0);
   if (forced > 0) return forced < max_cluster ? forced : max_cluster;
-  // CTAs per (sequence, kv head): one per 512 context rows, at most 8 (a
-  // 16-CTA cluster of one-CTA-per-SM kernels does not fit every GPC at once),
-  // and no more than about four CTAs per SM in all
-  int C = (ctx_max + 511) / 512;
+  // CTAs per (sequence, kv head), and no more than about four CTAs per SM in
+  // all.  The CUDA-core kernel (one CTA per SM): one per 512 context rows, at
+  // most 8 (a 16-CTA cluster of it does not fit every GPC at once).  The
+  // tensor-core kernel (two CTAs per SM): one per 256 rows, at most 16 -- at a
+  // single sequence, 8 kv heads and 4096 rows, 16 runs the step 1.3% faster
+  // than 8 (measured).
+  int C = (ctx_max + (tc ? 255 : 511)) / (tc ? 256 : 512);
   const int by_sms = (4 * num_sms + pairs - 1) / (pairs > 0 ? pairs : 1);
   if (C > by_sms) C = by_sms;
-  const int cap = max_cluster < 8 ? max_cluster : 8;
+  const int lim = tc ? 16 : 8;
+  const int cap = max_cluster < lim ? max_cluster : lim;
   return C < 1 ? 1 : (C > cap ? cap : C);
 }
 

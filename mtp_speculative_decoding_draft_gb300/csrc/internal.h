@@ -82,7 +82,7 @@ cudaError_t launch_attention(const DraftCtx &c, int cluster, cudaStream_t s, boo
 // p[0 .. n) = v (a reduced draft vocabulary's logits: -inf at the other ids)
 cudaError_t launch_fill(float *p, size_t n, float v, cudaStream_t s, bool pdl);
 size_t attention_smem_bytes(int Dh);
-int attention_cluster_size(int ctx_max, int pairs, int num_sms, int max_cluster);
+int attention_cluster_size(int ctx_max, int pairs, int num_sms, int max_cluster, bool tc);
 // Tensor-core decode attention (GQA groups of 2..16, head size 64 or 128).
 bool attention_tc_shape_ok(const DraftCtx &c);
 cudaError_t launch_attention_tc(const DraftCtx &c, int cluster, cudaStream_t s, bool pdl);
