@@ -76,17 +76,19 @@ NCU_TRAFFIC = {
         },
     },
     ("verify_kernel", "verify_sweep_b256_v151936_k3/greedy"): {
-        "bytes": 622490880 + 3303680,
+        "bytes": 622433792 + 3021568,
         "sources": {
-            "csrc/verify.cu": "4f9309d361b99df630507ea36fb54694c9eba1421090f06589088e4d4c20f9cd",
+            "csrc/verify.cu": "f1d0b3ef5cf32a7d7279611da02f31cfe03a82a9ebe687965352321e233997f4",
             "csrc/common.cuh": "fcd7bd8f56df32fc490b2c47f2fbc0f7f37047c578430d777438202c9279de66",
+            "csrc/internal.h": "b43fd6a70993fe8eec8ad2b42064359652d9ada36507a33922564512b9f7169a",
         },
     },
     ("verify_kernel", "verify_sweep_b256_v151936_k3/stochastic"): {
-        "bytes": 1297813760 + 3417088,
+        "bytes": 1301748992 + 3004160,
         "sources": {
-            "csrc/verify.cu": "4f9309d361b99df630507ea36fb54694c9eba1421090f06589088e4d4c20f9cd",
+            "csrc/verify.cu": "f1d0b3ef5cf32a7d7279611da02f31cfe03a82a9ebe687965352321e233997f4",
             "csrc/common.cuh": "fcd7bd8f56df32fc490b2c47f2fbc0f7f37047c578430d777438202c9279de66",
+            "csrc/internal.h": "b43fd6a70993fe8eec8ad2b42064359652d9ada36507a33922564512b9f7169a",
         },
     },
 }
