@@ -130,3 +130,32 @@ def test_step_reduced(mode):
         am, sm = stochastic_path_margins(target[b], g_log[b], g_tok[b], u["u_accept"][b], float(u["u_final"][b]),
                                          w.T)
         assert am < 1e-6 or sm < 1e-6, "sequence %d differs (margins %.3g %.3g)" % (b, am, sm)
+
+
+def test_bad_map_ids_flag_the_status():
+    """An id outside [0, V) in the map is reported, never written."""
+    w = RED
+    wts, ctx, u, vmap, head, m = _setup(w, 300)
+    bad = vmap.copy()
+    bad[7] = w.V + 5
+    bad[8] = -3
+    m.draft_logits.fill_(0.0)
+    bd.mtp_draft_reduced(m.dims, m.wptr, to_device_bf16(head), to_device(bad), m.h, m.last_tok, m.k_cache,
+                         m.v_cache, m.ctx_len, w.k, w.T, STOCH, to_device(u["u_draft"]), m.draft_tok,
+                         m.draft_logits, m.ws)
+    torch.cuda.synchronize()
+    assert m.status() & bd.STATUS_BAD_TOKEN
+    lg = m.draft_logits.view(w.B, w.k, w.V).cpu().numpy()
+    good = np.delete(bad, [7, 8])
+    outside = np.ones(w.V, bool)
+    outside[good] = False
+    assert np.all(lg[:, :, outside] == -np.inf)   # nothing landed outside the valid ids
+
+
+def test_reduced_arguments_rejected_on_the_host():
+    w = RED
+    wts, ctx, u, vmap, head, m = _setup(w, 300)
+    small_map, small_head = vmap[:100], head[:100]          # fewer than 128 rows
+    with pytest.raises(bd.MtpError):
+        bd.mtp_draft_reduced(m.dims, m.wptr, to_device_bf16(small_head), to_device(small_map), m.h, m.last_tok,
+                             m.k_cache, m.v_cache, m.ctx_len, w.k, w.T, GREEDY, None, m.draft_tok, None, m.ws)
