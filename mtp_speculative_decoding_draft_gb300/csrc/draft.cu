@@ -37,6 +37,7 @@ namespace mtp {
 
 // Shared memory: [ring: W*S*PC*2 B][mbarriers: W*S*8 B][part: rpc*P*BG f32]
 //                [ys: rpc*BG f32 (LM head)][scales: 2*B f32][red: 64 f32]
+//                [sq: W*BG*2 f32 (per-warp sums of squares)]
 template <int OP, int NV, int BG>
 __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(DraftCtx c, GemvPlan g) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -49,6 +50,7 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(DraftCtx c, GemvPlan
   float *ys = part + (size_t)g.rows_per_cta * P * BG;
   float *scales = ys + (OP == OP_LMHEAD ? (size_t)g.rows_per_cta * BG : 0);
   float *red = scales + 2 * c.B;
+  float *sq = red + 64;
 
   const int p = warp % P, rs = warp / P;
   const int row0 = blockIdx.x * g.rows_per_cta;
@@ -97,23 +99,42 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(DraftCtx c, GemvPlan
       if (threadIdx.x == 0) *c.n_active = (unsigned)c.B;
     }
   }
-  compute_scales<OP>(c, scales, red);
+  const bool fac = g.factor != 0;
+  if (!fac) compute_scales<OP>(c, scales, red);
 
   int n = 0;
   bool ok = true;
   for (int grp = 0; grp < g.ngroups; ++grp) {
     // this warp's activation slice for the group's batch rows
     float a[BG][NV][8];
+    float s0[BG], s1[BG];
 #pragma unroll
     for (int bb = 0; bb < BG; ++bb) {
       const int b = grp * BG + bb;
+      s0[bb] = 0.f;
+      s1[bb] = 0.f;
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
         const int v = lane + 32 * i;
-        if (b < c.B && v * 8 < ncols) act8<OP>(c, b, col0 + v * 8, scales, a[bb][i]);
-        else {
+        if (b < c.B && v * 8 < ncols) {
+          if (fac) act8_unscaled<OP>(c, b, col0 + v * 8, a[bb][i], s0[bb], s1[bb]);
+          else act8<OP>(c, b, col0 + v * 8, scales, a[bb][i]);
+        } else {
 #pragma unroll
           for (int t = 0; t < 8; ++t) a[bb][i][t] = 0.f;
+        }
+      }
+    }
+    if (fac) {
+      // the warps of the first row set cover the input once: their sums of
+      // squares, combined in warp order in the epilogue, give the norm's scale
+#pragma unroll
+      for (int bb = 0; bb < BG; ++bb) {
+        s0[bb] = warp_sum(s0[bb]);
+        if (OP == OP_FC) s1[bb] = warp_sum(s1[bb]);
+        if (lane == 0 && rs == 0) {
+          sq[(warp * BG + bb) * 2] = s0[bb];
+          sq[(warp * BG + bb) * 2 + 1] = s1[bb];
         }
       }
     }
@@ -149,7 +170,22 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(DraftCtx c, GemvPlan
     }
     __syncthreads();
 
-    // epilogue for this batch group
+    // epilogue for this batch group; the norm's scale(s) from the warps' sums
+    float sc0[BG], sc1[BG];
+#pragma unroll
+    for (int bb = 0; bb < BG; ++bb) {
+      sc0[bb] = 1.f;
+      sc1[bb] = 1.f;
+      if (fac) {
+        float t0 = 0.f, t1 = 0.f;
+        for (int w = 0; w < P; ++w) {
+          t0 += sq[(w * BG + bb) * 2];
+          t1 += sq[(w * BG + bb) * 2 + 1];
+        }
+        sc0[bb] = rsqrtf(t0 / (float)c.d + c.eps);
+        sc1[bb] = rsqrtf(t1 / (float)c.d + c.eps);
+      }
+    }
     for (int rl = threadIdx.x; rl < nrows; rl += kGemvThreads) {
       const int row = row0 + rl;
       if (OP == OP_GATEUP && (rl & 1)) continue;
@@ -158,7 +194,18 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(DraftCtx c, GemvPlan
         const int b = grp * BG + bb;
         if (b >= c.B) break;
         float y = 0.f;
-        for (int pp = 0; pp < P; ++pp) y += part[((size_t)rl * P + pp) * BG + bb];
+        if (fac && OP == OP_FC) {  // pieces of the embedding half, then of the hidden half
+          float ye = 0.f, yx = 0.f;
+          for (int pp = 0; pp < P; ++pp) {
+            const float v = part[((size_t)rl * P + pp) * BG + bb];
+            if (pp * g.PC < c.d) ye += v;
+            else yx += v;
+          }
+          y = sc0[bb] * ye + sc1[bb] * yx;
+        } else {
+          for (int pp = 0; pp < P; ++pp) y += part[((size_t)rl * P + pp) * BG + bb];
+          if (fac) y *= sc0[bb];
+        }
         if (OP == OP_FC) {
           c.x0[(size_t)b * c.d + row] = y;
         } else if (OP == OP_QKV) {
@@ -181,6 +228,7 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(DraftCtx c, GemvPlan
         } else if (OP == OP_GATEUP) {
           float up = 0.f;
           for (int pp = 0; pp < P; ++pp) up += part[((size_t)(rl + 1) * P + pp) * BG + bb];
+          if (fac) up *= sc0[bb];
           c.act[(size_t)b * c.F + (row >> 1)] = silu_f(y) * up;
         } else if (OP == OP_DOWN) {
           c.x2[(size_t)b * c.d + row] = __ldcg(&c.x1[(size_t)b * c.d + row]) + y;
@@ -278,11 +326,16 @@ GemvPlan plan_gemv(int op, int N, int K, int B, int num_sms) {
   g.rows_per_cta = rpc;
   g.grid = (N + rpc - 1) / rpc;
   g.stages = env_int("MTP_GEMV_STAGES", 6);
+  // the norm's scale after the dot products: the ops with an input norm, when
+  // no piece of the input projection straddles its two halves (and
+  // MTP_GEMV_FACTOR is not 0)
+  g.factor = (op == OP_FC || op == OP_QKV || op == OP_GATEUP || op == OP_LMHEAD) &&
+             (op != OP_FC || (K / 2) % g.PC == 0) && env_int("MTP_GEMV_FACTOR", 1) != 0;
   auto smem_for = [&](int stages) {
     size_t s = (size_t)kGemvWarps * stages * (g.PC * 2 + 8);
     s += (size_t)g.rows_per_cta * g.P * g.bg * 4;
     if (op == OP_LMHEAD) s += (size_t)g.rows_per_cta * g.bg * 4;
-    s += (size_t)2 * B * 4 + 64 * 4;
+    s += (size_t)2 * B * 4 + 64 * 4 + (size_t)kGemvWarps * 2 * 2 * 4;
     return s;
   };
   const int smem_cap = env_int("MTP_GEMV_SMEM_KB", 110) * 1024;

@@ -146,6 +146,49 @@ __device__ __forceinline__ void act8(const DraftCtx &c, int b, int col, const fl
   }
 }
 
+// The same eight values with the norm's gain but not its scale -- the launch
+// applies the scale to the finished dot products, W (s g x) = s (W (g x)), so
+// no CTA has to reduce the whole vector before it starts streaming -- and the
+// raw values' sum of squares added to sq0 (the first normalised vector) or sq1
+// (the input projection's second one, the hidden state).
+template <int OP>
+__device__ __forceinline__ void act8_unscaled(const DraftCtx &c, int b, int col, float *out, float &sq0,
+                                              float &sq1) {
+  const int d = c.d;
+  float g[8];
+  if (OP == OP_FC) {
+    if (col < d) {
+      load8_bf16(c.E + (size_t)depth_token(c, b) * d + col, out);
+      load8_bf16(c.g_emb + col, g);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        sq0 = fmaf(out[t], out[t], sq0);
+        out[t] *= g[t];
+      }
+    } else {
+      const int cc = col - d;
+      if (c.j == 0) load8_bf16(c.h + (size_t)b * d + cc, out);
+      else load8_f32(c.x2 + (size_t)b * d + cc, out);
+      load8_bf16(c.g_hid + cc, g);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        sq1 = fmaf(out[t], out[t], sq1);
+        out[t] *= g[t];
+      }
+    }
+  } else {
+    const float *x = OP == OP_QKV ? c.x0 : (OP == OP_GATEUP ? c.x1 : c.x2);
+    const uint16_t *gp = OP == OP_QKV ? c.g_attn : (OP == OP_GATEUP ? c.g_mlp : c.g_final);
+    load8_f32(x + (size_t)b * d + col, out);
+    load8_bf16(gp + col, g);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      sq0 = fmaf(out[t], out[t], sq0);
+      out[t] *= g[t];
+    }
+  }
+}
+
 template <int OP>
 __device__ __forceinline__ const uint16_t *weight_row(const DraftCtx &c, int row, int K) {
   if (OP == OP_FC) return c.fc + (size_t)row * K;

@@ -68,6 +68,7 @@ struct GemvPlan {
   int bg;            // batch rows per group (activation registers per lane)
   int ngroups;       // batch groups = ceil(B / bg)
   int stages;        // TMA ring depth per warp
+  int factor;        // the norm's scale applied to the finished dot products (else to the inputs)
   size_t smem;       // dynamic shared memory bytes
 };
 
