@@ -137,6 +137,9 @@ class ClockSampler:
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
+            if self.path:
+                self.f.close()
+                os.remove(self.path)
 
     def stop(self):
         if self.proc is None:
