@@ -1,0 +1,58 @@
+"""Host-side logic of bench.py: the algorithmic step bytes its roofline fraction
+divides by, for the plain chain and the next rows' options, and the traffic
+table's source check."""
+
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from mtp_speculative_decoding_draft_gb300 import workloads as W  # noqa: E402
+
+
+def test_single_sequence_step_bytes():
+    w = W.SINGLE_GREEDY
+    ctx = np.array([4096])
+    block = (w.d * 2 * w.d + (w.Hq + 2 * w.Hkv) * w.Dh * w.d + w.d * w.Hq * w.Dh + 3 * w.d * w.F + 5 * w.d)
+    weights = 3 * (block + w.V * w.d) * 2
+    kv = sum(4096 + j + 1 for j in range(3)) * w.Hkv * w.Dh * 2 * 2
+    target = 1 * 4 * w.V * 4
+    assert bench.step_bytes(w, ctx, False) == weights + kv + target
+    assert abs(bench.step_bytes(w, ctx, False) / 1e9 - 5.146) < 1e-3
+
+
+def test_options_change_the_counted_bytes():
+    w = W.SINGLE_GREEDY
+    ctx = np.array([4096])
+    full = bench.step_bytes(w, ctx, False)
+    per_row = w.Hkv * w.Dh * 2 * 2
+    # one module per depth: every depth sees its own context plus one row
+    assert full - bench.step_bytes(w, ctx, False, n_modules=3) == (1 + 2) * per_row
+    # a chain stopped after depth 0 streams one depth of weights and K/V
+    one = bench.step_bytes(w, ctx, False, depths=1)
+    assert full - one == 2 * (bench.block_elements(w) + w.V * w.d) * 2 + (4098 + 4099) * per_row
+    # a reduced head of 32768 rows
+    red = bench.step_bytes(w, ctx, False, head_rows=32768)
+    assert full - red == 3 * (w.V - 32768) * w.d * 2
+    assert bench.lmhead_bytes(w, False, 32768) == 32768 * w.d * 2
+
+
+def test_stochastic_counts_the_draft_logits():
+    w4 = W.replace(W.BATCHED_STOCHASTIC, B=4)
+    w = w4
+    ctx = np.array([1024, 2000, 5000, 8192])
+    assert bench.step_bytes(w4, ctx, True) - bench.step_bytes(w4, ctx, False) == 2 * 4 * w.k * w.V * 4
+
+
+def test_traffic_is_reported_only_for_unchanged_sources(tmp_path, monkeypatch):
+    key = ("lm_head_gemv", "single_greedy_b1_d4096_v151936_ctx4096")
+    rec = bench.NCU_TRAFFIC[key]
+    # a recorded digest that no longer matches the source: no figure
+    monkeypatch.setitem(bench.NCU_TRAFFIC, key, {"bytes": rec["bytes"],
+                                                 "sources": {"csrc/draft.cu": "0" * 64}})
+    assert bench.ncu_traffic(*key) is None
+    assert bench.ncu_traffic("no_such_kernel", "no_such_workload") is None
