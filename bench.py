@@ -58,21 +58,21 @@ def lmhead_bytes(w, logits_out, head_rows=None):
 # are unchanged; the summaries of the captures are kept under profiles/.
 NCU_TRAFFIC = {
     ("lm_head_gemv", "single_greedy_b1_d4096_v151936_ctx4096"): {
-        "bytes": 1244773888 + 2982656,
+        "bytes": 1244772352 + 2795008,
         "sources": {
-            "csrc/draft.cu": "2d187302ba21e967a2a538b7d5f44a9876b2ebac216babfa86527f46a3cc322c",
-            "csrc/draft_ops.cuh": "3067b6cc411842aa64b55c5c50ad63b20034f1eb2bdba96dc444c1983d92c325",
+            "csrc/draft.cu": "150a1fb1a79c6dc418cd759d08e2c0af891435de9b18f00a0d5bc4c80153bcf2",
+            "csrc/draft_ops.cuh": "02838a0228cd4eba3f617c4d99cab0d8f55f1b036294cb40b43d4b3e4160ca10",
             "csrc/common.cuh": "fcd7bd8f56df32fc490b2c47f2fbc0f7f37047c578430d777438202c9279de66",
-            "csrc/internal.h": "b43fd6a70993fe8eec8ad2b42064359652d9ada36507a33922564512b9f7169a",
+            "csrc/internal.h": "36ac497104c59fe318924b19460d7557a45577223a255efc0f7534c05d38008d",
         },
     },
     ("tc_gemm_kernel(LM head)", "batched_stochastic_b64_d4096_v151936_ctx1024-8192"): {
-        "bytes": 1248019712 + 7777280,
+        "bytes": 1248436992 + 7813632,
         "sources": {
             "csrc/tc.cu": "792cfe0e73815f8f7c27b8c8f32d9d2114544f1648f6d41af10c810afcce54fc",
             "csrc/tcgen05.cuh": "e128ff6d7c8451d618848063024b7cd0a98c722dd1b86ef0d04e6a07a9070ee7",
             "csrc/common.cuh": "fcd7bd8f56df32fc490b2c47f2fbc0f7f37047c578430d777438202c9279de66",
-            "csrc/internal.h": "b43fd6a70993fe8eec8ad2b42064359652d9ada36507a33922564512b9f7169a",
+            "csrc/internal.h": "36ac497104c59fe318924b19460d7557a45577223a255efc0f7534c05d38008d",
         },
     },
     ("verify_kernel", "verify_sweep_b256_v151936_k3/greedy"): {
@@ -80,7 +80,7 @@ NCU_TRAFFIC = {
         "sources": {
             "csrc/verify.cu": "f1d0b3ef5cf32a7d7279611da02f31cfe03a82a9ebe687965352321e233997f4",
             "csrc/common.cuh": "fcd7bd8f56df32fc490b2c47f2fbc0f7f37047c578430d777438202c9279de66",
-            "csrc/internal.h": "b43fd6a70993fe8eec8ad2b42064359652d9ada36507a33922564512b9f7169a",
+            "csrc/internal.h": "36ac497104c59fe318924b19460d7557a45577223a255efc0f7534c05d38008d",
         },
     },
     ("verify_kernel", "verify_sweep_b256_v151936_k3/stochastic"): {
@@ -88,7 +88,7 @@ NCU_TRAFFIC = {
         "sources": {
             "csrc/verify.cu": "f1d0b3ef5cf32a7d7279611da02f31cfe03a82a9ebe687965352321e233997f4",
             "csrc/common.cuh": "fcd7bd8f56df32fc490b2c47f2fbc0f7f37047c578430d777438202c9279de66",
-            "csrc/internal.h": "b43fd6a70993fe8eec8ad2b42064359652d9ada36507a33922564512b9f7169a",
+            "csrc/internal.h": "36ac497104c59fe318924b19460d7557a45577223a255efc0f7534c05d38008d",
         },
     },
 }
