@@ -217,6 +217,24 @@ def cpu_oracle_step_times(workload_name, depths, n):
     return [td / depths * w.k + tv for td, tv in json.loads(r.stdout.strip().splitlines()[-1])]
 
 
+def max_over_ranks(x, device="cuda"):
+    """The largest x over the ranks of the process group (x itself without one):
+    the slowest replica's time is the job's time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(ms_per_step, world):
+    """Whole-job steps per second: each of the world replicas ran its steps
+    within ms_per_step (the maximum over ranks)."""
+    return 1e3 / ms_per_step * world
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -258,15 +276,21 @@ def verify_bytes(w):
     return rows * w.V * 4
 
 
-def run_verify_only(args, w):
-    """spec_verify on the verify sweep: B sequences, k drafts, V-wide rows."""
+def run_verify_only(args, w, rank=0, world=1):
+    """spec_verify on the verify sweep: B sequences, k drafts, V-wide rows
+    (one replica per rank; rank 0 prints the line)."""
     import torch
+    import torch.distributed as dist
     from mtp_speculative_decoding_draft_gb300 import binding as bd
     from mtp_speculative_decoding_draft_gb300.build import build
     from mtp_speculative_decoding_draft_gb300.model import Verifier, to_device
 
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
-    build()
+    if rank == 0 or world == 1:
+        build()
+    if world > 1:
+        dist.barrier()
+        build()
     inp = W.verify_inputs(w)
     # drafts: the argmax of each draft row (a deterministic stand-in for a draw
     # from q; the verifier reads every row whatever the drafts are)
@@ -282,6 +306,8 @@ def run_verify_only(args, w):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
     clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
     clocks.start()
     n0 = bd.launch_count()
@@ -292,15 +318,23 @@ def run_verify_only(args, w):
         step()
     e1.record()
     torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
     launches = bd.launch_count() - n0
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
     assert bd.get_status(ver.ws) == 0
     out, L, acc = ver.results()
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
     peak, peak_kind = measured_peaks()
     vb = verify_bytes(w)
     ach = vb / (ms * 1e-3) / 1e9
-    line = {"metric": METRIC, "value": 1e3 / ms, "unit": "verify calls/s", "n_gpus": 1, "steps": args.steps,
+    line = {"metric": METRIC, "value": job_rate(ms, world), "unit": "verify calls/s", "n_gpus": world,
+            "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32 logits", "data": "synthetic (seeded)", "config": config_of(w, args),
             "accept_len_mean": float(L.mean()),
@@ -311,6 +345,9 @@ def run_verify_only(args, w):
                          "avg_launch_ms": ms, "launches": args.steps},
             "gpu_launches": int(launches), "clocks": clk}
     print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
 
 
 def run_ours(args):
@@ -332,7 +369,7 @@ def run_ours(args):
             w = W.with_k(w, args.k)
         if args.greedy:
             w = W.replace(w, mode=W.GREEDY)
-        return run_verify_only(args, w)
+        return run_verify_only(args, w, rank, world)
     if rank == 0 or world == 1:
         build()
     if world > 1:
@@ -404,11 +441,7 @@ def run_ours(args):
         dist.barrier()
     launches = bd.launch_count() - n0
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
     assert m.status() == 0, "device status word %d" % m.status()
     L = m.accept_len.cpu().numpy()
 
@@ -459,11 +492,7 @@ def run_ours(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
 
     if rank != 0:
         if world > 1:
@@ -479,7 +508,7 @@ def run_ours(args):
         depths = min(w.k, int(ke.max()) + 1) if w.B <= 4 else w.k
     hr = args.draft_vocab or None
     sb = step_bytes(w, ctx["ctx_len"], logits_out, nm, depths, hr)
-    steps_s = 1e3 / ms * world
+    steps_s = job_rate(ms, world)
     tokens_per_step = float(L.sum())
     lm_avg = lm_ms / max(lm_n, 1)
     lm_b = lmhead_bytes(w, logits_out, hr)
@@ -502,7 +531,7 @@ def run_ours(args):
                      "bytes_per_launch": lm_b, "avg_launch_ms": lm_avg, "launches": lm_n},
         "kernel_ms_per_step": {"lm_head": lm_ms / args.steps, "verify": ver_ms / args.steps,
                                "attention": att_ms / args.steps, "gemv_other": gem_ms / args.steps},
-        "e2e": {"value": 1e3 / e2e_ms * world, "unit": "steps/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_rate(e2e_ms, world), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
         "clocks": clk,
