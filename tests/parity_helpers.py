@@ -106,3 +106,34 @@ def bf16_ulp_ok(gpu_vals, ora_vals):
         i = np.unravel_index(int(np.argmax(np.abs(g - o) - tol)), g.shape)
         print("bf16 check: gpu %r oracle %r tol %.3g row max %.3g" % (g[i], o[i], tol[i], scale))
     return not bool(np.any(bad))
+
+
+def accept_threshold_bisection(decide, B, iters=34):
+    """The u at which each sequence's accept decision at position 0 flips.
+
+    decide(u) takes float32 uniforms [B] and returns which sequences accepted
+    their first draft.  The decision is u * q(d) < p(d), so acceptance is
+    monotone in u and the flip lies at p(d) / q(d).  Returns (lo, hi): every
+    sequence accepted at lo and rejected at hi."""
+    lo = np.zeros(B, np.float32)
+    hi = np.ones(B, np.float32)
+    for _ in range(iters):
+        mid = ((lo.astype(np.float64) + hi) / 2).astype(np.float32)
+        a = np.asarray(decide(mid), bool)
+        lo = np.where(a, mid, lo)
+        hi = np.where(a, hi, mid)
+    return lo, hi
+
+
+def constant_draft_ratio_case(B, V, T, seed):
+    """Target rows, a constant draft row (q = 1/V at every id) and, per
+    sequence, a draft token d whose V * p(d) is spread over (1e-3, 0.95):
+    the flip of u * q(d) < p(d) is then V * p(d)."""
+    rng = np.random.default_rng(seed)
+    t = (rng.standard_normal((B, 2, V)) * 3.0).astype(np.float32)
+    draft = np.zeros((B, 1, V), np.float32)
+    p = np.stack([softmax_T(t[b, 0], T) for b in range(B)])
+    want = np.exp(rng.uniform(np.log(1e-3), np.log(0.95), size=B))
+    d = np.array([[int(np.argmin(np.abs(p[b] * V - want[b])))] for b in range(B)], np.int32)
+    ratio = p[np.arange(B), d[:, 0]] * V
+    return t, draft, d, ratio

@@ -8,7 +8,7 @@ from mtp_speculative_decoding_draft_gb300 import workloads as W
 from mtp_speculative_decoding_draft_gb300.model import Verifier, to_device
 from oracle.block import select_token
 from oracle.verify import spec_verify as oracle_verify
-from parity_helpers import compare_verify
+from parity_helpers import accept_threshold_bisection, compare_verify, constant_draft_ratio_case
 
 pytestmark = pytest.mark.gpu
 
@@ -152,3 +152,32 @@ def test_bad_draft_token_sets_status():
     (g_out, g_len, _), st = _run(t, None, d, None, None, GREEDY, 1.0)
     assert st & bd.STATUS_BAD_TOKEN
     assert list(g_len) == [1, 1]                    # an invalid draft is never accepted
+
+
+@pytest.mark.parametrize("V,T", [(151936, 1.0), (20011, 0.7)])
+def test_acceptance_probabilities_within_1e5_relative(V, T):
+    """The softmax probabilities the verifier decides with, read off its
+    decisions: with a constant draft row q(d) = 1/V, so u * q(d) < p(d) flips
+    at V * p(d) as the kernel computes it.  Bisection on u_accept finds that
+    point to float precision; it must lie within 1e-5 relative of the float64
+    softmax."""
+    from mtp_speculative_decoding_draft_gb300 import binding as bd
+    B = 48
+    t, draft, d, ratio = constant_draft_ratio_case(B, V, T, seed=4401)
+    ver = Verifier(B, 1, V)
+    t_d, l_d, d_d = to_device(t), to_device(draft), to_device(d)
+    uf_d = to_device(np.full(B, 0.5, np.float32))
+
+    def decide(u):
+        ver(T, STOCH, t_d, l_d, d_d, to_device(u[:, None].copy()), uf_d)
+        _, _, acc = ver.results()
+        assert bd.get_status(ver.ws) == 0
+        return acc >= 1
+
+    lo, hi = accept_threshold_bisection(decide, B)
+    got = (lo.astype(np.float64) + hi) / 2
+    rel = np.abs(got - ratio) / ratio
+    print("V=%d T=%g: V*p(d) from the decisions, max relative error %.3g (bracket %.3g)"
+          % (V, T, rel.max(), float(np.max((hi - lo) / ratio))))
+    assert np.all(rel <= 1e-5), "sequence %d: %r vs %r" % (int(np.argmax(rel)), got[np.argmax(rel)],
+                                                           ratio[np.argmax(rel)])

@@ -247,3 +247,17 @@ def test_batched_outputs_bounds_and_padding():
         for b in range(B):
             assert np.all(out[b, :L[b]] >= 0) and np.all(out[b, L[b]:] == -1)
             assert list(out[b, :a[b]]) == list(d[b, :a[b]])
+
+
+def test_accept_threshold_bisection_recovers_p_over_q():
+    """The bisection the GPU test reads the verifier's probabilities with:
+    on the oracle's own decisions it finds V * p(d) for a constant draft row."""
+    from parity_helpers import accept_threshold_bisection, constant_draft_ratio_case
+    B, V, T = 6, 997, 0.8
+    t, draft, d, ratio = constant_draft_ratio_case(B, V, T, seed=4402)
+    uf = np.full(B, 0.5, np.float32)
+    lo, hi = accept_threshold_bisection(
+        lambda u: spec_verify(t, draft, d, STOCHASTIC, T, u[:, None], uf)[2] >= 1, B)
+    assert np.all(ratio < 1.0)
+    assert np.all((lo <= ratio * (1 + 1e-7)) & (ratio <= hi * (1 + 1e-7)))
+    assert np.all((hi - lo) <= 1e-8 + 2e-7 * ratio)
