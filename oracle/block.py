@@ -193,7 +193,7 @@ def dynamic_depths(draft_logits, mode, T, stop_p):
 
 
 def mtp_draft(W, dims, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode,
-              u_draft=None, seqs=None, vocab_map=None):
+              u_draft=None, seqs=None, vocab_map=None, forced_tok=None):
     """Run the module k times in a chain and return the drafts.
 
     h        [B, d] trunk hidden states (bf16 bits or reals).
@@ -203,11 +203,15 @@ def mtp_draft(W, dims, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode,
              ctx_len[b] + j are returned in k_new / v_new.
     u_draft  [B, k] uniforms for stochastic drafting (ignored when greedy).
     seqs     optional subset of sequence indices to evaluate (all by default).
+    forced_tok  [n, k] optional (teacher forcing): depth j+1 takes
+             forced_tok[i, j] as its input token instead of this chain's own
+             choice at depth j; the hidden state stays this chain's own, and
+             draft_tok still records this chain's own choices.
     Returns a dict with draft_tok [n,k], draft_logits [n,k,V] (float32 values),
     hidden [n,k,d] (x2 of every depth), k_new / v_new [n,k,Hkv,Dh] (bf16 values).
     """
     return mtp_draft_modules([(W, k_cache, v_cache)], dims, h, last_tok, ctx_len, k, T, mode,
-                             u_draft, seqs, vocab_map)
+                             u_draft, seqs, vocab_map, forced_tok)
 
 
 def module_of_depth(j, n_modules):
@@ -220,7 +224,7 @@ def module_of_depth(j, n_modules):
 
 
 def mtp_draft_modules(modules, dims, h, last_tok, ctx_len, k, T, mode, u_draft=None, seqs=None,
-                      vocab_map=None):
+                      vocab_map=None, forced_tok=None):
     """The chain over distinct modules.
 
     modules  list of (W, k_cache, v_cache): each module's weights and its own
@@ -282,5 +286,5 @@ def mtp_draft_modules(modules, dims, h, last_tok, ctx_len, k, T, mode, u_draft=N
         out["k_new"][:, j] = k_new
         out["v_new"][:, j] = v_new
         out["module"][j] = m
-        tok = out["draft_tok"][:, j].copy()
+        tok = out["draft_tok"][:, j].copy() if forced_tok is None else np.asarray(forced_tok)[:, j].astype(np.int64)
     return out

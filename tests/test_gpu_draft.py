@@ -47,8 +47,10 @@ def run_draft_parity(w, mode, T, ctx_fix=None, master=False, seqs=None):
     g_kc = m.k_cache.view(torch.int16).cpu().numpy().view(np.uint16)
     g_vc = m.v_cache.view(torch.int16).cpu().numpy().view(np.uint16)
     seqs = list(range(B)) if seqs is None else list(seqs)
+    # teacher-forced: oracle depth j+1 takes the GPU's draft j, so every depth
+    # is compared even past an excused divergence of the tokens
     ora = oracle_draft(wts, _dims(w, k), ctx["h"], ctx["last_tok"], ctx["k_cache"], ctx["v_cache"],
-                       ctx["ctx_len"], k, T, mode, u["u_draft"], seqs)
+                       ctx["ctx_len"], k, T, mode, u["u_draft"], seqs, forced_tok=g_tok[seqs])
     report = {"excused": 0, "rel_l2": []}
     for i, b in enumerate(seqs):
         L = int(ctx["ctx_len"][b])
@@ -69,7 +71,6 @@ def run_draft_parity(w, mode, T, ctx_fix=None, master=False, seqs=None):
                     margin = cdf_margin(z, float(u["u_draft"][b, j]))
                     assert margin < 2 * err / T + 1e-6, "seq %d depth %d: sample differs, margin %.3g" % (b, j, margin)
                 report["excused"] += 1
-                break   # the chains diverge from here on
         # rows outside the appended window are untouched
         mask = np.ones(g_kc.shape[2], bool)
         mask[L:L + k] = False

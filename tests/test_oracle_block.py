@@ -236,6 +236,34 @@ def test_chain_feeds_back_hidden_and_token():
             tok = res["draft_tok"][:, j]
 
 
+def test_teacher_forcing_feeds_the_given_tokens():
+    """forced_tok replaces only the token fed to the next depth: forcing the
+    chain's own drafts reproduces it bit for bit; forcing another token at
+    depth 0 leaves depth 0 as it was and runs depth 1 on (x2 of depth 0, the
+    forced token), with the chain's own choices still recorded."""
+    w, wts, _, ctx, dims = _tiny()
+    u = W.make_uniforms(w)["u_draft"]
+    args = (wts, dims, ctx["h"], ctx["last_tok"], ctx["k_cache"], ctx["v_cache"], ctx["ctx_len"], w.k, 0.8,
+            STOCHASTIC, u)
+    free = mtp_draft(*args)
+    same = mtp_draft(*args, forced_tok=free["draft_tok"])
+    for key in ("draft_tok", "draft_logits", "hidden", "k_new", "v_new"):
+        np.testing.assert_array_equal(same[key], free[key])
+    forced = free["draft_tok"].copy()
+    forced[0, 0] = (forced[0, 0] + 1) % w.V
+    tf = mtp_draft(*args, forced_tok=forced)
+    np.testing.assert_array_equal(tf["draft_logits"][:, 0], free["draft_logits"][:, 0])
+    np.testing.assert_array_equal(tf["hidden"][:, 0], free["hidden"][:, 0])
+    L = int(ctx["ctx_len"][0])
+    keys = np.concatenate([as_f64(ctx["k_cache"][0, :, :L, :]), tf["k_new"][0, 0][:, None]], axis=1)
+    values = np.concatenate([as_f64(ctx["v_cache"][0, :, :L, :]), tf["v_new"][0, 0][:, None]], axis=1)
+    x, logits, _, _ = draft_depth(wts, dims, tf["hidden"][:, 0], forced[:, 0], [keys], [values])
+    np.testing.assert_array_equal(round_f32(logits), tf["draft_logits"][:, 1])
+    assert not np.array_equal(tf["draft_logits"][:, 1], free["draft_logits"][:, 1])
+    from oracle.block import select_token
+    assert tf["draft_tok"][0, 1] == select_token(tf["draft_logits"][0, 1], STOCHASTIC, 0.8, float(u[0, 1]))
+
+
 def test_master_and_bf16_weights_agree_within_tolerance():
     """The bf16-rounded weights the GPU uses stay within the stated 1e-2 relative
     L2 of the fp32-master evaluation on the tiny workload."""
