@@ -264,6 +264,7 @@ def config_of(w, args):
             "Dh": w.Dh, "F": w.F,
             "V": w.V, "ctx": w.ctx if not isinstance(w.ctx, tuple) else list(w.ctx),
             "mode": "greedy" if w.mode == 0 else "stochastic", "T": w.T,
+            "launch": "cuda graph replay" if getattr(args, "graph", False) else "direct calls",
             "parallelism": "replicas%d" % args.gpus, "l2": "inputs larger than L2 (weights %.2f GB re-streamed per depth)"
             % ((block_elements(w) + w.V * w.d) * 2 / 1e9)}
 
@@ -422,6 +423,30 @@ def run_ours(args):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    graph, graph_launches = None, 0
+    if args.graph:
+        # one step captured in a CUDA graph (after the warm-up above, on a side
+        # stream first, as capture wants); the timed loop replays it
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        c0 = bd.launch_count()
+        with torch.cuda.graph(graph):
+            step()
+        graph_launches = bd.launch_count() - c0
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+
+    def run_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
+
     if world > 1:
         dist.barrier()
 
@@ -434,12 +459,13 @@ def run_ours(args):
     torch.cuda.synchronize()
     e0.record(stream)
     for _ in range(args.steps):
-        step()
+        run_step()
     e1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    launches = bd.launch_count() - n0
+    # a replay launches the captured kernels without passing through the host library
+    launches = graph_launches * args.steps if graph is not None else bd.launch_count() - n0
     clk = clocks.stop()
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
     assert m.status() == 0, "device status word %d" % m.status()
@@ -565,6 +591,8 @@ def main():
                          "below this (spec_step_dynamic)")
     ap.add_argument("--draft-vocab", type=int, default=0,
                     help="reduced draft vocabulary of this many ids (spec_step_reduced); 0 = the full head")
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of one step captured in a CUDA graph instead of direct calls")
     ap.add_argument("--modules", type=int, default=1,
                     help="distinct draft modules (depth j runs module min(j, modules-1)); 1 = one reused module")
     args = ap.parse_args()
