@@ -25,6 +25,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from mtp_speculative_decoding_draft_gb300 import workloads as W  # noqa: E402
+from mtp_speculative_decoding_draft_gb300.metrics import acceptance_metrics  # noqa: E402
 
 METRIC = "spec-decode steps/s & accepted tok/s (MTP draft+verify); % of HBM roofline"
 
@@ -339,6 +340,7 @@ def run_verify_only(args, w, rank=0, world=1):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32 logits", "data": "synthetic (seeded)", "config": config_of(w, args),
             "accept_len_mean": float(L.mean()),
+            "acceptance": acceptance_metrics(L, w.k),
             "roofline": {"bound": "hbm", "kernel": "verify_kernel", "achieved": ach, "peak": peak, "unit": "GB/s",
                          "frac": ach / peak, "peak_kind": peak_kind,
                          "traffic": ncu_traffic("verify_kernel", f"{w.name}/{'greedy' if w.mode == W.GREEDY else 'stochastic'}"),
@@ -548,6 +550,7 @@ def run_ours(args):
         "config": config_of(w, args),
         "accepted_tok_s": steps_s * tokens_per_step,
         "accept_len_mean": float(L.mean()),
+        "acceptance": acceptance_metrics(L, w.k),
         "k_eff_mean": float(m.k_eff.float().mean().item()) if args.stop_p is not None else None,
         "hbm_bytes_per_step": sb,
         "hbm_roofline_frac": sb / (ms * 1e-3) / 1e9 / peak,
