@@ -218,6 +218,27 @@ def cpu_oracle_step_times(workload_name, depths, n):
     return [td / depths * w.k + tv for td, tv in json.loads(r.stdout.strip().splitlines()[-1])]
 
 
+def host_cpu():
+    """The host's CPU as /proc/cpuinfo names it (model name, else the Arm
+    implementer and part codes), with its logical core count."""
+    import platform
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read().splitlines()
+        names = [ln.split(":", 1)[1].strip() for ln in info if ln.lower().startswith("model name")]
+        if names:
+            model = names[0]
+        else:
+            impl = [ln.split(":", 1)[1].strip() for ln in info if ln.startswith("CPU implementer")]
+            part = [ln.split(":", 1)[1].strip() for ln in info if ln.startswith("CPU part")]
+            if impl and part:
+                model = "%s implementer %s part %s" % (platform.machine(), impl[0], part[0])
+    except OSError:
+        pass
+    return {"host_cores": os.cpu_count(), "cpu": model or platform.machine()}
+
+
 def max_over_ranks(x, device="cuda"):
     """The largest x over the ranks of the process group (x itself without one):
     the slowest replica's time is the job's time."""
@@ -250,7 +271,8 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(w, args),
-            "cpu_baseline": {"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": dict({"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle", "sample": sample},
+                                 **host_cpu()),
             "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -568,9 +590,9 @@ def run_ours(args):
     if not args.no_cpu_baseline and world >= 1:
         try:
             t_step = cpu_oracle_step_times(args.workload, w.k, 1)[0]
-            line["cpu_baseline"] = {"value": 1.0 / t_step, "unit": "steps/s", "cores": 1, "kind": "oracle",
-                                    "sample": "one full step (all %d depths + verification) of this workload, "
-                                              "single-threaded float64 numpy" % w.k}
+            line["cpu_baseline"] = dict({"value": 1.0 / t_step, "unit": "steps/s", "cores": 1, "kind": "oracle",
+                                         "sample": "one full step (all %d depths + verification) of this workload, "
+                                                   "single-threaded float64 numpy" % w.k}, **host_cpu())
         except Exception as e:  # report, do not hide
             line["cpu_baseline"] = {"value": None, "error": str(e)[:300]}
     print(json.dumps(line), flush=True)

@@ -72,4 +72,5 @@ def test_reference_arm_under_the_launcher_prints_one_line():
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["value"] > 0 and line["e2e"]["value"] == line["value"]
-    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["host_cores"] >= 1 and line["cpu_baseline"]["cpu"]
