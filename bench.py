@@ -282,7 +282,8 @@ def config_of(w, args):
     sp = getattr(args, "stop_p", None)
     dv = getattr(args, "draft_vocab", 0)
     name = (w.name + ("_modules%d" % mods if mods > 1 else "") + ("_stop%g" % sp if sp is not None else "")
-            + ("_draftvocab%d" % dv if dv else ""))
+            + ("_draftvocab%d" % dv if dv else "")
+            + ("_correlated%g" % args.correlated if getattr(args, "correlated", 0) > 0 and w.mode == 0 else ""))
     return {"workload": name, "modules": mods, "stop_p": sp, "draft_vocab": dv or None, "B": w.B, "k": w.k, "d": w.d, "Hq": w.Hq, "Hkv": w.Hkv,
             "Dh": w.Dh, "F": w.F,
             "V": w.V, "ctx": w.ctx if not isinstance(w.ctx, tuple) else list(w.ctx),
@@ -413,14 +414,17 @@ def run_ours(args):
     caches = [W.make_module_cache(w, i) for i in range(1, nm)]
     m = DraftModule(w, wts, extra_modules=extra)
     m.set_context(ctx, caches)
-    if w.mode == 1:
-        # target = the module's own draft logits + noise growing with position
-        m.draft(w.T, w.mode, to_device(u["u_draft"]), logits=True)
+    draft_std = None
+    if w.mode == 1 or args.correlated > 0:
+        # target = the module's own draft logits + noise (growing with position
+        # for the stochastic workloads; N(0, SIGMA^2) at every position with --correlated SIGMA)
+        m.draft(w.T, w.mode, to_device(u["u_draft"]) if stoch else None, logits=True)
         torch.cuda.synchronize()
         dl = m.draft_logits.view(w.B, w.k, w.V).cpu().numpy()
+        sd, gr = (w.draft_noise_std0, w.noise_growth) if w.mode == 1 else (args.correlated, 1.0)
+        draft_std = float(np.mean(dl.std(axis=2)))
         target = W.draft_noise(W.Workload(w.name, B=w.B, k=w.k + 1, V=w.V, seed=w.seed,
-                                          draft_noise_std0=w.draft_noise_std0, noise_growth=w.noise_growth),
-                               w.k + 1)
+                                          draft_noise_std0=sd, noise_growth=gr), w.k + 1)
         for j in range(w.k + 1):
             target[:, j] += dl[:, min(j, w.k - 1)]
         m.set_context(ctx, caches)
@@ -573,6 +577,7 @@ def run_ours(args):
         "accepted_tok_s": steps_s * tokens_per_step,
         "accept_len_mean": float(L.mean()),
         "acceptance": acceptance_metrics(L, w.k),
+        "draft_logit_std": draft_std,
         "k_eff_mean": float(m.k_eff.float().mean().item()) if args.stop_p is not None else None,
         "hbm_bytes_per_step": sb,
         "hbm_roofline_frac": sb / (ms * 1e-3) / 1e9 / peak,
@@ -616,6 +621,9 @@ def main():
                          "below this (spec_step_dynamic)")
     ap.add_argument("--draft-vocab", type=int, default=0,
                     help="reduced draft vocabulary of this many ids (spec_step_reduced); 0 = the full head")
+    ap.add_argument("--correlated", type=float, default=0.0, metavar="SIGMA",
+                    help="greedy workloads: target logits = the draft's own logits + N(0, SIGMA^2) instead of "
+                         "i.i.d. N(0, 16); 0 = off")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of one step captured in a CUDA graph instead of direct calls")
     ap.add_argument("--modules", type=int, default=1,
