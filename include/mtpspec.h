@@ -346,6 +346,18 @@ int mtp_get_status(const void *ws, mtp_stream_t stream, int32_t *status);
 /* Zero the status word (asynchronously, on the stream). */
 int mtp_clear_status(void *ws, mtp_stream_t stream);
 
+/*
+ * Diagnostics.  Runs the library's two bounded mbarrier waits (the spinning
+ * and the parked form) on a barrier phase that no thread ever completes.
+ * Each gives up after the wait limit (2 s), sets MTP_STATUS_TIMEOUT in
+ * *status and returns; the context stays usable.
+ *   status  device int32, 4-byte aligned, owned by the caller; bits are OR-ed
+ *           in, never cleared here.
+ * Asynchronous on the stream (about 2 s of GPU time).  Returns MTP_OK,
+ * MTP_ERR_INVALID_ARG (null or misaligned status) or MTP_ERR_CUDA.
+ */
+int mtp_selftest_wait_timeout(int32_t *status, mtp_stream_t stream);
+
 /* Human-readable text for an MTP_ERR_* code. */
 const char *mtp_error_string(int code);
 

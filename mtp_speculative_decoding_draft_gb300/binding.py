@@ -97,6 +97,8 @@ def _lib():
         L.mtp_get_status.restype = I
         L.mtp_clear_status.argtypes = [P, P]
         L.mtp_clear_status.restype = I
+        L.mtp_selftest_wait_timeout.argtypes = [P, P]
+        L.mtp_selftest_wait_timeout.restype = I
         L.mtp_error_string.argtypes = [I]
         L.mtp_error_string.restype = ctypes.c_char_p
         L.mtp_profiler_enable.argtypes = [I]
@@ -375,6 +377,14 @@ def clear_status(ws, stream=None):
     rc = _lib().mtp_clear_status(_ptr(ws, "ws"), _stream(stream))
     if rc != 0:
         raise MtpError(rc, "mtp_clear_status")
+
+
+def selftest_wait_timeout(status, stream=None):
+    """Run the library's bounded waits on a phase nothing completes: they give
+    up after the wait limit and OR MTP_STATUS_TIMEOUT into status (device int32)."""
+    rc = _lib().mtp_selftest_wait_timeout(_ptr(status, "status", torch.int32, 1), _stream(stream))
+    if rc != 0:
+        raise MtpError(rc, "mtp_selftest_wait_timeout")
 
 
 def profiler_enable(on=True):

@@ -67,5 +67,7 @@ def test_host_side_validation_without_gpu(lib):
                                  None) == -1
     assert L.mtp_draft_reduced(ctypes.byref(dims), None, None, None, 0, None, None, None, None, None, 3, 1.0, 0,
                                None, None, None, None, 0, None) == -1   # no weights, no map
+    assert L.mtp_selftest_wait_timeout(None, None) == -1                # no status word
+    assert L.mtp_selftest_wait_timeout(ctypes.c_void_p(2), None) == -1  # misaligned status word
     assert L.mtp_error_string(-3) == b"workspace too small"
     assert L.spec_verify_workspace_size(4, 3, 100) >= 4
