@@ -56,3 +56,14 @@ def test_traffic_is_reported_only_for_unchanged_sources(tmp_path, monkeypatch):
                                                  "sources": {"csrc/draft.cu": "0" * 64}})
     assert bench.ncu_traffic(*key) is None
     assert bench.ncu_traffic("no_such_kernel", "no_such_workload") is None
+
+
+def test_batched_and_deep_chain_step_bytes_match_the_worked_totals():
+    """The hot-path scope's worked totals per step: about 9.1 GB for the batch of
+    64 (weights 5.09 GB, K/V about 3.62 GB at the mean context of 4608, logits
+    0.39 GB) and about 28.2 GB for the deep chain (weights 16.93 GB, K/V 10.74 GB,
+    logits 0.52 GB)."""
+    b64 = W.BATCHED_STOCHASTIC
+    assert abs(bench.step_bytes(b64, np.full(b64.B, 4608), True) / 1e9 - 9.1) < 0.05
+    deep = W.WORKLOADS["deep_chain_b32_k5_d5120_v256000_ctx16384"]
+    assert abs(bench.step_bytes(deep, np.full(deep.B, 16384), True) / 1e9 - 28.2) < 0.05
