@@ -203,19 +203,60 @@ def _oracle_samples(workload_name, depths, n):
     return out
 
 
+def _verify_workload(args):
+    """The verify sweep's workload with the --k and --greedy options applied."""
+    w = W.WORKLOADS[args.workload]
+    if args.k:
+        w = W.with_k(w, args.k)
+    if args.greedy:
+        w = W.replace(w, mode=W.GREEDY)
+    return w
+
+
+def _oracle_verify_samples(workload_name, k, greedy, n, n_seq):
+    """Time the oracle's verification of the verify sweep n times on its first
+    n_seq sequences; returns seconds per call scaled to all B sequences."""
+    from oracle.verify import spec_verify
+    import argparse as _ap
+    w = _verify_workload(_ap.Namespace(workload=workload_name, k=k, greedy=greedy))
+    inp = W.verify_inputs(w)
+    d = inp["draft_logits"].argmax(axis=2).astype(np.int32)   # as the GPU arm drafts
+    s = slice(0, min(n_seq, w.B))
+    out = []
+    for _ in range(n):
+        t0 = time.perf_counter()
+        spec_verify(inp["target_logits"][s], inp["draft_logits"][s], d[s], w.mode, w.T, inp["u_accept"][s],
+                    inp["u_final"][s])
+        out.append((time.perf_counter() - t0) * w.B / (s.stop - s.start))
+    return out
+
+
+def _single_threaded(code):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=3600)
+    if r.returncode != 0:
+        raise RuntimeError("oracle timing failed: " + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_oracle_verify_times(args, n, n_seq=16):
+    """Seconds per verify-sweep call of the oracle, in a fresh single-threaded
+    process, on a sample of n_seq sequences scaled to the batch."""
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench._oracle_verify_samples(%r, %d, %r, %d, %d)))"
+            % (ROOT, args.workload, args.k, bool(args.greedy), n, n_seq))
+    return _single_threaded(code)
+
+
 def cpu_oracle_step_times(workload_name, depths, n):
     """Step times of the oracle, measured in a fresh single-threaded process
     (BLAS pinned to one thread); each sample runs `depths` draft depths and
     the verification, and is scaled to the workload's k depths."""
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
     code = ("import json,sys; sys.path.insert(0, %r); import bench; "
             "print(json.dumps(bench._oracle_samples(%r, %d, %d)))" % (ROOT, workload_name, depths, n))
-    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=3600)
-    if r.returncode != 0:
-        raise RuntimeError("oracle timing failed: " + r.stderr[-2000:])
     w = W.WORKLOADS[workload_name]
-    return [td / depths * w.k + tv for td, tv in json.loads(r.stdout.strip().splitlines()[-1])]
+    return [td / depths * w.k + tv for td, tv in _single_threaded(code)]
 
 
 def host_cpu():
@@ -262,18 +303,27 @@ def run_reference(args):
     if rank != 0:
         return
     w = W.WORKLOADS[args.workload]
-    times = cpu_oracle_step_times(args.workload, 1, args.warmup + args.steps)[args.warmup:]
+    if w.verify_only:
+        w = _verify_workload(args)
+        n_seq = 16
+        times = cpu_oracle_verify_times(args, args.warmup + args.steps, n_seq)[args.warmup:]
+        unit = "verify calls/s"
+        sample = ("per call: the oracle verifies %d of the %d sequences in a single-threaded process; "
+                  "call time = that time x %d / %d" % (min(n_seq, w.B), w.B, w.B, min(n_seq, w.B)))
+    else:
+        times = cpu_oracle_step_times(args.workload, 1, args.warmup + args.steps)[args.warmup:]
+        unit = "steps/s"
+        sample = ("per step: the oracle runs one draft depth of this workload plus its verification in a "
+                  "single-threaded process; step time = %d x depth time + verify time" % w.k)
     t = float(np.mean(times))
     value = 1.0 / t
-    sample = ("per step: the oracle runs one draft depth of this workload plus its verification in a "
-              "single-threaded process; step time = %d x depth time + verify time" % w.k)
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": args.gpus,
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(w, args),
-            "cpu_baseline": dict({"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": dict({"value": value, "unit": unit, "cores": 1, "kind": "oracle", "sample": sample},
                                  **host_cpu()),
-            "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
@@ -289,8 +339,10 @@ def config_of(w, args):
             "V": w.V, "ctx": w.ctx if not isinstance(w.ctx, tuple) else list(w.ctx),
             "mode": "greedy" if w.mode == 0 else "stochastic", "T": w.T,
             "launch": "cuda graph replay" if getattr(args, "graph", False) else "direct calls",
-            "parallelism": "replicas%d" % args.gpus, "l2": "inputs larger than L2 (weights %.2f GB re-streamed per depth)"
-            % ((block_elements(w) + w.V * w.d) * 2 / 1e9)}
+            "parallelism": "replicas%d" % args.gpus,
+            "l2": ("inputs larger than L2 (%.2f GB of logits read per call)" % (verify_bytes(w) / 1e9) if w.verify_only
+                   else "inputs larger than L2 (weights %.2f GB re-streamed per depth)"
+                   % ((block_elements(w) + w.V * w.d) * 2 / 1e9))}
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -350,6 +402,37 @@ def run_verify_only(args, w, rank=0, world=1):
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
     assert bd.get_status(ver.ws) == 0
     out, L, acc = ver.results()
+
+    # end to end: the call's inputs from pinned host memory, its outputs read back
+    stream = torch.cuda.current_stream()
+    pairs = [(torch.from_numpy(inp["target_logits"]).pin_memory(), t_d), (torch.from_numpy(d).pin_memory(), d_d)]
+    if stoch:
+        pairs += [(torch.from_numpy(inp["draft_logits"]).pin_memory(), l_d),
+                  (torch.from_numpy(inp["u_accept"]).pin_memory(), ua), (torch.from_numpy(inp["u_final"]).pin_memory(), uf)]
+    outs = [(torch.empty(t.numel(), dtype=t.dtype).pin_memory(), t)
+            for t in (ver.out_tok, ver.accept_len, ver.num_accepted)]
+    h2d = sum(h.numel() * h.element_size() for h, _ in pairs)
+    d2h = sum(h.numel() * h.element_size() for h, _ in outs)
+
+    def e2e_step():
+        for h, dv in pairs:
+            dv.copy_(h, non_blocking=True)
+        step()
+        for h, dv in outs:
+            h.copy_(dv, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    if world > 1:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    assert bd.get_status(ver.ws) == 0
     if rank != 0:
         if world > 1:
             dist.barrier()
@@ -369,7 +452,19 @@ def run_verify_only(args, w, rank=0, world=1):
                          "traffic": ncu_traffic("verify_kernel", f"{w.name}/{'greedy' if w.mode == W.GREEDY else 'stochastic'}"),
                          "bytes_per_launch": vb,
                          "avg_launch_ms": ms, "launches": args.steps},
+            "e2e": {"value": job_rate(e2e_ms, world), "unit": "verify calls/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
             "gpu_launches": int(launches), "clocks": clk}
+    if not args.no_cpu_baseline:
+        try:
+            n_seq = 16
+            t_call = cpu_oracle_verify_times(args, 1, n_seq)[0]
+            line["cpu_baseline"] = dict({"value": 1.0 / t_call, "unit": "verify calls/s", "cores": 1, "kind": "oracle",
+                                         "sample": "the oracle verifies %d of the %d sequences, single-threaded "
+                                                   "float64 numpy; scaled to the batch" % (min(n_seq, w.B), w.B)},
+                                        **host_cpu())
+        except Exception as e:  # report, do not hide
+            line["cpu_baseline"] = {"value": None, "error": str(e)[:300]}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -391,11 +486,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
     w = W.WORKLOADS[args.workload]
     if w.verify_only:
-        if args.k:
-            w = W.with_k(w, args.k)
-        if args.greedy:
-            w = W.replace(w, mode=W.GREEDY)
-        return run_verify_only(args, w, rank, world)
+        return run_verify_only(args, _verify_workload(args), rank, world)
     if rank == 0 or world == 1:
         build()
     if world > 1:
