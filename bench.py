@@ -176,8 +176,9 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- CPU oracle timing
 
-def _oracle_samples(workload_name, depths, n):
-    """Generate the workload once, then time the oracle n times on `depths`
+def _oracle_samples(workload_name, depths, n, budget_s=None):
+    """Generate the workload once, then time the oracle up to n times (fewer
+    once budget_s seconds have passed since the first, at least once) on `depths`
     draft depths plus the verification of one step; returns a list of
     (seconds for the depths, seconds for the verification)."""
     from oracle.block import Dims, mtp_draft
@@ -189,6 +190,7 @@ def _oracle_samples(workload_name, depths, n):
     tl = W.target_logits(w)
     dims = Dims(w.B, w.d, w.Hq, w.Hkv, w.Dh, w.F, w.V, w.Lmax, w.eps)
     out = []
+    start = time.perf_counter()
     for _ in range(n):
         t0 = time.perf_counter()
         dr = mtp_draft(wts, dims, ctx["h"], ctx["last_tok"], ctx["k_cache"], ctx["v_cache"], ctx["ctx_len"],
@@ -199,7 +201,10 @@ def _oracle_samples(workload_name, depths, n):
         dl = np.zeros((w.B, w.k, w.V))
         dl[:, :depths] = dr["draft_logits"]
         spec_verify(tl, dl, dt, w.mode, w.T, u["u_accept"], u["u_final"])
-        out.append((t1 - t0, time.perf_counter() - t1))
+        t2 = time.perf_counter()
+        out.append((t1 - t0, t2 - t1))
+        if budget_s is not None and t2 - start > budget_s:
+            break
     return out
 
 
@@ -213,9 +218,10 @@ def _verify_workload(args):
     return w
 
 
-def _oracle_verify_samples(workload_name, k, greedy, n, n_seq):
-    """Time the oracle's verification of the verify sweep n times on its first
-    n_seq sequences; returns seconds per call scaled to all B sequences."""
+def _oracle_verify_samples(workload_name, k, greedy, n, n_seq, budget_s=None):
+    """Time the oracle's verification of the verify sweep up to n times (fewer
+    once budget_s seconds have passed since the first, at least once) on its
+    first n_seq sequences; returns seconds per call scaled to all B sequences."""
     from oracle.verify import spec_verify
     import argparse as _ap
     w = _verify_workload(_ap.Namespace(workload=workload_name, k=k, greedy=greedy))
@@ -223,11 +229,15 @@ def _oracle_verify_samples(workload_name, k, greedy, n, n_seq):
     d = inp["draft_logits"].argmax(axis=2).astype(np.int32)   # as the GPU arm drafts
     s = slice(0, min(n_seq, w.B))
     out = []
+    start = time.perf_counter()
     for _ in range(n):
         t0 = time.perf_counter()
         spec_verify(inp["target_logits"][s], inp["draft_logits"][s], d[s], w.mode, w.T, inp["u_accept"][s],
                     inp["u_final"][s])
-        out.append((time.perf_counter() - t0) * w.B / (s.stop - s.start))
+        t1 = time.perf_counter()
+        out.append((t1 - t0) * w.B / (s.stop - s.start))
+        if budget_s is not None and t1 - start > budget_s:
+            break
     return out
 
 
@@ -240,21 +250,21 @@ def _single_threaded(code):
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
-def cpu_oracle_verify_times(args, n, n_seq=16):
+def cpu_oracle_verify_times(args, n, n_seq=16, budget_s=None):
     """Seconds per verify-sweep call of the oracle, in a fresh single-threaded
     process, on a sample of n_seq sequences scaled to the batch."""
     code = ("import json,sys; sys.path.insert(0, %r); import bench; "
-            "print(json.dumps(bench._oracle_verify_samples(%r, %d, %r, %d, %d)))"
-            % (ROOT, args.workload, args.k, bool(args.greedy), n, n_seq))
+            "print(json.dumps(bench._oracle_verify_samples(%r, %d, %r, %d, %d, %r)))"
+            % (ROOT, args.workload, args.k, bool(args.greedy), n, n_seq, budget_s))
     return _single_threaded(code)
 
 
-def cpu_oracle_step_times(workload_name, depths, n):
+def cpu_oracle_step_times(workload_name, depths, n, budget_s=None):
     """Step times of the oracle, measured in a fresh single-threaded process
     (BLAS pinned to one thread); each sample runs `depths` draft depths and
     the verification, and is scaled to the workload's k depths."""
     code = ("import json,sys; sys.path.insert(0, %r); import bench; "
-            "print(json.dumps(bench._oracle_samples(%r, %d, %d)))" % (ROOT, workload_name, depths, n))
+            "print(json.dumps(bench._oracle_samples(%r, %d, %d, %r)))" % (ROOT, workload_name, depths, n, budget_s))
     w = W.WORKLOADS[workload_name]
     return [td / depths * w.k + tv for td, tv in _single_threaded(code)]
 
@@ -298,23 +308,35 @@ def job_rate(ms_per_step, world):
     return 1e3 / ms_per_step * world
 
 
+# Wall-clock seconds the reference arm's timing loop runs at most, so that its
+# run ends within a few minutes whatever --steps asks for.
+REFERENCE_BUDGET_S = 90.0
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     w = W.WORKLOADS[args.workload]
+    n_req = args.warmup + args.steps
     if w.verify_only:
         w = _verify_workload(args)
         n_seq = 16
-        times = cpu_oracle_verify_times(args, args.warmup + args.steps, n_seq)[args.warmup:]
+        times = cpu_oracle_verify_times(args, n_req, n_seq, budget_s=REFERENCE_BUDGET_S)
         unit = "verify calls/s"
         sample = ("per call: the oracle verifies %d of the %d sequences in a single-threaded process; "
                   "call time = that time x %d / %d" % (min(n_seq, w.B), w.B, w.B, min(n_seq, w.B)))
     else:
-        times = cpu_oracle_step_times(args.workload, 1, args.warmup + args.steps)[args.warmup:]
+        times = cpu_oracle_step_times(args.workload, 1, n_req, budget_s=REFERENCE_BUDGET_S)
         unit = "steps/s"
         sample = ("per step: the oracle runs one draft depth of this workload plus its verification in a "
                   "single-threaded process; step time = %d x depth time + verify time" % w.k)
+    # warm-up samples are dropped; with the time budget fewer than the requested
+    # steps may have run (at least one is timed)
+    skip = min(args.warmup, len(times) - 1)
+    times = times[skip:]
+    sample += ("; %d timed samples (%d requested, within about %d s)"
+               % (len(times), args.steps, REFERENCE_BUDGET_S))
     t = float(np.mean(times))
     value = 1.0 / t
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,

@@ -67,3 +67,16 @@ def test_batched_and_deep_chain_step_bytes_match_the_worked_totals():
     assert abs(bench.step_bytes(b64, np.full(b64.B, 4608), True) / 1e9 - 9.1) < 0.05
     deep = W.WORKLOADS["deep_chain_b32_k5_d5120_v256000_ctx16384"]
     assert abs(bench.step_bytes(deep, np.full(deep.B, 16384), True) / 1e9 - 28.2) < 0.05
+
+
+def test_oracle_timing_stops_at_its_budget():
+    """The reference arm's oracle loop ends after its wall-clock budget, with at
+    least one timed sample, however many steps were asked for."""
+    import time
+    t0 = time.perf_counter()
+    out = bench._oracle_samples("tiny_b1_d64_v1000", 1, 10 ** 7, budget_s=0.3)
+    assert 1 <= len(out) < 10 ** 7
+    assert time.perf_counter() - t0 < 30.0
+    assert all(a > 0 and b > 0 for a, b in out)
+    one = bench._oracle_samples("tiny_b1_d64_v1000", 1, 10 ** 7, budget_s=0.0)
+    assert len(one) == 1
