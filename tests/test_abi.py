@@ -71,3 +71,33 @@ def test_host_side_validation_without_gpu(lib):
     assert L.mtp_selftest_wait_timeout(ctypes.c_void_p(2), None) == -1  # misaligned status word
     assert L.mtp_error_string(-3) == b"workspace too small"
     assert L.spec_verify_workspace_size(4, 3, 100) >= 4
+
+
+def test_variant_arguments_are_checked_on_the_host(lib):
+    """The next rows' own argument rules, before any device work: each call
+    with valid arguments gets as far as the workspace-size check (-3, no
+    workspace given); the same call with one bad value is refused (-1).
+    The pointers are never dereferenced on these paths."""
+    from mtp_speculative_decoding_draft_gb300 import binding as bd
+    L = bd.library()
+    dims = bd.make_dims(1, 256, 4, 2, 64, 768, 5003, 300)
+    w = bd.MtpWeights(*[ctypes.c_void_p(4096 * (i + 1)) for i in range(len(bd.WEIGHT_FIELDS))])
+    h, tok, kc, vc, cl, ud, dt, dl, ke = [ctypes.c_void_p(1 << (20 + i)) for i in range(9)]
+    ws = ctypes.c_void_p(1 << 30)
+
+    def dynamic(stop_p):
+        return L.mtp_draft_dynamic(ctypes.byref(dims), ctypes.byref(w), h, tok, kc, vc, cl, 3, 1.0, 1,
+                                   ctypes.c_float(stop_p), ud, dt, dl, ke, ws, 0, None)
+
+    assert dynamic(0.5) == -3 and dynamic(0.0) == -3
+    for bad in (-0.5, float("nan"), float("inf")):       # stop_p must be finite and >= 0
+        assert dynamic(bad) == -1
+
+    head, vmap = ctypes.c_void_p(1 << 26), ctypes.c_void_p(1 << 27)
+
+    def reduced(n):
+        return L.mtp_draft_reduced(ctypes.byref(dims), ctypes.byref(w), head, vmap, n, h, tok, kc, vc, cl, 3, 1.0,
+                                   1, ud, dt, dl, ws, 0, None)
+
+    assert reduced(128) == -3 and reduced(5003) == -3
+    assert reduced(127) == -1 and reduced(5004) == -1      # 128 <= N <= V
