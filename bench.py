@@ -423,7 +423,7 @@ def run_verify_only(args, w, rank=0, world=1):
     clk = clocks.stop()
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
     assert bd.get_status(ver.ws) == 0
-    out, L, acc = ver.results()
+    _, L, _ = ver.results()
 
     # end to end: the call's inputs from pinned host memory, its outputs read back
     stream = torch.cuda.current_stream()
@@ -618,9 +618,9 @@ def run_ours(args):
         step()
     torch.cuda.synchronize()
     lm_ms, lm_n = bd.profiler_read(bd.KC_LMHEAD)
-    ver_ms, ver_n = bd.profiler_read(bd.KC_VERIFY)
-    att_ms, att_n = bd.profiler_read(bd.KC_ATTN)
-    gem_ms, gem_n = bd.profiler_read(bd.KC_GEMV)
+    ver_ms, _ = bd.profiler_read(bd.KC_VERIFY)
+    att_ms, _ = bd.profiler_read(bd.KC_ATTN)
+    gem_ms, _ = bd.profiler_read(bd.KC_GEMV)
     bd.profiler_enable(False)
 
     # end to end: per-step inputs from pinned host memory, results read back
