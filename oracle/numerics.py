@@ -17,7 +17,8 @@ BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127
 def bf16_bits_to_f64(bits):
     """Widen bf16 bit patterns (uint16) to float64 exactly."""
     u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
-    return u.view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):   # signalling-NaN patterns widen to NaN
+        return u.view(np.float32).astype(np.float64)
 
 
 def round_bf16(x):
