@@ -80,3 +80,24 @@ def test_oracle_timing_stops_at_its_budget():
     assert all(a > 0 and b > 0 for a, b in out)
     one = bench._oracle_samples("tiny_b1_d64_v1000", 1, 10 ** 7, budget_s=0.0)
     assert len(one) == 1
+
+
+def test_options_parse_and_name_the_workload():
+    """Every option is accepted, and each run's config names what it ran."""
+    import argparse
+    import subprocess
+    import sys as _sys
+    r = subprocess.run([_sys.executable, os.path.join(ROOT, "bench.py"), "--help"], capture_output=True,
+                       text=True, timeout=120)
+    assert r.returncode == 0
+    for opt in ("--graph", "--correlated", "--modules", "--stop-p", "--draft-vocab", "--impl", "--greedy"):
+        assert opt in r.stdout
+    base = dict(gpus=1, modules=1, stop_p=None, draft_vocab=0, correlated=0.0, graph=False, k=0, greedy=False)
+    cfg = bench.config_of(W.SINGLE_GREEDY, argparse.Namespace(**dict(base, correlated=0.1, graph=True)))
+    assert cfg["workload"] == W.SINGLE_GREEDY.name + "_correlated0.1" and cfg["launch"] == "cuda graph replay"
+    cfg = bench.config_of(W.SINGLE_GREEDY, argparse.Namespace(**dict(base, modules=3)))
+    assert cfg["workload"].endswith("_modules3") and cfg["launch"] == "direct calls"
+    w = bench._verify_workload(argparse.Namespace(workload=W.VERIFY_SWEEP.name, k=5, greedy=True))
+    assert w.k == 5 and w.mode == W.GREEDY
+    cfg = bench.config_of(w, argparse.Namespace(**base))
+    assert "logits read per call" in cfg["l2"]
