@@ -477,7 +477,7 @@ def run_verify_only(args, w, rank=0, world=1):
             "e2e": {"value": job_rate(e2e_ms, world), "unit": "verify calls/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": int(launches), "clocks": clk}
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:   # rank 0 at N = 1 only
         try:
             n_seq = 16
             t_call = cpu_oracle_verify_times(args, 1, n_seq)[0]
@@ -705,7 +705,7 @@ def run_ours(args):
         "gpu_launches": int(launches),
         "clocks": clk,
     }
-    if not args.no_cpu_baseline and world >= 1:
+    if not args.no_cpu_baseline and world == 1:   # rank 0 at N = 1 only
         try:
             t_step = cpu_oracle_step_times(args.workload, w.k, 1)[0]
             line["cpu_baseline"] = dict({"value": 1.0 / t_step, "unit": "steps/s", "cores": 1, "kind": "oracle",
