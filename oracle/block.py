@@ -106,7 +106,7 @@ class Dims:
         self.F, self.V, self.Lmax, self.eps = F, V, Lmax, eps
 
 
-def draft_depth(W, dims, x, tok, keys, values):
+def draft_depth(W, dims, x, tok, keys, values, trace=None):
     """One application of the MTP module to a group of sequences (steps a1-a6).
 
     W       dict of weights: E [V,d], fc [d,2d], wq [Hq*Dh,d], wk/wv [Hkv*Dh,d],
@@ -116,6 +116,8 @@ def draft_depth(W, dims, x, tok, keys, values):
     tok     [n] input token ids.
     keys    list of n arrays [Hkv, T_b, Dh]: the visible cache of each sequence
             before this depth; values likewise.
+    trace   optional dict: receives "attn_in" [n, d], the attention input n
+            (the vector the Q/K/V projections multiply), for error estimates.
     Returns (x2 [n,d], logits [n,V] float64, k_new [n,Hkv,Dh], v_new [n,Hkv,Dh]);
     k_new / v_new are already rounded to bf16 (they are stored in a bf16 cache
     and the current position attends to the stored values).
@@ -128,6 +130,8 @@ def draft_depth(W, dims, x, tok, keys, values):
     x0 = linear(W["fc"], u)
 
     nrm = rmsnorm(x0, W["g_attn"], eps)
+    if trace is not None:
+        trace["attn_in"] = nrm
     q = linear(W["wq"], nrm).reshape(n, dims.Hq, dims.Dh)
     k_new = round_bf16(linear(W["wk"], nrm)).reshape(n, dims.Hkv, dims.Dh)
     v_new = round_bf16(linear(W["wv"], nrm)).reshape(n, dims.Hkv, dims.Dh)
@@ -208,7 +212,9 @@ def mtp_draft(W, dims, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode,
              choice at depth j; the hidden state stays this chain's own, and
              draft_tok still records this chain's own choices.
     Returns a dict with draft_tok [n,k], draft_logits [n,k,V] (float32 values),
-    hidden [n,k,d] (x2 of every depth), k_new / v_new [n,k,Hkv,Dh] (bf16 values).
+    hidden [n,k,d] (x2 of every depth), k_new / v_new [n,k,Hkv,Dh] (bf16 values)
+    and attn_in [n,k,d] (each depth's attention input, the vector the K/V
+    projections multiply).
     """
     return mtp_draft_modules([(W, k_cache, v_cache)], dims, h, last_tok, ctx_len, k, T, mode,
                              u_draft, seqs, vocab_map, forced_tok)
@@ -263,13 +269,16 @@ def mtp_draft_modules(modules, dims, h, last_tok, ctx_len, k, T, mode, u_draft=N
         "v_new": np.zeros((n, k, dims.Hkv, dims.Dh), dtype=np.float64),
         "module": np.zeros(k, dtype=np.int64),
         "row": np.zeros((n, k), dtype=np.int64),
+        "attn_in": np.zeros((n, k, dims.d), dtype=np.float64),
     }
     for j in range(k):
         m = module_of_depth(j, len(modules))
         W = modules[m][0]
         for i in range(n):
             out["row"][i, j] = keys[m][i].shape[1]
-        x, logits, k_new, v_new = draft_depth(W, dims, x, tok, keys[m], values[m])
+        tr = {}
+        x, logits, k_new, v_new = draft_depth(W, dims, x, tok, keys[m], values[m], trace=tr)
+        out["attn_in"][:, j] = tr["attn_in"]
         logits = round_f32(logits)
         for i, b in enumerate(seqs):
             u = None if mode == GREEDY else float(u_draft[b][j])
