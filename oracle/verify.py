@@ -103,6 +103,44 @@ def spec_verify(target_logits, draft_logits, draft_tok, mode, T=1.0,
     return out_tok, accept_len, num_accepted
 
 
+def target_logits_from_hidden(head, hidden):
+    """The target's logits at every verified position, formed from its final
+    hidden states: t[..., v] = sum_i head[v, i] * hidden[..., i], in float64.
+
+    "The Tiny Draft Model Hidden Inside Qwen", section "How the draft becomes
+    real output": the target runs once over all candidate positions and its
+    vocabulary head gives its own distribution at each of them.  head [V, d] is
+    that head (the shared embedding matrix), hidden [..., d] what the head
+    consumes at each position (the target's final hidden state after its final
+    norm); both bf16 bits or reals, widened exactly.
+
+    Parity: pinned by one-hot hidden states (a single column of the head
+    comes out, which a transposed operand would not give), by linearity, and
+    by an element-by-element loop on a small case.
+    """
+    from .block import linear
+    from .numerics import as_f64
+    return linear(head, as_f64(hidden))
+
+
+def spec_verify_fused(head, hidden, draft_logits, draft_tok, mode, T=1.0, u_accept=None, u_final=None,
+                      seqs=None):
+    """Verification from the target's hidden states instead of its logits: the
+    logits come from ``target_logits_from_hidden`` (never stored as float32)
+    and the rule is ``spec_verify``'s, unchanged.
+
+    hidden [B, k+1, d]; other arguments and the result as ``spec_verify``.
+    """
+    hidden = np.asarray(hidden)
+    B = hidden.shape[0]
+    seqs = list(range(B)) if seqs is None else list(seqs)
+    t = target_logits_from_hidden(head, hidden[seqs])
+    dl = None if draft_logits is None else np.asarray(draft_logits)[seqs]
+    ua = None if u_accept is None else np.asarray(u_accept)[seqs]
+    uf = None if u_final is None else np.asarray(u_final)[seqs]
+    return spec_verify(t, dl, np.asarray(draft_tok)[seqs], mode, T, ua, uf)
+
+
 def spec_step(W, dims, h, last_tok, k_cache, v_cache, ctx_len, k, T, mode,
               target_logits, u_draft=None, u_accept=None, u_final=None, seqs=None, stop_p=None,
               vocab_map=None):
