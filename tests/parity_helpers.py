@@ -10,19 +10,114 @@ Tolerances (stated once here, used by every GPU test):
 * draft logits: relative L2 <= 1e-2 against the float32-master oracle (the
   stated bar) and <= 1e-3 against the oracle on the same bf16 weights;
 * draft tokens: greedy identical except where the oracle's top-2 gap is below
-  1e-2; stochastic identical except where the CDF margin is below
-  2 * max|logit error| / T + 1e-6 (the largest shift the measured logit error
-  can cause); the chain is not compared past an excused divergence;
-* appended K/V rows (bf16): within one bf16 unit in the last place.
+  2 * max|logit error| (no smaller gap can be swapped by that error);
+  stochastic identical except where u * S lies within SAMPLE_BAND * S of a CDF
+  boundary of the oracle's draw, as for the verifier's draws; the chains are
+  teacher-forced, so every depth is compared past an excused divergence;
+* appended K/V rows (bf16): |gpu - oracle| <= ulp_bf16(max(|gpu|, |oracle|))
+  + KV_C * 2^-24 * sum_i |w_i n_i| for each entry (w the projection's weight
+  row, n the oracle's attention input).  Both sides round a dot product to
+  bf16: the two roundings together stay within one ulp of the larger value,
+  and the kernel's float32 value differs from the exact one by at most
+  KV_C u sum|w_i n_i| (u = 2^-24; KV_C covers the kernels' accumulation depth
+  and the float32 error the activation brings from the earlier steps).
+
+Every excused decision (a token or an accept/reject that differs inside its
+band) is recorded with its margin; ``excused_bound`` caps them per test, and
+the session writes them out (tests/conftest.py).
 """
+
+import json
+import os
 
 import numpy as np
 
+from oracle.numerics import as_f64
 from oracle.sampling import softmax_T
 from oracle.verify import residual
 
 ACCEPT_BAND = 1e-6
 SAMPLE_BAND = 1e-6
+# Allowance for a K/V entry's float32 error, in units of 2^-24 sum_i |w_i n_i|.
+# The GEMV adds a lane's 32 products in order, then 5 shuffle levels, the pieces
+# of the row (up to 8) and the norm's scale: depth <= 46, so a dot product of
+# exact operands is within 46 u sum|w n|.  The activation n carries the error of
+# the earlier float32 steps (the input projection's own dot products and the
+# norm), which random-sign roundings keep well below that; 64 covers both.
+KV_C = 64.0
+
+_RECORDS = []
+_KV_WORST = {}
+
+
+def _test_name():
+    return os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+
+
+def record_excused(kind, seq, depth, margin, band):
+    """Note one excused decision: kind ("draft_token", "verify", ...), where it
+    happened, the oracle's margin to the boundary and the band it fell inside."""
+    _RECORDS.append({"test": _test_name(), "kind": kind, "seq": int(seq), "depth": int(depth),
+                     "margin": float(margin), "band": float(band)})
+
+
+def excuse_verify(b, am, sm, band=ACCEPT_BAND):
+    """A sequence whose verification outputs differ from the oracle's is excused
+    only when the oracle's accept margin or its final draw's CDF margin is
+    inside the band; records it and returns 1."""
+    assert am < band or sm < band, "sequence %d differs (margins %.3g %.3g)" % (b, am, sm)
+    record_excused("verify", b, -1, min(am, sm), band)
+    return 1
+
+
+def excuse_draft_token(mode, b, j, gpu_logits, ora_logits, u, T):
+    """A draft token that differs from the teacher-forced oracle's at depth j
+    is excused only inside its band (module docstring); records it, returns 1."""
+    ol = np.asarray(ora_logits, np.float64)
+    if mode == 0:
+        err = float(np.max(np.abs(np.asarray(gpu_logits, np.float64) - ol)))
+        gap = top2_gap(ol)
+        assert gap < 2 * err, "seq %d depth %d: argmax differs, top-2 gap %.3g, logit error %.3g" % (b, j, gap, err)
+        record_excused("draft_argmax", b, j, gap, 2 * err)
+    else:
+        margin = cdf_margin(np.exp((ol - ol.max()) / T), float(u))
+        assert margin < SAMPLE_BAND, "seq %d depth %d: sample differs, CDF margin %.3g" % (b, j, margin)
+        record_excused("draft_sample", b, j, margin, SAMPLE_BAND)
+    return 1
+
+
+# Share of a test's decisions that may be excused.  Argmax and verification
+# decisions: 1%.  Stochastic draft samples over a large vocabulary: 10% -- at
+# V = 256000 and T = 0.7 neighbouring CDF boundaries lie about 4e-6 of the total
+# apart, so the float rounding of the logits (CDF shifts near 1e-7) flips a few
+# percent of the draws; each such draw still has to lie within SAMPLE_BAND of
+# its boundary (measured: 8 of 160 deep-chain draws, margins 1.6e-8 .. 2.2e-7).
+EXCUSED_SHARE = {"default": 0.01, "draft_sample": 0.10}
+
+
+def excused_bound(n_decisions, kind="default"):
+    """Most excused decisions a test may have among n_decisions (at least one):
+    a systematic shift of the kernels' decisions would exceed it."""
+    return max(1, int(np.floor(EXCUSED_SHARE.get(kind, EXCUSED_SHARE["default"]) * n_decisions)))
+
+
+def check_excused(n_excused, n_decisions, what="", kind="default"):
+    bound = excused_bound(n_decisions, kind)
+    _RECORDS.append({"test": _test_name(), "kind": "summary", "what": what, "decisions": int(n_decisions),
+                     "excused": int(n_excused), "bound": int(bound)})
+    assert n_excused <= bound, "%s: %d of %d decisions excused (bound %d)" % (what, n_excused, n_decisions, bound)
+
+
+def write_report(path):
+    """Write the collected records as JSON (nothing if none were collected)."""
+    if not _RECORDS and not _KV_WORST:
+        return None
+    d = os.path.dirname(path)
+    if d:
+        os.makedirs(d, exist_ok=True)
+    with open(path, "w") as f:
+        json.dump({"kv_error_ratio_worst": _KV_WORST, "records": _RECORDS}, f, indent=1)
+    return path
 
 
 def stochastic_path_margins(target, draft, d, ua, uf, T):
@@ -75,6 +170,7 @@ def compare_verify(gpu, ora, mode, target=None, draft=None, d=None, ua=None, uf=
         assert am < ACCEPT_BAND or sm < SAMPLE_BAND, (
             "sequence %d differs: gpu %s/%d oracle %s/%d (margins %.3g, %.3g)"
             % (b, g_out[b], g_len[b], o_out[b], o_len[b], am, sm))
+        record_excused("verify", b, int(o_len[b]) - 1, min(am, sm), ACCEPT_BAND)
         excused += 1
     return excused
 
@@ -90,21 +186,40 @@ def top2_gap(z):
     return float(z[-1] - z[-2]) if z.size > 1 else np.inf
 
 
-def bf16_ulp_ok(gpu_vals, ora_vals):
-    """Every value within one bf16 ulp (relative spacing 2^-7 of the larger
-    magnitude), or, for a value near zero, within 2^-12 of the row's largest
-    magnitude: the values are float32 dot products (absolute error about
-    2^-24 of the sum of the terms' magnitudes) rounded to bf16, so an entry
-    that cancels to near zero can land past its own ulp.  Prints the worst
-    entry when the check fails."""
+def bf16_ulp(x):
+    """Spacing of bf16 values at |x|: 2^(floor(log2|x|) - 7) for normal
+    numbers, 2^-133 below the smallest normal."""
+    ax = np.abs(np.asarray(x, np.float64))
+    _, e = np.frexp(ax)
+    return np.where(ax >= 2.0 ** -126, np.ldexp(1.0, e - 8), 2.0 ** -133)
+
+
+def kv_sum_abs(W, attn_in):
+    """sum_i |w_i n_i| for every K and V entry a depth appends: attn_in [n, d]
+    the oracle's attention input, W the module's weights.  Returns (mk, mv),
+    each [n, Hkv, Dh]-shaped as the rows ([n, Hkv*Dh] flattened)."""
+    a = np.abs(np.asarray(attn_in, np.float64))
+    return a @ np.abs(as_f64(W["wk"])).T, a @ np.abs(as_f64(W["wv"])).T
+
+
+def bf16_ulp_ok(gpu_vals, ora_vals, sum_abs, c=KV_C):
+    """Every value within ulp_bf16(max(|gpu|, |oracle|)) + c 2^-24 sum_abs (see
+    the module docstring).  Records the worst ratio of the float32 part
+    (|gpu - oracle| - ulp) / (2^-24 sum_abs) per test; prints the worst entry
+    when the check fails."""
     g = np.asarray(gpu_vals, np.float64)
     o = np.asarray(ora_vals, np.float64)
-    scale = float(np.max(np.abs(o))) if o.size else 0.0
-    tol = np.maximum(np.abs(g), np.abs(o)) * 2.0 ** -7 + 2.0 ** -12 * scale + 1e-30
-    bad = np.abs(g - o) > tol
+    m = np.asarray(sum_abs, np.float64).reshape(g.shape)
+    ulp = bf16_ulp(np.maximum(np.abs(g), np.abs(o)))
+    unit = 2.0 ** -24 * m + 1e-300
+    ratio = (np.abs(g - o) - ulp) / unit
+    worst = float(np.max(ratio)) if ratio.size else 0.0
+    t = _test_name()
+    _KV_WORST[t] = max(_KV_WORST.get(t, -np.inf), worst)
+    bad = ratio > c
     if np.any(bad):
-        i = np.unravel_index(int(np.argmax(np.abs(g - o) - tol)), g.shape)
-        print("bf16 check: gpu %r oracle %r tol %.3g row max %.3g" % (g[i], o[i], tol[i], scale))
+        i = np.unravel_index(int(np.argmax(ratio)), g.shape)
+        print("bf16 check: gpu %r oracle %r ulp %.3g sum|w n| %.3g ratio %.3g" % (g[i], o[i], ulp[i], m[i], ratio[i]))
     return not bool(np.any(bad))
 
 

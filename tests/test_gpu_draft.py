@@ -8,7 +8,7 @@ from mtp_speculative_decoding_draft_gb300 import workloads as W
 from mtp_speculative_decoding_draft_gb300.model import DraftModule, to_device
 from oracle.block import Dims, mtp_draft as oracle_draft
 from oracle.numerics import bf16_bits_to_f64
-from parity_helpers import bf16_ulp_ok, cdf_margin, rel_l2, top2_gap
+from parity_helpers import bf16_ulp_ok, check_excused, excuse_draft_token, kv_sum_abs, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -41,6 +41,7 @@ def run_draft_parity(w, mode, T, ctx_fix=None, master=False, seqs=None):
     m.draft(T, mode, to_device(u["u_draft"]) if mode == STOCH else None, logits=True)
     torch.cuda.synchronize()
     assert m.status() == 0
+    m.check_canaries()
     B, k, V = w.B, w.k, w.V
     g_tok = m.draft_tok.view(B, k).cpu().numpy()
     g_log = m.draft_logits.view(B, k, V).cpu().numpy()
@@ -52,6 +53,8 @@ def run_draft_parity(w, mode, T, ctx_fix=None, master=False, seqs=None):
     ora = oracle_draft(wts, _dims(w, k), ctx["h"], ctx["last_tok"], ctx["k_cache"], ctx["v_cache"],
                        ctx["ctx_len"], k, T, mode, u["u_draft"], seqs, forced_tok=g_tok[seqs])
     report = {"excused": 0, "rel_l2": []}
+    # sum_i |w_i n_i| of every appended K/V entry, per depth
+    mags = [kv_sum_abs(wts, ora["attn_in"][:, j]) for j in range(k)]
     for i, b in enumerate(seqs):
         L = int(ctx["ctx_len"][b])
         for j in range(k):
@@ -60,22 +63,18 @@ def run_draft_parity(w, mode, T, ctx_fix=None, master=False, seqs=None):
             report["rel_l2"].append(e)
             assert e <= 1e-3, "seq %d depth %d: logits rel L2 %.3g" % (b, j, e)
             # the rows this depth appended to the caches
-            assert bf16_ulp_ok(bf16_bits_to_f64(g_kc[b, :, L + j, :]), ora["k_new"][i, j])
-            assert bf16_ulp_ok(bf16_bits_to_f64(g_vc[b, :, L + j, :]), ora["v_new"][i, j])
+            assert bf16_ulp_ok(bf16_bits_to_f64(g_kc[b, :, L + j, :]), ora["k_new"][i, j], mags[j][0][i]), \
+                "seq %d depth %d: K row" % (b, j)
+            assert bf16_ulp_ok(bf16_bits_to_f64(g_vc[b, :, L + j, :]), ora["v_new"][i, j], mags[j][1][i]), \
+                "seq %d depth %d: V row" % (b, j)
             if g_tok[b, j] != ora["draft_tok"][i, j]:
-                if mode == GREEDY:
-                    assert top2_gap(ol) < 1e-2, "seq %d depth %d: argmax differs, gap %.3g" % (b, j, top2_gap(ol))
-                else:
-                    err = float(np.max(np.abs(g_log[b, j] - ol)))
-                    z = np.exp((ol - ol.max()) / T)
-                    margin = cdf_margin(z, float(u["u_draft"][b, j]))
-                    assert margin < 2 * err / T + 1e-6, "seq %d depth %d: sample differs, margin %.3g" % (b, j, margin)
-                report["excused"] += 1
+                report["excused"] += excuse_draft_token(mode, b, j, g_log[b, j], ol, u["u_draft"][b, j], T)
         # rows outside the appended window are untouched
         mask = np.ones(g_kc.shape[2], bool)
         mask[L:L + k] = False
         assert np.array_equal(g_kc[b][:, mask], ctx["k_cache"][b][:, mask])
         assert np.array_equal(g_vc[b][:, mask], ctx["v_cache"][b][:, mask])
+    check_excused(report["excused"], len(seqs) * k, "draft tokens", "draft_sample" if mode == STOCH else "default")
     if master:
         om = oracle_draft(full, _dims(w, k), ctx["h"], ctx["last_tok"], ctx["k_cache"], ctx["v_cache"],
                           ctx["ctx_len"], 1, T, mode, u["u_draft"], seqs)

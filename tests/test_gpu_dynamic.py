@@ -12,7 +12,7 @@ from mtp_speculative_decoding_draft_gb300 import workloads as W
 from mtp_speculative_decoding_draft_gb300.model import DraftModule, to_device
 from oracle.block import Dims, draft_confidence, dynamic_depths, mtp_draft as oracle_draft
 from oracle.verify import spec_verify as oracle_verify
-from parity_helpers import cdf_margin, rel_l2, stochastic_path_margins, top2_gap
+from parity_helpers import check_excused, excuse_draft_token, excuse_verify, rel_l2, stochastic_path_margins
 
 pytestmark = pytest.mark.gpu
 
@@ -61,21 +61,20 @@ def _check_kept(w, mode, wts, ctx, u, stop_p, g_keff, g_log, g_tok, seqs):
     ora = oracle_draft(wts, _dims(w), ctx["h"], ctx["last_tok"], ctx["k_cache"], ctx["v_cache"],
                        ctx["ctx_len"], w.k, w.T, mode, u["u_draft"], seqs, forced_tok=forced)
     o_keff = dynamic_depths(ora["draft_logits"], mode, w.T, stop_p)
+    excused, n_tok = 0, 0
     for i, b in enumerate(seqs):
         upto = min(int(o_keff[i]), w.k - 1)
         for j in range(upto + 1):
             ol = ora["draft_logits"][i, j]
             assert rel_l2(g_log[b, j], ol) <= 1e-3, "seq %d depth %d" % (b, j)
+            n_tok += j < upto
             if j < upto and g_tok[b, j] != ora["draft_tok"][i, j]:
-                if mode == GREEDY:
-                    assert top2_gap(ol) < 1e-2
-                else:
-                    err = float(np.max(np.abs(g_log[b, j] - ol)))
-                    assert cdf_margin(np.exp((ol - ol.max()) / w.T), float(u["u_draft"][b, j])) < 2 * err / w.T + 1e-6
+                excused += excuse_draft_token(mode, b, j, g_log[b, j], ol, u["u_draft"][b, j], w.T)
         if g_keff[b] != o_keff[i]:
             conf = [draft_confidence(ora["draft_logits"][i, j], mode, w.T) for j in range(upto + 1)]
             near = min(abs(c / stop_p - 1.0) for c in conf)
             assert near < 1e-3, "seq %d: k_eff %d, oracle %d" % (b, g_keff[b], o_keff[i])
+    check_excused(excused, max(n_tok, 1), "draft tokens", "draft_sample" if mode == STOCH else "default")
     return o_keff
 
 
@@ -162,6 +161,7 @@ def test_verify_dynamic(mode):
         g_len = alen.cpu().numpy()
         o_out, o_len, o_acc = oracle_verify(t, dl, d, mode, w.T, inp["u_accept"], inp["u_final"], k_eff=ke)
         assert np.all(g_len <= ke + 1) and np.array_equal(nacc.cpu().numpy(), g_len - 1)
+        n_exc = 0
         for b in range(w.B):
             if np.array_equal(g_out[b], o_out[b]) and g_len[b] == o_len[b]:
                 continue
@@ -169,7 +169,8 @@ def test_verify_dynamic(mode):
             kb = int(ke[b])
             am, sm = stochastic_path_margins(t[b, :kb + 1], dl[b, :kb], d[b, :kb], inp["u_accept"][b, :kb],
                                              float(inp["u_final"][b]), w.T)
-            assert am < 1e-6 or sm < 1e-6, "sequence %d differs (margins %.3g %.3g)" % (b, am, sm)
+            n_exc += excuse_verify(b, am, sm)
+        check_excused(n_exc, w.B, "verify outputs")
 
 
 @pytest.mark.parametrize("mode", [GREEDY, STOCH])
@@ -204,6 +205,7 @@ def test_step_dynamic(mode):
     assert np.all((g_len >= 1) & (g_len <= g_keff + 1))
     o_out, o_len, _ = oracle_verify(target, g_log.astype(np.float64), g_tok, mode, w.T, u["u_accept"], u["u_final"],
                                     k_eff=g_keff)
+    n_exc = 0
     for b in seqs:
         if np.array_equal(g_out[b], o_out[b]) and g_len[b] == o_len[b]:
             continue
@@ -211,4 +213,5 @@ def test_step_dynamic(mode):
         kb = int(g_keff[b])
         am, sm = stochastic_path_margins(target[b, :kb + 1], g_log[b, :kb].astype(np.float64), g_tok[b, :kb],
                                          u["u_accept"][b, :kb], float(u["u_final"][b]), w.T)
-        assert am < 1e-6 or sm < 1e-6, "sequence %d differs (margins %.3g %.3g)" % (b, am, sm)
+        n_exc += excuse_verify(b, am, sm)
+    check_excused(n_exc, len(seqs), "verify outputs")

@@ -9,11 +9,12 @@ import torch
 
 from mtp_speculative_decoding_draft_gb300 import binding as bd
 from mtp_speculative_decoding_draft_gb300 import workloads as W
-from mtp_speculative_decoding_draft_gb300.model import to_device, to_device_bf16
+from mtp_speculative_decoding_draft_gb300.model import Guarded, to_device, to_device_bf16
 from oracle.block import Dims, mtp_draft_modules as oracle_draft_modules
 from oracle.numerics import bf16_bits_to_f64
 from oracle.verify import spec_verify as oracle_verify
-from parity_helpers import bf16_ulp_ok, cdf_margin, rel_l2, stochastic_path_margins, top2_gap
+from parity_helpers import (bf16_ulp_ok, check_excused, excuse_draft_token, excuse_verify, kv_sum_abs, rel_l2,
+                            stochastic_path_margins)
 
 pytestmark = pytest.mark.gpu
 
@@ -49,13 +50,14 @@ class Modules:
                              to_device_bf16(vc)))
         self.arr = bd.make_modules(self.dev)
         self.dims = bd.make_dims(w.B, w.d, w.Hq, w.Hkv, w.Dh, w.F, w.V, w.Lmax, w.eps)
-        self.ws = bd.alloc_workspace(bd.workspace_size(self.dims, w.k))
+        self.guard = Guarded()
+        self.ws = self.guard.alloc("workspace", bd.workspace_size(self.dims, w.k), torch.uint8)
         self.h = to_device_bf16(self.ctx["h"])
         self.last_tok = to_device(self.ctx["last_tok"].astype(np.int32))
         self.ctx_len = to_device(self.ctx["ctx_len"].astype(np.int32))
         B, k, V = w.B, w.k, w.V
-        self.draft_tok = torch.zeros(B * k, dtype=torch.int32, device="cuda")
-        self.draft_logits = torch.zeros(B * k * V, dtype=torch.float32, device="cuda")
+        self.draft_tok = self.guard.alloc("draft_tok", B * k, torch.int32)
+        self.draft_logits = self.guard.alloc("draft_logits", B * k * V, torch.float32)
 
     def caches(self):
         return [(kc.view(torch.int16).cpu().numpy().view(np.uint16), vc.view(torch.int16).cpu().numpy().view(np.uint16))
@@ -71,12 +73,16 @@ def check_draft(M, ora, mode, T, u, seqs):
     j+1 takes the GPU's draft j), so every depth is compared."""
     w = M.w
     B, k, V = w.B, w.k, w.V
+    torch.cuda.synchronize()
+    M.guard.check()
     g_tok = M.draft_tok.view(B, k).cpu().numpy()
     g_log = M.draft_logits.view(B, k, V).cpu().numpy()
     caches = M.caches()
     n_mod = len(M.host)
     written = [np.zeros((B, w.Lmax), bool) for _ in range(n_mod)]
     excused = 0
+    # sum_i |w_i n_i| of every appended K/V entry, per depth (that depth's module)
+    mags = [kv_sum_abs(M.host[int(ora["module"][j])][0], ora["attn_in"][:, j]) for j in range(k)]
     for i, b in enumerate(seqs):
         for j in range(k):
             m = int(ora["module"][j])
@@ -85,16 +91,10 @@ def check_draft(M, ora, mode, T, u, seqs):
             ol = ora["draft_logits"][i, j]
             assert rel_l2(g_log[b, j], ol) <= 1e-3, "seq %d depth %d" % (b, j)
             gk, gv = caches[m]
-            assert bf16_ulp_ok(bf16_bits_to_f64(gk[b, :, row, :]), ora["k_new"][i, j])
-            assert bf16_ulp_ok(bf16_bits_to_f64(gv[b, :, row, :]), ora["v_new"][i, j])
+            assert bf16_ulp_ok(bf16_bits_to_f64(gk[b, :, row, :]), ora["k_new"][i, j], mags[j][0][i]), (b, j)
+            assert bf16_ulp_ok(bf16_bits_to_f64(gv[b, :, row, :]), ora["v_new"][i, j], mags[j][1][i]), (b, j)
             if g_tok[b, j] != ora["draft_tok"][i, j]:
-                if mode == GREEDY:
-                    assert top2_gap(ol) < 1e-2
-                else:
-                    err = float(np.max(np.abs(g_log[b, j] - ol)))
-                    margin = cdf_margin(np.exp((ol - ol.max()) / T), float(u[b, j]))
-                    assert margin < 2 * err / T + 1e-6
-                excused += 1
+                excused += excuse_draft_token(mode, b, j, g_log[b, j], ol, u[b, j], T)
     # every row no depth wrote is untouched, in every module's cache
     for m in range(n_mod):
         gk, gv = caches[m]
@@ -103,6 +103,7 @@ def check_draft(M, ora, mode, T, u, seqs):
             keep = ~written[m][b]
             assert np.array_equal(gk[b][:, keep], kc[b][:, keep]), "module %d seq %d" % (m, b)
             assert np.array_equal(gv[b][:, keep], vc[b][:, keep]), "module %d seq %d" % (m, b)
+    check_excused(excused, len(seqs) * k, "draft tokens", "draft_sample" if mode == STOCH else "default")
     return excused
 
 
@@ -152,9 +153,9 @@ def test_spec_step_modules_stochastic():
     for b in seqs:
         for j in range(k + 1):
             target[b, j] += ora["draft_logits"][b, min(j, k - 1)].astype(np.float32)
-    out_tok = torch.zeros(B * (k + 1), dtype=torch.int32, device="cuda")
-    alen = torch.zeros(B, dtype=torch.int32, device="cuda")
-    nacc = torch.zeros(B, dtype=torch.int32, device="cuda")
+    out_tok = M.guard.alloc("out_tok", B * (k + 1), torch.int32)
+    alen = M.guard.alloc("accept_len", B, torch.int32)
+    nacc = M.guard.alloc("num_accepted", B, torch.int32)
     bd.spec_step_modules(M.dims, M.arr, M.h, M.last_tok, M.ctx_len, k, w.T, STOCH, to_device(uu["u_draft"]),
                          to_device(target), to_device(uu["u_accept"]), to_device(uu["u_final"]), M.draft_tok,
                          M.draft_logits, out_tok, alen, nacc, M.ws)
@@ -171,9 +172,11 @@ def test_spec_step_modules_stochastic():
     # verification of the GPU's own drafts, re-done by the oracle
     o_out, o_len, _ = oracle_verify(target, g_log.astype(np.float64), g_tok, STOCH, w.T, uu["u_accept"],
                                     uu["u_final"])
+    n_exc = 0
     for b in seqs:
         if np.array_equal(g_out[b], o_out[b]) and g_len[b] == o_len[b]:
             continue
         am, sm = stochastic_path_margins(target[b], g_log[b].astype(np.float64), g_tok[b], uu["u_accept"][b],
                                          float(uu["u_final"][b]), w.T)
-        assert am < 1e-6 or sm < 1e-6, "sequence %d: outputs differ (margins %.3g %.3g)" % (b, am, sm)
+        n_exc += excuse_verify(b, am, sm)
+    check_excused(n_exc, len(seqs), "verify outputs")

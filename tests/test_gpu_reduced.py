@@ -13,7 +13,8 @@ from mtp_speculative_decoding_draft_gb300.model import DraftModule, to_device, t
 from oracle.block import Dims, mtp_draft as oracle_draft
 from oracle.numerics import bf16_bits_to_f64
 from oracle.verify import spec_verify as oracle_verify
-from parity_helpers import bf16_ulp_ok, cdf_margin, rel_l2, stochastic_path_margins, top2_gap
+from parity_helpers import (bf16_ulp_ok, check_excused, excuse_draft_token, excuse_verify, kv_sum_abs, rel_l2,
+                            stochastic_path_margins)
 
 pytestmark = pytest.mark.gpu
 
@@ -61,6 +62,8 @@ def test_draft_reduced(w, mode):
     outside = np.ones(V, bool)
     outside[vmap] = False
     ids = set(vmap.tolist())
+    mags = [kv_sum_abs(wts, ora["attn_in"][:, j]) for j in range(k)]
+    excused = 0
     for i, b in enumerate(seqs):
         L = int(ctx["ctx_len"][b])
         for j in range(k):
@@ -68,13 +71,10 @@ def test_draft_reduced(w, mode):
             ol = ora["draft_logits"][i, j][vmap]
             assert rel_l2(g_log[b, j][vmap], ol) <= 1e-3, "seq %d depth %d" % (b, j)
             assert int(g_tok[b, j]) in ids
-            assert bf16_ulp_ok(bf16_bits_to_f64(g_kc[b, :, L + j, :]), ora["k_new"][i, j])
+            assert bf16_ulp_ok(bf16_bits_to_f64(g_kc[b, :, L + j, :]), ora["k_new"][i, j], mags[j][0][i]), (b, j)
             if g_tok[b, j] != ora["draft_tok"][i, j]:
-                if mode == GREEDY:
-                    assert top2_gap(ol) < 1e-2
-                else:
-                    err = float(np.max(np.abs(g_log[b, j][vmap] - ol)))
-                    assert cdf_margin(np.exp((ol - ol.max()) / w.T), float(u["u_draft"][b, j])) < 2 * err / w.T + 1e-6
+                excused += excuse_draft_token(mode, b, j, g_log[b, j][vmap], ol, u["u_draft"][b, j], w.T)
+    check_excused(excused, len(seqs) * k, "draft tokens", "draft_sample" if mode == STOCH else "default")
 
 
 @pytest.mark.parametrize("w", [RED, RED_TC], ids=["gemv", "tensor_core"])
@@ -123,13 +123,15 @@ def test_step_reduced(mode):
     g_out = m.out_tok.view(B, k + 1).cpu().numpy()
     g_len = m.accept_len.cpu().numpy()
     o_out, o_len, _ = oracle_verify(target, g_log, g_tok, mode, w.T, u["u_accept"], u["u_final"])
+    n_exc = 0
     for b in range(B):
         if np.array_equal(g_out[b], o_out[b]) and g_len[b] == o_len[b]:
             continue
         assert mode == STOCH, "greedy sequence %d differs" % b
         am, sm = stochastic_path_margins(target[b], g_log[b], g_tok[b], u["u_accept"][b], float(u["u_final"][b]),
                                          w.T)
-        assert am < 1e-6 or sm < 1e-6, "sequence %d differs (margins %.3g %.3g)" % (b, am, sm)
+        n_exc += excuse_verify(b, am, sm)
+    check_excused(n_exc, B, "verify outputs")
 
 
 def test_bad_map_ids_flag_the_status():
