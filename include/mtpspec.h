@@ -152,14 +152,20 @@ int mtp_draft(const MtpDims *dims, const MtpWeights *w, const void *h,
  * Arguments and results as mtp_draft, except:
  *   status  optional device int32: if not NULL, the status word (MTP_STATUS_*
  *           bits) of this call is copied there, on the stream, after the chain.
- * Limits: mtp_workspace_size(dims, k) must not exceed MTP_STATIC_SCRATCH_BYTES
- * (else MTP_ERR_SCRATCH_LIMIT, nothing launched).  The first call on a device
- * does that device's set-up (it loads the library's device image and looks up
- * the scratch array's address), so make it before any stream capture.  Each
- * call zeroes the scratch's status word and counters on the stream before the
- * chain.  There is one scratch array per device: calls that overlap in time on
- * the same device (two streams, or two host threads) race on it and must be
- * serialised by the caller.
+ * Limits: the call keeps no logits and no verifier state in its scratch, so it
+ * needs mtp_workspace_size(dims, k) less those two regions: the activations,
+ * the LM-head partials and, for batches of 5 or more, the tensor-core buffers.
+ * That must not exceed MTP_STATIC_SCRATCH_BYTES (else MTP_ERR_SCRATCH_LIMIT,
+ * nothing launched).  At d = 4096, V = 151936 and F = 12288 a batch of up to 4
+ * sequences fits (about 0.17 MB per sequence); at d = 256 batches of 3 fit at
+ * any vocabulary size.  The first call on a device does that device's set-up
+ * (it loads the library's device image and looks up the scratch array's
+ * address), so make it before any stream capture; the lookup is made again
+ * when the device's context has changed (after cudaDeviceReset, for one).
+ * Each call zeroes the scratch's status word and counters on the stream
+ * before the chain.  There is one scratch array per device: calls that
+ * overlap in time on the same device (two streams, or two host threads) race
+ * on it and must be serialised by the caller.
  */
 #define MTP_STATIC_SCRATCH_BYTES ((size_t)4 << 20)
 int mtp_draft_noalloc(const MtpDims *dims, const MtpWeights *w, const void *h,

@@ -6,6 +6,8 @@
 #include <mutex>
 #include <vector>
 
+#include <cuda.h>
+
 #include "internal.h"
 #include "mtpspec.h"
 
@@ -13,6 +15,37 @@ namespace mtp {
 
 static std::atomic<long long> g_launches{0};
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+// The unique id of the calling thread's current CUDA context (0 when there is
+// none, or the driver cannot say).  Per-device state that belongs to a context
+// -- a device address inside this module, the kernels' attributes -- is keyed
+// on it, so that a context created anew after cudaDeviceReset is set up again
+// instead of being handed addresses of the old one.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+unsigned long long context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 namespace {
 
@@ -23,6 +56,7 @@ size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct DevInfo {
   bool init = false;
+  unsigned long long ctx = 0;  // context the attributes were set in
   int sms = 0;
   int max_cluster = 8;
 };
@@ -34,11 +68,13 @@ int device_info(DevInfo *out) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MTP_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
   DevInfo &di = g_dev[dev];
-  if (!di.init) {
+  const unsigned long long cid = context_id();
+  if (!di.init || cid == 0 || cid != di.ctx) {
     if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MTP_ERR_CUDA;
     di.max_cluster = 16;  // the non-portable size; the automatic choice stays at 8 or less
     if (verify_set_attributes() != cudaSuccess) return MTP_ERR_CUDA;
     if (tc_set_attributes() != cudaSuccess) return MTP_ERR_CUDA;
+    di.ctx = context_id();  // set up (made current) by the calls above
     di.init = true;
   }
   *out = di;
@@ -69,7 +105,10 @@ struct WsLayout {
 
 MtpShape shape_of(const MtpDims &d) { return MtpShape{d.B, d.d, d.Hq, d.Hkv, d.Dh, d.F, d.V}; }
 
-WsLayout draft_layout(const MtpDims &d, int k) {
+// draft_only: the layout of a draft-only call that keeps no logits in its
+// workspace and runs no verification (mtp_draft_noalloc's scratch): the logits
+// and verifier-state regions are left out.
+WsLayout draft_layout(const MtpDims &d, int k, bool draft_only = false) {
   WsLayout L{};
   size_t off = 0;
   L.status = off;
@@ -91,9 +130,9 @@ WsLayout draft_layout(const MtpDims &d, int k) {
   L.lm_part = off;
   off += up((size_t)d.B * kMaxLmGrid * 4 * 4);
   L.logits = off;
-  off += up((size_t)d.B * k * d.V * 4);
+  if (!draft_only) off += up((size_t)d.B * k * d.V * 4);
   L.vstate = off;
-  off += up(verify_state_bytes(d.B, k, d.V));
+  if (!draft_only) off += up(verify_state_bytes(d.B, k, d.V));
   L.tc = tc_shape_ok(shape_of(d));
   if (L.tc) {
     L.tz = tc_sizes(shape_of(d));
@@ -176,7 +215,7 @@ struct DraftOpts {
 int prepare_draft(const MtpDims *dims, const MtpModule *mods, int nmod, const void *h, const int32_t *last_tok,
                   const int32_t *ctx_len, int k, float T, int mode, const float *u_draft, int32_t *draft_tok,
                   float *draft_logits, void *ws, size_t ws_bytes, bool logits_in_ws, const DraftOpts &o,
-                  Draft *out) {
+                  Draft *out, bool draft_only = false) {
   int rc = check_dims(dims, k);
   if (rc) return rc;
   if (o.k_eff && (!aligned16(o.k_eff) || !(o.stop_p >= 0.f && o.stop_p < 1e30f))) return MTP_ERR_INVALID_ARG;
@@ -199,7 +238,8 @@ int prepare_draft(const MtpDims *dims, const MtpModule *mods, int nmod, const vo
   if (mode == MTP_STOCHASTIC && !logits_in_ws && !aligned16(draft_logits)) return MTP_ERR_INVALID_ARG;
   if (draft_logits && !aligned16(draft_logits)) return MTP_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MTP_ERR_INVALID_ARG;
-  const WsLayout L = draft_layout(*dims, k);
+  if (draft_only && logits_in_ws) return MTP_ERR_INVALID_ARG;
+  const WsLayout L = draft_layout(*dims, k, draft_only);
   if (ws_bytes < L.total) return MTP_ERR_WORKSPACE;
   DevInfo di;
   if ((rc = device_info(&di))) return rc;
@@ -332,24 +372,30 @@ __device__ __align__(256) unsigned char g_static_scratch[MTP_STATIC_SCRATCH_BYTE
 
 struct ScratchSlot {
   bool init = false;
+  unsigned long long ctx = 0;  // context the address belongs to
   void *ptr = nullptr;
 };
 ScratchSlot g_scratch_slot[64];
 
-// The device address of g_static_scratch on the current device, looked up once
-// per device (with that device current).
+// The device address of g_static_scratch on the current device, looked up
+// once per device and context (with that device current): after
+// cudaDeviceReset the next call runs in a new context, where the module may
+// sit at another address, so the lookup is made again.
 int static_scratch(void **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MTP_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
   ScratchSlot &sl = g_scratch_slot[dev];
-  if (!sl.init) {
+  const unsigned long long cid = context_id();
+  if (!sl.init || cid == 0 || cid != sl.ctx) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) {
       cudaGetLastError();
+      sl.init = false;
       return MTP_ERR_CUDA;
     }
     sl.ptr = p;
+    sl.ctx = context_id();  // made current by the lookup if there was none
     sl.init = true;
   }
   *out = sl.ptr;
@@ -436,7 +482,7 @@ int mtp_draft_noalloc(const MtpDims *dims, const MtpWeights *w, const void *h, c
                       mtp_stream_t stream) {
   int rc = check_dims(dims, k);
   if (rc) return rc;
-  if (draft_layout(*dims, k).total > MTP_STATIC_SCRATCH_BYTES) return MTP_ERR_SCRATCH_LIMIT;
+  if (draft_layout(*dims, k, true).total > MTP_STATIC_SCRATCH_BYTES) return MTP_ERR_SCRATCH_LIMIT;
   if (status && (reinterpret_cast<uintptr_t>(status) & 3u) != 0) return MTP_ERR_INVALID_ARG;
   if (!w) return MTP_ERR_INVALID_ARG;
   void *scratch = nullptr;
@@ -444,7 +490,7 @@ int mtp_draft_noalloc(const MtpDims *dims, const MtpWeights *w, const void *h, c
   const MtpModule one{*w, k_cache, v_cache};
   Draft D;
   rc = prepare_draft(dims, &one, 1, h, last_tok, ctx_len, k, T, mode, u_draft, draft_tok, draft_logits, scratch,
-                     MTP_STATIC_SCRATCH_BYTES, false, DraftOpts{}, &D);
+                     MTP_STATIC_SCRATCH_BYTES, false, DraftOpts{}, &D, true);
   if (rc) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the status word and the LM-head ticket counter (the first two aligned

@@ -369,13 +369,14 @@ MapCache g_maps;
 template <int DH>
 cudaError_t launch_tc(const DraftCtx &c, int cluster, cudaStream_t s, bool pdl) {
   using Ly = TcLayout<DH>;
-  static bool attr_done = false;
+  static unsigned long long attr_ctx = 0;  // the context the attributes were set in
   auto kern = attn_tc_kernel<DH>;
-  if (!attr_done) {
+  const unsigned long long cid = context_id();
+  if (cid == 0 || cid != attr_ctx) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Ly::SMEM);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    attr_ctx = cid;
   }
   AttnTcArgs a;
   {

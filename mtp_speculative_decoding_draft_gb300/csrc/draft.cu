@@ -347,11 +347,12 @@ GemvPlan plan_gemv(int op, int N, int K, int B, int num_sms) {
 template <int OP, int NV, int BG>
 static cudaError_t launch_one(const DraftCtx &c, const GemvPlan &g, cudaStream_t s, bool pdl) {
   auto kern = gemv_kernel<OP, NV, BG>;
-  static bool attr_done = false;  // per process; all devices share the limit
-  if (!attr_done) {
+  static unsigned long long attr_ctx = 0;  // the context the attribute was set in
+  const unsigned long long cid = context_id();
+  if (cid == 0 || cid != attr_ctx) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    attr_ctx = cid;
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(g.grid);
@@ -733,13 +734,14 @@ int attention_cluster_size(int ctx_max, int pairs, int num_sms, int max_cluster,
 template <int DH, int GM>
 static cudaError_t launch_attn(const DraftCtx &c, int cluster, cudaStream_t s, bool pdl) {
   auto kern = attn_kernel<DH, GM>;
-  static bool attr_done = false;
+  static unsigned long long attr_ctx = 0;  // the context the attributes were set in
   const size_t smem = attention_smem_bytes(DH);
-  if (!attr_done) {
+  const unsigned long long cid = context_id();
+  if (cid == 0 || cid != attr_ctx) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    attr_ctx = cid;
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(cluster, c.Hkv, c.B);

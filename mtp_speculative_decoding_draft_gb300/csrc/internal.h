@@ -148,5 +148,8 @@ cudaError_t verify_set_attributes();
 
 // bookkeeping shared with api.cu
 void note_launch();
+// Unique id of the calling thread's current CUDA context (0 if there is none):
+// kernel attributes and device addresses are set up again when it changes.
+unsigned long long context_id();
 
 }  // namespace mtp

@@ -19,6 +19,43 @@ def to_device(x, device="cuda"):
     return torch.from_numpy(np.ascontiguousarray(x)).to(device)
 
 
+CANARY_BYTES = 4096
+CANARY_BYTE = 0xA5
+
+
+class Guarded:
+    """Device buffers with CANARY_BYTES of a fixed byte pattern on both sides.
+
+    alloc() returns the usable (zeroed, contiguous) middle part; check() raises
+    if any kernel wrote into a guard band.  The middle starts CANARY_BYTES past
+    the allocation, so it keeps the allocation's 256-byte alignment."""
+
+    def __init__(self, device="cuda"):
+        self.device = device
+        self.bufs = []
+
+    def alloc(self, name, numel, dtype):
+        es = torch.empty(0, dtype=dtype).element_size()
+        pad = CANARY_BYTES // es
+        buf = torch.empty(int(numel) + 2 * pad, dtype=dtype, device=self.device)
+        buf.view(torch.uint8).fill_(CANARY_BYTE)
+        mid = buf[pad:pad + int(numel)]
+        mid.zero_()
+        self.bufs.append((name, buf, pad, int(numel)))
+        return mid
+
+    def check(self):
+        for name, buf, pad, n in self.bufs:
+            raw = buf.view(torch.uint8)
+            nb = pad * buf.element_size()
+            head = raw[:nb]
+            tail = raw[raw.numel() - nb:]
+            bad_h = int((head != CANARY_BYTE).sum().item())
+            bad_t = int((tail != CANARY_BYTE).sum().item())
+            if bad_h or bad_t:
+                raise AssertionError("%s: %d bytes written before and %d after the buffer" % (name, bad_h, bad_t))
+
+
 class DraftModule:
     """The MTP module's weights on the device plus the per-step buffers.
 
@@ -40,13 +77,16 @@ class DraftModule:
         self.mods = None
         self.dims = bd.make_dims(w.B, w.d, w.Hq, w.Hkv, w.Dh, w.F, w.V, w.ctx_max + self.k, w.eps)
         self.wptr = bd.make_weights(self.weights)
-        self.ws = bd.alloc_workspace(bd.workspace_size(self.dims, self.k), device)
+        # outputs and workspace inside canary bands (check_canaries)
+        self.guard = Guarded(device)
+        g = self.guard
+        self.ws = g.alloc("workspace", max(256, bd.workspace_size(self.dims, self.k)), torch.uint8)
         B, k, V = w.B, self.k, w.V
-        self.draft_tok = torch.zeros(B * k, dtype=torch.int32, device=device)
-        self.draft_logits = torch.zeros(B * k * V, dtype=torch.float32, device=device)
-        self.out_tok = torch.zeros(B * (k + 1), dtype=torch.int32, device=device)
-        self.accept_len = torch.zeros(B, dtype=torch.int32, device=device)
-        self.num_accepted = torch.zeros(B, dtype=torch.int32, device=device)
+        self.draft_tok = g.alloc("draft_tok", B * k, torch.int32)
+        self.draft_logits = g.alloc("draft_logits", B * k * V, torch.float32)
+        self.out_tok = g.alloc("out_tok", B * (k + 1), torch.int32)
+        self.accept_len = g.alloc("accept_len", B, torch.int32)
+        self.num_accepted = g.alloc("num_accepted", B, torch.int32)
 
     def set_context(self, ctx, extra_caches=()):
         """Upload h, last_tok, ctx_len and the K/V caches (numpy from workloads);
@@ -89,7 +129,7 @@ class DraftModule:
                      logits=True, stream=None):
         """spec_step with the dynamic draft length; self.k_eff receives the drafts kept."""
         if not hasattr(self, "k_eff"):
-            self.k_eff = torch.zeros(self.w.B, dtype=torch.int32, device=self.device)
+            self.k_eff = self.guard.alloc("k_eff", self.w.B, torch.int32)
         bd.spec_step_dynamic(self.dims, self.wptr, self.h, self.last_tok, self.k_cache, self.v_cache,
                              self.ctx_len, self.k, T, mode, stop_p, u_draft, target_logits, u_accept, u_final,
                              self.draft_tok, self.draft_logits if logits else None, self.k_eff, self.out_tok,
@@ -110,22 +150,33 @@ class DraftModule:
     def status(self, stream=None):
         return bd.get_status(self.ws, stream)
 
+    def check_canaries(self):
+        """Raise if any call wrote outside an output or the workspace."""
+        torch.cuda.synchronize()
+        self.guard.check()
+
 
 class Verifier:
     """Buffers for spec_verify on B sequences of depth k over V tokens."""
 
     def __init__(self, B, k, V, device="cuda"):
         self.B, self.k, self.V = B, k, V
-        self.ws = bd.alloc_workspace(bd.verify_workspace_size(B, k, V), device)
-        self.out_tok = torch.zeros(B * (k + 1), dtype=torch.int32, device=device)
-        self.accept_len = torch.zeros(B, dtype=torch.int32, device=device)
-        self.num_accepted = torch.zeros(B, dtype=torch.int32, device=device)
+        self.guard = Guarded(device)
+        g = self.guard
+        self.ws = g.alloc("workspace", max(256, bd.verify_workspace_size(B, k, V)), torch.uint8)
+        self.out_tok = g.alloc("out_tok", B * (k + 1), torch.int32)
+        self.accept_len = g.alloc("accept_len", B, torch.int32)
+        self.num_accepted = g.alloc("num_accepted", B, torch.int32)
 
     def __call__(self, T, mode, target_logits, draft_logits, draft_tok, u_accept=None, u_final=None,
                  stream=None):
         bd.spec_verify(self.B, self.k, self.V, T, mode, target_logits, draft_logits, draft_tok,
                        u_accept, u_final, self.out_tok, self.accept_len, self.num_accepted, self.ws,
                        stream)
+
+    def check_canaries(self):
+        torch.cuda.synchronize()
+        self.guard.check()
 
     def results(self):
         torch.cuda.synchronize()
