@@ -222,12 +222,17 @@ def _oracle_verify_samples(workload_name, k, greedy, n, n_seq, budget_s=None):
     """Time the oracle's verification of the verify sweep up to n times (fewer
     once budget_s seconds have passed since the first, at least once) on its
     first n_seq sequences; returns seconds per call scaled to all B sequences."""
+    from oracle.block import STOCHASTIC, select_token
     from oracle.verify import spec_verify
     import argparse as _ap
     w = _verify_workload(_ap.Namespace(workload=workload_name, k=k, greedy=greedy))
     inp = W.verify_inputs(w)
-    d = inp["draft_logits"].argmax(axis=2).astype(np.int32)   # as the GPU arm drafts
     s = slice(0, min(n_seq, w.B))
+    # drafts drawn from q at u_draft, as the GPU arm draws them
+    d = np.zeros((w.B, w.k), np.int32)
+    for b in range(s.start, s.stop):
+        for j in range(w.k):
+            d[b, j] = select_token(inp["draft_logits"][b, j], STOCHASTIC, w.T, float(inp["u_draft"][b, j]))
     out = []
     start = time.perf_counter()
     for _ in range(n):
@@ -262,7 +267,8 @@ def cpu_oracle_verify_times(args, n, n_seq=16, budget_s=None):
 def cpu_oracle_step_times(workload_name, depths, n, budget_s=None):
     """Step times of the oracle, measured in a fresh single-threaded process
     (BLAS pinned to one thread); each sample runs `depths` draft depths and
-    the verification, and is scaled to the workload's k depths."""
+    the verification, and is scaled to the workload's k depths (a full step
+    when depths = k)."""
     code = ("import json,sys; sys.path.insert(0, %r); import bench; "
             "print(json.dumps(bench._oracle_samples(%r, %d, %d, %r)))" % (ROOT, workload_name, depths, n, budget_s))
     w = W.WORKLOADS[workload_name]
@@ -311,6 +317,10 @@ def job_rate(ms_per_step, world):
 # Wall-clock seconds the reference arm's timing loop runs at most, so that its
 # run ends within a few minutes whatever --steps asks for.
 REFERENCE_BUDGET_S = 90.0
+# The GPU arm's CPU baseline: the median of this many full oracle steps, fewer
+# if they take longer than the budget (at least one).
+CPU_BASELINE_STEPS = 10
+CPU_BASELINE_BUDGET_S = 45
 
 
 def run_reference(args):
@@ -327,10 +337,10 @@ def run_reference(args):
         sample = ("per call: the oracle verifies %d of the %d sequences in a single-threaded process; "
                   "call time = that time x %d / %d" % (min(n_seq, w.B), w.B, w.B, min(n_seq, w.B)))
     else:
-        times = cpu_oracle_step_times(args.workload, 1, n_req, budget_s=REFERENCE_BUDGET_S)
+        times = cpu_oracle_step_times(args.workload, w.k, n_req, budget_s=REFERENCE_BUDGET_S)
         unit = "steps/s"
-        sample = ("per step: the oracle runs one draft depth of this workload plus its verification in a "
-                  "single-threaded process; step time = %d x depth time + verify time" % w.k)
+        sample = ("per step: the oracle runs one full step of this workload (all %d draft depths and the "
+                  "verification) in a single-threaded process" % w.k)
     # warm-up samples are dropped; with the time budget fewer than the requested
     # steps may have run (at least one is timed)
     skip = min(args.warmup, len(times) - 1)
@@ -369,6 +379,22 @@ def config_of(w, args):
 
 # ----------------------------------------------------------------------------- GPU arm
 
+def drafts_from_q(draft_logits, u_draft, T):
+    """Draft tokens drawn from q = softmax(draft / T) at u_draft by the inverse
+    CDF (the smallest i whose running sum exceeds u times the total), on the
+    device in float64: the verify sweep's drafts, sampled as a drafter samples
+    them.  draft_logits [B, k, V] and u_draft [B, k] are CUDA tensors; returns
+    int32 [B, k].  (Input preparation, outside the timed region.)"""
+    import torch
+    z = draft_logits.double() / T
+    z = z - z.amax(dim=-1, keepdim=True)
+    C = torch.cumsum(torch.exp(z), dim=-1)
+    del z
+    t = u_draft.double().unsqueeze(-1) * C[..., -1:]
+    idx = torch.searchsorted(C, t, right=True).squeeze(-1)
+    return idx.clamp_(max=draft_logits.shape[-1] - 1).to(torch.int32).contiguous()
+
+
 def verify_bytes(w):
     """Algorithmic bytes of one spec_verify: every logit row read once."""
     rows = w.B * (w.k + 1) + (w.B * w.k if w.mode == 1 else 0)
@@ -391,10 +417,10 @@ def run_verify_only(args, w, rank=0, world=1):
         dist.barrier()
         build()
     inp = W.verify_inputs(w)
-    # drafts: the argmax of each draft row (a deterministic stand-in for a draw
-    # from q; the verifier reads every row whatever the drafts are)
-    d = inp["draft_logits"].argmax(axis=2).astype(np.int32)
-    t_d, l_d, d_d = to_device(inp["target_logits"]), to_device(inp["draft_logits"]), to_device(d)
+    t_d, l_d = to_device(inp["target_logits"]), to_device(inp["draft_logits"])
+    # drafts drawn from q at u_draft (the rejection rate the config states)
+    d_d = drafts_from_q(l_d.view(w.B, w.k, w.V), to_device(inp["u_draft"]), w.T)
+    d = d_d.cpu().numpy()
     ua, uf = to_device(inp["u_accept"]), to_device(inp["u_final"])
     ver = Verifier(w.B, w.k, w.V)
     stoch = w.mode == 1
@@ -491,6 +517,133 @@ def run_verify_only(args, w, rank=0, world=1):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- secondary workloads
+
+SECONDARY_STEPS = 50
+
+
+def _targets_from_own_draft(m, w, u, sd, growth):
+    """Target logits = the module's own (untimed) draft logits + noise whose std
+    is sd at position 0 and grows by `growth` per position; the bonus row reuses
+    the last draft row.  Returns (target [B, k+1, V] float32, mean draft-logit std)."""
+    import torch
+    from mtp_speculative_decoding_draft_gb300.model import to_device
+    stoch = w.mode == 1
+    m.draft(w.T, w.mode, to_device(u["u_draft"]) if stoch else None, logits=True)
+    torch.cuda.synchronize()
+    dl = m.draft_logits.view(w.B, w.k, w.V).cpu().numpy()
+    target = W.draft_noise(W.Workload(w.name, B=w.B, k=w.k + 1, V=w.V, seed=w.seed,
+                                      draft_noise_std0=sd, noise_growth=growth), w.k + 1)
+    for j in range(w.k + 1):
+        target[:, j] += dl[:, min(j, w.k - 1)]
+    return target, float(np.mean(dl.std(axis=2)))
+
+
+def secondary_step(w, steps, warmup, peak):
+    """spec_step on another workload (direct calls, inputs resident), CUDA-event
+    timed with its own clock samples: steps/s, ms and the fraction of the step's
+    HBM roofline."""
+    import torch
+    from mtp_speculative_decoding_draft_gb300 import binding as bd
+    from mtp_speculative_decoding_draft_gb300.model import DraftModule, to_device
+    wts = W.make_weights(w)
+    ctx = W.make_context(w)
+    u = W.make_uniforms(w)
+    m = DraftModule(w, wts)
+    m.set_context(ctx)
+    target, _ = _targets_from_own_draft(m, w, u, w.draft_noise_std0, w.noise_growth)
+    m.set_context(ctx)
+    stoch = w.mode == 1
+    td = to_device(target)
+    ud, ua, uf = (to_device(u[n]) if stoch else None for n in ("u_draft", "u_accept", "u_final"))
+
+    def step():
+        m.step(w.T, w.mode, td, ud, ua, uf, logits=stoch)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / steps
+    assert m.status() == 0, "device status word %d" % m.status()
+    L = m.accept_len.cpu().numpy()
+    sb = step_bytes(w, ctx["ctx_len"], stoch)
+    out = {"workload": w.name, "value": 1e3 / ms, "unit": "steps/s", "ms_per_step": ms, "steps": steps,
+           "warmup": warmup, "accepted_tok_s": 1e3 / ms * float(L.sum()), "accept_len_mean": float(L.mean()),
+           "hbm_bytes_per_step": sb, "hbm_roofline_frac": sb / (ms * 1e-3) / 1e9 / peak, "clocks": clk}
+    del m, td
+    torch.cuda.empty_cache()
+    return out
+
+
+def secondary_verify(k, greedy, steps, warmup, peak):
+    """spec_verify on the verify sweep at depth k (drafts drawn from q), CUDA-event
+    timed with its own clock samples: ms per call and the fraction of the copy
+    peak on the algorithmic bytes."""
+    import torch
+    from mtp_speculative_decoding_draft_gb300 import binding as bd
+    from mtp_speculative_decoding_draft_gb300.model import Verifier, to_device
+    w = W.with_k(W.VERIFY_SWEEP, k)
+    if greedy:
+        w = W.replace(w, mode=W.GREEDY)
+    inp = W.verify_inputs(w)
+    t_d, l_d = to_device(inp["target_logits"]), to_device(inp["draft_logits"])
+    d_d = drafts_from_q(l_d.view(w.B, w.k, w.V), to_device(inp["u_draft"]), w.T)
+    ua, uf = to_device(inp["u_accept"]), to_device(inp["u_final"])
+    ver = Verifier(w.B, w.k, w.V)
+    stoch = w.mode == 1
+
+    def call():
+        ver(w.T, w.mode, t_d, l_d if stoch else None, d_d, ua if stoch else None, uf if stoch else None)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / steps
+    assert bd.get_status(ver.ws) == 0
+    _, L, _ = ver.results()
+    vb = verify_bytes(w)
+    out = {"workload": "%s/%s" % (w.name, "greedy" if greedy else "stochastic"), "ms_per_call": ms,
+           "calls_s": 1e3 / ms, "steps": steps, "warmup": warmup, "bytes_per_call": vb,
+           "achieved_gbs": vb / (ms * 1e-3) / 1e9, "frac": vb / (ms * 1e-3) / 1e9 / peak,
+           "accept_len_mean": float(L.mean()), "drafts": "drawn from q at u_draft", "clocks": clk}
+    del ver, t_d, l_d
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_secondary(peak, steps=SECONDARY_STEPS, warmup=5):
+    """The batched stochastic workload's step and the verify sweep at k = 3
+    (greedy and stochastic), each timed in this process; failures are reported
+    in place of the figures."""
+    out = {}
+    for key, fn in (("batched_stochastic_step", lambda: secondary_step(W.BATCHED_STOCHASTIC, steps, warmup, peak)),
+                    ("verify_sweep_k3_greedy", lambda: secondary_verify(3, True, 4 * steps, warmup, peak)),
+                    ("verify_sweep_k3_stochastic", lambda: secondary_verify(3, False, 4 * steps, warmup, peak))):
+        try:
+            out[key] = fn()
+        except Exception as e:  # report, do not hide
+            out[key] = {"error": str(e)[:300]}
+    return out
 
 
 def run_ours(args):
@@ -705,12 +858,20 @@ def run_ours(args):
         "gpu_launches": int(launches),
         "clocks": clk,
     }
+    if not args.no_secondary and world == 1 and args.workload == W.SINGLE_GREEDY.name and not (
+            args.graph or args.stop_p is not None or args.draft_vocab or nm > 1 or args.correlated):
+        line["secondary"] = run_secondary(peak)
     if not args.no_cpu_baseline and world == 1:   # rank 0 at N = 1 only
         try:
-            t_step = cpu_oracle_step_times(args.workload, w.k, 1)[0]
+            ts = cpu_oracle_step_times(args.workload, w.k, CPU_BASELINE_STEPS, budget_s=CPU_BASELINE_BUDGET_S)
+            t_step = float(np.median(ts))
             line["cpu_baseline"] = dict({"value": 1.0 / t_step, "unit": "steps/s", "cores": 1, "kind": "oracle",
-                                         "sample": "one full step (all %d depths + verification) of this workload, "
-                                                   "single-threaded float64 numpy" % w.k}, **host_cpu())
+                                         "steps_timed": len(ts), "step_s_min": float(min(ts)),
+                                         "step_s_max": float(max(ts)),
+                                         "sample": "median of %d full steps (all %d depths + verification) of this "
+                                                   "workload, single-threaded float64 numpy (up to %d steps within "
+                                                   "%d s)" % (len(ts), w.k, CPU_BASELINE_STEPS, CPU_BASELINE_BUDGET_S)},
+                                        **host_cpu())
         except Exception as e:  # report, do not hide
             line["cpu_baseline"] = {"value": None, "error": str(e)[:300]}
     print(json.dumps(line), flush=True)
@@ -727,6 +888,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=W.SINGLE_GREEDY.name, choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the batched-stochastic step and verify-sweep figures added to the default line")
     ap.add_argument("--k", type=int, default=0, help="draft depth for the verify sweep (1..5)")
     ap.add_argument("--greedy", action="store_true", help="greedy verification for the verify sweep")
     ap.add_argument("--stop-p", type=float, default=None,
