@@ -345,6 +345,44 @@ int spec_step_reduced(const MtpDims *dims, const MtpWeights *w,
                       int32_t *out_tok, int32_t *accept_len, int32_t *num_accepted,
                       void *ws, size_t ws_bytes, mtp_stream_t stream);
 
+/*
+ * Verification from the target's hidden states.  [P4] "How the draft becomes
+ * real output": the target runs once over every candidate position and its
+ * own vocabulary head gives its distribution at each of them.  This call
+ * takes what that head consumes -- the target's final hidden state after its
+ * final norm, one row per position -- together with the head itself, and
+ * forms the target logits t = head . h inside the verification (bf16
+ * operands, fp32 accumulation on the tensor cores), so that the [B, k+1, V]
+ * logits never have to be written by one kernel and read back by another.
+ * The decisions are spec_verify's, same rule, same uniforms.
+ *
+ *   d             hidden width (multiple of 8)
+ *   head          [V, d] bf16: the target's vocabulary head (with the pages'
+ *                 shared head, the embedding matrix E of MtpWeights)
+ *   target_hidden [B, k+1, d] bf16: row (b, j) is the head's input at
+ *                 position j of sequence b (after the context and the first j
+ *                 drafts)
+ *   draft_logits, draft_tok, u_accept, u_final, out_tok, accept_len,
+ *   num_accepted  as spec_verify (the draft logits, u_accept and u_final may
+ *                 be NULL when greedy)
+ *   ws, ws_bytes  workspace of at least spec_verify_fused_workspace_size()
+ *                 bytes, 256-byte aligned; its first word is the status word
+ *                 (mtp_get_status).  Greedy keeps only per-(row, 256-token
+ *                 tile) partials there; stochastic also keeps the target's
+ *                 fp32 logits, since its one residual draw per sequence needs
+ *                 every element of the first rejecting row.
+ * Returns MTP_OK or MTP_ERR_*.  A draft token outside [0, V) is never
+ * accepted and sets MTP_STATUS_BAD_TOKEN.
+ */
+size_t spec_verify_fused_workspace_size(int B, int k, int V, int d, int mode);
+
+int spec_verify_fused(int B, int k, int V, int d, float T, int mode,
+                      const void *head, const void *target_hidden,
+                      const float *draft_logits, const int32_t *draft_tok,
+                      const float *u_accept, const float *u_final,
+                      int32_t *out_tok, int32_t *accept_len, int32_t *num_accepted,
+                      void *ws, size_t ws_bytes, mtp_stream_t stream);
+
 /* Wait for the stream, then copy the workspace's status word (MTP_STATUS_* bits)
  * to *status.  Returns MTP_OK or MTP_ERR_*. */
 int mtp_get_status(const void *ws, mtp_stream_t stream, int32_t *status);

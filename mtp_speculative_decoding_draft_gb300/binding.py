@@ -93,6 +93,10 @@ def _lib():
         L.spec_step_reduced.argtypes = [ctypes.POINTER(MtpDims), ctypes.POINTER(MtpWeights), P, P, I, P, P, P, P,
                                         P, I, F, I, P, P, P, P, P, P, P, P, P, P, Z, P]
         L.spec_step_reduced.restype = I
+        L.spec_verify_fused_workspace_size.argtypes = [I, I, I, I, I]
+        L.spec_verify_fused_workspace_size.restype = Z
+        L.spec_verify_fused.argtypes = [I, I, I, I, F, I, P, P, P, P, P, P, P, P, P, P, Z, P]
+        L.spec_verify_fused.restype = I
         L.mtp_get_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
         L.mtp_get_status.restype = I
         L.mtp_clear_status.argtypes = [P, P]
@@ -363,6 +367,28 @@ def spec_step_reduced(dims, weights, head_rows, vocab_map, h, last_tok, k_cache,
         _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
     if rc != 0:
         raise MtpError(rc, "spec_step_reduced")
+
+
+def fused_workspace_size(B, k, V, d, mode):
+    return int(_lib().spec_verify_fused_workspace_size(int(B), int(k), int(V), int(d), int(mode)))
+
+
+def spec_verify_fused(B, k, V, d, T, mode, head, target_hidden, draft_logits, draft_tok, u_accept, u_final,
+                      out_tok, accept_len, num_accepted, ws, stream=None):
+    """spec_verify from the target's hidden states: head [V, d] bf16 (the
+    target's vocabulary head) and target_hidden [B, k+1, d] bf16 (what the head
+    consumes at each position) instead of target logits."""
+    rc = _lib().spec_verify_fused(
+        int(B), int(k), int(V), int(d), float(T), int(mode), _ptr(head, "head", torch.bfloat16, V * d),
+        _ptr(target_hidden, "target_hidden", torch.bfloat16, B * (k + 1) * d),
+        _ptr(draft_logits, "draft_logits", torch.float32, B * k * V),
+        _ptr(draft_tok, "draft_tok", torch.int32, B * k),
+        _ptr(u_accept, "u_accept", torch.float32, B * k), _ptr(u_final, "u_final", torch.float32, B),
+        _ptr(out_tok, "out_tok", torch.int32, B * (k + 1)), _ptr(accept_len, "accept_len", torch.int32, B),
+        _ptr(num_accepted, "num_accepted", torch.int32, B),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
+    if rc != 0:
+        raise MtpError(rc, "spec_verify_fused")
 
 
 def get_status(ws, stream=None):

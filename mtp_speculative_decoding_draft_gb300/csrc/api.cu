@@ -74,6 +74,7 @@ int device_info(DevInfo *out) {
     di.max_cluster = 16;  // the non-portable size; the automatic choice stays at 8 or less
     if (verify_set_attributes() != cudaSuccess) return MTP_ERR_CUDA;
     if (tc_set_attributes() != cudaSuccess) return MTP_ERR_CUDA;
+    if (fused_set_attributes() != cudaSuccess) return MTP_ERR_CUDA;
     di.ctx = context_id();  // set up (made current) by the calls above
     di.init = true;
   }
@@ -607,6 +608,41 @@ int spec_step(const MtpDims *dims, const MtpWeights *w, const void *h, const int
   const MtpModule one{*w, k_cache, v_cache};
   return spec_step_modules(dims, &one, 1, h, last_tok, ctx_len, k, T, mode, u_draft, target_logits, u_accept,
                            u_final, draft_tok, draft_logits, out_tok, accept_len, num_accepted, ws, ws_bytes, stream);
+}
+
+size_t spec_verify_fused_workspace_size(int B, int k, int V, int d, int mode) {
+  if (!fused_shape_ok(B, k, V, d) || (mode != MTP_GREEDY && mode != MTP_STOCHASTIC)) return 0;
+  return fused_workspace_bytes(B, k, V, d, mode);
+}
+
+int spec_verify_fused(int B, int k, int V, int d, float T, int mode, const void *head, const void *target_hidden,
+                      const float *draft_logits, const int32_t *draft_tok, const float *u_accept,
+                      const float *u_final, int32_t *out_tok, int32_t *accept_len, int32_t *num_accepted, void *ws,
+                      size_t ws_bytes, mtp_stream_t stream) {
+  if (!fused_shape_ok(B, k, V, d)) return MTP_ERR_INVALID_ARG;
+  if (mode != MTP_GREEDY && mode != MTP_STOCHASTIC) return MTP_ERR_INVALID_ARG;
+  if (mode == MTP_STOCHASTIC && !(T > 0.f && T < 1e30f)) return MTP_ERR_INVALID_ARG;
+  const void *ptrs[] = {head, target_hidden, draft_tok, out_tok, accept_len, num_accepted, ws};
+  for (const void *p : ptrs)
+    if (!aligned16(p)) return MTP_ERR_INVALID_ARG;
+  if (mode == MTP_STOCHASTIC && (!aligned16(draft_logits) || !aligned16(u_accept) || !aligned16(u_final)))
+    return MTP_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MTP_ERR_INVALID_ARG;
+  if (ws_bytes < fused_workspace_bytes(B, k, V, d, mode)) return MTP_ERR_WORKSPACE;
+  if (!tc_available()) return MTP_ERR_CUDA;
+  DevInfo di;
+  int rc = device_info(&di);
+  if (rc) return rc;
+  FusedCall fc{};
+  fc.B = B; fc.k = k; fc.V = V; fc.d = d; fc.mode = mode; fc.T = T;
+  fc.head = head; fc.hidden = target_hidden; fc.draft = draft_logits; fc.draft_tok = draft_tok;
+  fc.u_accept = u_accept; fc.u_final = u_final;
+  fc.out_tok = out_tok; fc.accept_len = accept_len; fc.num_accepted = num_accepted;
+  fc.ws = ws;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = timed(MTP_KC_VERIFY, s, [&] { return launch_fused_verify(fc, s, use_pdl()); });
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return cuda_rc(e);
 }
 
 int mtp_get_status(const void *ws, mtp_stream_t stream, int32_t *status) {

@@ -146,6 +146,24 @@ bool plan_verify(int B, int k, int V, VerifyPlan *p);
 cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s, bool pdl);
 cudaError_t verify_set_attributes();
 
+// Verification from the target's hidden states (fused.cu).
+struct FusedCall {
+  int B, k, V, d, mode;
+  float T;
+  const void *head;       // [V, d] bf16
+  const void *hidden;     // [B (k+1), d] bf16
+  const float *draft;     // [B, k, V] (stochastic)
+  const int *draft_tok;   // [B, k]
+  const float *u_accept;  // [B, k]
+  const float *u_final;   // [B]
+  int *out_tok, *accept_len, *num_accepted;
+  void *ws;               // fused_workspace_bytes(), 256-byte aligned; starts with the status word
+};
+bool fused_shape_ok(int B, int k, int V, int d);
+size_t fused_workspace_bytes(int B, int k, int V, int d, int mode);
+cudaError_t fused_set_attributes();
+cudaError_t launch_fused_verify(const FusedCall &fc, cudaStream_t s, bool pdl);
+
 // bookkeeping shared with api.cu
 void note_launch();
 // Unique id of the calling thread's current CUDA context (0 if there is none):

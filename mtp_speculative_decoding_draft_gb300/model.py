@@ -182,3 +182,31 @@ class Verifier:
         torch.cuda.synchronize()
         return (self.out_tok.view(self.B, self.k + 1).cpu().numpy(), self.accept_len.cpu().numpy(),
                 self.num_accepted.cpu().numpy())
+
+
+class FusedVerifier:
+    """Buffers for spec_verify_fused on B sequences of depth k over V tokens
+    with hidden width d (outputs and workspace inside canary bands)."""
+
+    def __init__(self, B, k, V, d, mode, device="cuda"):
+        self.B, self.k, self.V, self.d, self.mode = B, k, V, d, mode
+        self.guard = Guarded(device)
+        g = self.guard
+        self.ws = g.alloc("workspace", max(256, bd.fused_workspace_size(B, k, V, d, mode)), torch.uint8)
+        self.out_tok = g.alloc("out_tok", B * (k + 1), torch.int32)
+        self.accept_len = g.alloc("accept_len", B, torch.int32)
+        self.num_accepted = g.alloc("num_accepted", B, torch.int32)
+
+    def __call__(self, T, head, target_hidden, draft_logits, draft_tok, u_accept=None, u_final=None, stream=None):
+        bd.spec_verify_fused(self.B, self.k, self.V, self.d, T, self.mode, head, target_hidden, draft_logits,
+                             draft_tok, u_accept, u_final, self.out_tok, self.accept_len, self.num_accepted, self.ws,
+                             stream)
+
+    def check_canaries(self):
+        torch.cuda.synchronize()
+        self.guard.check()
+
+    def results(self):
+        torch.cuda.synchronize()
+        return (self.out_tok.view(self.B, self.k + 1).cpu().numpy(), self.accept_len.cpu().numpy(),
+                self.num_accepted.cpu().numpy())
