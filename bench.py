@@ -246,6 +246,44 @@ def _oracle_verify_samples(workload_name, k, greedy, n, n_seq, budget_s=None):
     return out
 
 
+def _oracle_fused_samples(workload_name, greedy, n, n_seq, budget_s=None):
+    """Time the oracle's verification from hidden states on the first n_seq
+    sequences of the fused workload, up to n times (fewer once budget_s seconds
+    have passed, at least once); seconds per call scaled to all B sequences."""
+    from oracle.block import STOCHASTIC, select_token
+    from oracle.verify import spec_verify_fused, target_logits_from_hidden
+    w = W.WORKLOADS[workload_name]
+    if greedy:
+        w = W.replace(w, mode=W.GREEDY)
+    inp = W.fused_inputs(w)
+    s = list(range(min(n_seq, w.B)))
+    # the sampled sequences' draft logits and tokens (inputs of the call, prepared untimed)
+    draft = np.zeros((w.B, w.k, w.V))
+    draft[s] = target_logits_from_hidden(inp["head"], inp["hidden"][s])[:, :w.k] + inp["noise"][s]
+    d = np.zeros((w.B, w.k), np.int32)
+    for b in s:
+        for j in range(w.k):
+            d[b, j] = select_token(draft[b, j], STOCHASTIC, w.T, float(inp["u_draft"][b, j]))
+    out = []
+    start = time.perf_counter()
+    for _ in range(n):
+        t0 = time.perf_counter()
+        spec_verify_fused(inp["head"], inp["hidden"], draft, d, w.mode, w.T, inp["u_accept"], inp["u_final"],
+                          seqs=s)
+        t1 = time.perf_counter()
+        out.append((t1 - t0) * w.B / len(s))
+        if budget_s is not None and t1 - start > budget_s:
+            break
+    return out
+
+
+def cpu_oracle_fused_times(args, n, n_seq=4, budget_s=None):
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench._oracle_fused_samples(%r, %r, %d, %d, %r)))"
+            % (ROOT, args.workload, bool(args.greedy), n, n_seq, budget_s))
+    return _single_threaded(code)
+
+
 def _single_threaded(code):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
@@ -329,7 +367,16 @@ def run_reference(args):
         return
     w = W.WORKLOADS[args.workload]
     n_req = args.warmup + args.steps
-    if w.verify_only:
+    if w.fused:
+        if args.greedy:
+            w = W.replace(w, mode=W.GREEDY)
+        n_seq = 4
+        times = cpu_oracle_fused_times(args, n_req, n_seq, budget_s=REFERENCE_BUDGET_S)
+        unit = "verify calls/s"
+        sample = ("per call: the oracle forms the target logits from the hidden states and verifies %d of the "
+                  "%d sequences in a single-threaded process; call time = that time x %d / %d"
+                  % (n_seq, w.B, w.B, n_seq))
+    elif w.verify_only:
         w = _verify_workload(args)
         n_seq = 16
         times = cpu_oracle_verify_times(args, n_req, n_seq, budget_s=REFERENCE_BUDGET_S)
@@ -367,12 +414,13 @@ def config_of(w, args):
             + ("_draftvocab%d" % dv if dv else "")
             + ("_correlated%g" % args.correlated if getattr(args, "correlated", 0) > 0 and w.mode == 0 else ""))
     return {"workload": name, "modules": mods, "stop_p": sp, "draft_vocab": dv or None, "B": w.B, "k": w.k, "d": w.d, "Hq": w.Hq, "Hkv": w.Hkv,
-            "Dh": w.Dh, "F": w.F,
+            "Dh": w.Dh, "F": w.F, "fused": bool(w.fused),
             "V": w.V, "ctx": w.ctx if not isinstance(w.ctx, tuple) else list(w.ctx),
             "mode": "greedy" if w.mode == 0 else "stochastic", "T": w.T,
             "launch": "cuda graph replay" if getattr(args, "graph", False) else "direct calls",
             "parallelism": "replicas%d" % args.gpus,
-            "l2": ("inputs larger than L2 (%.2f GB of logits read per call)" % (verify_bytes(w) / 1e9) if w.verify_only
+            "l2": ("inputs larger than L2 (the %.2f GB head streamed per call)" % (w.V * w.d * 2 / 1e9) if w.fused
+                   else "inputs larger than L2 (%.2f GB of logits read per call)" % (verify_bytes(w) / 1e9) if w.verify_only
                    else "inputs larger than L2 (weights %.2f GB re-streamed per depth)"
                    % ((block_elements(w) + w.V * w.d) * 2 / 1e9))}
 
@@ -399,6 +447,167 @@ def verify_bytes(w):
     """Algorithmic bytes of one spec_verify: every logit row read once."""
     rows = w.B * (w.k + 1) + (w.B * w.k if w.mode == 1 else 0)
     return rows * w.V * 4
+
+
+def fused_bytes(w):
+    """Algorithmic bytes of one spec_verify_fused call that it certainly moves:
+    the head and the hidden states read once; stochastic also writes the
+    target's fp32 logits (its draw reads back only the rows it reaches, not
+    counted)."""
+    Na = w.B * (w.k + 1)
+    return w.V * w.d * 2 + Na * w.d * 2 + (Na * w.V * 4 if w.mode == 1 else 0)
+
+
+def fused_flops(w):
+    return 2.0 * w.B * (w.k + 1) * w.V * w.d
+
+
+def measured_tflops():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p))["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
+def _fused_setup(w):
+    """Device inputs of the fused workload: head, hidden, the draft's logits
+    (the target's own head . hidden plus the seeded noise, formed here with a
+    plain float32 matmul as input preparation) and drafts drawn from q."""
+    import torch
+    from mtp_speculative_decoding_draft_gb300.model import FusedVerifier, to_device, to_device_bf16
+    inp = W.fused_inputs(w)
+    head_d, hid_d = to_device_bf16(inp["head"]), to_device_bf16(inp["hidden"])
+    tl = torch.matmul(hid_d.view(-1, w.d).float(), head_d.view(w.V, w.d).float().T).view(w.B, w.k + 1, w.V)
+    draft = (tl[:, :w.k] + to_device(inp["noise"])).contiguous()
+    del tl
+    torch.cuda.empty_cache()
+    dtok = drafts_from_q(draft, to_device(inp["u_draft"]), w.T)
+    ua, uf = to_device(inp["u_accept"]), to_device(inp["u_final"])
+    fv = FusedVerifier(w.B, w.k, w.V, w.d, w.mode)
+    return inp, head_d, hid_d, draft, dtok, ua, uf, fv
+
+
+def time_fused(w, steps, warmup, peak):
+    """spec_verify_fused on the fused workload, CUDA-event timed with its own
+    clock samples."""
+    import torch
+    from mtp_speculative_decoding_draft_gb300 import binding as bd
+    inp, head_d, hid_d, draft, dtok, ua, uf, fv = _fused_setup(w)
+    stoch = w.mode == 1
+
+    def call():
+        fv(w.T, head_d, hid_d, draft if stoch else None, dtok, ua if stoch else None, uf if stoch else None)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / steps
+    assert bd.get_status(fv.ws) == 0
+    _, L, _ = fv.results()
+    tf, tf_kind = measured_tflops()
+    fb = fused_bytes(w)
+    out = {"workload": "%s/%s" % (w.name, "stochastic" if stoch else "greedy"), "ms_per_call": ms,
+           "calls_s": 1e3 / ms, "steps": steps, "warmup": warmup, "bytes_per_call": fb,
+           "achieved_gbs": fb / (ms * 1e-3) / 1e9, "frac": fb / (ms * 1e-3) / 1e9 / peak,
+           "tflops": fused_flops(w) / (ms * 1e-3) / 1e12, "tensor_frac": fused_flops(w) / (ms * 1e-3) / 1e12 / tf,
+           "tensor_peak_kind": tf_kind, "accept_len_mean": float(L.mean()), "clocks": clk}
+    return out, (inp, head_d, hid_d, draft, dtok, ua, uf, fv, call)
+
+
+def run_fused_only(args, w, rank=0, world=1):
+    """spec_verify_fused on the fused workload (one replica per rank)."""
+    import torch
+    import torch.distributed as dist
+    from mtp_speculative_decoding_draft_gb300.build import build
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    if rank == 0 or world == 1:
+        build()
+    if world > 1:
+        dist.barrier()
+        build()
+    if args.greedy:
+        w = W.replace(w, mode=W.GREEDY)
+    peak, peak_kind = measured_peaks()
+    from mtp_speculative_decoding_draft_gb300 import binding as bd
+    n0 = bd.launch_count()
+    res, (inp, head_d, hid_d, draft, dtok, ua, uf, fv, call) = time_fused(w, args.steps, args.warmup, peak)
+    launches = bd.launch_count() - n0 - 2 * args.warmup
+    ms = max_over_ranks(res["ms_per_call"])
+    # end to end: per call the hidden states, the draft's logits and tokens and
+    # the uniforms from pinned host memory (the head stays resident, like any
+    # weight), the outputs read back
+    stoch = w.mode == 1
+    stream = torch.cuda.current_stream()
+    pairs = [(hid_d.cpu().pin_memory(), hid_d), (dtok.cpu().pin_memory(), dtok)]
+    if stoch:
+        pairs += [(draft.cpu().pin_memory(), draft), (ua.cpu().pin_memory(), ua), (uf.cpu().pin_memory(), uf)]
+    outs = [(torch.empty(t.numel(), dtype=t.dtype).pin_memory(), t) for t in (fv.out_tok, fv.accept_len, fv.num_accepted)]
+    h2d = sum(h.numel() * h.element_size() for h, _ in pairs)
+    d2h = sum(h.numel() * h.element_size() for h, _ in outs)
+
+    def e2e_call():
+        for h, dv in pairs:
+            dv.copy_(h, non_blocking=True)
+        call()
+        for h, dv in outs:
+            h.copy_(dv, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(max(1, args.warmup)):
+        e2e_call()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+    fb = fused_bytes(w)
+    ach = fb / (ms * 1e-3) / 1e9
+    _, L, _ = fv.results()
+    line = {"metric": METRIC, "value": job_rate(ms, world), "unit": "verify calls/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 head and hidden / fp32 accumulate",
+            "data": "synthetic (seeded)", "config": config_of(w, args),
+            "accept_len_mean": float(L.mean()), "acceptance": acceptance_metrics(L, w.k),
+            "roofline": {"bound": "hbm", "kernel": "fv_gemm_kernel + fv_finish_kernel", "achieved": ach,
+                         "peak": peak, "unit": "GB/s", "frac": ach / peak, "peak_kind": peak_kind,
+                         "traffic": None, "bytes_per_launch": fb, "avg_launch_ms": ms, "launches": args.steps,
+                         "tflops": res["tflops"], "tensor_frac": res["tensor_frac"]},
+            "e2e": {"value": job_rate(e2e_ms, world), "unit": "verify calls/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": int(launches), "clocks": res["clocks"]}
+    if not args.no_cpu_baseline and world == 1:
+        try:
+            ts = cpu_oracle_fused_times(args, 3, 4, budget_s=60)
+            t_call = float(np.median(ts))
+            line["cpu_baseline"] = dict({"value": 1.0 / t_call, "unit": "verify calls/s", "cores": 1, "kind": "oracle",
+                                         "sample": "median of %d calls: the oracle forms the logits and verifies 4 of "
+                                                   "the %d sequences, single-threaded float64 numpy; scaled to the "
+                                                   "batch" % (len(ts), w.B)}, **host_cpu())
+        except Exception as e:  # report, do not hide
+            line["cpu_baseline"] = {"value": None, "error": str(e)[:300]}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
 
 
 def run_verify_only(args, w, rank=0, world=1):
@@ -632,13 +841,17 @@ def secondary_verify(k, greedy, steps, warmup, peak):
 
 
 def run_secondary(peak, steps=SECONDARY_STEPS, warmup=5):
-    """The batched stochastic workload's step and the verify sweep at k = 3
-    (greedy and stochastic), each timed in this process; failures are reported
-    in place of the figures."""
+    """The batched stochastic workload's step, the verify sweep at k = 3 and the
+    verification from hidden states at the batched shape (greedy and stochastic
+    each), timed in this process; failures are reported in place of the
+    figures."""
     out = {}
     for key, fn in (("batched_stochastic_step", lambda: secondary_step(W.BATCHED_STOCHASTIC, steps, warmup, peak)),
                     ("verify_sweep_k3_greedy", lambda: secondary_verify(3, True, 4 * steps, warmup, peak)),
-                    ("verify_sweep_k3_stochastic", lambda: secondary_verify(3, False, 4 * steps, warmup, peak))):
+                    ("verify_sweep_k3_stochastic", lambda: secondary_verify(3, False, 4 * steps, warmup, peak)),
+                    ("fused_verify_b64_k3_greedy",
+                     lambda: time_fused(W.replace(W.FUSED_VERIFY, mode=W.GREEDY), steps, warmup, peak)[0]),
+                    ("fused_verify_b64_k3_stochastic", lambda: time_fused(W.FUSED_VERIFY, steps, warmup, peak)[0])):
         try:
             out[key] = fn()
         except Exception as e:  # report, do not hide
@@ -660,6 +873,8 @@ def run_ours(args):
     if world > 1:
         dist.init_process_group("nccl")
     w = W.WORKLOADS[args.workload]
+    if w.fused:
+        return run_fused_only(args, w, rank, world)
     if w.verify_only:
         return run_verify_only(args, _verify_workload(args), rank, world)
     if rank == 0 or world == 1:

@@ -17,13 +17,16 @@
 //   logits: the residual draw needs every element of the first rejecting row
 //   once the target's normaliser is known, and reading that row back is far
 //   cheaper than streaming E a second time to recompute it.
-// fv_finish_kernel: one CTA per sequence combines the partials of its k+1
-//   rows in vocabulary-tile order and takes the decisions of spec_verify (the
-//   same rule): greedy longest prefix; stochastic u q(d) < p(d) position by
-//   position with the draft row's normaliser from one pass over it, then the
-//   inverse-CDF draw at u_final over max(0, p - q) of the first rejecting row
-//   (over p if that is identically zero), or over p of row k when every draft
-//   is accepted.  Only the rows the decisions reach are read.
+// fv_draft_stats_kernel (stochastic, first): the draft rows' per-tile (max,
+//   sum of exp2) in the same tiling, every draft logit read once.
+// fv_finish_kernel: one CTA per sequence combines the partials of its rows in
+//   vocabulary-tile order and takes the decisions of spec_verify (the same
+//   rule): greedy longest prefix; stochastic u q(d) < p(d) position by
+//   position, then the inverse-CDF draw at u_final -- over max(0, p - q) of the
+//   first rejecting row (over p if that is identically zero), which takes one
+//   pass over that row's target and draft logits, or over p of row k when
+//   every draft is accepted, whose tile masses follow from the partials so
+//   that only the crossing tile is read again.
 #include <cuda.h>
 #include <stdlib.h>
 
@@ -43,9 +46,9 @@ constexpr uint32_t kATile = kMRows * kBK * 2;  // 16 KB
 constexpr uint32_t kBTile = kVt * kBK * 2;     // 32 KB
 constexpr int kMaxMt = 2;         // hidden-row tiles per unit: 2 x 256 TMEM columns
 constexpr int kSmemBudget = 227 * 1024 - 1024 - 256;
-constexpr int kFinThreads = 256;
+constexpr int kFinThreads = 512;
 constexpr int kFinWarps = kFinThreads / 32;
-constexpr int kMaxChunks = 4096;  // inverse-CDF chunk sums per row, at most
+constexpr int kMaxChunks = 4096;  // inverse-CDF chunk sums per row, at most (chunks of whole tiles)
 
 __host__ __device__ inline uint32_t fv_stage_bytes(int mt) { return (uint32_t)mt * kATile + kBTile; }
 
@@ -62,12 +65,13 @@ struct FvArgs {
   int n_mt, groups;       // 128-row tiles per unit; row groups of n_mt tiles
   int n_vt, kbs;          // 256-row vocabulary tiles; 64-wide k-blocks
   int stages, nunits;     // ring depth; (group, vocabulary tile) units
-  int chunk;              // elements per chunk of the finish kernel's draws
+  int chunk;              // elements per chunk of the finish kernel's draws (whole 256-token tiles)
   const int *draft_tok;   // [B, k]
   const float *draft;     // [B, k, V] (stochastic)
   const float *u_accept;  // [B, k]
   const float *u_final;   // [B]
   float4 *part;           // [Na, n_vt] (max, sum of exp2 | argmax) per row and tile
+  float4 *dpart;          // [B k, n_vt] (max, sum of exp2) of the draft rows (stochastic)
   float *tgt;             // [Na, V] stored logits (stochastic), else null
   int *status;
 };
@@ -259,6 +263,50 @@ __global__ void __launch_bounds__(kFvThreads, 1) fv_gemm_kernel(const __grid_con
   }
 }
 
+// ---------------------------------------------------------------- draft-row statistics (stochastic)
+
+// Per (draft row, 256-token tile): (max, sum of exp2((x - max) log2e / T)) of
+// the draft logits, in the target partials' tiling.  One warp per tile (each
+// lane 8 elements), eight tiles a CTA: every draft logit is read once.
+__global__ void __launch_bounds__(256) fv_draft_stats_kernel(const FvArgs g) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp, r = blockIdx.y;  // tile, draft row b k + j
+  grid_dep_launch();
+  // It reads only the caller's draft logits, so it runs beside the GEMM; it
+  // waits for the GEMM before completing, so that the finish kernel's wait on
+  // this kernel covers both.
+  if (t < g.n_vt) {
+    const float *row = g.draft + (size_t)r * g.V;
+    const int e0 = t * kVt, n = min(kVt, g.V - e0);
+    float x[8];
+    if (n == kVt && (reinterpret_cast<uintptr_t>(row + e0) & 15u) == 0) {
+      const float4 a = __ldcg(reinterpret_cast<const float4 *>(row + e0) + lane);
+      const float4 b = __ldcg(reinterpret_cast<const float4 *>(row + e0) + 32 + lane);
+      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+      x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = (i < 4 ? 4 * lane + i : 128 + 4 * lane + i - 4);
+        x[i] = e < n ? __ldcg(row + e0 + e) : -INFINITY;
+      }
+    }
+    float m = x[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) m = fmaxf(m, x[i]);
+    m = warp_max(m);
+    float s = 0.f;
+    if (m != -INFINITY) {
+      const float mc = m * g.c;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s += ex2f(fmaf(x[i], g.c, -mc));
+    }
+    s = warp_sum(s);
+    if (lane == 0) g.dpart[(size_t)r * g.n_vt + t] = make_float4(m, s, 0.f, 0.f);
+  }
+  grid_dep_wait();
+}
+
 // ---------------------------------------------------------------- finish kernel
 
 namespace {
@@ -274,55 +322,73 @@ __device__ __forceinline__ double fv_warp_incl_scan(double v) {
 }
 
 struct FinShared {
-  float M[9];
-  double Z[9];
+  float M[9], Ml[8];
+  double Z[9], Zl[8];
   int I[9];
-  float red_f[kFinWarps];
-  double red_d[kFinWarps];
-  int red_i[kFinWarps];
   int chosen;
   double csum[kMaxChunks];
 };
 
-// Block-wide (max over the block of m, then sum over threads of s 2^((m - M) c))
-// -- this thread holds (m, s) over its own elements.  Every thread gets both.
-__device__ void block_lse(FinShared &sh, float m, float s, float c, float &Mout, double &Zout) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float wm = warp_max(m);
-  if (lane == 0) sh.red_f[warp] = wm;
-  __syncthreads();
-  float M = -INFINITY;
-  for (int w = 0; w < kFinWarps; ++w) M = fmaxf(M, sh.red_f[w]);
-  double z = (m == -INFINITY || M == -INFINITY) ? 0.0 : (double)s * (double)ex2f((m - M) * c);
-  z = warp_sum_d(z);
-  if (lane == 0) sh.red_d[warp] = z;
-  __syncthreads();
-  double Z = 0.0;
-  for (int w = 0; w < kFinWarps; ++w) Z += sh.red_d[w];
-  __syncthreads();
-  Mout = M;
-  Zout = Z;
+// Sampling weight of an element: the residual max(0, p - q) (kind 0), the
+// target probability p (kind 1), the unnormalised target weight (kind 2).
+struct Wt {
+  int kind;
+  float Mt, iZt, Ml, iZl, c;
+};
+
+__device__ __forceinline__ float wval(const Wt &w, float t, float l) {
+  const float e = ex2f((t - w.Mt) * w.c);
+  if (w.kind == 2) return e;
+  const float p = e * w.iZt;
+  if (w.kind == 1) return p;
+  return fmaxf(0.f, p - ex2f((l - w.Ml) * w.c) * w.iZl);
 }
 
-// Inverse-CDF draw over weights wfn(i), i in [0, V): the smallest i with C_i >
-// u S (C the running sum in index order, S the total), else the last index of
-// positive weight; -1 if every weight is zero.  Chunk sums in float64 by the
-// whole block (each lane adds its elements in float, the lanes in float64),
-// then warp 0 scans the chunks and rescans the crossing chunk in float64.
-template <class WFn>
-__device__ int block_inverse_cdf(FinShared &sh, WFn wfn, int V, int chunk, double u) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nch = (V + chunk - 1) / chunk;
-  for (int ch = warp; ch < nch; ch += kFinWarps) {
-    const int e0 = ch * chunk, e1 = min(V, e0 + chunk);
-    float s = 0.f;
-    for (int i = e0 + lane; i < e1; i += 32) s += wfn(i);
-    const double t = warp_sum_d((double)s);
-    if (lane == 0) sh.csum[ch] = t;
+// Row j's (max, partition sum relative to it) from its per-tile partials, in
+// tile order per lane, lanes combined in a fixed tree (warp-collective).  The
+// lane's partials are loaded eight at a time, so that their loads overlap.
+__device__ __forceinline__ void combine_lse(const float4 *pp, int n_vt, float c, float &M, double &Z) {
+  const int lane = threadIdx.x & 31;
+  float m = -INFINITY;
+  double z = 0.0;
+  for (int t0 = lane; t0 < n_vt; t0 += 8 * 32) {  // online over batches of eight tiles
+    float2 p[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int t = t0 + 32 * i;
+      const float4 v = t < n_vt ? __ldcg(&pp[t]) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+      p[i] = make_float2(v.x, v.y);
+    }
+    float bm = p[0].x;
+#pragma unroll
+    for (int i = 1; i < 8; ++i) bm = fmaxf(bm, p[i].x);
+    if (bm > m) {
+      if (m != -INFINITY) z *= (double)ex2f((m - bm) * c);
+      m = bm;
+    }
+    if (m != -INFINITY)
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (p[i].x != -INFINITY) z += (double)p[i].y * (double)ex2f((p[i].x - m) * c);
   }
+  // lanes: rescale to the warp maximum, then sum in a fixed tree
+  const float wm = warp_max(m);
+  z = (m == -INFINITY) ? 0.0 : z * (double)ex2f((m - wm) * c);
+  M = wm;
+  Z = warp_sum_d(z);
+}
+
+// The inverse-CDF draw once the chunk masses csum[0, nch) are in shared
+// memory (chunk = chunk_len elements): the smallest i with C_i > u S, else the
+// last index of positive weight, -1 if all weights are zero.  Warp 0 scans the
+// chunks, then rescans the crossing chunk in float64 (lane l a contiguous run
+// of chunk_len / 32 elements), with weights wval(w, t[i], l[i]).
+__device__ int draw_from_chunks(FinShared &sh, const Wt &w, const float *trow, const float *lrow, int V,
+                                int chunk_len, double u) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nch = (V + chunk_len - 1) / chunk_len;
   __syncthreads();
   if (warp == 0) {
-    // total, then the first chunk whose running sum passes u S
     double tot = 0.0;
     for (int b = 0; b < nch; b += 32) {
       const double x = b + lane < nch ? sh.csum[b + lane] : 0.0;
@@ -347,22 +413,21 @@ __device__ int block_inverse_cdf(FinShared &sh, WFn wfn, int V, int chunk, doubl
     int found = -1;
     const int ch = cross >= 0 ? cross : lastpos;
     if (ch >= 0) {
-      // rescan chunk ch: lane l a contiguous run of chunk / 32 elements
-      const int per = chunk / 32;
-      const int e0 = ch * chunk + lane * per, e1 = min(V, e0 + per);
+      const int per = chunk_len / 32;
+      const int e0 = ch * chunk_len + lane * per, e1 = min(V, e0 + per);
       double ls = 0.0;
       int lp = -1;
       for (int i = e0; i < e1; ++i) {
-        const float w = wfn(i);
-        ls += (double)w;
-        if (w > 0.f) lp = i;
+        const float x = wval(w, __ldcg(trow + i), w.kind == 0 ? __ldcg(lrow + i) : 0.f);
+        ls += (double)x;
+        if (x > 0.f) lp = i;
       }
       const double inc = fv_warp_incl_scan(ls);
       int f = 0x7fffffff;
       if (cross >= 0 && before + inc > tgt) {
         double r = before + (inc - ls);
         for (int i = e0; i < e1; ++i) {
-          r += (double)wfn(i);
+          r += (double)wval(w, __ldcg(trow + i), w.kind == 0 ? __ldcg(lrow + i) : 0.f);
           if (r > tgt) {
             f = i;
             break;
@@ -379,14 +444,73 @@ __device__ int block_inverse_cdf(FinShared &sh, WFn wfn, int V, int chunk, doubl
     if (lane == 0) sh.chosen = found;
   }
   __syncthreads();
-  const int r = sh.chosen;
-  __syncthreads();
-  return r;
+  return sh.chosen;
+}
+
+// Chunk masses of a target-only weight (kinds 1 and 2) from the row's tile
+// partials: a tile's mass is its sum of exp2((t - m) c) rescaled to the row's
+// maximum (and, for kind 1, divided by the partition sum).
+__device__ void chunk_masses_from_partials(FinShared &sh, const float4 *pp, int n_vt, int tiles_per_chunk,
+                                           const Wt &w) {
+  const int nch = (n_vt + tiles_per_chunk - 1) / tiles_per_chunk;
+  for (int ch = threadIdx.x; ch < nch; ch += kFinThreads) {
+    double s = 0.0;
+    for (int t = ch * tiles_per_chunk; t < min(n_vt, (ch + 1) * tiles_per_chunk); ++t) {
+      const float4 p = __ldcg(&pp[t]);
+      if (p.x != -INFINITY) s += (double)p.y * (double)ex2f((p.x - w.Mt) * w.c);
+    }
+    sh.csum[ch] = w.kind == 1 ? s * (double)w.iZt : s;
+  }
+}
+
+// Chunk masses of the residual weight by a pass over both rows: warp w takes
+// chunks w, w + warps, ... four at a time, each lane 16-byte loads of its
+// elements of both rows issued together.
+__device__ void chunk_masses_residual(FinShared &sh, const Wt &w, const float *trow, const float *lrow, int V,
+                                      int chunk_len) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nch = (V + chunk_len - 1) / chunk_len;
+  const bool vec = ((reinterpret_cast<uintptr_t>(trow) | reinterpret_cast<uintptr_t>(lrow)) & 15u) == 0;
+  constexpr int kU = 4;  // chunks per warp and round
+  for (int c0 = warp * kU; c0 < nch; c0 += kFinWarps * kU) {
+    float s[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) s[u] = 0.f;
+    const int nfull = (V / chunk_len);  // chunks without a ragged end
+    if (vec && c0 + kU <= nfull) {
+      // chunk_len / 128 float4 per lane and row per chunk
+      for (int q = 0; q < chunk_len / 128; ++q) {
+        float4 tv[kU], lv[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const size_t e = (size_t)(c0 + u) * chunk_len + (size_t)(q * 32 + lane) * 4;
+          tv[u] = __ldcg(reinterpret_cast<const float4 *>(trow + e));
+          lv[u] = __ldcg(reinterpret_cast<const float4 *>(lrow + e));
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+          s[u] += wval(w, tv[u].x, lv[u].x) + wval(w, tv[u].y, lv[u].y) + wval(w, tv[u].z, lv[u].z) +
+                  wval(w, tv[u].w, lv[u].w);
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int e0 = (c0 + u) * chunk_len, e1 = min(V, e0 + chunk_len);
+        for (int i = e0 + lane; i < e1; i += 32) s[u] += wval(w, __ldcg(trow + i), __ldcg(lrow + i));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const float t = warp_sum(s[u]);  // float: float64 is a small fraction of the float rate here
+      if (lane == 0 && c0 + u < nch) sh.csum[c0 + u] = (double)t;
+    }
+  }
 }
 
 }  // namespace
 
-// One CTA per sequence: the decisions of spec_verify from the GEMM's partials.
+// One CTA per sequence: the decisions of spec_verify from the GEMM's
+// partials (and, stochastic, the draft rows' partials), then the draw.
 template <int MODE>
 __global__ void __launch_bounds__(kFinThreads) fv_finish_kernel(const FvArgs g, FvOut o) {
   extern __shared__ __align__(16) unsigned char fin_smem[];
@@ -396,34 +520,47 @@ __global__ void __launch_bounds__(kFinThreads) fv_finish_kernel(const FvArgs g, 
   const float c = g.c;
   grid_dep_wait();
   grid_dep_launch();
-  // combine each row's partials in vocabulary-tile order (fixed lane order)
+  // each row's statistics from its partials, in vocabulary-tile order
   for (int j = warp; j <= k; j += kFinWarps) {
     const float4 *pp = g.part + (size_t)(b * (k + 1) + j) * g.n_vt;
-    float m = -INFINITY;
-    int idx = 0x7fffffff;
-    for (int t = lane; t < g.n_vt; t += 32) {
-      const float4 p = __ldcg(&pp[t]);
-      if (MODE == 0) argmax_merge(m, idx, p.x, __float_as_int(p.y));
-      else m = fmaxf(m, p.x);
-    }
     if (MODE == 0) {
-      warp_argmax(m, idx);
-    } else {
-      m = warp_max(m);
-    }
-    double z = 0.0;
-    if (MODE == 1 && m != -INFINITY)
-      for (int t = lane; t < g.n_vt; t += 32) {
-        const float4 p = __ldcg(&pp[t]);
-        if (p.x != -INFINITY) z += (double)p.y * (double)ex2f((p.x - m) * c);
+      float m = -INFINITY;
+      int idx = 0x7fffffff;
+      for (int t0 = lane; t0 < g.n_vt; t0 += 8 * 32) {  // eight partials in flight per lane
+        float4 p[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int t = t0 + 32 * i;
+          p[i] = t < g.n_vt ? __ldcg(&pp[t]) : make_float4(-INFINITY, __int_as_float(0x7fffffff), 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) argmax_merge(m, idx, p[i].x, __float_as_int(p[i].y));
       }
-    z = warp_sum_d(z);
-    if (lane == 0) {
-      sh.M[j] = m;
-      sh.Z[j] = z;
-      sh.I[j] = idx;
+      warp_argmax(m, idx);
+      if (lane == 0) {
+        sh.M[j] = m;
+        sh.I[j] = idx;
+      }
+    } else {
+      float m;
+      double z;
+      combine_lse(pp, g.n_vt, c, m, z);
+      if (lane == 0) {
+        sh.M[j] = m;
+        sh.Z[j] = z;
+      }
     }
   }
+  if (MODE == 1)
+    for (int j = warp; j < k; j += kFinWarps) {
+      float m;
+      double z;
+      combine_lse(g.dpart + (size_t)(b * k + j) * g.n_vt, g.n_vt, c, m, z);
+      if (lane == 0) {
+        sh.Ml[j] = m;
+        sh.Zl[j] = z;
+      }
+    }
   __syncthreads();
   const int *dt = g.draft_tok + (size_t)b * k;
   int n_acc = 0, tok = 0, flags = 0;
@@ -443,61 +580,56 @@ __global__ void __launch_bounds__(kFinThreads) fv_finish_kernel(const FvArgs g, 
       tok = 0;
     }
   } else {
-    // position by position: the draft row's normaliser, then u q(d) < p(d)
-    int rej = -1;
-    float Ml = -INFINITY;
-    double Zl = 0.0;
-    const float *drow = nullptr;
-    for (int j = 0; j < k; ++j) {
-      const int d = __ldg(&dt[j]);
-      drow = g.draft + ((size_t)b * k + j) * V;
-      float m = -INFINITY, s = 0.f;
-      for (int i = threadIdx.x; i < V; i += kFinThreads) {  // online (max, sum) of this thread's elements
-        const float x = __ldcg(drow + i);
-        if (x > m) {
-          if (m != -INFINITY) s *= ex2f((m - x) * c);
-          m = x;
+    // position by position: u q(d) < p(d), taken by thread 0 and shared
+    if (threadIdx.x == 0) {
+      int rj = -1, fl = 0;
+      for (int j = 0; j < k; ++j) {
+        const int d = __ldg(&dt[j]);
+        if (d < 0 || d >= V) {
+          fl |= kStatusBadToken;
+          rj = j;
+          break;
         }
-        if (m != -INFINITY) s += ex2f((x - m) * c);
+        if (!(sh.M[j] > -INFINITY) || !(sh.Ml[j] > -INFINITY)) fl |= kStatusNonFinite;
+        const double td = (double)__ldcg(g.tgt + (size_t)(b * (k + 1) + j) * V + d);
+        const double ld = (double)__ldcg(g.draft + ((size_t)b * k + j) * V + d);
+        const double p = exp2((td - (double)sh.M[j]) * (double)c) / sh.Z[j];
+        const double q = exp2((ld - (double)sh.Ml[j]) * (double)c) / sh.Zl[j];
+        const double ua = (double)__ldg(&g.u_accept[(size_t)b * k + j]);
+        if (!(ua * q < p)) {
+          rj = j;
+          break;
+        }
       }
-      block_lse(sh, m, s, c, Ml, Zl);
-      if (d < 0 || d >= V) {
-        flags |= kStatusBadToken;
-        rej = j;
-        break;
-      }
-      if (!(sh.M[j] > -INFINITY) || !(Ml > -INFINITY)) flags |= kStatusNonFinite;
-      const double td = (double)__ldcg(g.tgt + (size_t)(b * (k + 1) + j) * V + d);
-      const double ld = (double)__ldcg(drow + d);
-      const double p = exp2((td - (double)sh.M[j]) * (double)c) / sh.Z[j];
-      const double q = exp2((ld - (double)Ml) * (double)c) / Zl;
-      const double ua = (double)__ldg(&g.u_accept[(size_t)b * k + j]);
-      if (!(ua * q < p)) {
-        rej = j;
-        break;
-      }
+      sh.I[0] = rj;
+      sh.I[1] = fl;
     }
+    __syncthreads();
+    const int rej = sh.I[0];
+    flags |= sh.I[1];
     const double uf = (double)__ldg(&g.u_final[b]);
+    const int row = b * (k + 1) + (rej >= 0 ? rej : k);
+    const float *trow = g.tgt + (size_t)row * V;
+    const float *lrow = rej >= 0 ? g.draft + ((size_t)b * k + rej) * V : trow;
+    const int r = rej >= 0 ? rej : k;
+    Wt w{2, sh.M[r], (float)(1.0 / sh.Z[r]), rej >= 0 ? sh.Ml[rej] : 0.f,
+         rej >= 0 ? (float)(1.0 / sh.Zl[rej]) : 0.f, c};
     int chosen;
     if (rej >= 0) {
       n_acc = rej;
-      const float *trow = g.tgt + (size_t)(b * (k + 1) + rej) * V;
-      const float Mt = sh.M[rej], iZt = (float)(1.0 / sh.Z[rej]), iZl = (float)(1.0 / Zl);
-      auto resid = [&](int i) -> float {
-        const float p = ex2f((__ldcg(trow + i) - Mt) * c) * iZt;
-        return fmaxf(0.f, p - ex2f((__ldcg(drow + i) - Ml) * c) * iZl);
-      };
-      chosen = block_inverse_cdf(sh, resid, V, g.chunk, uf);
+      w.kind = 0;
+      chunk_masses_residual(sh, w, trow, lrow, V, g.chunk);
+      chosen = draw_from_chunks(sh, w, trow, lrow, V, g.chunk, uf);
       if (chosen < 0) {  // p = q everywhere: draw from p itself
-        auto pw = [&](int i) -> float { return ex2f((__ldcg(trow + i) - Mt) * c) * iZt; };
-        chosen = block_inverse_cdf(sh, pw, V, g.chunk, uf);
+        w.kind = 1;
+        __syncthreads();
+        chunk_masses_from_partials(sh, g.part + (size_t)row * g.n_vt, g.n_vt, g.chunk / kVt, w);
+        chosen = draw_from_chunks(sh, w, trow, lrow, V, g.chunk, uf);
       }
     } else {
       n_acc = k;
-      const float *trow = g.tgt + (size_t)(b * (k + 1) + k) * V;
-      const float Mt = sh.M[k];
-      auto pw = [&](int i) -> float { return ex2f((__ldcg(trow + i) - Mt) * c); };
-      chosen = block_inverse_cdf(sh, pw, V, g.chunk, uf);
+      chunk_masses_from_partials(sh, g.part + (size_t)row * g.n_vt, g.n_vt, g.chunk / kVt, w);
+      chosen = draw_from_chunks(sh, w, trow, lrow, V, g.chunk, uf);
     }
     if (chosen < 0) {
       flags |= kStatusNonFinite;
@@ -545,7 +677,10 @@ size_t fused_workspace_bytes(int B, int k, int V, int d, int mode) {
   const size_t n_vt = ((size_t)V + kVt - 1) / kVt;
   size_t n = 256;                   // status word
   n += up256(Na * n_vt * 16);       // partials
-  if (mode == 1) n += up256(Na * (size_t)V * 4);  // stored logits (the draws read them)
+  if (mode == 1) {
+    n += up256((size_t)B * k * n_vt * 16);  // the draft rows' partials
+    n += up256(Na * (size_t)V * 4);         // stored logits (the residual draw reads one row)
+  }
   return n;
 }
 
@@ -588,10 +723,12 @@ cudaError_t launch_fused_verify(const FusedCall &fc, cudaStream_t s, bool pdl) {
   p += 256;
   g.part = reinterpret_cast<float4 *>(p);
   p += up256((size_t)g.Na * g.n_vt * 16);
-  g.tgt = fc.mode == 1 ? reinterpret_cast<float *>(p) : nullptr;
-  int chunk = (fc.V + kMaxChunks - 1) / kMaxChunks;
-  chunk = chunk < 512 ? 512 : (chunk + 31) / 32 * 32;
-  g.chunk = chunk;
+  if (fc.mode == 1) {
+    g.dpart = reinterpret_cast<float4 *>(p);
+    p += up256((size_t)fc.B * fc.k * g.n_vt * 16);
+    g.tgt = reinterpret_cast<float *>(p);
+  }
+  g.chunk = kVt * ((g.n_vt + kMaxChunks - 1) / kMaxChunks);  // whole tiles, at most kMaxChunks chunks
 
   FvMaps maps{};
   if (!make_bf16_map(&maps.hid, fc.hidden, (uint64_t)fc.d, (uint64_t)g.Na, (uint64_t)fc.d, kMRows))
@@ -599,6 +736,7 @@ cudaError_t launch_fused_verify(const FusedCall &fc, cudaStream_t s, bool pdl) {
   if (!make_bf16_map(&maps.head, fc.head, (uint64_t)fc.d, (uint64_t)fc.V, (uint64_t)fc.d, kVt))
     return cudaErrorInvalidValue;
 
+  cudaError_t e = cudaSuccess;
   const size_t smem = (size_t)g.stages * fv_stage_bytes(g.n_mt) + (size_t)(2 * g.stages + 4) * 8 + 16 + 1024;
   const int sms = fv_sms();
   cudaLaunchConfig_t cfg{};
@@ -608,9 +746,23 @@ cudaError_t launch_fused_verify(const FusedCall &fc, cudaStream_t s, bool pdl) {
   cfg.stream = s;
   cfg.numAttrs = 0;
   note_launch();
-  cudaError_t e = fc.mode == 1 ? cudaLaunchKernelEx(&cfg, fv_gemm_kernel<1>, maps, g)
-                               : cudaLaunchKernelEx(&cfg, fv_gemm_kernel<0>, maps, g);
+  e = fc.mode == 1 ? cudaLaunchKernelEx(&cfg, fv_gemm_kernel<1>, maps, g)
+                   : cudaLaunchKernelEx(&cfg, fv_gemm_kernel<0>, maps, g);
   if (e != cudaSuccess) return e;
+  cudaLaunchAttribute pattr[1];
+  pattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pattr[0].val.programmaticStreamSerializationAllowed = 1;
+  if (fc.mode == 1) {  // the draft rows' statistics, beside the GEMM (it needs no smem)
+    cudaLaunchConfig_t dcfg{};
+    dcfg.gridDim = dim3((unsigned)((g.n_vt + 7) / 8), (unsigned)(fc.B * fc.k));
+    dcfg.blockDim = dim3(256);
+    dcfg.stream = s;
+    dcfg.attrs = pattr;
+    dcfg.numAttrs = pdl ? 1 : 0;
+    note_launch();
+    e = cudaLaunchKernelEx(&dcfg, fv_draft_stats_kernel, g);
+    if (e != cudaSuccess) return e;
+  }
 
   FvOut o{fc.out_tok, fc.accept_len, fc.num_accepted};
   cudaLaunchConfig_t fcfg{};

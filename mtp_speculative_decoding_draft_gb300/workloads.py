@@ -59,6 +59,7 @@ class Workload:
     draft_noise_std0: float = 1.0
     noise_growth: float = 1.0
     verify_only: bool = False
+    fused: bool = False          # verification from the target's hidden states
     seed: int = 1000
     notes: str = field(default="", compare=False)
 
@@ -91,7 +92,13 @@ DEEP_CHAIN = Workload(
     Hkv=8, Dh=128, F=17408, ctx=16384, T=0.7, mode=STOCHASTIC,
     draft_noise_std0=0.75, noise_growth=1.5, seed=1005)
 
-WORKLOADS = {w.name: w for w in (TINY, SINGLE_GREEDY, BATCHED_STOCHASTIC, VERIFY_SWEEP, DEEP_CHAIN)}
+# Verification from the target's hidden states at the batched workload's shape:
+# 64 sequences, k = 3 (256 verified positions), hidden 4096, vocabulary 151936.
+FUSED_VERIFY = Workload(
+    "fused_verify_b64_k3_d4096_v151936", B=64, k=3, V=151936, d=4096, T=1.0, mode=STOCHASTIC,
+    draft_noise_std0=0.3, verify_only=True, fused=True, seed=1006)
+
+WORKLOADS = {w.name: w for w in (TINY, SINGLE_GREEDY, BATCHED_STOCHASTIC, VERIFY_SWEEP, DEEP_CHAIN, FUSED_VERIFY)}
 
 
 def with_k(w, k):
@@ -272,6 +279,19 @@ def draft_noise(w, positions):
     for j in range(positions):
         z[:, j] *= np.float32(w.draft_noise_std0 * (w.noise_growth ** j))
     return z
+
+
+def fused_inputs(w):
+    """Inputs of a verification from hidden states: head [V, d] bf16 N(0, w_std^2)
+    (the shared embedding of this seed), hidden [B, k+1, d] bf16 N(0, 1), the
+    draft's noise [B, k, V] float32 N(0, draft_noise_std0^2) and the uniforms.
+    The consumer forms draft = head . hidden + noise for the k draft
+    positions, and draws the draft tokens from q."""
+    out = {"head": to_bf16_bits(normal(w.seed, "w.E", (w.V, w.d), std=w.w_std)),
+           "hidden": to_bf16_bits(normal(w.seed, "hidden_target", (w.B, w.k + 1, w.d))),
+           "noise": normal(w.seed, "noise", (w.B, w.k, w.V), std=w.draft_noise_std0)}
+    out.update(make_uniforms(w))
+    return out
 
 
 def verify_inputs(w):

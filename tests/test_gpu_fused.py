@@ -45,12 +45,17 @@ def _inputs(B, k, V, d, T, seed, noise=0.5, hidden_std=1.0):
     return head, hidden, t, draft, dtok, u
 
 
+def _up256(n):
+    return (n + 255) // 256 * 256
+
+
 def _stored_logits(fv):
     """The stochastic call's fp32 logits [B (k+1), V] from its workspace: after
-    the 256-byte status slot and the per-(row, 256-token tile) partials."""
+    the 256-byte status slot, the per-(row, 256-token tile) partials of the
+    target rows and those of the draft rows."""
     Na = fv.B * (fv.k + 1)
     n_vt = (fv.V + VT - 1) // VT
-    off = 256 + (Na * n_vt * 16 + 255) // 256 * 256
+    off = 256 + _up256(Na * n_vt * 16) + _up256(fv.B * fv.k * n_vt * 16)
     raw = fv.ws[off:off + Na * fv.V * 4]
     return raw.view(torch.float32).view(Na, fv.V).cpu().numpy()
 
