@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(BUILD, "libmtpspec.so")
-SOURCES = ("api.cu", "draft.cu", "verify.cu", "tc.cu", "attn_tc.cu", "diag.cu", "fused.cu")
+SOURCES = ("api.cu", "draft.cu", "verify.cu", "tc.cu", "attn_tc.cu", "diag.cu", "fused.cu", "chain.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,5 +1,6 @@
 // C-ABI entry points of libmtpspec: argument validation, workspace layout and
 // the launch sequence of the draft chain and the verifier on one stream.
+#include <math.h>
 #include <stdlib.h>
 
 #include <atomic>
@@ -303,9 +304,72 @@ bool use_pdl() {
   return !(v && v[0] == '0');
 }
 
+// The GEMV path's ops in cooperative chain launches, when MTP_CHAIN=1:
+// [input projection, QKV] of depth 0, then per depth its attention and [output
+// projection, gate/up, down, LM head + draft selection] followed by the next
+// depth's [input projection, QKV].  Off by default: at the single-sequence
+// workload one launch per op, chained by programmatic dependent launch,
+// measured faster (1077 against 911 steps/s).
+bool use_chain(const Draft &D) {
+  const char *v = getenv("MTP_CHAIN");
+  if (!(v && v[0] == '1') || D.tc) return false;
+  const GemvPlan *ps[] = {&D.fc, &D.qkv, &D.wo, &D.gateup, &D.down, &D.lm};
+  for (const GemvPlan *p : ps)
+    if (!chain_op_ok(*p)) return false;
+  return true;
+}
+
+DraftCtx depth_ctx(const Draft &D, int j) {
+  DraftCtx c = D.c;
+  const int m = j < D.nmod ? j : D.nmod - 1;  // depth j runs module min(j, nmod - 1)
+  use_module(c, D.mods[m]);
+  c.j = j;
+  c.jc = j - m;
+  c.zero_counters = j == 0;
+  return c;
+}
+
+cudaError_t run_draft_chain(Draft &D, cudaStream_t s, bool pdl) {
+  cudaError_t e = cudaSuccess;
+  if (D.c.vmap && D.c.logits) {  // a reduced head writes only its ids: the rest of each row is -inf
+    e = launch_fill(D.c.logits, (size_t)D.c.B * D.c.k * D.c.V, -INFINITY, s, pdl);
+    if (e) return e;
+  }
+  ChainArgs a{};
+  a.bar = D.c.lm_cnt + 8;  // two words of the counters' slot
+  a.status = D.c.status;
+  a.c[0] = depth_ctx(D, 0);
+  a.c[1] = a.c[0];
+  a.ops[0] = ChainOp{OP_FC, 0, D.fc};
+  a.ops[1] = ChainOp{OP_QKV, 0, D.qkv};
+  a.nops = 2;
+  a.select_after = -1;
+  if ((e = timed(MTP_KC_GEMV, s, [&] { return launch_chain(a, s); }))) return e;
+  for (int j = 0; j < D.c.k; ++j) {
+    const DraftCtx cj = depth_ctx(D, j);
+    if ((e = timed(MTP_KC_ATTN, s, [&] { return launch_attention(cj, D.attn_cluster, s, pdl); }))) return e;
+    a.c[0] = cj;
+    a.ops[0] = ChainOp{OP_WO, 0, D.wo};
+    a.ops[1] = ChainOp{OP_GATEUP, 0, D.gateup};
+    a.ops[2] = ChainOp{OP_DOWN, 0, D.down};
+    a.ops[3] = ChainOp{OP_LMHEAD, 0, D.lm};
+    a.nops = 4;
+    a.select_after = 3;
+    if (j + 1 < D.c.k) {
+      a.c[1] = depth_ctx(D, j + 1);
+      a.ops[4] = ChainOp{OP_FC, 1, D.fc};
+      a.ops[5] = ChainOp{OP_QKV, 1, D.qkv};
+      a.nops = 6;
+    }
+    if ((e = timed(MTP_KC_LMHEAD, s, [&] { return launch_chain(a, s); }))) return e;
+  }
+  return e;
+}
+
 cudaError_t run_draft(Draft &D, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
   const bool pdl = use_pdl();
+  if (use_chain(D)) return run_draft_chain(D, s, pdl);
   if (D.c.vmap && D.c.logits) {  // a reduced head writes only its ids: the rest of each row is -inf
     e = launch_fill(D.c.logits, (size_t)D.c.B * D.c.k * D.c.V, -INFINITY, s, pdl);
     if (e) return e;

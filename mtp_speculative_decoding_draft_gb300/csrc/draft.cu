@@ -170,110 +170,9 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(DraftCtx c, GemvPlan
     }
     __syncthreads();
 
-    // epilogue for this batch group; the norm's scale(s) from the warps' sums
-    float sc0[BG], sc1[BG];
-#pragma unroll
-    for (int bb = 0; bb < BG; ++bb) {
-      sc0[bb] = 1.f;
-      sc1[bb] = 1.f;
-      if (fac) {
-        float t0 = 0.f, t1 = 0.f;
-        for (int w = 0; w < P; ++w) {
-          t0 += sq[(w * BG + bb) * 2];
-          t1 += sq[(w * BG + bb) * 2 + 1];
-        }
-        sc0[bb] = rsqrtf(t0 / (float)c.d + c.eps);
-        sc1[bb] = rsqrtf(t1 / (float)c.d + c.eps);
-      }
-    }
-    for (int rl = threadIdx.x; rl < nrows; rl += kGemvThreads) {
-      const int row = row0 + rl;
-      if (OP == OP_GATEUP && (rl & 1)) continue;
-#pragma unroll
-      for (int bb = 0; bb < BG; ++bb) {
-        const int b = grp * BG + bb;
-        if (b >= c.B) break;
-        float y = 0.f;
-        if (fac && OP == OP_FC) {  // pieces of the embedding half, then of the hidden half
-          float ye = 0.f, yx = 0.f;
-          for (int pp = 0; pp < P; ++pp) {
-            const float v = part[((size_t)rl * P + pp) * BG + bb];
-            if (pp * g.PC < c.d) ye += v;
-            else yx += v;
-          }
-          y = sc0[bb] * ye + sc1[bb] * yx;
-        } else {
-          for (int pp = 0; pp < P; ++pp) y += part[((size_t)rl * P + pp) * BG + bb];
-          if (fac) y *= sc0[bb];
-        }
-        if (OP == OP_FC) {
-          c.x0[(size_t)b * c.d + row] = y;
-        } else if (OP == OP_QKV) {
-          const int nq = c.Hq * c.Dh, nkv = c.Hkv * c.Dh;
-          if (row < nq) {
-            c.q[(size_t)b * nq + row] = y;
-          } else {
-            int r = row - nq;
-            uint16_t *cache = r < nkv ? c.kc : c.vc;
-            if (r >= nkv) r -= nkv;
-            const int kvh = r / c.Dh, dd = r % c.Dh;
-            int L = __ldg(&c.ctx_len[b]);
-            if (L < 0 || L + c.k > c.Lmax) set_status(c.status, kStatusBadCtx);
-            L = min(max(L, 0), c.Lmax - c.k);
-            const size_t idx = (((size_t)b * c.Hkv + kvh) * c.Lmax + L + c.jc) * c.Dh + dd;
-            cache[idx] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
-          }
-        } else if (OP == OP_WO) {
-          c.x1[(size_t)b * c.d + row] = __ldcg(&c.x0[(size_t)b * c.d + row]) + y;
-        } else if (OP == OP_GATEUP) {
-          float up = 0.f;
-          for (int pp = 0; pp < P; ++pp) up += part[((size_t)(rl + 1) * P + pp) * BG + bb];
-          if (fac) up *= sc0[bb];
-          c.act[(size_t)b * c.F + (row >> 1)] = silu_f(y) * up;
-        } else if (OP == OP_DOWN) {
-          c.x2[(size_t)b * c.d + row] = __ldcg(&c.x1[(size_t)b * c.d + row]) + y;
-        } else {  // LM head
-          if (c.logits) {
-            const int v = vocab_id(c, row);
-            if (v >= 0) c.logits[((size_t)b * c.k + c.j) * c.V + v] = y;
-          }
-          ys[(size_t)rl * BG + bb] = y;
-        }
-      }
-    }
-
-    if (OP == OP_LMHEAD) {
-      __syncthreads();
-      const float cT = kLog2e / c.T;
-      for (int bb = 0; bb < BG; ++bb) {
-        const int b = grp * BG + bb;
-        if (b >= c.B) break;
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-        for (int rl = threadIdx.x; rl < nrows; rl += kGemvThreads) argmax_merge(bv, bi, ys[(size_t)rl * BG + bb], row0 + rl);
-        warp_argmax(bv, bi);
-        __syncthreads();
-        if (lane == 0) {
-          red[warp] = bv;
-          red[kGemvWarps + warp] = __int_as_float(bi);
-        }
-        __syncthreads();
-        float m = -INFINITY;
-        int mi = 0x7fffffff;
-        for (int w = 0; w < kGemvWarps; ++w) argmax_merge(m, mi, red[w], __float_as_int(red[kGemvWarps + w]));
-        float s = 0.f;
-        if ((c.mode == 1 || c.k_eff) && m != -INFINITY)
-          for (int rl = threadIdx.x; rl < nrows; rl += kGemvThreads) s += exp2f((ys[(size_t)rl * BG + bb] - m) * cT);
-        s = block_sum_256(s, red + 2 * kGemvWarps);
-        if (threadIdx.x == 0) {
-          float *pp = c.lm_part + ((size_t)b * c.lm_grid + blockIdx.x) * 4;
-          pp[0] = m;
-          pp[1] = s;
-          pp[2] = __int_as_float(mi);
-          pp[3] = 0.f;
-        }
-      }
-    }
+    // epilogue for this batch group (the norm's scales, the op's outputs and,
+    // for the LM head, this CTA's partials)
+    gemv_epilogue<OP, BG>(c, P, g.PC, row0, nrows, grp, fac, part, sq, ys, red, (int)blockIdx.x);
     __syncthreads();
   }
 

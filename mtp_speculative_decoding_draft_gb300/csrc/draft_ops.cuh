@@ -208,6 +208,125 @@ __device__ __forceinline__ const uint16_t *weight_row(const DraftCtx &c, int row
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + __expf(-z)); }
 
 
+// The epilogue of one weight-streaming GEMV pass over batch group grp, run by
+// the whole CTA: every row's P piece sums (part, in shared memory), the input
+// norm's scale(s) from the warps' sums of squares (sq), the op's output -- x0;
+// q and the bf16 K/V append; x1 = x0 + y; the SwiGLU product; x2 = x1 + y; the
+// logits -- and, for the LM head, this CTA's (max, sum of exp2, argmax)
+// partial per sequence in lm_part[b][cta].  ys and red are shared scratch.
+template <int OP, int BG>
+__device__ void gemv_epilogue(const DraftCtx &c, int P, int PC, int row0, int nrows, int grp, bool fac,
+                              const float *part, const float *sq, float *ys, float *red, int cta) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  (void)PC;
+  // epilogue for this batch group; the norm's scale(s) from the warps' sums
+  float sc0[BG], sc1[BG];
+#pragma unroll
+  for (int bb = 0; bb < BG; ++bb) {
+    sc0[bb] = 1.f;
+    sc1[bb] = 1.f;
+    if (fac) {
+      float t0 = 0.f, t1 = 0.f;
+      for (int w = 0; w < P; ++w) {
+        t0 += sq[(w * BG + bb) * 2];
+        t1 += sq[(w * BG + bb) * 2 + 1];
+      }
+      sc0[bb] = rsqrtf(t0 / (float)c.d + c.eps);
+      sc1[bb] = rsqrtf(t1 / (float)c.d + c.eps);
+    }
+  }
+  for (int rl = threadIdx.x; rl < nrows; rl += kGemvThreads) {
+    const int row = row0 + rl;
+    if (OP == OP_GATEUP && (rl & 1)) continue;
+#pragma unroll
+    for (int bb = 0; bb < BG; ++bb) {
+      const int b = grp * BG + bb;
+      if (b >= c.B) break;
+      float y = 0.f;
+      if (fac && OP == OP_FC) {  // pieces of the embedding half, then of the hidden half
+        float ye = 0.f, yx = 0.f;
+        for (int pp = 0; pp < P; ++pp) {
+          const float v = part[((size_t)rl * P + pp) * BG + bb];
+          if (pp * PC < c.d) ye += v;
+          else yx += v;
+        }
+        y = sc0[bb] * ye + sc1[bb] * yx;
+      } else {
+        for (int pp = 0; pp < P; ++pp) y += part[((size_t)rl * P + pp) * BG + bb];
+        if (fac) y *= sc0[bb];
+      }
+      if (OP == OP_FC) {
+        c.x0[(size_t)b * c.d + row] = y;
+      } else if (OP == OP_QKV) {
+        const int nq = c.Hq * c.Dh, nkv = c.Hkv * c.Dh;
+        if (row < nq) {
+          c.q[(size_t)b * nq + row] = y;
+        } else {
+          int r = row - nq;
+          uint16_t *cache = r < nkv ? c.kc : c.vc;
+          if (r >= nkv) r -= nkv;
+          const int kvh = r / c.Dh, dd = r % c.Dh;
+          int L = __ldg(&c.ctx_len[b]);
+          if (L < 0 || L + c.k > c.Lmax) set_status(c.status, kStatusBadCtx);
+          L = min(max(L, 0), c.Lmax - c.k);
+          const size_t idx = (((size_t)b * c.Hkv + kvh) * c.Lmax + L + c.jc) * c.Dh + dd;
+          cache[idx] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+        }
+      } else if (OP == OP_WO) {
+        c.x1[(size_t)b * c.d + row] = __ldcg(&c.x0[(size_t)b * c.d + row]) + y;
+      } else if (OP == OP_GATEUP) {
+        float up = 0.f;
+        for (int pp = 0; pp < P; ++pp) up += part[((size_t)(rl + 1) * P + pp) * BG + bb];
+        if (fac) up *= sc0[bb];
+        c.act[(size_t)b * c.F + (row >> 1)] = silu_f(y) * up;
+      } else if (OP == OP_DOWN) {
+        c.x2[(size_t)b * c.d + row] = __ldcg(&c.x1[(size_t)b * c.d + row]) + y;
+      } else {  // LM head
+        if (c.logits) {
+          const int v = vocab_id(c, row);
+          if (v >= 0) c.logits[((size_t)b * c.k + c.j) * c.V + v] = y;
+        }
+        ys[(size_t)rl * BG + bb] = y;
+      }
+    }
+  }
+
+  if (OP == OP_LMHEAD) {
+    __syncthreads();
+    const float cT = kLog2e / c.T;
+    for (int bb = 0; bb < BG; ++bb) {
+      const int b = grp * BG + bb;
+      if (b >= c.B) break;
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int rl = threadIdx.x; rl < nrows; rl += kGemvThreads) argmax_merge(bv, bi, ys[(size_t)rl * BG + bb], row0 + rl);
+      warp_argmax(bv, bi);
+      __syncthreads();
+      if (lane == 0) {
+        red[warp] = bv;
+        red[kGemvWarps + warp] = __int_as_float(bi);
+      }
+      __syncthreads();
+      float m = -INFINITY;
+      int mi = 0x7fffffff;
+      for (int w = 0; w < kGemvWarps; ++w) argmax_merge(m, mi, red[w], __float_as_int(red[kGemvWarps + w]));
+      float s = 0.f;
+      if ((c.mode == 1 || c.k_eff) && m != -INFINITY)
+        for (int rl = threadIdx.x; rl < nrows; rl += kGemvThreads) s += exp2f((ys[(size_t)rl * BG + bb] - m) * cT);
+      s = block_sum_256(s, red + 2 * kGemvWarps);
+      // a launch wider than the LM head's plan (several ops in one launch) has
+      // CTAs without vocabulary rows: they own no partial slot
+      if (threadIdx.x == 0 && cta < c.lm_grid) {
+        float *pp = c.lm_part + ((size_t)b * c.lm_grid + cta) * 4;
+        pp[0] = m;
+        pp[1] = s;
+        pp[2] = __int_as_float(mi);
+        pp[3] = 0.f;
+      }
+    }
+  }
+}
+
 // Dynamic draft length: a sequence still drafting stops at this depth when the
 // draft's largest probability (1 / the partition sum relative to the largest
 // term) is below stop_p; it keeps the c.j drafts before this one.

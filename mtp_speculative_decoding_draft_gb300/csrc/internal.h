@@ -78,6 +78,26 @@ constexpr int kAttnThreads = 288;  // 8 compute warps and a K/V streaming warp
 constexpr int kMaxGroup = 8;        // Hq / Hkv
 
 GemvPlan plan_gemv(int op, int N, int K, int B, int num_sms);
+
+// Several GEMV ops in one cooperative launch (chain.cu): ops[o] runs op
+// ops[o].op of context c[ops[o].ctx] with plan ops[o].g, a grid barrier between
+// consecutive ops; the barrier after op select_after picks the draft token.
+constexpr int kMaxChainOps = 8;
+constexpr size_t kChainSmemCap = 110 * 1024;  // per CTA: two CTAs per SM
+struct ChainOp {
+  int op, ctx;
+  GemvPlan g;
+};
+struct ChainArgs {
+  DraftCtx c[2];
+  ChainOp ops[kMaxChainOps];
+  int nops, select_after;
+  int ring_bytes, part_floats, ys_floats;  // set by launch_chain
+  unsigned *bar;  // [0] arrivals, [1] generation: workspace words, zero before the first use
+  int *status;
+};
+bool chain_op_ok(const GemvPlan &g);
+cudaError_t launch_chain(ChainArgs a, cudaStream_t s);
 cudaError_t launch_gemv(const DraftCtx &c, const GemvPlan &g, cudaStream_t s, bool pdl);
 cudaError_t launch_attention(const DraftCtx &c, int cluster, cudaStream_t s, bool pdl);
 // p[0 .. n) = v (a reduced draft vocabulary's logits: -inf at the other ids)
