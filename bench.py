@@ -59,12 +59,12 @@ def lmhead_bytes(w, logits_out, head_rows=None):
 # are unchanged; the summaries of the captures are kept under profiles/.
 NCU_TRAFFIC = {
     ("lm_head_gemv", "single_greedy_b1_d4096_v151936_ctx4096"): {
-        "bytes": 1244772352 + 2795008,
+        "bytes": 1244772608 + 2793984,
         "sources": {
-            "csrc/draft.cu": "150a1fb1a79c6dc418cd759d08e2c0af891435de9b18f00a0d5bc4c80153bcf2",
-            "csrc/draft_ops.cuh": "02838a0228cd4eba3f617c4d99cab0d8f55f1b036294cb40b43d4b3e4160ca10",
-            "csrc/common.cuh": "fcd7bd8f56df32fc490b2c47f2fbc0f7f37047c578430d777438202c9279de66",
-            "csrc/internal.h": "36ac497104c59fe318924b19460d7557a45577223a255efc0f7534c05d38008d",
+            "csrc/draft.cu": "34b4d3651e4401a69bfbc02728f99a661ae9b365079eda9047ff2b0d50de1bd3",
+            "csrc/draft_ops.cuh": "ad62698d95aa35a07e07854a0daa62b73bffc314f886982abd3a02a0da033f38",
+            "csrc/common.cuh": "9c6db2af79ca058026581ad7509766387747f9f2081071a926314ddfcaaa4558",
+            "csrc/internal.h": "b5cdd7b6f37b6d3da52e697e9b5412db147f23f3f48a5181b9da5c8ab3be61c6",
         },
     },
     ("tc_gemm_kernel(LM head)", "batched_stochastic_b64_d4096_v151936_ctx1024-8192"): {
@@ -90,6 +90,15 @@ NCU_TRAFFIC = {
             "csrc/verify.cu": "f1d0b3ef5cf32a7d7279611da02f31cfe03a82a9ebe687965352321e233997f4",
             "csrc/common.cuh": "fcd7bd8f56df32fc490b2c47f2fbc0f7f37047c578430d777438202c9279de66",
             "csrc/internal.h": "36ac497104c59fe318924b19460d7557a45577223a255efc0f7534c05d38008d",
+        },
+    },
+    ("fv_gemm_kernel + fv_finish_kernel", "fused_verify_b64_k3_d4096_v151936/greedy"): {
+        "bytes": 1251173888 + 3772672,
+        "sources": {
+            "csrc/fused.cu": "860beae2657e823bf31ae8b401fc0936627cd8f9527797abca67c5395227a06a",
+            "csrc/tcgen05.cuh": "e128ff6d7c8451d618848063024b7cd0a98c722dd1b86ef0d04e6a07a9070ee7",
+            "csrc/common.cuh": "9c6db2af79ca058026581ad7509766387747f9f2081071a926314ddfcaaa4558",
+            "csrc/internal.h": "b5cdd7b6f37b6d3da52e697e9b5412db147f23f3f48a5181b9da5c8ab3be61c6",
         },
     },
 }
@@ -589,7 +598,9 @@ def run_fused_only(args, w, rank=0, world=1):
             "accept_len_mean": float(L.mean()), "acceptance": acceptance_metrics(L, w.k),
             "roofline": {"bound": "hbm", "kernel": "fv_gemm_kernel + fv_finish_kernel", "achieved": ach,
                          "peak": peak, "unit": "GB/s", "frac": ach / peak, "peak_kind": peak_kind,
-                         "traffic": None, "bytes_per_launch": fb, "avg_launch_ms": ms, "launches": args.steps,
+                         "traffic": ncu_traffic("fv_gemm_kernel + fv_finish_kernel",
+                                                "%s/%s" % (w.name, "stochastic" if w.mode == 1 else "greedy")),
+                         "bytes_per_launch": fb, "avg_launch_ms": ms, "launches": args.steps,
                          "tflops": res["tflops"], "tensor_frac": res["tensor_frac"]},
             "e2e": {"value": job_rate(e2e_ms, world), "unit": "verify calls/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},

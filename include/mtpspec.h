@@ -58,7 +58,9 @@ enum {
     MTP_STATUS_TIMEOUT = 1,    /* a bounded wait gave up; results of that call are invalid */
     MTP_STATUS_BAD_TOKEN = 2,  /* a token id outside [0, V); token 0 was used instead */
     MTP_STATUS_BAD_CTX = 4,    /* ctx_len[b] < 0 or ctx_len[b] + k > Lmax; clamped */
-    MTP_STATUS_NONFINITE = 8   /* a logit row without a finite maximum */
+    MTP_STATUS_NONFINITE = 8,  /* a logit row without a finite maximum */
+    MTP_STATUS_BOUNDS = 16     /* only a library built with MTP_BOUNDS: an index outside
+                                  its buffer was found and that access skipped */
 };
 
 typedef enum { MTP_GREEDY = 0, MTP_STOCHASTIC = 1 } MtpMode;

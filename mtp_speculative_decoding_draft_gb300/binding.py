@@ -11,7 +11,7 @@ import os
 
 import torch
 
-from .build import LIB
+from .build import library_path
 
 GREEDY = 0
 STOCHASTIC = 1
@@ -22,6 +22,7 @@ STATUS_TIMEOUT = 1
 STATUS_BAD_TOKEN = 2
 STATUS_BAD_CTX = 4
 STATUS_NONFINITE = 8
+STATUS_BOUNDS = 16
 
 
 class MtpError(RuntimeError):
@@ -54,9 +55,11 @@ _LIB = None
 def _lib():
     global _LIB
     if _LIB is None:
-        if not os.path.exists(LIB):
-            raise RuntimeError("libmtpspec.so is not built (%s); run __graft_entry__.build()" % LIB)
-        L = ctypes.CDLL(LIB)
+        lib = library_path()
+        if not os.path.exists(lib):
+            raise RuntimeError("%s is not built; run __graft_entry__.build() (or build(variant=...) for "
+                               "MTP_LIB_VARIANT)" % lib)
+        L = ctypes.CDLL(lib)
         P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         L.mtp_workspace_size.argtypes = [ctypes.POINTER(MtpDims), I]
         L.mtp_workspace_size.restype = Z

@@ -3,6 +3,11 @@
 Each CUDA translation unit is compiled in parallel, then linked into one shared
 library with the CUDA runtime linked statically.  ptxas resource usage
 (registers, spills, shared memory) is kept in _build/ptxas.log.
+
+variant="bounds" builds the bounds-checked library (-DMTP_BOUNDS: an index
+outside its buffer sets MTP_STATUS_BOUNDS and the access is skipped) into
+_build_bounds/libmtpspec_bounds.so; the binding loads it when the environment
+sets MTP_LIB_VARIANT=bounds.
 """
 
 import os
@@ -17,6 +22,18 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(BUILD, "libmtpspec.so")
+VARIANTS = {"": (BUILD, LIB, []),
+            "bounds": (os.path.join(PKG, "_build_bounds"),
+                       os.path.join(PKG, "_build_bounds", "libmtpspec_bounds.so"), ["-DMTP_BOUNDS"])}
+
+
+def library_path(variant=None):
+    """The shared library the binding loads: the default build, or the one
+    MTP_LIB_VARIANT names."""
+    v = os.environ.get("MTP_LIB_VARIANT", "") if variant is None else variant
+    if v not in VARIANTS:
+        raise RuntimeError("unknown MTP_LIB_VARIANT %r (known: %s)" % (v, ", ".join(repr(k) for k in VARIANTS)))
+    return VARIANTS[v][1]
 SOURCES = ("api.cu", "draft.cu", "verify.cu", "tc.cu", "attn_tc.cu", "diag.cu", "fused.cu", "chain.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -28,24 +45,26 @@ def nvcc():
     return exe
 
 
-def _needs_rebuild():
-    if not os.path.exists(LIB):
+def _needs_rebuild(lib):
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "mtpspec.h"), __file__]
     return any(os.path.getmtime(p) > t for p in deps)
 
 
-def build(force=False, verbose=False):
-    """Compile and link the library if any source is newer; return its path."""
-    if not force and not _needs_rebuild():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force=False, verbose=False, variant=""):
+    """Compile and link the library (the default one, or a variant) if any
+    source is newer; return its path."""
+    build_dir, lib, extra = VARIANTS[variant]
+    if not force and not _needs_rebuild(lib):
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
     flags = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
-             "-I", INCLUDE, "-I", CSRC] + ARCH
+             "-I", INCLUDE, "-I", CSRC] + ARCH + extra
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         cmd = [nvcc(), "-c", os.path.join(CSRC, src), "-o", obj] + flags
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, obj, r
@@ -57,18 +76,18 @@ def build(force=False, verbose=False):
         log.append("==== %s\n%s" % (src, r.stderr))
         if r.returncode != 0:
             raise RuntimeError("nvcc failed on %s:\n%s" % (src, r.stderr[-6000:]))
-    with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
+    with open(os.path.join(build_dir, "ptxas.log"), "w") as f:
         f.write("\n".join(log))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc(), "-shared", "-o", tmp] + [o for _, o, _ in results] + ARCH + ["-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s" % r.stderr[-6000:])
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     if verbose:
-        print("built", LIB, file=sys.stderr)
-    return LIB
+        print("built", lib, file=sys.stderr)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True)
+    build(force="--force" in sys.argv, verbose=True, variant="bounds" if "--bounds" in sys.argv else "")

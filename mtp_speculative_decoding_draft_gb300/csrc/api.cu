@@ -50,7 +50,6 @@ unsigned long long context_id() {
 
 namespace {
 
-constexpr int kMaxLmGrid = 2048;   // upper bound on LM-head CTAs (workspace sizing)
 constexpr size_t kAlign = 256;
 
 size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }

@@ -15,6 +15,7 @@ constexpr int kStatusTimeout = 1;
 constexpr int kStatusBadToken = 2;
 constexpr int kStatusBadCtx = 4;
 constexpr int kStatusNonFinite = 8;
+constexpr int kStatusBounds = 16;  // bounds-checked build: an index outside its buffer, access skipped
 
 // A wait that has not finished after this long gives up and flags the status.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -22,6 +23,18 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 __device__ __forceinline__ void set_status(int *status, int bits) {
   if (status) atomicOr(status, bits);
 }
+
+// Bounds-checked build (compiled with -DMTP_BOUNDS): an index outside its
+// buffer sets kStatusBounds in the status word and the access is skipped --
+// no trap, the context stays usable.  The default build checks nothing.
+#ifdef MTP_BOUNDS
+__device__ __forceinline__ bool in_bounds(bool ok, int *status) {
+  if (!ok) set_status(status, kStatusBounds);
+  return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool in_bounds(bool, int *) { return true; }
+#endif
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;

@@ -256,12 +256,12 @@ __device__ void gemv_epilogue(const DraftCtx &c, int P, int PC, int row0, int nr
         if (fac) y *= sc0[bb];
       }
       if (OP == OP_FC) {
-        c.x0[(size_t)b * c.d + row] = y;
+        if (in_bounds(row < c.d, c.status)) c.x0[(size_t)b * c.d + row] = y;
       } else if (OP == OP_QKV) {
         const int nq = c.Hq * c.Dh, nkv = c.Hkv * c.Dh;
         if (row < nq) {
           c.q[(size_t)b * nq + row] = y;
-        } else {
+        } else if (in_bounds(row < nq + 2 * nkv, c.status)) {
           int r = row - nq;
           uint16_t *cache = r < nkv ? c.kc : c.vc;
           if (r >= nkv) r -= nkv;
@@ -270,21 +270,22 @@ __device__ void gemv_epilogue(const DraftCtx &c, int P, int PC, int row0, int nr
           if (L < 0 || L + c.k > c.Lmax) set_status(c.status, kStatusBadCtx);
           L = min(max(L, 0), c.Lmax - c.k);
           const size_t idx = (((size_t)b * c.Hkv + kvh) * c.Lmax + L + c.jc) * c.Dh + dd;
-          cache[idx] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+          if (in_bounds(L + c.jc < c.Lmax && kvh < c.Hkv, c.status))
+            cache[idx] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
         }
       } else if (OP == OP_WO) {
-        c.x1[(size_t)b * c.d + row] = __ldcg(&c.x0[(size_t)b * c.d + row]) + y;
+        if (in_bounds(row < c.d, c.status)) c.x1[(size_t)b * c.d + row] = __ldcg(&c.x0[(size_t)b * c.d + row]) + y;
       } else if (OP == OP_GATEUP) {
         float up = 0.f;
         for (int pp = 0; pp < P; ++pp) up += part[((size_t)(rl + 1) * P + pp) * BG + bb];
         if (fac) up *= sc0[bb];
-        c.act[(size_t)b * c.F + (row >> 1)] = silu_f(y) * up;
+        if (in_bounds((row >> 1) < c.F, c.status)) c.act[(size_t)b * c.F + (row >> 1)] = silu_f(y) * up;
       } else if (OP == OP_DOWN) {
-        c.x2[(size_t)b * c.d + row] = __ldcg(&c.x1[(size_t)b * c.d + row]) + y;
+        if (in_bounds(row < c.d, c.status)) c.x2[(size_t)b * c.d + row] = __ldcg(&c.x1[(size_t)b * c.d + row]) + y;
       } else {  // LM head
         if (c.logits) {
           const int v = vocab_id(c, row);
-          if (v >= 0) c.logits[((size_t)b * c.k + c.j) * c.V + v] = y;
+          if (v >= 0 && in_bounds(v < c.V && c.j < c.k, c.status)) c.logits[((size_t)b * c.k + c.j) * c.V + v] = y;
         }
         ys[(size_t)rl * BG + bb] = y;
       }
@@ -316,7 +317,7 @@ __device__ void gemv_epilogue(const DraftCtx &c, int P, int PC, int row0, int nr
       s = block_sum_256(s, red + 2 * kGemvWarps);
       // a launch wider than the LM head's plan (several ops in one launch) has
       // CTAs without vocabulary rows: they own no partial slot
-      if (threadIdx.x == 0 && cta < c.lm_grid) {
+      if (threadIdx.x == 0 && cta < c.lm_grid && in_bounds(c.lm_grid <= kMaxLmGrid, c.status)) {
         float *pp = c.lm_part + ((size_t)b * c.lm_grid + cta) * 4;
         pp[0] = m;
         pp[1] = s;
@@ -445,7 +446,7 @@ __device__ inline void lm_select_warp(const DraftCtx &c, int G, int rpc) {
       tok = found != 0x7fffffff ? found : (lp >= 0 ? lp : Mi);
     }
     if (finite) tok = vocab_id(c, tok);  // head row -> vocabulary id
-    if (lane == 0) c.draft_tok[b * c.k + c.j] = tok;
+    if (lane == 0 && in_bounds(c.j < c.k, c.status)) c.draft_tok[b * c.k + c.j] = tok;
     if (lane == 0 && c.k_eff && finite) stop_check(c, b, 1.0 / Z);
   }
   if (lane == 0) *c.lm_cnt = 0u;

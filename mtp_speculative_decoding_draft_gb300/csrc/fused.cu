@@ -249,7 +249,8 @@ __global__ void __launch_bounds__(kFvThreads, 1) fv_gemm_kernel(const __grid_con
             }
           }
         }
-        if (valid) g.part[(size_t)row * g.n_vt + vt] = make_float4(M, MODE == 0 ? __int_as_float(I) : Ssum, 0.f, 0.f);
+        if (valid && in_bounds(vt < g.n_vt, g.status))
+          g.part[(size_t)row * g.n_vt + vt] = make_float4(M, MODE == 0 ? __int_as_float(I) : Ssum, 0.f, 0.f);
       }
       tc_fence_before();
       __syncwarp();

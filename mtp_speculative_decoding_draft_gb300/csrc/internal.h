@@ -73,6 +73,7 @@ struct GemvPlan {
 };
 
 constexpr int kGemvWarps = 8;
+constexpr int kMaxLmGrid = 2048;  // LM-head CTAs at most: the workspace holds that many partials per sequence
 constexpr int kGemvThreads = kGemvWarps * 32;
 constexpr int kAttnThreads = 288;  // 8 compute warps and a K/V streaming warp
 constexpr int kMaxGroup = 8;        // Hq / Hkv

@@ -410,8 +410,9 @@ __global__ void __launch_bounds__(kPrepThreads) tc_mid_kernel(DraftCtx c, TcBufs
         if (rr >= nkv) rr -= nkv;
         const int kvh = rr / c.Dh, dd = rr % c.Dh;  // 8 | Dh: the eight stay in one head
         uint16_t *dst = cache + (((size_t)b * c.Hkv + kvh) * c.Lmax + L + c.jc) * c.Dh + dd;
+        if (in_bounds(L + c.jc < c.Lmax && kvh < c.Hkv && dd + 8 <= c.Dh, c.status))
 #pragma unroll
-        for (int q = 0; q < 8; ++q) dst[q] = __bfloat16_as_ushort(__float2bfloat16_rn(y[q]));
+          for (int q = 0; q < 8; ++q) dst[q] = __bfloat16_as_ushort(__float2bfloat16_rn(y[q]));
       }
     }
     return;
@@ -522,7 +523,7 @@ __global__ void __launch_bounds__(kSelThreads) tc_select_part_kernel(DraftCtx c,
     for (int i = 0; i < 32; ++i) sum += exp2f(fmaf(x[i], cT, -mc));
     sum = warp_sum(sum);
   }
-  if (lane == 0) part[(size_t)b * nq + q] = make_float4(M, __int_as_float(I), sum, 0.f);
+  if (lane == 0 && in_bounds(b < c.B && q < nq, c.status)) part[(size_t)b * nq + q] = make_float4(M, __int_as_float(I), sum, 0.f);
 }
 
 __global__ void __launch_bounds__(32) tc_select_fin_kernel(DraftCtx c, const float *logits, size_t bstride,
@@ -630,7 +631,7 @@ __global__ void __launch_bounds__(32) tc_select_fin_kernel(DraftCtx c, const flo
     tok = found != 0x7fffffff ? found : (lastpos >= 0 ? lastpos : I);
   }
   if (finite) tok = vocab_id(c, tok);  // head row -> vocabulary id
-  if (lane == 0) c.draft_tok[b * c.k + c.j] = tok;
+  if (lane == 0 && in_bounds(b < c.B && c.j < c.k, c.status)) c.draft_tok[b * c.k + c.j] = tok;
   if (lane == 0 && c.k_eff && finite) stop_check(c, b, 1.0 / Z);
 }
 

@@ -385,6 +385,7 @@ __device__ __forceinline__ ItemInfo decode(const VerifyArgs &a, unsigned idx) {
   const unsigned B = (unsigned)a.B;
   it.j = (int)(idx / B);
   it.b = (int)(idx % B);
+  if (!in_bounds(it.j <= a.k && it.b < a.B, a.status)) return it;  // a stop item
   it.kb = a.k;
   if (a.k_eff) it.kb = min(max(__ldcg(&a.k_eff[it.b]), 0), a.k);
   if (a.mode == 0 || it.j > it.kb) it.kind = kItemGreedy;
@@ -773,6 +774,7 @@ __device__ void record(const VerifyArgs &a, int b, int j, int kb, int word, int 
   const int lane = threadIdx.x & 31, k = a.k, V = a.V;
   unsigned long long *rb = a.rec + (size_t)b * (k + 1);
   const unsigned long long mine = ((unsigned long long)(unsigned)tok << 32) | (unsigned)(word | kRecWritten);
+  if (!in_bounds(b < a.B && j <= k, a.status)) return;
   if (j != last_position(a)) {
     if (lane == 0) st_relaxed_u64(rb + j, mine);
     return;

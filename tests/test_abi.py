@@ -101,3 +101,16 @@ def test_variant_arguments_are_checked_on_the_host(lib):
 
     assert reduced(128) == -3 and reduced(5003) == -3
     assert reduced(127) == -1 and reduced(5004) == -1      # 128 <= N <= V
+
+
+def test_noalloc_limit_counts_the_draft_only_layout(lib):
+    """mtp_draft_noalloc keeps no logits and no verifier state in its scratch:
+    at d 4096, F 12288, V 151936 a batch of 4 passes the 4 MiB limit (and then
+    fails on its missing weights, before any device work) while a batch of 5,
+    which takes the tensor-core path's buffers, is refused."""
+    from mtp_speculative_decoding_draft_gb300 import binding as bd
+    L = bd.library()
+    for B, want in ((4, -1), (5, -5)):
+        dims = bd.make_dims(B, 4096, 32, 8, 128, 12288, 151936, 4099)
+        assert L.mtp_draft_noalloc(ctypes.byref(dims), None, None, None, None, None, None, 3, 1.0, 0, None, None,
+                                   None, None, None) == want
