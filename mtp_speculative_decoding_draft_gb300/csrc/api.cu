@@ -8,6 +8,7 @@
 #include <vector>
 
 #include <cuda.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "internal.h"
 #include "mtpspec.h"
@@ -365,15 +366,43 @@ cudaError_t run_draft_chain(Draft &D, cudaStream_t s, bool pdl) {
   return e;
 }
 
+// NVTX ranges around each call and each depth's launches (MTP_NVTX=1; the
+// header-only NVTX API costs nothing unless a profiling tool is attached).
+bool use_nvtx() {
+  static const bool on = [] {
+    const char *v = getenv("MTP_NVTX");
+    return v && v[0] == '1';
+  }();
+  return on;
+}
+
+struct NvtxRange {
+  bool on;
+  explicit NvtxRange(const char *name) : on(use_nvtx()) {
+    if (on) nvtxRangePushA(name);
+  }
+  ~NvtxRange() {
+    if (on) nvtxRangePop();
+  }
+};
+
+const char *depth_name(int j) {
+  static const char *names[8] = {"mtp depth 0", "mtp depth 1", "mtp depth 2", "mtp depth 3",
+                                 "mtp depth 4", "mtp depth 5", "mtp depth 6", "mtp depth 7"};
+  return names[j & 7];
+}
+
 cudaError_t run_draft(Draft &D, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
   const bool pdl = use_pdl();
+  NvtxRange call_range("mtp_draft chain");
   if (use_chain(D)) return run_draft_chain(D, s, pdl);
   if (D.c.vmap && D.c.logits) {  // a reduced head writes only its ids: the rest of each row is -inf
     e = launch_fill(D.c.logits, (size_t)D.c.B * D.c.k * D.c.V, -INFINITY, s, pdl);
     if (e) return e;
   }
   for (int j = 0; j < D.c.k && e == cudaSuccess; ++j) {
+    NvtxRange depth_range(depth_name(j));
     DraftCtx c = D.c;
     // depth j runs module min(j, nmod - 1), at the next row of that module's cache
     const int m = j < D.nmod ? j : D.nmod - 1;
@@ -585,6 +614,7 @@ int spec_verify_dynamic(int B, int k, int V, float T, int mode, const float *tar
   if (rc) return rc;
   a.status = static_cast<int *>(ws);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  NvtxRange r("spec verify");
   cudaError_t e = timed(MTP_KC_VERIFY, s, [&] { return launch_verify(a, s, false); });
   if (e == cudaSuccess) e = cudaGetLastError();
   return cuda_rc(e);
@@ -616,7 +646,10 @@ static int step_call(const MtpDims *dims, const MtpModule *modules, int n_module
   a.status = D.c.status;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = run_draft(D, s);
-  if (e == cudaSuccess) e = timed(MTP_KC_VERIFY, s, [&] { return launch_verify(a, s, use_pdl()); });
+  if (e == cudaSuccess) {
+    NvtxRange r("spec verify");
+    e = timed(MTP_KC_VERIFY, s, [&] { return launch_verify(a, s, use_pdl()); });
+  }
   if (e == cudaSuccess) e = cudaGetLastError();
   return cuda_rc(e);
 }
@@ -703,6 +736,7 @@ int spec_verify_fused(int B, int k, int V, int d, float T, int mode, const void 
   fc.out_tok = out_tok; fc.accept_len = accept_len; fc.num_accepted = num_accepted;
   fc.ws = ws;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  NvtxRange r("spec verify fused");
   cudaError_t e = timed(MTP_KC_VERIFY, s, [&] { return launch_fused_verify(fc, s, use_pdl()); });
   if (e == cudaSuccess) e = cudaGetLastError();
   return cuda_rc(e);
