@@ -34,7 +34,8 @@ def library_path(variant=None):
     if v not in VARIANTS:
         raise RuntimeError("unknown MTP_LIB_VARIANT %r (known: %s)" % (v, ", ".join(repr(k) for k in VARIANTS)))
     return VARIANTS[v][1]
-SOURCES = ("api.cu", "draft.cu", "verify.cu", "tc.cu", "attn_tc.cu", "diag.cu", "fused.cu", "chain.cu")
+SOURCES = ("api.cu", "draft.cu", "verify.cu", "verify_split.cu", "tc.cu", "attn_tc.cu", "diag.cu", "fused.cu",
+           "chain.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -304,6 +304,14 @@ bool use_pdl() {
   return !(v && v[0] == '0');
 }
 
+// Stochastic verification by the streaming kernel of verify_split.cu (the
+// default; MTP_VERIFY_SPLIT=0 takes the cluster kernel of verify.cu, which
+// greedy verification always takes).
+bool use_verify_split() {
+  const char *v = getenv("MTP_VERIFY_SPLIT");
+  return !(v && v[0] == '0');
+}
+
 // The GEMV path's ops in cooperative chain launches, when MTP_CHAIN=1:
 // [input projection, QKV] of depth 0, then per depth its attention and [output
 // projection, gate/up, down, LM head + draft selection] followed by the next
@@ -454,6 +462,7 @@ int prepare_verify(int B, int k, int V, float T, int mode, const float *target, 
   a->k_eff = k_eff;
   if (!plan_verify(B, k, V, &a->p)) return MTP_ERR_UNSUPPORTED_SHAPE;
   verify_bind_state(*a, state);
+  a->split = mode == MTP_STOCHASTIC && use_verify_split() && split_shape_ok(B, k, V);
   return MTP_OK;
 }
 

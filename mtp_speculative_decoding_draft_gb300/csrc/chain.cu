@@ -39,16 +39,6 @@ namespace {
 
 constexpr int kRingSlots = 8;  // pieces in flight per warp, at most
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_release_u32(unsigned *p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 // Runtime form of weight_row<OP>.
 __device__ __forceinline__ const uint16_t *op_weight_row(const DraftCtx &c, int op, int row, int K) {
   switch (op) {

@@ -82,12 +82,6 @@ struct FvOut {
 
 namespace {
 
-// 2^x, hardware approximation (relative error about 2^-22; -inf gives +0).
-__device__ __forceinline__ float ex2f(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 }  // namespace
 
@@ -222,7 +216,7 @@ __global__ void __launch_bounds__(kFvThreads, 1) fv_gemm_kernel(const __grid_con
             for (int t = 0; t < 32; ++t)
               if (t < nv) cm = fmaxf(cm, v[t]);
             if (cm > M) {
-              if (M != -INFINITY) Ssum *= ex2f((M - cm) * c);
+              if (M != -INFINITY) Ssum *= ex2_approx((M - cm) * c);
               M = cm;
             }
             if (M != -INFINITY) {
@@ -230,8 +224,8 @@ __global__ void __launch_bounds__(kFvThreads, 1) fv_gemm_kernel(const __grid_con
               float s0 = 0.f, s1 = 0.f;
 #pragma unroll
               for (int t = 0; t < 32; t += 2) {
-                if (t < nv) s0 += ex2f(fmaf(v[t], c, -mc));
-                if (t + 1 < nv) s1 += ex2f(fmaf(v[t + 1], c, -mc));
+                if (t < nv) s0 += ex2_approx(fmaf(v[t], c, -mc));
+                if (t + 1 < nv) s1 += ex2_approx(fmaf(v[t + 1], c, -mc));
               }
               Ssum += s0 + s1;
             }
@@ -300,7 +294,7 @@ __global__ void __launch_bounds__(256) fv_draft_stats_kernel(const FvArgs g) {
     if (m != -INFINITY) {
       const float mc = m * g.c;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) s += ex2f(fmaf(x[i], g.c, -mc));
+      for (int i = 0; i < 8; ++i) s += ex2_approx(fmaf(x[i], g.c, -mc));
     }
     s = warp_sum(s);
     if (lane == 0) g.dpart[(size_t)r * g.n_vt + t] = make_float4(m, s, 0.f, 0.f);
@@ -338,11 +332,11 @@ struct Wt {
 };
 
 __device__ __forceinline__ float wval(const Wt &w, float t, float l) {
-  const float e = ex2f((t - w.Mt) * w.c);
+  const float e = ex2_approx((t - w.Mt) * w.c);
   if (w.kind == 2) return e;
   const float p = e * w.iZt;
   if (w.kind == 1) return p;
-  return fmaxf(0.f, p - ex2f((l - w.Ml) * w.c) * w.iZl);
+  return fmaxf(0.f, p - ex2_approx((l - w.Ml) * w.c) * w.iZl);
 }
 
 // Row j's (max, partition sum relative to it) from its per-tile partials, in
@@ -364,17 +358,17 @@ __device__ __forceinline__ void combine_lse(const float4 *pp, int n_vt, float c,
 #pragma unroll
     for (int i = 1; i < 8; ++i) bm = fmaxf(bm, p[i].x);
     if (bm > m) {
-      if (m != -INFINITY) z *= (double)ex2f((m - bm) * c);
+      if (m != -INFINITY) z *= (double)ex2_approx((m - bm) * c);
       m = bm;
     }
     if (m != -INFINITY)
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        if (p[i].x != -INFINITY) z += (double)p[i].y * (double)ex2f((p[i].x - m) * c);
+        if (p[i].x != -INFINITY) z += (double)p[i].y * (double)ex2_approx((p[i].x - m) * c);
   }
   // lanes: rescale to the warp maximum, then sum in a fixed tree
   const float wm = warp_max(m);
-  z = (m == -INFINITY) ? 0.0 : z * (double)ex2f((m - wm) * c);
+  z = (m == -INFINITY) ? 0.0 : z * (double)ex2_approx((m - wm) * c);
   M = wm;
   Z = warp_sum_d(z);
 }
@@ -458,7 +452,7 @@ __device__ void chunk_masses_from_partials(FinShared &sh, const float4 *pp, int 
     double s = 0.0;
     for (int t = ch * tiles_per_chunk; t < min(n_vt, (ch + 1) * tiles_per_chunk); ++t) {
       const float4 p = __ldcg(&pp[t]);
-      if (p.x != -INFINITY) s += (double)p.y * (double)ex2f((p.x - w.Mt) * w.c);
+      if (p.x != -INFINITY) s += (double)p.y * (double)ex2_approx((p.x - w.Mt) * w.c);
     }
     sh.csum[ch] = w.kind == 1 ? s * (double)w.iZt : s;
   }

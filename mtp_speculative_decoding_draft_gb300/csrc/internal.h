@@ -141,6 +141,12 @@ struct VerifyPlan {
   unsigned total;  // work items: one per position of one sequence
 };
 
+// A sequence's first rejection, for the residual draw of verify_split.cu.
+struct alignas(16) SplitRec {
+  float Mt, iZt, Ml, iZl;  // target / draft row max and inverse partition sum
+  int j, flags, pad0, pad1;
+};
+
 struct VerifyArgs {
   int B, k, V, mode;
   float T;
@@ -159,6 +165,16 @@ struct VerifyArgs {
   unsigned *hint;        // [B] k + 1 - (earliest position known to reject), or 0
   unsigned long long *rec;  // [B, k+1] per position: flags | token << 32, 0 until written
   VerifyPlan p;
+  // the ticketed stochastic kernel (verify_split.cu), when split is set
+  int split;
+  int snch;                // 32768-element chunks a row
+  int sNA, sNB, sD;        // statistics / residual items a sequence; lag of the residual group in sequences
+  int shint;               // L2 policy: 0 normal; 1 pair rows evict_last, the rest evict_first; 2 pair rows normal
+  unsigned *sseq;          // [B, 4] statistics arrivals, residual arrivals, decision, -- (state: zero, left zero)
+  SplitRec *srec;          // [B] the rejection each sequence's residual items draw from
+  float2 *spart;           // [B, 2k+1, snch] chunk (max, sum of exp2)
+  double *cmass;           // [B, snch] residual chunk masses
+  float *smass;            // [B, snch, 64] residual masses of the chunks' 512-element sub-chunks
 };
 
 size_t verify_state_bytes(int B, int k, int V);
@@ -166,6 +182,11 @@ void verify_bind_state(VerifyArgs &a, void *state);
 bool plan_verify(int B, int k, int V, VerifyPlan *p);
 cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s, bool pdl);
 cudaError_t verify_set_attributes();
+int split_chunks(int V);
+bool split_shape_ok(int B, int k, int V);
+size_t split_state_bytes(int B, int k, int V);
+void split_bind_state(VerifyArgs &a, void *state, int lag_items);
+cudaError_t launch_verify_split(const VerifyArgs &a, cudaStream_t s, bool pdl);
 
 // Verification from the target's hidden states (fused.cu).
 struct FusedCall {

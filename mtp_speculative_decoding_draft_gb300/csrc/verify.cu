@@ -197,22 +197,16 @@ __device__ bool wait_phase(uint64_t *bar, uint32_t parity, int *status) {
   }
 }
 
-// 2^x, hardware approximation (relative error about 2^-22; -inf gives +0).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 // Sampling weight of one element: residual max(0, p - q) (kind 0), target p
 // (kind 1), unnormalised target weight exp2((t - Mt) c) (kind 2).
 __device__ __forceinline__ float weight(int kind, float t, float l, float Mt, float Ml, float iZt, float iZl,
                                         float c) {
-  const float e = ex2((t - Mt) * c);
+  const float e = ex2_approx((t - Mt) * c);
   if (kind == 2) return e;
   const float p = e * iZt;
   if (kind == 1) return p;
-  return fmaxf(0.f, p - ex2((l - Ml) * c) * iZl);
+  return fmaxf(0.f, p - ex2_approx((l - Ml) * c) * iZl);
 }
 
 __device__ __forceinline__ double warp_incl_scan_d(double v) {
@@ -327,8 +321,8 @@ __device__ __forceinline__ float lane_sumexp16(const float (&x)[16], float M, fl
   float s0 = 0.f, s1 = 0.f;
 #pragma unroll
   for (int i = 0; i < 16; i += 2) {
-    s0 += ex2(fmaf(x[i], c, -mc));
-    s1 += ex2(fmaf(x[i + 1], c, -mc));
+    s0 += ex2_approx(fmaf(x[i], c, -mc));
+    s1 += ex2_approx(fmaf(x[i + 1], c, -mc));
   }
   return s0 + s1;
 }
@@ -875,8 +869,8 @@ __device__ void decider(const VerifyArgs &a, Shared &sh, int d, int rank, int C,
       double z0 = 0.0, z1 = 0.0;
       for (int p = lane; p < P; p += 32) {
         const float4 q = ss.stats[p];
-        if (q.x != -INFINITY) z0 += (double)q.y * (double)ex2((q.x - m0) * c);
-        if (pair && q.z != -INFINITY) z1 += (double)q.w * (double)ex2((q.z - m1) * c);
+        if (q.x != -INFINITY) z0 += (double)q.y * (double)ex2_approx((q.x - m0) * c);
+        if (pair && q.z != -INFINITY) z1 += (double)q.w * (double)ex2_approx((q.z - m1) * c);
       }
       mine.z0 = warp_sum_d(z0);
       mine.z1 = warp_sum_d(z1);
@@ -897,8 +891,8 @@ __device__ void decider(const VerifyArgs &a, Shared &sh, int d, int rank, int C,
       continue;
     }
     const float M0 = warp_max(xr.m0), M1 = warp_max(xr.m1);
-    const double Z0 = warp_sum_d(lane < C && xr.m0 != -INFINITY ? xr.z0 * (double)ex2((xr.m0 - M0) * c) : 0.0);
-    const double Z1 = warp_sum_d(lane < C && xr.m1 != -INFINITY ? xr.z1 * (double)ex2((xr.m1 - M1) * c) : 0.0);
+    const double Z0 = warp_sum_d(lane < C && xr.m0 != -INFINITY ? xr.z0 * (double)ex2_approx((xr.m0 - M0) * c) : 0.0);
+    const double Z1 = warp_sum_d(lane < C && xr.m1 != -INFINITY ? xr.z1 * (double)ex2_approx((xr.m1 - M1) * c) : 0.0);
     const unsigned hint0 = (unsigned)__shfl_sync(kFull, xr.i0, 0);
     const float td = __shfl_sync(kFull, v, 0), ldv = __shfl_sync(kFull, v, 1);
     const float ua = __shfl_sync(kFull, v, 2), uf = __shfl_sync(kFull, v, 3);
@@ -930,7 +924,7 @@ __device__ void decider(const VerifyArgs &a, Shared &sh, int d, int rank, int C,
     const float iZt = (float)(1.0 / Z0), iZl = pair ? (float)(1.0 / Z1) : 0.f;
     auto bonus_mass = [&](int p) -> double {
       const float4 q = ss.stats[p];
-      return q.x == -INFINITY ? 0.0 : (double)q.y * (double)ex2((q.x - Mt) * c);
+      return q.x == -INFINITY ? 0.0 : (double)q.y * (double)ex2_approx((q.x - Mt) * c);
     };
     Xchg mine2 = none2;
     const int p0 = 2 * lane, p1 = 2 * lane + 1;
@@ -1102,10 +1096,10 @@ int max_clusters(int C) {
 }  // namespace
 
 size_t verify_state_bytes(int B, int k, int V) {
-  (void)V;
   size_t n = 256;                       // claim / exit counters
   n += up256((size_t)B * 4);            // rejection hints
   n += up256((size_t)B * (k + 1) * 8);  // per-position records
+  n += split_state_bytes(B, k, V);      // the ticketed stochastic kernel's
   return n;
 }
 
@@ -1116,6 +1110,10 @@ void verify_bind_state(VerifyArgs &a, void *state) {
   a.hint = reinterpret_cast<unsigned *>(p);
   p += up256((size_t)a.B * 4);
   a.rec = reinterpret_cast<unsigned long long *>(p);
+  p += up256((size_t)a.B * (a.k + 1) * 8);
+  // residual items start about this many 128 KB items after their sequence's statistics
+  split_bind_state(a, p, (int)std::max(1ll, std::min(1ll << 20, env_int("MTP_SPLIT_LAG", 256))));
+  a.shint = (int)std::max(0ll, std::min(2ll, env_int("MTP_SPLIT_HINT", 1)));
 }
 
 bool plan_verify(int B, int k, int V, VerifyPlan *p) {
@@ -1144,6 +1142,7 @@ cudaError_t verify_set_attributes() {
 }
 
 cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s, bool pdl) {
+  if (a.split) return launch_verify_split(a, s, pdl);
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)(a.p.G * a.p.C));
   cfg.blockDim = dim3(kVerifyThreads);

@@ -1,0 +1,54 @@
+"""GPU parity of stochastic verification on both of its kernels.
+
+Stochastic spec_verify runs on the streaming kernel (one CTA per chunk of
+32768 logits; the CTA that completes a sequence decides and draws) unless
+MTP_VERIFY_SPLIT=0 selects the cluster kernel.  The main verify tests run the
+default; here the cluster kernel gets the same stochastic checks, and both
+get vocabularies that span several 32768-element chunks with ragged tails,
+unaligned rows and a one-element last chunk."""
+
+import numpy as np
+import pytest
+
+from mtp_speculative_decoding_draft_gb300 import workloads as W
+from test_gpu_verify import STOCH, _case, _check, _draft_tokens_from_q
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(params=["split", "cluster"])
+def kernel(request, monkeypatch):
+    monkeypatch.setenv("MTP_VERIFY_SPLIT", "1" if request.param == "split" else "0")  # read at every call
+    return request.param
+
+
+@pytest.mark.parametrize("B,k,V,T", [(7, 3, 2 * 32768 + 5, 0.9),   # odd V: unaligned rows, ragged tail
+                                     (3, 2, 3 * 32768, 1.0),       # whole chunks only
+                                     (5, 4, 32768 + 1, 1.2),       # a one-element last chunk
+                                     (37, 3, 5003, 1.0),           # one ragged chunk
+                                     (3, 8, 777, 1.0)])            # the deepest draft
+def test_stochastic_multi_chunk(kernel, B, k, V, T):
+    t, l, d, ua, uf = _case(B, k, V, T, seed=7700 + B * 10 + k)
+    exc, L = _check(t, l, d, ua, uf, STOCH, T)
+    assert L.min() >= 1
+
+
+def test_stochastic_everything_accepted(kernel):
+    """draft == target: every draft is accepted, so the bonus draw (from the
+    chunk statistics, then one chunk's sub-chunks) makes every emitted token."""
+    rng = np.random.default_rng(77)
+    B, k, V = 12, 3, 2 * 32768 + 1000
+    t = (rng.standard_normal((B, k + 1, V)) * 3).astype(np.float32)
+    d = rng.integers(0, V, size=(B, k)).astype(np.int32)
+    ua = rng.random((B, k)).astype(np.float32)
+    uf = rng.random(B).astype(np.float32)
+    exc, L = _check(t, t[:, :k].copy(), d, ua, uf, STOCH, 1.0)
+    assert np.all(L == k + 1)
+
+
+def test_stochastic_sweep_k3_full_size(kernel):
+    w = W.with_k(W.VERIFY_SWEEP, 3)
+    inp = W.verify_inputs(w)
+    d = _draft_tokens_from_q(inp["draft_logits"], inp["u_draft"], w.T)
+    exc, L = _check(inp["target_logits"], inp["draft_logits"], d, inp["u_accept"], inp["u_final"], STOCH, w.T)
+    print("%s kernel: mean accepted length %.3f, excused %d" % (kernel, L.mean(), exc))
