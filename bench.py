@@ -870,6 +870,52 @@ def run_secondary(peak, steps=SECONDARY_STEPS, warmup=5):
     return out
 
 
+def print_trace(step, n_steps, torch, bd):
+    """Diagnostic (--trace N): run N steps with the launch-tracing library and
+    print the live kernel timeline -- per launch its start, dependency release
+    and end on the GPU's global timer -- for the last step, and per kernel kind
+    the mean time it adds to the timeline (its end past everything before it)."""
+    bd.trace_read()                      # drop the warm-up's records
+    n0 = bd.launch_count()
+    for _ in range(n_steps):
+        step()
+    torch.cuda.synchronize()
+    per_step = (bd.launch_count() - n0) // n_steps
+    recs = bd.trace_read()
+    if not recs or per_step < 1:
+        raise SystemExit("no trace records: run with the trace build (MTP_LIB_VARIANT=trace)")
+    t_first = recs[0]["start"]
+    cur = t_first
+    agg = {}
+    for r in recs:
+        excl = max(0, r["end"] - max(r["start"], cur))
+        gap = max(0, r["start"] - cur)
+        cur = max(cur, r["end"])
+        a = agg.setdefault(r["name"], [0, 0.0, 0.0, 0.0, 0.0])
+        a[0] += 1
+        a[1] += r["end"] - r["start"]
+        a[2] += (r["end"] - r["dep"]) if r["dep"] else 0.0
+        a[3] += excl
+        a[4] += gap
+    total = cur - t_first
+    print("traced %d steps, %d launches, %.1f us per step" % (n_steps, len(recs), total / 1e3 / n_steps))
+    print("%-28s %6s %10s %12s %12s %10s" % ("kernel", "count", "span us", "after dep us", "adds us", "gap us"))
+    for name, (n, span, dep, excl, gap) in sorted(agg.items(), key=lambda kv: -kv[1][3]):
+        print("%-28s %6d %10.2f %12.2f %12.2f %10.2f" % (name, n, span / n / 1e3, dep / n / 1e3, excl / n / 1e3,
+                                                         gap / n / 1e3))
+    last = recs[-per_step:]
+    t0 = last[0]["start"]
+    print("\nlast step (us from its first launch's start; marks: the kernel's intermediate points)")
+    print("%-28s %9s %9s %9s %9s   %s" % ("kernel", "start", "dep", "end", "span", "marks"))
+
+    def rel(t):
+        return "%9.2f" % ((t - t0) / 1e3) if t else "%9s" % "-"
+    for r in last:
+        print("%-28s %s %s %s %9.2f   %s" % (r["name"], rel(r["start"]), rel(r["dep"]), rel(r["end"]),
+                                            (r["end"] - r["start"]) / 1e3,
+                                            " ".join(rel(m).strip() for m in r["marks"] if m)))
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -943,6 +989,8 @@ def run_ours(args):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    if args.trace:
+        return print_trace(step, args.trace, torch, bd)
     graph, graph_launches = None, 0
     if args.graph:
         # one step captured in a CUDA graph (after the warm-up above, on a side
@@ -1128,9 +1176,17 @@ def main():
                          "i.i.d. N(0, 16); 0 = off")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of one step captured in a CUDA graph instead of direct calls")
+    ap.add_argument("--trace", type=int, default=0, metavar="N",
+                    help="diagnostic: run N steps on the launch-tracing build and print the live kernel "
+                         "timeline instead of the JSON line")
     ap.add_argument("--modules", type=int, default=1,
                     help="distinct draft modules (depth j runs module min(j, modules-1)); 1 = one reused module")
     args = ap.parse_args()
+    if args.trace:
+        # the launch-tracing library, built and selected before the binding loads one
+        from mtp_speculative_decoding_draft_gb300.build import build
+        build(variant="trace")
+        os.environ["MTP_LIB_VARIANT"] = "trace"
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":

@@ -420,6 +420,51 @@ int mtp_profiler_enable(int on);
 int mtp_profiler_read(int kernel_class, double *total_ms, int64_t *launches);
 int64_t mtp_launch_count(void);
 
+/*
+ * Launch trace, for the library built with MTP_TRACE (build variant "trace",
+ * loaded by the binding when MTP_LIB_VARIANT=trace).  Every kernel records,
+ * on the GPU's global nanosecond timer, when its first CTA started, when the
+ * first CTA got past its wait for the previous kernel (programmatic dependent
+ * launch; 0 where the kernel does not record it), when the last CTA reached
+ * each of up to four intermediate points of the kernel (the GEMV: activations
+ * loaded, last weight piece used, epilogue done; tensor-core attention: query
+ * staged, last tile done, CTA merged, cluster combined) and when the last CTA
+ * finished.  Unlike the event profiler above it leaves the launch chain
+ * intact, so it shows the live overlap of the chained kernels.
+ *
+ * mtp_trace_read() copies up to max_entries records (in no particular order)
+ * into `entries` (host memory, owned by the caller) and clears the device
+ * buffers.  Call it once the traced work has completed (after a device or
+ * stream synchronisation).  A buffer holds 4096 launches per source file; a
+ * later launch can overwrite an unread record of one 4096 launches earlier.
+ * Returns the number of records written (>= 0), MTP_ERR_INVALID_ARG for a
+ * null buffer with max_entries > 0, MTP_ERR_UNSUPPORTED_SHAPE from a library
+ * built without MTP_TRACE, or MTP_ERR_CUDA.
+ */
+enum {
+    MTP_TK_GEMV = 0,        /* + the op: 0 input projection, 1 QKV, 2 output projection,
+                               3 gate/up, 4 down, 5 LM head */
+    MTP_TK_ATTN = 10,       /* CUDA-core decode attention */
+    MTP_TK_ATTN_TC = 11,    /* tensor-core decode attention */
+    MTP_TK_VERIFY = 20,     /* cluster verification kernel */
+    MTP_TK_VERIFY_SPLIT = 21, /* ticketed stochastic verification kernel */
+    MTP_TK_TC_GEMM = 30,    /* tcgen05 GEMM of the batched path */
+    MTP_TK_TC_AUX = 31,     /* the batched path's prologue / select / scatter kernels */
+    MTP_TK_FUSED_GEMM = 40, /* spec_verify_fused: head GEMM */
+    MTP_TK_FUSED_AUX = 41,  /* spec_verify_fused: draft statistics and finish */
+    MTP_TK_CHAIN = 50       /* chain launch of several GEMV ops */
+};
+typedef struct MtpTraceEntry {
+    uint64_t launch;      /* the launch's grid id */
+    int32_t kind;         /* MTP_TK_* */
+    int32_t reserved;
+    uint64_t t_start_ns;  /* first CTA started */
+    uint64_t t_dep_ns;    /* first CTA past its wait for the previous kernel, or 0 */
+    uint64_t t_end_ns;    /* last CTA finished */
+    uint64_t t_mark_ns[4]; /* the last CTA to reach each of the kernel's intermediate marks, or 0 */
+} MtpTraceEntry;
+int mtp_trace_read(MtpTraceEntry *entries, int max_entries);
+
 #ifdef __cplusplus
 }
 #endif

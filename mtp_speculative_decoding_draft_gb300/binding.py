@@ -114,6 +114,8 @@ def _lib():
         L.mtp_profiler_read.restype = I
         L.mtp_launch_count.argtypes = []
         L.mtp_launch_count.restype = ctypes.c_int64
+        L.mtp_trace_read.argtypes = [P, I]
+        L.mtp_trace_read.restype = I
         _LIB = L
     return _LIB
 
@@ -431,3 +433,27 @@ def profiler_read(kernel_class):
 
 def launch_count():
     return int(_lib().mtp_launch_count())
+
+
+class MtpTraceEntry(ctypes.Structure):
+    _fields_ = [("launch", ctypes.c_uint64), ("kind", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("t_start_ns", ctypes.c_uint64), ("t_dep_ns", ctypes.c_uint64), ("t_end_ns", ctypes.c_uint64),
+                ("t_mark_ns", ctypes.c_uint64 * 4)]
+
+
+TRACE_KIND_NAMES = {0: "gemv input projection", 1: "gemv QKV", 2: "gemv output projection", 3: "gemv gate/up",
+                    4: "gemv down", 5: "gemv LM head", 10: "attention", 11: "attention (tensor cores)",
+                    20: "verify (cluster)", 21: "verify (ticketed)", 30: "tc GEMM", 31: "tc prologue/select",
+                    40: "fused verify GEMM", 41: "fused verify stats/finish", 50: "chain"}
+
+
+def trace_read(max_entries=16384):
+    """The launch-trace records since the last read (library built with
+    MTP_TRACE), as dicts sorted by start time.  Call after synchronising."""
+    buf = (MtpTraceEntry * max_entries)()
+    n = _lib().mtp_trace_read(ctypes.cast(buf, ctypes.c_void_p), max_entries)
+    if n < 0:
+        raise MtpError(n, "mtp_trace_read")
+    out = [dict(launch=e.launch, kind=e.kind, name=TRACE_KIND_NAMES.get(e.kind, str(e.kind)),
+                start=e.t_start_ns, dep=e.t_dep_ns, end=e.t_end_ns, marks=list(e.t_mark_ns)) for e in buf[:n]]
+    return sorted(out, key=lambda r: r["start"])

@@ -7,7 +7,10 @@ library with the CUDA runtime linked statically.  ptxas resource usage
 variant="bounds" builds the bounds-checked library (-DMTP_BOUNDS: an index
 outside its buffer sets MTP_STATUS_BOUNDS and the access is skipped) into
 _build_bounds/libmtpspec_bounds.so; the binding loads it when the environment
-sets MTP_LIB_VARIANT=bounds.
+sets MTP_LIB_VARIANT=bounds.  variant="trace" builds the launch-tracing
+library (-DMTP_TRACE: every kernel stamps its start, dependency release and
+end on the GPU's global timer; mtp_trace_read) into _build_trace/, loaded
+with MTP_LIB_VARIANT=trace.
 """
 
 import os
@@ -24,7 +27,9 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(BUILD, "libmtpspec.so")
 VARIANTS = {"": (BUILD, LIB, []),
             "bounds": (os.path.join(PKG, "_build_bounds"),
-                       os.path.join(PKG, "_build_bounds", "libmtpspec_bounds.so"), ["-DMTP_BOUNDS"])}
+                       os.path.join(PKG, "_build_bounds", "libmtpspec_bounds.so"), ["-DMTP_BOUNDS"]),
+            "trace": (os.path.join(PKG, "_build_trace"),
+                      os.path.join(PKG, "_build_trace", "libmtpspec_trace.so"), ["-DMTP_TRACE"])}
 
 
 def library_path(variant=None):

@@ -505,6 +505,22 @@ int static_scratch(void **out) {
 }
 
 }  // namespace
+static_assert(kTkGemv == MTP_TK_GEMV && kTkAttn == MTP_TK_ATTN && kTkAttnTc == MTP_TK_ATTN_TC &&
+                  kTkVerify == MTP_TK_VERIFY && kTkVerifySplit == MTP_TK_VERIFY_SPLIT && kTkTcGemm == MTP_TK_TC_GEMM &&
+                  kTkTcAux == MTP_TK_TC_AUX && kTkFusedGemm == MTP_TK_FUSED_GEMM &&
+                  kTkFusedAux == MTP_TK_FUSED_AUX && kTkChain == MTP_TK_CHAIN,
+              "trace kinds match the header");
+
+// the launch-trace collectors of the kernel files (MTP_TRACE_COLLECTOR)
+int trace_collect_draft(TraceRec *, int);
+int trace_collect_attn_tc(TraceRec *, int);
+int trace_collect_verify(TraceRec *, int);
+int trace_collect_verify_split(TraceRec *, int);
+int trace_collect_tc(TraceRec *, int);
+int trace_collect_fused(TraceRec *, int);
+int trace_collect_chain(TraceRec *, int);
+int trace_collect_diag(TraceRec *, int);
+
 }  // namespace mtp
 
 using namespace mtp;
@@ -803,5 +819,37 @@ int mtp_profiler_read(int kernel_class, double *total_ms, int64_t *launches) {
 }
 
 int64_t mtp_launch_count(void) { return (int64_t)g_launches.load(); }
+
+int mtp_trace_read(MtpTraceEntry *entries, int max_entries) {
+#ifndef MTP_TRACE
+  (void)entries;
+  (void)max_entries;
+  return MTP_ERR_UNSUPPORTED_SHAPE;
+#else
+  if (max_entries < 0 || (max_entries > 0 && !entries)) return MTP_ERR_INVALID_ARG;
+  using Collector = int (*)(mtp::TraceRec *, int);
+  static const Collector collectors[] = {mtp::trace_collect_draft, mtp::trace_collect_attn_tc,
+                                         mtp::trace_collect_verify,
+                                         mtp::trace_collect_verify_split, mtp::trace_collect_tc,
+                                         mtp::trace_collect_fused, mtp::trace_collect_chain,
+                                         mtp::trace_collect_diag};
+  static mtp::TraceRec recs[mtp::kTraceSlots];
+  int n = 0;
+  for (Collector col : collectors) {
+    const int got = col(recs, mtp::kTraceSlots);
+    if (got < 0) return MTP_ERR_CUDA;
+    for (int i = 0; i < got && n < max_entries; ++i, ++n) {
+      entries[n].launch = recs[i].grid;
+      entries[n].kind = recs[i].kind;
+      entries[n].reserved = 0;
+      entries[n].t_start_ns = ~recs[i].nstart;
+      entries[n].t_dep_ns = recs[i].ndep ? ~recs[i].ndep : 0ull;
+      entries[n].t_end_ns = recs[i].end;
+      for (int m = 0; m < 4; ++m) entries[n].t_mark_ns[m] = recs[i].mark[m];
+    }
+  }
+  return n;
+#endif
+}
 
 }  // extern "C"

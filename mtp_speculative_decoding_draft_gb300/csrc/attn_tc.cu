@@ -34,6 +34,7 @@ constexpr int kTcStages = 3;     // ring stages
 constexpr int kTcThreads = 32 * (kTcWarps + 1);
 constexpr int kBox = 64 * kTcRows * 2;  // one 64-dim x 64-row box: 8 KB
 constexpr unsigned kFullMask = 0xffffffffu;
+constexpr int kMaxCluster = 16;  // CTAs per (sequence, kv head) at most
 
 struct AttnTcArgs {
   CUtensorMap mk, mv;  // [B*Hkv*Lmax, Dh] bf16 views of the caches
@@ -95,6 +96,7 @@ __device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 12
 
 template <int DH>
 __global__ void __launch_bounds__(kTcThreads, 2) attn_tc_kernel(const __grid_constant__ AttnTcArgs p) {
+  trace_start(kTkAttnTc);
   using Ly = TcLayout<DH>;
   constexpr int NB = Ly::NB, KS = DH / 16, ND = DH / 8;
   extern __shared__ unsigned char smem_raw[];
@@ -166,23 +168,34 @@ __global__ void __launch_bounds__(kTcThreads, 2) attn_tc_kernel(const __grid_con
     // ------------------------------------------------ compute warps
     grid_dep_wait();  // q comes from this depth's projection
     grid_dep_launch();
+    trace_dep(kTkAttnTc);
     // the group's query heads, rows 0..15 (zero past the group), in three bf16 terms
     const int nq = c.Hq * DH;
-    for (int idx = tid; idx < 16 * DH / 2; idx += 32 * kTcWarps) {
-      const int h = idx / (DH / 2), e = 2 * (idx % (DH / 2));
-      float x = 0.f, y = 0.f;
-      if (h < group) {
-        const float *q = c.q + (size_t)b * nq + ((size_t)g * group + h) * DH + e;
-        x = __ldcg(q);
-        y = __ldcg(q + 1);
+    {
+      // every load first (one round trip), then the splits and stores
+      constexpr int PER = 16 * DH / 2 / (32 * kTcWarps);
+      float2 qv[PER];
+#pragma unroll
+      for (int t = 0; t < PER; ++t) {
+        const int idx = tid + t * 32 * kTcWarps;
+        const int h = idx / (DH / 2), e = 2 * (idx % (DH / 2));
+        qv[t] = h < group ? __ldcg(reinterpret_cast<const float2 *>(c.q + (size_t)b * nq +
+                                                                     ((size_t)g * group + h) * DH + e))
+                          : make_float2(0.f, 0.f);
       }
-      uint32_t th, tm, tl;
-      split3(x, y, th, tm, tl);
-      *reinterpret_cast<uint32_t *>(qs + (0 * 16 + h) * Ly::QLD + e) = th;
-      *reinterpret_cast<uint32_t *>(qs + (1 * 16 + h) * Ly::QLD + e) = tm;
-      *reinterpret_cast<uint32_t *>(qs + (2 * 16 + h) * Ly::QLD + e) = tl;
+#pragma unroll
+      for (int t = 0; t < PER; ++t) {
+        const int idx = tid + t * 32 * kTcWarps;
+        const int h = idx / (DH / 2), e = 2 * (idx % (DH / 2));
+        uint32_t th, tm, tl;
+        split3(qv[t].x, qv[t].y, th, tm, tl);
+        *reinterpret_cast<uint32_t *>(qs + (0 * 16 + h) * Ly::QLD + e) = th;
+        *reinterpret_cast<uint32_t *>(qs + (1 * 16 + h) * Ly::QLD + e) = tm;
+        *reinterpret_cast<uint32_t *>(qs + (2 * 16 + h) * Ly::QLD + e) = tl;
+      }
     }
     named_sync(1, 32 * kTcWarps);
+    trace_mark(kTkAttnTc, 0);  // query staged
 
     const int gq = lane >> 2, tq = lane & 3;  // fragment row / column-pair of this lane
     const float scale = rsqrtf((float)DH) * kLog2e;
@@ -295,6 +308,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) attn_tc_kernel(const __grid_con
     }
     // the warp's state for heads gq < group: (m, l) and O[gq][8n + 2tq, +1]
     named_sync(1, 32 * kTcWarps);  // every warp is past the ring: it now holds the states
+    trace_mark(kTkAttnTc, 1);      // last tile done
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int h = gq + 8 * hh;
@@ -336,21 +350,38 @@ __global__ void __launch_bounds__(kTcThreads, 2) attn_tc_kernel(const __grid_con
   }
   // combine across the cluster: CTA r finalises pairs (h, e) r, r + C, ...
   const int nq = c.Hq * DH;
+  trace_mark(kTkAttnTc, 2);  // CTA merged
   cluster_sync();
   for (int idx = rank + C * tid; idx < group * DH; idx += C * kTcThreads) {
     const int h = idx / DH, e = idx % DH;
+    // every peer's (m, l, o) first: the remote loads are independent, so they
+    // are all in flight at once
+    float mr[kMaxCluster], lr[kMaxCluster], orr[kMaxCluster];
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) {
+      if (r < C) {
+        mr[r] = *dsmem_ptr(&mrun[h], r);
+        lr[r] = *dsmem_ptr(&lrun[h], r);
+        orr[r] = *dsmem_ptr(&qo[h * DH + e], r);
+      }
+    }
     float M = -INFINITY, Ls = 0.f, O = 0.f;
-    for (int r = 0; r < C; ++r) M = fmaxf(M, *dsmem_ptr(&mrun[h], r));
-    for (int r = 0; r < C; ++r) {
-      const float mr = *dsmem_ptr(&mrun[h], r);
-      if (mr == -INFINITY) continue;
-      const float wgt = exp2f(mr - M);
-      Ls = fmaf(*dsmem_ptr(&lrun[h], r), wgt, Ls);
-      O = fmaf(*dsmem_ptr(&qo[h * DH + e], r), wgt, O);
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r)
+      if (r < C) M = fmaxf(M, mr[r]);
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) {
+      if (r < C && mr[r] != -INFINITY) {
+        const float wgt = exp2f(mr[r] - M);
+        Ls = fmaf(lr[r], wgt, Ls);
+        O = fmaf(orr[r], wgt, O);
+      }
     }
     c.o[(size_t)b * nq + ((size_t)g * group + h) * DH + e] = O / Ls;
   }
+  trace_mark(kTkAttnTc, 3);  // cluster combined
   cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
+  trace_end(kTkAttnTc);
 }
 
 // ---------------------------------------------------------------- host side
@@ -428,5 +459,7 @@ bool attention_tc_shape_ok(const DraftCtx &c) {
 cudaError_t launch_attention_tc(const DraftCtx &c, int cluster, cudaStream_t s, bool pdl) {
   return c.Dh == 64 ? launch_tc<64>(c, cluster, s, pdl) : launch_tc<128>(c, cluster, s, pdl);
 }
+
+MTP_TRACE_COLLECTOR(attn_tc)
 
 }  // namespace mtp

@@ -291,6 +291,7 @@ __device__ bool run_op_any(const ChainArgs &a, const ChainOp &co, Ring &ring, in
 //                [part: max rows x P x BG][ys: LM-head rows x BG][red: 64][sq: 8 x BG x 2]
 template <int NVM, int BG>
 __global__ void __launch_bounds__(kGemvThreads, 2) chain_kernel(const __grid_constant__ ChainArgs a) {
+  trace_start(kTkChain);
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Ring ring;
@@ -339,6 +340,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) chain_kernel(const __grid_con
     for (uint32_t q = ring.n_con; q < ring.n_iss; ++q)
       if (!mbar_sleep_wait(&ring.bars[q & (kRingSlots - 1)], (q / kRingSlots) & 1u, a.status)) break;
   __syncwarp();
+  trace_end(kTkChain);
 }
 
 // ---------------------------------------------------------------- host side
@@ -416,5 +418,7 @@ cudaError_t launch_chain(ChainArgs a, cudaStream_t s) {
     default: return launch_chain_t<9, 1>(a, grid, smem, s);
   }
 }
+
+MTP_TRACE_COLLECTOR(chain)
 
 }  // namespace mtp

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "internal.h"
+
 namespace mtp {
 
 // Status bits (mirror MTP_STATUS_* of the public header).
@@ -227,6 +229,62 @@ __device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
+
+// ---------------------------------------------------------------- launch trace
+//
+// Built with -DMTP_TRACE: thread 0 of every CTA folds the global timer into
+// its launch's record (slot = grid id mod kTraceSlots) at the kernel's start,
+// after its wait for the previous kernel and at its end.  Each source file
+// has its own record array (internal linkage) and its own collector,
+// trace_collect_<file>(), defined by MTP_TRACE_COLLECTOR at the file's end.
+// Start and dependency times are stored complemented so that one atomicMax
+// keeps the earliest.  Without MTP_TRACE the marks compile to nothing.
+// (TraceRec, kTraceSlots and the record kinds are in internal.h)
+
+#ifdef MTP_TRACE
+static __device__ TraceRec g_trace[kTraceSlots];
+
+__device__ __forceinline__ TraceRec &trace_rec(int kind) {
+  unsigned long long g;
+  asm volatile("mov.u64 %0, %%gridid;" : "=l"(g));
+  TraceRec &r = g_trace[g % kTraceSlots];
+  r.grid = g;
+  r.kind = kind;
+  return r;
+}
+__device__ __forceinline__ void trace_start(int kind) {
+  if (threadIdx.x == 0) atomicMax(&trace_rec(kind).nstart, ~global_timer_ns());
+}
+__device__ __forceinline__ void trace_dep(int kind) {
+  if (threadIdx.x == 0) atomicMax(&trace_rec(kind).ndep, ~global_timer_ns());
+}
+__device__ __forceinline__ void trace_end(int kind) {
+  if (threadIdx.x == 0) atomicMax(&trace_rec(kind).end, global_timer_ns());
+}
+__device__ __forceinline__ void trace_mark(int kind, int i) {
+  if (threadIdx.x == 0) atomicMax(&trace_rec(kind).mark[i & 3], global_timer_ns());
+}
+#define MTP_TRACE_COLLECTOR(name)                                                                   \
+  int trace_collect_##name(TraceRec *out, int max) {                                               \
+    static TraceRec host[kTraceSlots];                                                             \
+    if (cudaMemcpyFromSymbol(host, g_trace, sizeof(host)) != cudaSuccess) return -1;               \
+    void *dev = nullptr;                                                                           \
+    if (cudaGetSymbolAddress(&dev, g_trace) != cudaSuccess) return -1;                             \
+    if (cudaMemset(dev, 0, sizeof(host)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) \
+      return -1;                                                                                   \
+    int n = 0;                                                                                     \
+    for (int i = 0; i < kTraceSlots && n < max; ++i)                                               \
+      if (host[i].grid != 0ull) out[n++] = host[i];                                                \
+    return n;                                                                                      \
+  }
+#else
+__device__ __forceinline__ void trace_start(int) {}
+__device__ __forceinline__ void trace_dep(int) {}
+__device__ __forceinline__ void trace_end(int) {}
+__device__ __forceinline__ void trace_mark(int, int) {}
+#define MTP_TRACE_COLLECTOR(name) \
+  int trace_collect_##name(TraceRec *, int) { return 0; }
+#endif
 
 // ---------------------------------------------------------------- PDL
 

@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(64, 1) wait_selftest_kernel(int *status) {
 }
 
 }  // namespace
+MTP_TRACE_COLLECTOR(diag)
+
 }  // namespace mtp
 
 extern "C" int mtp_selftest_wait_timeout(int32_t *status, mtp_stream_t stream) {

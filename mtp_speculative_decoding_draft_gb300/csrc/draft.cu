@@ -40,6 +40,7 @@ namespace mtp {
 //                [sq: W*BG*2 f32 (per-warp sums of squares)]
 template <int OP, int NV, int BG>
 __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(DraftCtx c, GemvPlan g) {
+  trace_start(kTkGemv + OP);
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = g.stages, P = g.P, R = kGemvWarps / P;
@@ -76,11 +77,13 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(DraftCtx c, GemvPlan
     bulk_g2s_hint(ring + (size_t)stage * PCB, weight_row<OP>(c, row0 + rl, g.K) + col0, piece_bytes, &bars[stage],
                   pol);
   };
+  const int pre = min(g.pre, S);
   if (lane == 0)
-    for (int n = 0; n < min(S, total_units); ++n) issue(n);
+    for (int n = 0; n < min(pre, total_units); ++n) issue(n);
 
   grid_dep_wait();
   grid_dep_launch();
+  trace_dep(kTkGemv + OP);
 
   // Dynamic draft length: once every sequence has stopped drafting, the later
   // depths have nothing to do -- let the weight copies already issued land and
@@ -88,8 +91,9 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(DraftCtx c, GemvPlan
   // same value).
   if (c.n_active && c.j > 0 && *reinterpret_cast<volatile unsigned *>(c.n_active) == 0u) {
     if (lane == 0)
-      for (int n = 0; n < min(S, total_units); ++n)
+      for (int n = 0; n < min(pre, total_units); ++n)
         if (!mbar_sleep_wait(&bars[n], 0u, c.status)) break;
+    trace_end(kTkGemv + OP);
     return;
   }
   if (OP == OP_FC && c.zero_counters && blockIdx.x == 0) {
@@ -138,6 +142,12 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(DraftCtx c, GemvPlan
         }
       }
     }
+    if (grp == 0) {
+      trace_mark(kTkGemv + OP, 0);  // activations loaded
+      // the rest of the first ring fill, after the activation loads
+      if (lane == 0)
+        for (int q = pre; q < min(S, total_units); ++q) issue(q);
+    }
     for (int u = 0; u < units_per_group && ncols > 0; ++u, ++n) {
       const int stage = n % S;
       if (ok) ok = mbar_sleep_wait(&bars[stage], (uint32_t)(n / S) & 1u, c.status);
@@ -169,13 +179,16 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(DraftCtx c, GemvPlan
       }
     }
     __syncthreads();
+    trace_mark(kTkGemv + OP, 1);  // the group's last weight piece used
 
     // epilogue for this batch group (the norm's scales, the op's outputs and,
     // for the LM head, this CTA's partials)
     gemv_epilogue<OP, BG>(c, P, g.PC, row0, nrows, grp, fac, part, sq, ys, red, (int)blockIdx.x);
     __syncthreads();
+    trace_mark(kTkGemv + OP, 2);  // epilogue done
   }
 
+  trace_end(kTkGemv + OP);
   if (OP != OP_LMHEAD) return;
 
   // ---- draft-token selection by the last CTA to finish
@@ -184,12 +197,14 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(DraftCtx c, GemvPlan
   __syncthreads();
   if (threadIdx.x == 0) s_last = atomicAdd(c.lm_cnt, 1u) == gridDim.x - 1;
   __syncthreads();
+  trace_end(kTkGemv + OP);
   if (!s_last) return;
   __threadfence();
   if (warp == 0) {
     lm_select_warp(c, c.lm_grid, c.lm_rpc);
     if (lane == 0) *c.lm_cnt = 0u;
   }
+  trace_end(kTkGemv + OP);
 }
 
 // ---------------------------------------------------------------- planning / launch
@@ -225,6 +240,7 @@ GemvPlan plan_gemv(int op, int N, int K, int B, int num_sms) {
   g.rows_per_cta = rpc;
   g.grid = (N + rpc - 1) / rpc;
   g.stages = env_int("MTP_GEMV_STAGES", 6);
+  g.pre = env_int("MTP_GEMV_PRE", 6);
   // the norm's scale after the dot products: the ops with an input norm, when
   // no piece of the input projection straddles its two halves (and
   // MTP_GEMV_FACTOR is not 0)
@@ -365,6 +381,7 @@ __device__ __forceinline__ void unpack_row(const RowVec<DPL> &r, float *out) {
 // distributed shared memory.
 template <int DH, int GM>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(DraftCtx c) {
+  trace_start(kTkAttn);
   constexpr int DPL = DH / 16, NW = kAttnWarps, U = attn_unroll(GM);
   constexpr int TT = 2 * U * NW;        // rows per tile
   constexpr int TILE = TT * DH;         // elements of one K (or V) tile
@@ -590,6 +607,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(DraftCtx c) {
     c.o[(size_t)b * nq + ((size_t)g * group + h) * DH + e] = O / Ls;
   }
   cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
+  trace_end(kTkAttn);
 }
 
 __global__ void __launch_bounds__(256) fill_kernel(float *p, size_t n, float v) {
@@ -677,5 +695,7 @@ cudaError_t launch_attention(const DraftCtx &c, int cluster, cudaStream_t s, boo
     default: return launch_attn_g<128>(c, cluster, s, pdl);
   }
 }
+
+MTP_TRACE_COLLECTOR(draft)
 
 }  // namespace mtp

@@ -93,6 +93,7 @@ namespace {
 template <int MODE>
 __global__ void __launch_bounds__(kFvThreads, 1) fv_gemm_kernel(const __grid_constant__ FvMaps maps,
                                                                   const FvArgs g) {
+  trace_start(kTkFusedGemm);
   extern __shared__ unsigned char smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   unsigned char *sm = smem_raw + pad;
@@ -256,6 +257,7 @@ __global__ void __launch_bounds__(kFvThreads, 1) fv_gemm_kernel(const __grid_con
     tc_fence_after();
     tmem_dealloc(tmem, (uint32_t)(nbuf * ncols));
   }
+  trace_end(kTkFusedGemm);
 }
 
 // ---------------------------------------------------------------- draft-row statistics (stochastic)
@@ -264,6 +266,7 @@ __global__ void __launch_bounds__(kFvThreads, 1) fv_gemm_kernel(const __grid_con
 // the draft logits, in the target partials' tiling.  One warp per tile (each
 // lane 8 elements), eight tiles a CTA: every draft logit is read once.
 __global__ void __launch_bounds__(256) fv_draft_stats_kernel(const FvArgs g) {
+  trace_start(kTkFusedAux);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp, r = blockIdx.y;  // tile, draft row b k + j
   grid_dep_launch();
@@ -300,6 +303,7 @@ __global__ void __launch_bounds__(256) fv_draft_stats_kernel(const FvArgs g) {
     if (lane == 0) g.dpart[(size_t)r * g.n_vt + t] = make_float4(m, s, 0.f, 0.f);
   }
   grid_dep_wait();
+  trace_end(kTkFusedAux);
 }
 
 // ---------------------------------------------------------------- finish kernel
@@ -508,6 +512,7 @@ __device__ void chunk_masses_residual(FinShared &sh, const Wt &w, const float *t
 // partials (and, stochastic, the draft rows' partials), then the draw.
 template <int MODE>
 __global__ void __launch_bounds__(kFinThreads) fv_finish_kernel(const FvArgs g, FvOut o) {
+  trace_start(kTkFusedAux);
   extern __shared__ __align__(16) unsigned char fin_smem[];
   FinShared &sh = *reinterpret_cast<FinShared *>(fin_smem);
   const int b = blockIdx.x, k = g.k, V = g.V;
@@ -641,6 +646,7 @@ __global__ void __launch_bounds__(kFinThreads) fv_finish_kernel(const FvArgs g, 
     o.num_accepted[b] = n_acc;
     if (flags) set_status(g.status, flags);
   }
+  trace_end(kTkFusedAux);
 }
 
 // ---------------------------------------------------------------- host side
@@ -774,5 +780,7 @@ cudaError_t launch_fused_verify(const FusedCall &fc, cudaStream_t s, bool pdl) {
   return fc.mode == 1 ? cudaLaunchKernelEx(&fcfg, fv_finish_kernel<1>, g, o)
                       : cudaLaunchKernelEx(&fcfg, fv_finish_kernel<0>, g, o);
 }
+
+MTP_TRACE_COLLECTOR(fused)
 
 }  // namespace mtp

@@ -68,6 +68,7 @@ struct GemvPlan {
   int bg;            // batch rows per group (activation registers per lane)
   int ngroups;       // batch groups = ceil(B / bg)
   int stages;        // TMA ring depth per warp
+  int pre;           // stages requested before the wait for the previous kernel (the rest after the activations)
   int factor;        // the norm's scale applied to the finished dot products (else to the inputs)
   size_t smem;       // dynamic shared memory bytes
 };
@@ -205,6 +206,18 @@ bool fused_shape_ok(int B, int k, int V, int d);
 size_t fused_workspace_bytes(int B, int k, int V, int d, int mode);
 cudaError_t fused_set_attributes();
 cudaError_t launch_fused_verify(const FusedCall &fc, cudaStream_t s, bool pdl);
+
+// Launch-trace record (a build with MTP_TRACE; common.cuh): start and
+// dependency times stored complemented, so that atomicMax keeps the earliest.
+struct TraceRec {
+  unsigned long long grid, nstart, ndep, end;
+  unsigned long long mark[4];  // the last CTA to reach each of a kernel's intermediate marks
+  int kind, pad[3];
+};
+constexpr int kTraceSlots = 4096;
+// record kinds: the MTP_TK_* values of the public header
+constexpr int kTkGemv = 0, kTkAttn = 10, kTkAttnTc = 11, kTkVerify = 20, kTkVerifySplit = 21, kTkTcGemm = 30,
+              kTkTcAux = 31, kTkFusedGemm = 40, kTkFusedAux = 41, kTkChain = 50;
 
 // bookkeeping shared with api.cu
 void note_launch();

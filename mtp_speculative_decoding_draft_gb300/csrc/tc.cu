@@ -109,6 +109,7 @@ __device__ __forceinline__ TcUnit tc_unit(const TcGemmArgs &g, int u) {
 template <bool FUSE>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ TcMaps maps,
                                                                   const TcGemmArgs g) {
+  trace_start(kTkTcGemm);
   extern __shared__ unsigned char smem_raw[];
   // SW128 tiles need 1024-byte alignment
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -266,6 +267,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     tc_fence_after();
     tmem_dealloc(tmem, (uint32_t)(nbuf * ncols));
   }
+  trace_end(kTkTcGemm);
 }
 
 // ---------------------------------------------------------------- per-sequence kernels
@@ -315,6 +317,7 @@ __device__ __forceinline__ float sumsq8(const float *v, float acc) {
 // Input of the input projection: [rms(E[tok]) g_emb ; rms(x) g_hid], x = h at
 // depth 0, else the previous depth's x2.
 __global__ void __launch_bounds__(kPrepThreads) tc_prep_fc_kernel(DraftCtx c, TcBufs t) {
+  trace_start(kTkTcAux);
   __shared__ float red[2 * kGemvWarps];
   const int b = blockIdx.x, d = c.d;
   grid_dep_wait();
@@ -363,10 +366,12 @@ __global__ void __launch_bounds__(kPrepThreads) tc_prep_fc_kernel(DraftCtx c, Tc
     for (int q = 0; q < 8; ++q) x[q] = x[q] * r1 * g[q];
     store_split8(t, b, d + i, x);
   }
+  trace_end(kTkTcAux);
 }
 
 // Input of the output projection: the attention output as is.
 __global__ void __launch_bounds__(kPrepThreads) tc_prep_wo_kernel(DraftCtx c, TcBufs t) {
+  trace_start(kTkTcAux);
   const int b = blockIdx.x, n = c.Hq * c.Dh;
   grid_dep_wait();
   grid_dep_launch();
@@ -375,6 +380,7 @@ __global__ void __launch_bounds__(kPrepThreads) tc_prep_wo_kernel(DraftCtx c, Tc
     load8_f32(c.o + (size_t)b * n + i, v);
     store_split8(t, b, i, v);
   }
+  trace_end(kTkTcAux);
 }
 
 // Sum the split-K partials of OP for sequence b (CTA r of the sequence's
@@ -382,6 +388,7 @@ __global__ void __launch_bounds__(kPrepThreads) tc_prep_wo_kernel(DraftCtx c, Tc
 // the next GEMM's input terms.
 template <int OP>
 __global__ void __launch_bounds__(kPrepThreads) tc_mid_kernel(DraftCtx c, TcBufs t, int ks, int N) {
+  trace_start(kTkTcAux);
   __shared__ float red[kGemvWarps];
   __shared__ float css;  // this CTA's sum of squares, read by the cluster's other CTAs
   const int b = blockIdx.y, d = c.d, NC = (int)gridDim.x, r = (int)blockIdx.x;
@@ -415,6 +422,7 @@ __global__ void __launch_bounds__(kPrepThreads) tc_mid_kernel(DraftCtx c, TcBufs
           for (int q = 0; q < 8; ++q) dst[q] = __bfloat16_as_ushort(__float2bfloat16_rn(y[q]));
       }
     }
+    trace_end(kTkTcAux);
     return;
   }
   if (OP == OP_GATEUP) {  // SwiGLU: gate rows [0, F), up rows [F, 2F)
@@ -427,6 +435,7 @@ __global__ void __launch_bounds__(kPrepThreads) tc_mid_kernel(DraftCtx c, TcBufs
       for (int q = 0; q < 8; ++q) gt[q] = silu_f(gt[q]) * up[q];
       store_split8(t, b, i, gt);
     }
+    trace_end(kTkTcAux);
     return;
   }
   // FC -> x0, WO -> x1 = x0 + y, DOWN -> x2 = x1 + y; then the next input
@@ -463,6 +472,7 @@ __global__ void __launch_bounds__(kPrepThreads) tc_mid_kernel(DraftCtx c, TcBufs
     store_split8(t, b, i, y);
   }
   cluster_sync();  // no CTA leaves before its peers have read its sum
+  trace_end(kTkTcAux);
 }
 
 // Draft-token selection over the batch's logits rows, in two launches.
@@ -480,6 +490,7 @@ __host__ __device__ inline int sel_subs(int V) { return (V + kSelSub - 1) / kSel
 
 __global__ void __launch_bounds__(kSelThreads) tc_select_part_kernel(DraftCtx c, const float *logits, size_t bstride,
                                                                      float4 *part) {
+  trace_start(kTkTcAux);
   const int b = blockIdx.y, V = c.Vd, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int q = blockIdx.x * kSelWarps + warp, nq = sel_subs(V);
   grid_dep_wait();
@@ -524,10 +535,12 @@ __global__ void __launch_bounds__(kSelThreads) tc_select_part_kernel(DraftCtx c,
     sum = warp_sum(sum);
   }
   if (lane == 0 && in_bounds(b < c.B && q < nq, c.status)) part[(size_t)b * nq + q] = make_float4(M, __int_as_float(I), sum, 0.f);
+  trace_end(kTkTcAux);
 }
 
 __global__ void __launch_bounds__(32) tc_select_fin_kernel(DraftCtx c, const float *logits, size_t bstride,
                                                            const float4 *part) {
+  trace_start(kTkTcAux);
   const int b = blockIdx.x, V = c.Vd, lane = threadIdx.x, nq = sel_subs(V);
   grid_dep_wait();
   grid_dep_launch();
@@ -633,12 +646,14 @@ __global__ void __launch_bounds__(32) tc_select_fin_kernel(DraftCtx c, const flo
   if (finite) tok = vocab_id(c, tok);  // head row -> vocabulary id
   if (lane == 0 && in_bounds(b < c.B && c.j < c.k, c.status)) c.draft_tok[b * c.k + c.j] = tok;
   if (lane == 0 && c.k_eff && finite) stop_check(c, b, 1.0 / Z);
+  trace_end(kTkTcAux);
 }
 
 // A reduced draft vocabulary: head row i's logit to its vocabulary id in the
 // caller's full-vocabulary logits (the other ids hold -inf from the start of
 // the call).
 __global__ void __launch_bounds__(256) tc_scatter_logits_kernel(DraftCtx c, const float *lg) {
+  trace_start(kTkTcAux);
   const int b = blockIdx.y;
   grid_dep_wait();
   grid_dep_launch();
@@ -646,6 +661,7 @@ __global__ void __launch_bounds__(256) tc_scatter_logits_kernel(DraftCtx c, cons
     const int v = vocab_id(c, i);
     if (v >= 0) c.logits[((size_t)b * c.k + c.j) * c.V + v] = __ldcg(&lg[(size_t)b * c.Vd + i]);
   }
+  trace_end(kTkTcAux);
 }
 
 // ---------------------------------------------------------------- host side
@@ -1020,5 +1036,7 @@ cudaError_t run_lmhead_tc(const DraftCtx &c, const TcBufs &t, cudaStream_t s, bo
   return launch(tc_scatter_logits_kernel, dim3((c.Vd + 255) / 256 < 64 ? (c.Vd + 255) / 256 : 64, c.B), 256, 0, s,
                 pdl, c, (const float *)lg);
 }
+
+MTP_TRACE_COLLECTOR(tc)
 
 }  // namespace mtp

@@ -1008,6 +1008,7 @@ __device__ void decider(const VerifyArgs &a, Shared &sh, int d, int rank, int C,
 }  // namespace
 
 __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(VerifyArgs a) {
+  trace_start(kTkVerify);
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Shared &sh = *reinterpret_cast<Shared *>(smem_raw);
   float *ring = reinterpret_cast<float *>(smem_raw + kHdr);
@@ -1059,6 +1060,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(VerifyArgs a)
     }
   }
   grid_dep_wait();
+  trace_end(kTkVerify);
 }
 
 // ---------------------------------------------------------------- host side
@@ -1160,5 +1162,7 @@ cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s, bool pdl) {
   note_launch();
   return cudaLaunchKernelEx(&cfg, verify_kernel, a);
 }
+
+MTP_TRACE_COLLECTOR(verify)
 
 }  // namespace mtp

@@ -551,9 +551,11 @@ __device__ void residual_item(Shared &sh, const VerifyArgs &a, int b, int ch) {
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 4) verify_split_kernel(const VerifyArgs a) {
+  trace_start(kTkVerifySplit);
   __shared__ Shared sh;
   grid_dep_wait();  // the draft rows may come from the drafter
   grid_dep_launch();
+  trace_dep(kTkVerifySplit);
   if (threadIdx.x == 0) sh.ticket = atomicAdd(&a.ctl[0], 1u);
   __syncthreads();
   const Item it = decode_ticket(a, sh.ticket);
@@ -563,6 +565,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_split_kernel(const VerifyA
     else
       statistics_item(sh, a, it.b, it.local);
   }
+  trace_end(kTkVerifySplit);
 }
 
 // ---------------------------------------------------------------- host side
@@ -617,5 +620,7 @@ cudaError_t launch_verify_split(const VerifyArgs &a, cudaStream_t s, bool pdl) {
   note_launch();
   return cudaLaunchKernelEx(&cfg, verify_split_kernel, a);
 }
+
+MTP_TRACE_COLLECTOR(verify_split)
 
 }  // namespace mtp

@@ -114,3 +114,20 @@ def test_noalloc_limit_counts_the_draft_only_layout(lib):
         dims = bd.make_dims(B, 4096, 32, 8, 128, 12288, 151936, 4099)
         assert L.mtp_draft_noalloc(ctypes.byref(dims), None, None, None, None, None, None, 3, 1.0, 0, None, None,
                                    None, None, None) == want
+
+
+def test_trace_read_needs_the_trace_build(lib):
+    """The launch trace exists only in the library built with MTP_TRACE; the
+    default build answers MTP_ERR_UNSUPPORTED_SHAPE without touching a GPU."""
+    from mtp_speculative_decoding_draft_gb300 import binding as bd
+    assert bd.library().mtp_trace_read(None, 0) == -2
+    with pytest.raises(bd.MtpError):
+        bd.trace_read(4)
+
+
+def test_trace_build_variant_compiles():
+    from mtp_speculative_decoding_draft_gb300 import build
+    path = build.build(variant="trace")
+    L = ctypes.CDLL(path)
+    assert hasattr(L, "mtp_trace_read")
+    assert L.mtp_trace_read(None, 5) == -1      # a null buffer for 5 records
