@@ -651,6 +651,8 @@ def run_verify_only(args, w, rank=0, world=1):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    if args.trace:
+        return print_trace(step, args.trace, torch, bd)
     if world > 1:
         dist.barrier()
     clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))

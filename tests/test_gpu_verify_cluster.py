@@ -25,7 +25,9 @@ def kernel(request, monkeypatch):
 @pytest.mark.parametrize("B,k,V,T", [(7, 3, 2 * 32768 + 5, 0.9),   # odd V: unaligned rows, ragged tail
                                      (3, 2, 3 * 32768, 1.0),       # whole chunks only
                                      (5, 4, 32768 + 1, 1.2),       # a one-element last chunk
+                                     (6, 3, 3 * 8192 + 4, 1.1),    # a 4-logit tail
                                      (37, 3, 5003, 1.0),           # one ragged chunk
+                                     (40, 2, 5004, 0.8),           # aligned rows below one chunk
                                      (3, 8, 777, 1.0)])            # the deepest draft
 def test_stochastic_multi_chunk(kernel, B, k, V, T):
     t, l, d, ua, uf = _case(B, k, V, T, seed=7700 + B * 10 + k)
