@@ -59,46 +59,37 @@ def lmhead_bytes(w, logits_out, head_rows=None):
 # are unchanged; the summaries of the captures are kept under profiles/.
 NCU_TRAFFIC = {
     ("lm_head_gemv", "single_greedy_b1_d4096_v151936_ctx4096"): {
-        "bytes": 1244772608 + 2793984,
+        "bytes": 1244775424 + 2836992,
         "sources": {
-            "csrc/draft.cu": "34b4d3651e4401a69bfbc02728f99a661ae9b365079eda9047ff2b0d50de1bd3",
+            "csrc/draft.cu": "676f8d49f732a1dd64718ab494595f3138735d323cd0ad43c44d9c3c89978e7d",
             "csrc/draft_ops.cuh": "ad62698d95aa35a07e07854a0daa62b73bffc314f886982abd3a02a0da033f38",
-            "csrc/common.cuh": "9c6db2af79ca058026581ad7509766387747f9f2081071a926314ddfcaaa4558",
-            "csrc/internal.h": "b5cdd7b6f37b6d3da52e697e9b5412db147f23f3f48a5181b9da5c8ab3be61c6",
-        },
-    },
-    ("tc_gemm_kernel(LM head)", "batched_stochastic_b64_d4096_v151936_ctx1024-8192"): {
-        "bytes": 1248436992 + 7813632,
-        "sources": {
-            "csrc/tc.cu": "792cfe0e73815f8f7c27b8c8f32d9d2114544f1648f6d41af10c810afcce54fc",
-            "csrc/tcgen05.cuh": "e128ff6d7c8451d618848063024b7cd0a98c722dd1b86ef0d04e6a07a9070ee7",
-            "csrc/common.cuh": "fcd7bd8f56df32fc490b2c47f2fbc0f7f37047c578430d777438202c9279de66",
-            "csrc/internal.h": "36ac497104c59fe318924b19460d7557a45577223a255efc0f7534c05d38008d",
+            "csrc/common.cuh": "ccc7be3ffbab76f32e48e064231311046ac5ebb3caee7e3f3df14b4629b22b95",
+            "csrc/internal.h": "2ab350d5622c22f47de0c469aabd5010981632626e75291fc2273994f1968187",
         },
     },
     ("verify_kernel", "verify_sweep_b256_v151936_k3/greedy"): {
-        "bytes": 622433792 + 3021568,
+        "bytes": 622426624 + 2995968,
         "sources": {
-            "csrc/verify.cu": "f1d0b3ef5cf32a7d7279611da02f31cfe03a82a9ebe687965352321e233997f4",
-            "csrc/common.cuh": "fcd7bd8f56df32fc490b2c47f2fbc0f7f37047c578430d777438202c9279de66",
-            "csrc/internal.h": "36ac497104c59fe318924b19460d7557a45577223a255efc0f7534c05d38008d",
+            "csrc/verify.cu": "5666bbd8cb2c586706845ad948da9b4a804e29544b6de62c7b9e185710960f4d",
+            "csrc/common.cuh": "ccc7be3ffbab76f32e48e064231311046ac5ebb3caee7e3f3df14b4629b22b95",
+            "csrc/internal.h": "2ab350d5622c22f47de0c469aabd5010981632626e75291fc2273994f1968187",
         },
     },
-    ("verify_kernel", "verify_sweep_b256_v151936_k3/stochastic"): {
-        "bytes": 1301748992 + 3004160,
+    ("verify_split_kernel", "verify_sweep_b256_v151936_k3/stochastic"): {
+        "bytes": 1248843520 + 3457024,
         "sources": {
-            "csrc/verify.cu": "f1d0b3ef5cf32a7d7279611da02f31cfe03a82a9ebe687965352321e233997f4",
-            "csrc/common.cuh": "fcd7bd8f56df32fc490b2c47f2fbc0f7f37047c578430d777438202c9279de66",
-            "csrc/internal.h": "36ac497104c59fe318924b19460d7557a45577223a255efc0f7534c05d38008d",
+            "csrc/verify_split.cu": "364ca393ddea89b834b5563c439eec3d8b073a44c2b3a90feb26df1a5f59e31a",
+            "csrc/common.cuh": "ccc7be3ffbab76f32e48e064231311046ac5ebb3caee7e3f3df14b4629b22b95",
+            "csrc/internal.h": "2ab350d5622c22f47de0c469aabd5010981632626e75291fc2273994f1968187",
         },
     },
     ("fv_gemm_kernel + fv_finish_kernel", "fused_verify_b64_k3_d4096_v151936/greedy"): {
-        "bytes": 1251173888 + 3772672,
+        "bytes": 1250075392 + 3688192 + 2441984,
         "sources": {
-            "csrc/fused.cu": "860beae2657e823bf31ae8b401fc0936627cd8f9527797abca67c5395227a06a",
+            "csrc/fused.cu": "5b1bc8195a89aed511bb6d471b486494514ea57e956a36a89ea4bb551e94cb07",
             "csrc/tcgen05.cuh": "e128ff6d7c8451d618848063024b7cd0a98c722dd1b86ef0d04e6a07a9070ee7",
-            "csrc/common.cuh": "9c6db2af79ca058026581ad7509766387747f9f2081071a926314ddfcaaa4558",
-            "csrc/internal.h": "b5cdd7b6f37b6d3da52e697e9b5412db147f23f3f48a5181b9da5c8ab3be61c6",
+            "csrc/common.cuh": "ccc7be3ffbab76f32e48e064231311046ac5ebb3caee7e3f3df14b4629b22b95",
+            "csrc/internal.h": "2ab350d5622c22f47de0c469aabd5010981632626e75291fc2273994f1968187",
         },
     },
 }
@@ -452,6 +443,14 @@ def drafts_from_q(draft_logits, u_draft, T):
     return idx.clamp_(max=draft_logits.shape[-1] - 1).to(torch.int32).contiguous()
 
 
+def verify_kernel_name(w):
+    """The kernel spec_verify runs: the cluster kernel for greedy mode (and
+    for stochastic mode under MTP_VERIFY_SPLIT=0), else the ticketed one."""
+    if w.mode == W.GREEDY or os.environ.get("MTP_VERIFY_SPLIT", "1").startswith("0"):
+        return "verify_kernel"
+    return "verify_split_kernel"
+
+
 def verify_bytes(w):
     """Algorithmic bytes of one spec_verify: every logit row read once."""
     rows = w.B * (w.k + 1) + (w.B * w.k if w.mode == 1 else 0)
@@ -711,15 +710,16 @@ def run_verify_only(args, w, rank=0, world=1):
     peak, peak_kind = measured_peaks()
     vb = verify_bytes(w)
     ach = vb / (ms * 1e-3) / 1e9
+    vkernel = verify_kernel_name(w)
     line = {"metric": METRIC, "value": job_rate(ms, world), "unit": "verify calls/s", "n_gpus": world,
             "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32 logits", "data": "synthetic (seeded)", "config": config_of(w, args),
             "accept_len_mean": float(L.mean()),
             "acceptance": acceptance_metrics(L, w.k),
-            "roofline": {"bound": "hbm", "kernel": "verify_kernel", "achieved": ach, "peak": peak, "unit": "GB/s",
+            "roofline": {"bound": "hbm", "kernel": vkernel, "achieved": ach, "peak": peak, "unit": "GB/s",
                          "frac": ach / peak, "peak_kind": peak_kind,
-                         "traffic": ncu_traffic("verify_kernel", f"{w.name}/{'greedy' if w.mode == W.GREEDY else 'stochastic'}"),
+                         "traffic": ncu_traffic(vkernel, f"{w.name}/{'greedy' if w.mode == W.GREEDY else 'stochastic'}"),
                          "bytes_per_launch": vb,
                          "avg_launch_ms": ms, "launches": args.steps},
             "e2e": {"value": job_rate(e2e_ms, world), "unit": "verify calls/s", "h2d_bytes_per_step": h2d,

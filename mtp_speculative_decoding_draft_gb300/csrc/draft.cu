@@ -240,7 +240,10 @@ GemvPlan plan_gemv(int op, int N, int K, int B, int num_sms) {
   g.rows_per_cta = rpc;
   g.grid = (N + rpc - 1) / rpc;
   g.stages = env_int("MTP_GEMV_STAGES", 6);
-  g.pre = env_int("MTP_GEMV_PRE", 6);
+  // four of the six stages before the wait: the rest after the activation
+  // loads, which the full fill would queue behind (measured 1085 -> 1091
+  // steps/s at the single-sequence workload)
+  g.pre = env_int("MTP_GEMV_PRE", 4);
   // the norm's scale after the dot products: the ops with an input norm, when
   // no piece of the input projection straddles its two halves (and
   // MTP_GEMV_FACTOR is not 0)

@@ -327,16 +327,6 @@ __device__ __forceinline__ float lane_sumexp16(const float (&x)[16], float M, fl
   return s0 + s1;
 }
 
-// (max, sum exp2((x - max) c)) of two parts over the warp, reductions interleaved.
-__device__ __forceinline__ void part_lse2(const float (&x)[16], const float (&y)[16], float c, float2 &rx,
-                                          float2 &ry) {
-  const float mx = redux_max(lane_max16(x)), my = redux_max(lane_max16(y));
-  float sx = lane_sumexp16(x, mx, c), sy = lane_sumexp16(y, my, c);
-  warp_sum2(sx, sy);
-  rx = make_float2(mx, sx);
-  ry = make_float2(my, sy);
-}
-
 // Four warp sums with their shuffle rounds interleaved.
 __device__ __forceinline__ void warp_sum4(float (&v)[4]) {
 #pragma unroll
