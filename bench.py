@@ -547,6 +547,17 @@ def run_fused_only(args, w, rank=0, world=1):
         w = W.replace(w, mode=W.GREEDY)
     peak, peak_kind = measured_peaks()
     from mtp_speculative_decoding_draft_gb300 import binding as bd
+    if args.trace:
+        _, head_d, hid_d, draft, dtok, ua, uf, fv = _fused_setup(w)
+        stoch = w.mode == 1
+
+        def traced_call():
+            fv(w.T, head_d, hid_d, draft if stoch else None, dtok, ua if stoch else None, uf if stoch else None)
+
+        for _ in range(args.warmup):
+            traced_call()
+        torch.cuda.synchronize()
+        return print_trace(traced_call, args.trace, torch, bd)
     n0 = bd.launch_count()
     res, (inp, head_d, hid_d, draft, dtok, ua, uf, fv, call) = time_fused(w, args.steps, args.warmup, peak)
     launches = bd.launch_count() - n0 - 2 * args.warmup

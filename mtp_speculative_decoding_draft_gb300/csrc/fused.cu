@@ -49,6 +49,10 @@ constexpr int kSmemBudget = 227 * 1024 - 1024 - 256;
 constexpr int kFinThreads = 512;
 constexpr int kFinWarps = kFinThreads / 32;
 constexpr int kMaxChunks = 4096;  // inverse-CDF chunk sums per row, at most (chunks of whole tiles)
+constexpr int kResChunk = 8192;   // logits of both rows of a rejecting pair per residual CTA
+constexpr int kResThreads = 256;
+constexpr int kResSub = 512;      // residual sub-chunk
+constexpr int kResSubs = kResChunk / kResSub;  // 16
 
 __host__ __device__ inline uint32_t fv_stage_bytes(int mt) { return (uint32_t)mt * kATile + kBTile; }
 
@@ -57,6 +61,12 @@ __host__ __device__ inline uint32_t fv_stage_bytes(int mt) { return (uint32_t)mt
 struct FvMaps {
   CUtensorMap hid;   // [Na, d] bf16, boxes of 128 rows x 64 columns
   CUtensorMap head;  // [V, d] bf16, boxes of 256 rows x 64 columns
+};
+
+// A sequence's first rejection, for the residual kernel (j < 0: none).
+struct alignas(16) FvRes {
+  float Mt, iZt, Ml, iZl;  // target / draft row max and inverse partition sum
+  int j, row, pad0, pad1;  // the rejecting position; its target row b (k+1) + j
 };
 
 struct FvArgs {
@@ -74,6 +84,12 @@ struct FvArgs {
   float4 *dpart;          // [B k, n_vt] (max, sum of exp2) of the draft rows (stochastic)
   float *tgt;             // [Na, V] stored logits (stochastic), else null
   int *status;
+  // stochastic: the residual draw, spread over one CTA per kResChunk logits
+  int nrc;                // residual chunks per row
+  FvRes *rrec;            // [B] the first rejection of each sequence
+  unsigned *rcnt;         // [B] residual CTAs arrived (zeroed by the finish kernel)
+  float *rsub;            // [B, nrc, kResSubs] residual sub-chunk masses
+  double *rcm;            // [B, nrc] residual chunk masses
 };
 
 struct FvOut {
@@ -263,44 +279,58 @@ __global__ void __launch_bounds__(kFvThreads, 1) fv_gemm_kernel(const __grid_con
 // ---------------------------------------------------------------- draft-row statistics (stochastic)
 
 // Per (draft row, 256-token tile): (max, sum of exp2((x - max) log2e / T)) of
-// the draft logits, in the target partials' tiling.  One warp per tile (each
-// lane 8 elements), eight tiles a CTA: every draft logit is read once.
+// the draft logits, in the target partials' tiling.  A few CTAs per SM take
+// the (row, tile) items grid-stride, a warp four tiles at a time (each lane
+// 8 elements of each, loads issued together): every draft logit is read once.
+// It reads only the caller's draft logits, so it runs beside the GEMM (which
+// leaves room for it on every SM); it waits for the GEMM once its work is
+// done, so that the finish kernel's wait on this kernel covers both.
 __global__ void __launch_bounds__(256) fv_draft_stats_kernel(const FvArgs g) {
   trace_start(kTkFusedAux);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp, r = blockIdx.y;  // tile, draft row b k + j
   grid_dep_launch();
-  // It reads only the caller's draft logits, so it runs beside the GEMM; it
-  // waits for the GEMM before completing, so that the finish kernel's wait on
-  // this kernel covers both.
-  if (t < g.n_vt) {
-    const float *row = g.draft + (size_t)r * g.V;
-    const int e0 = t * kVt, n = min(kVt, g.V - e0);
-    float x[8];
-    if (n == kVt && (reinterpret_cast<uintptr_t>(row + e0) & 15u) == 0) {
-      const float4 a = __ldcg(reinterpret_cast<const float4 *>(row + e0) + lane);
-      const float4 b = __ldcg(reinterpret_cast<const float4 *>(row + e0) + 32 + lane);
-      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-      x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-    } else {
+  const long long total = (long long)g.Na / (g.k + 1) * g.k * g.n_vt;  // B k rows x n_vt tiles
+  const long long stride = (long long)gridDim.x * 8 * 4;
+  for (long long i0 = ((long long)blockIdx.x * 8 + warp) * 4; i0 < total; i0 += stride) {
+    float x[4][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = (i < 4 ? 4 * lane + i : 128 + 4 * lane + i - 4);
-        x[i] = e < n ? __ldcg(row + e0 + e) : -INFINITY;
+    for (int u = 0; u < 4; ++u) {
+      const long long i = i0 + u;
+      const int r = (int)(i / g.n_vt), t = (int)(i - (long long)r * g.n_vt);
+      const float *row = g.draft + (size_t)r * g.V;
+      const int e0 = t * kVt, n = i < total ? min(kVt, g.V - e0) : 0;
+      if (n == kVt && (reinterpret_cast<uintptr_t>(row + e0) & 15u) == 0) {
+        const float4 a = __ldcg(reinterpret_cast<const float4 *>(row + e0) + lane);
+        const float4 b = __ldcg(reinterpret_cast<const float4 *>(row + e0) + 32 + lane);
+        x[u][0] = a.x; x[u][1] = a.y; x[u][2] = a.z; x[u][3] = a.w;
+        x[u][4] = b.x; x[u][5] = b.y; x[u][6] = b.z; x[u][7] = b.w;
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int e = (q < 4 ? 4 * lane + q : 128 + 4 * lane + q - 4);
+          x[u][q] = e < n ? __ldcg(row + e0 + e) : -INFINITY;
+        }
       }
     }
-    float m = x[0];
 #pragma unroll
-    for (int i = 1; i < 8; ++i) m = fmaxf(m, x[i]);
-    m = warp_max(m);
-    float s = 0.f;
-    if (m != -INFINITY) {
-      const float mc = m * g.c;
+    for (int u = 0; u < 4; ++u) {
+      const long long i = i0 + u;
+      float m = x[u][0];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) s += ex2_approx(fmaf(x[i], g.c, -mc));
+      for (int q = 1; q < 8; ++q) m = fmaxf(m, x[u][q]);
+      m = warp_max(m);
+      float sum = 0.f;
+      if (m != -INFINITY) {
+        const float mc = m * g.c;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) sum += ex2_approx(fmaf(x[u][q], g.c, -mc));
+      }
+      sum = warp_sum(sum);
+      if (lane == 0 && i < total) {
+        const int r = (int)(i / g.n_vt), t = (int)(i - (long long)r * g.n_vt);
+        g.dpart[(size_t)r * g.n_vt + t] = make_float4(m, sum, 0.f, 0.f);
+      }
     }
-    s = warp_sum(s);
-    if (lane == 0) g.dpart[(size_t)r * g.n_vt + t] = make_float4(m, s, 0.f, 0.f);
   }
   grid_dep_wait();
   trace_end(kTkFusedAux);
@@ -416,20 +446,44 @@ __device__ int draw_from_chunks(FinShared &sh, const Wt &w, const float *trow, c
       const int e0 = ch * chunk_len + lane * per, e1 = min(V, e0 + per);
       double ls = 0.0;
       int lp = -1;
-      for (int i = e0; i < e1; ++i) {
-        const float x = wval(w, __ldcg(trow + i), w.kind == 0 ? __ldcg(lrow + i) : 0.f);
-        ls += (double)x;
-        if (x > 0.f) lp = i;
-      }
-      const double inc = fv_warp_incl_scan(ls);
       int f = 0x7fffffff;
-      if (cross >= 0 && before + inc > tgt) {
-        double r = before + (inc - ls);
+      if (per <= 16) {
+        // the lane's weights in registers, every load issued at once
+        float xv[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int i = e0 + q;
+          xv[q] = q < per && i < e1 ? wval(w, __ldcg(trow + i), w.kind == 0 ? __ldcg(lrow + i) : 0.f) : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          ls += (double)xv[q];
+          if (xv[q] > 0.f) lp = e0 + q;
+        }
+        const double inc = fv_warp_incl_scan(ls);
+        if (cross >= 0 && before + inc > tgt) {
+          double r = before + (inc - ls);
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            r += (double)xv[q];
+            if (f == 0x7fffffff && xv[q] > 0.f && r > tgt) f = e0 + q;
+          }
+        }
+      } else {
         for (int i = e0; i < e1; ++i) {
-          r += (double)wval(w, __ldcg(trow + i), w.kind == 0 ? __ldcg(lrow + i) : 0.f);
-          if (r > tgt) {
-            f = i;
-            break;
+          const float x = wval(w, __ldcg(trow + i), w.kind == 0 ? __ldcg(lrow + i) : 0.f);
+          ls += (double)x;
+          if (x > 0.f) lp = i;
+        }
+        const double inc = fv_warp_incl_scan(ls);
+        if (cross >= 0 && before + inc > tgt) {
+          double r = before + (inc - ls);
+          for (int i = e0; i < e1; ++i) {
+            r += (double)wval(w, __ldcg(trow + i), w.kind == 0 ? __ldcg(lrow + i) : 0.f);
+            if (r > tgt) {
+              f = i;
+              break;
+            }
           }
         }
       }
@@ -459,50 +513,6 @@ __device__ void chunk_masses_from_partials(FinShared &sh, const float4 *pp, int 
       if (p.x != -INFINITY) s += (double)p.y * (double)ex2_approx((p.x - w.Mt) * w.c);
     }
     sh.csum[ch] = w.kind == 1 ? s * (double)w.iZt : s;
-  }
-}
-
-// Chunk masses of the residual weight by a pass over both rows: warp w takes
-// chunks w, w + warps, ... four at a time, each lane 16-byte loads of its
-// elements of both rows issued together.
-__device__ void chunk_masses_residual(FinShared &sh, const Wt &w, const float *trow, const float *lrow, int V,
-                                      int chunk_len) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nch = (V + chunk_len - 1) / chunk_len;
-  const bool vec = ((reinterpret_cast<uintptr_t>(trow) | reinterpret_cast<uintptr_t>(lrow)) & 15u) == 0;
-  constexpr int kU = 4;  // chunks per warp and round
-  for (int c0 = warp * kU; c0 < nch; c0 += kFinWarps * kU) {
-    float s[kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u) s[u] = 0.f;
-    const int nfull = (V / chunk_len);  // chunks without a ragged end
-    if (vec && c0 + kU <= nfull) {
-      // chunk_len / 128 float4 per lane and row per chunk
-      for (int q = 0; q < chunk_len / 128; ++q) {
-        float4 tv[kU], lv[kU];
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          const size_t e = (size_t)(c0 + u) * chunk_len + (size_t)(q * 32 + lane) * 4;
-          tv[u] = __ldcg(reinterpret_cast<const float4 *>(trow + e));
-          lv[u] = __ldcg(reinterpret_cast<const float4 *>(lrow + e));
-        }
-#pragma unroll
-        for (int u = 0; u < kU; ++u)
-          s[u] += wval(w, tv[u].x, lv[u].x) + wval(w, tv[u].y, lv[u].y) + wval(w, tv[u].z, lv[u].z) +
-                  wval(w, tv[u].w, lv[u].w);
-      }
-    } else {
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int e0 = (c0 + u) * chunk_len, e1 = min(V, e0 + chunk_len);
-        for (int i = e0 + lane; i < e1; i += 32) s[u] += wval(w, __ldcg(trow + i), __ldcg(lrow + i));
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const float t = warp_sum(s[u]);  // float: float64 is a small fraction of the float rate here
-      if (lane == 0 && c0 + u < nch) sh.csum[c0 + u] = (double)t;
-    }
   }
 }
 
@@ -580,19 +590,30 @@ __global__ void __launch_bounds__(kFinThreads) fv_finish_kernel(const FvArgs g, 
       tok = 0;
     }
   } else {
-    // position by position: u q(d) < p(d), taken by thread 0 and shared
-    if (threadIdx.x == 0) {
+    // position by position: u q(d) < p(d), taken by thread 0 and shared; the
+    // logits at the draft tokens are loaded by lanes j of warp 0 at once
+    if (warp == 0) {
+      float tdl = 0.f, ldl = 0.f;
+      int dl = -1;
+      if (lane < k) {
+        dl = __ldg(&dt[lane]);
+        if (dl >= 0 && dl < V) {
+          tdl = __ldcg(g.tgt + (size_t)(b * (k + 1) + lane) * V + dl);
+          ldl = __ldcg(g.draft + ((size_t)b * k + lane) * V + dl);
+        }
+      }
       int rj = -1, fl = 0;
       for (int j = 0; j < k; ++j) {
-        const int d = __ldg(&dt[j]);
+        const int d = __shfl_sync(0xffffffffu, dl, j);
+        const float tdj = __shfl_sync(0xffffffffu, tdl, j), ldj = __shfl_sync(0xffffffffu, ldl, j);
         if (d < 0 || d >= V) {
           fl |= kStatusBadToken;
           rj = j;
           break;
         }
         if (!(sh.M[j] > -INFINITY) || !(sh.Ml[j] > -INFINITY)) fl |= kStatusNonFinite;
-        const double td = (double)__ldcg(g.tgt + (size_t)(b * (k + 1) + j) * V + d);
-        const double ld = (double)__ldcg(g.draft + ((size_t)b * k + j) * V + d);
+        const double td = (double)tdj;
+        const double ld = (double)ldj;
         const double p = exp2((td - (double)sh.M[j]) * (double)c) / sh.Z[j];
         const double q = exp2((ld - (double)sh.Ml[j]) * (double)c) / sh.Zl[j];
         const double ua = (double)__ldg(&g.u_accept[(size_t)b * k + j]);
@@ -601,8 +622,10 @@ __global__ void __launch_bounds__(kFinThreads) fv_finish_kernel(const FvArgs g, 
           break;
         }
       }
-      sh.I[0] = rj;
-      sh.I[1] = fl;
+      if (lane == 0) {
+        sh.I[0] = rj;
+        sh.I[1] = fl;
+      }
     }
     __syncthreads();
     const int rej = sh.I[0];
@@ -616,22 +639,23 @@ __global__ void __launch_bounds__(kFinThreads) fv_finish_kernel(const FvArgs g, 
          rej >= 0 ? (float)(1.0 / sh.Zl[rej]) : 0.f, c};
     int chosen;
     if (rej >= 0) {
+      // the residual draw: the residual kernel's CTAs, one per chunk of the pair
       n_acc = rej;
-      w.kind = 0;
-      chunk_masses_residual(sh, w, trow, lrow, V, g.chunk);
-      chosen = draw_from_chunks(sh, w, trow, lrow, V, g.chunk, uf);
-      if (chosen < 0) {  // p = q everywhere: draw from p itself
-        w.kind = 1;
-        __syncthreads();
-        chunk_masses_from_partials(sh, g.part + (size_t)row * g.n_vt, g.n_vt, g.chunk / kVt, w);
-        chosen = draw_from_chunks(sh, w, trow, lrow, V, g.chunk, uf);
+      if (threadIdx.x == 0) {
+        float4 *r4 = reinterpret_cast<float4 *>(&g.rrec[b]);
+        r4[0] = make_float4(w.Mt, w.iZt, w.Ml, w.iZl);
+        reinterpret_cast<int4 *>(r4)[1] = make_int4(rej, row, 0, 0);
+        g.rcnt[b] = 0u;
       }
+      chosen = -2;  // written by the residual kernel
     } else {
       n_acc = k;
       chunk_masses_from_partials(sh, g.part + (size_t)row * g.n_vt, g.n_vt, g.chunk / kVt, w);
       chosen = draw_from_chunks(sh, w, trow, lrow, V, g.chunk, uf);
     }
-    if (chosen < 0) {
+    if (rej < 0 && threadIdx.x == 0)  // no residual draw for this sequence
+      reinterpret_cast<int4 *>(&g.rrec[b])[1] = make_int4(-1, 0, 0, 0);
+    if (chosen == -1) {
       flags |= kStatusNonFinite;
       chosen = 0;
     }
@@ -639,12 +663,204 @@ __global__ void __launch_bounds__(kFinThreads) fv_finish_kernel(const FvArgs g, 
   }
   if (threadIdx.x <= k) {
     const int t = threadIdx.x;
-    o.out_tok[(size_t)b * (k + 1) + t] = t < n_acc ? __ldg(&dt[t]) : (t == n_acc ? tok : -1);
+    if (!(t == n_acc && tok == -2))
+      o.out_tok[(size_t)b * (k + 1) + t] = t < n_acc ? __ldg(&dt[t]) : (t == n_acc ? tok : -1);
   }
   if (threadIdx.x == 0) {
     o.accept_len[b] = n_acc + 1;
     o.num_accepted[b] = n_acc;
     if (flags) set_status(g.status, flags);
+  }
+  trace_end(kTkFusedAux);
+}
+
+// ---------------------------------------------------------------- residual kernel
+
+namespace {
+
+// One warp: the crossing of u x (total of mass(0..n-1), summed in index
+// order): the smallest index whose running sum passes it, with the mass
+// before it; else the last index of positive mass (before = -1); else -1.
+template <typename F>
+__device__ int fv_warp_cross(F mass, int n, double u, double &tgt, double &before_out) {
+  const int lane = threadIdx.x & 31;
+  double tot = 0.0;
+  for (int b = 0; b < n; b += 32)
+    tot += __shfl_sync(0xffffffffu, fv_warp_incl_scan(b + lane < n ? mass(b + lane) : 0.0), 31);
+  tgt = u * tot;
+  int cross = -1, lastpos = -1;
+  double before = 0.0, run = 0.0;
+  for (int b = 0; b < n && cross < 0; b += 32) {
+    const double x = b + lane < n ? mass(b + lane) : 0.0;
+    const double incl = fv_warp_incl_scan(x);
+    const unsigned hit = __ballot_sync(0xffffffffu, b + lane < n && run + incl > tgt);
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      cross = b + l;
+      before = run + __shfl_sync(0xffffffffu, incl - x, l);
+    }
+    const unsigned pos = __ballot_sync(0xffffffffu, b + lane < n && x > 0.0);
+    if (pos) lastpos = b + 31 - __clz(pos);
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  before_out = cross >= 0 ? before : -1.0;
+  return cross >= 0 ? cross : lastpos;
+}
+
+// One warp: in the `len` elements from e0 (lane l a contiguous run of len / 32),
+// the element whose running sum (`before` ahead of e0) passes tgt; before < 0,
+// or nothing passing: the last element of positive weight; -1 if none.
+__device__ int fv_warp_rescan(const Wt &w, const float *trow, const float *lrow, int V, int e0, int len,
+                              double before, double tgt) {
+  const int lane = threadIdx.x & 31;
+  const int per = len / 32;
+  const int a0 = e0 + lane * per, a1 = min(V, a0 + per);
+  const bool pair = w.kind == 0;
+  double ls = 0.0;
+  int lp = -1;
+  for (int i = a0; i < a1; ++i) {
+    const float x = wval(w, __ldcg(trow + i), pair ? __ldcg(lrow + i) : 0.f);
+    ls += (double)x;
+    if (x > 0.f) lp = i;
+  }
+  const double inc = fv_warp_incl_scan(ls);
+  int f = 0x7fffffff;
+  if (before >= 0.0 && before + inc > tgt) {
+    double r = before + (inc - ls);
+    for (int i = a0; i < a1; ++i) {
+      const float x = wval(w, __ldcg(trow + i), pair ? __ldcg(lrow + i) : 0.f);
+      r += (double)x;
+      if (x > 0.f && r > tgt) {
+        f = i;
+        break;
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    f = min(f, __shfl_xor_sync(0xffffffffu, f, o));
+    lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
+  }
+  return f != 0x7fffffff ? f : lp;
+}
+
+}  // namespace
+
+// The residual draw of the stochastic call, after the finish kernel: CTA
+// (c, b) sums max(0, p - q) over the 16 sub-chunks of chunk c of sequence b's
+// rejecting pair (the stored target row and the draft row); the CTA that
+// completes the sequence finds the crossing chunk, then sub-chunk, then element
+// (float64 running sums in index order), and writes the replacement token.
+// Sequences without a rejection have nothing to do here.
+__global__ void __launch_bounds__(kResThreads) fv_residual_kernel(const FvArgs g, FvOut o) {
+  trace_start(kTkFusedAux);
+  __shared__ float sub[kResSubs];
+  __shared__ int s_last, s_tok;
+  const int ch = blockIdx.x, b = blockIdx.y, V = g.V, k = g.k;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dep_wait();  // the finish kernel's records
+  grid_dep_launch();
+  const float4 *r4 = reinterpret_cast<const float4 *>(&g.rrec[b]);
+  const float4 rx = __ldcg(r4);
+  const int4 ry = __ldcg(reinterpret_cast<const int4 *>(r4 + 1));
+  const int j = ry.x, row = ry.y;
+  if (j < 0 || !in_bounds(j < k && row == b * (k + 1) + j, g.status)) {
+    trace_end(kTkFusedAux);
+    return;
+  }
+  const Wt w{0, rx.x, rx.y, rx.z, rx.w, g.c};
+  const float *trow = g.tgt + (size_t)row * V, *lrow = g.draft + ((size_t)b * k + j) * V;
+  const bool vec = ((reinterpret_cast<uintptr_t>(trow) | reinterpret_cast<uintptr_t>(lrow)) & 15u) == 0;
+  // sub-chunks warp and warp + 8, a lane 4 float4 of each row of a sub-chunk
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int s = warp + 8 * h;
+    const int e0 = ch * kResChunk + s * kResSub;
+    float acc = 0.f;
+    if (vec && e0 + kResSub <= V) {
+      float4 tv[4], lv[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        tv[q] = __ldcg(reinterpret_cast<const float4 *>(trow + e0) + lane + 32 * q);
+        lv[q] = __ldcg(reinterpret_cast<const float4 *>(lrow + e0) + lane + 32 * q);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        acc += (wval(w, tv[q].x, lv[q].x) + wval(w, tv[q].y, lv[q].y)) +
+               (wval(w, tv[q].z, lv[q].z) + wval(w, tv[q].w, lv[q].w));
+    } else {
+      for (int i = e0 + lane; i < min(V, e0 + kResSub); i += 32) acc += wval(w, __ldcg(trow + i), __ldcg(lrow + i));
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) sub[s] = acc;
+  }
+  __syncthreads();
+  if (threadIdx.x < kResSubs) g.rsub[((size_t)b * g.nrc + ch) * kResSubs + threadIdx.x] = sub[threadIdx.x];
+  if (threadIdx.x == 0) {
+    double cm = 0.0;
+    for (int s = 0; s < kResSubs; ++s) cm += (double)sub[s];
+    g.rcm[(size_t)b * g.nrc + ch] = cm;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned arrived = atomic_add_acq_rel(&g.rcnt[b], 1u) + 1u;
+    s_last = arrived == (unsigned)g.nrc;
+    if (s_last) g.rcnt[b] = 0u;  // left zero
+  }
+  __syncthreads();
+  if (!s_last) {
+    trace_end(kTkFusedAux);
+    return;
+  }
+  if (warp == 0) {
+    const double u = (double)__ldg(&g.u_final[b]);
+    const double *cm = g.rcm + (size_t)b * g.nrc;
+    double tgt, base;
+    const int cx = fv_warp_cross([&](int i) { return __ldcg(&cm[i]); }, g.nrc, u, tgt, base);
+    int tok = -1;
+    if (cx >= 0) {
+      const float *sm = g.rsub + ((size_t)b * g.nrc + cx) * kResSubs;
+      // within the chunk: its sub-chunk masses against tgt - base
+      const double rel = base >= 0.0 ? tgt - base : 1e300;
+      const double x = lane < kResSubs ? (double)__ldcg(&sm[lane]) : 0.0;
+      const double incl = fv_warp_incl_scan(x);
+      const unsigned hit = __ballot_sync(0xffffffffu, lane < kResSubs && incl > rel);
+      const unsigned pos = __ballot_sync(0xffffffffu, lane < kResSubs && x > 0.0);
+      int s = -1;
+      double bef = -1.0;
+      if (hit) {
+        s = __ffs(hit) - 1;
+        bef = base + __shfl_sync(0xffffffffu, incl - x, s);
+      } else if (pos) {
+        s = 31 - __clz(pos);
+      }
+      if (s >= 0) tok = fv_warp_rescan(w, trow, lrow, V, cx * kResChunk + s * kResSub, kResSub, bef, tgt);
+    }
+    if (tok < 0) {
+      // the residual is zero everywhere (p = q): draw from p itself, over the
+      // row's 256-token tile masses from the GEMM's partials
+      const float4 *pp = g.part + (size_t)row * g.n_vt;
+      const Wt wp{2, w.Mt, 0.f, 0.f, 0.f, g.c};
+      double tg2, bf2;
+      const int tile = fv_warp_cross(
+          [&](int i) {
+            const float4 p = __ldcg(&pp[i]);
+            return p.x == -INFINITY ? 0.0 : (double)p.y * (double)ex2_approx((p.x - wp.Mt) * wp.c);
+          },
+          g.n_vt, u, tg2, bf2);
+      if (tile >= 0) tok = fv_warp_rescan(wp, trow, trow, V, tile * kVt, kVt, bf2, tg2);
+    }
+    if (lane == 0) s_tok = tok;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int tok = s_tok;
+    if (tok < 0) {
+      set_status(g.status, kStatusNonFinite);
+      tok = 0;
+    }
+    o.out_tok[(size_t)b * (k + 1) + j] = tok;
   }
   trace_end(kTkFusedAux);
 }
@@ -681,6 +897,11 @@ size_t fused_workspace_bytes(int B, int k, int V, int d, int mode) {
   if (mode == 1) {
     n += up256((size_t)B * k * n_vt * 16);  // the draft rows' partials
     n += up256(Na * (size_t)V * 4);         // stored logits (the residual draw reads one row)
+    const size_t nrc = ((size_t)V + kResChunk - 1) / kResChunk;
+    n += up256((size_t)B * sizeof(FvRes));  // residual records
+    n += up256((size_t)B * 4);              // residual arrival counters
+    n += up256((size_t)B * nrc * kResSubs * 4);
+    n += up256((size_t)B * nrc * 8);
   }
   return n;
 }
@@ -728,6 +949,15 @@ cudaError_t launch_fused_verify(const FusedCall &fc, cudaStream_t s, bool pdl) {
     g.dpart = reinterpret_cast<float4 *>(p);
     p += up256((size_t)fc.B * fc.k * g.n_vt * 16);
     g.tgt = reinterpret_cast<float *>(p);
+    p += up256((size_t)g.Na * fc.V * 4);
+    g.nrc = (fc.V + kResChunk - 1) / kResChunk;
+    g.rrec = reinterpret_cast<FvRes *>(p);
+    p += up256((size_t)fc.B * sizeof(FvRes));
+    g.rcnt = reinterpret_cast<unsigned *>(p);
+    p += up256((size_t)fc.B * 4);
+    g.rsub = reinterpret_cast<float *>(p);
+    p += up256((size_t)fc.B * g.nrc * kResSubs * 4);
+    g.rcm = reinterpret_cast<double *>(p);
   }
   g.chunk = kVt * ((g.n_vt + kMaxChunks - 1) / kMaxChunks);  // whole tiles, at most kMaxChunks chunks
 
@@ -755,7 +985,7 @@ cudaError_t launch_fused_verify(const FusedCall &fc, cudaStream_t s, bool pdl) {
   pattr[0].val.programmaticStreamSerializationAllowed = 1;
   if (fc.mode == 1) {  // the draft rows' statistics, beside the GEMM (it needs no smem)
     cudaLaunchConfig_t dcfg{};
-    dcfg.gridDim = dim3((unsigned)((g.n_vt + 7) / 8), (unsigned)(fc.B * fc.k));
+    dcfg.gridDim = dim3((unsigned)(2 * sms));  // grid-stride: two CTAs an SM, beside the GEMM's
     dcfg.blockDim = dim3(256);
     dcfg.stream = s;
     dcfg.attrs = pattr;
@@ -777,8 +1007,17 @@ cudaError_t launch_fused_verify(const FusedCall &fc, cudaStream_t s, bool pdl) {
   fcfg.attrs = attr;
   fcfg.numAttrs = pdl ? 1 : 0;
   note_launch();
-  return fc.mode == 1 ? cudaLaunchKernelEx(&fcfg, fv_finish_kernel<1>, g, o)
-                      : cudaLaunchKernelEx(&fcfg, fv_finish_kernel<0>, g, o);
+  if (fc.mode == 0) return cudaLaunchKernelEx(&fcfg, fv_finish_kernel<0>, g, o);
+  e = cudaLaunchKernelEx(&fcfg, fv_finish_kernel<1>, g, o);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t rcfg{};
+  rcfg.gridDim = dim3((unsigned)g.nrc, (unsigned)fc.B);
+  rcfg.blockDim = dim3(kResThreads);
+  rcfg.stream = s;
+  rcfg.attrs = attr;
+  rcfg.numAttrs = pdl ? 1 : 0;
+  note_launch();
+  return cudaLaunchKernelEx(&rcfg, fv_residual_kernel, g, o);
 }
 
 MTP_TRACE_COLLECTOR(fused)
