@@ -84,13 +84,14 @@ NCU_TRAFFIC = {
         },
     },
     ("fv_gemm_kernel + fv_finish_kernel", "fused_verify_b64_k3_d4096_v151936/greedy"): {
-        "bytes": 1250075392 + 3688192 + 2441984,
+        "bytes": 1250740224 + 3649280 + 2441984,
         "sources": {
-            "csrc/fused.cu": "5b1bc8195a89aed511bb6d471b486494514ea57e956a36a89ea4bb551e94cb07",
+            "csrc/fused.cu": "77ac3c64137bcb4309c1e318cef07d37dcb96255ecb2c97106329e14c5209632",
             "csrc/tcgen05.cuh": "e128ff6d7c8451d618848063024b7cd0a98c722dd1b86ef0d04e6a07a9070ee7",
             "csrc/common.cuh": "ccc7be3ffbab76f32e48e064231311046ac5ebb3caee7e3f3df14b4629b22b95",
             "csrc/internal.h": "2ab350d5622c22f47de0c469aabd5010981632626e75291fc2273994f1968187",
         },
+    },
     },
 }
 
