@@ -92,7 +92,6 @@ NCU_TRAFFIC = {
             "csrc/internal.h": "2ab350d5622c22f47de0c469aabd5010981632626e75291fc2273994f1968187",
         },
     },
-    },
 }
 
 
