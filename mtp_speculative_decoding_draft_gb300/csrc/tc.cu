@@ -545,31 +545,11 @@ __global__ void __launch_bounds__(32) tc_select_fin_kernel(DraftCtx c, const flo
   grid_dep_wait();
   grid_dep_launch();
   const float4 *pp = part + (size_t)b * nq;
-  // lane l owns sub-segments [l per, (l+1) per) in order; up to kSelStage of
-  // them are loaded into registers at once and reused below
+  // lane l owns sub-segments [l per, (l+1) per) in order
   const int per = (nq + 31) / 32, q0 = min(nq, lane * per), q1 = min(nq, q0 + per);
-  constexpr int kSelStage = 8;
-  const bool staged = per <= kSelStage;
-  float4 pv[kSelStage];
-#pragma unroll
-  for (int i = 0; i < kSelStage; ++i)
-    pv[i] = staged && q0 + i < q1 ? __ldcg(&pp[q0 + i]) : make_float4(-INFINITY, __int_as_float(0x7fffffff), 0.f, 0.f);
-  auto part_at = [&](int q) -> float4 {
-    if (staged) {
-      float4 v = pv[0];
-#pragma unroll
-      for (int i = 1; i < kSelStage; ++i)
-        if (q - q0 == i) v = pv[i];
-      return v;
-    }
-    return __ldcg(&pp[q]);
-  };
   float M = -INFINITY;
   int I = 0x7fffffff;
-  for (int q = q0; q < q1; ++q) {
-    const float4 v = part_at(q);
-    argmax_merge(M, I, v.x, __float_as_int(v.y));
-  }
+  for (int q = q0; q < q1; ++q) argmax_merge(M, I, pp[q].x, __float_as_int(pp[q].y));
   warp_argmax(M, I);
   int tok = I;
   const bool finite = !(M == -INFINITY || !(M == M));
@@ -580,7 +560,7 @@ __global__ void __launch_bounds__(32) tc_select_fin_kernel(DraftCtx c, const flo
   int lastq = -1;
   if (finite && (c.mode == 1 || c.k_eff)) {
     for (int q = q0; q < q1; ++q) {
-      const float4 v = part_at(q);
+      const float4 v = pp[q];
       const double m = v.x == -INFINITY ? 0.0 : (double)v.z * (double)exp2f((v.x - M) * cT);
       own += m;
       if (m > 0.0) lastq = q;
@@ -606,7 +586,7 @@ __global__ void __launch_bounds__(32) tc_select_fin_kernel(DraftCtx c, const flo
       if (lane == cl) {
         double cum = incl - own;
         for (int q = q0; q < q1; ++q) {
-          const float4 v = part_at(q);
+          const float4 v = pp[q];
           const double m = v.x == -INFINITY ? 0.0 : (double)v.z * (double)exp2f((v.x - M) * cT);
           if (cum + m > target) {
             qs = q;
