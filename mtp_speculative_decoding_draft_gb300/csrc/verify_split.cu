@@ -327,37 +327,54 @@ __device__ void decide(Shared &sh, const VerifyArgs &a, int b, int kb) {
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
+  // the accept decisions in order, in warp 0: lane j loads the logits at draft
+  // token j first, so the positions' loads are in flight together
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int dl = -1;
+    float tdl = 0.f, ldl = 0.f;
+    if (lane < kb) {
+      dl = __ldg(&a.draft_tok[(size_t)b * k + lane]);
+      if (dl >= 0 && dl < V) {
+        tdl = __ldg(seq_row(a, b, lane) + dl);
+        ldl = __ldg(seq_row(a, b, k + 1 + lane) + dl);
+      }
+    }
     int rj = -1, fl = 0;
     for (int j = 0; j < kb; ++j) {
-      const int d = __ldg(&a.draft_tok[(size_t)b * k + j]);
+      const int d = __shfl_sync(0xffffffffu, dl, j);
+      const float tdj = __shfl_sync(0xffffffffu, tdl, j), ldj = __shfl_sync(0xffffffffu, ldl, j);
       if (d < 0 || d >= V) {
         fl |= kStatusBadToken;
         rj = j;
         break;
       }
       if (!(sh.M[j] > -INFINITY) || !(sh.M[k + 1 + j] > -INFINITY)) fl |= kStatusNonFinite;
-      const double td = (double)__ldg(seq_row(a, b, j) + d);
-      const double ld = (double)__ldg(seq_row(a, b, k + 1 + j) + d);
-      const double p = exp2((td - (double)sh.M[j]) * (double)c) / sh.Z[j];
-      const double q = exp2((ld - (double)sh.M[k + 1 + j]) * (double)c) / sh.Z[k + 1 + j];
+      const double p = exp2(((double)tdj - (double)sh.M[j]) * (double)c) / sh.Z[j];
+      const double q = exp2(((double)ldj - (double)sh.M[k + 1 + j]) * (double)c) / sh.Z[k + 1 + j];
       const double ua = (double)__ldg(&a.u_accept[(size_t)b * k + j]);
       if (!(ua * q < p)) {
         rj = j;
         break;
       }
     }
-    sh.rej = rj;
-    sh.flags = fl;
-    if (rj >= 0) {
-      SplitRec r;
-      r.Mt = sh.M[rj];
-      r.iZt = (float)(1.0 / sh.Z[rj]);
-      r.Ml = sh.M[k + 1 + rj];
-      r.iZl = (float)(1.0 / sh.Z[k + 1 + rj]);
-      r.j = rj;
-      r.flags = fl;
-      a.srec[b] = r;
+    if (lane == 0) {
+      sh.rej = rj;
+      sh.flags = fl;
+      if (rj >= 0) {
+        SplitRec r;
+        r.Mt = sh.M[rj];
+        r.iZt = (float)(1.0 / sh.Z[rj]);
+        r.Ml = sh.M[k + 1 + rj];
+        r.iZl = (float)(1.0 / sh.Z[k + 1 + rj]);
+        r.j = rj;
+        r.flags = fl;
+        a.srec[b] = r;
+        __threadfence();
+      }
+      // published at once: the residual items of the sequence wait for it (a
+      // bonus draw's outputs need nothing of theirs)
+      st_release_u32(&a.sseq[4 * b + 2], rj >= 0 ? kDecidedReject : kDecidedDone);
     }
   }
   __syncthreads();
@@ -367,11 +384,6 @@ __device__ void decide(Shared &sh, const VerifyArgs &a, int b, int kb) {
     const int chosen =
         draw_from_stats(sh, w, a.spart + ((size_t)b * R + kb) * nch, nch, seq_row(a, b, kb), V, (double)__ldg(&a.u_final[b]));
     write_outputs(a, b, kb, chosen, sh.flags);
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();  // the record and the outputs, written by several threads
-    st_release_u32(&a.sseq[4 * b + 2], rj >= 0 ? kDecidedReject : kDecidedDone);
   }
 }
 
