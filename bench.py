@@ -68,25 +68,25 @@ NCU_TRAFFIC = {
         },
     },
     ("verify_kernel", "verify_sweep_b256_v151936_k3/greedy"): {
-        "bytes": 622426624 + 2995968,
+        "bytes": 622433280 + 3166720,
         "sources": {
-            "csrc/verify.cu": "5666bbd8cb2c586706845ad948da9b4a804e29544b6de62c7b9e185710960f4d",
+            "csrc/verify.cu": "60f2c266be9ff5946ad75c6869db05da5ca758bd1a3b7af83ee767041e6fb62a",
             "csrc/common.cuh": "ccc7be3ffbab76f32e48e064231311046ac5ebb3caee7e3f3df14b4629b22b95",
             "csrc/internal.h": "2ab350d5622c22f47de0c469aabd5010981632626e75291fc2273994f1968187",
         },
     },
     ("verify_split_kernel", "verify_sweep_b256_v151936_k3/stochastic"): {
-        "bytes": 1248843520 + 3457024,
+        "bytes": 1262258176 + 3521280,
         "sources": {
-            "csrc/verify_split.cu": "364ca393ddea89b834b5563c439eec3d8b073a44c2b3a90feb26df1a5f59e31a",
+            "csrc/verify_split.cu": "3c1d73fc44927cc4ca9bcd268d2f795d08ba5d569f1b8cbdc5cddaea0fdd9ec8",
             "csrc/common.cuh": "ccc7be3ffbab76f32e48e064231311046ac5ebb3caee7e3f3df14b4629b22b95",
             "csrc/internal.h": "2ab350d5622c22f47de0c469aabd5010981632626e75291fc2273994f1968187",
         },
     },
     ("fv_gemm_kernel + fv_finish_kernel", "fused_verify_b64_k3_d4096_v151936/greedy"): {
-        "bytes": 1250740224 + 3649280 + 2441984,
+        "bytes": 1250702848 + 3722496 + 2442240,
         "sources": {
-            "csrc/fused.cu": "77ac3c64137bcb4309c1e318cef07d37dcb96255ecb2c97106329e14c5209632",
+            "csrc/fused.cu": "d480c2e556aabb8667e40ba353e195c76031a75a1b4a6ce2bd79b062a8731cb9",
             "csrc/tcgen05.cuh": "e128ff6d7c8451d618848063024b7cd0a98c722dd1b86ef0d04e6a07a9070ee7",
             "csrc/common.cuh": "ccc7be3ffbab76f32e48e064231311046ac5ebb3caee7e3f3df14b4629b22b95",
             "csrc/internal.h": "2ab350d5622c22f47de0c469aabd5010981632626e75291fc2273994f1968187",

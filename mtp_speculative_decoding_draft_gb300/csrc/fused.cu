@@ -368,9 +368,11 @@ struct Wt {
 __device__ __forceinline__ float wval(const Wt &w, float t, float l) {
   const float e = ex2_approx((t - w.Mt) * w.c);
   if (w.kind == 2) return e;
-  const float p = e * w.iZt;
+  // both products rounded on their own (no fused multiply-add): where p and q
+  // are equal the residual must be exactly zero, so that the draw falls back to p
+  const float p = __fmul_rn(e, w.iZt);
   if (w.kind == 1) return p;
-  return fmaxf(0.f, p - ex2_approx((l - w.Ml) * w.c) * w.iZl);
+  return fmaxf(0.f, p - __fmul_rn(ex2_approx((l - w.Ml) * w.c), w.iZl));
 }
 
 // Row j's (max, partition sum relative to it) from its per-tile partials, in

@@ -204,9 +204,11 @@ __device__ __forceinline__ float weight(int kind, float t, float l, float Mt, fl
                                         float c) {
   const float e = ex2_approx((t - Mt) * c);
   if (kind == 2) return e;
-  const float p = e * iZt;
+  // both products rounded on their own (no fused multiply-add): where p and q
+  // are equal the residual must be exactly zero, so that the draw falls back to p
+  const float p = __fmul_rn(e, iZt);
   if (kind == 1) return p;
-  return fmaxf(0.f, p - ex2_approx((l - Ml) * c) * iZl);
+  return fmaxf(0.f, p - __fmul_rn(ex2_approx((l - Ml) * c), iZl));
 }
 
 __device__ __forceinline__ double warp_incl_scan_d(double v) {

@@ -108,7 +108,9 @@ struct Wt {
 __device__ __forceinline__ float wval(const Wt &w, float t, float l) {
   const float e = ex2_approx((t - w.Mt) * w.c);
   if (w.kind == 2) return e;
-  return fmaxf(0.f, e * w.iZt - ex2_approx((l - w.Ml) * w.c) * w.iZl);
+  // both products rounded on their own (no fused multiply-add): where p and q
+  // are equal the residual must be exactly zero, so that the draw falls back to p
+  return fmaxf(0.f, __fmul_rn(e, w.iZt) - __fmul_rn(ex2_approx((l - w.Ml) * w.c), w.iZl));
 }
 
 __device__ __forceinline__ float wsum4(const Wt &w, float4 t, float4 l) {

@@ -111,7 +111,8 @@ def run_fused_parity(B, k, V, d, T, seed, noise=0.5):
     return g_s, gg
 
 
-@pytest.mark.parametrize("B,k,V,d,T", [(3, 3, 5003, 256, 1.0),       # one 128-row tile, ragged vocabulary
+@pytest.mark.parametrize("B,k,V,d,T", [(1, 3, 9000, 128, 1.0),       # one sequence: two residual chunks
+                                       (3, 3, 5003, 256, 1.0),       # one 128-row tile, ragged vocabulary
                                        (37, 2, 20011, 512, 0.7),     # 111 rows
                                        (50, 3, 4099, 320, 1.3),      # two row tiles, the second partial
                                        (100, 3, 3001, 192, 1.0)])    # two row groups: the head streams twice

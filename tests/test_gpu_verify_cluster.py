@@ -54,3 +54,23 @@ def test_stochastic_sweep_k3_full_size(kernel):
     d = _draft_tokens_from_q(inp["draft_logits"], inp["u_draft"], w.T)
     exc, L = _check(inp["target_logits"], inp["draft_logits"], d, inp["u_accept"], inp["u_final"], STOCH, w.T)
     print("%s kernel: mean accepted length %.3f, excused %d" % (kernel, L.mean(), exc))
+
+
+def test_stochastic_residual_zero_draws_from_p(kernel):
+    """Identical target and draft rows, with the same masked (-inf) entries,
+    and a draft token at a masked position: p(d) = q(d) = 0, so u q(d) < p(d)
+    fails and the position rejects, while max(0, p - q) is zero everywhere.
+    The rule then draws from p itself, as the oracle does."""
+    rng = np.random.default_rng(78)
+    B, k, V = 6, 2, 3 * 8192 + 4
+    t = (rng.standard_normal((B, k + 1, V)) * 3).astype(np.float32)
+    mask = rng.random(V) < 0.05
+    t[:, :, mask] = -np.inf
+    masked = np.nonzero(mask)[0]
+    l = t[:, :k].copy()
+    d = np.array([[int(rng.choice(masked)) if j == 0 else int(rng.integers(0, V)) for j in range(k)]
+                  for _ in range(B)], np.int32)
+    ua = rng.random((B, k)).astype(np.float32)
+    uf = rng.random(B).astype(np.float32)
+    exc, L = _check(t, l, d, ua, uf, STOCH, 1.0)
+    assert np.all(L == 1)   # every sequence rejects its first draft
