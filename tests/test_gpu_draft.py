@@ -101,6 +101,13 @@ def test_gqa_group_of_five(mode):
     run_draft_parity(GQA5, mode, GQA5.T)
 
 
+@pytest.mark.parametrize("T", [0.05, 20.0])
+def test_stochastic_temperature_extremes(T):
+    """The draft sampler at a near one-hot and a near-uniform temperature."""
+    r = run_draft_parity(MID, STOCH, T, ctx_fix=[1, 64, 200])
+    print("mid T=%g max rel L2 %.3g excused %d" % (T, max(r["rel_l2"]), r["excused"]))
+
+
 def test_single_greedy_full_size():
     r = run_draft_parity(W.SINGLE_GREEDY, GREEDY, 1.0)
     print("full-size greedy: rel L2 per depth", ["%.2e" % e for e in r["rel_l2"]])

@@ -40,3 +40,11 @@ TC40 = W.Workload("tc_b40_d384_v4099", B=40, k=3, V=4099, d=384, Hq=6, Hkv=2, Dh
 def test_tc_batch_of_40(mode):
     r = run_draft_parity(TC40, mode, TC40.T, seqs=[0, 17, 31, 32, 39])
     print("tc40 mode=%d max rel L2 %.3g excused %d" % (mode, max(r["rel_l2"]), r["excused"]))
+
+
+@pytest.mark.parametrize("T", [0.05, 20.0])
+def test_tc_stochastic_temperature_extremes(T):
+    """The tensor-core path's sampler at a near one-hot and a near-uniform
+    temperature."""
+    r = run_draft_parity(TC20, STOCH, T)
+    print("tc20 T=%g max rel L2 %.3g excused %d" % (T, max(r["rel_l2"]), r["excused"]))

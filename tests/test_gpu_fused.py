@@ -115,7 +115,9 @@ def run_fused_parity(B, k, V, d, T, seed, noise=0.5):
                                        (3, 3, 5003, 256, 1.0),       # one 128-row tile, ragged vocabulary
                                        (37, 2, 20011, 512, 0.7),     # 111 rows
                                        (50, 3, 4099, 320, 1.3),      # two row tiles, the second partial
-                                       (100, 3, 3001, 192, 1.0)])    # two row groups: the head streams twice
+                                       (100, 3, 3001, 192, 1.0),     # two row groups: the head streams twice
+                                       (6, 3, 9000, 128, 0.05),      # near one-hot rows
+                                       (6, 3, 9000, 128, 20.0)])     # near-uniform rows, small residual
 def test_fused_ragged_shapes(B, k, V, d, T):
     run_fused_parity(B, k, V, d, T, seed=9000 + B)
 

@@ -74,3 +74,14 @@ def test_stochastic_residual_zero_draws_from_p(kernel):
     uf = rng.random(B).astype(np.float32)
     exc, L = _check(t, l, d, ua, uf, STOCH, 1.0)
     assert np.all(L == 1)   # every sequence rejects its first draft
+
+
+@pytest.mark.parametrize("T", [0.05, 20.0])
+def test_stochastic_temperature_extremes(kernel, T):
+    """Near one-hot (T = 0.05: scaled logits spread over hundreds, most exp2
+    terms underflow) and near uniform (T = 20: p and q differ by a few percent,
+    so the residual max(0, p - q) is a small difference of close values) over
+    a vocabulary of three sub-chunk groups and a 4-logit tail."""
+    t, l, d, ua, uf = _case(24, 3, 3 * 8192 + 4, T, seed=7800 + int(T * 10))
+    exc, L = _check(t, l, d, ua, uf, STOCH, T)
+    print("%s kernel T=%g: mean accepted length %.3f, excused %d" % (kernel, T, L.mean(), exc))

@@ -235,6 +235,25 @@ def test_low_temperature_reduces_to_greedy():
         assert (g_out, g_a) == (s_out, s_a)
 
 
+def test_high_temperature_reduces_to_uniform():
+    """As T grows, p_j and q_j both tend to 1/V, so p(d)/q(d) -> 1: every draft
+    with u < 1 - O(1/T) is accepted and the bonus token is the uniform draw
+    floor(u V) of the inverse CDF."""
+    rng = np.random.default_rng(52)
+    V, k, T = 257, 4, 1e9
+    for _ in range(100):
+        t = rng.standard_normal((k + 1, V)) * 5
+        l = rng.standard_normal((k, V)) * 5
+        d = [int(x) for x in rng.integers(0, V, size=k)]
+        ua = rng.random(k) * 0.999
+        uf = float(rng.random())
+        if abs(uf * V - round(uf * V)) < 1e-6:
+            continue
+        out, a = verify_stochastic_one(t, l, d, ua, uf, T)
+        assert a == k and out[:k] == d
+        assert out[k] == int(np.floor(uf * V))
+
+
 def test_batched_outputs_bounds_and_padding():
     rng = np.random.default_rng(61)
     B, k, V = 40, 4, 300
