@@ -76,9 +76,10 @@ NCU_TRAFFIC = {
         },
     },
     ("verify_split_kernel", "verify_sweep_b256_v151936_k3/stochastic"): {
-        "bytes": 1262258176 + 3521280,
+        "bytes": 1169289216 + 2980096,
         "sources": {
-            "csrc/verify_split.cu": "3c1d73fc44927cc4ca9bcd268d2f795d08ba5d569f1b8cbdc5cddaea0fdd9ec8",
+            "csrc/verify_split.cu": "1534709eb14d8469051a94bbcbc6af85b9f5506abe030c97f2b325b311dc5dae",
+            "csrc/verify.cu": "f5fc0310bc0803d8610b522263a676741829b2d28da6924a064b3d3158681d56",
             "csrc/common.cuh": "ccc7be3ffbab76f32e48e064231311046ac5ebb3caee7e3f3df14b4629b22b95",
             "csrc/internal.h": "2ab350d5622c22f47de0c469aabd5010981632626e75291fc2273994f1968187",
         },

@@ -1106,8 +1106,8 @@ void verify_bind_state(VerifyArgs &a, void *state) {
   a.rec = reinterpret_cast<unsigned long long *>(p);
   p += up256((size_t)a.B * (a.k + 1) * 8);
   // residual items start about this many 128 KB items after their sequence's statistics
-  split_bind_state(a, p, (int)std::max(1ll, std::min(1ll << 20, env_int("MTP_SPLIT_LAG", 256))));
-  a.shint = (int)std::max(0ll, std::min(2ll, env_int("MTP_SPLIT_HINT", 1)));
+  split_bind_state(a, p, (int)std::max(1ll, std::min(1ll << 20, env_int("MTP_SPLIT_LAG", 512))));
+  a.shint = (int)std::max(0ll, std::min(12ll, env_int("MTP_SPLIT_HINT", 4)));
 }
 
 bool plan_verify(int B, int k, int V, VerifyPlan *p) {

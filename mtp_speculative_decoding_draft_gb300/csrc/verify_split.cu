@@ -402,10 +402,11 @@ __device__ void statistics_item(Shared &sh, const VerifyArgs &a, int b, int loca
     const float *src = seq_row(a, b, i);
     const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
     // pair rows (t_j, q_j, j < kb) may be read again by the residual pass
-    const bool pair_row = i <= k ? i < kb : true;
+    // (hint 3 + n: only the pairs j <= n are kept, the first rejection's usual positions)
+    const bool pair_row = (i <= k ? i < kb : true) && (a.shint < 3 || (i <= k ? i : i - (k + 1)) <= a.shint - 3);
     const uint64_t pol = a.shint == 0 ? l2_policy_evict_normal_all()
                          : !pair_row  ? l2_policy_evict_first()
-                         : a.shint == 1 ? l2_policy_evict_last() : l2_policy_evict_normal_all();
+                         : a.shint != 2 ? l2_policy_evict_last() : l2_policy_evict_normal_all();
 #pragma unroll 1
     for (int p = 0; p < kPasses; ++p) {
       const int e0 = ch * kChunk + p * kPiece, n = min(kPiece, V - e0);
