@@ -68,9 +68,9 @@ NCU_TRAFFIC = {
         },
     },
     ("verify_kernel", "verify_sweep_b256_v151936_k3/greedy"): {
-        "bytes": 622433280 + 3166720,
+        "bytes": 622470656 + 2755328,
         "sources": {
-            "csrc/verify.cu": "60f2c266be9ff5946ad75c6869db05da5ca758bd1a3b7af83ee767041e6fb62a",
+            "csrc/verify.cu": "f5fc0310bc0803d8610b522263a676741829b2d28da6924a064b3d3158681d56",
             "csrc/common.cuh": "ccc7be3ffbab76f32e48e064231311046ac5ebb3caee7e3f3df14b4629b22b95",
             "csrc/internal.h": "2ab350d5622c22f47de0c469aabd5010981632626e75291fc2273994f1968187",
         },
