@@ -17,16 +17,20 @@
 //   logits: the residual draw needs every element of the first rejecting row
 //   once the target's normaliser is known, and reading that row back is far
 //   cheaper than streaming E a second time to recompute it.
-// fv_draft_stats_kernel (stochastic, first): the draft rows' per-tile (max,
-//   sum of exp2) in the same tiling, every draft logit read once.
+// fv_draft_stats_kernel (stochastic, beside the GEMM): the draft rows'
+//   per-tile (max, sum of exp2) in the same tiling, every draft logit read
+//   once; its warps claim tiles from a counter, so that however many of its
+//   CTAs find room beside the GEMM's, those take all the tiles.
 // fv_finish_kernel: one CTA per sequence combines the partials of its rows in
 //   vocabulary-tile order and takes the decisions of spec_verify (the same
-//   rule): greedy longest prefix; stochastic u q(d) < p(d) position by
-//   position, then the inverse-CDF draw at u_final -- over max(0, p - q) of the
-//   first rejecting row (over p if that is identically zero), which takes one
-//   pass over that row's target and draft logits, or over p of row k when
-//   every draft is accepted, whose tile masses follow from the partials so
-//   that only the crossing tile is read again.
+//   rule): greedy longest prefix and the argmax; stochastic u q(d) < p(d) at
+//   every position at once, the first rejection as the position-by-position
+//   rule finds it.
+// fv_residual_kernel (stochastic): the inverse-CDF draw at u_final -- over
+//   max(0, p - q) of the first rejecting pair (over p if that is identically
+//   zero), one CTA per 16384 logits of the pair, or over p of row k when every
+//   draft is accepted, whose tile masses follow from the partials so that only
+//   the crossing tile is read again.
 #include <cuda.h>
 #include <stdlib.h>
 
@@ -48,11 +52,11 @@ constexpr int kMaxMt = 2;         // hidden-row tiles per unit: 2 x 256 TMEM col
 constexpr int kSmemBudget = 227 * 1024 - 1024 - 256;
 constexpr int kFinThreads = 512;
 constexpr int kFinWarps = kFinThreads / 32;
-constexpr int kMaxChunks = 4096;  // inverse-CDF chunk sums per row, at most (chunks of whole tiles)
-constexpr int kResChunk = 8192;   // logits of both rows of a rejecting pair per residual CTA
+constexpr int kResChunk = 16384;  // logits of both rows of a rejecting pair per residual CTA
 constexpr int kResThreads = 256;
 constexpr int kResSub = 512;      // residual sub-chunk
-constexpr int kResSubs = kResChunk / kResSub;  // 16
+constexpr int kResSubs = kResChunk / kResSub;  // 32 (one warp's lanes take them)
+static_assert(kResSubs <= 32 && kResSubs % 8 == 0, "sub-chunks of a residual CTA");
 
 __host__ __device__ inline uint32_t fv_stage_bytes(int mt) { return (uint32_t)mt * kATile + kBTile; }
 
@@ -75,7 +79,6 @@ struct FvArgs {
   int n_mt, groups;       // 128-row tiles per unit; row groups of n_mt tiles
   int n_vt, kbs;          // 256-row vocabulary tiles; 64-wide k-blocks
   int stages, nunits;     // ring depth; (group, vocabulary tile) units
-  int chunk;              // elements per chunk of the finish kernel's draws (whole 256-token tiles)
   const int *draft_tok;   // [B, k]
   const float *draft;     // [B, k, V] (stochastic)
   const float *u_accept;  // [B, k]
@@ -84,6 +87,7 @@ struct FvArgs {
   float4 *dpart;          // [B k, n_vt] (max, sum of exp2) of the draft rows (stochastic)
   float *tgt;             // [Na, V] stored logits (stochastic), else null
   int *status;
+  unsigned *dctr;         // draft tiles claimed (in the status slot; zeroed by the finish kernel)
   // stochastic: the residual draw, spread over one CTA per kResChunk logits
   int nrc;                // residual chunks per row
   FvRes *rrec;            // [B] the first rejection of each sequence
@@ -287,11 +291,16 @@ __global__ void __launch_bounds__(kFvThreads, 1) fv_gemm_kernel(const __grid_con
 // done, so that the finish kernel's wait on this kernel covers both.
 __global__ void __launch_bounds__(256) fv_draft_stats_kernel(const FvArgs g) {
   trace_start(kTkFusedAux);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31;
   grid_dep_launch();
   const long long total = (long long)g.Na / (g.k + 1) * g.k * g.n_vt;  // B k rows x n_vt tiles
-  const long long stride = (long long)gridDim.x * 8 * 4;
-  for (long long i0 = ((long long)blockIdx.x * 8 + warp) * 4; i0 < total; i0 += stride) {
+  // each warp claims four tiles at a time: however many of the CTAs find room
+  // beside the GEMM's, those that run take all the tiles
+  for (;;) {
+    long long i0 = 0;
+    if (lane == 0) i0 = (long long)atomicAdd(g.dctr, 4u);
+    i0 = __shfl_sync(0xffffffffu, i0, 0);
+    if (i0 >= total) break;
     float x[4][8];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -332,7 +341,10 @@ __global__ void __launch_bounds__(256) fv_draft_stats_kernel(const FvArgs g) {
       }
     }
   }
+  __syncthreads();
+  trace_mark(kTkFusedAux, 0);  // this CTA found no tile left
   grid_dep_wait();
+  trace_dep(kTkFusedAux);
   trace_end(kTkFusedAux);
 }
 
@@ -354,8 +366,6 @@ struct FinShared {
   float M[9], Ml[8];
   double Z[9], Zl[8];
   int I[9];
-  int chosen;
-  double csum[kMaxChunks];
 };
 
 // Sampling weight of an element: the residual max(0, p - q) (kind 0), the
@@ -377,29 +387,30 @@ __device__ __forceinline__ float wval(const Wt &w, float t, float l) {
 
 // Row j's (max, partition sum relative to it) from its per-tile partials, in
 // tile order per lane, lanes combined in a fixed tree (warp-collective).  The
-// lane's partials are loaded eight at a time, so that their loads overlap.
+// lane's (max, sum) pairs are loaded 24 at a time (all of them, up to 768
+// tiles a row), so that their loads overlap.
 __device__ __forceinline__ void combine_lse(const float4 *pp, int n_vt, float c, float &M, double &Z) {
+  constexpr int NB = 24;
   const int lane = threadIdx.x & 31;
   float m = -INFINITY;
   double z = 0.0;
-  for (int t0 = lane; t0 < n_vt; t0 += 8 * 32) {  // online over batches of eight tiles
-    float2 p[8];
+  for (int t0 = lane; t0 < n_vt; t0 += NB * 32) {  // online over batches of NB tiles
+    float2 p[NB];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < NB; ++i) {
       const int t = t0 + 32 * i;
-      const float4 v = t < n_vt ? __ldcg(&pp[t]) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
-      p[i] = make_float2(v.x, v.y);
+      p[i] = t < n_vt ? __ldcg(reinterpret_cast<const float2 *>(pp + t)) : make_float2(-INFINITY, 0.f);
     }
     float bm = p[0].x;
 #pragma unroll
-    for (int i = 1; i < 8; ++i) bm = fmaxf(bm, p[i].x);
+    for (int i = 1; i < NB; ++i) bm = fmaxf(bm, p[i].x);
     if (bm > m) {
       if (m != -INFINITY) z *= (double)ex2_approx((m - bm) * c);
       m = bm;
     }
     if (m != -INFINITY)
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < NB; ++i)
         if (p[i].x != -INFINITY) z += (double)p[i].y * (double)ex2_approx((p[i].x - m) * c);
   }
   // lanes: rescale to the warp maximum, then sum in a fixed tree
@@ -409,121 +420,12 @@ __device__ __forceinline__ void combine_lse(const float4 *pp, int n_vt, float c,
   Z = warp_sum_d(z);
 }
 
-// The inverse-CDF draw once the chunk masses csum[0, nch) are in shared
-// memory (chunk = chunk_len elements): the smallest i with C_i > u S, else the
-// last index of positive weight, -1 if all weights are zero.  Warp 0 scans the
-// chunks, then rescans the crossing chunk in float64 (lane l a contiguous run
-// of chunk_len / 32 elements), with weights wval(w, t[i], l[i]).
-__device__ int draw_from_chunks(FinShared &sh, const Wt &w, const float *trow, const float *lrow, int V,
-                                int chunk_len, double u) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nch = (V + chunk_len - 1) / chunk_len;
-  __syncthreads();
-  if (warp == 0) {
-    double tot = 0.0;
-    for (int b = 0; b < nch; b += 32) {
-      const double x = b + lane < nch ? sh.csum[b + lane] : 0.0;
-      tot += __shfl_sync(0xffffffffu, fv_warp_incl_scan(x), 31);
-    }
-    const double tgt = u * tot;
-    int cross = -1, lastpos = -1;
-    double before = 0.0, run = 0.0;
-    for (int b = 0; b < nch && cross < 0; b += 32) {
-      const double x = b + lane < nch ? sh.csum[b + lane] : 0.0;
-      const double incl = fv_warp_incl_scan(x);
-      const unsigned hit = __ballot_sync(0xffffffffu, b + lane < nch && run + incl > tgt);
-      if (hit) {
-        const int l = __ffs(hit) - 1;
-        cross = b + l;
-        before = run + __shfl_sync(0xffffffffu, incl - x, l);
-      }
-      const unsigned pos = __ballot_sync(0xffffffffu, b + lane < nch && x > 0.0);
-      if (pos) lastpos = b + 31 - __clz(pos);
-      run += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    int found = -1;
-    const int ch = cross >= 0 ? cross : lastpos;
-    if (ch >= 0) {
-      const int per = chunk_len / 32;
-      const int e0 = ch * chunk_len + lane * per, e1 = min(V, e0 + per);
-      double ls = 0.0;
-      int lp = -1;
-      int f = 0x7fffffff;
-      if (per <= 16) {
-        // the lane's weights in registers, every load issued at once
-        float xv[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int i = e0 + q;
-          xv[q] = q < per && i < e1 ? wval(w, __ldcg(trow + i), w.kind == 0 ? __ldcg(lrow + i) : 0.f) : 0.f;
-        }
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          ls += (double)xv[q];
-          if (xv[q] > 0.f) lp = e0 + q;
-        }
-        const double inc = fv_warp_incl_scan(ls);
-        if (cross >= 0 && before + inc > tgt) {
-          double r = before + (inc - ls);
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            r += (double)xv[q];
-            if (f == 0x7fffffff && xv[q] > 0.f && r > tgt) f = e0 + q;
-          }
-        }
-      } else {
-        for (int i = e0; i < e1; ++i) {
-          const float x = wval(w, __ldcg(trow + i), w.kind == 0 ? __ldcg(lrow + i) : 0.f);
-          ls += (double)x;
-          if (x > 0.f) lp = i;
-        }
-        const double inc = fv_warp_incl_scan(ls);
-        if (cross >= 0 && before + inc > tgt) {
-          double r = before + (inc - ls);
-          for (int i = e0; i < e1; ++i) {
-            r += (double)wval(w, __ldcg(trow + i), w.kind == 0 ? __ldcg(lrow + i) : 0.f);
-            if (r > tgt) {
-              f = i;
-              break;
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        f = min(f, __shfl_xor_sync(0xffffffffu, f, o));
-        lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
-      }
-      found = f != 0x7fffffff ? f : lp;
-    }
-    if (lane == 0) sh.chosen = found;
-  }
-  __syncthreads();
-  return sh.chosen;
-}
-
-// Chunk masses of a target-only weight (kinds 1 and 2) from the row's tile
-// partials: a tile's mass is its sum of exp2((t - m) c) rescaled to the row's
-// maximum (and, for kind 1, divided by the partition sum).
-__device__ void chunk_masses_from_partials(FinShared &sh, const float4 *pp, int n_vt, int tiles_per_chunk,
-                                           const Wt &w) {
-  const int nch = (n_vt + tiles_per_chunk - 1) / tiles_per_chunk;
-  for (int ch = threadIdx.x; ch < nch; ch += kFinThreads) {
-    double s = 0.0;
-    for (int t = ch * tiles_per_chunk; t < min(n_vt, (ch + 1) * tiles_per_chunk); ++t) {
-      const float4 p = __ldcg(&pp[t]);
-      if (p.x != -INFINITY) s += (double)p.y * (double)ex2_approx((p.x - w.Mt) * w.c);
-    }
-    sh.csum[ch] = w.kind == 1 ? s * (double)w.iZt : s;
-  }
-}
-
 }  // namespace
 
 // One CTA per sequence: the decisions of spec_verify from the GEMM's
 // partials (and, stochastic, the draft rows' partials), then the draw.
 template <int MODE>
-__global__ void __launch_bounds__(kFinThreads) fv_finish_kernel(const FvArgs g, FvOut o) {
+__global__ void __launch_bounds__(kFinThreads, 1) fv_finish_kernel(const FvArgs g, FvOut o) {
   trace_start(kTkFusedAux);
   extern __shared__ __align__(16) unsigned char fin_smem[];
   FinShared &sh = *reinterpret_cast<FinShared *>(fin_smem);
@@ -532,6 +434,8 @@ __global__ void __launch_bounds__(kFinThreads) fv_finish_kernel(const FvArgs g, 
   const float c = g.c;
   grid_dep_wait();
   grid_dep_launch();
+  trace_dep(kTkFusedAux);
+  if (MODE == 1 && b == 0 && threadIdx.x == 0) *g.dctr = 0u;  // the draft statistics have ended: left zero
   // each row's statistics from its partials, in vocabulary-tile order
   for (int j = warp; j <= k; j += kFinWarps) {
     const float4 *pp = g.part + (size_t)(b * (k + 1) + j) * g.n_vt;
@@ -563,8 +467,8 @@ __global__ void __launch_bounds__(kFinThreads) fv_finish_kernel(const FvArgs g, 
       }
     }
   }
-  if (MODE == 1)
-    for (int j = warp; j < k; j += kFinWarps) {
+  if (MODE == 1)  // the draft rows on the warps after the target rows'
+    for (int j = (warp + kFinWarps - (k + 1) % kFinWarps) % kFinWarps; j < k; j += kFinWarps) {
       float m;
       double z;
       combine_lse(g.dpart + (size_t)(b * k + j) * g.n_vt, g.n_vt, c, m, z);
@@ -574,6 +478,7 @@ __global__ void __launch_bounds__(kFinThreads) fv_finish_kernel(const FvArgs g, 
       }
     }
   __syncthreads();
+  trace_mark(kTkFusedAux, 0);  // rows' statistics combined
   const int *dt = g.draft_tok + (size_t)b * k;
   int n_acc = 0, tok = 0, flags = 0;
   if (MODE == 0) {
@@ -592,76 +497,52 @@ __global__ void __launch_bounds__(kFinThreads) fv_finish_kernel(const FvArgs g, 
       tok = 0;
     }
   } else {
-    // position by position: u q(d) < p(d), taken by thread 0 and shared; the
-    // logits at the draft tokens are loaded by lanes j of warp 0 at once
+    // u q(d) < p(d) at every position at once, lane j of warp 0 position j
+    // (its token, the logits there and its uniform loaded together); the
+    // first rejection and the flags are those of taking them in order
     if (warp == 0) {
       float tdl = 0.f, ldl = 0.f;
       int dl = -1;
+      double ua = 0.0;
       if (lane < k) {
         dl = __ldg(&dt[lane]);
+        ua = (double)__ldg(&g.u_accept[(size_t)b * k + lane]);
         if (dl >= 0 && dl < V) {
           tdl = __ldcg(g.tgt + (size_t)(b * (k + 1) + lane) * V + dl);
           ldl = __ldcg(g.draft + ((size_t)b * k + lane) * V + dl);
         }
       }
-      int rj = -1, fl = 0;
-      for (int j = 0; j < k; ++j) {
-        const int d = __shfl_sync(0xffffffffu, dl, j);
-        const float tdj = __shfl_sync(0xffffffffu, tdl, j), ldj = __shfl_sync(0xffffffffu, ldl, j);
-        if (d < 0 || d >= V) {
-          fl |= kStatusBadToken;
-          rj = j;
-          break;
-        }
-        if (!(sh.M[j] > -INFINITY) || !(sh.Ml[j] > -INFINITY)) fl |= kStatusNonFinite;
-        const double td = (double)tdj;
-        const double ld = (double)ldj;
-        const double p = exp2((td - (double)sh.M[j]) * (double)c) / sh.Z[j];
-        const double q = exp2((ld - (double)sh.Ml[j]) * (double)c) / sh.Zl[j];
-        const double ua = (double)__ldg(&g.u_accept[(size_t)b * k + j]);
-        if (!(ua * q < p)) {
-          rj = j;
-          break;
-        }
+      const bool valid = dl >= 0 && dl < V;
+      bool finite = true, accept = true;
+      if (lane < k && valid) {
+        finite = sh.M[lane] > -INFINITY && sh.Ml[lane] > -INFINITY;
+        const double p = exp2(((double)tdl - (double)sh.M[lane]) * (double)c) / sh.Z[lane];
+        const double q = exp2(((double)ldl - (double)sh.Ml[lane]) * (double)c) / sh.Zl[lane];
+        accept = ua * q < p;
       }
+      int fl;
+      const int rj = first_rejection(k, valid, finite, accept, fl);
       if (lane == 0) {
         sh.I[0] = rj;
         sh.I[1] = fl;
       }
     }
     __syncthreads();
+    trace_mark(kTkFusedAux, 1);  // decisions taken
     const int rej = sh.I[0];
     flags |= sh.I[1];
-    const double uf = (double)__ldg(&g.u_final[b]);
-    const int row = b * (k + 1) + (rej >= 0 ? rej : k);
-    const float *trow = g.tgt + (size_t)row * V;
-    const float *lrow = rej >= 0 ? g.draft + ((size_t)b * k + rej) * V : trow;
+    // the draw is the residual kernel's: over max(0, p - q) of the rejected
+    // pair, or over p of row k when every draft is accepted
     const int r = rej >= 0 ? rej : k;
-    Wt w{2, sh.M[r], (float)(1.0 / sh.Z[r]), rej >= 0 ? sh.Ml[rej] : 0.f,
-         rej >= 0 ? (float)(1.0 / sh.Zl[rej]) : 0.f, c};
-    int chosen;
-    if (rej >= 0) {
-      // the residual draw: the residual kernel's CTAs, one per chunk of the pair
-      n_acc = rej;
-      if (threadIdx.x == 0) {
-        float4 *r4 = reinterpret_cast<float4 *>(&g.rrec[b]);
-        r4[0] = make_float4(w.Mt, w.iZt, w.Ml, w.iZl);
-        reinterpret_cast<int4 *>(r4)[1] = make_int4(rej, row, 0, 0);
-        g.rcnt[b] = 0u;
-      }
-      chosen = -2;  // written by the residual kernel
-    } else {
-      n_acc = k;
-      chunk_masses_from_partials(sh, g.part + (size_t)row * g.n_vt, g.n_vt, g.chunk / kVt, w);
-      chosen = draw_from_chunks(sh, w, trow, lrow, V, g.chunk, uf);
+    n_acc = r;
+    if (threadIdx.x == 0) {
+      float4 *r4 = reinterpret_cast<float4 *>(&g.rrec[b]);
+      r4[0] = make_float4(sh.M[r], (float)(1.0 / sh.Z[r]), rej >= 0 ? sh.Ml[rej] : 0.f,
+                          rej >= 0 ? (float)(1.0 / sh.Zl[rej]) : 0.f);
+      reinterpret_cast<int4 *>(r4)[1] = make_int4(r, b * (k + 1) + r, 0, 0);
+      g.rcnt[b] = 0u;
     }
-    if (rej < 0 && threadIdx.x == 0)  // no residual draw for this sequence
-      reinterpret_cast<int4 *>(&g.rrec[b])[1] = make_int4(-1, 0, 0, 0);
-    if (chosen == -1) {
-      flags |= kStatusNonFinite;
-      chosen = 0;
-    }
-    tok = chosen;
+    tok = -2;  // written by the residual kernel
   }
   if (threadIdx.x <= k) {
     const int t = threadIdx.x;
@@ -709,32 +590,50 @@ __device__ int fv_warp_cross(F mass, int n, double u, double &tgt, double &befor
   return cross >= 0 ? cross : lastpos;
 }
 
-// One warp: in the `len` elements from e0 (lane l a contiguous run of len / 32),
+// One warp: in the LEN elements from e0 (lane l a contiguous run of LEN / 32,
+// its weights taken eight at a time with the eight loads issued together),
 // the element whose running sum (`before` ahead of e0) passes tgt; before < 0,
 // or nothing passing: the last element of positive weight; -1 if none.
-__device__ int fv_warp_rescan(const Wt &w, const float *trow, const float *lrow, int V, int e0, int len,
-                              double before, double tgt) {
+template <int LEN>
+__device__ int fv_warp_rescan(const Wt &w, const float *trow, const float *lrow, int V, int e0, double before,
+                              double tgt) {
+  constexpr int PER = LEN / 32, G = 8;
+  static_assert(PER % G == 0, "whole batches");
   const int lane = threadIdx.x & 31;
-  const int per = len / 32;
-  const int a0 = e0 + lane * per, a1 = min(V, a0 + per);
+  const int a0 = e0 + lane * PER;
   const bool pair = w.kind == 0;
   double ls = 0.0;
   int lp = -1;
-  for (int i = a0; i < a1; ++i) {
-    const float x = wval(w, __ldcg(trow + i), pair ? __ldcg(lrow + i) : 0.f);
-    ls += (double)x;
-    if (x > 0.f) lp = i;
+#pragma unroll 1
+  for (int q0 = 0; q0 < PER; q0 += G) {
+    float x[G];
+#pragma unroll
+    for (int q = 0; q < G; ++q) {
+      const int i = a0 + q0 + q;
+      x[q] = i < V ? wval(w, __ldcg(trow + i), pair ? __ldcg(lrow + i) : 0.f) : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < G; ++q) {
+      ls += (double)x[q];
+      if (x[q] > 0.f) lp = a0 + q0 + q;
+    }
   }
   const double inc = fv_warp_incl_scan(ls);
   int f = 0x7fffffff;
   if (before >= 0.0 && before + inc > tgt) {
     double r = before + (inc - ls);
-    for (int i = a0; i < a1; ++i) {
-      const float x = wval(w, __ldcg(trow + i), pair ? __ldcg(lrow + i) : 0.f);
-      r += (double)x;
-      if (x > 0.f && r > tgt) {
-        f = i;
-        break;
+#pragma unroll 1
+    for (int q0 = 0; q0 < PER && f == 0x7fffffff; q0 += G) {
+      float x[G];
+#pragma unroll
+      for (int q = 0; q < G; ++q) {
+        const int i = a0 + q0 + q;
+        x[q] = i < V ? wval(w, __ldcg(trow + i), pair ? __ldcg(lrow + i) : 0.f) : 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < G; ++q) {
+        r += (double)x[q];
+        if (f == 0x7fffffff && x[q] > 0.f && r > tgt) f = a0 + q0 + q;
       }
     }
   }
@@ -746,118 +645,189 @@ __device__ int fv_warp_rescan(const Wt &w, const float *trow, const float *lrow,
   return f != 0x7fffffff ? f : lp;
 }
 
+struct ResShared {
+  float sub[kResSubs];
+  double wtot[kResThreads / 32];
+  int wlast[kResThreads / 32];
+  int last, tok;
+};
+
+// Block-collective: a draw from p of target row `row` at u, the tile masses
+// from the GEMM's partials (a tile's sum of exp2((t - m) c) rescaled to the
+// row's maximum Mt).  Each warp sums a contiguous run of tiles; warp 0 finds
+// the run holding the crossing from the runs' totals, then the tile within it
+// (all running sums in index order), then rescans that tile's logits.
+// Returns the token, -1 if every weight is zero.
+__device__ int draw_p_tiles(ResShared &rs, const FvArgs &g, int row, float Mt, double u) {
+  constexpr int W = kResThreads / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = g.n_vt, wrun = (n + W - 1) / W;
+  const float4 *pp = g.part + (size_t)row * n;
+  auto mass = [&](int i) {
+    const float2 p = __ldcg(reinterpret_cast<const float2 *>(pp + i));
+    return p.x == -INFINITY ? 0.0 : (double)p.y * (double)ex2_approx((p.x - Mt) * g.c);
+  };
+  {
+    const int c0 = warp * wrun, c1 = min(n, c0 + wrun);
+    double tot = 0.0;
+    int lastpos = -1;
+    for (int b = c0; b < c1; b += 32) {
+      const double x = b + lane < c1 ? mass(b + lane) : 0.0;
+      tot += __shfl_sync(0xffffffffu, fv_warp_incl_scan(x), 31);
+      const unsigned pos = __ballot_sync(0xffffffffu, b + lane < c1 && x > 0.0);
+      if (pos) lastpos = b + 31 - __clz(pos);
+    }
+    if (lane == 0) {
+      rs.wtot[warp] = tot;
+      rs.wlast[warp] = lastpos;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const double x = lane < W ? rs.wtot[lane] : 0.0;
+    const double incl = fv_warp_incl_scan(x);
+    const double tgt = u * __shfl_sync(0xffffffffu, incl, 31);
+    const unsigned hit = __ballot_sync(0xffffffffu, lane < W && incl > tgt);
+    int cross = -1;
+    double before = -1.0;
+    if (hit) {
+      // the run's tiles (and, should rounding carry the crossing past it, the next)
+      const int cw = __ffs(hit) - 1;
+      double run = __shfl_sync(0xffffffffu, incl - x, cw);
+      for (int b = cw * wrun; b < n && cross < 0; b += 32) {
+        const double y = b + lane < n ? mass(b + lane) : 0.0;
+        const double in2 = fv_warp_incl_scan(y);
+        const unsigned h2 = __ballot_sync(0xffffffffu, b + lane < n && run + in2 > tgt);
+        if (h2) {
+          const int l = __ffs(h2) - 1;
+          cross = b + l;
+          before = run + __shfl_sync(0xffffffffu, in2 - y, l);
+        }
+        run += __shfl_sync(0xffffffffu, in2, 31);
+      }
+    }
+    if (cross < 0) {  // nothing passes: the last tile of positive mass
+      const unsigned pw = __ballot_sync(0xffffffffu, lane < W && rs.wlast[lane] >= 0);
+      if (pw) cross = rs.wlast[31 - __clz(pw)];
+      before = -1.0;
+    }
+    int tok = -1;
+    if (cross >= 0) {
+      const Wt wp{2, Mt, 0.f, 0.f, 0.f, g.c};
+      const float *trow = g.tgt + (size_t)row * g.V;
+      tok = fv_warp_rescan<kVt>(wp, trow, trow, g.V, cross * kVt, before, tgt);
+    }
+    if (lane == 0) rs.tok = tok;
+  }
+  __syncthreads();
+  return rs.tok;
+}
+
 }  // namespace
 
-// The residual draw of the stochastic call, after the finish kernel: CTA
-// (c, b) sums max(0, p - q) over the 16 sub-chunks of chunk c of sequence b's
-// rejecting pair (the stored target row and the draft row); the CTA that
-// completes the sequence finds the crossing chunk, then sub-chunk, then element
-// (float64 running sums in index order), and writes the replacement token.
-// Sequences without a rejection have nothing to do here.
-__global__ void __launch_bounds__(kResThreads) fv_residual_kernel(const FvArgs g, FvOut o) {
+// The draws of the stochastic call, after the finish kernel.  After a
+// rejection at j, CTA (c, b) sums max(0, p - q) over the 32 sub-chunks of
+// chunk c of sequence b's rejected pair (the stored target row and the draft
+// row); the CTA that completes the sequence finds the crossing chunk, then
+// sub-chunk, then element (float64 running sums in index order), and writes
+// the replacement token.  With every draft accepted, CTA (0, b) makes the
+// bonus draw from p of row k over the GEMM's tile partials.
+__global__ void __launch_bounds__(kResThreads, 4) fv_residual_kernel(const FvArgs g, FvOut o) {
   trace_start(kTkFusedAux);
-  __shared__ float sub[kResSubs];
-  __shared__ int s_last, s_tok;
+  __shared__ ResShared rs;
   const int ch = blockIdx.x, b = blockIdx.y, V = g.V, k = g.k;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   grid_dep_wait();  // the finish kernel's records
   grid_dep_launch();
+  trace_dep(kTkFusedAux);
   const float4 *r4 = reinterpret_cast<const float4 *>(&g.rrec[b]);
   const float4 rx = __ldcg(r4);
   const int4 ry = __ldcg(reinterpret_cast<const int4 *>(r4 + 1));
   const int j = ry.x, row = ry.y;
-  if (j < 0 || !in_bounds(j < k && row == b * (k + 1) + j, g.status)) {
+  if (!in_bounds(j >= 0 && j <= k && row == b * (k + 1) + j, g.status) || (j == k && ch != 0)) {
     trace_end(kTkFusedAux);
     return;
   }
-  const Wt w{0, rx.x, rx.y, rx.z, rx.w, g.c};
-  const float *trow = g.tgt + (size_t)row * V, *lrow = g.draft + ((size_t)b * k + j) * V;
-  const bool vec = ((reinterpret_cast<uintptr_t>(trow) | reinterpret_cast<uintptr_t>(lrow)) & 15u) == 0;
-  // sub-chunks warp and warp + 8, a lane 4 float4 of each row of a sub-chunk
+  const double u = (double)__ldg(&g.u_final[b]);
+  int tok = -1;
+  if (j < k) {
+    const Wt w{0, rx.x, rx.y, rx.z, rx.w, g.c};
+    const float *trow = g.tgt + (size_t)row * V, *lrow = g.draft + ((size_t)b * k + j) * V;
+    const bool vec = ((reinterpret_cast<uintptr_t>(trow) | reinterpret_cast<uintptr_t>(lrow)) & 15u) == 0;
+    // sub-chunks warp + 8 h, a lane 4 float4 of each row of a sub-chunk
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int s = warp + 8 * h;
-    const int e0 = ch * kResChunk + s * kResSub;
-    float acc = 0.f;
-    if (vec && e0 + kResSub <= V) {
-      float4 tv[4], lv[4];
+    for (int h = 0; h < kResSubs / 8; ++h) {
+      const int s = warp + 8 * h;
+      const int e0 = ch * kResChunk + s * kResSub;
+      float acc = 0.f;
+      if (vec && e0 + kResSub <= V) {
+        float4 tv[4], lv[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        tv[q] = __ldcg(reinterpret_cast<const float4 *>(trow + e0) + lane + 32 * q);
-        lv[q] = __ldcg(reinterpret_cast<const float4 *>(lrow + e0) + lane + 32 * q);
+        for (int q = 0; q < 4; ++q) {
+          tv[q] = __ldcg(reinterpret_cast<const float4 *>(trow + e0) + lane + 32 * q);
+          lv[q] = __ldcg(reinterpret_cast<const float4 *>(lrow + e0) + lane + 32 * q);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          acc += (wval(w, tv[q].x, lv[q].x) + wval(w, tv[q].y, lv[q].y)) +
+                 (wval(w, tv[q].z, lv[q].z) + wval(w, tv[q].w, lv[q].w));
+      } else {
+        for (int i = e0 + lane; i < min(V, e0 + kResSub); i += 32) acc += wval(w, __ldcg(trow + i), __ldcg(lrow + i));
       }
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        acc += (wval(w, tv[q].x, lv[q].x) + wval(w, tv[q].y, lv[q].y)) +
-               (wval(w, tv[q].z, lv[q].z) + wval(w, tv[q].w, lv[q].w));
-    } else {
-      for (int i = e0 + lane; i < min(V, e0 + kResSub); i += 32) acc += wval(w, __ldcg(trow + i), __ldcg(lrow + i));
+      acc = warp_sum(acc);
+      if (lane == 0) rs.sub[s] = acc;
     }
-    acc = warp_sum(acc);
-    if (lane == 0) sub[s] = acc;
-  }
-  __syncthreads();
-  if (threadIdx.x < kResSubs) g.rsub[((size_t)b * g.nrc + ch) * kResSubs + threadIdx.x] = sub[threadIdx.x];
-  if (threadIdx.x == 0) {
-    double cm = 0.0;
-    for (int s = 0; s < kResSubs; ++s) cm += (double)sub[s];
-    g.rcm[(size_t)b * g.nrc + ch] = cm;
-  }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned arrived = atomic_add_acq_rel(&g.rcnt[b], 1u) + 1u;
-    s_last = arrived == (unsigned)g.nrc;
-    if (s_last) g.rcnt[b] = 0u;  // left zero
-  }
-  __syncthreads();
-  if (!s_last) {
-    trace_end(kTkFusedAux);
-    return;
-  }
-  if (warp == 0) {
-    const double u = (double)__ldg(&g.u_final[b]);
-    const double *cm = g.rcm + (size_t)b * g.nrc;
-    double tgt, base;
-    const int cx = fv_warp_cross([&](int i) { return __ldcg(&cm[i]); }, g.nrc, u, tgt, base);
-    int tok = -1;
-    if (cx >= 0) {
-      const float *sm = g.rsub + ((size_t)b * g.nrc + cx) * kResSubs;
-      // within the chunk: its sub-chunk masses against tgt - base
-      const double rel = base >= 0.0 ? tgt - base : 1e300;
-      const double x = lane < kResSubs ? (double)__ldcg(&sm[lane]) : 0.0;
-      const double incl = fv_warp_incl_scan(x);
-      const unsigned hit = __ballot_sync(0xffffffffu, lane < kResSubs && incl > rel);
-      const unsigned pos = __ballot_sync(0xffffffffu, lane < kResSubs && x > 0.0);
-      int s = -1;
-      double bef = -1.0;
-      if (hit) {
-        s = __ffs(hit) - 1;
-        bef = base + __shfl_sync(0xffffffffu, incl - x, s);
-      } else if (pos) {
-        s = 31 - __clz(pos);
+    __syncthreads();
+    if (threadIdx.x < kResSubs) g.rsub[((size_t)b * g.nrc + ch) * kResSubs + threadIdx.x] = rs.sub[threadIdx.x];
+    if (threadIdx.x == 0) {
+      double cm = 0.0;
+      for (int s = 0; s < kResSubs; ++s) cm += (double)rs.sub[s];
+      g.rcm[(size_t)b * g.nrc + ch] = cm;
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const unsigned arrived = atomic_add_acq_rel(&g.rcnt[b], 1u) + 1u;
+      rs.last = arrived == (unsigned)g.nrc;
+      if (rs.last) g.rcnt[b] = 0u;  // left zero
+    }
+    __syncthreads();
+    if (!rs.last) {
+      trace_end(kTkFusedAux);
+      return;
+    }
+    if (warp == 0) {
+      const double *cm = g.rcm + (size_t)b * g.nrc;
+      double tgt, base;
+      const int cx = fv_warp_cross([&](int i) { return __ldcg(&cm[i]); }, g.nrc, u, tgt, base);
+      int t = -1;
+      if (cx >= 0) {
+        const float *sm = g.rsub + ((size_t)b * g.nrc + cx) * kResSubs;
+        // within the chunk: its sub-chunk masses against tgt - base
+        const double rel = base >= 0.0 ? tgt - base : 1e300;
+        const double x = lane < kResSubs ? (double)__ldcg(&sm[lane]) : 0.0;
+        const double incl = fv_warp_incl_scan(x);
+        const unsigned hit = __ballot_sync(0xffffffffu, lane < kResSubs && incl > rel);
+        const unsigned pos = __ballot_sync(0xffffffffu, lane < kResSubs && x > 0.0);
+        int s = -1;
+        double bef = -1.0;
+        if (hit) {
+          s = __ffs(hit) - 1;
+          bef = base + __shfl_sync(0xffffffffu, incl - x, s);
+        } else if (pos) {
+          s = 31 - __clz(pos);
+        }
+        if (s >= 0) t = fv_warp_rescan<kResSub>(w, trow, lrow, V, cx * kResChunk + s * kResSub, bef, tgt);
       }
-      if (s >= 0) tok = fv_warp_rescan(w, trow, lrow, V, cx * kResChunk + s * kResSub, kResSub, bef, tgt);
+      if (lane == 0) rs.tok = t;
     }
-    if (tok < 0) {
-      // the residual is zero everywhere (p = q): draw from p itself, over the
-      // row's 256-token tile masses from the GEMM's partials
-      const float4 *pp = g.part + (size_t)row * g.n_vt;
-      const Wt wp{2, w.Mt, 0.f, 0.f, 0.f, g.c};
-      double tg2, bf2;
-      const int tile = fv_warp_cross(
-          [&](int i) {
-            const float4 p = __ldcg(&pp[i]);
-            return p.x == -INFINITY ? 0.0 : (double)p.y * (double)ex2_approx((p.x - wp.Mt) * wp.c);
-          },
-          g.n_vt, u, tg2, bf2);
-      if (tile >= 0) tok = fv_warp_rescan(wp, trow, trow, V, tile * kVt, kVt, bf2, tg2);
-    }
-    if (lane == 0) s_tok = tok;
+    __syncthreads();
+    tok = rs.tok;
   }
-  __syncthreads();
+  // every draft accepted (the bonus draw), or a residual that is zero
+  // everywhere (p = q, so the draw falls back to p itself): p of the row
+  if (tok < 0) tok = draw_p_tiles(rs, g, row, rx.x, u);
   if (threadIdx.x == 0) {
-    int tok = s_tok;
     if (tok < 0) {
       set_status(g.status, kStatusNonFinite);
       tok = 0;
@@ -918,6 +888,11 @@ cudaError_t fused_set_attributes() {
     e = cudaFuncSetAttribute(fv_finish_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, f_bytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(fv_finish_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, f_bytes);
+  // the draft rows' statistics run beside the GEMM: ask for the same
+  // shared-memory carveout, so that an SM holding a GEMM CTA can take them
+  if (e == cudaSuccess && getenv("MTP_FV_CARVEOUT") && getenv("MTP_FV_CARVEOUT")[0] == '1')
+    e = cudaFuncSetAttribute(fv_draft_stats_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
   return e;
 }
 
@@ -944,6 +919,7 @@ cudaError_t launch_fused_verify(const FusedCall &fc, cudaStream_t s, bool pdl) {
   g.u_final = fc.u_final;
   char *p = static_cast<char *>(fc.ws);
   g.status = reinterpret_cast<int *>(p);
+  g.dctr = reinterpret_cast<unsigned *>(p + 128);
   p += 256;
   g.part = reinterpret_cast<float4 *>(p);
   p += up256((size_t)g.Na * g.n_vt * 16);
@@ -961,7 +937,6 @@ cudaError_t launch_fused_verify(const FusedCall &fc, cudaStream_t s, bool pdl) {
     p += up256((size_t)fc.B * g.nrc * kResSubs * 4);
     g.rcm = reinterpret_cast<double *>(p);
   }
-  g.chunk = kVt * ((g.n_vt + kMaxChunks - 1) / kMaxChunks);  // whole tiles, at most kMaxChunks chunks
 
   FvMaps maps{};
   if (!make_bf16_map(&maps.hid, fc.hidden, (uint64_t)fc.d, (uint64_t)g.Na, (uint64_t)fc.d, kMRows))

@@ -207,24 +207,41 @@ __device__ int warp_rescan(const Wt &w, const float *trow, const float *lrow, in
   const int lane = threadIdx.x & 31;
   constexpr int PER = kSub / 32;
   const bool pair = w.kind == 0;
-  const int e0 = s * kSub + lane * PER, e1 = min(V, e0 + PER);
+  const int e0 = s * kSub + lane * PER;
+  // the lane's weights eight at a time, the eight loads issued together
+  constexpr int G = 8;
   double ls = 0.0;
   int lp = -1;
-  for (int i = e0; i < e1; ++i) {
-    const float x = wval(w, __ldcg(trow + i), pair ? __ldcg(lrow + i) : 0.f);
-    ls += (double)x;
-    if (x > 0.f) lp = i;
+#pragma unroll 1
+  for (int q0 = 0; q0 < PER; q0 += G) {
+    float x[G];
+#pragma unroll
+    for (int q = 0; q < G; ++q) {
+      const int i = e0 + q0 + q;
+      x[q] = i < V ? wval(w, __ldcg(trow + i), pair ? __ldcg(lrow + i) : 0.f) : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < G; ++q) {
+      ls += (double)x[q];
+      if (x[q] > 0.f) lp = e0 + q0 + q;
+    }
   }
   const double inc = incl_scan_d(ls);
   int f = 0x7fffffff;
   if (before >= 0.0 && before + inc > tgt) {
     double r = before + (inc - ls);
-    for (int i = e0; i < e1; ++i) {
-      const float x = wval(w, __ldcg(trow + i), pair ? __ldcg(lrow + i) : 0.f);
-      r += (double)x;
-      if (x > 0.f && r > tgt) {
-        f = i;
-        break;
+#pragma unroll 1
+    for (int q0 = 0; q0 < PER && f == 0x7fffffff; q0 += G) {
+      float x[G];
+#pragma unroll
+      for (int q = 0; q < G; ++q) {
+        const int i = e0 + q0 + q;
+        x[q] = i < V ? wval(w, __ldcg(trow + i), pair ? __ldcg(lrow + i) : 0.f) : 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < G; ++q) {
+        r += (double)x[q];
+        if (f == 0x7fffffff && x[q] > 0.f && r > tgt) f = e0 + q0 + q;
       }
     }
   }
@@ -329,37 +346,32 @@ __device__ void decide(Shared &sh, const VerifyArgs &a, int b, int kb) {
     }
   }
   __syncthreads();
-  // the accept decisions in order, in warp 0: lane j loads the logits at draft
-  // token j first, so the positions' loads are in flight together
+  // u q(d) < p(d) at every kept position at once, lane j of warp 0 position
+  // j (its token, the logits there and its uniform loaded together); the
+  // first rejection and the flags are those of taking them in order
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     int dl = -1;
     float tdl = 0.f, ldl = 0.f;
+    double ua = 0.0;
     if (lane < kb) {
       dl = __ldg(&a.draft_tok[(size_t)b * k + lane]);
+      ua = (double)__ldg(&a.u_accept[(size_t)b * k + lane]);
       if (dl >= 0 && dl < V) {
         tdl = __ldg(seq_row(a, b, lane) + dl);
         ldl = __ldg(seq_row(a, b, k + 1 + lane) + dl);
       }
     }
-    int rj = -1, fl = 0;
-    for (int j = 0; j < kb; ++j) {
-      const int d = __shfl_sync(0xffffffffu, dl, j);
-      const float tdj = __shfl_sync(0xffffffffu, tdl, j), ldj = __shfl_sync(0xffffffffu, ldl, j);
-      if (d < 0 || d >= V) {
-        fl |= kStatusBadToken;
-        rj = j;
-        break;
-      }
-      if (!(sh.M[j] > -INFINITY) || !(sh.M[k + 1 + j] > -INFINITY)) fl |= kStatusNonFinite;
-      const double p = exp2(((double)tdj - (double)sh.M[j]) * (double)c) / sh.Z[j];
-      const double q = exp2(((double)ldj - (double)sh.M[k + 1 + j]) * (double)c) / sh.Z[k + 1 + j];
-      const double ua = (double)__ldg(&a.u_accept[(size_t)b * k + j]);
-      if (!(ua * q < p)) {
-        rj = j;
-        break;
-      }
+    const bool valid = dl >= 0 && dl < V;
+    bool finite = true, accept = true;
+    if (lane < kb && valid) {
+      finite = sh.M[lane] > -INFINITY && sh.M[k + 1 + lane] > -INFINITY;
+      const double p = exp2(((double)tdl - (double)sh.M[lane]) * (double)c) / sh.Z[lane];
+      const double q = exp2(((double)ldl - (double)sh.M[k + 1 + lane]) * (double)c) / sh.Z[k + 1 + lane];
+      accept = ua * q < p;
     }
+    int fl;
+    const int rj = first_rejection(kb, valid, finite, accept, fl);
     if (lane == 0) {
       sh.rej = rj;
       sh.flags = fl;
