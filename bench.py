@@ -76,18 +76,20 @@ NCU_TRAFFIC = {
         },
     },
     ("verify_split_kernel", "verify_sweep_b256_v151936_k3/stochastic"): {
-        "bytes": 1169289216 + 2980096,
+        "bytes": 1165680640 + 2998272,
         "sources": {
-            "csrc/verify_split.cu": "1534709eb14d8469051a94bbcbc6af85b9f5506abe030c97f2b325b311dc5dae",
+            "csrc/verify_split.cu": "229e8184ad8c3bca85cd2169b6ae383f21ce3bbeb911cf5b13e7d23562851043",
+            "csrc/verify_rule.cuh": "ea886aaf8280a01a05f400afc2d1e3873420801473ab364cfacf465340a0eb5b",
             "csrc/verify.cu": "f5fc0310bc0803d8610b522263a676741829b2d28da6924a064b3d3158681d56",
             "csrc/common.cuh": "ccc7be3ffbab76f32e48e064231311046ac5ebb3caee7e3f3df14b4629b22b95",
             "csrc/internal.h": "2ab350d5622c22f47de0c469aabd5010981632626e75291fc2273994f1968187",
         },
     },
     ("fv_gemm_kernel + fv_finish_kernel", "fused_verify_b64_k3_d4096_v151936/greedy"): {
-        "bytes": 1250702848 + 3722496 + 2442240,
+        "bytes": 1250486528 + 4050432 + 2442240,
         "sources": {
-            "csrc/fused.cu": "d480c2e556aabb8667e40ba353e195c76031a75a1b4a6ce2bd79b062a8731cb9",
+            "csrc/fused.cu": "05994466aa93f37ec2e519d2518c65c2240abdaf995b6fcec71b6339d6629c3a",
+            "csrc/verify_rule.cuh": "ea886aaf8280a01a05f400afc2d1e3873420801473ab364cfacf465340a0eb5b",
             "csrc/tcgen05.cuh": "e128ff6d7c8451d618848063024b7cd0a98c722dd1b86ef0d04e6a07a9070ee7",
             "csrc/common.cuh": "ccc7be3ffbab76f32e48e064231311046ac5ebb3caee7e3f3df14b4629b22b95",
             "csrc/internal.h": "2ab350d5622c22f47de0c469aabd5010981632626e75291fc2273994f1968187",

@@ -35,6 +35,7 @@
 #include <stdlib.h>
 
 #include "common.cuh"
+#include "verify_rule.cuh"
 #include "internal.h"
 #include "tcgen05.cuh"
 
@@ -888,11 +889,6 @@ cudaError_t fused_set_attributes() {
     e = cudaFuncSetAttribute(fv_finish_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, f_bytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(fv_finish_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, f_bytes);
-  // the draft rows' statistics run beside the GEMM: ask for the same
-  // shared-memory carveout, so that an SM holding a GEMM CTA can take them
-  if (e == cudaSuccess && getenv("MTP_FV_CARVEOUT") && getenv("MTP_FV_CARVEOUT")[0] == '1')
-    e = cudaFuncSetAttribute(fv_draft_stats_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
   return e;
 }
 

@@ -28,6 +28,7 @@
 // A residual item waits only on statistics items with smaller tickets, which
 // were taken by CTAs already running, so every wait ends.
 #include "common.cuh"
+#include "verify_rule.cuh"
 #include "internal.h"
 
 namespace mtp {
