@@ -295,14 +295,22 @@ __device__ __forceinline__ void store_split8(const TcBufs &t, int b, int col, co
 }
 
 // Sum over the K splits of eight consecutive outputs (row n) of sequence b.
+// The split-K partials of eight outputs summed in split order; the splits'
+// loads four at a time, issued together (one after another they would cost
+// an L2 round trip per split).
 __device__ __forceinline__ void sum8(const float *part, int ks, size_t sstride, size_t boff, float *y) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) y[i] = 0.f;
-  for (int s = 0; s < ks; ++s) {
-    float v[8];
-    load8_f32(part + s * sstride + boff, v);
+  for (int s0 = 0; s0 < ks; s0 += 4) {
+    float v[4][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) y[i] += v[i];
+    for (int u = 0; u < 4; ++u)
+      if (s0 + u < ks) load8_f32(part + (size_t)(s0 + u) * sstride + boff, v[u]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (s0 + u < ks)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[i] += v[u][i];
   }
 }
 
