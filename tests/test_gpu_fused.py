@@ -168,3 +168,36 @@ def test_fused_invalid_arguments():
     with pytest.raises(bd.MtpError):      # workspace too small
         bd.spec_verify_fused(B, k, V, d, 1.0, GREEDY, h, x, None, dt, None, None, fv.out_tok, fv.accept_len,
                              fv.num_accepted, small)
+
+
+def test_fused_stochastic_out_of_range_tokens():
+    """Stochastic: a draft token outside [0, V) is never accepted; its position
+    is rejected and replaced by that position's residual draw, as after any
+    rejection.  The oracle defines no such token, so the expected outputs are
+    the oracle's on the call's own stored logits with, at that position, a
+    valid token where q(d) >= p(d) and u_accept = 1 (which rejects)."""
+    from oracle.sampling import softmax_T
+    B, k, V, d, T = 4, 3, 5003, 256, 1.0
+    head, hidden, t, draft, dtok, u = _inputs(B, k, V, d, T, seed=9300)
+    dtok = dtok.copy()
+    bad = {(0, 1): V + 7, (2, 0): -1}
+    for (b, j), v in bad.items():
+        dtok[b, j] = v
+    ua = u["u_accept"].copy()
+    ua[0, 0] = 0.0  # sequence 0 accepts position 0 (0 < p(d) / q(d))
+    fs = FusedVerifier(B, k, V, d, STOCH)
+    fs(T, to_device_bf16(head), to_device_bf16(hidden), to_device(draft), to_device(dtok), to_device(ua),
+       to_device(u["u_final"]))
+    g = fs.results()
+    fs.check_canaries()
+    assert bd.get_status(fs.ws) & bd.STATUS_BAD_TOKEN
+    G = _stored_logits(fs).reshape(B, k + 1, V).astype(np.float64)
+    l64 = draft.astype(np.float64)
+    d2, ua2 = dtok.copy(), ua.copy()
+    for (b, j) in bad:
+        d2[b, j] = int(np.argmax(softmax_T(l64[b, j], T) - softmax_T(G[b, j], T)))
+        ua2[b, j] = 1.0
+    o = oracle_verify(G, l64, d2, STOCH, T, ua2, u["u_final"])
+    exc = compare_verify(g, o, STOCH, G, l64, d2, ua2, u["u_final"], T)
+    check_excused(exc, B, "fused stochastic outputs with out-of-range tokens")
+    assert g[1][0] == 2 and g[1][2] == 1
