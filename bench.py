@@ -78,7 +78,7 @@ NCU_TRAFFIC = {
     ("verify_split_kernel", "verify_sweep_b256_v151936_k3/stochastic"): {
         "bytes": 1165680640 + 2998272,
         "sources": {
-            "csrc/verify_split.cu": "229e8184ad8c3bca85cd2169b6ae383f21ce3bbeb911cf5b13e7d23562851043",
+            "csrc/verify_split.cu": "80abf6cfe5259b2b43e8243c5342d705d37e519c4cb025db89ecaea85f0ffeae",
             "csrc/verify_rule.cuh": "ea886aaf8280a01a05f400afc2d1e3873420801473ab364cfacf465340a0eb5b",
             "csrc/verify.cu": "f5fc0310bc0803d8610b522263a676741829b2d28da6924a064b3d3158681d56",
             "csrc/common.cuh": "ccc7be3ffbab76f32e48e064231311046ac5ebb3caee7e3f3df14b4629b22b95",

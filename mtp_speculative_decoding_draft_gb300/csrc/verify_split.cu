@@ -8,23 +8,26 @@
 // Every CTA takes one work item by ticket (an atomic counter), so the order
 // in which items start is the ticket order whatever the hardware's dispatch
 // order.  Per sequence b there are two groups of items:
-//   statistics items, one per (row, 8192-element chunk) of its 2k+1 logit
+//   statistics items, one per (row, 32768-element chunk) of its 2k+1 logit
 //     rows (target rows t_0..t_k, draft rows q_0..q_{k-1}): the chunk's
-//     (max, sum of exp2((x - max) log2e / T)).  The item that completes the
-//     sequence (the last to arrive: a fence, then an atomic increment)
-//     combines the chunks into per-row (max, partition sum) and takes the
-//     accept decisions u q(d) < p(d) in order.  If every draft is accepted it
-//     also makes the bonus draw from p of t_k -- the chunk masses follow from
-//     the statistics, so only the crossing chunk is read again -- and writes
-//     the outputs.  It then publishes the decision (a release store).
-//   residual items, one per chunk, placed `lag` sequences later in ticket
+//     (max, sum of exp2((x - max) log2e / T)), read in four passes of 8192.
+//     The item that completes the sequence (the last to arrive: a fence,
+//     then an acquire-release increment) combines the chunks into per-row
+//     (max, partition sum), takes u q(d) < p(d) at every kept position at
+//     once (the first rejection as taking them in order finds it) and
+//     publishes the decision (a release store).  If every draft is accepted
+//     it then makes the bonus draw from p of the bonus row -- the chunk
+//     masses follow from the statistics, so only the crossing chunk is read
+//     again -- and writes the outputs.
+//   residual items, one per chunk, placed about `lag` items later in ticket
 //     order: each waits for the decision (acquire, bounded; by then it has
-//     almost always been made), and after a rejection at position j computes
-//     the masses of max(0, p_j - q_j) over its chunk's 512-element sub-chunks
-//     -- t_j and q_j were streamed a few microseconds before, so these reads
-//     are mostly L2 hits.  The last to arrive finds the crossing chunk, then
-//     sub-chunk, then element (float64 running sums, in index order), and
-//     writes the outputs.
+//     mostly been made), and after a rejection at position j computes the
+//     masses of max(0, p_j - q_j) over its chunk's 512-element sub-chunks.
+//     The pairs j <= 1, where the first rejection mostly falls, were read
+//     with an evict-last L2 policy and everything else evict-first, so these
+//     re-reads mostly hit L2.  The last to arrive finds the crossing chunk,
+//     then sub-chunk, then element (float64 running sums, in index order),
+//     and writes the outputs.
 // A residual item waits only on statistics items with smaller tickets, which
 // were taken by CTAs already running, so every wait ends.
 #include "common.cuh"
