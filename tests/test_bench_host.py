@@ -58,6 +58,18 @@ def test_traffic_is_reported_only_for_unchanged_sources(tmp_path, monkeypatch):
     assert bench.ncu_traffic("no_such_kernel", "no_such_workload") is None
 
 
+def test_default_line_traffic_matches_the_committed_sources():
+    """The default line's dominant kernel (the LM-head GEMV of the single
+    sequence) has a DRAM-traffic capture taken from the sources as committed:
+    a change to them that alters the kernel needs a new capture (and its
+    digests) before the line can report traffic again."""
+    key = ("lm_head_gemv", "single_greedy_b1_d4096_v151936_ctx4096")
+    t = bench.ncu_traffic(*key)
+    assert t is not None, "sources changed since the LM-head capture: take it again"
+    # within a few MB of the algorithmic bytes (the head once, 1.245 GB)
+    assert abs(t - 151936 * 4096 * 2) < 8e6
+
+
 def test_batched_and_deep_chain_step_bytes_match_the_worked_totals():
     """The hot-path scope's worked totals per step: about 9.1 GB for the batch of
     64 (weights 5.09 GB, K/V about 3.62 GB at the mean context of 4608, logits
