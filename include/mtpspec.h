@@ -451,7 +451,7 @@ enum {
     MTP_TK_TC_GEMM = 30,    /* tcgen05 GEMM of the batched path */
     MTP_TK_TC_AUX = 31,     /* the batched path's prologue / select / scatter kernels */
     MTP_TK_FUSED_GEMM = 40, /* spec_verify_fused: head GEMM */
-    MTP_TK_FUSED_AUX = 41,  /* spec_verify_fused: draft statistics and finish */
+    MTP_TK_FUSED_AUX = 41,  /* spec_verify_fused: draft statistics, decisions and draws */
     MTP_TK_CHAIN = 50       /* chain launch of several GEMV ops */
 };
 typedef struct MtpTraceEntry {

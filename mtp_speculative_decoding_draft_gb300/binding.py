@@ -444,7 +444,7 @@ class MtpTraceEntry(ctypes.Structure):
 TRACE_KIND_NAMES = {0: "gemv input projection", 1: "gemv QKV", 2: "gemv output projection", 3: "gemv gate/up",
                     4: "gemv down", 5: "gemv LM head", 10: "attention", 11: "attention (tensor cores)",
                     20: "verify (cluster)", 21: "verify (ticketed)", 30: "tc GEMM", 31: "tc prologue/select",
-                    40: "fused verify GEMM", 41: "fused verify stats/finish", 50: "chain"}
+                    40: "fused verify GEMM", 41: "fused verify aux (stats, decisions, draws)", 50: "chain"}
 
 
 def trace_read(max_entries=16384):
