@@ -373,8 +373,9 @@ int spec_step_reduced(const MtpDims *dims, const MtpWeights *w,
  *                 tile) partials there; stochastic also keeps the target's
  *                 fp32 logits, since its one residual draw per sequence needs
  *                 every element of the first rejecting row.
- * Returns MTP_OK or MTP_ERR_*.  A draft token outside [0, V) is never
- * accepted and sets MTP_STATUS_BAD_TOKEN.
+ * Returns MTP_OK or MTP_ERR_*; stochastic calls with B * k * ceil(V / 256) of
+ * 2^31 or more return MTP_ERR_UNSUPPORTED_SHAPE (and the workspace size 0).  A
+ * draft token outside [0, V) is never accepted and sets MTP_STATUS_BAD_TOKEN.
  */
 size_t spec_verify_fused_workspace_size(int B, int k, int V, int d, int mode);
 

@@ -733,6 +733,7 @@ int spec_step(const MtpDims *dims, const MtpWeights *w, const void *h, const int
 
 size_t spec_verify_fused_workspace_size(int B, int k, int V, int d, int mode) {
   if (!fused_shape_ok(B, k, V, d) || (mode != MTP_GREEDY && mode != MTP_STOCHASTIC)) return 0;
+  if (mode == MTP_STOCHASTIC && (long long)B * k * ((V + 255) / 256) >= (1ll << 31)) return 0;
   return fused_workspace_bytes(B, k, V, d, mode);
 }
 
@@ -743,6 +744,9 @@ int spec_verify_fused(int B, int k, int V, int d, float T, int mode, const void 
   if (!fused_shape_ok(B, k, V, d)) return MTP_ERR_INVALID_ARG;
   if (mode != MTP_GREEDY && mode != MTP_STOCHASTIC) return MTP_ERR_INVALID_ARG;
   if (mode == MTP_STOCHASTIC && !(T > 0.f && T < 1e30f)) return MTP_ERR_INVALID_ARG;
+  // the draft statistics' warps claim (row, 256-token tile) items from a
+  // 32-bit counter: past 2^31 items it could wrap before the last claim
+  if (mode == MTP_STOCHASTIC && (long long)B * k * ((V + 255) / 256) >= (1ll << 31)) return MTP_ERR_UNSUPPORTED_SHAPE;
   const void *ptrs[] = {head, target_hidden, draft_tok, out_tok, accept_len, num_accepted, ws};
   for (const void *p : ptrs)
     if (!aligned16(p)) return MTP_ERR_INVALID_ARG;

@@ -50,6 +50,12 @@ def test_host_side_validation_without_gpu(lib):
     assert L.mtp_workspace_size(ctypes.byref(bad), 3) == 0
     bad = bd.make_dims(1, 4096, 32, 8, 96, 12288, 151936, 4099)       # unsupported head size
     assert L.mtp_workspace_size(ctypes.byref(bad), 3) == 0
+    # verification from hidden states: a stochastic shape whose (row, 256-token
+    # tile) items reach 2^31 is refused (a 32-bit claim counter walks them);
+    # greedy has no such counter
+    assert bd.fused_workspace_size(1 << 20, 8, 256 * 256, 64, 1) == 0
+    assert bd.fused_workspace_size(1 << 20, 8, 256 * 256, 64, 0) > 0
+    assert bd.fused_workspace_size((1 << 20) - 1, 8, 256 * 256, 64, 1) > 0
     # argument errors are reported before any device work
     assert L.spec_verify(4, 0, 100, 1.0, 0, None, None, None, None, None, None, None, None, None, 0, None) == -1
     assert L.spec_verify(4, 3, 100, 1.0, 0, None, None, None, None, None, None, None, None, None, 0, None) == -1
